@@ -1,0 +1,318 @@
+/*
+ * Paged KV-cache attention: the plain CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this code.  It shares nothing with the
+ * CUDA library (no header, no helper, no constant) and the CUDA library never
+ * calls it.
+ *
+ * What it computes, and where the pages define it:
+ *   - the cache write ("How serving works in Tlaloc", section 1 "From a model
+ *     to DXIR", and section 2 "From DXIR to StableHLO", KV_CACHE_WRITE bullet):
+ *     every token whose slot is not -1 has its K row and V row copied into the
+ *     pool at that slot; slot -1 (padding) writes nothing;
+ *   - paged attention (same page, section 2, PAGED_ATTENTION bullet): a query
+ *     at position p reads the keys 0..p of its own sequence, found through the
+ *     sequence's block table, scores them with a dot product, takes a softmax
+ *     and returns the softmax-weighted sum of the values; the causal length is
+ *     position + 1 (section 1);
+ *   - the sliding window (section 3, "Sliding-window layers"): with window W
+ *     only positions p-W+1..p are read;
+ *   - the blockwise form (section 2, "Blockwise attention"): the same result
+ *     folded over key blocks of 2,048 positions with a running max, a running
+ *     sum and a running P.V;
+ *   - the KV sizing closed form ("Serving Models", "Count KV heads and
+ *     distinct stored tensors"): 2 * layers * H_kv * d_head * bytes per token.
+ *
+ * Everything is the plain definition written out: widen each stored value
+ * exactly to double, accumulate in double, in index order, one output at a
+ * time.  The only parallelism is over independent outputs (OpenMP), which does
+ * not change any output's arithmetic.
+ *
+ * Readings taken where the pages are silent:
+ *   - pool layout [num_pages][page_size][H_kv][d], so slot s is page s/ps,
+ *     offset s%ps;
+ *   - query head h reads KV head h / (H_q / H_kv);
+ *   - a query with causal length 0 (position -1, i.e. padding) outputs 0;
+ *   - the softmax subtracts the running maximum before exponentiating.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_OK = 0, OR_BAD_ARG = 1, OR_BAD_PAGE = 2, OR_NO_MEM = 3 };
+
+/* Exact widening of one stored element to double.  bf16 is the upper half of
+ * an IEEE binary32, so the widening is a 16-bit shift. */
+static double widen(const void* base, int64_t idx, int dtype) {
+  if (dtype == OR_F32) return (double)((const float*)base)[idx];
+  uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+static int64_t elem_size(int dtype) { return dtype == OR_F32 ? 4 : 2; }
+
+/* ---------------------------------------------------------------- write -- */
+
+int oracle_kv_cache_write(const void* k_new, const void* v_new, void* k_cache,
+                          void* v_cache, const int64_t* slot_mapping,
+                          int64_t n_tokens, int64_t num_pages, int64_t page_size,
+                          int64_t h_kv, int64_t d, int64_t elem_bytes) {
+  if (n_tokens < 0 || num_pages <= 0 || page_size <= 0 || h_kv <= 0 || d <= 0 ||
+      elem_bytes <= 0)
+    return OR_BAD_ARG;
+  const int64_t row_bytes = h_kv * d * elem_bytes; /* one token: all KV heads */
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot == -1) continue; /* padding: never written */
+    if (slot < 0 || slot >= num_pages * page_size) return OR_BAD_PAGE;
+    const int64_t page = slot / page_size;
+    const int64_t offset = slot % page_size;
+    const int64_t dst = (page * page_size + offset) * row_bytes;
+    memcpy((char*)k_cache + dst, (const char*)k_new + t * row_bytes, (size_t)row_bytes);
+    memcpy((char*)v_cache + dst, (const char*)v_new + t * row_bytes, (size_t)row_bytes);
+  }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------ attention -- */
+
+typedef struct {
+  const void* k_cache;
+  const void* v_cache;
+  int dtype;
+  const int32_t* bt_row; /* this sequence's block table row */
+  int32_t max_pages_per_seq;
+  int32_t num_pages, page_size, h_kv, d;
+} paged_seq;
+
+/* Element e of the K (or V) row of logical position j, KV head g. */
+static int kv_index(const paged_seq* s, int64_t j, int64_t g, int64_t* row_base) {
+  const int64_t logical_block = j / s->page_size;
+  if (logical_block >= s->max_pages_per_seq) return OR_BAD_PAGE;
+  const int64_t page = s->bt_row[logical_block];
+  if (page < 0 || page >= s->num_pages) return OR_BAD_PAGE;
+  const int64_t offset = j % s->page_size;
+  *row_base = ((page * s->page_size + offset) * s->h_kv + g) * s->d;
+  return OR_OK;
+}
+
+static double score(const paged_seq* s, const double* q, int64_t j, int64_t g,
+                    double scale, int* err) {
+  int64_t base;
+  if (kv_index(s, j, g, &base) != OR_OK) { *err = OR_BAD_PAGE; return 0.0; }
+  double dot = 0.0;
+  for (int64_t e = 0; e < s->d; ++e) dot += q[e] * widen(s->k_cache, base + e, s->dtype);
+  return scale * dot;
+}
+
+static void add_weighted_value(const paged_seq* s, int64_t j, int64_t g, double w,
+                               double* acc, int* err) {
+  int64_t base;
+  if (kv_index(s, j, g, &base) != OR_OK) { *err = OR_BAD_PAGE; return; }
+  for (int64_t e = 0; e < s->d; ++e) acc[e] += w * widen(s->v_cache, base + e, s->dtype);
+}
+
+/* One-pass form: scores of keys lo..p, softmax, weighted sum of values. */
+static int attend_one_pass(const paged_seq* s, const double* q, int64_t lo, int64_t p,
+                           int64_t g, double scale, double* out) {
+  const int64_t d = s->d;
+  for (int64_t e = 0; e < d; ++e) out[e] = 0.0;
+  if (p < lo) return OR_OK; /* no live key: output 0 */
+  const int64_t n = p - lo + 1;
+  double* sc = (double*)malloc((size_t)n * sizeof(double));
+  if (!sc) return OR_NO_MEM;
+  int err = OR_OK;
+  double m = -INFINITY;
+  for (int64_t j = lo; j <= p; ++j) {
+    sc[j - lo] = score(s, q, j, g, scale, &err);
+    if (sc[j - lo] > m) m = sc[j - lo];
+  }
+  double l = 0.0;
+  for (int64_t j = lo; j <= p; ++j) {
+    const double w = exp(sc[j - lo] - m);
+    l += w;
+    add_weighted_value(s, j, g, w, out, &err);
+  }
+  for (int64_t e = 0; e < d; ++e) out[e] /= l;
+  free(sc);
+  return err;
+}
+
+/* Blockwise form: the keys are visited in blocks [kb*blk, (kb+1)*blk) for kb
+ * from kb_first to kb_last, and each block is folded into a running max m, a
+ * running sum l and a running P.V acc:
+ *   m' = max(m, max_j s_j)
+ *   l  = l * exp(m - m') + sum_j exp(s_j - m')
+ *   acc = acc * exp(m - m') + sum_j exp(s_j - m') v_j
+ * A block holding none of the row's keys lo..p is skipped.  out = acc / l. */
+static int attend_blockwise(const paged_seq* s, const double* q, int64_t lo, int64_t p,
+                            int64_t g, double scale, int64_t blk, int64_t kb_first,
+                            int64_t kb_last, double* out) {
+  const int64_t d = s->d;
+  for (int64_t e = 0; e < d; ++e) out[e] = 0.0;
+  if (p < lo) return OR_OK;
+  double* sc = (double*)malloc((size_t)blk * sizeof(double));
+  double* acc = (double*)calloc((size_t)d, sizeof(double));
+  if (!sc || !acc) { free(sc); free(acc); return OR_NO_MEM; }
+  int err = OR_OK;
+  double m = -INFINITY, l = 0.0;
+  for (int64_t kb = kb_first; kb <= kb_last; ++kb) {
+    int64_t j0 = kb * blk, j1 = (kb + 1) * blk - 1;
+    if (j0 < lo) j0 = lo;
+    if (j1 > p) j1 = p;
+    if (j1 < j0) continue; /* block fully masked for this row */
+    double m_blk = -INFINITY;
+    for (int64_t j = j0; j <= j1; ++j) {
+      sc[j - j0] = score(s, q, j, g, scale, &err);
+      if (sc[j - j0] > m_blk) m_blk = sc[j - j0];
+    }
+    const double m_new = m > m_blk ? m : m_blk;
+    const double carry = exp(m - m_new); /* exp(-inf) = 0 on the first block */
+    l *= carry;
+    for (int64_t e = 0; e < d; ++e) acc[e] *= carry;
+    for (int64_t j = j0; j <= j1; ++j) {
+      const double w = exp(sc[j - j0] - m_new);
+      l += w;
+      add_weighted_value(s, j, g, w, acc, &err);
+    }
+    m = m_new;
+  }
+  for (int64_t e = 0; e < d; ++e) out[e] = acc[e] / l;
+  free(sc);
+  free(acc);
+  return err;
+}
+
+static int64_t window_lo(int64_t p, int64_t window) {
+  if (window <= 0) return 0;
+  const int64_t lo = p - window + 1;
+  return lo < 0 ? 0 : lo;
+}
+
+static void set_threads(int32_t n_threads) {
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+  (void)n_threads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Decode: one query token per sequence; sequence b has causal length
+ * context_lens[b] (its query sits at position context_lens[b] - 1).
+ * Computes the sequences listed in seqs[0..n_seqs) into out[n_seqs][H_q][d]. */
+int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                        int32_t dtype, const int32_t* block_table,
+                        int32_t max_pages_per_seq, const int32_t* context_lens,
+                        int32_t B, int32_t h_q, int32_t h_kv, int32_t d,
+                        int32_t num_pages, int32_t page_size, int32_t window,
+                        double scale, const int32_t* seqs, int32_t n_seqs, double* out,
+                        int32_t n_threads) {
+  if (B <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 || page_size <= 0 ||
+      num_pages <= 0 || max_pages_per_seq <= 0 || (dtype != OR_F32 && dtype != OR_BF16))
+    return OR_BAD_ARG;
+  for (int32_t i = 0; i < n_seqs; ++i)
+    if (seqs[i] < 0 || seqs[i] >= B) return OR_BAD_ARG;
+  const int64_t group = h_q / h_kv;
+  int status = OR_OK;
+  set_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t item = 0; item < (int64_t)n_seqs * h_q; ++item) {
+    const int64_t b = seqs[item / h_q], h = item % h_q, g = h / group;
+    paged_seq s = {k_cache, v_cache, dtype, block_table + b * max_pages_per_seq,
+                   max_pages_per_seq, num_pages, page_size, h_kv, d};
+    double* qv = (double*)malloc((size_t)d * sizeof(double));
+    double* o = out + item * d;
+    if (!qv) { status = OR_NO_MEM; continue; }
+    for (int64_t e = 0; e < d; ++e) qv[e] = widen(q, (b * h_q + h) * d + e, dtype);
+    const int64_t p = (int64_t)context_lens[b] - 1;
+    const int rc = attend_one_pass(&s, qv, window_lo(p, window), p, g, scale, o);
+    if (rc != OR_OK) status = rc;
+    free(qv);
+  }
+  return status;
+}
+
+/* Prefill: q[B][T][H_q][d], positions[B][T] (-1 = padding).  Token (b,t) has
+ * causal length positions[b][t] + 1 and reads its own row's block table.
+ * blockwise = 0: one-pass form; otherwise the blockwise fold over key blocks of
+ * key_block positions, visiting the call's block range from the first block
+ * any row can see to the block holding the call's last position.
+ * Computes the tokens listed (as b*T+t) in tokens[0..n_tokens) into
+ * out[n_tokens][H_q][d]. */
+int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache,
+                         int32_t dtype, const int32_t* block_table,
+                         int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
+                         int32_t T, int32_t h_q, int32_t h_kv, int32_t d,
+                         int32_t num_pages, int32_t page_size, int32_t window,
+                         double scale, int32_t blockwise, int32_t key_block,
+                         const int64_t* tokens, int64_t n_tokens, double* out,
+                         int32_t n_threads) {
+  if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 ||
+      page_size <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 ||
+      (dtype != OR_F32 && dtype != OR_BF16) || (blockwise && key_block <= 0))
+    return OR_BAD_ARG;
+  for (int64_t i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= (int64_t)B * T) return OR_BAD_ARG;
+  /* The call's block range, over every live token of the call. */
+  int64_t kb_first = INT64_MAX, kb_last = -1;
+  for (int64_t i = 0; i < (int64_t)B * T; ++i) {
+    const int64_t p = positions[i];
+    if (p < 0) continue;
+    const int64_t lo = window_lo(p, window);
+    if (blockwise) {
+      if (lo / key_block < kb_first) kb_first = lo / key_block;
+      if (p / key_block > kb_last) kb_last = p / key_block;
+    }
+  }
+  const int64_t group = h_q / h_kv;
+  int status = OR_OK;
+  set_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t item = 0; item < n_tokens * h_q; ++item) {
+    const int64_t bt_idx = tokens[item / h_q], h = item % h_q, g = h / group;
+    const int64_t b = bt_idx / T;
+    paged_seq s = {k_cache, v_cache, dtype, block_table + b * max_pages_per_seq,
+                   max_pages_per_seq, num_pages, page_size, h_kv, d};
+    double* qv = (double*)malloc((size_t)d * sizeof(double));
+    double* o = out + item * d;
+    if (!qv) { status = OR_NO_MEM; continue; }
+    for (int64_t e = 0; e < d; ++e) qv[e] = widen(q, (bt_idx * h_q + h) * d + e, dtype);
+    const int64_t p = positions[bt_idx];
+    const int64_t lo = window_lo(p, window);
+    int rc;
+    if (!blockwise || p < 0)
+      rc = attend_one_pass(&s, qv, lo, p, g, scale, o);
+    else
+      rc = attend_blockwise(&s, qv, lo, p, g, scale, key_block, kb_first, kb_last, o);
+    if (rc != OR_OK) status = rc;
+    free(qv);
+  }
+  return status;
+}
+
+/* ---------------------------------------------------------------- sizing -- */
+
+/* Bytes of K and V one token of one sequence occupies: 2 * L * H_kv * d * q
+ * ("Serving Models", "Count KV heads and distinct stored tensors"). */
+int64_t oracle_kv_bytes_per_token(int64_t layers, int64_t h_kv, int64_t d_head,
+                                  int64_t bytes_per_elem) {
+  return 2 * layers * h_kv * d_head * bytes_per_elem;
+}
+
+int64_t oracle_elem_size(int32_t dtype) { return elem_size(dtype); }
