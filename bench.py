@@ -1,0 +1,415 @@
+"""Benchmark: paged decode KV-read GB/s (and prefill TFLOP/s) on GB300.
+
+One step = one pass of the decode hot path over one batch: KV_CACHE_WRITE of
+the batch's new tokens, then paged-attention decode (plan + split-K kernel +
+combine), on the Llama-3-8B-shaped layer (B=64, H_q=32, H_kv=8, d=128, bf16,
+pages of 16, context lengths U[512, 8192], shuffled pool).  value = KV bytes
+the decode must read (sum over sequences of L * 2 * H_kv * d * 2 bytes) per
+second.  The batched-prefill workload (B=8 rows of 2,048 tokens) is timed
+after it and reported under "prefill" in TFLOP/s.
+
+--impl reference times the CPU oracle (the plain C double-precision
+definition) on the same workload and metric on the host cores.
+
+Multi-GPU (torchrun, one process per GPU): replicas only, every rank runs its
+own batch (weak scaling); the only collective is the max of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+METRIC = "paged decode KV-read GB/s (% of HBM peak); prefill TFLOP/s (% TC peak)"
+WORKLOAD = "Llama-3-8B-shaped decode layer: B=64, Hq=32, Hkv=8, d=128, bf16, page 16, L~U[512,8192]"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
+    except Exception:
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def reduce_over_ranks(elapsed_ms: float, units: float, device="cpu"):
+    """(max elapsed over ranks, sum of units over ranks); identity on one process."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(elapsed_ms), float(units)
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def kv_bytes(lengths, window, hkv, d, elem):
+    tot = 0
+    for L in lengths:
+        n = min(L, window) if window > 0 else L
+        tot += max(n, 0) * 2 * hkv * d * elem
+    return tot
+
+
+def prefill_flops(positions, hq, d, window=0):
+    import torch
+    p = positions.to(torch.int64)
+    live = p >= 0
+    n = p + 1
+    if window > 0:
+        n = torch.clamp(n, max=window)
+    return int((4 * hq * d * n[live]).sum().item())
+
+
+# ------------------------------------------------------------------ ours --
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tl.build_library()
+    stream = torch.cuda.current_stream()
+
+    # ---- decode workload, resident in HBM
+    case = wl.llama8b_decode(seed=args.seed + rank, device=dev)
+    g = wl.to_device(case, dev)
+    B, hq, hkv, d = case.B, case.Hq, case.Hkv, case.d
+    lengths = case.context_lens.tolist()
+    kvb = kv_bytes(lengths, case.window, hkv, d, 2)
+    q_bytes = B * hq * d * 2
+    bt_bytes = sum((L + 15) // 16 for L in lengths) * 4
+    ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
+    out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+
+    def step():
+        tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping)
+        tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                case.scale, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n_ev = args.steps
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_ev)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping)
+            dec_ev[i][0].record(stream)
+            tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                    case.scale, out=out, workspace=ws)
+            dec_ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    elapsed_ms, total_kvb = reduce_over_ranks(elapsed_ms, kvb, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = total_kvb / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API, inputs from pinned host memory
+    if True:
+        host = {n: getattr(case, n).cpu().pin_memory() for n in
+                ("q", "k_new", "v_new", "slot_mapping", "context_lens")}
+        host["block_table"] = case.block_table.cpu().pin_memory()
+        dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        out_host = torch.empty((B, hq, d), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * 4
+
+        def e2e_step():
+            for n, t in host.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            tl.tl_kv_cache_write(dev_in["k_new"], dev_in["v_new"], g.k_cache, g.v_cache,
+                                 dev_in["slot_mapping"])
+            tl.tl_paged_attn_decode(dev_in["q"], g.k_cache, g.v_cache, dev_in["block_table"],
+                                    dev_in["context_lens"], case.scale, out=out, workspace=ws)
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms, _ = reduce_over_ranks(s2.elapsed_time(e2) / args.steps, 0, dev)
+        e2e = {"value": round(total_kvb / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    # ---- prefill workload
+    pcase = wl.batched_prefill(seed=args.seed + rank, device=dev)
+    pg = wl.to_device(pcase, dev)
+    flops = prefill_flops(pcase.positions, pcase.Hq, pcase.d)
+    pout = torch.empty((pcase.B, pcase.T, pcase.Hq, pcase.d), dtype=torch.float32, device=dev)
+    pws = tl.alloc_workspace(tl.tl_paged_attn_prefill_workspace_size(
+        pcase.B, pcase.T, pcase.Hq, pcase.Hkv, pcase.d), dev)
+    kn = pg.k_new.view(-1, pcase.Hkv, pcase.d)
+    vn = pg.v_new.view(-1, pcase.Hkv, pcase.d)
+    tl.tl_kv_cache_write(kn, vn, pg.k_cache, pg.v_cache, pg.slot_mapping)
+
+    def pf():
+        tl.tl_paged_attn_prefill(pg.q, pg.k_cache, pg.v_cache, pg.block_table, pg.positions,
+                                 pcase.scale, out=pout, workspace=pws)
+
+    for _ in range(max(3, args.warmup)):
+        pf()
+    torch.cuda.synchronize()
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.prefill_steps)]
+    for a, b in pev:
+        a.record(stream)
+        pf()
+        b.record(stream)
+    torch.cuda.synchronize()
+    pf_ms = statistics.mean(a.elapsed_time(b) for a, b in pev)
+    # chunk write on its own (16K rows), for the write kernel's GB/s
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(10)]
+    for a, b in wev:
+        a.record(stream)
+        tl.tl_kv_cache_write(kn, vn, pg.k_cache, pg.v_cache, pg.slot_mapping)
+        b.record(stream)
+    torch.cuda.synchronize()
+    w_ms = statistics.mean(a.elapsed_time(b) for a, b in wev)
+    n_live = int((pcase.slot_mapping >= 0).sum().item())
+    w_bytes = n_live * pcase.Hkv * pcase.d * 2 * 2 * 2 + pcase.slot_mapping.numel() * 8
+
+    hbm, bf16, bf16_sus, src = peaks()
+    dec_alg = kvb + q_bytes + bt_bytes + B * hq * d * 4
+    achieved = dec_alg / (dec_ms * 1e-3) / 1e9
+    pf_tflops = flops / (pf_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    cpu = cpu_baseline(case, g, args) if not args.no_cpu_baseline else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) values, shuffled page pool)",
+        "config": {"workload": WORKLOAD, "batch": B, "Hq": hq, "Hkv": hkv, "d_head": d,
+                   "page_size": 16, "kv_bytes_per_step": kvb,
+                   "l2": "inputs larger than L2 (KV pool %.2f GB vs 129 MB L2)" % (
+                       g.k_cache.numel() * 4 / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_hbm_peak": round(value / world / hbm, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode (plan + split-K bf16 kernel + combine)",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                     else "fallback", "algorithmic_bytes_per_launch": dec_alg,
+                     "ms_per_launch": round(dec_ms, 5)},
+        "prefill": {"workload": "B=8 x T=2048 right-aligned, pads U{0..1500}, prior U{0..6144}, "
+                                "Hq=32, Hkv=8, d=128, bf16",
+                    "tflops": round(pf_tflops, 2), "ms_per_call": round(pf_ms, 4),
+                    "flops_per_call": flops,
+                    "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2),
+                                 "peak": bf16, "unit": "TFLOP/s",
+                                 "frac": round(pf_tflops / bf16, 4), "traffic": None,
+                                 "peak_source": f"{src} bf16_tflops (burst)"}},
+        "kv_cache_write": {"rows": n_live, "ms": round(w_ms, 5),
+                           "gbs": round(w_bytes / (w_ms * 1e-3) / 1e9, 1),
+                           "frac": round(w_bytes / (w_ms * 1e-3) / 1e9 / hbm, 4)},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def cpu_baseline(case, g, args):
+    """The oracle, as it stands, on the whole decode step of the same workload
+    (the write of the new rows, then attention for all sequences), all host
+    cores, repeated for about args.cpu_seconds."""
+    import oracle
+
+    kc = g.k_cache.cpu()
+    vc = g.v_cache.cpu()
+    q, kn, vn = case.q.cpu(), case.k_new.cpu(), case.v_new.cpu()
+    sm, bt, cl = case.slot_mapping.cpu(), case.block_table.cpu(), case.context_lens.cpu()
+    threads = os.cpu_count() or 1
+    kvb = kv_bytes(cl.tolist(), case.window, case.Hkv, case.d, 2)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.kv_cache_write(kn, vn, kc, vc, sm)
+        oracle.paged_decode(q, kc, vc, bt, cl, case.scale, window=case.window, threads=threads)
+        reps += 1
+        if time.perf_counter() - t0 >= args.cpu_seconds:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(kvb / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "sample": f"the full decode step ({case.B} sequences), "
+                                        f"{reps} repetitions, {dt:.3f} s each"}
+
+
+# ------------------------------------------------------------- reference --
+
+def run_reference(args):
+    """The oracle timed on this host's cores: each step is the whole decode
+    step of the benchmark workload (write + attention for all 64 sequences)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
+    case = wl.llama8b_decode(seed=args.seed, device="cpu")
+    threads = os.cpu_count() or 1
+    kvb = kv_bytes(case.context_lens.tolist(), case.window, case.Hkv, case.d, 2)
+
+    def step():
+        oracle.kv_cache_write(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                              case.slot_mapping)
+        oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table,
+                            case.context_lens, case.scale, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = kvb / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) values, shuffled page pool)",
+            "config": {"workload": WORKLOAD, "batch": case.B, "Hq": case.Hq, "Hkv": case.Hkv,
+                       "d_head": case.d, "page_size": 16, "kv_bytes_per_step": kvb},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"the full decode step ({case.B} sequences) per step"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * tl_paged_attn.h -- paged attention over a block-table KV cache, for GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, no framework types.
+ *
+ * The operations and their arguments follow "How serving works in Tlaloc":
+ *   - section 1 "From a model to DXIR": per layer, KV_CACHE_WRITE (K and V)
+ *     then PAGED_ATTENTION; a prefill call holds one right-aligned row per
+ *     sequence, padding tokens first with slot -1 (never written), each live
+ *     token with its own position, causal length = position + 1;
+ *   - section 2 "From DXIR to StableHLO": attention gathers the pages a
+ *     sequence's block table names, takes a dot, a masked softmax and a dot;
+ *     a prefill row's pages are shared by all its tokens; "Blockwise
+ *     attention": a context spanning several 2,048-key blocks is folded one
+ *     block at a time with a running max, sum and P.V, so no context-wide
+ *     score tensor exists;
+ *   - section 3 "The serving artifact": the pool is numBlocks pages of
+ *     blockSize tokens for K and for V; the argument roles are POSITIONS,
+ *     BLOCK_TABLES, SEQ_LENS, SLOT_MAPPING, KV_POOL_IN/OUT, and the pools are
+ *     updated in place; "Sliding-window layers": a window W reads positions
+ *     p-W+1 .. p only.
+ * Grouped-query sharing and the paging data structure follow "Serving Models",
+ * "Change the cache at the architectural level" and "Logical histories and
+ * physical pages".
+ *
+ * Conventions shared by every entry point
+ *   Layout.   k_cache, v_cache: [num_pages][page_size][H_kv][d], row-major,
+ *             so slot s = page * page_size + offset is one contiguous row of
+ *             H_kv * d elements.  block_table: [B][max_pages_per_seq] int32;
+ *             entry i of row b is the physical page of the sequence's logical
+ *             block i (positions i*page_size .. (i+1)*page_size-1); entries
+ *             past the sequence's last page are never read.  Query head h
+ *             reads KV head h / (H_q / H_kv).
+ *   Memory.   Every pointer is a DEVICE pointer owned by the caller, except
+ *             where stated.  The library allocates nothing.  Base pointers
+ *             must be 16-byte aligned.  All work is enqueued on `stream`
+ *             (a cudaStream_t; NULL = the legacy default stream); nothing
+ *             synchronises.
+ *   Errors.   Arguments are validated on the host before any launch; on a
+ *             non-TL_OK return nothing was enqueued and nothing was written.
+ *             Launch failures return TL_ERR_CUDA.  Values the host cannot see
+ *             (slots, block-table entries, lengths, positions) are checked on
+ *             the device: an access they would take out of range is skipped
+ *             (the key counts as masked, the row as not written) and the
+ *             matching TL_DEVERR_* bit is OR-ed into *error_word when
+ *             error_word is not NULL.  The kernels never wait on a flag.
+ *   Unused slots.  Slots of a listed page past a sequence's last position
+ *             may hold anything, NaN included: they are never weighted.
+ */
+#ifndef TL_PAGED_ATTN_H
+#define TL_PAGED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TL_OK = 0,
+  TL_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, misalignment */
+  TL_ERR_UNSUPPORTED = 2, /* valid, but not a shape or dtype this build runs */
+  TL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  TL_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+} tl_status;
+
+typedef enum {
+  TL_F32 = 0, /* IEEE binary32 */
+  TL_BF16 = 1 /* bfloat16 */
+} tl_dtype;
+
+/* Bits OR-ed into *error_word by the device-side checks. */
+#define TL_DEVERR_SLOT_RANGE 1u    /* a slot outside [0, num_pages*page_size), not -1 */
+#define TL_DEVERR_PAGE_RANGE 2u    /* a needed block-table entry outside [0, num_pages) */
+#define TL_DEVERR_CONTEXT_RANGE 4u /* a length / position past max_pages_per_seq*page_size */
+
+/* Name of a status, for messages (never NULL). */
+const char* tl_status_string(tl_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t tl_version(void);
+
+/*
+ * KV_CACHE_WRITE ("How serving works in Tlaloc", sections 1-2): for every
+ * token t in [0, n_tokens) with slot_mapping[t] != -1,
+ *     k_cache row slot_mapping[t] = k_new[t],  v_cache row slot_mapping[t] = v_new[t]
+ * byte for byte.  Slot -1 is padding and writes nothing.  The pools are
+ * updated in place; no other byte of them changes.
+ *   k_new, v_new   [n_tokens][H_kv][d] in `dtype`
+ *   k_cache, v_cache  [num_pages][page_size][H_kv][d] in `dtype`, in place
+ *   slot_mapping   [n_tokens] int64
+ *   Two live tokens with the same slot: which one lands is unspecified.
+ * Returns TL_ERR_INVALID_ARG for null pointers (n_tokens > 0), non-positive
+ * sizes, H_kv*d*elem not a multiple of 16 bytes, or misaligned pointers.
+ */
+tl_status tl_kv_cache_write(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                            const int64_t* slot_mapping, int32_t n_tokens, int32_t num_pages,
+                            int32_t page_size, int32_t h_kv, int32_t d, tl_dtype dtype,
+                            uint32_t* error_word, void* stream);
+
+/*
+ * Bytes of workspace tl_paged_attn_decode needs for these sizes (an upper
+ * bound that holds for every content of context_lens).  Returns 0 when the
+ * sizes are invalid.
+ */
+size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, int32_t h_kv, int32_t d);
+
+/*
+ * PAGED_ATTENTION, decode ("How serving works in Tlaloc", sections 1-3): one
+ * query token per sequence.  Sequence b has causal length L = context_lens[b]
+ * (its query sits at position L-1, its own K/V already written); with
+ * p = L-1 and lo = (window > 0 ? max(0, p-window+1) : 0), for every query
+ * head h (KV head g = h / (h_q/h_kv)):
+ *     s_j = scale * <q[b][h], K_g(j)>,  j = lo..p,  K_g(j) found through
+ *           page block_table[b][j / page_size], offset j % page_size
+ *     out[b][h] = sum_j softmax(s)_j * V_g(j)
+ * L <= 0 gives out[b][h] = 0.  Work is split across CTAs by ranges of pages
+ * (split-K) and merged with a log-sum-exp combine; the result does not depend
+ * on where the pages are in the pool, and repeats bit for bit.
+ *   q            [B][h_q][d] in `dtype`
+ *   k_cache, v_cache  as above, in `dtype` (read only)
+ *   block_table  [B][max_pages_per_seq] int32
+ *   context_lens [B] int32
+ *   out          [B][h_q][d] float32
+ *   scale        multiplies the dot products (e.g. 1/sqrt(d))
+ *   workspace    device scratch of at least
+ *                tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d) bytes,
+ *                256-byte aligned; its contents need no initialisation and
+ *                are garbage afterwards.  Calls that overlap in time must not
+ *                share a workspace.
+ * Supported: dtype TL_BF16 or TL_F32, d in {64, 128}, h_q % h_kv == 0 with
+ * h_q/h_kv <= 16, page_size in [1, 256].  Otherwise TL_ERR_UNSUPPORTED.
+ */
+tl_status tl_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_pages_per_seq,
+                               const int32_t* context_lens, float* out, int32_t B, int32_t h_q,
+                               int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size,
+                               int32_t window, float scale, tl_dtype dtype, void* workspace,
+                               size_t workspace_bytes, uint32_t* error_word, void* stream);
+
+/*
+ * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes).
+ */
+size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
+                                            int32_t d);
+
+/*
+ * PAGED_ATTENTION, batched prefill ("How serving works in Tlaloc", sections
+ * 1-2, "Blockwise attention"): B rows of T tokens.  Token (b,t) with position
+ * p = positions[b][t] >= 0 attends exactly like a decode query of causal
+ * length p+1 (and the same window rule) over its own row's pages; p < 0 marks
+ * padding, whose output is 0.  The keys are folded in blocks of 2,048
+ * positions with an online softmax; no score tensor wider than one tile
+ * exists.  A row's result does not depend on the other rows (batched equals
+ * solo, bit for bit).
+ *   q            [B][T][h_q][d] bf16
+ *   positions    [B][T] int32, -1 = padding
+ *   out          [B][T][h_q][d] float32
+ *   other arguments as for decode.
+ * Supported: dtype TL_BF16, d = 128, h_q % h_kv == 0, page_size a power of
+ * two in [8, 128].  Otherwise TL_ERR_UNSUPPORTED.
+ */
+tl_status tl_paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, int32_t max_pages_per_seq,
+                                const int32_t* positions, float* out, int32_t B, int32_t T,
+                                int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                int32_t page_size, int32_t window, float scale, tl_dtype dtype,
+                                void* workspace, size_t workspace_bytes, uint32_t* error_word,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TL_PAGED_ATTN_H */

@@ -1,0 +1,25 @@
+"""Paged attention over a block-table KV cache, for GB300 (sm_103a).
+
+The compute path is the C-ABI library libtlpa.so (hand-written CUDA kernels,
+declared in include/tl_paged_attn.h); this package builds it in-tree and binds
+it with the same names.  There is no CPU or framework fallback: calling an op
+without the built library, or without a CUDA device, raises.
+"""
+from .api import (TL_BF16, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noqa: F401
+                  TL_DEVERR_SLOT_RANGE, TL_ERR_CUDA, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED,
+                  TL_ERR_WORKSPACE, TL_F32, TL_OK, TLError, alloc_workspace,
+                  tl_kv_cache_write, tl_paged_attn_decode, tl_paged_attn_decode_workspace_size,
+                  tl_paged_attn_prefill, tl_paged_attn_prefill_workspace_size, tl_status_string,
+                  tl_version)
+from . import build as _build_module
+
+
+def build_library(force: bool = False) -> str:
+    """Compile libtlpa.so in-tree if it is missing or stale; returns its path."""
+    return _build_module.build(force=force)
+
+__all__ = [
+    "tl_kv_cache_write", "tl_paged_attn_decode", "tl_paged_attn_prefill",
+    "tl_paged_attn_decode_workspace_size", "tl_paged_attn_prefill_workspace_size",
+    "tl_status_string", "tl_version", "TLError", "build_library", "alloc_workspace",
+]

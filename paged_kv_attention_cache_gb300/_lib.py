@@ -1,0 +1,60 @@
+"""ctypes view of libtlpa.so (the C ABI of include/tl_paged_attn.h).
+
+Loading fails loudly when the library has not been built: there is no other
+implementation behind these names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+i32, i64, u32p, vp, sz, f32 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_size_t, ctypes.c_float)
+
+SIGNATURES = {
+    "tl_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "tl_version": ([], i32),
+    "tl_kv_cache_write": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, u32p, vp],
+                          ctypes.c_int),
+    "tl_paged_attn_decode_workspace_size": ([i32, i32, i32, i32], sz),
+    "tl_paged_attn_decode": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                              ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
+    "tl_paged_attn_prefill_workspace_size": ([i32, i32, i32, i32, i32], sz),
+    "tl_paged_attn_prefill": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                               i32, f32, ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
+}
+
+
+class TLNotBuilt(RuntimeError):
+    pass
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """The loaded library; with build_if_missing, compile it first if needed."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing:
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise TLNotBuilt(
+                    f"{_build.LIB} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` "
+                    "(or python -m paged_kv_attention_cache_gb300.build)")
+            lib = ctypes.CDLL(_build.LIB)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib

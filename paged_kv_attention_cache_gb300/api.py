@@ -1,0 +1,145 @@
+"""Python binding of the C ABI, with the same names.
+
+Argument marshalling only: every function checks that the tensors are CUDA,
+contiguous and of the expected dtype, passes their device pointers and sizes to
+libtlpa.so, and raises TLError on a non-TL_OK status.  No arithmetic of the
+path happens here; torch provides the device memory and the stream.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+TL_OK, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED, TL_ERR_CUDA, TL_ERR_WORKSPACE = range(5)
+TL_F32, TL_BF16 = 0, 1
+TL_DEVERR_SLOT_RANGE, TL_DEVERR_PAGE_RANGE, TL_DEVERR_CONTEXT_RANGE = 1, 2, 4
+
+_DTYPES = {torch.float32: TL_F32, torch.bfloat16: TL_BF16}
+
+
+class TLError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {tl_status_string(status)}")
+
+
+def tl_status_string(status: int) -> str:
+    return _lib.load().tl_status_string(int(status)).decode()
+
+
+def tl_version() -> int:
+    return int(_lib.load().tl_version())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check(status: int, where: str):
+    if status != TL_OK:
+        raise TLError(status, where)
+
+
+def tl_kv_cache_write(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                      error_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """In place: cache row slot_mapping[t] = new[t] for every t with slot != -1.
+    k_new/v_new [N, H_kv, d]; caches [num_pages, page_size, H_kv, d]."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    P, ps, hkv, d = k_cache.shape
+    st = _lib.load().tl_kv_cache_write(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+        slot_mapping.numel(), P, ps, hkv, d, _DTYPES.get(k_cache.dtype, -1), _ptr(error_word),
+        _stream(stream))
+    _check(st, "tl_kv_cache_write")
+
+
+def tl_paged_attn_decode_workspace_size(B: int, h_q: int, h_kv: int, d: int) -> int:
+    return int(_lib.load().tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d))
+
+
+def tl_paged_attn_prefill_workspace_size(B: int, T: int, h_q: int, h_kv: int, d: int) -> int:
+    return int(_lib.load().tl_paged_attn_prefill_workspace_size(B, T, h_q, h_kv, d))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A device byte buffer (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def tl_paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         block_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                         window: int = 0, out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         error_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[B, H_q, d] (float32): one query per sequence, causal length context_lens[b]."""
+    _need(q, "q", k_cache.dtype)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    B, hq, d = q.shape
+    P, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(tl_paged_attn_decode_workspace_size(B, hq, hkv, d), q.device)
+    st = _lib.load().tl_paged_attn_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(context_lens), _ptr(out), B, hq, hkv, d, P, ps, int(window), float(scale),
+        _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), workspace.numel(), _ptr(error_word),
+        _stream(stream))
+    _check(st, "tl_paged_attn_decode")
+    return out
+
+
+def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_table: torch.Tensor, positions: torch.Tensor, scale: float,
+                          window: int = 0, out: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None,
+                          error_word: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """out[B, T, H_q, d] (float32): right-aligned batched prefill, padding at position -1."""
+    _need(q, "q", k_cache.dtype)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(positions, "positions", torch.int32)
+    B, T, hq, d = q.shape
+    P, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, T, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(tl_paged_attn_prefill_workspace_size(B, T, hq, hkv, d),
+                                    q.device)
+    st = _lib.load().tl_paged_attn_prefill(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window), float(scale),
+        _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), workspace.numel(), _ptr(error_word),
+        _stream(stream))
+    _check(st, "tl_paged_attn_prefill")
+    return out

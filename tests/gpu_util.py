@@ -1,0 +1,111 @@
+"""Helpers for the GPU parity tests: run a case through the C ABI, and compute
+the oracle on host copies of the same bytes (for large cases on a sample of
+sequences / tokens, after copying only the pages those sequences use)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_attention_cache_gb300 as tl
+from paged_kv_attention_cache_gb300 import workloads as wl
+
+DEV = "cuda"
+
+
+def gpu_write(g, error_word=None):
+    hkv, d = g.k_cache.shape[2], g.k_cache.shape[3]
+    tl.tl_kv_cache_write(g.k_new.reshape(-1, hkv, d), g.v_new.reshape(-1, hkv, d), g.k_cache,
+                         g.v_cache, g.slot_mapping, error_word=error_word)
+
+
+def gpu_decode(g, window=None, error_word=None, out=None, workspace=None):
+    return tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                   g.scale, window=g.window if window is None else window,
+                                   error_word=error_word, out=out, workspace=workspace)
+
+
+def gpu_prefill(g, window=None, error_word=None):
+    return tl.tl_paged_attn_prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.positions,
+                                    g.scale, window=g.window if window is None else window,
+                                    error_word=error_word)
+
+
+def sub_pool(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor, rows,
+             n_pages_of_row):
+    """Host copies of only the pages the given rows use, with the rows' block
+    tables renumbered to the copy.  Pure data movement (torch index_select)."""
+    bt = block_table.cpu()
+    pages, tables = [], []
+    for b, n in zip(rows, n_pages_of_row):
+        ids = bt[b, :n].tolist()
+        tables.append(list(range(len(pages), len(pages) + n)))
+        pages += ids
+    if not pages:
+        pages = [0]
+    idx = torch.tensor(pages, dtype=torch.long, device=k_cache.device)
+    kc = k_cache.index_select(0, idx).cpu()
+    vc = v_cache.index_select(0, idx).cpu()
+    width = max(1, max((len(t) for t in tables), default=1))
+    new_bt = torch.full((len(rows), width), -1, dtype=torch.int32)
+    for i, t in enumerate(tables):
+        if t:
+            new_bt[i, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    return kc, vc, new_bt
+
+
+def oracle_decode_rows(g, rows, window=None, threads=0):
+    """Oracle output [len(rows), Hq, d] for sequences `rows` of a GPU case
+    (read from the GPU pool after the write)."""
+    ps = g.k_cache.shape[1]
+    lens = g.context_lens.cpu().tolist()
+    n_pages = [(max(lens[b], 0) + ps - 1) // ps for b in rows]
+    kc, vc, bt = sub_pool(g.k_cache, g.v_cache, g.block_table, rows, n_pages)
+    q = g.q[list(rows)].cpu()
+    cl = torch.tensor([lens[b] for b in rows], dtype=torch.int32)
+    w = g.window if window is None else window
+    return oracle.paged_decode(q, kc, vc, bt, cl, g.scale, window=w, threads=threads)
+
+
+def oracle_prefill_tokens(g, row, ts, window=None, threads=0):
+    """Oracle output [len(ts), Hq, d] for tokens ts of prefill row `row`."""
+    ps = g.k_cache.shape[1]
+    pos = g.positions[row].cpu()
+    last = int(pos.max().item())
+    kc, vc, bt = sub_pool(g.k_cache, g.v_cache, g.block_table, [row], [(last + ps) // ps])
+    q = g.q[row:row + 1].cpu()
+    w = g.window if window is None else window
+    return oracle.paged_prefill(q, kc, vc, bt, pos.view(1, -1), g.scale, window=w,
+                                tokens=np.asarray(ts, np.int64), threads=threads)
+
+
+def sample_rows(lengths, n, seed=0):
+    """A spread of rows: the shortest, the longest, and random others."""
+    L = np.asarray(lengths)
+    rng = np.random.default_rng(seed)
+    pick = {int(L.argmin()), int(L.argmax())}
+    others = rng.permutation(len(L))
+    for b in others:
+        if len(pick) >= n:
+            break
+        pick.add(int(b))
+    return sorted(pick)
+
+
+def permuted_pool(g, seed=123):
+    """The same contents at other physical pages: pool'[perm[i]] = pool[i] and
+    block_table' = perm[block_table]."""
+    P = g.k_cache.shape[0]
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    perm = torch.randperm(P, generator=gen).to(g.k_cache.device)
+    kc = torch.empty_like(g.k_cache)
+    vc = torch.empty_like(g.v_cache)
+    kc[perm] = g.k_cache
+    vc[perm] = g.v_cache
+    bt = g.block_table.long()
+    nbt = torch.where(bt >= 0, perm[bt.clamp(min=0)], bt).to(torch.int32)
+    return kc, vc, nbt
+
+
+def on_gpu(case):
+    return wl.to_device(case, DEV)

@@ -1,0 +1,102 @@
+"""The C-ABI library loads and exports every entry point its header declares;
+host-side argument checks refuse bad calls before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_attention_cache_gb300 as tl
+from paged_kv_attention_cache_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tl_paged_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tl_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("tl_kv_cache_write", "tl_paged_attn_decode", "tl_paged_attn_prefill"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no binding"
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.tl_status_string(s).decode().startswith("TL_")
+    assert tl.tl_version() >= 10000
+
+
+def test_workspace_sizes(lib):
+    assert tl.tl_paged_attn_decode_workspace_size(64, 32, 8, 128) > 0
+    assert tl.tl_paged_attn_decode_workspace_size(64, 30, 8, 128) == 0  # h_q % h_kv
+    assert tl.tl_paged_attn_decode_workspace_size(0, 32, 8, 128) == 0
+    assert tl.tl_paged_attn_prefill_workspace_size(8, 2048, 32, 8, 128) > 0
+    # the decode bound grows with B and h_q but not with context length
+    a = tl.tl_paged_attn_decode_workspace_size(64, 32, 8, 128)
+    b = tl.tl_paged_attn_decode_workspace_size(128, 32, 8, 128)
+    assert b > a
+
+
+def test_host_validation_refuses_before_any_launch(lib):
+    i = _lib
+    # negative token count / null pointers: refused on the host
+    assert lib.tl_kv_cache_write(None, None, None, None, None, -1, 4, 16, 8, 128, 1, None, None) == tl.TL_ERR_INVALID_ARG
+    assert lib.tl_kv_cache_write(None, None, None, None, None, 3, 4, 16, 8, 128, 1, None, None) == tl.TL_ERR_INVALID_ARG
+    # zero tokens is a no-op, even with null pointers
+    assert lib.tl_kv_cache_write(None, None, None, None, None, 0, 4, 16, 8, 128, 1, None, None) == tl.TL_OK
+    # misaligned pointers
+    assert lib.tl_kv_cache_write(8, 16, 32, 48, 64, 1, 4, 16, 8, 128, 1, None, None) == tl.TL_ERR_INVALID_ARG
+    # decode: null pointers, h_q % h_kv, unsupported head size, missing workspace
+    args = dict(q=256, k=512, v=768, bt=1024, maxp=4, cl=1280, out=1536, B=2, hq=8, hkv=2,
+                d=128, P=8, ps=16, w=0, sc=0.1, dt=1, ws=None, wsb=0, err=None, st=None)
+
+    def dec(**kw):
+        a = dict(args, **kw)
+        return lib.tl_paged_attn_decode(a["q"], a["k"], a["v"], a["bt"], a["maxp"], a["cl"],
+                                        a["out"], a["B"], a["hq"], a["hkv"], a["d"], a["P"],
+                                        a["ps"], a["w"], a["sc"], a["dt"], a["ws"], a["wsb"],
+                                        a["err"], a["st"])
+    assert dec(q=None) == tl.TL_ERR_INVALID_ARG
+    assert dec(hq=7) == tl.TL_ERR_INVALID_ARG
+    assert dec(d=96) == tl.TL_ERR_UNSUPPORTED
+    assert dec(dt=7) == tl.TL_ERR_UNSUPPORTED
+    assert dec(hq=34, hkv=2) == tl.TL_ERR_UNSUPPORTED  # group 17 > 16
+    assert dec(w=-1) == tl.TL_ERR_INVALID_ARG
+    assert dec() == tl.TL_ERR_WORKSPACE
+    assert dec(ws=2048 + 16, wsb=1 << 30) == tl.TL_ERR_WORKSPACE  # not 256-byte aligned
+
+    def pre(**kw):
+        a = dict(args, **kw)
+        return lib.tl_paged_attn_prefill(a["q"], a["k"], a["v"], a["bt"], a["maxp"], a["cl"],
+                                         a["out"], a["B"], 4, a["hq"], a["hkv"], a["d"], a["P"],
+                                         a["ps"], a["w"], a["sc"], a["dt"], a["ws"], a["wsb"],
+                                         a["err"], a["st"])
+    assert pre(q=None) == tl.TL_ERR_INVALID_ARG
+    assert pre(dt=0) == tl.TL_ERR_UNSUPPORTED  # prefill is bf16 only
+    assert pre(d=64) == tl.TL_ERR_UNSUPPORTED
+    assert pre(ps=12) == tl.TL_ERR_UNSUPPORTED
+
+
+def test_ops_refuse_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 2, 8)
+    with pytest.raises(TypeError):
+        tl.tl_kv_cache_write(x, x, torch.zeros(2, 4, 2, 8), torch.zeros(2, 4, 2, 8),
+                             torch.zeros(4, dtype=torch.int64))

@@ -1,0 +1,141 @@
+"""PAGED_ATTENTION decode on the GPU against the oracle: the five workloads at
+full size (sampled sequences), edge cases, invariants, device-side checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_cache_gb300 as tl
+from paged_kv_attention_cache_gb300 import workloads as wl
+from tests.gpu_util import (gpu_decode, gpu_write, on_gpu, oracle_decode_rows, permuted_pool,
+                            sample_rows)
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _write_then_decode(case):
+    g = on_gpu(case)
+    gpu_write(g)
+    out = gpu_decode(g)
+    torch.cuda.synchronize()
+    return g, out
+
+
+def test_tiny_f32_all_outputs():
+    case = wl.tiny_decode(seed=0)
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    g, out = _write_then_decode(case)
+    oracle.kv_cache_write(case.k_new, case.v_new, kc, vc, case.slot_mapping)
+    ref = oracle.paged_decode(case.q, kc, vc, case.block_table, case.context_lens, case.scale)
+    assert_close(out, ref, "tiny f32")
+
+
+@pytest.mark.parametrize("maker,n", [(wl.llama8b_decode, 10), (wl.longctx_decode, 8)])
+def test_full_size_workloads_sampled(maker, n):
+    case = maker(seed=0, device="cuda")
+    g, out = _write_then_decode(case)
+    rows = sample_rows(case.context_lens.tolist(), n)
+    ref = oracle_decode_rows(g, rows)
+    assert_close(out[rows], ref, maker.__name__)
+    assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_sliding_window_mix_sampled(layer):
+    case = wl.swa_decode(seed=0, device="cuda", layer=layer)
+    assert case.window == (4096 if layer == 0 else 0)
+    g, out = _write_then_decode(case)
+    rows = sample_rows(case.context_lens.tolist(), 6, seed=layer)
+    ref = oracle_decode_rows(g, rows)
+    assert_close(out[rows], ref, f"swa layer {layer}")
+
+
+EDGE_LENGTHS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 2047, 2048, 2049, 5000]
+
+
+@pytest.mark.parametrize("window", [0, 1, 16, 17, 100, 2048])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_edge_lengths_and_windows(window, dtype):
+    case = wl.decode_case(EDGE_LENGTHS, Hq=8, Hkv=2, d=128, dtype=dtype, window=window, seed=7,
+                          nan_unused=True)
+    g = on_gpu(case)
+    out = gpu_decode(g)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table,
+                              case.context_lens, case.scale, window=window)
+    assert_close(out, ref, f"edges w={window} {dtype}")
+    assert torch.all(out[0] == 0)  # length 0 gives 0
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 16), (16, 1), (40, 8), (64, 8), (32, 2)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_head_groupings(hq, hkv, d):
+    lens = [1, 40, 300, 1234]
+    case = wl.decode_case(lens, Hq=hq, Hkv=hkv, d=d, seed=11, nan_unused=True)
+    g = on_gpu(case)
+    out = gpu_decode(g)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table,
+                              case.context_lens, case.scale)
+    assert_close(out, ref, f"hq={hq} hkv={hkv} d={d}")
+
+
+@pytest.mark.parametrize("page_size", [1, 7, 8, 32, 256])
+def test_page_sizes(page_size):
+    lens = [1, 5, 100, 513, 1500]
+    case = wl.decode_case(lens, Hq=8, Hkv=2, d=128, page_size=page_size, window=300, seed=13,
+                          nan_unused=True)
+    g = on_gpu(case)
+    out = gpu_decode(g)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table,
+                              case.context_lens, case.scale, window=300)
+    assert_close(out, ref, f"page_size={page_size}")
+
+
+def test_page_placement_and_repeat_are_bit_identical():
+    case = wl.llama8b_decode(seed=3, device="cuda", B=16)
+    g = on_gpu(case)
+    a = gpu_decode(g)
+    b = gpu_decode(g)
+    kc, vc, bt = permuted_pool(g)
+    c = tl.tl_paged_attn_decode(g.q, kc, vc, bt, g.context_lens, g.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert torch.equal(a, c)
+
+
+def test_bad_block_table_entry_is_reported_not_faulted():
+    case = wl.decode_case([40, 100], Hq=4, Hkv=2, d=128, seed=17)
+    case.pool.block_table[1, 2] = case.num_pages + 5  # a page the pool does not have
+    case.pool.block_table[0, 0] = -3
+    g = on_gpu(case)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(g, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & tl.TL_DEVERR_PAGE_RANGE
+    assert torch.isfinite(out).all()
+
+
+def test_context_past_the_table_is_reported():
+    case = wl.decode_case([40, 100], Hq=4, Hkv=2, d=128, seed=19)
+    g = on_gpu(case)
+    g.context_lens = torch.tensor([40, 100 + 16 * 10], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(g, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & tl.TL_DEVERR_CONTEXT_RANGE
+    assert torch.all(out[1] == 0)
+
+
+def test_workspace_is_reused_across_calls_of_different_shapes():
+    ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(64, 64, 8, 128), "cuda")
+    for seed, lens in ((0, [3000, 10, 70000]), (1, [5] * 64)):
+        case = wl.decode_case(lens, Hq=64, Hkv=8, d=128, seed=seed)
+        g = on_gpu(case)
+        out = gpu_decode(g, workspace=ws)
+        torch.cuda.synchronize()
+        ref = oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table,
+                                  case.context_lens, case.scale)
+        assert_close(out, ref, f"workspace reuse {seed}")

@@ -1,0 +1,110 @@
+"""Batched right-aligned prefill on the GPU against the oracle's blockwise fold:
+the full-size batch (sampled tokens), edge cases, batched == solo bit for bit,
+page-placement invariance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_cache_gb300 as tl
+from paged_kv_attention_cache_gb300 import workloads as wl
+from tests.gpu_util import gpu_prefill, gpu_write, on_gpu, oracle_prefill_tokens, permuted_pool
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _tokens_to_check(case, row, n=24, seed=0):
+    pad = case.pads[row]
+    T = case.T
+    rng = np.random.default_rng(seed + row)
+    ts = {pad, min(pad + 1, T - 1), T - 1, T - 2, max(pad - 1, 0), 0}
+    ts |= set(rng.integers(0, T, size=n).tolist())
+    return sorted(t for t in ts if 0 <= t < T)
+
+
+def test_full_size_batch_sampled():
+    case = wl.batched_prefill(seed=0, device="cuda")
+    g = on_gpu(case)
+    gpu_write(g)
+    out = gpu_prefill(g)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    for row in range(case.B):
+        ts = _tokens_to_check(case, row)
+        ref = oracle_prefill_tokens(g, row, ts)
+        assert_close(out[row, ts], ref, f"row {row}")
+        pads = [t for t in ts if t < case.pads[row]]
+        if pads:
+            assert torch.all(out[row, pads] == 0)
+
+
+def test_batched_equals_solo_bit_for_bit():
+    case = wl.prefill_case([100, 0, 700], [3000, 0, 5000], T=1024, Hq=16, Hkv=4, d=128, seed=5)
+    g = on_gpu(case)
+    gpu_write(g)
+    both = gpu_prefill(g)
+    for row in range(case.B):
+        solo = tl.tl_paged_attn_prefill(g.q[row:row + 1].contiguous(), g.k_cache, g.v_cache,
+                                        g.block_table[row:row + 1].contiguous(),
+                                        g.positions[row:row + 1].contiguous(), g.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(solo[0], both[row]), f"row {row}"
+
+
+def test_page_placement_invariance():
+    case = wl.prefill_case([10, 300], [2100, 0], T=512, Hq=8, Hkv=2, d=128, seed=6)
+    g = on_gpu(case)
+    gpu_write(g)
+    a = gpu_prefill(g)
+    kc, vc, bt = permuted_pool(g)
+    b = tl.tl_paged_attn_prefill(g.q, kc, vc, bt, g.positions, g.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("window", [0, 1, 100, 2048, 2049])
+def test_block_edges_and_windows(window):
+    """Rows ending at and one past a 2,048-key block boundary, length 1, a row
+    with no live token, a window start crossing a block boundary, and a T that
+    is not a multiple of the tile."""
+    T = 130
+    pads = [0, 0, T - 1, T, 5, 60]
+    p0 = [2048 - T, 2049 - T, 0, 0, 4000, 2000]
+    case = wl.prefill_case(pads, p0, T=T, Hq=8, Hkv=2, d=128, window=window, seed=8,
+                           nan_unused=True)
+    g = on_gpu(case)
+    gpu_write(g)
+    out = gpu_prefill(g)
+    torch.cuda.synchronize()
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    # the oracle reads the pool after the oracle's own write of the chunk
+    oracle.kv_cache_write(case.k_new, case.v_new, kc, vc, case.slot_mapping)
+    ref = oracle.paged_prefill(case.q, kc, vc, case.block_table, case.positions, case.scale,
+                               window=window)
+    assert_close(out.reshape(ref.shape), ref, f"edges window={window}")
+    assert torch.all(out[3] == 0)  # the row with no live token
+
+
+def test_group_shapes():
+    for hq, hkv in ((8, 8), (32, 8), (16, 1)):
+        case = wl.prefill_case([7, 0], [100, 1500], T=200, Hq=hq, Hkv=hkv, d=128, seed=9)
+        g = on_gpu(case)
+        gpu_write(g)
+        out = gpu_prefill(g)
+        torch.cuda.synchronize()
+        kc, vc = case.k_cache.clone(), case.v_cache.clone()
+        oracle.kv_cache_write(case.k_new, case.v_new, kc, vc, case.slot_mapping)
+        ref = oracle.paged_prefill(case.q, kc, vc, case.block_table, case.positions, case.scale)
+        assert_close(out.reshape(ref.shape), ref, f"hq={hq} hkv={hkv}")
+
+
+def test_bad_page_is_reported_not_faulted():
+    case = wl.prefill_case([0], [500], T=64, Hq=8, Hkv=2, d=128, seed=10)
+    case.pool.block_table[0, 3] = case.num_pages + 100
+    g = on_gpu(case)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_prefill(g, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & tl.TL_DEVERR_PAGE_RANGE
+    assert torch.isfinite(out).all()
