@@ -153,7 +153,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     # ---- decode workload, resident in HBM
-    case = wl.llama8b_decode(seed=args.seed + rank, device=dev)
+    case = wl.llama8b_decode(seed=args.seed + rank, device=dev, B=args.batch)
     g = wl.to_device(case, dev)
     B, hq, hkv, d = case.B, case.Hq, case.Hkv, case.d
     lengths = case.context_lens.tolist()
@@ -179,6 +179,13 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # keep the same load running around the timed region so the sampler
+        # (100 ms period) has readings under it
+        t_end = time.time() + args.soak_seconds
+        while time.time() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
             tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping)
@@ -188,6 +195,11 @@ def run_ours(args):
             dec_ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
+        t_end = time.time() + (0.5 if args.soak_seconds > 0 else 0.0)
+        while time.time() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     elapsed_ms = start.elapsed_time(stop)
@@ -196,8 +208,9 @@ def run_ours(args):
     ms_per_step = elapsed_ms / args.steps
     value = total_kvb / (ms_per_step * 1e-3) / 1e9
 
+    e2e = None
     # ---- end to end through the public API, inputs from pinned host memory
-    if True:
+    if args.only in ("all", "decode-e2e"):
         host = {n: getattr(case, n).cpu().pin_memory() for n in
                 ("q", "k_new", "v_new", "slot_mapping", "context_lens")}
         host["block_table"] = case.block_table.cpu().pin_memory()
@@ -229,7 +242,65 @@ def run_ours(args):
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
-    # ---- prefill workload
+    hbm, bf16, bf16_sus, src = peaks()
+    dec_alg = kvb + q_bytes + bt_bytes + B * hq * d * 4
+    achieved = dec_alg / (dec_ms * 1e-3) / 1e9
+    prefill_line, write_line = None, None
+    if args.only in ("all", "prefill"):
+        prefill_line, write_line = run_prefill(args, rank, dev, stream, hbm, bf16, src)
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    cpu = cpu_baseline(case, g, args) if (args.only == "all" and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) values, shuffled page pool)",
+        "config": {"workload": WORKLOAD if B == 64 else WORKLOAD.replace("B=64", f"B={B}"),
+                   "batch": B, "Hq": hq, "Hkv": hkv, "d_head": d,
+                   "page_size": 16, "kv_bytes_per_step": kvb,
+                   "l2": "inputs larger than L2 (KV pool %.2f GB vs 129 MB L2)" % (
+                       g.k_cache.numel() * 4 / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_hbm_peak": round(value / world / hbm, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode (plan + split-K bf16 kernel + combine)",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                     else "fallback", "algorithmic_bytes_per_launch": dec_alg,
+                     "ms_per_launch": round(dec_ms, 5)},
+        "prefill": prefill_line,
+        "kv_cache_write": write_line,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_prefill(args, rank, dev, stream, hbm, bf16, src):
+    """Batched-prefill workload: TFLOP/s of the attention call, and the
+    16K-row chunk write's GB/s."""
+    import torch
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
     pcase = wl.batched_prefill(seed=args.seed + rank, device=dev)
     pg = wl.to_device(pcase, dev)
     flops = prefill_flops(pcase.positions, pcase.Hq, pcase.d)
@@ -266,63 +337,18 @@ def run_ours(args):
     w_ms = statistics.mean(a.elapsed_time(b) for a, b in wev)
     n_live = int((pcase.slot_mapping >= 0).sum().item())
     w_bytes = n_live * pcase.Hkv * pcase.d * 2 * 2 * 2 + pcase.slot_mapping.numel() * 8
-
-    hbm, bf16, bf16_sus, src = peaks()
-    dec_alg = kvb + q_bytes + bt_bytes + B * hq * d * 4
-    achieved = dec_alg / (dec_ms * 1e-3) / 1e9
     pf_tflops = flops / (pf_ms * 1e-3) / 1e12
-
-    if rank != 0:
-        if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
-        return
-    cpu = cpu_baseline(case, g, args) if not args.no_cpu_baseline else None
-    line = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) values, shuffled page pool)",
-        "config": {"workload": WORKLOAD, "batch": B, "Hq": hq, "Hkv": hkv, "d_head": d,
-                   "page_size": 16, "kv_bytes_per_step": kvb,
-                   "l2": "inputs larger than L2 (KV pool %.2f GB vs 129 MB L2)" % (
-                       g.k_cache.numel() * 4 / 1e9),
-                   "parallelism": f"replicas x{world}"},
-        "frac_of_hbm_peak": round(value / world / hbm, 4),
-        "roofline": {"bound": "hbm", "kernel": "decode (plan + split-K bf16 kernel + combine)",
-                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
-                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
-                     else "fallback", "algorithmic_bytes_per_launch": dec_alg,
-                     "ms_per_launch": round(dec_ms, 5)},
-        "prefill": {"workload": "B=8 x T=2048 right-aligned, pads U{0..1500}, prior U{0..6144}, "
-                                "Hq=32, Hkv=8, d=128, bf16",
-                    "tflops": round(pf_tflops, 2), "ms_per_call": round(pf_ms, 4),
-                    "flops_per_call": flops,
-                    "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2),
-                                 "peak": bf16, "unit": "TFLOP/s",
-                                 "frac": round(pf_tflops / bf16, 4), "traffic": None,
-                                 "peak_source": f"{src} bf16_tflops (burst)"}},
-        "kv_cache_write": {"rows": n_live, "ms": round(w_ms, 5),
-                           "gbs": round(w_bytes / (w_ms * 1e-3) / 1e9, 1),
-                           "frac": round(w_bytes / (w_ms * 1e-3) / 1e9 / hbm, 4)},
-        "e2e": e2e,
-        "cpu_baseline": cpu,
-        "gpu_launches": 4 * args.steps,
-        "clocks": clk.summary(),
-    }
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+    prefill_line = {
+        "workload": "B=8 x T=2048 right-aligned, pads U{0..1500}, prior U{0..6144}, "
+                    "Hq=32, Hkv=8, d=128, bf16",
+        "tflops": round(pf_tflops, 2), "ms_per_call": round(pf_ms, 4), "flops_per_call": flops,
+        "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2), "peak": bf16,
+                     "unit": "TFLOP/s", "frac": round(pf_tflops / bf16, 4), "traffic": None,
+                     "peak_source": f"{src} bf16_tflops (burst)"}}
+    write_line = {"rows": n_live, "ms": round(w_ms, 5),
+                  "gbs": round(w_bytes / (w_ms * 1e-3) / 1e9, 1),
+                  "frac": round(w_bytes / (w_ms * 1e-3) / 1e9 / hbm, 4)}
+    return prefill_line, write_line
 
 
 def cpu_baseline(case, g, args):
@@ -396,13 +422,16 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-seconds", type=float, default=2.0)
+    ap.add_argument("--batch", type=int, default=64, help="decode batch (64 = the workload)")
+    ap.add_argument("--only", choices=["all", "decode", "decode-e2e", "prefill"], default="all")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -63,6 +63,16 @@ TL_DEVINLINE uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// (a, b) ~ hi + lo with hi = bf16(a, b) and lo = bf16 of the remainders: the
+// pair carries about 16 significant bits, so a bf16 x bf16 product of the
+// pair with an exact bf16 operand keeps f32-level accuracy in two MMAs.
+TL_DEVINLINE void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  const float ah = __uint_as_float(hi << 16);
+  const float bh = __uint_as_float(hi & 0xffff0000u);
+  lo = pack_bf16x2(a - ah, b - bh);
+}
+
 TL_DEVINLINE float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));

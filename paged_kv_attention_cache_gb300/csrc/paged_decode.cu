@@ -381,56 +381,72 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodePa
       }
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      const float mn0 = fmaxf(m0, mx0);  // finite: every chunk holds a live key
-      const float c0 = fast_exp2(m0 - mn0);
+      const float mn0 = fmaxf(m0, mx0);
+      const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
+      const float c0 = fast_exp2(m0 - base0);
       m0 = mn0;
       float p[2][4];
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
-        p[n][0] = fast_exp2(s[n][0] - mn0);
-        p[n][1] = fast_exp2(s[n][1] - mn0);
+        p[n][0] = fast_exp2(s[n][0] - base0);
+        p[n][1] = fast_exp2(s[n][1] - base0);
       }
       l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-      float c1 = 1.f;
+      float c1 = c0;
       if (TWO_ROWS) {
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
         const float mn1 = fmaxf(m1, mx1);
-        c1 = fast_exp2(m1 - mn1);
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        c1 = fast_exp2(m1 - base1);
         m1 = mn1;
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
-          p[n][2] = fast_exp2(s[n][2] - mn1);
-          p[n][3] = fast_exp2(s[n][3] - mn1);
+          p[n][2] = fast_exp2(s[n][2] - base1);
+          p[n][3] = fast_exp2(s[n][3] - base1);
         }
         l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-      } else {
-        p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.f;
       }
+      // rows 8-15 carry either the second half of the group (TWO_ROWS) or the
+      // low bf16 part of rows 0-7's probabilities; both rescale with their row
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {
         o[n][0] *= c0;
         o[n][1] *= c0;
-        if (TWO_ROWS) {
-          o[n][2] *= c1;
-          o[n][3] *= c1;
-        }
+        o[n][2] *= c1;
+        o[n][3] *= c1;
       }
-      const uint32_t a0 = pack_bf16x2(p[0][0], p[0][1]);
-      const uint32_t a1 = TWO_ROWS ? pack_bf16x2(p[0][2], p[0][3]) : 0u;
-      const uint32_t a2 = pack_bf16x2(p[1][0], p[1][1]);
-      const uint32_t a3 = TWO_ROWS ? pack_bf16x2(p[1][2], p[1][3]) : 0u;
-      // O += P V
+      // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
+      uint32_t h0, l0w, h2, l2w;
+      split_bf16x2(p[0][0], p[0][1], h0, l0w);
+      split_bf16x2(p[1][0], p[1][1], h2, l2w);
       {
         const int mi = lane >> 3, ri = lane & 7;
         const int tok = (mi & 1) * 8 + ri;
+        if (!TWO_ROWS) {
+          // A rows 0-7 = hi part, rows 8-15 = lo part of the same query heads
 #pragma unroll
-        for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-          const int u = 2 * nd2 + (mi >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vaddr + tok * (D * 2) + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * nd2], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(o[2 * nd2 + 1], a0, a1, a2, a3, b2, b3);
+          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+            const int u = 2 * nd2 + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(vaddr + tok * (D * 2) + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
+            mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+          }
+        } else {
+          uint32_t h1, l1w, h3, l3w;
+          split_bf16x2(p[0][2], p[0][3], h1, l1w);
+          split_bf16x2(p[1][2], p[1][3], h3, l3w);
+#pragma unroll
+          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+            const int u = 2 * nd2 + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(vaddr + tok * (D * 2) + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
+            mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
+            mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
+            mma_bf16_16816(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+          }
         }
       }
       __syncwarp();
@@ -450,8 +466,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodePa
     if (qr < P.group) {
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {
-        mrow[qr * RS + n * 8 + qc] = o[n][0];
-        mrow[qr * RS + n * 8 + qc + 1] = o[n][1];
+        mrow[qr * RS + n * 8 + qc] = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
+        mrow[qr * RS + n * 8 + qc + 1] = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
       }
       if ((lane & 3) == 0) {
         mrow[qr * RS + D] = m0;

@@ -237,17 +237,21 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
         const int mi = lane >> 3, ri = lane & 7;
 #pragma unroll
         for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-          const uint32_t a0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-          const uint32_t a1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-          const uint32_t a2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-          const uint32_t a3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+          // P = hi + lo (bf16 pair): two MMAs keep f32-level accuracy
+          uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+          split_bf16x2(s[2 * kk][0], s[2 * kk][1], h0, l0);
+          split_bf16x2(s[2 * kk][2], s[2 * kk][3], h1, l1);
+          split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], h2, l2);
+          split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], h3, l3);
           const int key = kk * 16 + (mi & 1) * 8 + ri;
 #pragma unroll
           for (int nd2 = 0; nd2 < D / 16; ++nd2) {
             uint32_t b0, b1, b2, b3;
             ldmatrix_x4_trans(vaddr + swz(key, 2 * nd2 + (mi >> 1), D * 2), b0, b1, b2, b3);
-            mma_bf16_16816(o[2 * nd2], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(o[2 * nd2 + 1], a0, a1, a2, a3, b2, b3);
+            mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
+            mma_bf16_16816(o[2 * nd2], l0, l1, l2, l3, b0, b1);
+            mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
+            mma_bf16_16816(o[2 * nd2 + 1], l0, l1, l2, l3, b2, b3);
           }
         }
       }
