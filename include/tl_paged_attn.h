@@ -42,7 +42,9 @@
  *             the device: an access they would take out of range is skipped
  *             (the key counts as masked, the row as not written) and the
  *             matching TL_DEVERR_* bit is OR-ed into *error_word when
- *             error_word is not NULL.  The kernels never wait on a flag.
+ *             error_word is not NULL.  Pipeline waits inside a kernel are
+ *             bounded (about a second); one that gives up sets
+ *             TL_DEVERR_TIMEOUT and the kernel returns.
  *   Unused slots.  Slots of a listed page past a sequence's last position
  *             may hold anything, NaN included: they are never weighted.
  */
@@ -73,6 +75,7 @@ typedef enum {
 #define TL_DEVERR_SLOT_RANGE 1u    /* a slot outside [0, num_pages*page_size), not -1 */
 #define TL_DEVERR_PAGE_RANGE 2u    /* a needed block-table entry outside [0, num_pages) */
 #define TL_DEVERR_CONTEXT_RANGE 4u /* a length / position past max_pages_per_seq*page_size */
+#define TL_DEVERR_TIMEOUT 8u       /* an internal pipeline wait gave up (outputs invalid) */
 
 /* Name of a status, for messages (never NULL). */
 const char* tl_status_string(tl_status status);

@@ -90,6 +90,55 @@ TL_DEVINLINE float warp_sum(float v) {
   return v;
 }
 
+// ---------------------------------------------------------------- mbarrier --
+// Every wait in this library is bounded: after kWaitCycles of polling it sets
+// the CTA's abort flag and gives up, and every other wait of the CTA gives up
+// as soon as it sees the flag, so no kernel can spin forever.
+
+constexpr long long kWaitCycles = 1ll << 31;  // about one second at 2 GHz
+
+TL_DEVINLINE void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+TL_DEVINLINE void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+TL_DEVINLINE void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+TL_DEVINLINE void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// Arrive on `bar` once all of this thread's earlier cp.async copies have landed
+// (the arrival counts against the barrier's expected count).
+TL_DEVINLINE void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+TL_DEVINLINE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of `bar` with the given parity; false on timeout or abort.
+TL_DEVINLINE bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
 TL_DEVINLINE void report(uint32_t* error_word, uint32_t bit) {
   if (error_word) atomicOr(error_word, bit);
 }

@@ -1,41 +1,47 @@
 // PAGED_ATTENTION, decode: one query token per sequence, split-K over the
-// sequence's keys ("flash-decoding"), then a log-sum-exp combine.
+// sequence's keys ("flash-decoding") with a log-sum-exp merge of the splits.
 //
 // What it computes is defined in "How serving works in Tlaloc", section 2
 // (gather through the block table, dot, masked softmax, dot; causal length =
-// position + 1) and section 3 (sliding window p-W+1 .. p).  The split-K merge
-// is the same fold as the page's "Blockwise attention" bullet (running max,
-// running sum, running P.V), applied across CTAs instead of loop iterations.
+// position + 1) and section 3 (sliding window p-W+1 .. p).  The split merge
+// is the fold of the page's "Blockwise attention" bullet (running max, running
+// sum, running P.V), applied across work items instead of loop iterations.
 //
-// Three launches on the caller's stream:
-//   1. decode_plan_kernel (1 CTA): per sequence, the 16-key chunks it reads
-//      ([lo/16, p/16]); a split size (in chunks) that gives about
-//      kTargetItems work items for the whole batch; an exclusive scan of the
-//      splits per sequence.  Zeroes the work counter.
-//   2. decode_bf16_kernel / decode_f32_kernel (persistent, 2 CTAs per SM):
-//      CTAs take work items (split s, KV head g) from an atomic counter.  The 4
-//      warps of a CTA take the item's chunks round-robin; each warp streams its
-//      chunks' K and V rows from the pool into its own shared-memory ring with
-//      16-byte cp.async (3 stages), and keeps a running (max, sum, P.V) per
-//      query head of the group.  bf16: Q.K^T and P.V run on mma.sync
-//      m16n8k16 with the query-head group as the M rows, so the ALUs stay far
-//      from the limit even at 8 query heads per KV head.  The warps' states
-//      are merged in shared memory and written as one partial per (split,
-//      query head).
-//   3. decode_combine_kernel: one warp per (sequence, query head) merges the
-//      sequence's partials in split order.
+// Launches on the caller's stream:
+//   1. decode_plan_kernel (1 CTA): per sequence the 16-key chunks it reads
+//      ([lo/16, p/16]); a split size (in chunks) giving about kTargetItems
+//      work items for the batch; an exclusive scan of the splits per
+//      sequence.  Zeroes the work counter and the per-(sequence, KV head)
+//      completion counters, and writes the zero output of empty sequences.
+//   2. bf16: decode_bf16_ws_kernel, persistent, one CTA per SM, warp
+//      specialised.  A producer warp takes work items (split x KV head) from
+//      an atomic counter and streams each item's chunks (16 keys of K and V,
+//      8 KiB at d=128) with 16-byte cp.async into a ring of shared-memory
+//      stages, completing each stage on an mbarrier; the block table is read
+//      32 entries at a time, ahead of the copies.  Eight consumer warps take
+//      the item's chunks round-robin: Q.K^T and P.V on mma.sync m16n8k16 with
+//      the query-head group as the M rows, online softmax in registers.  At
+//      the end of an item the consumers merge their states in shared memory;
+//      a sequence with one split writes its output directly, otherwise the
+//      item writes a partial and the CTA that completes the last split of a
+//      (sequence, KV head) merges all its partials (no waiting: the
+//      completion counter is read once).  The producer runs ahead across item
+//      boundaries, so the memory pipe stays full while consumers merge.
+//      f32: decode_f32_kernel (CUDA-core dots in f32) writes partials, and
+//      decode_combine_kernel merges them.
 // Every reduction has a fixed order, so results repeat bit for bit and do not
 // depend on the pool's page placement.
 #include "common.cuh"
 
 namespace tl {
 
-constexpr int kChunk = 16;           // keys per step (one mma N=16 / K=16 tile)
-constexpr int kTargetItems = 8192;   // work items (split x KV head) per call
-constexpr int kMinSplitChunks = 8;   // 128 keys
-constexpr int kDecodeWarps = 4;
+constexpr int kChunk = 16;            // keys per step (one mma N=16 / K=16 tile)
+constexpr int kTargetItems = 12288;   // work items (split x KV head) per call
+constexpr int kMinSplitChunks = 8;    // 128 keys
+constexpr int kDecodeWarps = 4;       // f32 kernel
 constexpr int kDecodeThreads = kDecodeWarps * 32;
-constexpr int kStages = 3;
+constexpr int kConsumers = 8;         // bf16 kernel: consumer warps
+constexpr int kWsThreads = (kConsumers + 1) * 32;
 
 inline int64_t decode_max_splits(int B, int h_kv) {
   return (int64_t)(kTargetItems + h_kv - 1) / h_kv + B;
@@ -44,6 +50,7 @@ inline int64_t decode_max_splits(int B, int h_kv) {
 struct DecodeWorkspace {
   int32_t* ctrl;       // [0] split size in chunks, [1] total splits, [2] work counter
   int32_t* split_off;  // [B+1] first split of each sequence
+  int32_t* done;       // [B*h_kv] splits finished per (sequence, KV head)
   float* ml;           // [max_splits][h_q][2]   (running max in log2 units, sum)
   float* acc;          // [max_splits][h_q][d]   (unnormalised P.V)
 };
@@ -56,6 +63,8 @@ inline size_t decode_ws_layout(int B, int h_q, int h_kv, int d, DecodeWorkspace*
   off += 256;
   const size_t so = off;
   off = align_up(off + sizeof(int32_t) * (size_t)(B + 1), 256);
+  const size_t dn = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)B * h_kv, 256);
   const size_t ml = off;
   off = align_up(off + sizeof(float) * 2 * (size_t)ms * h_q, 256);
   const size_t acc = off;
@@ -63,6 +72,7 @@ inline size_t decode_ws_layout(int B, int h_q, int h_kv, int d, DecodeWorkspace*
   if (w) {
     w->ctrl = reinterpret_cast<int32_t*>(base + ctrl);
     w->split_off = reinterpret_cast<int32_t*>(base + so);
+    w->done = reinterpret_cast<int32_t*>(base + dn);
     w->ml = reinterpret_cast<float*>(base + ml);
     w->acc = reinterpret_cast<float*>(base + acc);
   }
@@ -77,7 +87,7 @@ struct DecodeParams {
   const int32_t* context_lens;
   float* out;
   int32_t max_pages_per_seq;
-  int32_t B, h_q, h_kv, group;
+  int32_t B, h_q, h_kv, group, d;
   int32_t num_pages, page_size, window;
   float scale_log2;  // scale * log2(e): scores are kept in log2 units
   DecodeWorkspace ws;
@@ -85,20 +95,21 @@ struct DecodeParams {
 };
 
 // Causal range of sequence b: keys lo..p (empty when L <= 0 or L too long).
-__device__ __forceinline__ void seq_range(const DecodeParams& P, int b, int& lo, int& p) {
+__device__ __forceinline__ void seq_range(const DecodeParams& P, int b, int& lo, int& p,
+                                          bool report_errors) {
   const int L = P.context_lens[b];
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
   p = L - 1;
   if (L > cap) {
-    report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
+    if (report_errors) report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
     p = -1;
   }
   lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
 }
 
-__device__ __forceinline__ int seq_chunks(const DecodeParams& P, int b) {
+__device__ __forceinline__ int seq_chunks(const DecodeParams& P, int b, bool report_errors) {
   int lo, p;
-  seq_range(P, b, lo, p);
+  seq_range(P, b, lo, p, report_errors);
   return p < 0 ? 0 : p / kChunk - lo / kChunk + 1;
 }
 
@@ -111,11 +122,12 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5;
   const int nwarps = nt >> 5;
   long long total = 0;
-  for (int b = tid; b < P.B; b += nt) total += seq_chunks(P, b);
+  for (int b = tid; b < P.B; b += nt) total += seq_chunks(P, b, true);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
   if (lane == 0) red[wid] = total;
   if (tid == 0) carry_s = 0;
+  for (int i = tid; i < P.B * P.h_kv; i += nt) P.ws.done[i] = 0;
   __syncthreads();
   long long total_chunks = 0;
   for (int w = 0; w < nwarps; ++w) total_chunks += red[w];
@@ -124,7 +136,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
   // exclusive scan of the splits per sequence, nt sequences at a time
   for (int base = 0; base < P.B; base += nt) {
     const int b = base + tid;
-    const int n = b < P.B ? (seq_chunks(P, b) + split - 1) / split : 0;
+    const int n = b < P.B ? (seq_chunks(P, b, false) + split - 1) / split : 0;
     int x = n;  // inclusive scan within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -157,348 +169,469 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
     P.ws.ctrl[1] = carry_s;
     P.ws.ctrl[2] = 0;
   }
+  // sequences with nothing to read output 0 (no work item writes them)
+  for (int b = 0; b < P.B; ++b) {
+    if (seq_chunks(P, b, false) > 0) continue;
+    float* o = P.out + (size_t)b * P.h_q * P.d;
+    for (int i = tid; i < P.h_q * P.d; i += nt) o[i] = 0.f;
+  }
 }
 
-// Work item -> (sequence, split within the sequence): the last b with
-// split_off[b] <= s.
+// Work item -> sequence: the last b with split_off[b] <= s.
 __device__ __forceinline__ int find_seq(const int32_t* split_off, int B, int s) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(split_off + mid) <= s) lo = mid; else hi = mid - 1;
+    if (__ldcg(split_off + mid) <= s) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 struct ItemInfo {
   int b, g, lo, p, c_begin, c_end;  // chunks [c_begin, c_end)
+  int s_global, nsplits;            // split index in the partial arrays; splits of b
 };
 
-__device__ __forceinline__ bool next_item(const DecodeParams& P, int* s_item, ItemInfo& it) {
-  if (threadIdx.x == 0) *s_item = atomicAdd(P.ws.ctrl + 2, 1);
-  __syncthreads();
-  const int item = *s_item;
-  const int total = P.ws.ctrl[1] * P.h_kv;
-  __syncthreads();  // everyone has read *s_item before it is rewritten
-  if (item >= total) return false;
+__device__ __forceinline__ void describe_item(const DecodeParams& P, int item, ItemInfo& it) {
   const int s = item / P.h_kv;
   it.g = item - s * P.h_kv;
   it.b = find_seq(P.ws.split_off, P.B, s);
-  const int split = P.ws.ctrl[0];
-  const int k = s - P.ws.split_off[it.b];
-  seq_range(P, it.b, it.lo, it.p);
+  const int split = __ldcg(P.ws.ctrl + 0);
+  const int s0 = __ldcg(P.ws.split_off + it.b);
+  it.nsplits = __ldcg(P.ws.split_off + it.b + 1) - s0;
+  it.s_global = s;
+  seq_range(P, it.b, it.lo, it.p, false);
   const int c0 = it.lo / kChunk, c1 = it.p / kChunk + 1;
-  it.c_begin = c0 + k * split;
+  it.c_begin = c0 + (s - s0) * split;
   it.c_end = min(c1, it.c_begin + split);
-  return true;
 }
 
-// Merge the per-warp states in shared memory and write the item's partial.
-// Warp w's rows start at merge + w*warp_stride: row r holds P.V in [0, D),
-// the running max (log2 units) at D and the running sum at D+1.
-template <int D>
-__device__ __forceinline__ void merge_and_store(const DecodeParams& P, const ItemInfo& it,
-                                                int s_global, const float* merge,
-                                                int warp_stride) {
-  constexpr int RS = D + 2;
-  for (int idx = threadIdx.x; idx < P.group * (D + 1); idx += kDecodeThreads) {
-    const int r = idx / (D + 1), e = idx - r * (D + 1);
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, merge[w * warp_stride + r * RS + D]);
-    float a = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) {
-      const float* mr = merge + w * warp_stride + r * RS;
-      const float f = mr[D] == -INFINITY ? 0.f : fast_exp2(mr[D] - M);
-      a += f * (e < D ? mr[e] : mr[D + 1]);
-    }
-    const size_t row = (size_t)s_global * P.h_q + (size_t)it.g * P.group + r;
-    if (e < D) {
-      P.ws.acc[row * D + e] = a;
-    } else {
-      P.ws.ml[row * 2 + 0] = M;
-      P.ws.ml[row * 2 + 1] = a;
-    }
-  }
-}
-
-__device__ __forceinline__ int item_split_index(const DecodeParams& P, const ItemInfo& it) {
-  return __ldg(P.ws.split_off + it.b) + (it.c_begin - it.lo / kChunk) / P.ws.ctrl[0];
-}
-
-// ------------------------------------------------------------ bf16 kernel --
+// ------------------------------------------------- bf16, warp specialised --
 //
-// Per warp and stage: K chunk then V chunk, 16 rows of D bf16 each.  Row r's
-// 16-byte unit u is stored at unit u ^ (r & 7) so that ldmatrix reads of 8
-// rows hit 8 different bank groups.
+// Shared memory: a ring of kRing stages (K chunk then V chunk, 16 rows of D
+// bf16 each; row r's 16-byte unit u sits at unit u ^ (r & 7) so that ldmatrix
+// reads of 8 rows hit 8 different bank groups), two Q slots (16 rows each),
+// and the consumers' merge rows.
 
 template <int D>
-struct Bf16Smem {
+struct WsSmem {
+  static constexpr int kRing = D == 128 ? 14 : 24;
   static constexpr int kRowBytes = D * 2;
-  static constexpr int kChunkBytes = kChunk * kRowBytes;      // one of K or V
-  static constexpr int kStageBytes = 2 * kChunkBytes;         // K + V
-  static constexpr int kWarpBytes = kStages * kStageBytes;
-  static constexpr int kMergeBytes = 16 * (D + 2) * 4;        // per warp
-  static_assert(kMergeBytes <= kWarpBytes, "merge area overlays the warp's ring");
-  static constexpr int kTotal = kDecodeWarps * kWarpBytes + 64;
+  static constexpr int kChunkBytes = kChunk * kRowBytes;  // one of K or V
+  static constexpr int kStageBytes = 2 * kChunkBytes;
+  static constexpr int kQBytes = 16 * kRowBytes;
+  static constexpr int kRS = D + 2;  // merge row: P.V, max, sum
+  static constexpr int kMergeBytes = kConsumers * 16 * kRS * 4;
+  static constexpr int kRingOff = 0;
+  static constexpr int kQOff = kRing * kStageBytes;
+  static constexpr int kMergeOff = kQOff + 2 * kQBytes;
+  static constexpr int kTotal = kMergeOff + kMergeBytes;
 };
 
-// Issue the cp.async copies of one chunk's K and V rows into a stage; returns
-// the mask of rows that hold a live key (bit r for row r).
-template <int D>
-__device__ __forceinline__ uint32_t issue_chunk(const DecodeParams& P, const ItemInfo& it,
-                                                int chunk, uint32_t stage_addr, int lane,
-                                                int elem_bytes) {
-  constexpr int U = D * 2 / 16;  // bf16: 16-byte units per row
-  const int r = lane >> 1;
-  const int j = chunk * kChunk + r;
-  bool live = j >= it.lo && j <= it.p;
-  int64_t page = 0;
-  if (live) {
-    page = __ldg(P.block_table + (size_t)it.b * P.max_pages_per_seq + j / P.page_size);
-    if (page < 0 || page >= P.num_pages) {
-      live = false;
-      report(P.error_word, TL_DEVERR_PAGE_RANGE);
-      page = 0;
-    }
-  }
-  const size_t row_elem =
-      (((size_t)page * P.page_size + (live ? j % P.page_size : 0)) * P.h_kv + it.g) * D;
-  const char* ks = static_cast<const char*>(P.k_cache) + row_elem * elem_bytes;
-  const char* vs = static_cast<const char*>(P.v_cache) + row_elem * elem_bytes;
-  const uint32_t kd = stage_addr + r * (D * 2);
-  const uint32_t vd = kd + Bf16Smem<D>::kChunkBytes;
-  const uint32_t nbytes = live ? 16u : 0u;
-#pragma unroll
-  for (int i = 0; i < U / 2; ++i) {
-    const int u = (lane & 1) + 2 * i;
-    const uint32_t phys = (uint32_t)((u ^ (r & 7)) << 4);
-    cp_async_16(kd + phys, ks + u * 16, nbytes);
-    cp_async_16(vd + phys, vs + u * 16, nbytes);
-  }
-  const uint32_t ballot = __ballot_sync(0xffffffffu, live);
-  uint32_t mask = 0;
-#pragma unroll
-  for (int rr = 0; rr < 16; ++rr) mask |= ((ballot >> (2 * rr)) & 1u) << rr;
-  return mask;
-}
+constexpr int kMaxRing = 24;
+
+struct ItemSlot {
+  int b, g, lo, p, c_begin, c_end, s_global, nsplits, first_gs;
+};
+
+struct WsShared {
+  unsigned long long full[kMaxRing], empty[kMaxRing], qfull[2], qempty[2], mfull, mdone, mdec;
+  uint32_t stage_mask[kMaxRing];
+  ItemSlot slot[2];
+  int abort_flag;
+  int last;
+};
 
 template <int D, bool TWO_ROWS>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodeParams P) {
+  using L = WsSmem<D>;
+  constexpr int kRing = L::kRing;
+  static_assert(kRing <= kMaxRing, "ring fits the barrier arrays");
+  constexpr int U = D / 8;  // 16-byte units per row
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int s_item;
+  __shared__ WsShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned char* wbase = smem + warp * Bf16Smem<D>::kWarpBytes;
-  const uint32_t wbase_u32 = smem_u32(wbase);
-  const int qr = lane >> 2, qc = (lane & 3) * 2;  // fragment row / column pair
-  ItemInfo it;
-  while (next_item(P, &s_item, it)) {
-    const int s_global = item_split_index(P, it);
-    // Q fragments (rows = query heads of the group, zero past the group)
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(P.q) +
-                              ((size_t)it.b * P.h_q + (size_t)it.g * P.group) * D;
-    uint32_t qa[D / 16][4];
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int e0 = ks * 16 + qc;
-      qa[ks][0] = qr < P.group ? *reinterpret_cast<const uint32_t*>(qb + qr * D + e0) : 0u;
-      qa[ks][2] = qr < P.group ? *reinterpret_cast<const uint32_t*>(qb + qr * D + e0 + 8) : 0u;
-      if (TWO_ROWS) {
-        qa[ks][1] =
-            qr + 8 < P.group ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * D + e0) : 0u;
-        qa[ks][3] = qr + 8 < P.group
-                        ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * D + e0 + 8)
-                        : 0u;
-      } else {
-        qa[ks][1] = 0u;
-        qa[ks][3] = 0u;
-      }
-    }
-    float o[D / 8][4];
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const uint32_t sbase = smem_u32(smem);
+  volatile int* abort_flag = &sh.abort_flag;
 
-    // this warp's chunks: c_begin + warp + 4*i
-    const int first = it.c_begin + warp;
-    const int n_my = first < it.c_end ? (it.c_end - first + kDecodeWarps - 1) / kDecodeWarps : 0;
-    // live-row masks of the chunks in flight, oldest first (registers)
-    uint32_t mq[kStages - 1];
-#pragma unroll
-    for (int st = 0; st < kStages - 1; ++st) {
-      mq[st] = 0u;
-      if (st < n_my)
-        mq[st] = issue_chunk<D>(P, it, first + st * kDecodeWarps,
-                                wbase_u32 + st * Bf16Smem<D>::kStageBytes, lane, 2);
-      cp_async_commit();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(smem_u32(&sh.full[i]), 33);  // 32 copy-completion arrivals + the mask
+      mbar_init(smem_u32(&sh.empty[i]), 1);
     }
-    for (int i = 0; i < n_my; ++i) {
-      uint32_t newest = 0u;
-      {
-        const int ni = i + kStages - 1;
-        if (ni < n_my)
-          newest = issue_chunk<D>(P, it, first + ni * kDecodeWarps,
-                                  wbase_u32 + (ni % kStages) * Bf16Smem<D>::kStageBytes, lane, 2);
-        cp_async_commit();
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh.qfull[i]), 33);
+      mbar_init(smem_u32(&sh.qempty[i]), kConsumers);
+    }
+    mbar_init(smem_u32(&sh.mfull), kConsumers);
+    mbar_init(smem_u32(&sh.mdone), kConsumers);
+    mbar_init(smem_u32(&sh.mdec), 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
+
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer
+    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(P.k_cache);
+    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(P.v_cache);
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
+    uint32_t gs = 0;
+    int win_b = -1, win_blk0 = 0, win_val = -1;
+    for (int item_seq = 0;; ++item_seq) {
+      int item = 0;
+      if (lane == 0) item = atomicAdd(P.ws.ctrl + 2, 1);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      const int slot = item_seq & 1;
+      if (!mbar_wait(smem_u32(&sh.qempty[slot]), ((item_seq >> 1) & 1) ^ 1, abort_flag)) break;
+      if (item >= total_items) {
+        if (lane == 0) sh.slot[slot].b = -1;
+        __syncwarp();
+        mbar_arrive(smem_u32(&sh.qfull[slot]));
+        if (lane == 0) mbar_arrive(smem_u32(&sh.qfull[slot]));
+        break;
       }
-      cp_async_wait<kStages - 1>();
+      ItemInfo it;
+      describe_item(P, item, it);
+      // Q rows of the group -> the slot (row-major, D bf16 per row)
+      const uint32_t qdst = sbase + L::kQOff + slot * L::kQBytes;
+      const __nv_bfloat16* qsrc = qg + ((size_t)it.b * P.h_q + (size_t)it.g * P.group) * D;
+      for (int idx = lane; idx < P.group * U; idx += 32)
+        cp_async_16(qdst + idx * 16, qsrc + idx * 8, 16u);
+      cp_async_mbar_arrive(smem_u32(&sh.qfull[slot]));
+      if (lane == 0) {
+        ItemSlot& d = sh.slot[slot];
+        d.b = it.b; d.g = it.g; d.lo = it.lo; d.p = it.p;
+        d.c_begin = it.c_begin; d.c_end = it.c_end;
+        d.s_global = it.s_global; d.nsplits = it.nsplits; d.first_gs = (int)gs;
+        mbar_arrive(smem_u32(&sh.qfull[slot]));
+      }
+      const int last_blk = it.p / P.page_size;
+      const int32_t* bt_row = P.block_table + (size_t)it.b * P.max_pages_per_seq;
+      bool stop = false;
+      for (int c = it.c_begin; c < it.c_end; ++c, ++gs) {
+        const int stage = (int)(gs % kRing);
+        if (!mbar_wait(smem_u32(&sh.empty[stage]), ((gs / kRing) & 1) ^ 1, abort_flag)) {
+          stop = true;
+          break;
+        }
+        const int j0 = c * kChunk;
+        // block-table window: 32 consecutive logical blocks of this sequence
+        const int bmin = j0 / P.page_size;
+        const int bmax = min((j0 + kChunk - 1) / P.page_size, last_blk);
+        if (win_b != it.b || bmin < win_blk0 || bmax >= win_blk0 + 32) {
+          win_b = it.b;
+          win_blk0 = bmin;
+          const int blk = win_blk0 + lane;
+          win_val = blk <= last_blk ? __ldg(bt_row + blk) : -1;
+        }
+        const int r = lane >> 1;
+        const int j = j0 + r;
+        bool live = j >= it.lo && j <= it.p;
+        const int src = live ? j / P.page_size - win_blk0 : 0;
+        int page = __shfl_sync(0xffffffffu, win_val, src & 31);
+        if (live && (page < 0 || page >= P.num_pages)) {
+          report(P.error_word, TL_DEVERR_PAGE_RANGE);
+          live = false;
+        }
+        if (!live) page = 0;
+        const size_t row =
+            (((size_t)page * P.page_size + (live ? j % P.page_size : 0)) * P.h_kv + it.g) * D;
+        const uint32_t kd = sbase + L::kRingOff + stage * L::kStageBytes + r * L::kRowBytes;
+        const uint32_t vd = kd + L::kChunkBytes;
+        const uint32_t nbytes = live ? 16u : 0u;
+#pragma unroll
+        for (int i = 0; i < U / 2; ++i) {
+          const int u = (lane & 1) + 2 * i;
+          const uint32_t phys = (uint32_t)((u ^ (r & 7)) << 4);
+          cp_async_16(kd + phys, kc + row + u * 8, nbytes);
+          cp_async_16(vd + phys, vc + row + u * 8, nbytes);
+        }
+        const uint32_t ballot = __ballot_sync(0xffffffffu, live);
+        cp_async_mbar_arrive(smem_u32(&sh.full[stage]));
+        if (lane == 0) {
+          uint32_t mask = 0;
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) mask |= ((ballot >> (2 * rr)) & 1u) << rr;
+          sh.stage_mask[stage] = mask;
+          mbar_arrive(smem_u32(&sh.full[stage]));
+        }
+      }
+      if (stop) break;
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int qr = lane >> 2, qc = (lane & 3) * 2;
+    float* merge = reinterpret_cast<float*>(smem + L::kMergeOff);
+    for (int item_seq = 0;; ++item_seq) {
+      const int slot = item_seq & 1;
+      if (!mbar_wait(smem_u32(&sh.qfull[slot]), (item_seq >> 1) & 1, abort_flag)) break;
+      const ItemSlot it = sh.slot[slot];
+      if (it.b < 0) break;
+      // Q fragments (rows = query heads of the group, zero past the group)
+      const unsigned char* qs = smem + L::kQOff + slot * L::kQBytes;
+      uint32_t qa[D / 16][4];
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int e0 = ks * 16 + qc;
+        qa[ks][0] =
+            qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0) * 2) : 0u;
+        qa[ks][2] =
+            qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0 + 8) * 2) : 0u;
+        if (TWO_ROWS) {
+          qa[ks][1] = qr + 8 < P.group
+                          ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0) * 2)
+                          : 0u;
+          qa[ks][3] = qr + 8 < P.group
+                          ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0 + 8) * 2)
+                          : 0u;
+        } else {
+          qa[ks][1] = 0u;
+          qa[ks][3] = 0u;
+        }
+      }
       __syncwarp();
-      const int st = i % kStages;
-      const uint32_t mask = mq[0];
+      if (lane == 0) mbar_arrive(smem_u32(&sh.qempty[slot]));
+
+      float o[D / 8][4];
 #pragma unroll
-      for (int k = 0; k < kStages - 2; ++k) mq[k] = mq[k + 1];
-      mq[kStages - 2] = newest;
-      const uint32_t kaddr = wbase_u32 + st * Bf16Smem<D>::kStageBytes;
-      const uint32_t vaddr = kaddr + Bf16Smem<D>::kChunkBytes;
-      // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys)
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int tok = (mi >> 1) * 8 + ri;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int u = 2 * ks + (mi & 1);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kaddr + tok * (D * 2) + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
-          mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+      for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      const int n_chunks = it.c_end - it.c_begin;
+      bool stop = false;
+      for (int k = warp; k < n_chunks; k += kConsumers) {
+        const uint32_t gs = (uint32_t)it.first_gs + (uint32_t)k;
+        const int stage = (int)(gs % kRing);
+        if (!mbar_wait(smem_u32(&sh.full[stage]), (gs / kRing) & 1, abort_flag)) {
+          stop = true;
+          break;
         }
-      }
-      // mask and scale (log2 units)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+        const uint32_t mask = sh.stage_mask[stage];
+        const uint32_t kaddr = sbase + L::kRingOff + stage * L::kStageBytes;
+        const uint32_t vaddr = kaddr + L::kChunkBytes;
+        // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys)
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          const int mi = lane >> 3, ri = lane & 7;
+          const int tok = (mi >> 1) * 8 + ri;
 #pragma unroll
-      for (int n = 0; n < 2; ++n) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = n * 8 + qc + e;
-          const bool ok = (mask >> key) & 1u;
-          s[n][e] = ok ? s[n][e] * P.scale_log2 : -INFINITY;
-          s[n][2 + e] = ok ? s[n][2 + e] * P.scale_log2 : -INFINITY;
-          mx0 = fmaxf(mx0, s[n][e]);
-          mx1 = fmaxf(mx1, s[n][2 + e]);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int u = 2 * ks + (mi & 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(kaddr + tok * L::kRowBytes + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          }
         }
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      const float mn0 = fmaxf(m0, mx0);
-      const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
-      const float c0 = fast_exp2(m0 - base0);
-      m0 = mn0;
-      float p[2][4];
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        p[n][0] = fast_exp2(s[n][0] - base0);
-        p[n][1] = fast_exp2(s[n][1] - base0);
-      }
-      l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-      float c1 = c0;
-      if (TWO_ROWS) {
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn1 = fmaxf(m1, mx1);
-        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        c1 = fast_exp2(m1 - base1);
-        m1 = mn1;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
-          p[n][2] = fast_exp2(s[n][2] - base1);
-          p[n][3] = fast_exp2(s[n][3] - base1);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = n * 8 + qc + e;
+            const bool ok = (mask >> key) & 1u;
+            s[n][e] = ok ? s[n][e] * P.scale_log2 : -INFINITY;
+            s[n][2 + e] = ok ? s[n][2 + e] * P.scale_log2 : -INFINITY;
+            mx0 = fmaxf(mx0, s[n][e]);
+            mx1 = fmaxf(mx1, s[n][2 + e]);
+          }
         }
-        l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-      }
-      // rows 8-15 carry either the second half of the group (TWO_ROWS) or the
-      // low bf16 part of rows 0-7's probabilities; both rescale with their row
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        const float mn0 = fmaxf(m0, mx0);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
+        const float c0 = fast_exp2(m0 - base0);
+        m0 = mn0;
+        float p[2][4];
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= c0;
-        o[n][1] *= c0;
-        o[n][2] *= c1;
-        o[n][3] *= c1;
-      }
-      // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
-      uint32_t h0, l0w, h2, l2w;
-      split_bf16x2(p[0][0], p[0][1], h0, l0w);
-      split_bf16x2(p[1][0], p[1][1], h2, l2w);
-      {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int tok = (mi & 1) * 8 + ri;
-        if (!TWO_ROWS) {
-          // A rows 0-7 = hi part, rows 8-15 = lo part of the same query heads
+        for (int n = 0; n < 2; ++n) {
+          p[n][0] = fast_exp2(s[n][0] - base0);
+          p[n][1] = fast_exp2(s[n][1] - base0);
+        }
+        l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        float c1 = c0;
+        if (TWO_ROWS) {
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+          const float mn1 = fmaxf(m1, mx1);
+          const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+          c1 = fast_exp2(m1 - base1);
+          m1 = mn1;
 #pragma unroll
-          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-            const int u = 2 * nd2 + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(vaddr + tok * (D * 2) + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
-            mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
-            mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+          for (int n = 0; n < 2; ++n) {
+            p[n][2] = fast_exp2(s[n][2] - base1);
+            p[n][3] = fast_exp2(s[n][3] - base1);
           }
-        } else {
-          uint32_t h1, l1w, h3, l3w;
-          split_bf16x2(p[0][2], p[0][3], h1, l1w);
-          split_bf16x2(p[1][2], p[1][3], h3, l3w);
+          l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        }
+        // rows 8-15 hold either the second half of the group (TWO_ROWS) or
+        // the low bf16 part of rows 0-7's probabilities; both rescale by row
 #pragma unroll
-          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-            const int u = 2 * nd2 + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(vaddr + tok * (D * 2) + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
-            mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
-            mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
-            mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
-            mma_bf16_16816(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+        for (int n = 0; n < D / 8; ++n) {
+          o[n][0] *= c0;
+          o[n][1] *= c0;
+          o[n][2] *= c1;
+          o[n][3] *= c1;
+        }
+        // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
+        uint32_t h0, l0w, h2, l2w;
+        split_bf16x2(p[0][0], p[0][1], h0, l0w);
+        split_bf16x2(p[1][0], p[1][1], h2, l2w);
+        {
+          const int mi = lane >> 3, ri = lane & 7;
+          const int tok = (mi & 1) * 8 + ri;
+          if (!TWO_ROWS) {
+#pragma unroll
+            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+              const int u = 2 * nd2 + (mi >> 1);
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4_trans(vaddr + tok * L::kRowBytes + ((u ^ (tok & 7)) << 4), b0, b1,
+                                b2, b3);
+              mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
+              mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+            }
+          } else {
+            uint32_t h1, l1w, h3, l3w;
+            split_bf16x2(p[0][2], p[0][3], h1, l1w);
+            split_bf16x2(p[1][2], p[1][3], h3, l3w);
+#pragma unroll
+            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+              const int u = 2 * nd2 + (mi >> 1);
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4_trans(vaddr + tok * L::kRowBytes + ((u ^ (tok & 7)) << 4), b0, b1,
+                                b2, b3);
+              mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
+              mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
+              mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
+              mma_bf16_16816(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+            }
           }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[stage]));
+      }
+      if (stop) break;
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      if (TWO_ROWS) {
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      }
+      // this warp's state -> its merge rows
+      constexpr int RS = L::kRS;
+      float* mrow = merge + warp * 16 * RS;
+      if (qr < P.group) {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          mrow[qr * RS + n * 8 + qc] = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
+          mrow[qr * RS + n * 8 + qc + 1] = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
+        }
+        if ((lane & 3) == 0) {
+          mrow[qr * RS + D] = m0;
+          mrow[qr * RS + D + 1] = l0;
+        }
+      }
+      if (TWO_ROWS && qr + 8 < P.group) {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          mrow[(qr + 8) * RS + n * 8 + qc] = o[n][2];
+          mrow[(qr + 8) * RS + n * 8 + qc + 1] = o[n][3];
+        }
+        if ((lane & 3) == 0) {
+          mrow[(qr + 8) * RS + D] = m1;
+          mrow[(qr + 8) * RS + D + 1] = l1;
         }
       }
       __syncwarp();
-    }
-    cp_async_wait<0>();
-    __syncwarp();
-    // quad sums, then the warp's state into its merge rows
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    if (TWO_ROWS) {
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    }
-    // the warp's state goes into the start of its own ring (its copies are done)
-    constexpr int RS = D + 2;
-    float* mrow = reinterpret_cast<float*>(wbase);
-    if (qr < P.group) {
+      if (lane == 0) mbar_arrive(smem_u32(&sh.mfull));
+      if (!mbar_wait(smem_u32(&sh.mfull), item_seq & 1, abort_flag)) break;
+      // merge the consumers' states: one output (single split) or one partial
+      const int ct = threadIdx.x;  // 0 .. 32*kConsumers-1
+      const bool single = it.nsplits == 1;
+      for (int idx = ct; idx < P.group * (D + 1); idx += 32 * kConsumers) {
+        const int r = idx / (D + 1), e = idx - r * (D + 1);
+        float M = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        mrow[qr * RS + n * 8 + qc] = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
-        mrow[qr * RS + n * 8 + qc + 1] = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
-      }
-      if ((lane & 3) == 0) {
-        mrow[qr * RS + D] = m0;
-        mrow[qr * RS + D + 1] = l0;
-      }
-    }
-    if (TWO_ROWS && qr + 8 < P.group) {
+        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, merge[(w * 16 + r) * RS + D]);
+        float a = 0.f, lsum = 0.f;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        mrow[(qr + 8) * RS + n * 8 + qc] = o[n][2];
-        mrow[(qr + 8) * RS + n * 8 + qc + 1] = o[n][3];
+        for (int w = 0; w < kConsumers; ++w) {
+          const float* mr = merge + (w * 16 + r) * RS;
+          const float f = mr[D] == -INFINITY ? 0.f : fast_exp2(mr[D] - M);
+          if (e < D) a += f * mr[e];
+          if (single || e == D) lsum += f * mr[D + 1];
+        }
+        const int h = it.g * P.group + r;
+        if (single) {
+          if (e < D) P.out[((size_t)it.b * P.h_q + h) * D + e] = lsum > 0.f ? a / lsum : 0.f;
+        } else {
+          const size_t rowi = (size_t)it.s_global * P.h_q + h;
+          if (e < D) {
+            P.ws.acc[rowi * D + e] = a;
+          } else {
+            P.ws.ml[rowi * 2 + 0] = M;
+            P.ws.ml[rowi * 2 + 1] = lsum;
+          }
+        }
       }
-      if ((lane & 3) == 0) {
-        mrow[(qr + 8) * RS + D] = m1;
-        mrow[(qr + 8) * RS + D + 1] = l1;
+      if (!single) __threadfence();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.mdone));
+      if (warp == 0) {
+        if (!mbar_wait(smem_u32(&sh.mdone), item_seq & 1, abort_flag)) break;
+        if (lane == 0) {
+          int last = 0;
+          if (!single) {
+            int* cnt = P.ws.done + (size_t)it.b * P.h_kv + it.g;
+            const int old = atomicAdd(cnt, 1);
+            last = old == it.nsplits - 1;
+            if (last) atomicExch(cnt, 0);
+          }
+          sh.last = last;
+          mbar_arrive(smem_u32(&sh.mdec));
+        }
+        __syncwarp();
+      }
+      if (!mbar_wait(smem_u32(&sh.mdec), item_seq & 1, abort_flag)) break;
+      if (sh.last) {
+        // this CTA finished the last split of (b, g): merge all its partials
+        __threadfence();
+        const int s0 = it.s_global - (it.c_begin - it.lo / kChunk) / __ldcg(P.ws.ctrl + 0);
+        for (int idx = ct; idx < P.group * D; idx += 32 * kConsumers) {
+          const int r = idx / D, e = idx - r * D;
+          const int h = it.g * P.group + r;
+          float M = -INFINITY;
+          for (int sp = 0; sp < it.nsplits; ++sp)
+            M = fmaxf(M, __ldcg(P.ws.ml + ((size_t)(s0 + sp) * P.h_q + h) * 2));
+          float a = 0.f, lsum = 0.f;
+          for (int sp = 0; sp < it.nsplits; ++sp) {
+            const size_t rowi = (size_t)(s0 + sp) * P.h_q + h;
+            const float mi = __ldcg(P.ws.ml + rowi * 2);
+            const float f = mi == -INFINITY ? 0.f : fast_exp2(mi - M);
+            lsum += f * __ldcg(P.ws.ml + rowi * 2 + 1);
+            a += f * __ldcg(P.ws.acc + rowi * D + e);
+          }
+          P.out[((size_t)it.b * P.h_q + h) * D + e] = lsum > 0.f ? a / lsum : 0.f;
+        }
       }
     }
-    __syncthreads();
-    merge_and_store<D>(P, it, s_global, reinterpret_cast<const float*>(smem),
-                       Bf16Smem<D>::kWarpBytes / 4);
-    __syncthreads();
   }
+  __syncthreads();  // every wait above is bounded, so every thread gets here
+  if (threadIdx.x == 0 && sh.abort_flag) report(P.error_word, TL_DEVERR_TIMEOUT);
 }
 
 // ------------------------------------------------------------- f32 kernel --
 //
 // IEEE f32 pools ("How serving works in Tlaloc": f32 keys and values, dots in
 // f32).  Computed on the CUDA cores in f32: no tensor-core rounding of the
-// operands.  Each warp walks its chunks one key at a time: lanes hold D/32
-// elements of each query head, a warp sum gives each score, and a scalar
-// online softmax folds it in.
+// operands.  CTAs take work items from the counter; each warp walks its
+// chunks one key at a time (lanes hold D/32 elements of each query head, a
+// warp sum gives each score, a scalar online softmax folds it in); the warps
+// merge in shared memory and write a partial that decode_combine_kernel
+// merges.
 
 constexpr int kF32MaxGroup = 16;
 
@@ -509,9 +642,15 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_f32_kernel(DecodeParams
   __shared__ float merge[kDecodeWarps][kF32MaxGroup][RS];
   __shared__ int s_item;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  ItemInfo it;
-  while (next_item(P, &s_item, it)) {
-    const int s_global = item_split_index(P, it);
+  const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
+  for (;;) {
+    if (threadIdx.x == 0) s_item = atomicAdd(P.ws.ctrl + 2, 1);
+    __syncthreads();
+    const int item = s_item;
+    __syncthreads();
+    if (item >= total_items) break;
+    ItemInfo it;
+    describe_item(P, item, it);
     const float* qb =
         static_cast<const float*>(P.q) + ((size_t)it.b * P.h_q + (size_t)it.g * P.group) * D;
     float qv[kF32MaxGroup][E], o[kF32MaxGroup][E], m[kF32MaxGroup], l[kF32MaxGroup];
@@ -570,7 +709,25 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_f32_kernel(DecodeParams
       }
     }
     __syncthreads();
-    merge_and_store<D>(P, it, s_global, &merge[0][0][0], kF32MaxGroup * RS);
+    for (int idx = threadIdx.x; idx < P.group * (D + 1); idx += kDecodeThreads) {
+      const int r = idx / (D + 1), e = idx - r * (D + 1);
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, merge[w][r][D]);
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecodeWarps; ++w) {
+        const float f = merge[w][r][D] == -INFINITY ? 0.f : fast_exp2(merge[w][r][D] - M);
+        a += f * (e < D ? merge[w][r][e] : merge[w][r][D + 1]);
+      }
+      const size_t rowi = (size_t)it.s_global * P.h_q + (size_t)it.g * P.group + r;
+      if (e < D) {
+        P.ws.acc[rowi * D + e] = a;
+      } else {
+        P.ws.ml[rowi * 2 + 0] = M;
+        P.ws.ml[rowi * 2 + 1] = a;
+      }
+    }
     __syncthreads();
   }
 }
@@ -585,22 +742,23 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams P) {
   if (wi >= (int64_t)P.B * P.h_q) return;
   const int b = (int)(wi / P.h_q), h = (int)(wi - (int64_t)b * P.h_q);
   const int s0 = P.ws.split_off[b], s1 = P.ws.split_off[b + 1];
+  if (s1 == s0) return;  // written by the plan kernel
   float* out = P.out + (size_t)wi * D;
   float M = -INFINITY;
   for (int s = s0; s < s1; ++s) M = fmaxf(M, P.ws.ml[((size_t)s * P.h_q + h) * 2]);
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float L = 0.f;
+  float Lsum = 0.f;
   for (int s = s0; s < s1; ++s) {
     const size_t row = (size_t)s * P.h_q + h;
     const float mi = P.ws.ml[row * 2];
     const float f = mi == -INFINITY ? 0.f : fast_exp2(mi - M);
-    L += f * P.ws.ml[row * 2 + 1];
+    Lsum += f * P.ws.ml[row * 2 + 1];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] += f * P.ws.acc[row * D + lane * E + e];
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) out[lane * E + e] = acc[e] * inv;
 }
@@ -654,6 +812,7 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   P.h_q = h_q;
   P.h_kv = h_kv;
   P.group = group;
+  P.d = d;
   P.num_pages = num_pages;
   P.page_size = page_size;
   P.window = window;
@@ -666,29 +825,28 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   decode_plan_kernel<<<1, 1024, 0, st>>>(P, target_splits);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
 
-  const int grid = num_sms() * 2;
   if (dtype == TL_BF16) {
-#define TL_LAUNCH_BF16(DD, TWO)                                                           \
+#define TL_LAUNCH_WS(DD, TWO)                                                             \
   do {                                                                                    \
-    auto kern = decode_bf16_kernel<DD, TWO>;                                              \
-    const int sm = Bf16Smem<DD>::kTotal;                                                  \
+    auto kern = decode_bf16_ws_kernel<DD, TWO>;                                           \
+    const int sm = WsSmem<DD>::kTotal;                                                    \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
         cudaSuccess)                                                                      \
       return TL_ERR_CUDA;                                                                 \
-    kern<<<grid, kDecodeThreads, sm, st>>>(P);                                            \
+    kern<<<num_sms(), kWsThreads, sm, st>>>(P);                                           \
   } while (0)
     if (d == 128) {
-      if (group > 8) TL_LAUNCH_BF16(128, true); else TL_LAUNCH_BF16(128, false);
+      if (group > 8) TL_LAUNCH_WS(128, true); else TL_LAUNCH_WS(128, false);
     } else {
-      if (group > 8) TL_LAUNCH_BF16(64, true); else TL_LAUNCH_BF16(64, false);
+      if (group > 8) TL_LAUNCH_WS(64, true); else TL_LAUNCH_WS(64, false);
     }
-#undef TL_LAUNCH_BF16
-  } else {
-    if (d == 128) decode_f32_kernel<128><<<grid, kDecodeThreads, 0, st>>>(P);
-    else decode_f32_kernel<64><<<grid, kDecodeThreads, 0, st>>>(P);
+#undef TL_LAUNCH_WS
+    return launch_status();
   }
+  const int grid = num_sms() * 2;
+  if (d == 128) decode_f32_kernel<128><<<grid, kDecodeThreads, 0, st>>>(P);
+  else decode_f32_kernel<64><<<grid, kDecodeThreads, 0, st>>>(P);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
-
   const int64_t warps = (int64_t)B * h_q;
   const unsigned cblocks = (unsigned)((warps + 3) / 4);
   if (d == 128) decode_combine_kernel<128><<<cblocks, 128, 0, st>>>(P);
