@@ -115,6 +115,14 @@ TL_DEVINLINE void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
 TL_DEVINLINE void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16), completing `bytes` of transaction count on `bar`.
+TL_DEVINLINE void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 TL_DEVINLINE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -136,6 +144,16 @@ TL_DEVINLINE bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_f
       return false;
     }
   }
+  return true;
+}
+
+// Bounded wait that ignores the abort flag: used to drain a CTA's own copies
+// in flight before it exits.
+TL_DEVINLINE bool mbar_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
   return true;
 }
 

@@ -51,6 +51,7 @@ struct DecodeWorkspace {
   int32_t* ctrl;       // [0] split size in chunks, [1] total splits, [2] work counter
   int32_t* split_off;  // [B+1] first split of each sequence
   int32_t* done;       // [B*h_kv] splits finished per (sequence, KV head)
+  int4* desc;          // [max_splits][2] per-split descriptor (see SplitDesc)
   float* ml;           // [max_splits][h_q][2]   (running max in log2 units, sum)
   float* acc;          // [max_splits][h_q][d]   (unnormalised P.V)
 };
@@ -65,6 +66,8 @@ inline size_t decode_ws_layout(int B, int h_q, int h_kv, int d, DecodeWorkspace*
   off = align_up(off + sizeof(int32_t) * (size_t)(B + 1), 256);
   const size_t dn = off;
   off = align_up(off + sizeof(int32_t) * (size_t)B * h_kv, 256);
+  const size_t ds = off;
+  off = align_up(off + 2 * sizeof(int4) * (size_t)ms, 256);
   const size_t ml = off;
   off = align_up(off + sizeof(float) * 2 * (size_t)ms * h_q, 256);
   const size_t acc = off;
@@ -73,6 +76,7 @@ inline size_t decode_ws_layout(int B, int h_q, int h_kv, int d, DecodeWorkspace*
     w->ctrl = reinterpret_cast<int32_t*>(base + ctrl);
     w->split_off = reinterpret_cast<int32_t*>(base + so);
     w->done = reinterpret_cast<int32_t*>(base + dn);
+    w->desc = reinterpret_cast<int4*>(base + ds);
     w->ml = reinterpret_cast<float*>(base + ml);
     w->acc = reinterpret_cast<float*>(base + acc);
   }
@@ -157,7 +161,17 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
     __syncthreads();
     const int carry = carry_s;
     const int before = carry + (wid > 0 ? warp_incl[wid - 1] : 0) + x - n;
-    if (b < P.B) P.ws.split_off[b] = before;
+    if (b < P.B) {
+      P.ws.split_off[b] = before;
+      int lo, p;
+      seq_range(P, b, lo, p, false);
+      const int c0 = lo / kChunk, c1 = p / kChunk + 1;
+      for (int k = 0; k < n; ++k) {
+        const int cb = c0 + k * split;
+        P.ws.desc[2 * (before + k)] = make_int4(b, cb, min(c1, cb + split), n);
+        P.ws.desc[2 * (before + k) + 1] = make_int4(lo, p, before, 0);
+      }
+    }
     const int chunk_total = warp_incl[nwarps - 1];
     __syncthreads();
     if (tid == 0) carry_s = carry + chunk_total;
@@ -177,48 +191,45 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
   }
 }
 
-// Work item -> sequence: the last b with split_off[b] <= s.
-__device__ __forceinline__ int find_seq(const int32_t* split_off, int B, int s) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldcg(split_off + mid) <= s) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 struct ItemInfo {
   int b, g, lo, p, c_begin, c_end;  // chunks [c_begin, c_end)
   int s_global, nsplits;            // split index in the partial arrays; splits of b
 };
 
+// Split descriptor written by the plan kernel: {b, c_begin, c_end, nsplits},
+// {lo, p, first split of b, 0}.
 __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, ItemInfo& it) {
   const int s = item / P.h_kv;
+  const int4 d0 = __ldcg(P.ws.desc + 2 * s), d1 = __ldcg(P.ws.desc + 2 * s + 1);
   it.g = item - s * P.h_kv;
-  it.b = find_seq(P.ws.split_off, P.B, s);
-  const int split = __ldcg(P.ws.ctrl + 0);
-  const int s0 = __ldcg(P.ws.split_off + it.b);
-  it.nsplits = __ldcg(P.ws.split_off + it.b + 1) - s0;
+  it.b = d0.x;
+  it.c_begin = d0.y;
+  it.c_end = d0.z;
+  it.nsplits = d0.w;
+  it.lo = d1.x;
+  it.p = d1.y;
   it.s_global = s;
-  seq_range(P, it.b, it.lo, it.p, false);
-  const int c0 = it.lo / kChunk, c1 = it.p / kChunk + 1;
-  it.c_begin = c0 + (s - s0) * split;
-  it.c_end = min(c1, it.c_begin + split);
 }
 
 // ------------------------------------------------- bf16, warp specialised --
 //
-// Shared memory: a ring of kRing stages (K chunk then V chunk, 16 rows of D
-// bf16 each; row r's 16-byte unit u sits at unit u ^ (r & 7) so that ldmatrix
-// reads of 8 rows hit 8 different bank groups), two Q slots (16 rows each),
-// and the consumers' merge rows.
+// Shared memory: a ring of kRing stages (16 K rows then 16 V rows of D bf16,
+// each row padded by 16 bytes so that ldmatrix reads of 8 rows hit 8
+// different bank groups), two Q slots (up to 16 contiguous rows), and the
+// consumers' merge rows.  Every row lands by a 1-D bulk copy (one per
+// producer lane: lanes 0-15 the K rows, 16-31 the V rows), completing on the
+// stage's mbarrier by transaction bytes; a row with no live key is copied
+// from a zero row, so padding and garbage past a sequence's end never reach
+// the MMAs.
 
 template <int D>
 struct WsSmem {
   static constexpr int kRing = D == 128 ? 14 : 24;
   static constexpr int kRowBytes = D * 2;
-  static constexpr int kChunkBytes = kChunk * kRowBytes;  // one of K or V
+  static constexpr int kRowStride = kRowBytes + 16;
+  static constexpr int kChunkBytes = kChunk * kRowStride;  // one of K or V
   static constexpr int kStageBytes = 2 * kChunkBytes;
+  static constexpr int kStageTx = 2 * kChunk * kRowBytes;   // bytes the copies bring
   static constexpr int kQBytes = 16 * kRowBytes;
   static constexpr int kRS = D + 2;  // merge row: P.V, max, sum
   static constexpr int kMergeBytes = kConsumers * 16 * kRS * 4;
@@ -229,6 +240,9 @@ struct WsSmem {
 };
 
 constexpr int kMaxRing = 24;
+
+// A row of zeros in global memory: the source of every masked row's copy.
+__device__ __align__(256) unsigned char g_zero_row[256];
 
 struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits, first_gs;
@@ -247,7 +261,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
   using L = WsSmem<D>;
   constexpr int kRing = L::kRing;
   static_assert(kRing <= kMaxRing, "ring fits the barrier arrays");
-  constexpr int U = D / 8;  // 16-byte units per row
+  static_assert(D * 2 <= 256, "a zero row covers one K/V row");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ WsShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -256,11 +270,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
-      mbar_init(smem_u32(&sh.full[i]), 33);  // 32 copy-completion arrivals + the mask
+      mbar_init(smem_u32(&sh.full[i]), 1);  // the producer's expect-tx arrival
       mbar_init(smem_u32(&sh.empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh.qfull[i]), 33);
+      mbar_init(smem_u32(&sh.qfull[i]), 1);
       mbar_init(smem_u32(&sh.qempty[i]), kConsumers);
     }
     mbar_init(smem_u32(&sh.mfull), kConsumers);
@@ -278,90 +292,114 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
     const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(P.k_cache);
     const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(P.v_cache);
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
+    const bool is_k = lane < 16;
+    const int r = lane & 15;  // the row this lane copies
     uint32_t gs = 0;
-    int win_b = -1, win_blk0 = 0, win_val = -1;
-    for (int item_seq = 0;; ++item_seq) {
-      int item = 0;
-      if (lane == 0) item = atomicAdd(P.ws.ctrl + 2, 1);
-      item = __shfl_sync(0xffffffffu, item, 0);
+    int item_seq = 0;
+    // software pipeline over items: the current item's descriptor and the
+    // first window of its block table are loaded one item ahead
+    int grab = 0;
+    if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
+    int cur = __shfl_sync(0xffffffffu, grab, 0);
+    if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);  // the next item, read later
+    ItemInfo ci;
+    int cwin_blk0 = 0, cwin = -1;
+    if (cur < total_items) {
+      describe_item(P, cur, ci);
+      cwin_blk0 = ci.c_begin * kChunk / P.page_size;
+      const int blk = cwin_blk0 + lane;
+      cwin = blk <= ci.p / P.page_size
+                 ? __ldg(P.block_table + (size_t)ci.b * P.max_pages_per_seq + blk)
+                 : -1;
+    }
+    for (;; ++item_seq) {
       const int slot = item_seq & 1;
       if (!mbar_wait(smem_u32(&sh.qempty[slot]), ((item_seq >> 1) & 1) ^ 1, abort_flag)) break;
-      if (item >= total_items) {
-        if (lane == 0) sh.slot[slot].b = -1;
-        __syncwarp();
-        mbar_arrive(smem_u32(&sh.qfull[slot]));
-        if (lane == 0) mbar_arrive(smem_u32(&sh.qfull[slot]));
+      if (cur >= total_items) {
+        if (lane == 0) {
+          sh.slot[slot].b = -1;
+          mbar_arrive(smem_u32(&sh.qfull[slot]));
+        }
         break;
       }
-      ItemInfo it;
-      describe_item(P, item, it);
-      // Q rows of the group -> the slot (row-major, D bf16 per row)
-      const uint32_t qdst = sbase + L::kQOff + slot * L::kQBytes;
-      const __nv_bfloat16* qsrc = qg + ((size_t)it.b * P.h_q + (size_t)it.g * P.group) * D;
-      for (int idx = lane; idx < P.group * U; idx += 32)
-        cp_async_16(qdst + idx * 16, qsrc + idx * 8, 16u);
-      cp_async_mbar_arrive(smem_u32(&sh.qfull[slot]));
+      const int nxt = __shfl_sync(0xffffffffu, grab, 0);
+      if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);  // the one after
+      ItemInfo ni;
+      const bool has_next = nxt < total_items;
+      if (has_next) describe_item(P, nxt, ni);  // in flight during this item
+      int nwin_blk0 = 0, nwin = -1;
       if (lane == 0) {
         ItemSlot& d = sh.slot[slot];
-        d.b = it.b; d.g = it.g; d.lo = it.lo; d.p = it.p;
-        d.c_begin = it.c_begin; d.c_end = it.c_end;
-        d.s_global = it.s_global; d.nsplits = it.nsplits; d.first_gs = (int)gs;
-        mbar_arrive(smem_u32(&sh.qfull[slot]));
+        d.b = ci.b; d.g = ci.g; d.lo = ci.lo; d.p = ci.p;
+        d.c_begin = ci.c_begin; d.c_end = ci.c_end;
+        d.s_global = ci.s_global; d.nsplits = ci.nsplits; d.first_gs = (int)gs;
+        const uint32_t qbytes = (uint32_t)(P.group * D * 2);
+        mbar_arrive_expect_tx(smem_u32(&sh.qfull[slot]), qbytes);
+        bulk_g2s(sbase + L::kQOff + slot * L::kQBytes,
+                 qg + ((size_t)ci.b * P.h_q + (size_t)ci.g * P.group) * D, qbytes,
+                 smem_u32(&sh.qfull[slot]));
       }
-      const int last_blk = it.p / P.page_size;
-      const int32_t* bt_row = P.block_table + (size_t)it.b * P.max_pages_per_seq;
+      const int last_blk = ci.p / P.page_size;
+      const int32_t* bt_row = P.block_table + (size_t)ci.b * P.max_pages_per_seq;
+      const int n_chunks = ci.c_end - ci.c_begin;
+      const int prefetch_at = min(3, n_chunks - 1);
       bool stop = false;
-      for (int c = it.c_begin; c < it.c_end; ++c, ++gs) {
+      for (int k = 0; k < n_chunks; ++k, ++gs) {
+        const int c = ci.c_begin + k;
         const int stage = (int)(gs % kRing);
         if (!mbar_wait(smem_u32(&sh.empty[stage]), ((gs / kRing) & 1) ^ 1, abort_flag)) {
           stop = true;
           break;
         }
         const int j0 = c * kChunk;
-        // block-table window: 32 consecutive logical blocks of this sequence
         const int bmin = j0 / P.page_size;
         const int bmax = min((j0 + kChunk - 1) / P.page_size, last_blk);
-        if (win_b != it.b || bmin < win_blk0 || bmax >= win_blk0 + 32) {
-          win_b = it.b;
-          win_blk0 = bmin;
-          const int blk = win_blk0 + lane;
-          win_val = blk <= last_blk ? __ldg(bt_row + blk) : -1;
+        if (bmin < cwin_blk0 || bmax >= cwin_blk0 + 32) {  // next 32 blocks
+          cwin_blk0 = bmin;
+          const int blk = cwin_blk0 + lane;
+          cwin = blk <= last_blk ? __ldg(bt_row + blk) : -1;
         }
-        const int r = lane >> 1;
         const int j = j0 + r;
-        bool live = j >= it.lo && j <= it.p;
-        const int src = live ? j / P.page_size - win_blk0 : 0;
-        int page = __shfl_sync(0xffffffffu, win_val, src & 31);
+        bool live = j >= ci.lo && j <= ci.p;
+        int page = __shfl_sync(0xffffffffu, cwin, live ? (j / P.page_size - cwin_blk0) & 31 : 0);
         if (live && (page < 0 || page >= P.num_pages)) {
           report(P.error_word, TL_DEVERR_PAGE_RANGE);
           live = false;
         }
-        if (!live) page = 0;
-        const size_t row =
-            (((size_t)page * P.page_size + (live ? j % P.page_size : 0)) * P.h_kv + it.g) * D;
-        const uint32_t kd = sbase + L::kRingOff + stage * L::kStageBytes + r * L::kRowBytes;
-        const uint32_t vd = kd + L::kChunkBytes;
-        const uint32_t nbytes = live ? 16u : 0u;
-#pragma unroll
-        for (int i = 0; i < U / 2; ++i) {
-          const int u = (lane & 1) + 2 * i;
-          const uint32_t phys = (uint32_t)((u ^ (r & 7)) << 4);
-          cp_async_16(kd + phys, kc + row + u * 8, nbytes);
-          cp_async_16(vd + phys, vc + row + u * 8, nbytes);
+        const uint32_t mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
+        const unsigned char* src = g_zero_row;
+        if (live) {
+          const size_t row =
+              (((size_t)page * P.page_size + j % P.page_size) * P.h_kv + ci.g) * D;
+          src = reinterpret_cast<const unsigned char*>((is_k ? kc : vc) + row);
         }
-        const uint32_t ballot = __ballot_sync(0xffffffffu, live);
-        cp_async_mbar_arrive(smem_u32(&sh.full[stage]));
+        const uint32_t dst = sbase + L::kRingOff + stage * L::kStageBytes +
+                             (is_k ? 0 : L::kChunkBytes) + r * L::kRowStride;
         if (lane == 0) {
-          uint32_t mask = 0;
-#pragma unroll
-          for (int rr = 0; rr < 16; ++rr) mask |= ((ballot >> (2 * rr)) & 1u) << rr;
           sh.stage_mask[stage] = mask;
-          mbar_arrive(smem_u32(&sh.full[stage]));
+          mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), L::kStageTx);
+        }
+        __syncwarp();
+        bulk_g2s(dst, src, L::kRowBytes, smem_u32(&sh.full[stage]));
+        if (k == prefetch_at && has_next) {
+          nwin_blk0 = ni.c_begin * kChunk / P.page_size;
+          const int blk = nwin_blk0 + lane;
+          nwin = blk <= ni.p / P.page_size
+                     ? __ldg(P.block_table + (size_t)ni.b * P.max_pages_per_seq + blk)
+                     : -1;
         }
       }
       if (stop) break;
+      cur = nxt;
+      ci = ni;
+      cwin_blk0 = nwin_blk0;
+      cwin = nwin;
     }
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    // drain: every copy this CTA issued has landed before it exits
+    for (uint32_t i = gs > (uint32_t)kRing ? gs - kRing : 0; i < gs; ++i)
+      mbar_drain(smem_u32(&sh.full[i % kRing]), (i / kRing) & 1);
+    for (int i = item_seq > 2 ? item_seq - 2 : 0; i < item_seq; ++i)
+      mbar_drain(smem_u32(&sh.qfull[i & 1]), (i >> 1) & 1);
   } else {
     // ------------------------------------------------------------ consumers
     const int qr = lane >> 2, qc = (lane & 3) * 2;
@@ -421,7 +459,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
           for (int ks = 0; ks < D / 16; ++ks) {
             const int u = 2 * ks + (mi & 1);
             uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(kaddr + tok * L::kRowBytes + ((u ^ (tok & 7)) << 4), b0, b1, b2, b3);
+            ldmatrix_x4(kaddr + tok * L::kRowStride + (u << 4), b0, b1, b2, b3);
             mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
             mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
           }
@@ -488,8 +526,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
             for (int nd2 = 0; nd2 < D / 16; ++nd2) {
               const int u = 2 * nd2 + (mi >> 1);
               uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(vaddr + tok * L::kRowBytes + ((u ^ (tok & 7)) << 4), b0, b1,
-                                b2, b3);
+              ldmatrix_x4_trans(vaddr + tok * L::kRowStride + (u << 4), b0, b1, b2, b3);
               mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
               mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
             }
@@ -501,8 +538,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
             for (int nd2 = 0; nd2 < D / 16; ++nd2) {
               const int u = 2 * nd2 + (mi >> 1);
               uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(vaddr + tok * L::kRowBytes + ((u ^ (tok & 7)) << 4), b0, b1,
-                                b2, b3);
+              ldmatrix_x4_trans(vaddr + tok * L::kRowStride + (u << 4), b0, b1, b2, b3);
               mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
               mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
               mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
