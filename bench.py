@@ -162,11 +162,13 @@ def run_ours(args):
     bt_bytes = sum((L + 15) // 16 for L in lengths) * 4
     ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
     out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
-        tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping)
+        tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping,
+                             error_word=err)
         tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
-                                case.scale, out=out, workspace=ws)
+                                case.scale, out=out, workspace=ws, error_word=err)
 
     for _ in range(args.warmup):
         step()
@@ -188,10 +190,11 @@ def run_ours(args):
             torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping)
+            tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping,
+                                 error_word=err)
             dec_ev[i][0].record(stream)
             tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
-                                    case.scale, out=out, workspace=ws)
+                                    case.scale, out=out, workspace=ws, error_word=err)
             dec_ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
@@ -202,6 +205,8 @@ def run_ours(args):
             torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during the timed decode steps")
     elapsed_ms = start.elapsed_time(stop)
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
     elapsed_ms, total_kvb = reduce_over_ranks(elapsed_ms, kvb, dev)

@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
     const int r = lane & 15;  // the row this lane copies
     uint32_t gs = 0;
     int item_seq = 0;
+    int last_q_item = -1;  // the latest item whose Q copy was issued
     // software pipeline over items: the current item's descriptor and the
     // first window of its block table are loaded one item ahead
     int grab = 0;
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
         d.s_global = ci.s_global; d.nsplits = ci.nsplits; d.first_gs = (int)gs;
         const uint32_t qbytes = (uint32_t)(P.group * D * 2);
         mbar_arrive_expect_tx(smem_u32(&sh.qfull[slot]), qbytes);
+        last_q_item = item_seq;
         bulk_g2s(sbase + L::kQOff + slot * L::kQBytes,
                  qg + ((size_t)ci.b * P.h_q + (size_t)ci.g * P.group) * D, qbytes,
                  smem_u32(&sh.qfull[slot]));
@@ -395,11 +397,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
       cwin_blk0 = nwin_blk0;
       cwin = nwin;
     }
-    // drain: every copy this CTA issued has landed before it exits
+    // drain: every copy this CTA issued has landed before it exits (the last
+    // kRing stages are each their stage's latest phase; the latest Q copy is
+    // its slot's latest phase)
+    bool drained = true;
     for (uint32_t i = gs > (uint32_t)kRing ? gs - kRing : 0; i < gs; ++i)
-      mbar_drain(smem_u32(&sh.full[i % kRing]), (i / kRing) & 1);
-    for (int i = item_seq > 2 ? item_seq - 2 : 0; i < item_seq; ++i)
-      mbar_drain(smem_u32(&sh.qfull[i & 1]), (i >> 1) & 1);
+      drained &= mbar_drain(smem_u32(&sh.full[i % kRing]), (i / kRing) & 1);
+    last_q_item = __shfl_sync(0xffffffffu, last_q_item, 0);
+    if (last_q_item >= 0)
+      drained &= mbar_drain(smem_u32(&sh.qfull[last_q_item & 1]), (last_q_item >> 1) & 1);
+    if (!drained) *abort_flag = 1;
   } else {
     // ------------------------------------------------------------ consumers
     const int qr = lane >> 2, qc = (lane & 3) * 2;

@@ -15,20 +15,37 @@ DEV = "cuda"
 
 def gpu_write(g, error_word=None):
     hkv, d = g.k_cache.shape[2], g.k_cache.shape[3]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV) if error_word is None else error_word
     tl.tl_kv_cache_write(g.k_new.reshape(-1, hkv, d), g.v_new.reshape(-1, hkv, d), g.k_cache,
-                         g.v_cache, g.slot_mapping, error_word=error_word)
+                         g.v_cache, g.slot_mapping, error_word=err)
+    if error_word is None:
+        assert int(err.item()) == 0, f"device error word {int(err.item())}"
+
+
+def _clean_error_word():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
 
 
 def gpu_decode(g, window=None, error_word=None, out=None, workspace=None):
-    return tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
-                                   g.scale, window=g.window if window is None else window,
-                                   error_word=error_word, out=out, workspace=workspace)
+    """Decode through the C ABI; without a caller error word, checks that the
+    device-side checks reported nothing (no range error, no timed-out wait)."""
+    err = _clean_error_word() if error_word is None else error_word
+    out = tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                  g.scale, window=g.window if window is None else window,
+                                  error_word=err, out=out, workspace=workspace)
+    if error_word is None:
+        assert int(err.item()) == 0, f"device error word {int(err.item())}"
+    return out
 
 
 def gpu_prefill(g, window=None, error_word=None):
-    return tl.tl_paged_attn_prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.positions,
-                                    g.scale, window=g.window if window is None else window,
-                                    error_word=error_word)
+    err = _clean_error_word() if error_word is None else error_word
+    out = tl.tl_paged_attn_prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.positions,
+                                   g.scale, window=g.window if window is None else window,
+                                   error_word=err)
+    if error_word is None:
+        assert int(err.item()) == 0, f"device error word {int(err.item())}"
+    return out
 
 
 def sub_pool(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor, rows,
