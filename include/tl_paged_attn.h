@@ -132,7 +132,9 @@ size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, int32_t h_kv,
  *                are garbage afterwards.  Calls that overlap in time must not
  *                share a workspace.
  * Supported: dtype TL_BF16 or TL_F32, d in {64, 128}, h_q % h_kv == 0 with
- * h_q/h_kv <= 16, page_size in [1, 256].  Otherwise TL_ERR_UNSUPPORTED.
+ * h_q/h_kv <= 16, page_size in [1, 256] (a multiple of 8 for TL_BF16, whose
+ * pages move as TMA boxes of 8 or 16 rows), num_pages*page_size < 2^31.
+ * Otherwise TL_ERR_UNSUPPORTED.
  */
 tl_status tl_paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_table, int32_t max_pages_per_seq,

@@ -1,6 +1,7 @@
 // Device helpers shared by the paged-attention kernels (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -123,6 +124,19 @@ TL_DEVINLINE void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32
       ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Tiled TMA load of a 3-D box, completing its bytes on `bar`.  The
+// innermost coordinate times the element size must be a multiple of 16 bytes.
+TL_DEVINLINE void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+TL_DEVINLINE void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
 TL_DEVINLINE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -172,6 +186,12 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int num_sms();  // SM count of the current device (cached per device)
+
+// Encode a tiled bf16 tensor map of `rank` dims (dims[0] innermost, strides
+// in bytes for dims 1..rank-1) with the given box and 128-byte swizzle when
+// `swizzle128`; out-of-range boxes fill with zeros.  False on failure.
+bool encode_bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides, const uint32_t* box, bool swizzle128);
 
 inline tl_status launch_status() {
   cudaError_t e = cudaGetLastError();

@@ -213,36 +213,36 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 
 // ------------------------------------------------- bf16, warp specialised --
 //
-// Shared memory: a ring of kRing stages (16 K rows then 16 V rows of D bf16,
-// each row padded by 16 bytes so that ldmatrix reads of 8 rows hit 8
-// different bank groups), two Q slots (up to 16 contiguous rows), and the
-// consumers' merge rows.  Every row lands by a 1-D bulk copy (one per
-// producer lane: lanes 0-15 the K rows, 16-31 the V rows), completing on the
-// stage's mbarrier by transaction bytes; a row with no live key is copied
-// from a zero row, so padding and garbage past a sequence's end never reach
-// the MMAs.
+// Shared memory (1024-byte aligned): a ring of kRing stages, each the chunk's
+// K then V as [row half (64 elements = 128 B)][16 rows][128 B] in the TMA
+// 128-byte swizzle (16-byte unit u of row r sits at unit u ^ (r & 7), so
+// ldmatrix reads of 8 rows hit 8 different bank groups); two Q slots (up to
+// 16 contiguous rows); the consumers' merge rows.  The producer fills a stage
+// with tiled TMA boxes of kBoxRows rows (one page run, 8 or 16 rows) from a
+// 3-D tensor map of the pool (d, H_kv, slot), 4 boxes per 8 KiB chunk at page
+// size 16, all completing on the stage's mbarrier by transaction bytes.  A
+// box of a block past the sequence's last page, or of a bad page, is given
+// an out-of-range slot and arrives as zeros.  V rows past the sequence's last
+// position in its last page are zeroed by the consumer (they may hold
+// anything), so only finite values meet the zero probabilities.
 
 template <int D>
 struct WsSmem {
-  static constexpr int kRing = D == 128 ? 14 : 24;
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kRowStride = kRowBytes + 16;
-  static constexpr int kChunkBytes = kChunk * kRowStride;  // one of K or V
+  static constexpr int kHalves = D / 64;
+  static constexpr int kRing = D == 128 ? 16 : 28;
+  static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one half
+  static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
   static constexpr int kStageBytes = 2 * kChunkBytes;
-  static constexpr int kStageTx = 2 * kChunk * kRowBytes;   // bytes the copies bring
-  static constexpr int kQBytes = 16 * kRowBytes;
+  static constexpr int kQBytes = 16 * D * 2;
   static constexpr int kRS = D + 2;  // merge row: P.V, max, sum
   static constexpr int kMergeBytes = kConsumers * 16 * kRS * 4;
   static constexpr int kRingOff = 0;
   static constexpr int kQOff = kRing * kStageBytes;
   static constexpr int kMergeOff = kQOff + 2 * kQBytes;
-  static constexpr int kTotal = kMergeOff + kMergeBytes;
+  static constexpr int kTotal = kMergeOff + kMergeBytes + 1024;  // + alignment slack
 };
 
-constexpr int kMaxRing = 24;
-
-// A row of zeros in global memory: the source of every masked row's copy.
-__device__ __align__(256) unsigned char g_zero_row[256];
+constexpr int kMaxRing = 28;
 
 struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits, first_gs;
@@ -257,15 +257,17 @@ struct WsShared {
 };
 
 template <int D, bool TWO_ROWS>
-__global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(kWsThreads, 1)
+    decode_bf16_ws_kernel(DecodeParams P, const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap vmap, int box_rows) {
   using L = WsSmem<D>;
   constexpr int kRing = L::kRing;
   static_assert(kRing <= kMaxRing, "ring fits the barrier arrays");
-  static_assert(D * 2 <= 256, "a zero row covers one K/V row");
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ WsShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (sbase - smem_u32(smem_raw));
   volatile int* abort_flag = &sh.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -289,16 +291,20 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
-    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(P.k_cache);
-    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(P.v_cache);
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
-    const bool is_k = lane < 16;
-    const int r = lane & 15;  // the row this lane copies
+    const int n_slots = P.num_pages * P.page_size;
+    const int nbox = kChunk / box_rows;             // boxes per half
+    const int nreq = 2 * L::kHalves * nbox;         // TMA requests per chunk
+    // this lane's request (if lane < nreq): K or V, row half, box
+    const int rq_kind = lane / (L::kHalves * nbox);
+    const int rq_rem = lane % (L::kHalves * nbox);
+    const int rq_half = rq_rem / nbox, rq_box = rq_rem % nbox;
+    const CUtensorMap* rq_map = rq_kind == 0 ? &kmap : &vmap;
     uint32_t gs = 0;
     int item_seq = 0;
     int last_q_item = -1;  // the latest item whose Q copy was issued
-    // software pipeline over items: the current item's descriptor and the
-    // first window of its block table are loaded one item ahead
+    // software pipeline over items: the next item's descriptor and the first
+    // window of its block table are loaded one item ahead
     int grab = 0;
     if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
     int cur = __shfl_sync(0xffffffffu, grab, 0);
@@ -336,10 +342,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
         d.s_global = ci.s_global; d.nsplits = ci.nsplits; d.first_gs = (int)gs;
         const uint32_t qbytes = (uint32_t)(P.group * D * 2);
         mbar_arrive_expect_tx(smem_u32(&sh.qfull[slot]), qbytes);
-        last_q_item = item_seq;
         bulk_g2s(sbase + L::kQOff + slot * L::kQBytes,
                  qg + ((size_t)ci.b * P.h_q + (size_t)ci.g * P.group) * D, qbytes,
                  smem_u32(&sh.qfull[slot]));
+        last_q_item = item_seq;
       }
       const int last_blk = ci.p / P.page_size;
       const int32_t* bt_row = P.block_table + (size_t)ci.b * P.max_pages_per_seq;
@@ -356,38 +362,42 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
         const int j0 = c * kChunk;
         const int bmin = j0 / P.page_size;
         const int bmax = min((j0 + kChunk - 1) / P.page_size, last_blk);
-        if (bmin < cwin_blk0 || bmax >= cwin_blk0 + 32) {  // next 32 blocks
+        if (bmin < cwin_blk0 || bmax >= cwin_blk0 + 32) {  // the next 32 blocks
           cwin_blk0 = bmin;
           const int blk = cwin_blk0 + lane;
           cwin = blk <= last_blk ? __ldg(bt_row + blk) : -1;
         }
-        const int j = j0 + r;
-        bool live = j >= ci.lo && j <= ci.p;
-        int page = __shfl_sync(0xffffffffu, cwin, live ? (j / P.page_size - cwin_blk0) & 31 : 0);
-        if (live && (page < 0 || page >= P.num_pages)) {
-          report(P.error_word, TL_DEVERR_PAGE_RANGE);
+        // live rows (lanes 0-15: row = lane)
+        const int jr = j0 + (lane & 15);
+        const int pr = __shfl_sync(0xffffffffu, cwin, (jr / P.page_size - cwin_blk0) & 31);
+        bool live = jr >= ci.lo && jr <= ci.p;
+        if (live && (pr < 0 || pr >= P.num_pages)) {
+          if (lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
           live = false;
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
-        const unsigned char* src = g_zero_row;
-        if (live) {
-          const size_t row =
-              (((size_t)page * P.page_size + j % P.page_size) * P.h_kv + ci.g) * D;
-          src = reinterpret_cast<const unsigned char*>((is_k ? kc : vc) + row);
-        }
-        const uint32_t dst = sbase + L::kRingOff + stage * L::kStageBytes +
-                             (is_k ? 0 : L::kChunkBytes) + r * L::kRowStride;
+        // this lane's box: rows rq_box*box_rows.. of the chunk
+        const int jb = j0 + rq_box * box_rows;
+        const int blk = jb / P.page_size;
+        const int pb = __shfl_sync(0xffffffffu, cwin, (blk - cwin_blk0) & 31);
+        const bool box_ok = blk <= last_blk && pb >= 0 && pb < P.num_pages;
+        const int slot0 = box_ok ? pb * P.page_size + jb % P.page_size : n_slots;
         if (lane == 0) {
           sh.stage_mask[stage] = mask;
-          mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), L::kStageTx);
+          mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), L::kStageBytes);
         }
         __syncwarp();
-        bulk_g2s(dst, src, L::kRowBytes, smem_u32(&sh.full[stage]));
+        if (lane < nreq) {
+          const uint32_t dst = sbase + L::kRingOff + stage * L::kStageBytes +
+                               rq_kind * L::kChunkBytes + rq_half * L::kHalfBytes +
+                               rq_box * box_rows * 128;
+          tma_load_3d(dst, rq_map, rq_half * 64, ci.g, slot0, smem_u32(&sh.full[stage]));
+        }
         if (k == prefetch_at && has_next) {
           nwin_blk0 = ni.c_begin * kChunk / P.page_size;
-          const int blk = nwin_blk0 + lane;
-          nwin = blk <= ni.p / P.page_size
-                     ? __ldg(P.block_table + (size_t)ni.b * P.max_pages_per_seq + blk)
+          const int nb = nwin_blk0 + lane;
+          nwin = nb <= ni.p / P.page_size
+                     ? __ldg(P.block_table + (size_t)ni.b * P.max_pages_per_seq + nb)
                      : -1;
         }
       }
@@ -457,6 +467,23 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
         const uint32_t mask = sh.stage_mask[stage];
         const uint32_t kaddr = sbase + L::kRingOff + stage * L::kStageBytes;
         const uint32_t vaddr = kaddr + L::kChunkBytes;
+        {
+          // V rows past the sequence's end (last chunk only) may hold anything
+          const int first_dead = it.p + 1 - (it.c_begin + k) * kChunk;
+          if (first_dead < kChunk) {
+            const int n_dead = kChunk - max(first_dead, 0);
+            for (int idx = lane; idx < n_dead * L::kHalves * 8; idx += 32) {
+              const int row = kChunk - n_dead + idx / (L::kHalves * 8);
+              const int hu = idx % (L::kHalves * 8);
+              const uint32_t a =
+                  vaddr + (hu >> 3) * L::kHalfBytes + row * 128 + ((hu & 7) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u)
+                           : "memory");
+            }
+            fence_proxy_async_smem();  // before the stage returns to the TMA
+            __syncwarp();
+          }
+        }
         // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys)
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
@@ -466,7 +493,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
           for (int ks = 0; ks < D / 16; ++ks) {
             const int u = 2 * ks + (mi & 1);
             uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(kaddr + tok * L::kRowStride + (u << 4), b0, b1, b2, b3);
+            ldmatrix_x4(kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4),
+                        b0, b1, b2, b3);
             mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
             mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
           }
@@ -533,7 +561,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
             for (int nd2 = 0; nd2 < D / 16; ++nd2) {
               const int u = 2 * nd2 + (mi >> 1);
               uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(vaddr + tok * L::kRowStride + (u << 4), b0, b1, b2, b3);
+              ldmatrix_x4_trans(vaddr + (u >> 3) * L::kHalfBytes + tok * 128 +
+                                    (((u & 7) ^ (tok & 7)) << 4),
+                                b0, b1, b2, b3);
               mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
               mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
             }
@@ -545,7 +575,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_bf16_ws_kernel(DecodePar
             for (int nd2 = 0; nd2 < D / 16; ++nd2) {
               const int u = 2 * nd2 + (mi >> 1);
               uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(vaddr + tok * L::kRowStride + (u << 4), b0, b1, b2, b3);
+              ldmatrix_x4_trans(vaddr + (u >> 3) * L::kHalfBytes + tok * 128 +
+                                    (((u & 7) ^ (tok & 7)) << 4),
+                                b0, b1, b2, b3);
               mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
               mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
               mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
@@ -839,6 +871,9 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   const int group = h_q / h_kv;
   if (dtype != TL_BF16 && dtype != TL_F32) return TL_ERR_UNSUPPORTED;
   if ((d != 64 && d != 128) || group > 16 || page_size > 256) return TL_ERR_UNSUPPORTED;
+  // the bf16 path moves pages with TMA boxes of 8 or 16 rows
+  if (dtype == TL_BF16 && page_size % 8 != 0) return TL_ERR_UNSUPPORTED;
+  if ((int64_t)num_pages * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
   const size_t need = decode_ws_layout(B, h_q, h_kv, d, nullptr, nullptr);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TL_ERR_WORKSPACE;
@@ -869,6 +904,15 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
 
   if (dtype == TL_BF16) {
+    // 3-D tensor maps of the pools: (d, H_kv, slot), boxes of 64 x 1 x box_rows
+    const int box_rows = page_size % 16 == 0 ? 16 : 8;
+    CUtensorMap kmap, vmap;
+    const uint64_t dims[3] = {(uint64_t)d, (uint64_t)h_kv, (uint64_t)num_pages * page_size};
+    const uint64_t strides[2] = {(uint64_t)d * 2, (uint64_t)h_kv * d * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)box_rows};
+    if (!encode_bf16_tensor_map(&kmap, k_cache, 3, dims, strides, box, true) ||
+        !encode_bf16_tensor_map(&vmap, v_cache, 3, dims, strides, box, true))
+      return TL_ERR_CUDA;
 #define TL_LAUNCH_WS(DD, TWO)                                                             \
   do {                                                                                    \
     auto kern = decode_bf16_ws_kernel<DD, TWO>;                                           \
@@ -876,7 +920,7 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
         cudaSuccess)                                                                      \
       return TL_ERR_CUDA;                                                                 \
-    kern<<<num_sms(), kWsThreads, sm, st>>>(P);                                           \
+    kern<<<num_sms(), kWsThreads, sm, st>>>(P, kmap, vmap, box_rows);                     \
   } while (0)
     if (d == 128) {
       if (group > 8) TL_LAUNCH_WS(128, true); else TL_LAUNCH_WS(128, false);

@@ -81,17 +81,29 @@ def test_head_groupings(hq, hkv, d):
     assert_close(out, ref, f"hq={hq} hkv={hkv} d={d}")
 
 
-@pytest.mark.parametrize("page_size", [1, 7, 8, 32, 256])
-def test_page_sizes(page_size):
+@pytest.mark.parametrize("page_size,dtype", [(8, torch.bfloat16), (16, torch.bfloat16),
+                                             (24, torch.bfloat16), (32, torch.bfloat16),
+                                             (256, torch.bfloat16), (1, torch.float32),
+                                             (7, torch.float32)])
+def test_page_sizes(page_size, dtype):
     lens = [1, 5, 100, 513, 1500]
     case = wl.decode_case(lens, Hq=8, Hkv=2, d=128, page_size=page_size, window=300, seed=13,
-                          nan_unused=True)
+                          nan_unused=True, dtype=dtype)
     g = on_gpu(case)
     out = gpu_decode(g)
     torch.cuda.synchronize()
     ref = oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table,
                               case.context_lens, case.scale, window=300)
     assert_close(out, ref, f"page_size={page_size}")
+
+
+def test_bf16_page_size_not_multiple_of_8_is_refused():
+    case = wl.decode_case([40], Hq=4, Hkv=2, d=128, page_size=7, seed=14)
+    g = on_gpu(case)
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                g.scale)
+    assert e.value.status == tl.TL_ERR_UNSUPPORTED
 
 
 def test_page_placement_and_repeat_are_bit_identical():
