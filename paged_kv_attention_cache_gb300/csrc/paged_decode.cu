@@ -31,6 +31,8 @@
 //      decode_combine_kernel merges them.
 // Every reduction has a fixed order, so results repeat bit for bit and do not
 // depend on the pool's page placement.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace tl {
@@ -40,8 +42,6 @@ constexpr int kTargetItems = 12288;   // work items (split x KV head) per call
 constexpr int kMinSplitChunks = 8;    // 128 keys
 constexpr int kDecodeWarps = 4;       // f32 kernel
 constexpr int kDecodeThreads = kDecodeWarps * 32;
-constexpr int kConsumers = 8;         // bf16 kernel: consumer warps
-constexpr int kWsThreads = (kConsumers + 1) * 32;
 
 inline int64_t decode_max_splits(int B, int h_kv) {
   return (int64_t)(kTargetItems + h_kv - 1) / h_kv + B;
@@ -211,489 +211,458 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
   it.s_global = s;
 }
 
-// ------------------------------------------------- bf16, warp specialised --
+// ------------------------------------------------------ bf16 decode kernel --
 //
-// Shared memory (1024-byte aligned): a ring of kRing stages, each the chunk's
-// K then V as [row half (64 elements = 128 B)][16 rows][128 B] in the TMA
-// 128-byte swizzle (16-byte unit u of row r sits at unit u ^ (r & 7), so
-// ldmatrix reads of 8 rows hit 8 different bank groups); two Q slots (up to
-// 16 contiguous rows); the consumers' merge rows.  The producer fills a stage
-// with tiled TMA boxes of kBoxRows rows (one page run, 8 or 16 rows) from a
-// 3-D tensor map of the pool (d, H_kv, slot), 4 boxes per 8 KiB chunk at page
-// size 16, all completing on the stage's mbarrier by transaction bytes.  A
-// box of a block past the sequence's last page, or of a bad page, is given
-// an out-of-range slot and arrives as zeros.  V rows past the sequence's last
-// position in its last page are zeroed by the consumer (they may hold
-// anything), so only finite values meet the zero probabilities.
+// Persistent, one CTA per SM, every warp independent (no CTA barrier after
+// set-up).  A warp owns whole work items (split x KV head), taken from an
+// atomic counter, and streams their 16-key chunks through a private ring of
+// kRingW shared-memory stages: one lane issues the chunk's tiled TMA boxes
+// (a 3-D tensor map of the pool (d, H_kv, slot), boxes of 8 or 16 rows = one
+// page run, 4 boxes per 8 KiB chunk at page size 16) completing on the stage's
+// mbarrier by transaction bytes, kRingW-1 chunks ahead of the chunk the warp
+// computes.  The stream runs across item boundaries: the next items'
+// descriptors and block-table windows are loaded two items ahead, and each
+// item's Q rows arrive by a bulk copy into one of kRingW Q slots.  Stage
+// layout: K then V as [row half (64 elements = 128 B)][16 rows][128 B] in the
+// TMA 128-byte swizzle (16-byte unit u of row r at unit u ^ (r & 7), so
+// ldmatrix reads of 8 rows hit 8 different bank groups).  A box of a block
+// past the sequence's last page, or of a bad page, gets an out-of-range slot
+// and arrives as zeros; V rows past the last position in the last page are
+// zeroed before use (they may hold anything).  At the end of an item the
+// warp writes the output (one split) or a partial straight from its
+// registers; the warp that completes the last split of a (sequence, KV head)
+// merges its partials (the completion counter is read once, nobody waits).
+
+constexpr int kRingW = 3;     // stages per warp
+constexpr int kMaxWarpsW = 8;
 
 template <int D>
-struct WsSmem {
+struct WarpSmem {
   static constexpr int kHalves = D / 64;
-  static constexpr int kRing = D == 128 ? 16 : 28;
   static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one half
   static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
-  static constexpr int kStageBytes = 2 * kChunkBytes;
-  static constexpr int kQBytes = 16 * D * 2;
-  static constexpr int kRS = D + 2;  // merge row: P.V, max, sum
-  static constexpr int kMergeBytes = kConsumers * 16 * kRS * 4;
-  static constexpr int kRingOff = 0;
-  static constexpr int kQOff = kRing * kStageBytes;
-  static constexpr int kMergeOff = kQOff + 2 * kQBytes;
-  static constexpr int kTotal = kMergeOff + kMergeBytes + 1024;  // + alignment slack
+  static constexpr int kStageBytes = 2 * kChunkBytes;       // multiple of 1024
+  __host__ __device__ static int qslot_bytes(int group) {
+    return (group * D * 2 + 1023) / 1024 * 1024;
+  }
+  __host__ __device__ static int warp_bytes(int group) {
+    return kRingW * (kStageBytes + qslot_bytes(group));
+  }
 };
-
-constexpr int kMaxRing = 28;
 
 struct ItemSlot {
-  int b, g, lo, p, c_begin, c_end, s_global, nsplits, first_gs;
+  int b, g, lo, p, c_begin, c_end, s_global, nsplits;
 };
 
-struct WsShared {
-  unsigned long long full[kMaxRing], empty[kMaxRing], qfull[2], qempty[2], mfull, mdone, mdec;
-  uint32_t stage_mask[kMaxRing];
-  ItemSlot slot[2];
+struct WarpShared {
+  unsigned long long full[kMaxWarpsW][kRingW], qfull[kMaxWarpsW][kRingW];
+  uint32_t stage_mask[kMaxWarpsW][kRingW];
+  ItemSlot slot[kMaxWarpsW][kRingW];
   int abort_flag;
-  int last;
 };
 
 template <int D, bool TWO_ROWS>
-__global__ void __launch_bounds__(kWsThreads, 1)
-    decode_bf16_ws_kernel(DecodeParams P, const __grid_constant__ CUtensorMap kmap,
-                          const __grid_constant__ CUtensorMap vmap, int box_rows) {
-  using L = WsSmem<D>;
-  constexpr int kRing = L::kRing;
-  static_assert(kRing <= kMaxRing, "ring fits the barrier arrays");
+__global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
+    decode_bf16_kernel(DecodeParams P, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, int box_rows) {
+  using L = WarpSmem<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ WsShared sh;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  unsigned char* smem = smem_raw + (sbase - smem_u32(smem_raw));
+  __shared__ WarpShared sh;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t sbase0 = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* smem0 = smem_raw + (sbase0 - smem_u32(smem_raw));
   volatile int* abort_flag = &sh.abort_flag;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(smem_u32(&sh.full[i]), 1);  // the producer's expect-tx arrival
-      mbar_init(smem_u32(&sh.empty[i]), 1);
+  if (threadIdx.x == 0) sh.abort_flag = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kRingW; ++i) {
+      mbar_init(smem_u32(&sh.full[w][i]), 1);
+      mbar_init(smem_u32(&sh.qfull[w][i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh.qfull[i]), 1);
-      mbar_init(smem_u32(&sh.qempty[i]), kConsumers);
-    }
-    mbar_init(smem_u32(&sh.mfull), kConsumers);
-    mbar_init(smem_u32(&sh.mdone), kConsumers);
-    mbar_init(smem_u32(&sh.mdec), 1);
-    sh.abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
+  const int qslot = L::qslot_bytes(P.group);
+  const uint32_t ring = sbase0 + w * L::warp_bytes(P.group);
+  const uint32_t qbase = ring + kRingW * L::kStageBytes;
+  const unsigned char* qbase_ptr = smem0 + (qbase - sbase0);
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
+  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
+  const int n_slots = P.num_pages * P.page_size;
+  const int nbox = kChunk / box_rows;      // boxes per row half
+  const int nreq = 2 * L::kHalves * nbox;  // TMA requests per chunk
+  const int rq_kind = lane / (L::kHalves * nbox);
+  const int rq_rem = lane % (L::kHalves * nbox);
+  const int rq_half = rq_rem / nbox, rq_box = rq_rem % nbox;
+  const CUtensorMap* rq_map = rq_kind == 0 ? &kmap : &vmap;
 
-  if (warp == kConsumers) {
-    // ------------------------------------------------------------ producer
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
-    const int n_slots = P.num_pages * P.page_size;
-    const int nbox = kChunk / box_rows;             // boxes per half
-    const int nreq = 2 * L::kHalves * nbox;         // TMA requests per chunk
-    // this lane's request (if lane < nreq): K or V, row half, box
-    const int rq_kind = lane / (L::kHalves * nbox);
-    const int rq_rem = lane % (L::kHalves * nbox);
-    const int rq_half = rq_rem / nbox, rq_box = rq_rem % nbox;
-    const CUtensorMap* rq_map = rq_kind == 0 ? &kmap : &vmap;
-    uint32_t gs = 0;
-    int item_seq = 0;
-    int last_q_item = -1;  // the latest item whose Q copy was issued
-    // software pipeline over items: the next item's descriptor and the first
-    // window of its block table are loaded one item ahead
-    int grab = 0;
+  // ---------------------------------------------------------- issue side
+  // items: icur (being issued), inext (descriptor and window loaded),
+  // inext2 (descriptor loading), grab (lane 0: the atomic for the one after)
+  ItemInfo icur, inext, inext2;
+  bool icur_live = false;
+  int icur_c = 0, iwin_blk0 = 0, iwin = -1, nwin_blk0 = 0, nwin = -1;
+  int id_next = total_items, id_next2 = total_items;
+  int grab = 0;
+  uint32_t gs_issue = 0;
+  int items_issued = 0;
+  {
+    int g0 = 0;
+    if (lane == 0) g0 = atomicAdd(P.ws.ctrl + 2, 1);
+    id_next = __shfl_sync(0xffffffffu, g0, 0);
+    if (lane == 0) g0 = atomicAdd(P.ws.ctrl + 2, 1);
+    id_next2 = __shfl_sync(0xffffffffu, g0, 0);
     if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
-    int cur = __shfl_sync(0xffffffffu, grab, 0);
-    if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);  // the next item, read later
-    ItemInfo ci;
-    int cwin_blk0 = 0, cwin = -1;
-    if (cur < total_items) {
-      describe_item(P, cur, ci);
-      cwin_blk0 = ci.c_begin * kChunk / P.page_size;
-      const int blk = cwin_blk0 + lane;
-      cwin = blk <= ci.p / P.page_size
-                 ? __ldg(P.block_table + (size_t)ci.b * P.max_pages_per_seq + blk)
+    if (id_next < total_items) {
+      describe_item(P, id_next, inext);
+      nwin_blk0 = inext.c_begin * kChunk / P.page_size;
+      const int blk = nwin_blk0 + lane;
+      nwin = blk <= inext.p / P.page_size
+                 ? __ldg(P.block_table + (size_t)inext.b * P.max_pages_per_seq + blk)
                  : -1;
     }
-    for (;; ++item_seq) {
-      const int slot = item_seq & 1;
-      if (!mbar_wait(smem_u32(&sh.qempty[slot]), ((item_seq >> 1) & 1) ^ 1, abort_flag)) break;
-      if (cur >= total_items) {
-        if (lane == 0) {
-          sh.slot[slot].b = -1;
-          mbar_arrive(smem_u32(&sh.qfull[slot]));
-        }
+    if (id_next2 < total_items) describe_item(P, id_next2, inext2);
+  }
+
+  // Start issuing the next item: publish its descriptor, copy its Q rows,
+  // advance the prefetch pipeline.  False when there is no item left.
+  auto start_item = [&]() -> bool {
+    if (id_next >= total_items) return false;
+    icur = inext;
+    iwin_blk0 = nwin_blk0;
+    iwin = nwin;
+    icur_c = icur.c_begin;
+    icur_live = true;
+    const int q = items_issued % kRingW;
+    if (lane == 0) {
+      ItemSlot& d = sh.slot[w][q];
+      d.b = icur.b; d.g = icur.g; d.lo = icur.lo; d.p = icur.p;
+      d.c_begin = icur.c_begin; d.c_end = icur.c_end;
+      d.s_global = icur.s_global; d.nsplits = icur.nsplits;
+      const uint32_t qbytes = (uint32_t)(P.group * D * 2);
+      mbar_arrive_expect_tx(smem_u32(&sh.qfull[w][q]), qbytes);
+      bulk_g2s(qbase + q * qslot,
+               qg + ((size_t)icur.b * P.h_q + (size_t)icur.g * P.group) * D, qbytes,
+               smem_u32(&sh.qfull[w][q]));
+    }
+    ++items_issued;
+    // pipeline: next2 -> next (its descriptor has arrived: load its window)
+    id_next = id_next2;
+    inext = inext2;
+    if (id_next < total_items) {
+      nwin_blk0 = inext.c_begin * kChunk / P.page_size;
+      const int blk = nwin_blk0 + lane;
+      nwin = blk <= inext.p / P.page_size
+                 ? __ldg(P.block_table + (size_t)inext.b * P.max_pages_per_seq + blk)
+                 : -1;
+    }
+    id_next2 = __shfl_sync(0xffffffffu, grab, 0);
+    if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
+    if (id_next2 < total_items) describe_item(P, id_next2, inext2);
+    return true;
+  };
+
+  // Issue the next chunk of the stream (starting a new item when needed).
+  auto issue_next = [&]() {
+    if (!icur_live && !start_item()) return;
+    const int stage = (int)(gs_issue % kRingW);
+    fence_proxy_async_smem();  // the stage's previous reads and zero stores come first
+    const int j0 = icur_c * kChunk;
+    const int last_blk = icur.p / P.page_size;
+    const int bmin = j0 / P.page_size;
+    const int bmax = min((j0 + kChunk - 1) / P.page_size, last_blk);
+    if (bmin < iwin_blk0 || bmax >= iwin_blk0 + 32) {  // the next 32 blocks
+      iwin_blk0 = bmin;
+      const int blk = iwin_blk0 + lane;
+      iwin = blk <= last_blk
+                 ? __ldg(P.block_table + (size_t)icur.b * P.max_pages_per_seq + blk)
+                 : -1;
+    }
+    const int jr = j0 + (lane & 15);
+    const int pr = __shfl_sync(0xffffffffu, iwin, (jr / P.page_size - iwin_blk0) & 31);
+    bool live = jr >= icur.lo && jr <= icur.p;
+    if (live && (pr < 0 || pr >= P.num_pages)) {
+      if (lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
+      live = false;
+    }
+    const uint32_t mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
+    const int jb = j0 + rq_box * box_rows;
+    const int blk = jb / P.page_size;
+    const int pb = __shfl_sync(0xffffffffu, iwin, (blk - iwin_blk0) & 31);
+    const bool box_ok = blk <= last_blk && pb >= 0 && pb < P.num_pages;
+    const int slot0 = box_ok ? pb * P.page_size + jb % P.page_size : n_slots;
+    const uint32_t bar = smem_u32(&sh.full[w][stage]);
+    if (lane == 0) {
+      sh.stage_mask[w][stage] = mask;
+      mbar_arrive_expect_tx(bar, L::kStageBytes);
+    }
+    __syncwarp();
+    if (lane < nreq)
+      tma_load_3d(ring + stage * L::kStageBytes + rq_kind * L::kChunkBytes +
+                      rq_half * L::kHalfBytes + rq_box * box_rows * 128,
+                  rq_map, rq_half * 64, icur.g, slot0, bar);
+    ++gs_issue;
+    if (++icur_c == icur.c_end) icur_live = false;
+  };
+
+  for (int t = 0; t < kRingW - 1; ++t) issue_next();
+
+  // -------------------------------------------------------- compute side
+  const int qr = lane >> 2, qc = (lane & 3) * 2;
+  uint32_t gs_c = 0;
+  int items_c = 0;
+  bool stop = false;
+  while (!stop && items_c < items_issued) {
+    const int q = items_c % kRingW;
+    if (!mbar_wait(smem_u32(&sh.qfull[w][q]), (items_c / kRingW) & 1, abort_flag)) break;
+    const ItemSlot it = sh.slot[w][q];
+    const unsigned char* qs = qbase_ptr + q * qslot;
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int e0 = ks * 16 + qc;
+      qa[ks][0] = qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0) * 2) : 0u;
+      qa[ks][2] =
+          qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0 + 8) * 2) : 0u;
+      if (TWO_ROWS) {
+        qa[ks][1] = qr + 8 < P.group
+                        ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0) * 2)
+                        : 0u;
+        qa[ks][3] = qr + 8 < P.group
+                        ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0 + 8) * 2)
+                        : 0u;
+      } else {
+        qa[ks][1] = 0u;
+        qa[ks][3] = 0u;
+      }
+    }
+    __syncwarp();
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int c = it.c_begin; c < it.c_end; ++c, ++gs_c) {
+      issue_next();  // keeps kRingW-1 chunks in flight ahead of this one
+      const int stage = (int)(gs_c % kRingW);
+      if (!mbar_wait(smem_u32(&sh.full[w][stage]), (gs_c / kRingW) & 1, abort_flag)) {
+        stop = true;
         break;
       }
-      const int nxt = __shfl_sync(0xffffffffu, grab, 0);
-      if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);  // the one after
-      ItemInfo ni;
-      const bool has_next = nxt < total_items;
-      if (has_next) describe_item(P, nxt, ni);  // in flight during this item
-      int nwin_blk0 = 0, nwin = -1;
-      if (lane == 0) {
-        ItemSlot& d = sh.slot[slot];
-        d.b = ci.b; d.g = ci.g; d.lo = ci.lo; d.p = ci.p;
-        d.c_begin = ci.c_begin; d.c_end = ci.c_end;
-        d.s_global = ci.s_global; d.nsplits = ci.nsplits; d.first_gs = (int)gs;
-        const uint32_t qbytes = (uint32_t)(P.group * D * 2);
-        mbar_arrive_expect_tx(smem_u32(&sh.qfull[slot]), qbytes);
-        bulk_g2s(sbase + L::kQOff + slot * L::kQBytes,
-                 qg + ((size_t)ci.b * P.h_q + (size_t)ci.g * P.group) * D, qbytes,
-                 smem_u32(&sh.qfull[slot]));
-        last_q_item = item_seq;
-      }
-      const int last_blk = ci.p / P.page_size;
-      const int32_t* bt_row = P.block_table + (size_t)ci.b * P.max_pages_per_seq;
-      const int n_chunks = ci.c_end - ci.c_begin;
-      const int prefetch_at = min(3, n_chunks - 1);
-      bool stop = false;
-      for (int k = 0; k < n_chunks; ++k, ++gs) {
-        const int c = ci.c_begin + k;
-        const int stage = (int)(gs % kRing);
-        if (!mbar_wait(smem_u32(&sh.empty[stage]), ((gs / kRing) & 1) ^ 1, abort_flag)) {
-          stop = true;
-          break;
-        }
-        const int j0 = c * kChunk;
-        const int bmin = j0 / P.page_size;
-        const int bmax = min((j0 + kChunk - 1) / P.page_size, last_blk);
-        if (bmin < cwin_blk0 || bmax >= cwin_blk0 + 32) {  // the next 32 blocks
-          cwin_blk0 = bmin;
-          const int blk = cwin_blk0 + lane;
-          cwin = blk <= last_blk ? __ldg(bt_row + blk) : -1;
-        }
-        // live rows (lanes 0-15: row = lane)
-        const int jr = j0 + (lane & 15);
-        const int pr = __shfl_sync(0xffffffffu, cwin, (jr / P.page_size - cwin_blk0) & 31);
-        bool live = jr >= ci.lo && jr <= ci.p;
-        if (live && (pr < 0 || pr >= P.num_pages)) {
-          if (lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
-          live = false;
-        }
-        const uint32_t mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
-        // this lane's box: rows rq_box*box_rows.. of the chunk
-        const int jb = j0 + rq_box * box_rows;
-        const int blk = jb / P.page_size;
-        const int pb = __shfl_sync(0xffffffffu, cwin, (blk - cwin_blk0) & 31);
-        const bool box_ok = blk <= last_blk && pb >= 0 && pb < P.num_pages;
-        const int slot0 = box_ok ? pb * P.page_size + jb % P.page_size : n_slots;
-        if (lane == 0) {
-          sh.stage_mask[stage] = mask;
-          mbar_arrive_expect_tx(smem_u32(&sh.full[stage]), L::kStageBytes);
-        }
-        __syncwarp();
-        if (lane < nreq) {
-          const uint32_t dst = sbase + L::kRingOff + stage * L::kStageBytes +
-                               rq_kind * L::kChunkBytes + rq_half * L::kHalfBytes +
-                               rq_box * box_rows * 128;
-          tma_load_3d(dst, rq_map, rq_half * 64, ci.g, slot0, smem_u32(&sh.full[stage]));
-        }
-        if (k == prefetch_at && has_next) {
-          nwin_blk0 = ni.c_begin * kChunk / P.page_size;
-          const int nb = nwin_blk0 + lane;
-          nwin = nb <= ni.p / P.page_size
-                     ? __ldg(P.block_table + (size_t)ni.b * P.max_pages_per_seq + nb)
-                     : -1;
+      const uint32_t mask = sh.stage_mask[w][stage];
+      const uint32_t kaddr = ring + stage * L::kStageBytes;
+      const uint32_t vaddr = kaddr + L::kChunkBytes;
+      {
+        // V rows past the sequence's end (its last chunk only) may hold anything
+        const int first_dead = it.p + 1 - c * kChunk;
+        if (first_dead < kChunk) {
+          const int n_dead = kChunk - max(first_dead, 0);
+          for (int idx = lane; idx < n_dead * L::kHalves * 8; idx += 32) {
+            const int row = kChunk - n_dead + idx / (L::kHalves * 8);
+            const int hu = idx % (L::kHalves * 8);
+            const uint32_t a = vaddr + (hu >> 3) * L::kHalfBytes + row * 128 + ((hu & 7) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u)
+                         : "memory");
+          }
+          __syncwarp();
         }
       }
-      if (stop) break;
-      cur = nxt;
-      ci = ni;
-      cwin_blk0 = nwin_blk0;
-      cwin = nwin;
-    }
-    // drain: every copy this CTA issued has landed before it exits (the last
-    // kRing stages are each their stage's latest phase; the latest Q copy is
-    // its slot's latest phase)
-    bool drained = true;
-    for (uint32_t i = gs > (uint32_t)kRing ? gs - kRing : 0; i < gs; ++i)
-      drained &= mbar_drain(smem_u32(&sh.full[i % kRing]), (i / kRing) & 1);
-    last_q_item = __shfl_sync(0xffffffffu, last_q_item, 0);
-    if (last_q_item >= 0)
-      drained &= mbar_drain(smem_u32(&sh.qfull[last_q_item & 1]), (last_q_item >> 1) & 1);
-    if (!drained) *abort_flag = 1;
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int qr = lane >> 2, qc = (lane & 3) * 2;
-    float* merge = reinterpret_cast<float*>(smem + L::kMergeOff);
-    for (int item_seq = 0;; ++item_seq) {
-      const int slot = item_seq & 1;
-      if (!mbar_wait(smem_u32(&sh.qfull[slot]), (item_seq >> 1) & 1, abort_flag)) break;
-      const ItemSlot it = sh.slot[slot];
-      if (it.b < 0) break;
-      // Q fragments (rows = query heads of the group, zero past the group)
-      const unsigned char* qs = smem + L::kQOff + slot * L::kQBytes;
-      uint32_t qa[D / 16][4];
+      // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys)
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int mi = lane >> 3, ri = lane & 7;
+        const int tok = (mi >> 1) * 8 + ri;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int e0 = ks * 16 + qc;
-        qa[ks][0] =
-            qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0) * 2) : 0u;
-        qa[ks][2] =
-            qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0 + 8) * 2) : 0u;
-        if (TWO_ROWS) {
-          qa[ks][1] = qr + 8 < P.group
-                          ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0) * 2)
-                          : 0u;
-          qa[ks][3] = qr + 8 < P.group
-                          ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0 + 8) * 2)
-                          : 0u;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int u = 2 * ks + (mi & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4),
+                      b0, b1, b2, b3);
+          mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        }
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = n * 8 + qc + e;
+          const bool ok = (mask >> key) & 1u;
+          s[n][e] = ok ? s[n][e] * P.scale_log2 : -INFINITY;
+          s[n][2 + e] = ok ? s[n][2 + e] * P.scale_log2 : -INFINITY;
+          mx0 = fmaxf(mx0, s[n][e]);
+          mx1 = fmaxf(mx1, s[n][2 + e]);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      const float mn0 = fmaxf(m0, mx0);
+      const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
+      const float c0 = fast_exp2(m0 - base0);
+      m0 = mn0;
+      float p[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        p[n][0] = fast_exp2(s[n][0] - base0);
+        p[n][1] = fast_exp2(s[n][1] - base0);
+      }
+      l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+      float c1 = c0;
+      if (TWO_ROWS) {
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn1 = fmaxf(m1, mx1);
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        c1 = fast_exp2(m1 - base1);
+        m1 = mn1;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          p[n][2] = fast_exp2(s[n][2] - base1);
+          p[n][3] = fast_exp2(s[n][3] - base1);
+        }
+        l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+      }
+      // rows 8-15 hold either the second half of the group (TWO_ROWS) or the
+      // low bf16 part of rows 0-7's probabilities; both rescale with their row
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= c0;
+        o[n][1] *= c0;
+        o[n][2] *= c1;
+        o[n][3] *= c1;
+      }
+      // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
+      uint32_t h0, l0w, h2, l2w;
+      split_bf16x2(p[0][0], p[0][1], h0, l0w);
+      split_bf16x2(p[1][0], p[1][1], h2, l2w);
+      {
+        const int mi = lane >> 3, ri = lane & 7;
+        const int tok = (mi & 1) * 8 + ri;
+        if (!TWO_ROWS) {
+#pragma unroll
+          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+            const int u = 2 * nd2 + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(
+                vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                b1, b2, b3);
+            mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
+            mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+          }
         } else {
-          qa[ks][1] = 0u;
-          qa[ks][3] = 0u;
+          uint32_t h1, l1w, h3, l3w;
+          split_bf16x2(p[0][2], p[0][3], h1, l1w);
+          split_bf16x2(p[1][2], p[1][3], h3, l3w);
+#pragma unroll
+          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+            const int u = 2 * nd2 + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(
+                vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                b1, b2, b3);
+            mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
+            mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
+            mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
+            mma_bf16_16816(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+          }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.qempty[slot]));
-
-      float o[D / 8][4];
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      const int n_chunks = it.c_end - it.c_begin;
-      bool stop = false;
-      for (int k = warp; k < n_chunks; k += kConsumers) {
-        const uint32_t gs = (uint32_t)it.first_gs + (uint32_t)k;
-        const int stage = (int)(gs % kRing);
-        if (!mbar_wait(smem_u32(&sh.full[stage]), (gs / kRing) & 1, abort_flag)) {
-          stop = true;
-          break;
-        }
-        const uint32_t mask = sh.stage_mask[stage];
-        const uint32_t kaddr = sbase + L::kRingOff + stage * L::kStageBytes;
-        const uint32_t vaddr = kaddr + L::kChunkBytes;
-        {
-          // V rows past the sequence's end (last chunk only) may hold anything
-          const int first_dead = it.p + 1 - (it.c_begin + k) * kChunk;
-          if (first_dead < kChunk) {
-            const int n_dead = kChunk - max(first_dead, 0);
-            for (int idx = lane; idx < n_dead * L::kHalves * 8; idx += 32) {
-              const int row = kChunk - n_dead + idx / (L::kHalves * 8);
-              const int hu = idx % (L::kHalves * 8);
-              const uint32_t a =
-                  vaddr + (hu >> 3) * L::kHalfBytes + row * 128 + ((hu & 7) << 4);
-              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u)
-                           : "memory");
-            }
-            fence_proxy_async_smem();  // before the stage returns to the TMA
-            __syncwarp();
-          }
-        }
-        // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys)
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-          const int mi = lane >> 3, ri = lane & 7;
-          const int tok = (mi >> 1) * 8 + ri;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const int u = 2 * ks + (mi & 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4),
-                        b0, b1, b2, b3);
-            mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-          }
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = n * 8 + qc + e;
-            const bool ok = (mask >> key) & 1u;
-            s[n][e] = ok ? s[n][e] * P.scale_log2 : -INFINITY;
-            s[n][2 + e] = ok ? s[n][2 + e] * P.scale_log2 : -INFINITY;
-            mx0 = fmaxf(mx0, s[n][e]);
-            mx1 = fmaxf(mx1, s[n][2 + e]);
-          }
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        const float mn0 = fmaxf(m0, mx0);
-        const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
-        const float c0 = fast_exp2(m0 - base0);
-        m0 = mn0;
-        float p[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          p[n][0] = fast_exp2(s[n][0] - base0);
-          p[n][1] = fast_exp2(s[n][1] - base0);
-        }
-        l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        float c1 = c0;
-        if (TWO_ROWS) {
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn1 = fmaxf(m1, mx1);
-          const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-          c1 = fast_exp2(m1 - base1);
-          m1 = mn1;
-#pragma unroll
-          for (int n = 0; n < 2; ++n) {
-            p[n][2] = fast_exp2(s[n][2] - base1);
-            p[n][3] = fast_exp2(s[n][3] - base1);
-          }
-          l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-        }
-        // rows 8-15 hold either the second half of the group (TWO_ROWS) or
-        // the low bf16 part of rows 0-7's probabilities; both rescale by row
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          o[n][0] *= c0;
-          o[n][1] *= c0;
-          o[n][2] *= c1;
-          o[n][3] *= c1;
-        }
-        // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
-        uint32_t h0, l0w, h2, l2w;
-        split_bf16x2(p[0][0], p[0][1], h0, l0w);
-        split_bf16x2(p[1][0], p[1][1], h2, l2w);
-        {
-          const int mi = lane >> 3, ri = lane & 7;
-          const int tok = (mi & 1) * 8 + ri;
-          if (!TWO_ROWS) {
-#pragma unroll
-            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-              const int u = 2 * nd2 + (mi >> 1);
-              uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(vaddr + (u >> 3) * L::kHalfBytes + tok * 128 +
-                                    (((u & 7) ^ (tok & 7)) << 4),
-                                b0, b1, b2, b3);
-              mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
-              mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
-            }
-          } else {
-            uint32_t h1, l1w, h3, l3w;
-            split_bf16x2(p[0][2], p[0][3], h1, l1w);
-            split_bf16x2(p[1][2], p[1][3], h3, l3w);
-#pragma unroll
-            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-              const int u = 2 * nd2 + (mi >> 1);
-              uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(vaddr + (u >> 3) * L::kHalfBytes + tok * 128 +
-                                    (((u & 7) ^ (tok & 7)) << 4),
-                                b0, b1, b2, b3);
-              mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
-              mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
-              mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
-              mma_bf16_16816(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[stage]));
-      }
-      if (stop) break;
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-      if (TWO_ROWS) {
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      }
-      // this warp's state -> its merge rows
-      constexpr int RS = L::kRS;
-      float* mrow = merge + warp * 16 * RS;
+    }
+    if (stop) break;
+    // ------------------------------------------------------ finish the item
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    if (TWO_ROWS) {
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    }
+    const bool single = it.nsplits == 1;
+    const int h0r = it.g * P.group + qr, h1r = h0r + 8;
+    if (single) {
+      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
       if (qr < P.group) {
+        float* dst = P.out + ((size_t)it.b * P.h_q + h0r) * D + qc;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
-          mrow[qr * RS + n * 8 + qc] = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
-          mrow[qr * RS + n * 8 + qc + 1] = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
-        }
-        if ((lane & 3) == 0) {
-          mrow[qr * RS + D] = m0;
-          mrow[qr * RS + D + 1] = l0;
+          const float a = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
+          const float bb = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
+          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(a * i0, bb * i0);
         }
       }
       if (TWO_ROWS && qr + 8 < P.group) {
+        float* dst = P.out + ((size_t)it.b * P.h_q + h1r) * D + qc;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2] * i1, o[n][3] * i1);
+      }
+    } else {
+      if (qr < P.group) {
+        const size_t rowi = (size_t)it.s_global * P.h_q + h0r;
+        float* dst = P.ws.acc + rowi * D + qc;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
-          mrow[(qr + 8) * RS + n * 8 + qc] = o[n][2];
-          mrow[(qr + 8) * RS + n * 8 + qc + 1] = o[n][3];
+          const float a = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
+          const float bb = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
+          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(a, bb);
         }
-        if ((lane & 3) == 0) {
-          mrow[(qr + 8) * RS + D] = m1;
-          mrow[(qr + 8) * RS + D + 1] = l1;
-        }
+        if ((lane & 3) == 0) *reinterpret_cast<float2*>(P.ws.ml + rowi * 2) = make_float2(m0, l0);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.mfull));
-      if (!mbar_wait(smem_u32(&sh.mfull), item_seq & 1, abort_flag)) break;
-      // merge the consumers' states: one output (single split) or one partial
-      const int ct = threadIdx.x;  // 0 .. 32*kConsumers-1
-      const bool single = it.nsplits == 1;
-      for (int idx = ct; idx < P.group * (D + 1); idx += 32 * kConsumers) {
-        const int r = idx / (D + 1), e = idx - r * (D + 1);
-        float M = -INFINITY;
+      if (TWO_ROWS && qr + 8 < P.group) {
+        const size_t rowi = (size_t)it.s_global * P.h_q + h1r;
+        float* dst = P.ws.acc + rowi * D + qc;
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, merge[(w * 16 + r) * RS + D]);
-        float a = 0.f, lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-          const float* mr = merge + (w * 16 + r) * RS;
-          const float f = mr[D] == -INFINITY ? 0.f : fast_exp2(mr[D] - M);
-          if (e < D) a += f * mr[e];
-          if (single || e == D) lsum += f * mr[D + 1];
-        }
-        const int h = it.g * P.group + r;
-        if (single) {
-          if (e < D) P.out[((size_t)it.b * P.h_q + h) * D + e] = lsum > 0.f ? a / lsum : 0.f;
-        } else {
-          const size_t rowi = (size_t)it.s_global * P.h_q + h;
-          if (e < D) {
-            P.ws.acc[rowi * D + e] = a;
-          } else {
-            P.ws.ml[rowi * 2 + 0] = M;
-            P.ws.ml[rowi * 2 + 1] = lsum;
-          }
-        }
+        for (int n = 0; n < D / 8; ++n)
+          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2], o[n][3]);
+        if ((lane & 3) == 0) *reinterpret_cast<float2*>(P.ws.ml + rowi * 2) = make_float2(m1, l1);
       }
-      if (!single) __threadfence();
+      __threadfence();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.mdone));
-      if (warp == 0) {
-        if (!mbar_wait(smem_u32(&sh.mdone), item_seq & 1, abort_flag)) break;
-        if (lane == 0) {
-          int last = 0;
-          if (!single) {
-            int* cnt = P.ws.done + (size_t)it.b * P.h_kv + it.g;
-            const int old = atomicAdd(cnt, 1);
-            last = old == it.nsplits - 1;
-            if (last) atomicExch(cnt, 0);
-          }
-          sh.last = last;
-          mbar_arrive(smem_u32(&sh.mdec));
-        }
-        __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        int* cnt = P.ws.done + (size_t)it.b * P.h_kv + it.g;
+        last = atomicAdd(cnt, 1) == it.nsplits - 1;
+        if (last) atomicExch(cnt, 0);
       }
-      if (!mbar_wait(smem_u32(&sh.mdec), item_seq & 1, abort_flag)) break;
-      if (sh.last) {
-        // this CTA finished the last split of (b, g): merge all its partials
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        // this warp finished the last split of (b, g): merge all its partials
         __threadfence();
         const int s0 = it.s_global - (it.c_begin - it.lo / kChunk) / __ldcg(P.ws.ctrl + 0);
-        for (int idx = ct; idx < P.group * D; idx += 32 * kConsumers) {
-          const int r = idx / D, e = idx - r * D;
+        constexpr int E = D / 32;
+        for (int r = 0; r < P.group; ++r) {
           const int h = it.g * P.group + r;
           float M = -INFINITY;
           for (int sp = 0; sp < it.nsplits; ++sp)
             M = fmaxf(M, __ldcg(P.ws.ml + ((size_t)(s0 + sp) * P.h_q + h) * 2));
-          float a = 0.f, lsum = 0.f;
+          float a[E], lsum = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) a[e] = 0.f;
           for (int sp = 0; sp < it.nsplits; ++sp) {
             const size_t rowi = (size_t)(s0 + sp) * P.h_q + h;
             const float mi = __ldcg(P.ws.ml + rowi * 2);
             const float f = mi == -INFINITY ? 0.f : fast_exp2(mi - M);
             lsum += f * __ldcg(P.ws.ml + rowi * 2 + 1);
-            a += f * __ldcg(P.ws.acc + rowi * D + e);
+#pragma unroll
+            for (int e = 0; e < E; ++e) a[e] += f * __ldcg(P.ws.acc + rowi * D + lane * E + e);
           }
-          P.out[((size_t)it.b * P.h_q + h) * D + e] = lsum > 0.f ? a / lsum : 0.f;
+          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) P.out[((size_t)it.b * P.h_q + h) * D + lane * E + e] = a[e] * inv;
         }
       }
     }
+    ++items_c;
   }
+  // drain: every copy this warp issued has landed before it exits (each is
+  // the latest phase of its barrier)
+  bool drained = true;
+  for (uint32_t i = gs_c; i < gs_issue; ++i)
+    drained &= mbar_drain(smem_u32(&sh.full[w][i % kRingW]), (i / kRingW) & 1);
+  for (int i = items_c; i < items_issued; ++i)
+    drained &= mbar_drain(smem_u32(&sh.qfull[w][i % kRingW]), (i / kRingW) & 1);
+  if (!drained) *abort_flag = 1;
   __syncthreads();  // every wait above is bounded, so every thread gets here
   if (threadIdx.x == 0 && sh.abort_flag) report(P.error_word, TL_DEVERR_TIMEOUT);
 }
@@ -913,21 +882,23 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
     if (!encode_bf16_tensor_map(&kmap, k_cache, 3, dims, strides, box, true) ||
         !encode_bf16_tensor_map(&vmap, v_cache, 3, dims, strides, box, true))
       return TL_ERR_CUDA;
-#define TL_LAUNCH_WS(DD, TWO)                                                             \
+#define TL_LAUNCH_W(DD, TWO)                                                              \
   do {                                                                                    \
-    auto kern = decode_bf16_ws_kernel<DD, TWO>;                                           \
-    const int sm = WsSmem<DD>::kTotal;                                                    \
+    auto kern = decode_bf16_kernel<DD, TWO>;                                              \
+    const int per_warp = WarpSmem<DD>::warp_bytes(group);                                 \
+    const int warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);               \
+    const int sm = warps * per_warp + 1024;                                               \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
         cudaSuccess)                                                                      \
       return TL_ERR_CUDA;                                                                 \
-    kern<<<num_sms(), kWsThreads, sm, st>>>(P, kmap, vmap, box_rows);                     \
+    kern<<<num_sms(), warps * 32, sm, st>>>(P, kmap, vmap, box_rows);                     \
   } while (0)
     if (d == 128) {
-      if (group > 8) TL_LAUNCH_WS(128, true); else TL_LAUNCH_WS(128, false);
+      if (group > 8) TL_LAUNCH_W(128, true); else TL_LAUNCH_W(128, false);
     } else {
-      if (group > 8) TL_LAUNCH_WS(64, true); else TL_LAUNCH_WS(64, false);
+      if (group > 8) TL_LAUNCH_W(64, true); else TL_LAUNCH_W(64, false);
     }
-#undef TL_LAUNCH_WS
+#undef TL_LAUNCH_W
     return launch_status();
   }
   const int grid = num_sms() * 2;
