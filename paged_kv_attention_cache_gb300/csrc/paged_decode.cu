@@ -233,8 +233,14 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 // registers; the warp that completes the last split of a (sequence, KV head)
 // merges its partials (the completion counter is read once, nobody waits).
 
-constexpr int kRingW = 3;     // stages per warp
-constexpr int kMaxWarpsW = 8;
+#ifndef TL_DECODE_RING
+#define TL_DECODE_RING 3
+#endif
+#ifndef TL_DECODE_WARPS
+#define TL_DECODE_WARPS 8
+#endif
+constexpr int kRingW = TL_DECODE_RING;      // stages per warp
+constexpr int kMaxWarpsW = TL_DECODE_WARPS;
 
 template <int D>
 struct WarpSmem {
@@ -366,7 +372,6 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   auto issue_next = [&]() {
     if (!icur_live && !start_item()) return;
     const int stage = (int)(gs_issue % kRingW);
-    fence_proxy_async_smem();  // the stage's previous reads and zero stores come first
     const int j0 = icur_c * kChunk;
     const int last_blk = icur.p / P.page_size;
     const int bmin = j0 / P.page_size;
@@ -464,6 +469,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u)
                          : "memory");
           }
+          fence_proxy_async_smem();  // these stores precede the stage's next TMA fill
           __syncwarp();
         }
       }
