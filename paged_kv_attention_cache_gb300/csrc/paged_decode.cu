@@ -11,24 +11,20 @@
 //   1. decode_plan_kernel (1 CTA): per sequence the 16-key chunks it reads
 //      ([lo/16, p/16]); a split size (in chunks) giving about kTargetItems
 //      work items for the batch; an exclusive scan of the splits per
-//      sequence.  Zeroes the work counter and the per-(sequence, KV head)
-//      completion counters, and writes the zero output of empty sequences.
-//   2. bf16: decode_bf16_ws_kernel, persistent, one CTA per SM, warp
-//      specialised.  A producer warp takes work items (split x KV head) from
-//      an atomic counter and streams each item's chunks (16 keys of K and V,
-//      8 KiB at d=128) with 16-byte cp.async into a ring of shared-memory
-//      stages, completing each stage on an mbarrier; the block table is read
-//      32 entries at a time, ahead of the copies.  Eight consumer warps take
-//      the item's chunks round-robin: Q.K^T and P.V on mma.sync m16n8k16 with
-//      the query-head group as the M rows, online softmax in registers.  At
-//      the end of an item the consumers merge their states in shared memory;
+//      sequence, and one descriptor per split.  Zeroes the work counter and
+//      writes the zero output of empty sequences.
+//   2. bf16: decode_bf16_kernel, persistent, one CTA per SM, every warp
+//      independent: a warp takes work items (split x KV head) from an atomic
+//      counter and streams their chunks (16 keys of K and V, 8 KiB at d=128)
+//      through its own ring of shared-memory stages filled by TMA; Q.K^T and
+//      P.V run on mma.sync m16n8k16 with the query-head group as the M rows,
+//      online softmax in registers (details below).  At the end of an item
+//      the warp writes from its registers:
 //      a sequence with one split writes its output directly, otherwise the
-//      item writes a partial and the CTA that completes the last split of a
-//      (sequence, KV head) merges all its partials (no waiting: the
-//      completion counter is read once).  The producer runs ahead across item
-//      boundaries, so the memory pipe stays full while consumers merge.
-//      f32: decode_f32_kernel (CUDA-core dots in f32) writes partials, and
-//      decode_combine_kernel merges them.
+//      item writes a partial.
+//      f32: decode_f32_kernel (CUDA-core dots in f32) writes partials.
+//   3. decode_combine_kernel merges the partials of sequences with several
+//      splits, one warp per (sequence, query head).
 // Every reduction has a fixed order, so results repeat bit for bit and do not
 // depend on the pool's page placement.
 #include <algorithm>
@@ -38,7 +34,10 @@
 namespace tl {
 
 constexpr int kChunk = 16;            // keys per step (one mma N=16 / K=16 tile)
-constexpr int kTargetItems = 12288;   // work items (split x KV head) per call
+#ifndef TL_DECODE_ITEMS
+#define TL_DECODE_ITEMS 12288
+#endif
+constexpr int kTargetItems = TL_DECODE_ITEMS;  // work items (split x KV head) per call
 constexpr int kMinSplitChunks = 8;    // 128 keys
 constexpr int kDecodeWarps = 4;       // f32 kernel
 constexpr int kDecodeThreads = kDecodeWarps * 32;
@@ -50,7 +49,6 @@ inline int64_t decode_max_splits(int B, int h_kv) {
 struct DecodeWorkspace {
   int32_t* ctrl;       // [0] split size in chunks, [1] total splits, [2] work counter
   int32_t* split_off;  // [B+1] first split of each sequence
-  int32_t* done;       // [B*h_kv] splits finished per (sequence, KV head)
   int4* desc;          // [max_splits][2] per-split descriptor (see SplitDesc)
   float* ml;           // [max_splits][h_q][2]   (running max in log2 units, sum)
   float* acc;          // [max_splits][h_q][d]   (unnormalised P.V)
@@ -64,8 +62,6 @@ inline size_t decode_ws_layout(int B, int h_q, int h_kv, int d, DecodeWorkspace*
   off += 256;
   const size_t so = off;
   off = align_up(off + sizeof(int32_t) * (size_t)(B + 1), 256);
-  const size_t dn = off;
-  off = align_up(off + sizeof(int32_t) * (size_t)B * h_kv, 256);
   const size_t ds = off;
   off = align_up(off + 2 * sizeof(int4) * (size_t)ms, 256);
   const size_t ml = off;
@@ -75,7 +71,6 @@ inline size_t decode_ws_layout(int B, int h_q, int h_kv, int d, DecodeWorkspace*
   if (w) {
     w->ctrl = reinterpret_cast<int32_t*>(base + ctrl);
     w->split_off = reinterpret_cast<int32_t*>(base + so);
-    w->done = reinterpret_cast<int32_t*>(base + dn);
     w->desc = reinterpret_cast<int4*>(base + ds);
     w->ml = reinterpret_cast<float*>(base + ml);
     w->acc = reinterpret_cast<float*>(base + acc);
@@ -131,7 +126,6 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
   if (lane == 0) red[wid] = total;
   if (tid == 0) carry_s = 0;
-  for (int i = tid; i < P.B * P.h_kv; i += nt) P.ws.done[i] = 0;
   __syncthreads();
   long long total_chunks = 0;
   for (int w = 0; w < nwarps; ++w) total_chunks += red[w];
@@ -230,8 +224,7 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 // and arrives as zeros; V rows past the last position in the last page are
 // zeroed before use (they may hold anything).  At the end of an item the
 // warp writes the output (one split) or a partial straight from its
-// registers; the warp that completes the last split of a (sequence, KV head)
-// merges its partials (the completion counter is read once, nobody waits).
+// registers.
 
 #ifndef TL_DECODE_RING
 #define TL_DECODE_RING 3
@@ -623,41 +616,6 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2], o[n][3]);
         if ((lane & 3) == 0) *reinterpret_cast<float2*>(P.ws.ml + rowi * 2) = make_float2(m1, l1);
       }
-      __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        int* cnt = P.ws.done + (size_t)it.b * P.h_kv + it.g;
-        last = atomicAdd(cnt, 1) == it.nsplits - 1;
-        if (last) atomicExch(cnt, 0);
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        // this warp finished the last split of (b, g): merge all its partials
-        __threadfence();
-        const int s0 = it.s_global - (it.c_begin - it.lo / kChunk) / __ldcg(P.ws.ctrl + 0);
-        constexpr int E = D / 32;
-        for (int r = 0; r < P.group; ++r) {
-          const int h = it.g * P.group + r;
-          float M = -INFINITY;
-          for (int sp = 0; sp < it.nsplits; ++sp)
-            M = fmaxf(M, __ldcg(P.ws.ml + ((size_t)(s0 + sp) * P.h_q + h) * 2));
-          float a[E], lsum = 0.f;
-#pragma unroll
-          for (int e = 0; e < E; ++e) a[e] = 0.f;
-          for (int sp = 0; sp < it.nsplits; ++sp) {
-            const size_t rowi = (size_t)(s0 + sp) * P.h_q + h;
-            const float mi = __ldcg(P.ws.ml + rowi * 2);
-            const float f = mi == -INFINITY ? 0.f : fast_exp2(mi - M);
-            lsum += f * __ldcg(P.ws.ml + rowi * 2 + 1);
-#pragma unroll
-            for (int e = 0; e < E; ++e) a[e] += f * __ldcg(P.ws.acc + rowi * D + lane * E + e);
-          }
-          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-#pragma unroll
-          for (int e = 0; e < E; ++e) P.out[((size_t)it.b * P.h_q + h) * D + lane * E + e] = a[e] * inv;
-        }
-      }
     }
     ++items_c;
   }
@@ -783,34 +741,66 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_f32_kernel(DecodeParams
 }
 
 // --------------------------------------------------------------- combine --
+//
+// One warp per (sequence, query head) merges the sequence's split partials in
+// split order: the lanes read the splits' (max, sum) pairs (32 at a time) and
+// reduce the maximum; each split's weight exp2(m_i - M) is broadcast from its
+// lane while the lanes sum the weighted P.V rows (8 splits in flight).
+// Sequences with one split were written by the main kernel when
+// skip_single is set.
 
 template <int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams P, int skip_single) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
-  const int64_t wi = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int64_t wi = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (wi >= (int64_t)P.B * P.h_q) return;
   const int b = (int)(wi / P.h_q), h = (int)(wi - (int64_t)b * P.h_q);
-  const int s0 = P.ws.split_off[b], s1 = P.ws.split_off[b + 1];
-  if (s1 == s0) return;  // written by the plan kernel
-  float* out = P.out + (size_t)wi * D;
+  const int s0 = __ldg(P.ws.split_off + b), ns = __ldg(P.ws.split_off + b + 1) - s0;
+  if (ns == 0 || (ns == 1 && skip_single)) return;
+  const float* ml = P.ws.ml + ((size_t)s0 * P.h_q + h) * 2;
+  const float* acc = P.ws.acc + ((size_t)s0 * P.h_q + h) * D + lane * E;
+  const size_t ml_stride = (size_t)P.h_q * 2, acc_stride = (size_t)P.h_q * D;
   float M = -INFINITY;
-  for (int s = s0; s < s1; ++s) M = fmaxf(M, P.ws.ml[((size_t)s * P.h_q + h) * 2]);
-  float acc[E];
+  for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, __ldg(ml + sp * ml_stride));
+  M = warp_max(M);
+  float a[E], lsum = 0.f;
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float Lsum = 0.f;
-  for (int s = s0; s < s1; ++s) {
-    const size_t row = (size_t)s * P.h_q + h;
-    const float mi = P.ws.ml[row * 2];
-    const float f = mi == -INFINITY ? 0.f : fast_exp2(mi - M);
-    Lsum += f * P.ws.ml[row * 2 + 1];
+  for (int e = 0; e < E; ++e) a[e] = 0.f;
+  for (int base = 0; base < ns; base += 32) {
+    const int sp = base + lane;
+    float f = 0.f;
+    if (sp < ns) {
+      const float mi = __ldg(ml + sp * ml_stride);
+      f = mi == -INFINITY ? 0.f : fast_exp2(mi - M);
+      lsum += f * __ldg(ml + sp * ml_stride + 1);
+    }
+    const int cnt = min(32, ns - base);
+    int j = 0;
+    for (; j + 8 <= cnt; j += 8) {
+      float v[8][E], fj[8];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] += f * P.ws.acc[row * D + lane * E + e];
+      for (int u = 0; u < 8; ++u) {
+        fj[u] = __shfl_sync(0xffffffffu, f, j + u);
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[u][e] = __ldg(acc + (size_t)(base + j + u) * acc_stride + e);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[e] += fj[u] * v[u][e];
+    }
+    for (; j < cnt; ++j) {
+      const float fj = __shfl_sync(0xffffffffu, f, j);
+#pragma unroll
+      for (int e = 0; e < E; ++e) a[e] += fj * __ldg(acc + (size_t)(base + j) * acc_stride + e);
+    }
   }
-  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+  lsum = warp_sum(lsum);
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  float* out = P.out + (size_t)wi * D + lane * E;
 #pragma unroll
-  for (int e = 0; e < E; ++e) out[lane * E + e] = acc[e] * inv;
+  for (int e = 0; e < E; ++e) out[e] = a[e] * inv;
 }
 
 }  // namespace tl
@@ -905,15 +895,18 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
       if (group > 8) TL_LAUNCH_W(64, true); else TL_LAUNCH_W(64, false);
     }
 #undef TL_LAUNCH_W
+    if (launch_status() != TL_OK) return TL_ERR_CUDA;
+    const unsigned cblocks = (unsigned)(((int64_t)B * h_q + 7) / 8);
+    if (d == 128) decode_combine_kernel<128><<<cblocks, 256, 0, st>>>(P, 1);
+    else decode_combine_kernel<64><<<cblocks, 256, 0, st>>>(P, 1);
     return launch_status();
   }
   const int grid = num_sms() * 2;
   if (d == 128) decode_f32_kernel<128><<<grid, kDecodeThreads, 0, st>>>(P);
   else decode_f32_kernel<64><<<grid, kDecodeThreads, 0, st>>>(P);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
-  const int64_t warps = (int64_t)B * h_q;
-  const unsigned cblocks = (unsigned)((warps + 3) / 4);
-  if (d == 128) decode_combine_kernel<128><<<cblocks, 128, 0, st>>>(P);
-  else decode_combine_kernel<64><<<cblocks, 128, 0, st>>>(P);
+  const unsigned cblocks = (unsigned)(((int64_t)B * h_q + 7) / 8);
+  if (d == 128) decode_combine_kernel<128><<<cblocks, 256, 0, st>>>(P, 0);
+  else decode_combine_kernel<64><<<cblocks, 256, 0, st>>>(P, 0);
   return launch_status();
 }
