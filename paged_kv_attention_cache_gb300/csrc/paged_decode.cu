@@ -11,8 +11,7 @@
 //   1. decode_plan_kernel (1 CTA): per sequence the 16-key chunks it reads
 //      ([lo/16, p/16]); a split size (in chunks) giving about kTargetItems
 //      work items for the batch; an exclusive scan of the splits per
-//      sequence, and one descriptor per split.  Zeroes the work counter and
-//      writes the zero output of empty sequences.
+//      sequence, and one descriptor per split.  Zeroes the work counter.
 //   2. bf16: decode_bf16_kernel, persistent, one CTA per SM, every warp
 //      independent: a warp takes work items (split x KV head) from an atomic
 //      counter and streams their chunks (16 keys of K and V, 8 KiB at d=128)
@@ -24,7 +23,8 @@
 //      item writes a partial.
 //      f32: decode_f32_kernel (CUDA-core dots in f32) writes partials.
 //   3. decode_combine_kernel merges the partials of sequences with several
-//      splits, one warp per (sequence, query head).
+//      splits, one warp per (sequence, query head), and writes the zero
+//      output of sequences with nothing to read.
 // Every reduction has a fixed order, so results repeat bit for bit and do not
 // depend on the pool's page placement.
 #include <algorithm>
@@ -176,12 +176,6 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
     P.ws.ctrl[0] = split;
     P.ws.ctrl[1] = carry_s;
     P.ws.ctrl[2] = 0;
-  }
-  // sequences with nothing to read output 0 (no work item writes them)
-  for (int b = 0; b < P.B; ++b) {
-    if (seq_chunks(P, b, false) > 0) continue;
-    float* o = P.out + (size_t)b * P.h_q * P.d;
-    for (int i = tid; i < P.h_q * P.d; i += nt) o[i] = 0.f;
   }
 }
 
@@ -747,7 +741,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_f32_kernel(DecodeParams
 // reduce the maximum; each split's weight exp2(m_i - M) is broadcast from its
 // lane while the lanes sum the weighted P.V rows (8 splits in flight).
 // Sequences with one split were written by the main kernel when
-// skip_single is set.
+// skip_single is set; sequences with none output 0.
 
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams P, int skip_single) {
@@ -757,7 +751,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams P, int
   if (wi >= (int64_t)P.B * P.h_q) return;
   const int b = (int)(wi / P.h_q), h = (int)(wi - (int64_t)b * P.h_q);
   const int s0 = __ldg(P.ws.split_off + b), ns = __ldg(P.ws.split_off + b + 1) - s0;
-  if (ns == 0 || (ns == 1 && skip_single)) return;
+  if (ns == 0) {  // nothing to read: the output is 0
+    float* out = P.out + (size_t)wi * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = 0.f;
+    return;
+  }
+  if (ns == 1 && skip_single) return;
   const float* ml = P.ws.ml + ((size_t)s0 * P.h_q + h) * 2;
   const float* acc = P.ws.acc + ((size_t)s0 * P.h_q + h) * D + lane * E;
   const size_t ml_stride = (size_t)P.h_q * 2, acc_stride = (size_t)P.h_q * D;
