@@ -144,6 +144,32 @@ tl_status tl_paged_attn_decode(const void* q, const void* k_cache, const void* v
                                size_t workspace_bytes, uint32_t* error_word, void* stream);
 
 /*
+ * Decode without any device allocation, for callers that cannot allocate on
+ * this path: a host framework that owns all device memory through its own
+ * pool, or a latency-bound loop that cannot afford an allocator call.  There
+ * is no counterpart in the paper; it is a deployment convenience.
+ *
+ * Same arguments, result and errors as tl_paged_attn_decode, without the
+ * workspace: the scratch comes from a fixed array of
+ * TL_DECODE_NOALLOC_SCRATCH_BYTES inside the library's device memory, which
+ * every GPU that loads the library holds until the process exits.  The first
+ * call on a device (with that device current) looks up the array's address;
+ * make that first call before any stream capture.  Returns TL_ERR_WORKSPACE
+ * when tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d) exceeds the
+ * array (for example B=64, h_q=32, h_kv=8, d=128 needs about 27 MB and fits).
+ * All calls on a device share the array, which keeps the last call's
+ * contents (nothing in it needs to start at zero); calls whose GPU work
+ * overlaps (other streams or host threads) race on it and must be serialised.
+ */
+#define TL_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, int32_t max_pages_per_seq,
+                                       const int32_t* context_lens, float* out, int32_t B,
+                                       int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                       int32_t page_size, int32_t window, float scale,
+                                       tl_dtype dtype, uint32_t* error_word, void* stream);
+
+/*
  * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes).
  */
 size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,

@@ -8,7 +8,8 @@ without the built library, or without a CUDA device, raises.
 from .api import (TL_BF16, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noqa: F401
                   TL_DEVERR_SLOT_RANGE, TL_ERR_CUDA, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED,
                   TL_ERR_WORKSPACE, TL_F32, TL_OK, TLError, alloc_workspace,
-                  tl_kv_cache_write, tl_paged_attn_decode, tl_paged_attn_decode_workspace_size,
+                  TL_DECODE_NOALLOC_SCRATCH_BYTES, tl_kv_cache_write, tl_paged_attn_decode,
+                  tl_paged_attn_decode_noalloc, tl_paged_attn_decode_workspace_size,
                   tl_paged_attn_prefill, tl_paged_attn_prefill_workspace_size, tl_status_string,
                   tl_version)
 from . import build as _build_module
@@ -19,7 +20,8 @@ def build_library(force: bool = False) -> str:
     return _build_module.build(force=force)
 
 __all__ = [
-    "tl_kv_cache_write", "tl_paged_attn_decode", "tl_paged_attn_prefill",
+    "tl_kv_cache_write", "tl_paged_attn_decode", "tl_paged_attn_decode_noalloc",
+    "tl_paged_attn_prefill",
     "tl_paged_attn_decode_workspace_size", "tl_paged_attn_prefill_workspace_size",
     "tl_status_string", "tl_version", "TLError", "build_library", "alloc_workspace",
 ]

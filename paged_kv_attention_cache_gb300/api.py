@@ -116,6 +116,33 @@ def tl_paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
     return out
 
 
+TL_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def tl_paged_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 block_table: torch.Tensor, context_lens: torch.Tensor,
+                                 scale: float, out: torch.Tensor, window: int = 0,
+                                 error_word: Optional[torch.Tensor] = None,
+                                 stream=None) -> torch.Tensor:
+    """Decode into a caller-provided `out` without any device allocation: the
+    scratch is a fixed array inside the library (see the C header); calls on a
+    device share it, so calls that overlap on the GPU must be serialised."""
+    _need(q, "q", k_cache.dtype)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    _need(out, "out", torch.float32)
+    B, hq, d = q.shape
+    P, ps, hkv, _ = k_cache.shape
+    st = _lib.load().tl_paged_attn_decode_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(context_lens), _ptr(out), B, hq, hkv, d, P, ps, int(window), float(scale),
+        _DTYPES.get(k_cache.dtype, -1), _ptr(error_word), _stream(stream))
+    _check(st, "tl_paged_attn_decode_noalloc")
+    return out
+
+
 def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                           block_table: torch.Tensor, positions: torch.Tensor, scale: float,
                           window: int = 0, out: Optional[torch.Tensor] = None,

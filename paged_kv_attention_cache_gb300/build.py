@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtlpa.so")
 
-SOURCES = ["api.cu", "kv_cache_write.cu", "paged_decode.cu", "paged_prefill.cu"]
+SOURCES = ["api.cu", "kv_cache_write.cu", "paged_decode.cu", "paged_prefill.cu",
+           "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "-I" + CSRC, "--expt-relaxed-constexpr"]
