@@ -13,6 +13,7 @@
 // row, and its arithmetic does not depend on B, so a row gives the same bits
 // batched or alone.
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace tl {
 
@@ -279,6 +280,370 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
   }
 }
 
+
+// ------------------------------------------------------- tcgen05 prefill --
+//
+// One CTA per (query tile, KV head, row): the tile packs tokens_per_tile =
+// 128/group consecutive tokens of one row with all `group` query heads that
+// share the KV head, as the 128 M rows (row r = token r/group, head r%group),
+// so one K/V tile feeds all of them.  The CTA folds the key range its live
+// tokens can see ([min lo, max p]) in tiles of 128 keys.
+//   warp 0      TMA producer: the Q tile once (a 3-D map (d, H_q, token),
+//               box 64 x group x tokens), then K and V tiles into rings of
+//               kKS / kVS stages, 16-row boxes of the pool map, one per page
+//               run; boxes past the sequence or on bad pages load zeros; the
+//               last V tile's rows past the CTA's last position are zeroed.
+//   warp 1      TMEM owner (allocates 512 columns) and MMA issuer (one lane):
+//               S_j = Q K_j^T into TMEM buffer j%2 (M=128, N=128, K=128:
+//               8 MMAs from smem descriptors), then O += P_j V_j with P_j
+//               read from TMEM (hi and lo bf16 parts: 16 MMAs).
+//   warps 2-5   softmax, one thread per M row: load S_j from TMEM, mask by
+//               the row's causal / window range, running max in log2 units
+//               with a lazy rescale (O and the sum are rescaled only when
+//               the max grows by more than 2^8), write P_j = hi + lo bf16
+//               into S_j's own TMEM columns, then the epilogue O / l.
+// S is double-buffered, so the tensor core computes S_{j+1} while the
+// softmax works on S_j.  All waits are bounded.
+constexpr int kTcKS = 3;             // K stages
+constexpr int kTcVS = 2;             // V stages
+constexpr int kTcThreads = 6 * 32;
+constexpr int kTcTileBytes = 32768;  // 128 rows x 128 d x bf16
+constexpr int kTcSmem = (1 + kTcKS + kTcVS) * kTcTileBytes + 1024;
+constexpr float kRescaleLog2 = 8.f;
+
+struct TcShared {
+  unsigned long long q_full, k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS], v_fix;
+  unsigned long long s_full[2], p_full[2], pv_done[2], mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct TcRange {
+  int kmin, kmax;  // key range of the tile's live tokens (kmax < 0: none)
+};
+
+// Every warp computes the tile's key range itself (no shared state needed).
+__device__ __forceinline__ TcRange tc_tile_range(const PrefillParams& P, int b, int t0, int tpt,
+                                                 int64_t cap) {
+  int kmin = INT32_MAX, kmax = -1;
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i < tpt; i += 32) {
+    const int t = t0 + i;
+    if (t >= P.T) break;
+    int p = P.positions[(size_t)b * P.T + t];
+    if (p >= cap) p = -1;
+    if (p >= 0) {
+      const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
+      kmin = min(kmin, lo);
+      kmax = max(kmax, p);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  return {kmin, kmax};
+}
+
+__device__ __forceinline__ void tma_load_3d_tc(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                               int c2, uint32_t bar) {
+  tma_load_3d(dst, map, c0, c1, c2, bar);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, int box_rows) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ TcShared sh;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t sQ = sbase, sK = sbase + kTcTileBytes, sV = sK + kTcKS * kTcTileBytes;
+  volatile int* abort_flag = &sh.abort_flag;
+
+  const int tpt = 128 / P.group;                 // tokens per tile
+  const int rows_used = tpt * P.group;
+  const int n_qt = (P.T + tpt - 1) / tpt;
+  const int qt = n_qt - 1 - (int)blockIdx.x;     // latest (heaviest) tiles first
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int t0 = qt * tpt;
+  const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
+  const TcRange rg = tc_tile_range(P, b, t0, tpt, cap);
+
+  if (rg.kmax < 0) {  // no live token: the outputs are 0
+    for (int idx = threadIdx.x; idx < rows_used * 32; idx += kTcThreads) {
+      const int r = idx >> 5, c = (idx & 31) * 4;
+      const int t = t0 + r / P.group;
+      if (t < P.T)
+        *reinterpret_cast<float4*>(
+            P.out + (((size_t)b * P.T + t) * P.h_q + (size_t)g * P.group + r % P.group) * 128 + c) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  const int tile0 = rg.kmin / 128, n_tiles = rg.kmax / 128 - tile0 + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sh.q_full), 1);
+    for (int i = 0; i < kTcKS; ++i) {
+      mbar_init(smem_u32(&sh.k_full[i]), 1);
+      mbar_init(smem_u32(&sh.k_empty[i]), 1);
+    }
+    for (int i = 0; i < kTcVS; ++i) {
+      mbar_init(smem_u32(&sh.v_full[i]), 1);
+      mbar_init(smem_u32(&sh.v_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&sh.v_fix), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh.s_full[i]), 1);
+      mbar_init(smem_u32(&sh.p_full[i]), 4);
+      mbar_init(smem_u32(&sh.pv_done[i]), 1);
+    }
+    mbar_init(smem_u32(&sh.mma_drain), 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tc::alloc(smem_u32(&sh.tmem_base), 512);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  constexpr uint32_t kColO = 256;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- TMA
+    const int nbox = 128 / box_rows;  // boxes per row half of a tile
+    const int n_slots = P.num_pages * P.page_size;
+    const int32_t* bt_row = P.block_table + (size_t)b * P.max_pages_per_seq;
+    const int last_blk = rg.kmax / P.page_size;
+    int win_blk0 = -1, win = -1;
+    uint32_t k_issued = 0, v_issued = 0;
+    bool ok = true;
+    if (lane == 0) {
+      const uint32_t qbytes = (uint32_t)(64 * rows_used * 2);
+      mbar_arrive_expect_tx(smem_u32(&sh.q_full), 2 * qbytes);
+      for (int h = 0; h < 2; ++h)
+        tma_load_3d(sQ + h * (kTcTileBytes / 2), &qmap, h * 64, g * P.group, b * P.T + t0,
+                    smem_u32(&sh.q_full));
+    }
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int key0 = (tile0 + j) * 128;
+      // block-table window covering this tile's blocks
+      const int bmin = key0 / P.page_size;
+      const int bmax = min((key0 + 127) / P.page_size, last_blk);
+      if (win_blk0 < 0 || bmin < win_blk0 || bmax >= win_blk0 + 32) {
+        win_blk0 = bmin;
+        const int blk = win_blk0 + lane;
+        win = blk <= last_blk ? __ldg(bt_row + blk) : -1;
+      }
+      // this lane's box (lanes < 2*nbox): half = lane / nbox, box = lane % nbox
+      const int half = lane / nbox, bi = lane % nbox;
+      const int kb = key0 + bi * box_rows;
+      const int blk = kb / P.page_size;
+      const int pg = __shfl_sync(0xffffffffu, win, (blk - win_blk0) & 31);
+      const bool box_ok = blk <= last_blk && pg >= 0 && pg < P.num_pages;
+      if (blk <= last_blk && !box_ok && lane < 2 * nbox) report(P.error_word, TL_DEVERR_PAGE_RANGE);
+      const int slot0 = box_ok ? pg * P.page_size + kb % P.page_size : n_slots;
+      const uint32_t boff = half * (kTcTileBytes / 2) + bi * box_rows * 128;
+      // K tile
+      {
+        const int st = j % kTcKS;
+        if (!mbar_wait(smem_u32(&sh.k_empty[st]), ((j / kTcKS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.k_full[st]), kTcTileBytes);
+        __syncwarp();
+        if (lane < 2 * nbox)
+          tma_load_3d(sK + st * kTcTileBytes + boff, &kmap, half * 64, g, slot0,
+                      smem_u32(&sh.k_full[st]));
+        ++k_issued;
+      }
+      // V tile
+      {
+        const int st = j % kTcVS;
+        if (!mbar_wait(smem_u32(&sh.v_empty[st]), ((j / kTcVS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcTileBytes);
+        __syncwarp();
+        if (lane < 2 * nbox)
+          tma_load_3d(sV + st * kTcTileBytes + boff, &vmap, half * 64, g, slot0,
+                      smem_u32(&sh.v_full[st]));
+        ++v_issued;
+        if (j == n_tiles - 1) {
+          // rows past the CTA's last position may hold anything: zero them
+          if (!mbar_wait(smem_u32(&sh.v_full[st]), (j / kTcVS) & 1, abort_flag)) { ok = false; break; }
+          const int first_dead = rg.kmax + 1 - key0;  // 1..128
+          const uint32_t vt = sV + st * kTcTileBytes;
+          for (int idx = lane; idx < (128 - first_dead) * 16; idx += 32) {
+            const int row = first_dead + (idx >> 4), hu = idx & 15;
+            const uint32_t a = vt + (hu >> 3) * (kTcTileBytes / 2) + row * 128 + ((hu & 7) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sh.v_fix));
+        }
+      }
+    }
+    // drain: the copies this warp issued have landed before the CTA exits
+    bool drained = true;
+    for (uint32_t i = k_issued > (uint32_t)kTcKS ? k_issued - kTcKS : 0; i < k_issued; ++i)
+      drained &= mbar_drain(smem_u32(&sh.k_full[i % kTcKS]), (i / kTcKS) & 1);
+    for (uint32_t i = v_issued > (uint32_t)kTcVS ? v_issued - kTcVS : 0; i < v_issued; ++i)
+      drained &= mbar_drain(smem_u32(&sh.v_full[i % kTcVS]), (i / kTcVS) & 1);
+    drained &= mbar_drain(smem_u32(&sh.q_full), 0);
+    if (!drained) *abort_flag = 1;
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idS = tc::idesc_bf16(128, 128, 0, 0);
+      const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
+      bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort_flag);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kTcKS;
+        if (!mbar_wait(smem_u32(&sh.k_full[st]), (j / kTcKS) & 1, abort_flag)) return false;
+        tc::fence_after();
+        const uint32_t kt = sK + st * kTcTileBytes;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * (kTcTileBytes / 2) + (k & 3) * 32;
+          tc::mma_ss(tmem + (j & 1) * 128, tc::sdesc(sQ + off, 16, 1024),
+                     tc::sdesc(kt + off, 16, 1024), idS, k > 0);
+        }
+        tc::commit(smem_u32(&sh.k_empty[st]));
+        tc::commit(smem_u32(&sh.s_full[j & 1]));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_tiles > 1) ok = issue_s(1);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (!mbar_wait(smem_u32(&sh.p_full[j & 1]), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        const int vst = j % kTcVS;
+        const bool last = j == n_tiles - 1;
+        if (!mbar_wait(last ? smem_u32(&sh.v_fix) : smem_u32(&sh.v_full[vst]),
+                       last ? 0 : (j / kTcVS) & 1, abort_flag)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t vt = sV + vst * kTcTileBytes;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            tc::mma_ts(tmem + kColO, tmem + (j & 1) * 128 + part * 64 + k * 8,
+                       tc::sdesc(vt + k * 2048, kTcTileBytes / 2, 1024), idPV,
+                       (j > 0 || part > 0 || k > 0) ? 1u : 0u);
+        }
+        tc::commit(smem_u32(&sh.v_empty[vst]));
+        tc::commit(smem_u32(&sh.pv_done[j & 1]));
+        if (j + 2 < n_tiles && !issue_s(j + 2)) { ok = false; break; }
+      }
+      // every MMA this thread issued is done before TMEM is released
+      tc::commit(smem_u32(&sh.mma_drain));
+      if (!mbar_drain(smem_u32(&sh.mma_drain), 0)) *abort_flag = 1;
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- softmax
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int t = t0 + row / P.group, h = g * P.group + row % P.group;
+    int p = -1;
+    if (row < rows_used && t < P.T) {
+      p = P.positions[(size_t)b * P.T + t];
+      if (p >= cap) {
+        report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
+        p = -1;
+      }
+    }
+    const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!mbar_wait(smem_u32(&sh.s_full[j & 1]), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc::fence_after();
+      const uint32_t sb = tmem + lane_base + (j & 1) * 128;
+      float s[128];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc::ld32(sb + q * 32, s + q * 32);
+      tc::wait_ld();
+      const int key0 = (tile0 + j) * 128;
+      const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        s[c] = (c >= cmin && c <= cmax) ? s[c] * P.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[c]);
+      }
+      const bool need = l > 0.f && mt > m_used + kRescaleLog2;
+      if (__any_sync(0xffffffffu, need)) {
+        // rescale O (and l) by 2^(m_used - mt) before this tile's P.V lands
+        if (!mbar_wait(smem_u32(&sh.pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        const float corr = need ? fast_exp2(m_used - mt) : 1.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float o[32];
+          tc::ld32(tmem + lane_base + kColO + q * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tc::st32(tmem + lane_base + kColO + q * 32, o);
+        }
+        tc::wait_st();
+        if (need) {
+          l *= corr;
+          m_used = mt;
+        }
+      }
+      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t hi[16], lw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = fast_exp2(s[q * 32 + 2 * i] - base);
+          const float bb = fast_exp2(s[q * 32 + 2 * i + 1] - base);
+          l += a + bb;
+          split_bf16x2(a, bb, hi[i], lw[i]);
+        }
+        tc::st16(sb + q * 16, hi);
+        tc::st16(sb + 64 + q * 16, lw);
+      }
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[j & 1]));
+    }
+    // epilogue: O / l
+    if (ok && mbar_wait(smem_u32(&sh.pv_done[(n_tiles - 1) & 1]), ((n_tiles - 1) >> 1) & 1,
+                        abort_flag)) {
+      tc::fence_after();
+      const float inv = (p >= 0 && l > 0.f) ? 1.f / l : 0.f;
+      float* dst = P.out + (((size_t)b * P.T + t) * P.h_q + h) * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float o[32];
+        tc::ld32(tmem + lane_base + kColO + q * 32, o);
+        tc::wait_ld();
+        if (row < rows_used && t < P.T) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + q * 32 + i) =
+                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+        }
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();  // every wait above is bounded, so every thread gets here
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && sh.abort_flag) report(P.error_word, TL_DEVERR_TIMEOUT);
+}
 }  // namespace tl
 
 extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q,
@@ -330,12 +695,30 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   P.window = window;
   P.scale_log2 = scale * kLog2e;
   P.error_word = error_word;
-  const int n_qt = (T + kPfRows - 1) / kPfRows;
-  if (B > 65535 || h_q > 65535) return TL_ERR_UNSUPPORTED;
-  auto kern = prefill_mma_kernel<128>;
-  const int sm = PfSmem<128>::kTotal;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) != cudaSuccess)
+  if (h_q / h_kv > 128 || B > 65535 || h_kv > 65535) return TL_ERR_UNSUPPORTED;
+  if ((int64_t)num_pages * page_size >= ((int64_t)1 << 31) || (int64_t)B * T >= ((int64_t)1 << 31))
+    return TL_ERR_UNSUPPORTED;
+  const int group = h_q / h_kv;
+  const int tpt = 128 / group;
+  const int box_rows = page_size % 16 == 0 ? 16 : 8;
+  CUtensorMap qmap, kmap, vmap;
+  {
+    const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
+    const uint64_t qs[2] = {128 * 2, (uint64_t)h_q * 128 * 2};
+    const uint32_t qb[3] = {64, (uint32_t)group, (uint32_t)tpt};
+    const uint64_t kd[3] = {128, (uint64_t)h_kv, (uint64_t)num_pages * page_size};
+    const uint64_t ks[2] = {128 * 2, (uint64_t)h_kv * 128 * 2};
+    const uint32_t kb[3] = {64, 1, (uint32_t)box_rows};
+    if (!encode_bf16_tensor_map(&qmap, q, 3, qd, qs, qb, true) ||
+        !encode_bf16_tensor_map(&kmap, k_cache, 3, kd, ks, kb, true) ||
+        !encode_bf16_tensor_map(&vmap, v_cache, 3, kd, ks, kb, true))
+      return TL_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTcSmem) != cudaSuccess)
     return TL_ERR_CUDA;
-  kern<<<dim3(n_qt, h_q, B), kPfThreads, sm, (cudaStream_t)stream>>>(P);
+  const int n_qt = (T + tpt - 1) / tpt;
+  prefill_tc_kernel<<<dim3(n_qt, h_kv, B), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
+      P, qmap, kmap, vmap, box_rows);
   return launch_status();
 }
