@@ -188,8 +188,9 @@ size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, i
  *   positions    [B][T] int32, -1 = padding
  *   out          [B][T][h_q][d] float32
  *   other arguments as for decode.
- * Supported: dtype TL_BF16, d = 128, h_q % h_kv == 0, page_size a power of
- * two in [8, 128].  Otherwise TL_ERR_UNSUPPORTED.
+ * Supported: dtype TL_BF16, d = 128, h_q % h_kv == 0 with h_q/h_kv <= 128,
+ * page_size a power of two in [8, 128].  Otherwise TL_ERR_UNSUPPORTED.
+ * scale must be positive and finite (TL_ERR_INVALID_ARG otherwise).
  */
 tl_status tl_paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int32_t max_pages_per_seq,

@@ -287,28 +287,36 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
 // 128/group consecutive tokens of one row with all `group` query heads that
 // share the KV head, as the 128 M rows (row r = token r/group, head r%group),
 // so one K/V tile feeds all of them.  The CTA folds the key range its live
-// tokens can see ([min lo, max p]) in tiles of 128 keys.
+// tokens can see ([min lo, max p]) in tiles of kBN = 64 keys.  Two CTAs fit
+// on an SM (96 KiB of shared memory and 256 TMEM columns each), so one CTA's
+// softmax overlaps the other's MMAs.
 //   warp 0      TMA producer: the Q tile once (a 3-D map (d, H_q, token),
 //               box 64 x group x tokens), then K and V tiles into rings of
-//               kKS / kVS stages, 16-row boxes of the pool map, one per page
-//               run; boxes past the sequence or on bad pages load zeros; the
-//               last V tile's rows past the CTA's last position are zeroed.
-//   warp 1      TMEM owner (allocates 512 columns) and MMA issuer (one lane):
-//               S_j = Q K_j^T into TMEM buffer j%2 (M=128, N=128, K=128:
-//               8 MMAs from smem descriptors), then O += P_j V_j with P_j
-//               read from TMEM (hi and lo bf16 parts: 16 MMAs).
+//               kKS / kVS stages, boxes of 8 or 16 rows of the pool map (one
+//               page run each); boxes past the sequence or on bad pages load
+//               zeros; the last V tile's rows past the CTA's last position
+//               are zeroed.
+//   warp 1      TMEM owner (256 columns) and MMA issuer (one lane): S_j =
+//               Q K_j^T into TMEM buffer j%2 (M=128, N=64, K=128: 8 MMAs from
+//               shared-memory descriptors), then O += P_j V_j with P_j read
+//               from TMEM (hi and lo bf16 parts: 8 MMAs of K=16).
 //   warps 2-5   softmax, one thread per M row: load S_j from TMEM, mask by
-//               the row's causal / window range, running max in log2 units
-//               with a lazy rescale (O and the sum are rescaled only when
-//               the max grows by more than 2^8), write P_j = hi + lo bf16
-//               into S_j's own TMEM columns, then the epilogue O / l.
+//               the row's causal / window range (skipped when the whole warp
+//               sees only live keys), running max in log2 units with a lazy
+//               rescale (O and the sum change only when the max grows by
+//               more than 2^8), write P_j = hi + lo bf16 into S_j's own
+//               columns, then the epilogue O / l.
 // S is double-buffered, so the tensor core computes S_{j+1} while the
 // softmax works on S_j.  All waits are bounded.
-constexpr int kTcKS = 3;             // K stages
+constexpr int kBN = 64;              // keys per tile
+constexpr int kTcKS = 2;             // K stages
 constexpr int kTcVS = 2;             // V stages
 constexpr int kTcThreads = 6 * 32;
-constexpr int kTcTileBytes = 32768;  // 128 rows x 128 d x bf16
-constexpr int kTcSmem = (1 + kTcKS + kTcVS) * kTcTileBytes + 1024;
+constexpr int kTcQBytes = 32768;     // 128 rows x 128 d x bf16
+constexpr int kTcKVBytes = kBN * 256;  // 64 keys x 128 d x bf16 (two 8 KiB halves)
+constexpr int kTcSmem = kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
+constexpr uint32_t kTcCols = 256;    // TMEM: S0 [0,64), S1 [64,128), O [128,256)
+constexpr uint32_t kColO = 128;
 constexpr float kRescaleLog2 = 8.f;
 
 struct TcShared {
@@ -346,12 +354,7 @@ __device__ __forceinline__ TcRange tc_tile_range(const PrefillParams& P, int b, 
   return {kmin, kmax};
 }
 
-__device__ __forceinline__ void tma_load_3d_tc(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                               int c2, uint32_t bar) {
-  tma_load_3d(dst, map, c0, c1, c2, bar);
-}
-
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, int box_rows) {
@@ -359,8 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ TcShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  unsigned char* smem = smem_raw + (sbase - smem_u32(smem_raw));
-  const uint32_t sQ = sbase, sK = sbase + kTcTileBytes, sV = sK + kTcKS * kTcTileBytes;
+  const uint32_t sQ = sbase, sK = sbase + kTcQBytes, sV = sK + kTcKS * kTcKVBytes;
   volatile int* abort_flag = &sh.abort_flag;
 
   const int tpt = 128 / P.group;                 // tokens per tile
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     return;
   }
-  const int tile0 = rg.kmin / 128, n_tiles = rg.kmax / 128 - tile0 + 1;
+  const int tile0 = rg.kmin / kBN, n_tiles = rg.kmax / kBN - tile0 + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sh.q_full), 1);
@@ -405,34 +407,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sh.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tc::alloc(smem_u32(&sh.tmem_base), 512);
+  if (warp == 1) tc::alloc(smem_u32(&sh.tmem_base), kTcCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = sh.tmem_base;
-  constexpr uint32_t kColO = 256;
 
   if (warp == 0) {
     // -------------------------------------------------------------- TMA
-    const int nbox = 128 / box_rows;  // boxes per row half of a tile
+    const int nbox = kBN / box_rows;  // boxes per row half of a tile
     const int n_slots = P.num_pages * P.page_size;
     const int32_t* bt_row = P.block_table + (size_t)b * P.max_pages_per_seq;
     const int last_blk = rg.kmax / P.page_size;
     int win_blk0 = -1, win = -1;
     uint32_t k_issued = 0, v_issued = 0;
-    bool ok = true;
     if (lane == 0) {
       const uint32_t qbytes = (uint32_t)(64 * rows_used * 2);
       mbar_arrive_expect_tx(smem_u32(&sh.q_full), 2 * qbytes);
       for (int h = 0; h < 2; ++h)
-        tma_load_3d(sQ + h * (kTcTileBytes / 2), &qmap, h * 64, g * P.group, b * P.T + t0,
+        tma_load_3d(sQ + h * (kTcQBytes / 2), &qmap, h * 64, g * P.group, b * P.T + t0,
                     smem_u32(&sh.q_full));
     }
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int key0 = (tile0 + j) * 128;
-      // block-table window covering this tile's blocks
+    for (int j = 0; j < n_tiles; ++j) {
+      const int key0 = (tile0 + j) * kBN;
       const int bmin = key0 / P.page_size;
-      const int bmax = min((key0 + 127) / P.page_size, last_blk);
+      const int bmax = min((key0 + kBN - 1) / P.page_size, last_blk);
       if (win_blk0 < 0 || bmin < win_blk0 || bmax >= win_blk0 + 32) {
         win_blk0 = bmin;
         const int blk = win_blk0 + lane;
@@ -446,36 +445,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool box_ok = blk <= last_blk && pg >= 0 && pg < P.num_pages;
       if (blk <= last_blk && !box_ok && lane < 2 * nbox) report(P.error_word, TL_DEVERR_PAGE_RANGE);
       const int slot0 = box_ok ? pg * P.page_size + kb % P.page_size : n_slots;
-      const uint32_t boff = half * (kTcTileBytes / 2) + bi * box_rows * 128;
-      // K tile
+      const uint32_t boff = half * (kTcKVBytes / 2) + bi * box_rows * 128;
       {
         const int st = j % kTcKS;
-        if (!mbar_wait(smem_u32(&sh.k_empty[st]), ((j / kTcKS) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.k_full[st]), kTcTileBytes);
+        if (!mbar_wait(smem_u32(&sh.k_empty[st]), ((j / kTcKS) & 1) ^ 1, abort_flag)) break;
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.k_full[st]), kTcKVBytes);
         __syncwarp();
         if (lane < 2 * nbox)
-          tma_load_3d(sK + st * kTcTileBytes + boff, &kmap, half * 64, g, slot0,
+          tma_load_3d(sK + st * kTcKVBytes + boff, &kmap, half * 64, g, slot0,
                       smem_u32(&sh.k_full[st]));
         ++k_issued;
       }
-      // V tile
       {
         const int st = j % kTcVS;
-        if (!mbar_wait(smem_u32(&sh.v_empty[st]), ((j / kTcVS) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcTileBytes);
+        if (!mbar_wait(smem_u32(&sh.v_empty[st]), ((j / kTcVS) & 1) ^ 1, abort_flag)) break;
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcKVBytes);
         __syncwarp();
         if (lane < 2 * nbox)
-          tma_load_3d(sV + st * kTcTileBytes + boff, &vmap, half * 64, g, slot0,
+          tma_load_3d(sV + st * kTcKVBytes + boff, &vmap, half * 64, g, slot0,
                       smem_u32(&sh.v_full[st]));
         ++v_issued;
         if (j == n_tiles - 1) {
           // rows past the CTA's last position may hold anything: zero them
-          if (!mbar_wait(smem_u32(&sh.v_full[st]), (j / kTcVS) & 1, abort_flag)) { ok = false; break; }
-          const int first_dead = rg.kmax + 1 - key0;  // 1..128
-          const uint32_t vt = sV + st * kTcTileBytes;
-          for (int idx = lane; idx < (128 - first_dead) * 16; idx += 32) {
+          if (!mbar_wait(smem_u32(&sh.v_full[st]), (j / kTcVS) & 1, abort_flag)) break;
+          const int first_dead = rg.kmax + 1 - key0;  // 1..kBN
+          const uint32_t vt = sV + st * kTcKVBytes;
+          for (int idx = lane; idx < (kBN - first_dead) * 16; idx += 32) {
             const int row = first_dead + (idx >> 4), hu = idx & 15;
-            const uint32_t a = vt + (hu >> 3) * (kTcTileBytes / 2) + row * 128 + ((hu & 7) << 4);
+            const uint32_t a = vt + (hu >> 3) * (kTcKVBytes / 2) + row * 128 + ((hu & 7) << 4);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
           }
           fence_proxy_async_smem();
@@ -495,19 +492,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t idS = tc::idesc_bf16(128, 128, 0, 0);
+      const uint32_t idS = tc::idesc_bf16(128, kBN, 0, 0);
       const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
       bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort_flag);
       auto issue_s = [&](int j) -> bool {
         const int st = j % kTcKS;
         if (!mbar_wait(smem_u32(&sh.k_full[st]), (j / kTcKS) & 1, abort_flag)) return false;
         tc::fence_after();
-        const uint32_t kt = sK + st * kTcTileBytes;
+        const uint32_t kt = sK + st * kTcKVBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * (kTcTileBytes / 2) + (k & 3) * 32;
-          tc::mma_ss(tmem + (j & 1) * 128, tc::sdesc(sQ + off, 16, 1024),
-                     tc::sdesc(kt + off, 16, 1024), idS, k > 0);
+          const uint32_t qo = (k >> 2) * (kTcQBytes / 2) + (k & 3) * 32;
+          const uint32_t ko = (k >> 2) * (kTcKVBytes / 2) + (k & 3) * 32;
+          tc::mma_ss(tmem + (j & 1) * kBN, tc::sdesc(sQ + qo, 16, 1024),
+                     tc::sdesc(kt + ko, 16, 1024), idS, k > 0);
         }
         tc::commit(smem_u32(&sh.k_empty[st]));
         tc::commit(smem_u32(&sh.s_full[j & 1]));
@@ -516,24 +514,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (ok) ok = issue_s(0);
       if (ok && n_tiles > 1) ok = issue_s(1);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        if (!mbar_wait(smem_u32(&sh.p_full[j & 1]), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&sh.p_full[j & 1]), (j >> 1) & 1, abort_flag)) break;
         const int vst = j % kTcVS;
         const bool last = j == n_tiles - 1;
         if (!mbar_wait(last ? smem_u32(&sh.v_fix) : smem_u32(&sh.v_full[vst]),
-                       last ? 0 : (j / kTcVS) & 1, abort_flag)) { ok = false; break; }
+                       last ? 0 : (j / kTcVS) & 1, abort_flag))
+          break;
         tc::fence_after();
-        const uint32_t vt = sV + vst * kTcTileBytes;
+        const uint32_t vt = sV + vst * kTcKVBytes;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            tc::mma_ts(tmem + kColO, tmem + (j & 1) * 128 + part * 64 + k * 8,
-                       tc::sdesc(vt + k * 2048, kTcTileBytes / 2, 1024), idPV,
+          for (int k = 0; k < kBN / 16; ++k)
+            tc::mma_ts(tmem + kColO, tmem + (j & 1) * kBN + part * (kBN / 2) + k * 8,
+                       tc::sdesc(vt + k * 2048, kTcKVBytes / 2, 1024), idPV,
                        (j > 0 || part > 0 || k > 0) ? 1u : 0u);
         }
         tc::commit(smem_u32(&sh.v_empty[vst]));
         tc::commit(smem_u32(&sh.pv_done[j & 1]));
-        if (j + 2 < n_tiles && !issue_s(j + 2)) { ok = false; break; }
+        if (j + 2 < n_tiles && !issue_s(j + 2)) break;
       }
       // every MMA this thread issued is done before TMEM is released
       tc::commit(smem_u32(&sh.mma_drain));
@@ -554,24 +553,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
-    float m_used = -INFINITY, l = 0.f;
+    const float sc = P.scale_log2;
+    float m_used = -INFINITY, l = 0.f;  // running max of the raw scores (x sc = log2 units)
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       if (!mbar_wait(smem_u32(&sh.s_full[j & 1]), (j >> 1) & 1, abort_flag)) { ok = false; break; }
       tc::fence_after();
-      const uint32_t sb = tmem + lane_base + (j & 1) * 128;
-      float s[128];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tc::ld32(sb + q * 32, s + q * 32);
+      const uint32_t sb = tmem + lane_base + (j & 1) * kBN;
+      float s[kBN];
+      tc::ld32(sb, s);
+      tc::ld32(sb + 32, s + 32);
       tc::wait_ld();
-      const int key0 = (tile0 + j) * 128;
+      const int key0 = (tile0 + j) * kBN;
       const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
-      float mt = -INFINITY;
+      if (!__all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1)) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = (c >= cmin && c <= cmax) ? s[c] * P.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[c]);
+        for (int c = 0; c < kBN; ++c)
+          s[c] = (c >= cmin && c <= cmax) ? s[c] : -INFINITY;
       }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
       const bool need = l > 0.f && mt > m_used + kRescaleLog2;
       if (__any_sync(0xffffffffu, need)) {
         // rescale O (and l) by 2^(m_used - mt) before this tile's P.V lands
@@ -598,19 +604,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (m_used == -INFINITY) m_used = mt;  // first live key of this row
       const float base = m_used == -INFINITY ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t hi[16], lw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = fast_exp2(s[q * 32 + 2 * i] - base);
-          const float bb = fast_exp2(s[q * 32 + 2 * i + 1] - base);
-          l += a + bb;
+          const float a = fast_exp2(fmaf(s[q * 32 + 2 * i], sc, -base));
+          const float bb = fast_exp2(fmaf(s[q * 32 + 2 * i + 1], sc, -base));
+          ls[i & 3] += a + bb;
           split_bf16x2(a, bb, hi[i], lw[i]);
         }
         tc::st16(sb + q * 16, hi);
-        tc::st16(sb + 64 + q * 16, lw);
+        tc::st16(sb + kBN / 2 + q * 16, lw);
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
@@ -640,10 +648,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();  // every wait above is bounded, so every thread gets here
   if (warp == 1) {
     tc::fence_after();
-    tc::dealloc(tmem, 512);
+    tc::dealloc(tmem, kTcCols);
   }
   if (threadIdx.x == 0 && sh.abort_flag) report(P.error_word, TL_DEVERR_TIMEOUT);
 }
+
 }  // namespace tl
 
 extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q,
@@ -672,6 +681,7 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
       (reinterpret_cast<uintptr_t>(positions) & 3u))
     return TL_ERR_INVALID_ARG;
   if (h_q % h_kv) return TL_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || scale > 3.0e38f) return TL_ERR_INVALID_ARG;
   if (dtype != TL_BF16 || d != 128 || (page_size & (page_size - 1)) || page_size < 8 ||
       page_size > 128)
     return TL_ERR_UNSUPPORTED;
