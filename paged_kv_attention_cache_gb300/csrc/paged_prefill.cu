@@ -296,18 +296,19 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
 //               page run each); boxes past the sequence or on bad pages load
 //               zeros; the last V tile's rows past the CTA's last position
 //               are zeroed.
-//   warp 1      TMEM owner (256 columns) and MMA issuer (one lane): S_j =
-//               Q K_j^T into TMEM buffer j%2 (M=128, N=64, K=128: 8 MMAs from
-//               shared-memory descriptors), then O += P_j V_j with P_j read
+//   warp 1      TMEM owner (256 columns: S [0,64), P [64,128), O [128,256))
+//               and MMA issuer (one lane): S_{j+1} = Q K_{j+1}^T (M=128,
+//               N=64, K=128: 8 MMAs from shared-memory descriptors) as soon
+//               as the softmax has read S_j, then O += P_j V_j with P_j read
 //               from TMEM (hi and lo bf16 parts: 8 MMAs of K=16).
-//   warps 2-5   softmax, one thread per M row: load S_j from TMEM, mask by
-//               the row's causal / window range (skipped when the whole warp
-//               sees only live keys), running max in log2 units with a lazy
-//               rescale (O and the sum change only when the max grows by
-//               more than 2^8), write P_j = hi + lo bf16 into S_j's own
-//               columns, then the epilogue O / l.
-// S is double-buffered, so the tensor core computes S_{j+1} while the
-// softmax works on S_j.  All waits are bounded.
+//   warps 2-5   softmax, one thread per M row: load S_j from TMEM and free
+//               it, mask by the row's causal / window range (skipped when the
+//               whole warp sees only live keys), running max in log2 units
+//               with a lazy rescale (O and the sum change only when the max
+//               grows by more than 2^8), then, once P_{j-1}.V_{j-1} is done,
+//               write P_j = hi + lo bf16, then the epilogue O / l.
+// The tensor core computes S_{j+1} while the softmax works on S_j, and
+// P_j.V_j while the softmax works on S_{j+1}.  All waits are bounded.
 constexpr int kBN = 64;              // keys per tile
 constexpr int kTcKS = 2;             // K stages
 constexpr int kTcVS = 2;             // V stages
@@ -315,13 +316,14 @@ constexpr int kTcThreads = 6 * 32;
 constexpr int kTcQBytes = 32768;     // 128 rows x 128 d x bf16
 constexpr int kTcKVBytes = kBN * 256;  // 64 keys x 128 d x bf16 (two 8 KiB halves)
 constexpr int kTcSmem = kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
-constexpr uint32_t kTcCols = 256;    // TMEM: S0 [0,64), S1 [64,128), O [128,256)
+constexpr uint32_t kTcCols = 256;    // TMEM: S [0,64), P [64,128), O [128,256)
+constexpr uint32_t kColP = 64;
 constexpr uint32_t kColO = 128;
 constexpr float kRescaleLog2 = 8.f;
 
 struct TcShared {
   unsigned long long q_full, k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS], v_fix;
-  unsigned long long s_full[2], p_full[2], pv_done[2], mma_drain;
+  unsigned long long s_full, s_free, p_full, pv_done, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -398,11 +400,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(smem_u32(&sh.v_empty[i]), 1);
     }
     mbar_init(smem_u32(&sh.v_fix), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.p_full[i]), 4);
-      mbar_init(smem_u32(&sh.pv_done[i]), 1);
-    }
+    mbar_init(smem_u32(&sh.s_full), 1);
+    mbar_init(smem_u32(&sh.s_free), 4);
+    mbar_init(smem_u32(&sh.p_full), 4);
+    mbar_init(smem_u32(&sh.pv_done), 1);
     mbar_init(smem_u32(&sh.mma_drain), 1);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -504,17 +505,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         for (int k = 0; k < 8; ++k) {
           const uint32_t qo = (k >> 2) * (kTcQBytes / 2) + (k & 3) * 32;
           const uint32_t ko = (k >> 2) * (kTcKVBytes / 2) + (k & 3) * 32;
-          tc::mma_ss(tmem + (j & 1) * kBN, tc::sdesc(sQ + qo, 16, 1024),
-                     tc::sdesc(kt + ko, 16, 1024), idS, k > 0);
+          tc::mma_ss(tmem, tc::sdesc(sQ + qo, 16, 1024), tc::sdesc(kt + ko, 16, 1024), idS,
+                     k > 0);
         }
         tc::commit(smem_u32(&sh.k_empty[st]));
-        tc::commit(smem_u32(&sh.s_full[j & 1]));
+        tc::commit(smem_u32(&sh.s_full));
         return true;
       };
       if (ok) ok = issue_s(0);
-      if (ok && n_tiles > 1) ok = issue_s(1);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        if (!mbar_wait(smem_u32(&sh.p_full[j & 1]), (j >> 1) & 1, abort_flag)) break;
+        if (j + 1 < n_tiles) {  // S_{j+1} once the softmax has read S_j
+          if (!mbar_wait(smem_u32(&sh.s_free), j & 1, abort_flag)) break;
+          if (!issue_s(j + 1)) break;
+        }
+        if (!mbar_wait(smem_u32(&sh.p_full), j & 1, abort_flag)) break;
         const int vst = j % kTcVS;
         const bool last = j == n_tiles - 1;
         if (!mbar_wait(last ? smem_u32(&sh.v_fix) : smem_u32(&sh.v_full[vst]),
@@ -526,13 +530,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int k = 0; k < kBN / 16; ++k)
-            tc::mma_ts(tmem + kColO, tmem + (j & 1) * kBN + part * (kBN / 2) + k * 8,
+            tc::mma_ts(tmem + kColO, tmem + kColP + part * (kBN / 2) + k * 8,
                        tc::sdesc(vt + k * 2048, kTcKVBytes / 2, 1024), idPV,
                        (j > 0 || part > 0 || k > 0) ? 1u : 0u);
         }
         tc::commit(smem_u32(&sh.v_empty[vst]));
-        tc::commit(smem_u32(&sh.pv_done[j & 1]));
-        if (j + 2 < n_tiles && !issue_s(j + 2)) break;
+        tc::commit(smem_u32(&sh.pv_done));
       }
       // every MMA this thread issued is done before TMEM is released
       tc::commit(smem_u32(&sh.mma_drain));
@@ -557,13 +560,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     float m_used = -INFINITY, l = 0.f;  // running max of the raw scores (x sc = log2 units)
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!mbar_wait(smem_u32(&sh.s_full[j & 1]), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(smem_u32(&sh.s_full), j & 1, abort_flag)) { ok = false; break; }
       tc::fence_after();
-      const uint32_t sb = tmem + lane_base + (j & 1) * kBN;
       float s[kBN];
-      tc::ld32(sb, s);
-      tc::ld32(sb + 32, s + 32);
+      tc::ld32(tmem + lane_base, s);
+      tc::ld32(tmem + lane_base + 32, s + 32);
       tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free));  // S_{j+1} may overwrite it
       const int key0 = (tile0 + j) * kBN;
       const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
       if (!__all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1)) {
@@ -579,14 +584,29 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
       const bool need = l > 0.f && mt > m_used + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        // rescale O (and l) by 2^(m_used - mt) before this tile's P.V lands
-        if (!mbar_wait(smem_u32(&sh.pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+      float corr = 1.f;
+      if (need) {
+        corr = fast_exp2(m_used - mt);
+        m_used = mt;
+      }
+      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+      uint32_t hi[kBN / 2], lw[kBN / 2];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kBN / 2; ++i) {
+        const float a = fast_exp2(fmaf(s[2 * i], sc, -base));
+        const float bb = fast_exp2(fmaf(s[2 * i + 1], sc, -base));
+        ls[i & 3] += a + bb;
+        split_bf16x2(a, bb, hi[i], lw[i]);
+      }
+      l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      // P_{j-1}.V_{j-1} must be done: P's columns are reused and O is stable
+      if (j > 0) {
+        if (!mbar_wait(smem_u32(&sh.pv_done), (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc::fence_after();
-        const float corr = need ? fast_exp2(m_used - mt) : 1.f;
+      }
+      if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float o[32];
@@ -596,37 +616,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           for (int i = 0; i < 32; ++i) o[i] *= corr;
           tc::st32(tmem + lane_base + kColO + q * 32, o);
         }
-        tc::wait_st();
-        if (need) {
-          l *= corr;
-          m_used = mt;
-        }
       }
-      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t hi[16], lw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = fast_exp2(fmaf(s[q * 32 + 2 * i], sc, -base));
-          const float bb = fast_exp2(fmaf(s[q * 32 + 2 * i + 1], sc, -base));
-          ls[i & 3] += a + bb;
-          split_bf16x2(a, bb, hi[i], lw[i]);
-        }
-        tc::st16(sb + q * 16, hi);
-        tc::st16(sb + kBN / 2 + q * 16, lw);
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tc::st16(tmem + lane_base + kColP, hi);
+      tc::st16(tmem + lane_base + kColP + 16, hi + 16);
+      tc::st16(tmem + lane_base + kColP + kBN / 2, lw);
+      tc::st16(tmem + lane_base + kColP + kBN / 2 + 16, lw + 16);
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[j & 1]));
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full));
     }
     // epilogue: O / l
-    if (ok && mbar_wait(smem_u32(&sh.pv_done[(n_tiles - 1) & 1]), ((n_tiles - 1) >> 1) & 1,
-                        abort_flag)) {
+    if (ok && mbar_wait(smem_u32(&sh.pv_done), (n_tiles - 1) & 1, abort_flag)) {
       tc::fence_after();
       const float inv = (p >= 0 && l > 0.f) ? 1.f / l : 0.f;
       float* dst = P.out + (((size_t)b * P.T + t) * P.h_q + h) * 128;
