@@ -309,16 +309,27 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
 //               write P_j = hi + lo bf16, then the epilogue O / l.
 // The tensor core computes S_{j+1} while the softmax works on S_j, and
 // P_j.V_j while the softmax works on S_{j+1}.  All waits are bounded.
-constexpr int kBN = 64;              // keys per tile
-constexpr int kTcKS = 2;             // K stages
-constexpr int kTcVS = 2;             // V stages
+#ifndef TL_PREFILL_BN
+#define TL_PREFILL_BN 64
+#endif
+#ifndef TL_PREFILL_KS
+#define TL_PREFILL_KS 2
+#endif
+#ifndef TL_PREFILL_VS
+#define TL_PREFILL_VS 2
+#endif
+constexpr int kBN = TL_PREFILL_BN;   // keys per tile (64: two CTAs per SM; 128: one)
+constexpr int kTcKS = TL_PREFILL_KS; // K stages
+constexpr int kTcVS = TL_PREFILL_VS; // V stages
+constexpr int kTcCtasPerSm = kBN == 64 ? 2 : 1;
 constexpr int kTcThreads = 6 * 32;
 constexpr int kTcQBytes = 32768;     // 128 rows x 128 d x bf16
-constexpr int kTcKVBytes = kBN * 256;  // 64 keys x 128 d x bf16 (two 8 KiB halves)
+constexpr int kTcKVBytes = kBN * 256;  // kBN keys x 128 d x bf16 (two halves)
 constexpr int kTcSmem = kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
-constexpr uint32_t kTcCols = 256;    // TMEM: S [0,64), P [64,128), O [128,256)
-constexpr uint32_t kColP = 64;
-constexpr uint32_t kColO = 128;
+// TMEM: S [0,kBN), P [kBN,2kBN) (hi then lo bf16 halves), O [2kBN, 2kBN+128)
+constexpr uint32_t kColP = kBN;
+constexpr uint32_t kColO = 2 * kBN;
+constexpr uint32_t kTcCols = kBN == 64 ? 256 : 512;
 constexpr float kRescaleLog2 = 8.f;
 
 struct TcShared {
@@ -356,7 +367,7 @@ __device__ __forceinline__ TcRange tc_tile_range(const PrefillParams& P, int b, 
   return {kmin, kmax};
 }
 
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, int box_rows) {
@@ -563,8 +574,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (!mbar_wait(smem_u32(&sh.s_full), j & 1, abort_flag)) { ok = false; break; }
       tc::fence_after();
       float s[kBN];
-      tc::ld32(tmem + lane_base, s);
-      tc::ld32(tmem + lane_base + 32, s + 32);
+#pragma unroll
+      for (int q = 0; q < kBN / 32; ++q) tc::ld32(tmem + lane_base + q * 32, s + q * 32);
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
@@ -617,10 +628,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           tc::st32(tmem + lane_base + kColO + q * 32, o);
         }
       }
-      tc::st16(tmem + lane_base + kColP, hi);
-      tc::st16(tmem + lane_base + kColP + 16, hi + 16);
-      tc::st16(tmem + lane_base + kColP + kBN / 2, lw);
-      tc::st16(tmem + lane_base + kColP + kBN / 2 + 16, lw + 16);
+#pragma unroll
+      for (int q = 0; q < kBN / 32; ++q) {
+        tc::st16(tmem + lane_base + kColP + q * 16, hi + q * 16);
+        tc::st16(tmem + lane_base + kColP + kBN / 2 + q * 16, lw + q * 16);
+      }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
