@@ -283,72 +283,64 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
 
 // ------------------------------------------------------- tcgen05 prefill --
 //
-// One CTA per (query tile, KV head, row): the tile packs tokens_per_tile =
-// 128/group consecutive tokens of one row with all `group` query heads that
-// share the KV head, as the 128 M rows (row r = token r/group, head r%group),
-// so one K/V tile feeds all of them.  The CTA folds the key range its live
-// tokens can see ([min lo, max p]) in tiles of kBN = 64 keys.  Two CTAs fit
-// on an SM (96 KiB of shared memory and 256 TMEM columns each), so one CTA's
-// softmax overlaps the other's MMAs.
-//   warp 0      TMA producer: the Q tile once (a 3-D map (d, H_q, token),
-//               box 64 x group x tokens), then K and V tiles into rings of
-//               kKS / kVS stages, boxes of 8 or 16 rows of the pool map (one
-//               page run each); boxes past the sequence or on bad pages load
+// One CTA per (pair of query tiles, KV head, row).  A query tile packs
+// tokens_per_tile = 128/group consecutive tokens of one row with all `group`
+// query heads that share the KV head, as the 128 M rows (row r = token
+// r/group, head r%group); the CTA holds two consecutive tiles (Q0, Q1), so
+// every K/V tile it streams feeds 256 rows.  Keys are folded in tiles of 128
+// over the range the CTA's live tokens can see ([min lo, max p]); every MMA
+// has N = 128 (keys for S, head dimension for P.V), the width at which the
+// 5th-generation tensor core runs near its peak.
+//   warp 0      TMA producer: Q0 and Q1 once (a 3-D map (d, H_q, token), box
+//               64 x group x tokens), then K and V tiles into rings of kKS /
+//               kVS stages, boxes of 8 or 16 rows of the pool map (one page
+//               run each); boxes past the sequence or on bad pages load
 //               zeros; the last V tile's rows past the CTA's last position
 //               are zeroed.
-//   warp 1      TMEM owner (256 columns: S [0,64), P [64,128), O [128,256))
-//               and MMA issuer (one lane): S_{j+1} = Q K_{j+1}^T (M=128,
-//               N=64, K=128: 8 MMAs from shared-memory descriptors) as soon
-//               as the softmax has read S_j, then O += P_j V_j with P_j read
-//               from TMEM (hi and lo bf16 parts: 8 MMAs of K=16).
-//   warps 2-5   softmax, one thread per M row: load S_j from TMEM and free
-//               it, mask by the row's causal / window range (skipped when the
-//               whole warp sees only live keys), running max in log2 units
-//               with a lazy rescale (O and the sum change only when the max
-//               grows by more than 2^8), then, once P_{j-1}.V_{j-1} is done,
-//               write P_j = hi + lo bf16, then the epilogue O / l.
-// The tensor core computes S_{j+1} while the softmax works on S_j, and
-// P_j.V_j while the softmax works on S_{j+1}.  All waits are bounded.
-#ifndef TL_PREFILL_BN
-#define TL_PREFILL_BN 64
-#endif
-#ifndef TL_PREFILL_KS
-#define TL_PREFILL_KS 2
-#endif
-#ifndef TL_PREFILL_VS
-#define TL_PREFILL_VS 2
-#endif
-constexpr int kBN = TL_PREFILL_BN;   // keys per tile (64: two CTAs per SM; 128: one)
-constexpr int kTcKS = TL_PREFILL_KS; // K stages
-constexpr int kTcVS = TL_PREFILL_VS; // V stages
-constexpr int kTcCtasPerSm = kBN == 64 ? 2 : 1;
-constexpr int kTcThreads = 6 * 32;
-constexpr int kTcQBytes = 32768;     // 128 rows x 128 d x bf16
-constexpr int kTcKVBytes = kBN * 256;  // kBN keys x 128 d x bf16 (two halves)
-constexpr int kTcSmem = kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
-// TMEM: S [0,kBN), P [kBN,2kBN) (hi then lo bf16 halves), O [2kBN, 2kBN+128)
-constexpr uint32_t kColP = kBN;
-constexpr uint32_t kColO = 2 * kBN;
-constexpr uint32_t kTcCols = kBN == 64 ? 256 : 512;
+//   warp 1      TMEM owner (512 columns: S0/P0 [0,128), S1/P1 [128,256),
+//               O0 [256,384), O1 [384,512)) and MMA issuer (one lane), in the
+//               order PV0_j, S0_{j+1}, PV1_j, S1_{j+1}: S_a = Q_a K^T (8 MMAs,
+//               K = 128 from shared-memory descriptors), O_a += P_a V (16
+//               MMAs: hi and lo bf16 parts of P, A read from TMEM).
+//   warps 2-5   softmax for Q0, warps 6-9 for Q1, one thread per M row: load
+//               S_a in 32-column chunks (max pass), mask by the row's causal
+//               / window range (skipped when the whole warp sees only live
+//               keys), running max in log2 units with a lazy rescale (O and
+//               the sum change only when the max grows by more than 2^8),
+//               then a second pass writes P = hi + lo bf16 over each chunk's
+//               own columns; finally the epilogue O / l.
+// While one warpgroup computes softmax on its tile, the tensor core works on
+// the other tile, so the two overlap.  P_a aliases S_a: S_a(j+1) is issued
+// after PV_a(j) and the tensor core runs a thread's MMAs in order, and when
+// S_a(j+1) is complete so is PV_a(j) (its O is stable for a rescale).  All
+// waits are bounded.
+constexpr int kBN = 128;             // keys per tile
+constexpr int kTcKS = 2;             // K stages
+constexpr int kTcVS = 2;             // V stages
+constexpr int kTcThreads = 10 * 32;
+constexpr int kTcQBytes = 32768;     // one query tile: 128 rows x 128 d x bf16
+constexpr int kTcKVBytes = kBN * 256;  // 128 keys x 128 d x bf16 (two 16 KiB halves)
+constexpr int kTcSmem = 2 * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
+constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
 struct TcShared {
   unsigned long long q_full, k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS], v_fix;
-  unsigned long long s_full, s_free, p_full, pv_done, mma_drain;
+  unsigned long long s_full[2], p_full[2], o_done[2], mma_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct TcRange {
-  int kmin, kmax;  // key range of the tile's live tokens (kmax < 0: none)
+  int kmin, kmax;  // key range of the CTA's live tokens (kmax < 0: none)
 };
 
-// Every warp computes the tile's key range itself (no shared state needed).
-__device__ __forceinline__ TcRange tc_tile_range(const PrefillParams& P, int b, int t0, int tpt,
+// Every warp computes the CTA's key range itself (no shared state needed).
+__device__ __forceinline__ TcRange tc_tile_range(const PrefillParams& P, int b, int t0, int ntok,
                                                  int64_t cap) {
   int kmin = INT32_MAX, kmax = -1;
   const int lane = threadIdx.x & 31;
-  for (int i = lane; i < tpt; i += 32) {
+  for (int i = lane; i < ntok; i += 32) {
     const int t = t0 + i;
     if (t >= P.T) break;
     int p = P.positions[(size_t)b * P.T + t];
@@ -367,7 +359,7 @@ __device__ __forceinline__ TcRange tc_tile_range(const PrefillParams& P, int b, 
   return {kmin, kmax};
 }
 
-__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
+__global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, int box_rows) {
@@ -375,25 +367,26 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   __shared__ TcShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase, sK = sbase + kTcQBytes, sV = sK + kTcKS * kTcKVBytes;
+  const uint32_t sQ = sbase, sK = sbase + 2 * kTcQBytes, sV = sK + kTcKS * kTcKVBytes;
   volatile int* abort_flag = &sh.abort_flag;
 
-  const int tpt = 128 / P.group;                 // tokens per tile
+  const int tpt = 128 / P.group;                 // tokens per query tile
   const int rows_used = tpt * P.group;
-  const int n_qt = (P.T + tpt - 1) / tpt;
-  const int qt = n_qt - 1 - (int)blockIdx.x;     // latest (heaviest) tiles first
+  const int n_pairs = (P.T + 2 * tpt - 1) / (2 * tpt);
+  const int qp = n_pairs - 1 - (int)blockIdx.x;  // latest (heaviest) pairs first
   const int g = blockIdx.y, b = blockIdx.z;
-  const int t0 = qt * tpt;
+  const int t0 = qp * 2 * tpt;
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
-  const TcRange rg = tc_tile_range(P, b, t0, tpt, cap);
+  const TcRange rg = tc_tile_range(P, b, t0, 2 * tpt, cap);
 
   if (rg.kmax < 0) {  // no live token: the outputs are 0
-    for (int idx = threadIdx.x; idx < rows_used * 32; idx += kTcThreads) {
+    for (int idx = threadIdx.x; idx < 2 * rows_used * 32; idx += kTcThreads) {
       const int r = idx >> 5, c = (idx & 31) * 4;
-      const int t = t0 + r / P.group;
+      const int a = r / rows_used, rr = r % rows_used;
+      const int t = t0 + a * tpt + rr / P.group;
       if (t < P.T)
         *reinterpret_cast<float4*>(
-            P.out + (((size_t)b * P.T + t) * P.h_q + (size_t)g * P.group + r % P.group) * 128 + c) =
+            P.out + (((size_t)b * P.T + t) * P.h_q + (size_t)g * P.group + rr % P.group) * 128 + c) =
             make_float4(0.f, 0.f, 0.f, 0.f);
     }
     return;
@@ -411,10 +404,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       mbar_init(smem_u32(&sh.v_empty[i]), 1);
     }
     mbar_init(smem_u32(&sh.v_fix), 1);
-    mbar_init(smem_u32(&sh.s_full), 1);
-    mbar_init(smem_u32(&sh.s_free), 4);
-    mbar_init(smem_u32(&sh.p_full), 4);
-    mbar_init(smem_u32(&sh.pv_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh.s_full[i]), 1);
+      mbar_init(smem_u32(&sh.p_full[i]), 4);
+      mbar_init(smem_u32(&sh.o_done[i]), 1);
+    }
     mbar_init(smem_u32(&sh.mma_drain), 1);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -427,18 +421,19 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 
   if (warp == 0) {
     // -------------------------------------------------------------- TMA
-    const int nbox = kBN / box_rows;  // boxes per row half of a tile
+    const int nbox = kBN / box_rows;  // boxes per row half of a tile (8 or 16)
     const int n_slots = P.num_pages * P.page_size;
     const int32_t* bt_row = P.block_table + (size_t)b * P.max_pages_per_seq;
     const int last_blk = rg.kmax / P.page_size;
     int win_blk0 = -1, win = -1;
     uint32_t k_issued = 0, v_issued = 0;
     if (lane == 0) {
-      const uint32_t qbytes = (uint32_t)(64 * rows_used * 2);
-      mbar_arrive_expect_tx(smem_u32(&sh.q_full), 2 * qbytes);
-      for (int h = 0; h < 2; ++h)
-        tma_load_3d(sQ + h * (kTcQBytes / 2), &qmap, h * 64, g * P.group, b * P.T + t0,
-                    smem_u32(&sh.q_full));
+      const uint32_t qbytes = (uint32_t)(64 * rows_used * 2);  // one half of one tile
+      mbar_arrive_expect_tx(smem_u32(&sh.q_full), 4 * qbytes);
+      for (int a = 0; a < 2; ++a)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sQ + a * kTcQBytes + h * (kTcQBytes / 2), &qmap, h * 64, g * P.group,
+                      b * P.T + t0 + a * tpt, smem_u32(&sh.q_full));
     }
     for (int j = 0; j < n_tiles; ++j) {
       const int key0 = (tile0 + j) * kBN;
@@ -449,7 +444,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         const int blk = win_blk0 + lane;
         win = blk <= last_blk ? __ldg(bt_row + blk) : -1;
       }
-      // this lane's box (lanes < 2*nbox): half = lane / nbox, box = lane % nbox
+      // this lane's boxes: lanes < 2*nbox (two row halves); box bi of half
       const int half = lane / nbox, bi = lane % nbox;
       const int kb = key0 + bi * box_rows;
       const int blk = kb / P.page_size;
@@ -506,47 +501,61 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     if (lane == 0) {
       const uint32_t idS = tc::idesc_bf16(128, kBN, 0, 0);
       const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
-      bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort_flag);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kTcKS;
-        if (!mbar_wait(smem_u32(&sh.k_full[st]), (j / kTcKS) & 1, abort_flag)) return false;
-        tc::fence_after();
-        const uint32_t kt = sK + st * kTcKVBytes;
+      auto issue_s = [&](int a, int j) {  // S_a(j) into TMEM columns [128a, 128a+128)
+        const uint32_t kt = sK + (j % kTcKS) * kTcKVBytes;
+        const uint32_t qt = sQ + a * kTcQBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t qo = (k >> 2) * (kTcQBytes / 2) + (k & 3) * 32;
           const uint32_t ko = (k >> 2) * (kTcKVBytes / 2) + (k & 3) * 32;
-          tc::mma_ss(tmem, tc::sdesc(sQ + qo, 16, 1024), tc::sdesc(kt + ko, 16, 1024), idS,
-                     k > 0);
+          tc::mma_ss(tmem + a * 128, tc::sdesc(qt + qo, 16, 1024), tc::sdesc(kt + ko, 16, 1024),
+                     idS, k > 0);
         }
-        tc::commit(smem_u32(&sh.k_empty[st]));
-        tc::commit(smem_u32(&sh.s_full));
-        return true;
+        tc::commit(smem_u32(&sh.s_full[a]));
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles) {  // S_{j+1} once the softmax has read S_j
-          if (!mbar_wait(smem_u32(&sh.s_free), j & 1, abort_flag)) break;
-          if (!issue_s(j + 1)) break;
-        }
-        if (!mbar_wait(smem_u32(&sh.p_full), j & 1, abort_flag)) break;
-        const int vst = j % kTcVS;
-        const bool last = j == n_tiles - 1;
-        if (!mbar_wait(last ? smem_u32(&sh.v_fix) : smem_u32(&sh.v_full[vst]),
-                       last ? 0 : (j / kTcVS) & 1, abort_flag))
-          break;
-        tc::fence_after();
-        const uint32_t vt = sV + vst * kTcKVBytes;
+      auto issue_pv = [&](int a, int j) {  // O_a += P_a(j) V(j)
+        const uint32_t vt = sV + (j % kTcVS) * kTcKVBytes;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            tc::mma_ts(tmem + kColO, tmem + kColP + part * (kBN / 2) + k * 8,
+          for (int k = 0; k < kBN / 16; ++k)  // P chunk c = k/2 holds hi at +0, lo at +16
+            tc::mma_ts(tmem + 256 + a * 128,
+                       tmem + a * 128 + 32 * (k >> 1) + 8 * (k & 1) + 16 * part,
                        tc::sdesc(vt + k * 2048, kTcKVBytes / 2, 1024), idPV,
                        (j > 0 || part > 0 || k > 0) ? 1u : 0u);
         }
-        tc::commit(smem_u32(&sh.v_empty[vst]));
-        tc::commit(smem_u32(&sh.pv_done));
+      };
+      bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort_flag) &&
+                mbar_wait(smem_u32(&sh.k_full[0]), 0, abort_flag);
+      if (ok) {
+        tc::fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc::commit(smem_u32(&sh.k_empty[0]));
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const bool last = j == n_tiles - 1;
+        if (!last && !mbar_wait(smem_u32(&sh.k_full[(j + 1) % kTcKS]), ((j + 1) / kTcKS) & 1,
+                                abort_flag))
+          break;
+        if (!mbar_wait(last ? smem_u32(&sh.v_fix) : smem_u32(&sh.v_full[j % kTcVS]),
+                       last ? 0 : (j / kTcVS) & 1, abort_flag))
+          break;
+        if (!mbar_wait(smem_u32(&sh.p_full[0]), j & 1, abort_flag)) break;
+        tc::fence_after();
+        issue_pv(0, j);
+        if (last) tc::commit(smem_u32(&sh.o_done[0]));
+        else issue_s(0, j + 1);
+        if (!mbar_wait(smem_u32(&sh.p_full[1]), j & 1, abort_flag)) break;
+        tc::fence_after();
+        issue_pv(1, j);
+        tc::commit(smem_u32(&sh.v_empty[j % kTcVS]));
+        if (last) {
+          tc::commit(smem_u32(&sh.o_done[1]));
+        } else {
+          issue_s(1, j + 1);
+          tc::commit(smem_u32(&sh.k_empty[(j + 1) % kTcKS]));
+        }
       }
       // every MMA this thread issued is done before TMEM is released
       tc::commit(smem_u32(&sh.mma_drain));
@@ -555,9 +564,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- softmax
+    const int a = (warp - 2) >> 2;  // query tile of this warpgroup
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const int t = t0 + row / P.group, h = g * P.group + row % P.group;
+    const uint32_t colS = a * 128, colO = 256 + a * 128;
+    const int t = t0 + a * tpt + row / P.group, h = g * P.group + row % P.group;
     int p = -1;
     if (row < rows_used && t < P.T) {
       p = P.positions[(size_t)b * P.T + t];
@@ -568,30 +579,30 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     }
     const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
     const float sc = P.scale_log2;
-    float m_used = -INFINITY, l = 0.f;  // running max of the raw scores (x sc = log2 units)
+    float m_used = -INFINITY, l = 0.f;  // running max of the scores in log2 units
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!mbar_wait(smem_u32(&sh.s_full), j & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(smem_u32(&sh.s_full[a]), j & 1, abort_flag)) { ok = false; break; }
       tc::fence_after();
-      float s[kBN];
-#pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) tc::ld32(tmem + lane_base + q * 32, s + q * 32);
-      tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free));  // S_{j+1} may overwrite it
       const int key0 = (tile0 + j) * kBN;
       const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
-      if (!__all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1)) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          s[c] = (c >= cmin && c <= cmax) ? s[c] : -INFINITY;
-      }
+      const bool all_live = __all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1);
+      // pass 1: the tile's row maximum
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      for (int q = 0; q < kBN / 32; ++q) {
+        float s[32];
+        tc::ld32(tmem + lane_base + colS + q * 32, s);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = q * 32 + i;
+          const float v = (all_live || (c >= cmin && c <= cmax)) ? s[i] : -INFINITY;
+          mx[i & 7] = fmaxf(mx[i & 7], v);
+        }
+      }
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
       const bool need = l > 0.f && mt > m_used + kRescaleLog2;
@@ -600,53 +611,56 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         corr = fast_exp2(m_used - mt);
         m_used = mt;
       }
-      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-      uint32_t hi[kBN / 2], lw[kBN / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < kBN / 2; ++i) {
-        const float a = fast_exp2(fmaf(s[2 * i], sc, -base));
-        const float bb = fast_exp2(fmaf(s[2 * i + 1], sc, -base));
-        ls[i & 3] += a + bb;
-        split_bf16x2(a, bb, hi[i], lw[i]);
-      }
-      l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      // P_{j-1}.V_{j-1} must be done: P's columns are reused and O is stable
-      if (j > 0) {
-        if (!mbar_wait(smem_u32(&sh.pv_done), (j - 1) & 1, abort_flag)) { ok = false; break; }
-        tc::fence_after();
-      }
       if (__any_sync(0xffffffffu, need)) {
+        // PV_a(j-1) is complete (S_a(j) was issued after it): rescale O_a
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float o[32];
-          tc::ld32(tmem + lane_base + kColO + q * 32, o);
+          tc::ld32(tmem + lane_base + colO + q * 32, o);
           tc::wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tc::st32(tmem + lane_base + kColO + q * 32, o);
+          tc::st32(tmem + lane_base + colO + q * 32, o);
         }
       }
+      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+      // pass 2: P = exp2(s*sc - base) as hi + lo bf16 over each chunk's columns
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q = 0; q < kBN / 32; ++q) {
-        tc::st16(tmem + lane_base + kColP + q * 16, hi + q * 16);
-        tc::st16(tmem + lane_base + kColP + kBN / 2 + q * 16, lw + q * 16);
+        float s[32];
+        tc::ld32(tmem + lane_base + colS + q * 32, s);
+        tc::wait_ld();
+        uint32_t pk[32];  // [0,16) hi, [16,32) lo
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = q * 32 + 2 * i;
+          const bool l0 = all_live || (c >= cmin && c <= cmax);
+          const bool l1 = all_live || (c + 1 >= cmin && c + 1 <= cmax);
+          const float x0 = l0 ? fast_exp2(fmaf(s[2 * i], sc, -base)) : 0.f;
+          const float x1 = l1 ? fast_exp2(fmaf(s[2 * i + 1], sc, -base)) : 0.f;
+          ls[i & 3] += x0 + x1;
+          split_bf16x2(x0, x1, pk[i], pk[16 + i]);
+        }
+        tc::st16(tmem + lane_base + colS + q * 32, pk);
+        tc::st16(tmem + lane_base + colS + q * 32 + 16, pk + 16);
       }
+      l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[a]));
     }
     // epilogue: O / l
-    if (ok && mbar_wait(smem_u32(&sh.pv_done), (n_tiles - 1) & 1, abort_flag)) {
+    if (ok && mbar_wait(smem_u32(&sh.o_done[a]), 0, abort_flag)) {
       tc::fence_after();
       const float inv = (p >= 0 && l > 0.f) ? 1.f / l : 0.f;
       float* dst = P.out + (((size_t)b * P.T + t) * P.h_q + h) * 128;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float o[32];
-        tc::ld32(tmem + lane_base + kColO + q * 32, o);
+        tc::ld32(tmem + lane_base + colO + q * 32, o);
         tc::wait_ld();
         if (row < rows_used && t < P.T) {
 #pragma unroll
@@ -740,8 +754,8 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kTcSmem) != cudaSuccess)
     return TL_ERR_CUDA;
-  const int n_qt = (T + tpt - 1) / tpt;
-  prefill_tc_kernel<<<dim3(n_qt, h_kv, B), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
+  const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
+  prefill_tc_kernel<<<dim3(n_pairs, h_kv, B), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
       P, qmap, kmap, vmap, box_rows);
   return launch_status();
 }
