@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
 // S_a(j+1) is complete so is PV_a(j) (its O is stable for a rescale).  All
 // waits are bounded.
 constexpr int kBN = 128;             // keys per tile
-constexpr int kTcKS = 2;             // K stages
+constexpr int kTcKS = 3;             // K stages
 constexpr int kTcVS = 2;             // V stages
 constexpr int kTcThreads = 10 * 32;
 constexpr int kTcQBytes = 32768;     // one query tile: 128 rows x 128 d x bf16
@@ -535,17 +535,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const bool last = j == n_tiles - 1;
-        if (!last && !mbar_wait(smem_u32(&sh.k_full[(j + 1) % kTcKS]), ((j + 1) / kTcKS) & 1,
-                                abort_flag))
-          break;
         if (!mbar_wait(last ? smem_u32(&sh.v_fix) : smem_u32(&sh.v_full[j % kTcVS]),
                        last ? 0 : (j / kTcVS) & 1, abort_flag))
           break;
         if (!mbar_wait(smem_u32(&sh.p_full[0]), j & 1, abort_flag)) break;
         tc::fence_after();
         issue_pv(0, j);
-        if (last) tc::commit(smem_u32(&sh.o_done[0]));
-        else issue_s(0, j + 1);
+        if (last) {
+          tc::commit(smem_u32(&sh.o_done[0]));
+        } else {
+          if (!mbar_wait(smem_u32(&sh.k_full[(j + 1) % kTcKS]), ((j + 1) / kTcKS) & 1,
+                         abort_flag))
+            break;
+          tc::fence_after();
+          issue_s(0, j + 1);
+        }
         if (!mbar_wait(smem_u32(&sh.p_full[1]), j & 1, abort_flag)) break;
         tc::fence_after();
         issue_pv(1, j);
