@@ -303,12 +303,12 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParam
 //               K = 128 from shared-memory descriptors), O_a += P_a V (16
 //               MMAs: hi and lo bf16 parts of P, A read from TMEM).
 //   warps 2-5   softmax for Q0, warps 6-9 for Q1, one thread per M row: load
-//               S_a in 32-column chunks (max pass), mask by the row's causal
-//               / window range (skipped when the whole warp sees only live
-//               keys), running max in log2 units with a lazy rescale (O and
-//               the sum change only when the max grows by more than 2^8),
-//               then a second pass writes P = hi + lo bf16 over each chunk's
-//               own columns; finally the epilogue O / l.
+//               the row of S_a (four 32-column loads, one wait), mask by the
+//               row's causal / window range (skipped when the whole warp sees
+//               only live keys), running max in log2 units with a lazy
+//               rescale (O and the sum change only when the max grows by
+//               more than 2^8), write P = hi + lo bf16 over each 32-column
+//               chunk's own columns; finally the epilogue O / l.
 // While one warpgroup computes softmax on its tile, the tensor core works on
 // the other tile, so the two overlap.  P_a aliases S_a: S_a(j+1) is issued
 // after PV_a(j) and the tensor core runs a thread's MMAs in order, and when
@@ -591,22 +591,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int key0 = (tile0 + j) * kBN;
       const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
       const bool all_live = __all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1);
-      // pass 1: the tile's row maximum
+      // the tile's 128 scores of this row: four loads, one wait
+      float s[kBN];
+#pragma unroll
+      for (int q = 0; q < kBN / 32; ++q) tc::ld32(tmem + lane_base + colS + q * 32, s + q * 32);
+      tc::wait_ld();
+      if (!all_live) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) s[c] = (c >= cmin && c <= cmax) ? s[c] : -INFINITY;
+      }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) {
-        float s[32];
-        tc::ld32(tmem + lane_base + colS + q * 32, s);
-        tc::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = q * 32 + i;
-          const float v = (all_live || (c >= cmin && c <= cmax)) ? s[i] : -INFINITY;
-          mx[i & 7] = fmaxf(mx[i & 7], v);
-        }
-      }
+      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
       const bool need = l > 0.f && mt > m_used + kRescaleLog2;
@@ -615,8 +613,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         corr = fast_exp2(m_used - mt);
         m_used = mt;
       }
+      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+      // P = exp2(s*sc - base) as hi + lo bf16 over each 32-column chunk's own columns
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < kBN / 32; ++q) {
+        uint32_t pk[32];  // [0,16) hi, [16,32) lo
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = fast_exp2(fmaf(s[q * 32 + 2 * i], sc, -base));
+          const float x1 = fast_exp2(fmaf(s[q * 32 + 2 * i + 1], sc, -base));
+          ls[i & 3] += x0 + x1;
+          split_bf16x2(x0, x1, pk[i], pk[16 + i]);
+        }
+        tc::st16(tmem + lane_base + colS + q * 32, pk);
+        tc::st16(tmem + lane_base + colS + q * 32 + 16, pk + 16);
+      }
+      l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       if (__any_sync(0xffffffffu, need)) {
-        // PV_a(j-1) is complete (S_a(j) was issued after it): rescale O_a
+        // PV_a(j-1) is complete (S_a(j) was issued after it) and PV_a(j)
+        // waits for this tile's P: rescale O_a now
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float o[32];
@@ -627,30 +644,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::st32(tmem + lane_base + colO + q * 32, o);
         }
       }
-      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-      // pass 2: P = exp2(s*sc - base) as hi + lo bf16 over each chunk's columns
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) {
-        float s[32];
-        tc::ld32(tmem + lane_base + colS + q * 32, s);
-        tc::wait_ld();
-        uint32_t pk[32];  // [0,16) hi, [16,32) lo
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = q * 32 + 2 * i;
-          const bool l0 = all_live || (c >= cmin && c <= cmax);
-          const bool l1 = all_live || (c + 1 >= cmin && c + 1 <= cmax);
-          const float x0 = l0 ? fast_exp2(fmaf(s[2 * i], sc, -base)) : 0.f;
-          const float x1 = l1 ? fast_exp2(fmaf(s[2 * i + 1], sc, -base)) : 0.f;
-          ls[i & 3] += x0 + x1;
-          split_bf16x2(x0, x1, pk[i], pk[16 + i]);
-        }
-        tc::st16(tmem + lane_base + colS + q * 32, pk);
-        tc::st16(tmem + lane_base + colS + q * 32 + 16, pk + 16);
-      }
-      l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
