@@ -373,8 +373,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tpt = 128 / P.group;                 // tokens per query tile
   const int rows_used = tpt * P.group;
   const int n_pairs = (P.T + 2 * tpt - 1) / (2 * tpt);
-  const int qp = n_pairs - 1 - (int)blockIdx.x;  // latest (heaviest) pairs first
-  const int g = blockIdx.y, b = blockIdx.z;
+  // grid (row x KV head, pair): the latest (heaviest) pairs of every row and
+  // head launch first, so the long CTAs do not end up in the tail
+  const int qp = n_pairs - 1 - (int)blockIdx.y;
+  const int g = (int)blockIdx.x % P.h_kv, b = (int)blockIdx.x / P.h_kv;
   const int t0 = qp * 2 * tpt;
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
   const TcRange rg = tc_tile_range(P, b, t0, 2 * tpt, cap);
@@ -752,7 +754,8 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
                            kTcSmem) != cudaSuccess)
     return TL_ERR_CUDA;
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
-  prefill_tc_kernel<<<dim3(n_pairs, h_kv, B), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
+  if ((int64_t)B * h_kv > 0x7fffffff || n_pairs > 65535) return TL_ERR_UNSUPPORTED;
+  prefill_tc_kernel<<<dim3(B * h_kv, n_pairs), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
       P, qmap, kmap, vmap, box_rows);
   return launch_status();
 }
