@@ -252,7 +252,7 @@ def run_ours(args):
     achieved = dec_alg / (dec_ms * 1e-3) / 1e9
     prefill_line, write_line = None, None
     if args.only in ("all", "prefill"):
-        prefill_line, write_line = run_prefill(args, rank, dev, stream, hbm, bf16, src)
+        prefill_line, write_line = run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src)
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -298,7 +298,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_prefill(args, rank, dev, stream, hbm, bf16, src):
+def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
     """Batched-prefill workload: TFLOP/s of the attention call, and the
     16K-row chunk write's GB/s."""
     import torch
@@ -325,11 +325,17 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, src):
     torch.cuda.synchronize()
     pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.prefill_steps)]
-    for a, b in pev:
-        a.record(stream)
-        pf()
-        b.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as pclk:
+        t_end = time.time() + args.soak_seconds
+        while time.time() < t_end:  # the same load around the timed calls, for the sampler
+            for _ in range(10):
+                pf()
+            torch.cuda.synchronize()
+        for a, b in pev:
+            a.record(stream)
+            pf()
+            b.record(stream)
+        torch.cuda.synchronize()
     pf_ms = statistics.mean(a.elapsed_time(b) for a, b in pev)
     # chunk write on its own (16K rows), for the write kernel's GB/s
     wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -349,7 +355,9 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, src):
         "tflops": round(pf_tflops, 2), "ms_per_call": round(pf_ms, 4), "flops_per_call": flops,
         "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2), "peak": bf16,
                      "unit": "TFLOP/s", "frac": round(pf_tflops / bf16, 4), "traffic": None,
-                     "peak_source": f"{src} bf16_tflops (burst)"}}
+                     "peak_source": f"{src} bf16_tflops (burst)",
+                     "frac_of_sustained": round(pf_tflops / bf16_sus, 4)},
+        "clocks": pclk.summary()}
     write_line = {"rows": n_live, "ms": round(w_ms, 5),
                   "gbs": round(w_bytes / (w_ms * 1e-3) / 1e9, 1),
                   "frac": round(w_bytes / (w_ms * 1e-3) / 1e9 / hbm, 4)}
