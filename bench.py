@@ -311,7 +311,8 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
     flops = prefill_flops(pcase.positions, pcase.Hq, pcase.d)
     pout = torch.empty((pcase.B, pcase.T, pcase.Hq, pcase.d), dtype=torch.float32, device=dev)
     pws = tl.alloc_workspace(tl.tl_paged_attn_prefill_workspace_size(
-        pcase.B, pcase.T, pcase.Hq, pcase.Hkv, pcase.d), dev)
+        pcase.B, pcase.T, pcase.Hq, pcase.Hkv, pcase.d, pcase.block_table.shape[1],
+        pcase.page_size), dev)
     kn = pg.k_new.view(-1, pcase.Hkv, pcase.d)
     vn = pg.v_new.view(-1, pcase.Hkv, pcase.d)
     tl.tl_kv_cache_write(kn, vn, pg.k_cache, pg.v_cache, pg.slot_mapping)

@@ -76,6 +76,7 @@ typedef enum {
 #define TL_DEVERR_PAGE_RANGE 2u    /* a needed block-table entry outside [0, num_pages) */
 #define TL_DEVERR_CONTEXT_RANGE 4u /* a length / position past max_pages_per_seq*page_size */
 #define TL_DEVERR_TIMEOUT 8u       /* an internal pipeline wait gave up (outputs invalid) */
+#define TL_DEVERR_VALUE_RANGE 16u  /* prefill: a finite V entry beyond +-65504 (outputs invalid) */
 
 /* Name of a status, for messages (never NULL). */
 const char* tl_status_string(tl_status status);
@@ -170,27 +171,45 @@ tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const
                                        tl_dtype dtype, uint32_t* error_word, void* stream);
 
 /*
- * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes).
+ * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes): an
+ * fp16 copy of the V rows the call reads, [B][h_kv][max_pages_per_seq *
+ * page_size][d], i.e. B * h_kv * max_pages_per_seq * page_size * d * 2.  It
+ * does not depend on T or h_q (they are taken for the shape checks only).
  */
 size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
-                                            int32_t d);
+                                            int32_t d, int32_t max_pages_per_seq,
+                                            int32_t page_size);
 
 /*
  * PAGED_ATTENTION, batched prefill ("How serving works in Tlaloc", sections
  * 1-2, "Blockwise attention"): B rows of T tokens.  Token (b,t) with position
  * p = positions[b][t] >= 0 attends exactly like a decode query of causal
  * length p+1 (and the same window rule) over its own row's pages; p < 0 marks
- * padding, whose output is 0.  The keys are folded in blocks of 2,048
- * positions with an online softmax; no score tensor wider than one tile
+ * padding, whose output is 0.  The keys are folded tile by tile (128 keys,
+ * a finer fold than the pages' 2,048-key blocks; the result is the same up to
+ * rounding) with an online softmax; no score tensor wider than one tile
  * exists.  A row's result does not depend on the other rows (batched equals
  * solo, bit for bit).
  *   q            [B][T][h_q][d] bf16
  *   positions    [B][T] int32, -1 = padding
  *   out          [B][T][h_q][d] float32
+ *   workspace    device scratch of at least tl_paged_attn_prefill_workspace_size(
+ *                B, T, h_q, h_kv, d, max_pages_per_seq, page_size) bytes,
+ *                16-byte aligned (TL_ERR_WORKSPACE otherwise); it receives the
+ *                call's fp16 copy of V, so calls that may overlap on the GPU
+ *                must not share one.
  *   other arguments as for decode.
  * Supported: dtype TL_BF16, d = 128, h_q % h_kv == 0 with h_q/h_kv <= 128,
  * page_size a power of two in [8, 128].  Otherwise TL_ERR_UNSUPPORTED.
  * scale must be positive and finite (TL_ERR_INVALID_ARG otherwise).
+ * Arithmetic: Q.K^T with bf16 operands and f32 accumulation; P.V with P
+ * rounded to fp16 and V converted bf16 -> fp16 (exact for |v| in
+ * [2^-14, 65504]; smaller magnitudes land on fp16's subnormal grid, a change
+ * below 2^-25), f32 accumulation, and the softmax sum taken over the same
+ * rounded P, so each output is a convex combination of V rows with weights
+ * within 2^-11 relative of the exact ones.  A finite V entry beyond +-65504
+ * in a key range the call reads sets TL_DEVERR_VALUE_RANGE and leaves the
+ * outputs undefined.
  */
 tl_status tl_paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int32_t max_pages_per_seq,

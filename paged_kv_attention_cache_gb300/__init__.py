@@ -6,7 +6,7 @@ it with the same names.  There is no CPU or framework fallback: calling an op
 without the built library, or without a CUDA device, raises.
 """
 from .api import (TL_BF16, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noqa: F401
-                  TL_DEVERR_SLOT_RANGE, TL_ERR_CUDA, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED,
+                  TL_DEVERR_SLOT_RANGE, TL_DEVERR_TIMEOUT, TL_DEVERR_VALUE_RANGE, TL_ERR_CUDA, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED,
                   TL_ERR_WORKSPACE, TL_F32, TL_OK, TLError, alloc_workspace,
                   TL_DECODE_NOALLOC_SCRATCH_BYTES, tl_kv_cache_write, tl_paged_attn_decode,
                   tl_paged_attn_decode_noalloc, tl_paged_attn_decode_workspace_size,

@@ -16,6 +16,7 @@ from . import _lib
 TL_OK, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED, TL_ERR_CUDA, TL_ERR_WORKSPACE = range(5)
 TL_F32, TL_BF16 = 0, 1
 TL_DEVERR_SLOT_RANGE, TL_DEVERR_PAGE_RANGE, TL_DEVERR_CONTEXT_RANGE = 1, 2, 4
+TL_DEVERR_TIMEOUT, TL_DEVERR_VALUE_RANGE = 8, 16
 
 _DTYPES = {torch.float32: TL_F32, torch.bfloat16: TL_BF16}
 
@@ -80,8 +81,10 @@ def tl_paged_attn_decode_workspace_size(B: int, h_q: int, h_kv: int, d: int) -> 
     return int(_lib.load().tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d))
 
 
-def tl_paged_attn_prefill_workspace_size(B: int, T: int, h_q: int, h_kv: int, d: int) -> int:
-    return int(_lib.load().tl_paged_attn_prefill_workspace_size(B, T, h_q, h_kv, d))
+def tl_paged_attn_prefill_workspace_size(B: int, T: int, h_q: int, h_kv: int, d: int,
+                                         max_pages_per_seq: int, page_size: int) -> int:
+    return int(_lib.load().tl_paged_attn_prefill_workspace_size(B, T, h_q, h_kv, d,
+                                                                 max_pages_per_seq, page_size))
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
@@ -161,8 +164,9 @@ def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         out = torch.empty((B, T, hq, d), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32)
     if workspace is None:
-        workspace = alloc_workspace(tl_paged_attn_prefill_workspace_size(B, T, hq, hkv, d),
-                                    q.device)
+        workspace = alloc_workspace(
+            tl_paged_attn_prefill_workspace_size(B, T, hq, hkv, d, block_table.shape[1], ps),
+            q.device)
     st = _lib.load().tl_paged_attn_prefill(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window), float(scale),

@@ -5,22 +5,55 @@
 // keys are folded block by block into a running max, sum and P.V, so no score
 // tensor wider than one tile exists).
 //
-// Grid: (query tile of 64 tokens, query head, row).  Each CTA reads only the
-// key range its live tokens can see ([min lo, max p]), in tiles of 64 keys
-// gathered from the row's pages with 16-byte cp.async into a 2-stage shared
-// memory ring; Q.K^T and P.V run on mma.sync m16n8k16 (bf16 in, f32
-// accumulate), the online softmax in registers.  A CTA never touches another
-// row, and its arithmetic does not depend on B, so a row gives the same bits
-// batched or alone.
+// Two launches.  A pre-pass converts the V rows each row's tokens can see
+// from the bf16 pages to fp16, once, into the workspace, laid out as
+// [row][KV head][key][d] (exact for every finite V entry within +-65504;
+// larger ones are reported; keys past the row's last position are zeros).
+// Then the attention kernel runs one CTA per (pair of query tiles, KV head,
+// row) on the 5th-generation tensor core.  A query tile packs tokens_per_tile = 128/group consecutive
+// tokens of one row with all `group` query heads that share the KV head, as
+// the 128 M rows (row r = token r/group, head r%group); the CTA holds two
+// consecutive tiles (Q0, Q1), so every K/V tile it streams feeds 256 rows.
+// Keys are folded in tiles of 128 over the range the CTA's live tokens can
+// see ([min lo, max p]); every MMA has N = 128 (keys for S, head dimension for
+// P.V), the width at which the tensor core runs near its peak.
+//   warp 0      TMA producer: Q0 and Q1 once (a 3-D map (d, H_q, token), box
+//               64 x group x tokens), then K and V tiles into rings of kTcKS /
+//               kTcVS stages: K in boxes of 8 or 16 rows of the pool map (one
+//               page run each; boxes past the sequence or on bad pages load
+//               zeros), V as two 64 x 128 boxes of the fp16 workspace.
+//   warp 1      TMEM owner (512 columns: S0/P0 [0,128), S1/P1 [128,256),
+//               O0 [256,384), O1 [384,512)) and MMA issuer (one lane), in the
+//               order PV0_j, S0_{j+1}, PV1_j, S1_{j+1}: S_a = Q_a K^T (8 MMAs,
+//               bf16 operands from shared-memory descriptors), O_a += P_a V
+//               (8 MMAs, fp16, A read from TMEM).
+//   warps 2-5   softmax for Q0, warps 6-9 for Q1, one thread per M row: load
+//               the row of S_a (four 32-column loads, one wait), mask by the
+//               row's causal / window range (skipped when the whole warp sees
+//               only live keys), running max in log2 units with a lazy
+//               rescale (O and the sum change only when the max grows by
+//               more than 2^8), write P rounded to fp16 into the first 64
+//               columns of S_a, and add the rounded values to the row sum;
+//               finally the epilogue O / l.
+// P is rounded to fp16 rather than bf16: bf16's 8-bit significand makes the
+// weights of a peaked softmax off by up to 2^-9, which moves an output by
+// several 1e-3 when |V| is a few units; fp16's 11 bits and a sum over the same
+// rounded weights keep the output a convex combination of V rows with
+// weights within 2^-11 relative.  V is converted once per call rather than
+// per CTA: every V tile feeds all the CTAs of its row and head, and a
+// conversion inside the attention kernel would add two shared-memory passes
+// per tile per CTA next to the tensor core's own operand reads, which
+// already use most of that bandwidth.
+// While one warpgroup computes softmax on its tile, the tensor core works on
+// the other tile, so the two overlap.  P_a aliases S_a: S_a(j+1) is issued
+// after PV_a(j) and the tensor core runs a thread's MMAs in order, and when
+// S_a(j+1) is complete so is PV_a(j) (its O is stable for a rescale).  A CTA
+// never touches another row and its arithmetic does not depend on B, so a row
+// gives the same bits batched or alone.  All waits are bounded.
 #include "common.cuh"
 #include "tcgen05.cuh"
 
 namespace tl {
-
-constexpr int kPfRows = 64;     // query tokens per CTA
-constexpr int kPfKeys = 64;     // keys per tile
-constexpr int kPfWarps = 4;
-constexpr int kPfThreads = kPfWarps * 32;
 
 struct PrefillParams {
   const __nv_bfloat16* q;
@@ -36,296 +69,23 @@ struct PrefillParams {
   uint32_t* error_word;
 };
 
-template <int D>
-struct PfSmem {
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kQBytes = kPfRows * kRowBytes;
-  static constexpr int kTileBytes = kPfKeys * kRowBytes;  // K or V
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kTotal = kQBytes + 2 * kStageBytes;
-};
-
-__device__ __forceinline__ uint32_t swz(int row, int unit, int row_bytes) {
-  return (uint32_t)(row * row_bytes + ((unit ^ (row & 7)) << 4));
-}
-
-// Gather one tile of keys [j0, j0+64) of row b, KV head g: rows past
-// j_last (or on a bad page) are zero-filled.
-template <int D>
-__device__ __forceinline__ void load_kv_tile(const PrefillParams& P, int b, int g, int j0,
-                                             int j_last, uint32_t kdst, uint32_t vdst) {
-  constexpr int U = D / 8;  // 16-byte units per row
-  const int tid = threadIdx.x;
-  for (int r = tid >> 1; r < kPfKeys; r += kPfThreads / 2) {
-    const int j = j0 + r;
-    bool live = j <= j_last;
-    int64_t page = 0;
-    if (live) {
-      page = __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + j / P.page_size);
-      if (page < 0 || page >= P.num_pages) {
-        report(P.error_word, TL_DEVERR_PAGE_RANGE);
-        live = false;
-        page = 0;
-      }
-    }
-    const size_t row =
-        (((size_t)page * P.page_size + (live ? j % P.page_size : 0)) * P.h_kv + g) * D;
-    const __nv_bfloat16* ks = P.k_cache + row;
-    const __nv_bfloat16* vs = P.v_cache + row;
-    const uint32_t n = live ? 16u : 0u;
-#pragma unroll
-    for (int i = 0; i < U / 2; ++i) {
-      const int u = (tid & 1) + 2 * i;
-      cp_async_16(kdst + swz(r, u, D * 2), ks + u * 8, n);
-      cp_async_16(vdst + swz(r, u, D * 2), vs + u * 8, n);
-    }
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kPfThreads, 2) prefill_mma_kernel(PrefillParams P) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int s_range[2];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_qt = (P.T + kPfRows - 1) / kPfRows;
-  const int qt = n_qt - 1 - (int)blockIdx.x;  // heaviest (latest) tiles first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int g = h / P.group;
-  const int t0 = qt * kPfRows;
-  const int32_t* pos_row = P.positions + (size_t)b * P.T;
-  const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
-
-  // key range of the tile's live tokens
-  if (tid == 0) {
-    s_range[0] = INT32_MAX;
-    s_range[1] = -1;
-  }
-  __syncthreads();
-  if (tid < kPfRows && t0 + tid < P.T) {
-    int p = pos_row[t0 + tid];
-    if (p >= cap) {
-      report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
-      p = -1;
-    }
-    if (p >= 0) {
-      const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
-      atomicMin(&s_range[0], lo);
-      atomicMax(&s_range[1], p);
-    }
-  }
-  __syncthreads();
-  const int kmin = s_range[0], kmax = s_range[1];
-
-  const int qr = lane >> 2, qc = (lane & 3) * 2;
-  // this thread's two rows (tokens) and their causal ranges
-  const int tA = t0 + warp * 16 + qr, tB = tA + 8;
-  int pA = tA < P.T ? pos_row[tA] : -1, pB = tB < P.T ? pos_row[tB] : -1;
-  if (pA >= cap) pA = -1;
-  if (pB >= cap) pB = -1;
-  const int loA = (P.window > 0 && pA - P.window + 1 > 0) ? pA - P.window + 1 : 0;
-  const int loB = (P.window > 0 && pB - P.window + 1 > 0) ? pB - P.window + 1 : 0;
-
-  float o[D / 8][4];
-#pragma unroll
-  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-
-  if (kmax >= 0) {
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t qaddr = sbase;
-    const uint32_t stage0 = sbase + PfSmem<D>::kQBytes;
-    // Q tile (rows past T, or padding, load whatever is there: their output is 0)
-    {
-      constexpr int U = D / 8;
-      for (int r = tid >> 1; r < kPfRows; r += kPfThreads / 2) {
-        const int t = min(t0 + r, P.T - 1);
-        const __nv_bfloat16* src = P.q + (((size_t)b * P.T + t) * P.h_q + h) * D;
-#pragma unroll
-        for (int i = 0; i < U / 2; ++i) {
-          const int u = (tid & 1) + 2 * i;
-          cp_async_16(qaddr + swz(r, u, D * 2), src + u * 8, 16u);
-        }
-      }
-    }
-    const int tile_first = kmin / kPfKeys, tile_last = kmax / kPfKeys;
-    load_kv_tile<D>(P, b, g, tile_first * kPfKeys, kmax, stage0,
-                    stage0 + PfSmem<D>::kTileBytes);
-    cp_async_commit();
-
-    uint32_t qa[D / 16][4];
-    for (int kt = tile_first; kt <= tile_last; ++kt) {
-      const int st = (kt - tile_first) & 1;
-      if (kt < tile_last) {
-        const uint32_t nst = stage0 + (st ^ 1) * PfSmem<D>::kStageBytes;
-        load_kv_tile<D>(P, b, g, (kt + 1) * kPfKeys, kmax, nst, nst + PfSmem<D>::kTileBytes);
-      }
-      cp_async_commit();
-      cp_async_wait<1>();
-      __syncthreads();
-      if (kt == tile_first) {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int row = warp * 16 + (mi & 1) * 8 + ri;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          ldmatrix_x4(qaddr + swz(row, 2 * ks + (mi >> 1), D * 2), qa[ks][0], qa[ks][1],
-                      qa[ks][2], qa[ks][3]);
-      }
-      const uint32_t kaddr = stage0 + st * PfSmem<D>::kStageBytes;
-      const uint32_t vaddr = kaddr + PfSmem<D>::kTileBytes;
-      const int j0 = kt * kPfKeys;
-      // S = Q K^T (16 x 64 per warp)
-      float s[kPfKeys / 8][4];
-#pragma unroll
-      for (int n = 0; n < kPfKeys / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-      {
-        const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-        for (int n2 = 0; n2 < kPfKeys / 16; ++n2) {
-          const int key = n2 * 16 + (mi >> 1) * 8 + ri;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(kaddr + swz(key, 2 * ks + (mi & 1), D * 2), b0, b1, b2, b3);
-            mma_bf16_16816(s[2 * n2], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_bf16_16816(s[2 * n2 + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-          }
-        }
-      }
-      // mask, scale, online softmax
-      float mxA = -INFINITY, mxB = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < kPfKeys / 8; ++n) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int j = j0 + n * 8 + qc + e;
-          s[n][e] = (j >= loA && j <= pA) ? s[n][e] * P.scale_log2 : -INFINITY;
-          s[n][2 + e] = (j >= loB && j <= pB) ? s[n][2 + e] * P.scale_log2 : -INFINITY;
-          mxA = fmaxf(mxA, s[n][e]);
-          mxB = fmaxf(mxB, s[n][2 + e]);
-        }
-      }
-      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
-      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
-      mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
-      mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
-      const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
-      const float baseA = nA == -INFINITY ? 0.f : nA;  // a row with no live key yet
-      const float baseB = nB == -INFINITY ? 0.f : nB;
-      const float cA = fast_exp2(mA - baseA), cB = fast_exp2(mB - baseB);
-      mA = nA;
-      mB = nB;
-      float sumA = 0.f, sumB = 0.f;
-#pragma unroll
-      for (int n = 0; n < kPfKeys / 8; ++n) {
-        s[n][0] = fast_exp2(s[n][0] - baseA);
-        s[n][1] = fast_exp2(s[n][1] - baseA);
-        s[n][2] = fast_exp2(s[n][2] - baseB);
-        s[n][3] = fast_exp2(s[n][3] - baseB);
-        sumA += s[n][0] + s[n][1];
-        sumB += s[n][2] + s[n][3];
-      }
-      lA = lA * cA + sumA;
-      lB = lB * cB + sumB;
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= cA;
-        o[n][1] *= cA;
-        o[n][2] *= cB;
-        o[n][3] *= cB;
-      }
-      // O += P V
-      {
-        const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-        for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-          // P = hi + lo (bf16 pair): two MMAs keep f32-level accuracy
-          uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-          split_bf16x2(s[2 * kk][0], s[2 * kk][1], h0, l0);
-          split_bf16x2(s[2 * kk][2], s[2 * kk][3], h1, l1);
-          split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], h2, l2);
-          split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], h3, l3);
-          const int key = kk * 16 + (mi & 1) * 8 + ri;
-#pragma unroll
-          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(vaddr + swz(key, 2 * nd2 + (mi >> 1), D * 2), b0, b1, b2, b3);
-            mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
-            mma_bf16_16816(o[2 * nd2], l0, l1, l2, l3, b0, b1);
-            mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
-            mma_bf16_16816(o[2 * nd2 + 1], l0, l1, l2, l3, b2, b3);
-          }
-        }
-      }
-      __syncthreads();  // the stage is rewritten by the next iteration's loads
-    }
-    cp_async_wait<0>();
-  }
-  lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-  lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-  lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-  lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-  const float invA = (pA >= 0 && lA > 0.f) ? 1.f / lA : 0.f;
-  const float invB = (pB >= 0 && lB > 0.f) ? 1.f / lB : 0.f;
-  if (tA < P.T) {
-    float* dst = P.out + (((size_t)b * P.T + tA) * P.h_q + h) * D;
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n)
-      *reinterpret_cast<float2*>(dst + n * 8 + qc) = make_float2(o[n][0] * invA, o[n][1] * invA);
-  }
-  if (tB < P.T) {
-    float* dst = P.out + (((size_t)b * P.T + tB) * P.h_q + h) * D;
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n)
-      *reinterpret_cast<float2*>(dst + n * 8 + qc) = make_float2(o[n][2] * invB, o[n][3] * invB);
-  }
-}
-
-
-// ------------------------------------------------------- tcgen05 prefill --
-//
-// One CTA per (pair of query tiles, KV head, row).  A query tile packs
-// tokens_per_tile = 128/group consecutive tokens of one row with all `group`
-// query heads that share the KV head, as the 128 M rows (row r = token
-// r/group, head r%group); the CTA holds two consecutive tiles (Q0, Q1), so
-// every K/V tile it streams feeds 256 rows.  Keys are folded in tiles of 128
-// over the range the CTA's live tokens can see ([min lo, max p]); every MMA
-// has N = 128 (keys for S, head dimension for P.V), the width at which the
-// 5th-generation tensor core runs near its peak.
-//   warp 0      TMA producer: Q0 and Q1 once (a 3-D map (d, H_q, token), box
-//               64 x group x tokens), then K and V tiles into rings of kKS /
-//               kVS stages, boxes of 8 or 16 rows of the pool map (one page
-//               run each); boxes past the sequence or on bad pages load
-//               zeros; the last V tile's rows past the CTA's last position
-//               are zeroed.
-//   warp 1      TMEM owner (512 columns: S0/P0 [0,128), S1/P1 [128,256),
-//               O0 [256,384), O1 [384,512)) and MMA issuer (one lane), in the
-//               order PV0_j, S0_{j+1}, PV1_j, S1_{j+1}: S_a = Q_a K^T (8 MMAs,
-//               K = 128 from shared-memory descriptors), O_a += P_a V (16
-//               MMAs: hi and lo bf16 parts of P, A read from TMEM).
-//   warps 2-5   softmax for Q0, warps 6-9 for Q1, one thread per M row: load
-//               the row of S_a (four 32-column loads, one wait), mask by the
-//               row's causal / window range (skipped when the whole warp sees
-//               only live keys), running max in log2 units with a lazy
-//               rescale (O and the sum change only when the max grows by
-//               more than 2^8), write P = hi + lo bf16 over each 32-column
-//               chunk's own columns; finally the epilogue O / l.
-// While one warpgroup computes softmax on its tile, the tensor core works on
-// the other tile, so the two overlap.  P_a aliases S_a: S_a(j+1) is issued
-// after PV_a(j) and the tensor core runs a thread's MMAs in order, and when
-// S_a(j+1) is complete so is PV_a(j) (its O is stable for a rescale).  All
-// waits are bounded.
 constexpr int kBN = 128;             // keys per tile
 constexpr int kTcKS = 3;             // K stages
 constexpr int kTcVS = 2;             // V stages
 constexpr int kTcThreads = 10 * 32;
+constexpr int kCvtThreads = 256;
 constexpr int kTcQBytes = 32768;     // one query tile: 128 rows x 128 d x bf16
-constexpr int kTcKVBytes = kBN * 256;  // 128 keys x 128 d x bf16 (two 16 KiB halves)
+constexpr int kTcKVBytes = kBN * 256;  // 128 keys x 128 d x 16-bit (two 16 KiB halves)
 constexpr int kTcSmem = 2 * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
 constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;
+// bf16 bit patterns (sign cleared) of the finite values fp16 cannot hold:
+// [65536, max finite]; 65280 (0x477F) is the largest bf16 below fp16's
+// overflow threshold.
+constexpr uint32_t kBf16TooBig = 0x4780u, kBf16Inf = 0x7F80u;
 
 struct TcShared {
-  unsigned long long q_full, k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS], v_fix;
+  unsigned long long q_full, k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS];
   unsigned long long s_full[2], p_full[2], o_done[2], mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -357,6 +117,103 @@ __device__ __forceinline__ TcRange tc_tile_range(const PrefillParams& P, int b, 
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
   return {kmin, kmax};
+}
+
+// Two f32 -> one f16x2 register (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The two halves of an f16x2 register as f32 (exact).
+__device__ __forceinline__ void unpack_f16x2(uint32_t x, float& lo, float& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+      : "=f"(lo), "=f"(hi)
+      : "r"(x));
+}
+// Two bf16 (one register) -> two fp16 (one register).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+  return pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// ------------------------------------------------------- V pre-pass --
+// Grid (key tile of 128, row).  Each CTA first finds its row's live
+// positions [pmin, pmax]; the attention kernel reads V keys in
+// [start, end): start = the first key any live token can see, rounded down
+// to a tile, end = pmax + 1 rounded up to a tile (clamped to the workspace).
+// One warp per key: its h_kv x 128 values are contiguous in the pool.
+__global__ void __launch_bounds__(kCvtThreads)
+    prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int max_ctx) {
+  __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
+  const int b = (int)blockIdx.y, k0 = (int)blockIdx.x * kBN;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
+  int pmin = INT32_MAX, pmax = -1;
+  for (int t = threadIdx.x; t < P.T; t += kCvtThreads) {
+    const int p = P.positions[(size_t)b * P.T + t];
+    if (p >= 0 && p < cap) {
+      pmin = min(pmin, p);
+      pmax = max(pmax, p);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
+    pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
+  }
+  if (lane == 0) {
+    s_min[warp] = pmin;
+    s_max[warp] = pmax;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kCvtThreads / 32; ++w) {
+    pmin = min(pmin, s_min[w]);
+    pmax = max(pmax, s_max[w]);
+  }
+  if (pmax < 0) return;  // no live token: the attention kernel reads nothing
+  const int lo = (P.window > 0 && pmin - P.window + 1 > 0) ? pmin - P.window + 1 : 0;
+  const int start = lo / kBN * kBN, end = min((pmax / kBN + 1) * kBN, max_ctx);
+  if (k0 + kBN <= start || k0 >= end) return;
+  const int units = P.h_kv * 16;  // 16-byte units of one key (all KV heads)
+  uint32_t vmax = 0;              // max |bf16 bits| seen, per half-word
+  for (int r = warp; r < kBN; r += kCvtThreads / 32) {
+    const int k = k0 + r;
+    if (k < start || k >= end) continue;
+    const uint4* src = nullptr;
+    if (k <= pmax) {
+      const int page = __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + k / P.page_size);
+      if (page >= 0 && page < P.num_pages)
+        src = reinterpret_cast<const uint4*>(
+            P.v_cache + ((size_t)page * P.page_size + k % P.page_size) * P.h_kv * 128);
+      else if (lane == 0)
+        report(P.error_word, TL_DEVERR_PAGE_RANGE);
+    }
+    for (int u = lane; u < units; u += 32) {
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);  // keys past pmax, bad pages: zeros
+      if (src) {
+        x = __ldg(src + u);
+        vmax = max_u16x2(vmax, max_u16x2(max_u16x2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                         max_u16x2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
+        x = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                       bf16x2_to_f16x2(x.w));
+      }
+      *reinterpret_cast<uint4*>(ws + (((size_t)b * P.h_kv + (u >> 4)) * max_ctx + k) * 128 +
+                                (u & 15) * 8) = x;
+    }
+  }
+  const uint32_t m0 = vmax & 0xffffu, m1 = vmax >> 16;
+  if ((m0 >= kBf16TooBig && m0 < kBf16Inf) || (m1 >= kBf16TooBig && m1 < kBf16Inf))
+    report(P.error_word, TL_DEVERR_VALUE_RANGE);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -405,7 +262,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&sh.v_full[i]), 1);
       mbar_init(smem_u32(&sh.v_empty[i]), 1);
     }
-    mbar_init(smem_u32(&sh.v_fix), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.p_full[i]), 4);
@@ -468,26 +324,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       {
         const int st = j % kTcVS;
         if (!mbar_wait(smem_u32(&sh.v_empty[st]), ((j / kTcVS) & 1) ^ 1, abort_flag)) break;
-        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcKVBytes);
-        __syncwarp();
-        if (lane < 2 * nbox)
-          tma_load_3d(sV + st * kTcKVBytes + boff, &vmap, half * 64, g, slot0,
-                      smem_u32(&sh.v_full[st]));
-        ++v_issued;
-        if (j == n_tiles - 1) {
-          // rows past the CTA's last position may hold anything: zero them
-          if (!mbar_wait(smem_u32(&sh.v_full[st]), (j / kTcVS) & 1, abort_flag)) break;
-          const int first_dead = rg.kmax + 1 - key0;  // 1..kBN
-          const uint32_t vt = sV + st * kTcKVBytes;
-          for (int idx = lane; idx < (kBN - first_dead) * 16; idx += 32) {
-            const int row = first_dead + (idx >> 4), hu = idx & 15;
-            const uint32_t a = vt + (hu >> 3) * (kTcKVBytes / 2) + row * 128 + ((hu & 7) << 4);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sh.v_fix));
+        if (lane == 0) {
+          mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcKVBytes);
+          for (int hh = 0; hh < 2; ++hh)
+            tma_load_3d(sV + st * kTcKVBytes + hh * (kTcKVBytes / 2), &vmap, hh * 64, key0,
+                        b * P.h_kv + g, smem_u32(&sh.v_full[st]));
         }
+        __syncwarp();
+        ++v_issued;
       }
     }
     // drain: the copies this warp issued have landed before the CTA exits
@@ -502,7 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // -------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint32_t idS = tc::idesc_bf16(128, kBN, 0, 0);
-      const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
+      const uint32_t idPV = tc::idesc_f16(128, 128, 0, 1);
       auto issue_s = [&](int a, int j) {  // S_a(j) into TMEM columns [128a, 128a+128)
         const uint32_t kt = sK + (j % kTcKS) * kTcKVBytes;
         const uint32_t qt = sQ + a * kTcQBytes;
@@ -515,17 +359,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::commit(smem_u32(&sh.s_full[a]));
       };
-      auto issue_pv = [&](int a, int j) {  // O_a += P_a(j) V(j)
+      auto issue_pv = [&](int a, int j) {  // O_a += P_a(j) V(j), fp16
         const uint32_t vt = sV + (j % kTcVS) * kTcKVBytes;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-#pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)  // P chunk c = k/2 holds hi at +0, lo at +16
-            tc::mma_ts(tmem + 256 + a * 128,
-                       tmem + a * 128 + 32 * (k >> 1) + 8 * (k & 1) + 16 * part,
-                       tc::sdesc(vt + k * 2048, kTcKVBytes / 2, 1024), idPV,
-                       (j > 0 || part > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kBN / 16; ++k)  // keys [16k, 16k+16): P columns [8k, 8k+8)
+          tc::mma_ts(tmem + 256 + a * 128, tmem + a * 128 + 8 * k,
+                     tc::sdesc(vt + k * 2048, kTcKVBytes / 2, 1024), idPV,
+                     (j > 0 || k > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort_flag) &&
                 mbar_wait(smem_u32(&sh.k_full[0]), 0, abort_flag);
@@ -537,9 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const bool last = j == n_tiles - 1;
-        if (!mbar_wait(last ? smem_u32(&sh.v_fix) : smem_u32(&sh.v_full[j % kTcVS]),
-                       last ? 0 : (j / kTcVS) & 1, abort_flag))
-          break;
+        if (!mbar_wait(smem_u32(&sh.v_full[j % kTcVS]), (j / kTcVS) & 1, abort_flag)) break;
         if (!mbar_wait(smem_u32(&sh.p_full[0]), j & 1, abort_flag)) break;
         tc::fence_after();
         issue_pv(0, j);
@@ -604,11 +442,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
 #pragma unroll
-      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
+      for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[c + i], s[c + 8 + i]);
+      const float mt =
+          max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sc;
       const bool need = l > 0.f && mt > m_used + kRescaleLog2;
       float corr = 1.f;
       if (need) {
@@ -617,20 +457,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (m_used == -INFINITY) m_used = mt;  // first live key of this row
       const float base = m_used == -INFINITY ? 0.f : m_used;
-      // P = exp2(s*sc - base) as hi + lo bf16 over each 32-column chunk's own columns
+      // P = fp16(exp2(s*sc - base)), keys 2c and 2c+1 in column c; the sum
+      // takes the same rounded values
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q = 0; q < kBN / 32; ++q) {
-        uint32_t pk[32];  // [0,16) hi, [16,32) lo
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float x0 = fast_exp2(fmaf(s[q * 32 + 2 * i], sc, -base));
           const float x1 = fast_exp2(fmaf(s[q * 32 + 2 * i + 1], sc, -base));
-          ls[i & 3] += x0 + x1;
-          split_bf16x2(x0, x1, pk[i], pk[16 + i]);
+          pk[i] = pack_f16x2(x0, x1);
+          float r0, r1;
+          unpack_f16x2(pk[i], r0, r1);
+          ls[i & 3] += r0 + r1;
         }
-        tc::st16(tmem + lane_base + colS + q * 32, pk);
-        tc::st16(tmem + lane_base + colS + q * 32 + 16, pk + 16);
+        tc::st16(tmem + lane_base + colS + q * 16, pk);
       }
       l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       if (__any_sync(0xffffffffu, need)) {
@@ -682,9 +524,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }  // namespace tl
 
 extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q,
-                                                       int32_t h_kv, int32_t d) {
-  if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv) return 0;
-  return 256;
+                                                       int32_t h_kv, int32_t d,
+                                                       int32_t max_pages_per_seq,
+                                                       int32_t page_size) {
+  if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv ||
+      max_pages_per_seq <= 0 || page_size <= 0)
+    return 0;
+  // the fp16 copy of V: [B][h_kv][max_pages_per_seq * page_size][d]
+  return (size_t)B * h_kv * ((size_t)max_pages_per_seq * page_size) * d * 2;
 }
 
 extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
@@ -711,8 +558,10 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   if (dtype != TL_BF16 || d != 128 || (page_size & (page_size - 1)) || page_size < 8 ||
       page_size > 128)
     return TL_ERR_UNSUPPORTED;
-  (void)workspace;
-  (void)workspace_bytes;
+  if ((int64_t)max_pages_per_seq * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
+  const size_t ws_need = tl_paged_attn_prefill_workspace_size(B, T, h_q, h_kv, d,
+                                                              max_pages_per_seq, page_size);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_need) return TL_ERR_WORKSPACE;
   PrefillParams P;
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
@@ -737,6 +586,7 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   const int group = h_q / h_kv;
   const int tpt = 128 / group;
   const int box_rows = page_size % 16 == 0 ? 16 : 8;
+  const int max_ctx = max_pages_per_seq * page_size;
   CUtensorMap qmap, kmap, vmap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
@@ -745,9 +595,13 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
     const uint64_t kd[3] = {128, (uint64_t)h_kv, (uint64_t)num_pages * page_size};
     const uint64_t ks[2] = {128 * 2, (uint64_t)h_kv * 128 * 2};
     const uint32_t kb[3] = {64, 1, (uint32_t)box_rows};
+    // the workspace's fp16 V: (d, key, row x KV head), 16-bit elements like bf16
+    const uint64_t vd[3] = {128, (uint64_t)max_ctx, (uint64_t)B * h_kv};
+    const uint64_t vs[2] = {128 * 2, (uint64_t)max_ctx * 128 * 2};
+    const uint32_t vb[3] = {64, (uint32_t)kBN, 1};
     if (!encode_bf16_tensor_map(&qmap, q, 3, qd, qs, qb, true) ||
         !encode_bf16_tensor_map(&kmap, k_cache, 3, kd, ks, kb, true) ||
-        !encode_bf16_tensor_map(&vmap, v_cache, 3, kd, ks, kb, true))
+        !encode_bf16_tensor_map(&vmap, workspace, 3, vd, vs, vb, true))
       return TL_ERR_CUDA;
   }
   if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -755,6 +609,8 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
     return TL_ERR_CUDA;
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
   if ((int64_t)B * h_kv > 0x7fffffff || n_pairs > 65535) return TL_ERR_UNSUPPORTED;
+  prefill_v_f16_kernel<<<dim3((max_ctx + kBN - 1) / kBN, B), kCvtThreads, 0,
+                         (cudaStream_t)stream>>>(P, static_cast<uint16_t*>(workspace), max_ctx);
   prefill_tc_kernel<<<dim3(B * h_kv, n_pairs), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
       P, qmap, kmap, vmap, box_rows);
   return launch_status();

@@ -11,8 +11,9 @@
 //     1024 B between 8-key groups; a K step of 16 keys advances 2048 B;
 //   - the f32 accumulator of an M=128 MMA: row i in TMEM lane i, column j in
 //     column j; warp w reads lanes 32*(w%4)..+31 (32x32b shape);
-//   - a bf16 A operand in TMEM: row i in lane i, column c holds elements
-//     2c (low half) and 2c+1 (high half); a K step of 16 is 8 columns.
+//   - a 16-bit (bf16 or fp16) A operand in TMEM: row i in lane i, column c
+//     holds elements 2c (low half) and 2c+1 (high half); a K step of 16 is 8
+//     columns.
 #pragma once
 
 #include <stdint.h>
@@ -44,6 +45,12 @@ TC_DEVINLINE uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
 TC_DEVINLINE uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) |
          ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with fp16 A and B, f32 accumulator.
+TC_DEVINLINE uint32_t idesc_f16(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // D(tmem) (+)= A(smem desc) * B(smem desc)

@@ -108,3 +108,32 @@ def test_bad_page_is_reported_not_faulted():
     torch.cuda.synchronize()
     assert int(err.item()) & tl.TL_DEVERR_PAGE_RANGE
     assert torch.isfinite(out).all()
+
+
+def test_v_beyond_fp16_range_is_reported():
+    """P.V runs in fp16: a finite V entry beyond +-65504 in the keys a call
+    reads is reported (65280, the largest bf16 below fp16's overflow, is not)."""
+    case = wl.prefill_case([0], [500], T=64, Hq=8, Hkv=2, d=128, seed=11)
+    g = on_gpu(case)
+    gpu_write(g)
+    slot = case.pool.slot(0, 100)  # prior context every token sees
+    for val, flagged in ((65280.0, False), (-65536.0, True)):
+        vc = g.v_cache.clone()
+        vc.view(-1, case.Hkv, case.d)[slot, 1, 5] = val
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        tl.tl_paged_attn_prefill(g.q, g.k_cache, vc, g.block_table, g.positions, g.scale,
+                                 error_word=err)
+        torch.cuda.synchronize()
+        assert bool(int(err.item()) & tl.TL_DEVERR_VALUE_RANGE) == flagged, (val, int(err.item()))
+
+
+def test_small_workspace_is_refused():
+    case = wl.prefill_case([0], [100], T=32, Hq=8, Hkv=2, d=128, seed=12)
+    g = on_gpu(case)
+    need = tl.tl_paged_attn_prefill_workspace_size(1, 32, 8, 2, 128, g.block_table.shape[1],
+                                                   case.page_size)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_paged_attn_prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.positions, g.scale,
+                                 workspace=ws)
+    assert e.value.status == tl.TL_ERR_WORKSPACE
