@@ -21,8 +21,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-bool encode_bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                            const uint64_t* strides, const uint32_t* box, bool swizzle128) {
+static bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, const void* base,
+                              int rank, const uint64_t* dims, const uint64_t* strides,
+                              const uint32_t* box, bool swizzle128) {
   auto enc = tensor_map_encoder();
   if (!enc || rank < 1 || rank > 5) return false;
   cuuint64_t gdim[5], gstride[4];
@@ -34,11 +35,23 @@ bool encode_bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const 
     if (i + 1 < rank) gstride[i] = strides[i];
   }
   const CUresult r =
-      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gdim,
+      enc(map, type, (cuuint32_t)rank, const_cast<void*>(base), gdim,
           gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides, const uint32_t* box, bool swizzle128) {
+  return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box,
+                           swizzle128);
+}
+
+bool encode_f32_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides, const uint32_t* box, bool swizzle128) {
+  return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides, box,
+                           swizzle128);
 }
 
 int num_sms() {

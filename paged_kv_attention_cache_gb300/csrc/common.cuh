@@ -134,6 +134,23 @@ TL_DEVINLINE void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int 
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+// Tiled TMA store of a 4-D box from shared memory (bulk-group completion);
+// elements past the tensor's extent are not written.
+TL_DEVINLINE void tma_store_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                               uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+      : "memory");
+}
+TL_DEVINLINE void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until every committed bulk store of this thread has read its source.
+TL_DEVINLINE void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+TL_DEVINLINE void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
 TL_DEVINLINE void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
@@ -192,6 +209,9 @@ int num_sms();  // SM count of the current device (cached per device)
 // `swizzle128`; out-of-range boxes fill with zeros.  False on failure.
 bool encode_bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides, const uint32_t* box, bool swizzle128);
+// The same for f32 elements.
+bool encode_f32_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides, const uint32_t* box, bool swizzle128);
 
 inline tl_status launch_status() {
   cudaError_t e = cudaGetLastError();

@@ -7,16 +7,16 @@
 //
 // Two launches.  A pre-pass converts the V rows each row's tokens can see
 // from the bf16 pages to fp16, once, into the workspace, laid out as
-// [row][KV head][key][d] (exact for every finite V entry within +-65504;
-// larger ones are reported; keys past the row's last position are zeros).
-// Then the attention kernel runs one CTA per (pair of query tiles, KV head,
-// row) on the 5th-generation tensor core.  A query tile packs tokens_per_tile = 128/group consecutive
-// tokens of one row with all `group` query heads that share the KV head, as
-// the 128 M rows (row r = token r/group, head r%group); the CTA holds two
-// consecutive tiles (Q0, Q1), so every K/V tile it streams feeds 256 rows.
-// Keys are folded in tiles of 128 over the range the CTA's live tokens can
-// see ([min lo, max p]); every MMA has N = 128 (keys for S, head dimension for
-// P.V), the width at which the tensor core runs near its peak.
+// [row][KV head][key][d] (exact for |v| in [2^-14, 65504]; larger finite
+// values are reported; keys past the row's last position are zeros).  Then
+// the attention kernel runs one CTA per (pair of query tiles, KV head, row)
+// on the 5th-generation tensor core.  A query tile packs tokens_per_tile =
+// 128/group consecutive tokens of one row with all `group` query heads that
+// share the KV head, as the 128 M rows (row r = token r/group, head
+// r%group); the CTA holds two consecutive tiles (Q0, Q1), so every K/V tile
+// it streams feeds 256 rows.  Keys are folded in tiles of 128 over the range
+// the CTA's live tokens can see ([min lo, max p]); every MMA is M=128 x
+// N=128 x K=16 (N = keys for S, the head dimension for P.V).
 //   warp 0      TMA producer: Q0 and Q1 once (a 3-D map (d, H_q, token), box
 //               64 x group x tokens), then K and V tiles into rings of kTcKS /
 //               kTcVS stages: K in boxes of 8 or 16 rows of the pool map (one
@@ -34,7 +34,8 @@
 //               rescale (O and the sum change only when the max grows by
 //               more than 2^8), write P rounded to fp16 into the first 64
 //               columns of S_a, and add the rounded values to the row sum;
-//               finally the epilogue O / l.
+//               finally the epilogue: O / l staged in shared memory the
+//               finished tile no longer needs, written by TMA stores.
 // P is rounded to fp16 rather than bf16: bf16's 8-bit significand makes the
 // weights of a peaked softmax off by up to 2^-9, which moves an output by
 // several 1e-3 when |V| is a few units; fp16's 11 bits and a sum over the same
@@ -150,10 +151,15 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // positions [pmin, pmax]; the attention kernel reads V keys in
 // [start, end): start = the first key any live token can see, rounded down
 // to a tile, end = pmax + 1 rounded up to a tile (clamped to the workspace).
-// One warp per key: its h_kv x 128 values are contiguous in the pool.
+// The tile's page numbers go to shared memory; then every thread moves
+// 16-byte units (key-major: one key's h_kv x 128 values are contiguous in
+// the pool), kCvtUnroll independent loads in flight.
+constexpr int kCvtUnroll = 8;
+
 __global__ void __launch_bounds__(kCvtThreads)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int max_ctx) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
+  __shared__ int s_page[kBN];  // page of each key of the tile; -1: write zeros
   const int b = (int)blockIdx.y, k0 = (int)blockIdx.x * kBN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
@@ -184,31 +190,52 @@ __global__ void __launch_bounds__(kCvtThreads)
   const int lo = (P.window > 0 && pmin - P.window + 1 > 0) ? pmin - P.window + 1 : 0;
   const int start = lo / kBN * kBN, end = min((pmax / kBN + 1) * kBN, max_ctx);
   if (k0 + kBN <= start || k0 >= end) return;
-  const int units = P.h_kv * 16;  // 16-byte units of one key (all KV heads)
-  uint32_t vmax = 0;              // max |bf16 bits| seen, per half-word
-  for (int r = warp; r < kBN; r += kCvtThreads / 32) {
+  for (int r = threadIdx.x; r < kBN; r += kCvtThreads) {
     const int k = k0 + r;
-    if (k < start || k >= end) continue;
-    const uint4* src = nullptr;
+    int page = -1;  // keys past pmax: zeros
     if (k <= pmax) {
-      const int page = __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + k / P.page_size);
-      if (page >= 0 && page < P.num_pages)
-        src = reinterpret_cast<const uint4*>(
-            P.v_cache + ((size_t)page * P.page_size + k % P.page_size) * P.h_kv * 128);
-      else if (lane == 0)
+      page = __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + k / P.page_size);
+      if (page < 0 || page >= P.num_pages) {
         report(P.error_word, TL_DEVERR_PAGE_RANGE);
-    }
-    for (int u = lane; u < units; u += 32) {
-      uint4 x = make_uint4(0u, 0u, 0u, 0u);  // keys past pmax, bad pages: zeros
-      if (src) {
-        x = __ldg(src + u);
-        vmax = max_u16x2(vmax, max_u16x2(max_u16x2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
-                                         max_u16x2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
-        x = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
-                       bf16x2_to_f16x2(x.w));
+        page = -1;  // bad page: zeros
       }
-      *reinterpret_cast<uint4*>(ws + (((size_t)b * P.h_kv + (u >> 4)) * max_ctx + k) * 128 +
-                                (u & 15) * 8) = x;
+    }
+    s_page[r] = page;
+  }
+  __syncthreads();
+  const int r0 = max(start - k0, 0), r1 = min(end - k0, kBN);  // keys of the tile to write
+  const int units = P.h_kv * 16;                                // 16-byte units per key
+  const int total = (r1 - r0) * units;
+  uint32_t vmax = 0;  // max |bf16 bits| seen, per half-word
+  for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
+    uint4 x[kCvtUnroll];
+#pragma unroll
+    for (int i = 0; i < kCvtUnroll; ++i) {
+      const int idx = base + i * kCvtThreads + (int)threadIdx.x;
+      x[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < total) {
+        const int r = r0 + idx / units, u = idx % units;
+        const int page = s_page[r];
+        if (page >= 0)
+          x[i] = __ldg(reinterpret_cast<const uint4*>(
+                           P.v_cache +
+                           ((size_t)page * P.page_size + (k0 + r) % P.page_size) * P.h_kv * 128) +
+                       u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kCvtUnroll; ++i) {
+      const int idx = base + i * kCvtThreads + (int)threadIdx.x;
+      if (idx < total) {
+        const int r = r0 + idx / units, u = idx % units;
+        uint4 y = x[i];
+        vmax = max_u16x2(vmax, max_u16x2(max_u16x2(y.x & 0x7fff7fffu, y.y & 0x7fff7fffu),
+                                         max_u16x2(y.z & 0x7fff7fffu, y.w & 0x7fff7fffu)));
+        y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z),
+                       bf16x2_to_f16x2(y.w));
+        *reinterpret_cast<uint4*>(ws + (((size_t)b * P.h_kv + (u >> 4)) * max_ctx + k0 + r) * 128 +
+                                  (u & 15) * 8) = y;
+      }
     }
   }
   const uint32_t m0 = vmax & 0xffffu, m1 = vmax >> 16;
@@ -219,7 +246,8 @@ __global__ void __launch_bounds__(kCvtThreads)
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, int box_rows) {
+                      const __grid_constant__ CUtensorMap vmap,
+                      const __grid_constant__ CUtensorMap omap, int box_rows) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ TcShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -412,7 +440,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t colS = a * 128, colO = 256 + a * 128;
-    const int t = t0 + a * tpt + row / P.group, h = g * P.group + row % P.group;
+    const int t = t0 + a * tpt + row / P.group;
     int p = -1;
     if (row < rows_used && t < P.T) {
       p = P.positions[(size_t)b * P.T + t];
@@ -493,23 +521,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[a]));
     }
-    // epilogue: O / l
-    if (ok && mbar_wait(smem_u32(&sh.o_done[a]), 0, abort_flag)) {
+    // epilogue: O / l, staged in shared memory that the finished tile no
+    // longer needs (tile 0: the K ring, free once O_0 is done because every S
+    // MMA was issued before PV_0 of the last tile; tile 1: the Q tiles) as
+    // four 128-byte-swizzled quarters of d, then written by TMA stores whose
+    // box is the tile's (d quarter, heads of the group, tokens), clipped at T
+    const bool have = ok && mbar_wait(smem_u32(&sh.o_done[a]), 0, abort_flag);
+    const uint32_t stage = a == 0 ? sK : sQ;
+    if (have) {
       tc::fence_after();
       const float inv = (p >= 0 && l > 0.f) ? 1.f / l : 0.f;
-      float* dst = P.out + (((size_t)b * P.T + t) * P.h_q + h) * 128;
+      float o[128];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float o[32];
-        tc::ld32(tmem + lane_base + colO + q * 32, o);
-        tc::wait_ld();
-        if (row < rows_used && t < P.T) {
+      for (int q = 0; q < 4; ++q) tc::ld32(tmem + lane_base + colO + q * 32, o + q * 32);
+      tc::wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + q * 32 + i) =
-                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t adr = stage + q * 16384 + row * 128 + ((i ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(adr),
+                       "f"(o[q * 32 + 4 * i] * inv), "f"(o[q * 32 + 4 * i + 1] * inv),
+                       "f"(o[q * 32 + 4 * i + 2] * inv), "f"(o[q * 32 + 4 * i + 3] * inv)
+                       : "memory");
         }
-      }
+    }
+    fence_proxy_async_smem();
+    named_barrier(1 + a, 128);  // every thread of the warpgroup gets here
+    if ((warp & 3) == 2 && lane == 0 && !*abort_flag) {
+      for (int q = 0; q < 4; ++q)
+        tma_store_4d(&omap, q * 32, g * P.group, t0 + a * tpt, b, stage + q * 16384);
+      bulk_commit_group();
+      bulk_wait_read_all();
     }
   }
   tc::fence_before();
@@ -587,7 +630,7 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   const int tpt = 128 / group;
   const int box_rows = page_size % 16 == 0 ? 16 : 8;
   const int max_ctx = max_pages_per_seq * page_size;
-  CUtensorMap qmap, kmap, vmap;
+  CUtensorMap qmap, kmap, vmap, omap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
     const uint64_t qs[2] = {128 * 2, (uint64_t)h_q * 128 * 2};
@@ -599,6 +642,12 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
     const uint64_t vd[3] = {128, (uint64_t)max_ctx, (uint64_t)B * h_kv};
     const uint64_t vs[2] = {128 * 2, (uint64_t)max_ctx * 128 * 2};
     const uint32_t vb[3] = {64, (uint32_t)kBN, 1};
+    // the output, f32 (d, h_q, T, B): a TMA store box is one d quarter of a
+    // query tile, clipped at T
+    const uint64_t od[4] = {128, (uint64_t)h_q, (uint64_t)T, (uint64_t)B};
+    const uint64_t os[3] = {128 * 4, (uint64_t)h_q * 128 * 4, (uint64_t)T * h_q * 128 * 4};
+    const uint32_t ob[4] = {32, (uint32_t)group, (uint32_t)tpt, 1};
+    if (!encode_f32_tensor_map(&omap, out, 4, od, os, ob, true)) return TL_ERR_CUDA;
     if (!encode_bf16_tensor_map(&qmap, q, 3, qd, qs, qb, true) ||
         !encode_bf16_tensor_map(&kmap, k_cache, 3, kd, ks, kb, true) ||
         !encode_bf16_tensor_map(&vmap, workspace, 3, vd, vs, vb, true))
@@ -612,6 +661,6 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   prefill_v_f16_kernel<<<dim3((max_ctx + kBN - 1) / kBN, B), kCvtThreads, 0,
                          (cudaStream_t)stream>>>(P, static_cast<uint16_t*>(workspace), max_ctx);
   prefill_tc_kernel<<<dim3(B * h_kv, n_pairs), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
-      P, qmap, kmap, vmap, box_rows);
+      P, qmap, kmap, vmap, omap, box_rows);
   return launch_status();
 }
