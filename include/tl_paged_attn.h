@@ -171,10 +171,11 @@ tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const
                                        tl_dtype dtype, uint32_t* error_word, void* stream);
 
 /*
- * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes): an
- * fp16 copy of the V rows the call reads, [B][h_kv][max_pages_per_seq *
- * page_size][d], i.e. B * h_kv * max_pages_per_seq * page_size * d * 2.  It
- * does not depend on T or h_q (they are taken for the shape checks only).
+ * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes): a
+ * 256-byte header (the kernel's work counter) and an fp16 copy of the V rows
+ * the call reads, [B][h_kv][max_pages_per_seq * page_size][d], i.e.
+ * 256 + B * h_kv * max_pages_per_seq * page_size * d * 2.  It does not
+ * depend on T or h_q (they are taken for the shape checks only).
  */
 size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
                                             int32_t d, int32_t max_pages_per_seq,
@@ -195,9 +196,9 @@ size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, i
  *   out          [B][T][h_q][d] float32
  *   workspace    device scratch of at least tl_paged_attn_prefill_workspace_size(
  *                B, T, h_q, h_kv, d, max_pages_per_seq, page_size) bytes,
- *                16-byte aligned (TL_ERR_WORKSPACE otherwise); it receives the
- *                call's fp16 copy of V, so calls that may overlap on the GPU
- *                must not share one.
+ *                256-byte aligned (TL_ERR_WORKSPACE otherwise); it receives
+ *                the call's fp16 copy of V and work counter, so calls that may
+ *                overlap on the GPU must not share one.
  *   other arguments as for decode.
  * Supported: dtype TL_BF16, d = 128, h_q % h_kv == 0 with h_q/h_kv <= 128,
  * page_size a power of two in [8, 128].  Otherwise TL_ERR_UNSUPPORTED.

@@ -51,6 +51,8 @@
 // S_a(j+1) is complete so is PV_a(j) (its O is stable for a rescale).  A CTA
 // never touches another row and its arithmetic does not depend on B, so a row
 // gives the same bits batched or alone.  All waits are bounded.
+#include <algorithm>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -71,13 +73,18 @@ struct PrefillParams {
 };
 
 constexpr int kBN = 128;             // keys per tile
-constexpr int kTcKS = 3;             // K stages
+constexpr int kTcQB = 3;             // query-tile buffers (two in use, one filling)
+constexpr int kTcKS = 2;             // K stages
 constexpr int kTcVS = 2;             // V stages
-constexpr int kTcThreads = 10 * 32;
+constexpr int kTcWarps = 10;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kItemSlots = 4;        // work items fetched ahead of their use
+constexpr int kItemReaders = kTcWarps - 1;  // the MMA warp and the eight softmax warps
 constexpr int kCvtThreads = 256;
 constexpr int kTcQBytes = 32768;     // one query tile: 128 rows x 128 d x bf16
 constexpr int kTcKVBytes = kBN * 256;  // 128 keys x 128 d x 16-bit (two 16 KiB halves)
-constexpr int kTcSmem = 2 * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
+constexpr int kTcSmem = kTcQB * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
+constexpr size_t kWsHeader = 256;    // workspace bytes before the fp16 V copy (the item counter)
 constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 // bf16 bit patterns (sign cleared) of the finite values fp16 cannot hold:
@@ -86,8 +93,11 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kBf16TooBig = 0x4780u, kBf16Inf = 0x7F80u;
 
 struct TcShared {
-  unsigned long long q_full, k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS];
-  unsigned long long s_full[2], p_full[2], o_done[2], mma_drain;
+  unsigned long long q_full[kTcQB], q_free[kTcQB];
+  unsigned long long k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS];
+  unsigned long long s_full[2], p_full[2], o_done[2], o_free[2], stg_full[2], stg_free[2];
+  unsigned long long item_full[kItemSlots], item_empty[kItemSlots], mma_drain;
+  int item[kItemSlots];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -157,8 +167,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 constexpr int kCvtUnroll = 8;
 
 __global__ void __launch_bounds__(kCvtThreads)
-    prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int max_ctx) {
+    prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int max_ctx, int* counter) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;  // work items
   __shared__ int s_page[kBN];  // page of each key of the tile; -1: write zeros
   const int b = (int)blockIdx.y, k0 = (int)blockIdx.x * kBN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -243,45 +254,108 @@ __global__ void __launch_bounds__(kCvtThreads)
     report(P.error_word, TL_DEVERR_VALUE_RANGE);
 }
 
+// S_a = Q_a K^T into TMEM columns [128a, 128a+128): eight K=16 steps over
+// the 128-byte-swizzled K-major Q and K tiles; then a commit to s_full_a.
+__device__ __forceinline__ void tc_issue_s(uint32_t tmem, int a, uint32_t kbase, uint32_t qbase,
+                                           uint32_t s_full_a) {
+  const uint32_t idS = tc::idesc_bf16(128, kBN, 0, 0);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t off = (k >> 2) * (kTcQBytes / 2) + (k & 3) * 32;
+    tc::mma_ss(tmem + a * 128, tc::sdesc(qbase + off, 16, 1024), tc::sdesc(kbase + off, 16, 1024),
+               idS, k > 0);
+  }
+  tc::commit(s_full_a);
+}
+// O_a (+)= P_a V in fp16: P_a from TMEM (keys [16k, 16k+16) in columns
+// [8k, 8k+8) of S_a), V MN-major from shared memory.
+__device__ __forceinline__ void tc_issue_pv(uint32_t tmem, int a, uint32_t vbase, bool acc) {
+  const uint32_t idPV = tc::idesc_f16(128, 128, 0, 1);
+#pragma unroll
+  for (int k = 0; k < kBN / 16; ++k)
+    tc::mma_ts(tmem + 256 + a * 128, tmem + a * 128 + 8 * k,
+               tc::sdesc(vbase + k * 2048, kTcKVBytes / 2, 1024), idPV, (acc || k > 0) ? 1u : 0u);
+}
+
+// One work item: a pair of query tiles of one row and KV head.  Items are
+// numbered heaviest first (the latest pairs of every row and head, whose
+// tokens see the most keys, come first); every warp decodes the same item
+// itself (tc_tile_range is warp-wide).
+struct TcItem {
+  int b, g, t0, tile0, n_tiles;
+  TcRange rg;
+};
+
+__device__ __forceinline__ TcItem tc_item(const PrefillParams& P, int idx, int tpt, int n_pairs,
+                                          int64_t cap) {
+  TcItem it;
+  const int bh = P.B * P.h_kv;
+  const int qp = n_pairs - 1 - idx / bh, r = idx % bh;
+  it.b = r / P.h_kv;
+  it.g = r % P.h_kv;
+  it.t0 = qp * 2 * tpt;
+  it.rg = tc_tile_range(P, it.b, it.t0, 2 * tpt, cap);
+  it.tile0 = it.rg.kmax >= 0 ? it.rg.kmin / kBN : 0;
+  it.n_tiles = it.rg.kmax >= 0 ? it.rg.kmax / kBN - it.tile0 + 1 : 0;
+  return it;
+}
+
+// The seq-th work item of this CTA, -1 when the queue is exhausted or the
+// CTA aborts.  Warp 0 takes items from the global counter into a ring of
+// kItemSlots slots; the MMA and softmax warps read them (lane 0 frees the
+// slot).
+__device__ __forceinline__ int tc_fetch(TcShared& sh, uint32_t seq, int* counter, int n_items,
+                                        volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t slot = seq % kItemSlots, ph = (seq / kItemSlots) & 1;
+  int idx = -1;
+  if (threadIdx.x < 32) {
+    if (!mbar_wait(smem_u32(&sh.item_empty[slot]), ph ^ 1, abort_flag)) return -1;
+    if (lane == 0) {
+      const int v = atomicAdd(counter, 1);
+      sh.item[slot] = v < n_items ? v : -1;
+      mbar_arrive(smem_u32(&sh.item_full[slot]));
+    }
+    if (!mbar_wait(smem_u32(&sh.item_full[slot]), ph, abort_flag)) return -1;
+    idx = *reinterpret_cast<volatile int*>(&sh.item[slot]);
+  } else {
+    if (!mbar_wait(smem_u32(&sh.item_full[slot]), ph, abort_flag)) return -1;
+    idx = *reinterpret_cast<volatile int*>(&sh.item[slot]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh.item_empty[slot]));
+  }
+  return idx;
+}
+
+// Persistent attention kernel: one CTA per SM, work items from the counter
+// at the head of the workspace (zeroed by the V pre-pass).  Across items the
+// K / V rings keep streaming; the query tiles rotate over kTcQB buffers (the
+// s-th tile of this CTA, s = 2 x item + a, lives in buffer s % kTcQB), and a
+// finished tile's buffer stages its output for the TMA stores before the
+// tile three steps later is loaded into it.
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
-                      const __grid_constant__ CUtensorMap omap, int box_rows) {
+                      const __grid_constant__ CUtensorMap omap, int box_rows, int* counter) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ TcShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase, sK = sbase + 2 * kTcQBytes, sV = sK + kTcKS * kTcKVBytes;
+  const uint32_t sQ = sbase, sK = sbase + kTcQB * kTcQBytes, sV = sK + kTcKS * kTcKVBytes;
   volatile int* abort_flag = &sh.abort_flag;
 
-  const int tpt = 128 / P.group;                 // tokens per query tile
+  const int tpt = 128 / P.group;  // tokens per query tile
   const int rows_used = tpt * P.group;
   const int n_pairs = (P.T + 2 * tpt - 1) / (2 * tpt);
-  // grid (row x KV head, pair): the latest (heaviest) pairs of every row and
-  // head launch first, so the long CTAs do not end up in the tail
-  const int qp = n_pairs - 1 - (int)blockIdx.y;
-  const int g = (int)blockIdx.x % P.h_kv, b = (int)blockIdx.x / P.h_kv;
-  const int t0 = qp * 2 * tpt;
+  const int n_items = n_pairs * P.B * P.h_kv;
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
-  const TcRange rg = tc_tile_range(P, b, t0, 2 * tpt, cap);
-
-  if (rg.kmax < 0) {  // no live token: the outputs are 0
-    for (int idx = threadIdx.x; idx < 2 * rows_used * 32; idx += kTcThreads) {
-      const int r = idx >> 5, c = (idx & 31) * 4;
-      const int a = r / rows_used, rr = r % rows_used;
-      const int t = t0 + a * tpt + rr / P.group;
-      if (t < P.T)
-        *reinterpret_cast<float4*>(
-            P.out + (((size_t)b * P.T + t) * P.h_q + (size_t)g * P.group + rr % P.group) * 128 + c) =
-            make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    return;
-  }
-  const int tile0 = rg.kmin / kBN, n_tiles = rg.kmax / kBN - tile0 + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sh.q_full), 1);
+    for (int i = 0; i < kTcQB; ++i) {
+      mbar_init(smem_u32(&sh.q_full[i]), 1);
+      mbar_init(smem_u32(&sh.q_free[i]), 1);
+    }
     for (int i = 0; i < kTcKS; ++i) {
       mbar_init(smem_u32(&sh.k_full[i]), 1);
       mbar_init(smem_u32(&sh.k_empty[i]), 1);
@@ -294,6 +368,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.p_full[i]), 4);
       mbar_init(smem_u32(&sh.o_done[i]), 1);
+      mbar_init(smem_u32(&sh.o_free[i]), 4);
+      mbar_init(smem_u32(&sh.stg_full[i]), 128);
+      mbar_init(smem_u32(&sh.stg_free[i]), 1);
+    }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(smem_u32(&sh.item_full[i]), 1);
+      mbar_init(smem_u32(&sh.item_empty[i]), kItemReaders);
     }
     mbar_init(smem_u32(&sh.mma_drain), 1);
     sh.abort_flag = 0;
@@ -306,253 +387,345 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // -------------------------------------------------------------- TMA
+    // ------------------------------------------------------ K / V producer
     const int nbox = kBN / box_rows;  // boxes per row half of a tile (8 or 16)
     const int n_slots = P.num_pages * P.page_size;
-    const int32_t* bt_row = P.block_table + (size_t)b * P.max_pages_per_seq;
-    const int last_blk = rg.kmax / P.page_size;
-    int win_blk0 = -1, win = -1;
-    uint32_t k_issued = 0, v_issued = 0;
-    if (lane == 0) {
-      const uint32_t qbytes = (uint32_t)(64 * rows_used * 2);  // one half of one tile
-      mbar_arrive_expect_tx(smem_u32(&sh.q_full), 4 * qbytes);
-      for (int a = 0; a < 2; ++a)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sQ + a * kTcQBytes + h * (kTcQBytes / 2), &qmap, h * 64, g * P.group,
-                      b * P.T + t0 + a * tpt, smem_u32(&sh.q_full));
-    }
-    for (int j = 0; j < n_tiles; ++j) {
-      const int key0 = (tile0 + j) * kBN;
-      const int bmin = key0 / P.page_size;
-      const int bmax = min((key0 + kBN - 1) / P.page_size, last_blk);
-      if (win_blk0 < 0 || bmin < win_blk0 || bmax >= win_blk0 + 32) {
-        win_blk0 = bmin;
-        const int blk = win_blk0 + lane;
-        win = blk <= last_blk ? __ldg(bt_row + blk) : -1;
-      }
-      // this lane's boxes: lanes < 2*nbox (two row halves); box bi of half
-      const int half = lane / nbox, bi = lane % nbox;
-      const int kb = key0 + bi * box_rows;
-      const int blk = kb / P.page_size;
-      const int pg = __shfl_sync(0xffffffffu, win, (blk - win_blk0) & 31);
-      const bool box_ok = blk <= last_blk && pg >= 0 && pg < P.num_pages;
-      if (blk <= last_blk && !box_ok && lane < 2 * nbox) report(P.error_word, TL_DEVERR_PAGE_RANGE);
-      const int slot0 = box_ok ? pg * P.page_size + kb % P.page_size : n_slots;
-      const uint32_t boff = half * (kTcKVBytes / 2) + bi * box_rows * 128;
-      {
-        const int st = j % kTcKS;
-        if (!mbar_wait(smem_u32(&sh.k_empty[st]), ((j / kTcKS) & 1) ^ 1, abort_flag)) break;
-        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.k_full[st]), kTcKVBytes);
-        __syncwarp();
-        if (lane < 2 * nbox)
-          tma_load_3d(sK + st * kTcKVBytes + boff, &kmap, half * 64, g, slot0,
-                      smem_u32(&sh.k_full[st]));
-        ++k_issued;
-      }
-      {
-        const int st = j % kTcVS;
-        if (!mbar_wait(smem_u32(&sh.v_empty[st]), ((j / kTcVS) & 1) ^ 1, abort_flag)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcKVBytes);
-          for (int hh = 0; hh < 2; ++hh)
-            tma_load_3d(sV + st * kTcKVBytes + hh * (kTcKVBytes / 2), &vmap, hh * 64, key0,
-                        b * P.h_kv + g, smem_u32(&sh.v_full[st]));
+    uint32_t k_issued = 0, v_issued = 0, q_issued = 0;  // query tile s goes to buffer s % kTcQB
+    bool ok = true;
+    // query tile a of the item (lane 0): wait until its buffer's previous
+    // tile has been written out, then load it
+#define load_q(a)                                                                               \
+  {                                                                                             \
+    if (lane == 0) {                                                                            \
+      const uint32_t buf = q_issued % kTcQB, use = q_issued / kTcQB;                            \
+      if (mbar_wait(smem_u32(&sh.q_free[buf]), (use & 1) ^ 1, abort_flag)) {                    \
+        mbar_arrive_expect_tx(smem_u32(&sh.q_full[buf]), (uint32_t)(2 * 64 * rows_used * 2));   \
+        for (int h = 0; h < 2; ++h)                                                             \
+          tma_load_3d(sQ + buf * kTcQBytes + h * (kTcQBytes / 2), &qmap, h * 64,                \
+                      it.g * P.group, it.b * P.T + it.t0 + (a) * tpt, smem_u32(&sh.q_full[buf])); \
+        ++q_issued;                                                                             \
+      } else {                                                                                  \
+        ok = false;                                                                             \
+      }                                                                                         \
+    }                                                                                           \
+    ok = __shfl_sync(0xffffffffu, ok, 0);                                                       \
+    q_issued = __shfl_sync(0xffffffffu, q_issued, 0);                                           \
+  }
+    for (uint32_t seq = 0; ok; ++seq) {
+      const int idx = tc_fetch(sh, seq, counter, n_items, abort_flag);
+      if (idx < 0) break;
+      const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
+      if (it.rg.kmax < 0) continue;
+      const int32_t* bt_row = P.block_table + (size_t)it.b * P.max_pages_per_seq;
+      const int last_blk = it.rg.kmax / P.page_size;
+      int win_blk0 = -1, win = -1;
+      load_q(0)
+      for (int j = 0; j < it.n_tiles && ok; ++j) {
+        const int key0 = (it.tile0 + j) * kBN;
+        const int bmin = key0 / P.page_size;
+        const int bmax = min((key0 + kBN - 1) / P.page_size, last_blk);
+        if (win_blk0 < 0 || bmin < win_blk0 || bmax >= win_blk0 + 32) {
+          win_blk0 = bmin;
+          const int blk = win_blk0 + lane;
+          win = blk <= last_blk ? __ldg(bt_row + blk) : -1;
         }
-        __syncwarp();
-        ++v_issued;
+        // this lane's boxes: lanes < 2*nbox (two row halves); box bi of half
+        const int half = lane / nbox, bi = lane % nbox;
+        const int kb = key0 + bi * box_rows;
+        const int blk = kb / P.page_size;
+        const int pg = __shfl_sync(0xffffffffu, win, (blk - win_blk0) & 31);
+        const bool box_ok = blk <= last_blk && pg >= 0 && pg < P.num_pages;
+        if (blk <= last_blk && !box_ok && lane < 2 * nbox)
+          report(P.error_word, TL_DEVERR_PAGE_RANGE);
+        const int slot0 = box_ok ? pg * P.page_size + kb % P.page_size : n_slots;
+        const uint32_t boff = half * (kTcKVBytes / 2) + bi * box_rows * 128;
+        {
+          const uint32_t st = k_issued % kTcKS;
+          if (!mbar_wait(smem_u32(&sh.k_empty[st]), ((k_issued / kTcKS) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.k_full[st]), kTcKVBytes);
+          __syncwarp();
+          if (lane < 2 * nbox)
+            tma_load_3d(sK + st * kTcKVBytes + boff, &kmap, half * 64, it.g, slot0,
+                        smem_u32(&sh.k_full[st]));
+          ++k_issued;
+        }
+        {
+          const uint32_t st = v_issued % kTcVS;
+          if (!mbar_wait(smem_u32(&sh.v_empty[st]), ((v_issued / kTcVS) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcKVBytes);
+            for (int hh = 0; hh < 2; ++hh)
+              tma_load_3d(sV + st * kTcKVBytes + hh * (kTcKVBytes / 2), &vmap, hh * 64, key0,
+                          it.b * P.h_kv + it.g, smem_u32(&sh.v_full[st]));
+          }
+          __syncwarp();
+          ++v_issued;
+        }
+        if (j == 0) load_q(1)  // the second tile's buffer frees up later
       }
     }
+#undef load_q
     // drain: the copies this warp issued have landed before the CTA exits
     bool drained = true;
     for (uint32_t i = k_issued > (uint32_t)kTcKS ? k_issued - kTcKS : 0; i < k_issued; ++i)
       drained &= mbar_drain(smem_u32(&sh.k_full[i % kTcKS]), (i / kTcKS) & 1);
     for (uint32_t i = v_issued > (uint32_t)kTcVS ? v_issued - kTcVS : 0; i < v_issued; ++i)
       drained &= mbar_drain(smem_u32(&sh.v_full[i % kTcVS]), (i / kTcVS) & 1);
-    drained &= mbar_drain(smem_u32(&sh.q_full), 0);
+    for (uint32_t i = q_issued > (uint32_t)kTcQB ? q_issued - kTcQB : 0; i < q_issued; ++i)
+      drained &= mbar_drain(smem_u32(&sh.q_full[i % kTcQB]), (i / kTcQB) & 1);
     if (!drained) *abort_flag = 1;
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t idS = tc::idesc_bf16(128, kBN, 0, 0);
-      const uint32_t idPV = tc::idesc_f16(128, 128, 0, 1);
-      auto issue_s = [&](int a, int j) {  // S_a(j) into TMEM columns [128a, 128a+128)
-        const uint32_t kt = sK + (j % kTcKS) * kTcKVBytes;
-        const uint32_t qt = sQ + a * kTcQBytes;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t qo = (k >> 2) * (kTcQBytes / 2) + (k & 3) * 32;
-          const uint32_t ko = (k >> 2) * (kTcKVBytes / 2) + (k & 3) * 32;
-          tc::mma_ss(tmem + a * 128, tc::sdesc(qt + qo, 16, 1024), tc::sdesc(kt + ko, 16, 1024),
-                     idS, k > 0);
-        }
-        tc::commit(smem_u32(&sh.s_full[a]));
-      };
-      auto issue_pv = [&](int a, int j) {  // O_a += P_a(j) V(j), fp16
-        const uint32_t vt = sV + (j % kTcVS) * kTcKVBytes;
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)  // keys [16k, 16k+16): P columns [8k, 8k+8)
-          tc::mma_ts(tmem + 256 + a * 128, tmem + a * 128 + 8 * k,
-                     tc::sdesc(vt + k * 2048, kTcKVBytes / 2, 1024), idPV,
-                     (j > 0 || k > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort_flag) &&
-                mbar_wait(smem_u32(&sh.k_full[0]), 0, abort_flag);
-      if (ok) {
-        tc::fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        tc::commit(smem_u32(&sh.k_empty[0]));
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const bool last = j == n_tiles - 1;
-        if (!mbar_wait(smem_u32(&sh.v_full[j % kTcVS]), (j / kTcVS) & 1, abort_flag)) break;
-        if (!mbar_wait(smem_u32(&sh.p_full[0]), j & 1, abort_flag)) break;
-        tc::fence_after();
-        issue_pv(0, j);
-        if (last) {
-          tc::commit(smem_u32(&sh.o_done[0]));
-        } else {
-          if (!mbar_wait(smem_u32(&sh.k_full[(j + 1) % kTcKS]), ((j + 1) / kTcKS) & 1,
-                         abort_flag))
-            break;
+    // ---------------------------------------------------------------- MMA
+#define issue_s(a, kt, qbuf) \
+  tc_issue_s(tmem, (a), sK + ((kt) % kTcKS) * kTcKVBytes, sQ + (qbuf) * kTcQBytes, \
+             smem_u32(&sh.s_full[(a)]))
+#define issue_pv(a, vt, acc) tc_issue_pv(tmem, (a), sV + ((vt) % kTcVS) * kTcKVBytes, (acc))
+    uint32_t kt = 0, vt = 0, tiles = 0, n = 0;  // K / V tiles, S tiles, live items
+    bool ok = true;
+    for (uint32_t seq = 0; ok; ++seq) {
+      const int idx = tc_fetch(sh, seq, counter, n_items, abort_flag);
+      if (idx < 0) break;
+      const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
+      if (it.rg.kmax < 0) continue;
+      if (lane == 0) {
+        const uint32_t qb0 = (2 * n) % kTcQB, qb1 = (2 * n + 1) % kTcQB;
+        ok = mbar_wait(smem_u32(&sh.q_full[qb0]), ((2 * n) / kTcQB) & 1, abort_flag) &&
+             mbar_wait(smem_u32(&sh.k_full[kt % kTcKS]), (kt / kTcKS) & 1, abort_flag);
+        if (ok) {
           tc::fence_after();
-          issue_s(0, j + 1);
+          issue_s(0, kt, qb0);
         }
-        if (!mbar_wait(smem_u32(&sh.p_full[1]), j & 1, abort_flag)) break;
-        tc::fence_after();
-        issue_pv(1, j);
-        tc::commit(smem_u32(&sh.v_empty[j % kTcVS]));
-        if (last) {
-          tc::commit(smem_u32(&sh.o_done[1]));
-        } else {
-          issue_s(1, j + 1);
-          tc::commit(smem_u32(&sh.k_empty[(j + 1) % kTcKS]));
+        ok = ok && mbar_wait(smem_u32(&sh.q_full[qb1]), ((2 * n + 1) / kTcQB) & 1, abort_flag);
+        if (ok) {
+          tc::fence_after();
+          issue_s(1, kt, qb1);
+          tc::commit(smem_u32(&sh.k_empty[kt % kTcKS]));
         }
+        for (int j = 0; j < it.n_tiles && ok; ++j, ++tiles) {
+          const bool last = j == it.n_tiles - 1;
+          if (!mbar_wait(smem_u32(&sh.v_full[vt % kTcVS]), (vt / kTcVS) & 1, abort_flag) ||
+              !mbar_wait(smem_u32(&sh.p_full[0]), tiles & 1, abort_flag) ||
+              (j == 0 && n > 0 &&
+               !mbar_wait(smem_u32(&sh.o_free[0]), (n - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          issue_pv(0, vt, j > 0);
+          if (last) {
+            tc::commit(smem_u32(&sh.o_done[0]));
+          } else {
+            if (!mbar_wait(smem_u32(&sh.k_full[(kt + 1) % kTcKS]), ((kt + 1) / kTcKS) & 1,
+                           abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after();
+            issue_s(0, kt + 1, qb0);
+          }
+          if (!mbar_wait(smem_u32(&sh.p_full[1]), tiles & 1, abort_flag) ||
+              (j == 0 && n > 0 &&
+               !mbar_wait(smem_u32(&sh.o_free[1]), (n - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          issue_pv(1, vt, j > 0);
+          tc::commit(smem_u32(&sh.v_empty[vt % kTcVS]));
+          ++vt;
+          if (last) {
+            tc::commit(smem_u32(&sh.o_done[1]));
+          } else {
+            issue_s(1, kt + 1, qb1);
+            tc::commit(smem_u32(&sh.k_empty[(kt + 1) % kTcKS]));
+            ++kt;
+          }
+        }
+        ++kt;
+        ++n;
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+#undef issue_s
+#undef issue_pv
+    if (lane == 0) {
       // every MMA this thread issued is done before TMEM is released
       tc::commit(smem_u32(&sh.mma_drain));
       if (!mbar_drain(smem_u32(&sh.mma_drain), 0)) *abort_flag = 1;
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------- softmax
-    const int a = (warp - 2) >> 2;  // query tile of this warpgroup
+    // ------------------------------------------------- softmax, epilogue
+    const int a = (warp - 2) >> 2;  // query tile of this warpgroup (warps 2-5, 6-9)
     const int row = 32 * (warp & 3) + lane;
+    const int wtid = row;           // thread index inside the warpgroup
+    const bool leader = (warp & 3) == 2 && lane == 0;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t colS = a * 128, colO = 256 + a * 128;
-    const int t = t0 + a * tpt + row / P.group;
-    int p = -1;
-    if (row < rows_used && t < P.T) {
-      p = P.positions[(size_t)b * P.T + t];
-      if (p >= cap) {
-        report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
-        p = -1;
-      }
-    }
-    const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
     const float sc = P.scale_log2;
-    float m_used = -INFINITY, l = 0.f;  // running max of the scores in log2 units
+    uint32_t tiles = 0, n = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!mbar_wait(smem_u32(&sh.s_full[a]), j & 1, abort_flag)) { ok = false; break; }
-      tc::fence_after();
-      const int key0 = (tile0 + j) * kBN;
-      const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
-      const bool all_live = __all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1);
-      // the tile's 128 scores of this row: four loads, one wait
-      float s[kBN];
-#pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) tc::ld32(tmem + lane_base + colS + q * 32, s + q * 32);
-      tc::wait_ld();
-      if (!all_live) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) s[c] = (c >= cmin && c <= cmax) ? s[c] : -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
-#pragma unroll
-      for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[c + i], s[c + 8 + i]);
-      const float mt =
-          max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sc;
-      const bool need = l > 0.f && mt > m_used + kRescaleLog2;
-      float corr = 1.f;
-      if (need) {
-        corr = fast_exp2(m_used - mt);
-        m_used = mt;
-      }
-      if (m_used == -INFINITY) m_used = mt;  // first live key of this row
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-      // P = fp16(exp2(s*sc - base)), keys 2c and 2c+1 in column c; the sum
-      // takes the same rounded values
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = fast_exp2(fmaf(s[q * 32 + 2 * i], sc, -base));
-          const float x1 = fast_exp2(fmaf(s[q * 32 + 2 * i + 1], sc, -base));
-          pk[i] = pack_f16x2(x0, x1);
-          float r0, r1;
-          unpack_f16x2(pk[i], r0, r1);
-          ls[i & 3] += r0 + r1;
+    for (uint32_t seq = 0; ok; ++seq) {
+      const int idx = tc_fetch(sh, seq, counter, n_items, abort_flag);
+      if (idx < 0) break;
+      const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
+      const int ta0 = it.t0 + a * tpt;  // first token of this tile
+      if (it.rg.kmax < 0) {
+        // no live token in the pair: the outputs are 0 (coalesced, one row per warp step)
+        for (int e = wtid; e < rows_used * 32; e += 128) {
+          const int r = e >> 5, c = (e & 31) * 4, t = ta0 + r / P.group;
+          if (t < P.T)
+            *reinterpret_cast<float4*>(P.out + (((size_t)it.b * P.T + t) * P.h_q +
+                                                (size_t)it.g * P.group + r % P.group) *
+                                                   128 +
+                                       c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        tc::st16(tmem + lane_base + colS + q * 16, pk);
+        continue;
       }
-      l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      if (__any_sync(0xffffffffu, need)) {
-        // PV_a(j-1) is complete (S_a(j) was issued after it) and PV_a(j)
-        // waits for this tile's P: rescale O_a now
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float o[32];
-          tc::ld32(tmem + lane_base + colO + q * 32, o);
-          tc::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tc::st32(tmem + lane_base + colO + q * 32, o);
+      const int t = ta0 + row / P.group;
+      int p = -1;
+      if (row < rows_used && t < P.T) {
+        p = P.positions[(size_t)it.b * P.T + t];
+        if (p >= cap) {
+          report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
+          p = -1;
         }
       }
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[a]));
-    }
-    // epilogue: O / l, staged in shared memory that the finished tile no
-    // longer needs (tile 0: the K ring, free once O_0 is done because every S
-    // MMA was issued before PV_0 of the last tile; tile 1: the Q tiles) as
-    // four 128-byte-swizzled quarters of d, then written by TMA stores whose
-    // box is the tile's (d quarter, heads of the group, tokens), clipped at T
-    const bool have = ok && mbar_wait(smem_u32(&sh.o_done[a]), 0, abort_flag);
-    const uint32_t stage = a == 0 ? sK : sQ;
-    if (have) {
-      tc::fence_after();
+      const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
+      float m_used = -INFINITY, l = 0.f;  // running max of the scores in log2 units
+      for (int j = 0; j < it.n_tiles; ++j, ++tiles) {
+        if (!mbar_wait(smem_u32(&sh.s_full[a]), tiles & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        const int key0 = (it.tile0 + j) * kBN;
+        const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
+        const bool all_live = __all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1);
+        // the tile's 128 scores of this row: four loads, one wait
+        float s[kBN];
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) tc::ld32(tmem + lane_base + colS + q * 32, s + q * 32);
+        tc::wait_ld();
+        if (!all_live) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) s[c] = (c >= cmin && c <= cmax) ? s[c] : -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
+#pragma unroll
+        for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[c + i], s[c + 8 + i]);
+        const float mt =
+            max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sc;
+        const bool need = l > 0.f && mt > m_used + kRescaleLog2;
+        float corr = 1.f;
+        if (need) {
+          corr = fast_exp2(m_used - mt);
+          m_used = mt;
+        }
+        if (m_used == -INFINITY) m_used = mt;  // first live key of this row
+        const float base = m_used == -INFINITY ? 0.f : m_used;
+        // P = fp16(exp2(s*sc - base)), keys 2c and 2c+1 in column c; the sum
+        // takes the same rounded values
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = fast_exp2(fmaf(s[q * 32 + 2 * i], sc, -base));
+            const float x1 = fast_exp2(fmaf(s[q * 32 + 2 * i + 1], sc, -base));
+            pk[i] = pack_f16x2(x0, x1);
+            float r0, r1;
+            unpack_f16x2(pk[i], r0, r1);
+            ls[i & 3] += r0 + r1;
+          }
+          tc::st16(tmem + lane_base + colS + q * 16, pk);
+        }
+        l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        if (__any_sync(0xffffffffu, need)) {
+          // PV_a(j-1) is complete (S_a(j) was issued after it) and PV_a(j)
+          // waits for this tile's P: rescale O_a now (never at j = 0, where
+          // l is still 0)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float o[32];
+            tc::ld32(tmem + lane_base + colO + q * 32, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= corr;
+            tc::st32(tmem + lane_base + colO + q * 32, o);
+          }
+        }
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[a]));
+      }
+      if (!ok) break;
+      // epilogue: O / l.  The tile's own query buffer, free since its last S
+      // MMA, stages the output for TMA stores in two rounds of two
+      // 128-byte-swizzled d quarters (32 KiB each); then O_a is released to
+      // the next item's P.V and, after the second store has read it, the
+      // buffer to the query tile three steps later.
+      const uint32_t buf = (2 * n + a) % kTcQB, stage = sQ + buf * kTcQBytes;
       const float inv = (p >= 0 && l > 0.f) ? 1.f / l : 0.f;
-      float o[128];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tc::ld32(tmem + lane_base + colO + q * 32, o + q * 32);
-      tc::wait_ld();
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t adr = stage + q * 16384 + row * 128 + ((i ^ (row & 7)) << 4);
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(adr),
-                       "f"(o[q * 32 + 4 * i] * inv), "f"(o[q * 32 + 4 * i + 1] * inv),
-                       "f"(o[q * 32 + 4 * i + 2] * inv), "f"(o[q * 32 + 4 * i + 3] * inv)
-                       : "memory");
-        }
-    }
-    fence_proxy_async_smem();
-    named_barrier(1 + a, 128);  // every thread of the warpgroup gets here
-    if ((warp & 3) == 2 && lane == 0 && !*abort_flag) {
-      for (int q = 0; q < 4; ++q)
-        tma_store_4d(&omap, q * 32, g * P.group, t0 + a * tpt, b, stage + q * 16384);
-      bulk_commit_group();
-      bulk_wait_read_all();
+      ok = mbar_wait(smem_u32(&sh.o_done[a]), n & 1, abort_flag);
+      if (ok) tc::fence_after();
+      // round r: wait for the previous round's store to have read the
+      // staging area, move d quarters 2r, 2r+1 from TMEM to it one quarter at
+      // a time (after r = 1, release O_a), and let the leader store them
+#define TL_PREFILL_STAGE_ROUND(r)                                                              \
+  {                                                                                            \
+    const uint32_t R = 2 * n + (r); /* staging rounds of this warpgroup */                     \
+    if (R > 0 && !mbar_wait(smem_u32(&sh.stg_free[a]), (R - 1) & 1, abort_flag)) ok = false;   \
+    _Pragma("unroll") for (int qq = 0; qq < 2; ++qq) {                                         \
+      float o[32];                                                                             \
+      if (ok) {                                                                                \
+        tc::ld32(tmem + lane_base + colO + (2 * (r) + qq) * 32, o);                            \
+        tc::wait_ld();                                                                         \
+        _Pragma("unroll") for (int i = 0; i < 8; ++i) {                                        \
+          const uint32_t adr = stage + qq * 16384 + row * 128 + ((i ^ (row & 7)) << 4);        \
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(adr),                \
+                       "f"(o[4 * i] * inv), "f"(o[4 * i + 1] * inv), "f"(o[4 * i + 2] * inv),  \
+                       "f"(o[4 * i + 3] * inv)                                                 \
+                       : "memory");                                                            \
+        }                                                                                      \
+      }                                                                                        \
+    }                                                                                          \
+    if ((r) == 1) { /* O_a is out of TMEM: the next item's P.V may overwrite it */             \
+      tc::fence_before();                                                                      \
+      __syncwarp();                                                                            \
+      if (lane == 0) mbar_arrive(smem_u32(&sh.o_free[a]));                                     \
+    }                                                                                          \
+    fence_proxy_async_smem();                                                                  \
+    mbar_arrive(smem_u32(&sh.stg_full[a]));                                                    \
+    if (leader) {                                                                              \
+      if (mbar_wait(smem_u32(&sh.stg_full[a]), R & 1, abort_flag) && !*abort_flag) {           \
+        for (int qq = 0; qq < 2; ++qq)                                                         \
+          tma_store_4d(&omap, (2 * (r) + qq) * 32, it.g * P.group, ta0, it.b,                  \
+                       stage + qq * 16384);                                                    \
+        bulk_commit_group();                                                                   \
+        bulk_wait_read_all();                                                                  \
+      }                                                                                        \
+      mbar_arrive(smem_u32(&sh.stg_free[a]));                                                  \
+    }                                                                                          \
+  }
+      TL_PREFILL_STAGE_ROUND(0)
+      TL_PREFILL_STAGE_ROUND(1)
+#undef TL_PREFILL_STAGE_ROUND
+      if (leader) mbar_arrive(smem_u32(&sh.q_free[buf]));
+      ++n;
+      ok = ok && !*abort_flag;
     }
   }
   tc::fence_before();
@@ -573,8 +746,9 @@ extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv ||
       max_pages_per_seq <= 0 || page_size <= 0)
     return 0;
-  // the fp16 copy of V: [B][h_kv][max_pages_per_seq * page_size][d]
-  return (size_t)B * h_kv * ((size_t)max_pages_per_seq * page_size) * d * 2;
+  // a header (the attention kernel's work counter), then the fp16 copy of V:
+  // [B][h_kv][max_pages_per_seq * page_size][d]
+  return tl::kWsHeader + (size_t)B * h_kv * ((size_t)max_pages_per_seq * page_size) * d * 2;
 }
 
 extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
@@ -604,7 +778,8 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   if ((int64_t)max_pages_per_seq * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
   const size_t ws_need = tl_paged_attn_prefill_workspace_size(B, T, h_q, h_kv, d,
                                                               max_pages_per_seq, page_size);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_need) return TL_ERR_WORKSPACE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < ws_need)
+    return TL_ERR_WORKSPACE;
   PrefillParams P;
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
@@ -630,6 +805,8 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   const int tpt = 128 / group;
   const int box_rows = page_size % 16 == 0 ? 16 : 8;
   const int max_ctx = max_pages_per_seq * page_size;
+  int* counter = static_cast<int*>(workspace);
+  uint16_t* ws_v = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + kWsHeader);
   CUtensorMap qmap, kmap, vmap, omap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
@@ -650,17 +827,19 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
     if (!encode_f32_tensor_map(&omap, out, 4, od, os, ob, true)) return TL_ERR_CUDA;
     if (!encode_bf16_tensor_map(&qmap, q, 3, qd, qs, qb, true) ||
         !encode_bf16_tensor_map(&kmap, k_cache, 3, kd, ks, kb, true) ||
-        !encode_bf16_tensor_map(&vmap, workspace, 3, vd, vs, vb, true))
+        !encode_bf16_tensor_map(&vmap, ws_v, 3, vd, vs, vb, true))
       return TL_ERR_CUDA;
   }
   if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kTcSmem) != cudaSuccess)
     return TL_ERR_CUDA;
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
-  if ((int64_t)B * h_kv > 0x7fffffff || n_pairs > 65535) return TL_ERR_UNSUPPORTED;
+  const int64_t n_items = (int64_t)n_pairs * B * h_kv;
+  if (n_items > 0x7fffffff - 65536) return TL_ERR_UNSUPPORTED;
+  const int grid = (int)std::min<int64_t>(num_sms(), n_items);
   prefill_v_f16_kernel<<<dim3((max_ctx + kBN - 1) / kBN, B), kCvtThreads, 0,
-                         (cudaStream_t)stream>>>(P, static_cast<uint16_t*>(workspace), max_ctx);
-  prefill_tc_kernel<<<dim3(B * h_kv, n_pairs), kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
-      P, qmap, kmap, vmap, omap, box_rows);
+                         (cudaStream_t)stream>>>(P, ws_v, max_ctx, counter);
+  prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
+      P, qmap, kmap, vmap, omap, box_rows, counter);
   return launch_status();
 }
