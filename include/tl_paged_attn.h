@@ -171,11 +171,13 @@ tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const
                                        tl_dtype dtype, uint32_t* error_word, void* stream);
 
 /*
- * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes): a
- * 256-byte header (the kernel's work counter) and an fp16 copy of the V rows
- * the call reads, [B][h_kv][max_pages_per_seq * page_size][d], i.e.
- * 256 + B * h_kv * max_pages_per_seq * page_size * d * 2.  It does not
- * depend on T or h_q (they are taken for the shape checks only).
+ * Bytes of workspace tl_paged_attn_prefill needs (0 for invalid sizes): the
+ * kernel's work counter (256 bytes), the key-tile count and the schedule of
+ * every query-tile pair (two int32 arrays of B * n_pairs entries, each
+ * rounded up to 256 bytes; n_pairs = ceil(T / (2 * floor(128 / (h_q/h_kv))))),
+ * and an fp16 copy of the V rows the call reads,
+ * [B][h_kv][max_pages_per_seq * page_size][d] (B * h_kv * max_pages_per_seq *
+ * page_size * d * 2 bytes).
  */
 size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
                                             int32_t d, int32_t max_pages_per_seq,

@@ -70,6 +70,9 @@ struct PrefillParams {
   int32_t num_pages, page_size, window;
   float scale_log2;
   uint32_t* error_word;
+  int32_t n_pairs;       // query-tile pairs per row
+  int32_t* pair_tiles;   // [B][n_pairs] key tiles each pair reads (0: no live token)
+  int32_t* order;        // [B * n_pairs] pairs, most key tiles first
 };
 
 constexpr int kBN = 128;             // keys per tile
@@ -84,7 +87,23 @@ constexpr int kCvtThreads = 256;
 constexpr int kTcQBytes = 32768;     // one query tile: 128 rows x 128 d x bf16
 constexpr int kTcKVBytes = kBN * 256;  // 128 keys x 128 d x 16-bit (two 16 KiB halves)
 constexpr int kTcSmem = kTcQB * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
-constexpr size_t kWsHeader = 256;    // workspace bytes before the fp16 V copy (the item counter)
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 8192;   // key-tile counts at or above 8191 share the last bucket
+
+// Workspace layout: [counter | pair_tiles | order | fp16 V], each part
+// 256-byte aligned.
+struct WsLayout {
+  size_t tiles, order, v, total;
+};
+inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t max_ctx) {
+  const size_t pairs = (size_t)(B * n_pairs) * 4;
+  WsLayout L;
+  L.tiles = 256;
+  L.order = L.tiles + align_up(pairs, 256);
+  L.v = L.order + align_up(pairs, 256);
+  L.total = L.v + (size_t)B * h_kv * (size_t)max_ctx * 128 * 2;
+  return L;
+}
 constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 // bf16 bit patterns (sign cleared) of the finite values fp16 cannot hold:
@@ -174,6 +193,30 @@ __global__ void __launch_bounds__(kCvtThreads)
   const int b = (int)blockIdx.y, k0 = (int)blockIdx.x * kBN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
+  if (blockIdx.x == 0) {
+    // the key tiles every query-tile pair of row b reads (the attention
+    // kernel's own range rule), for the heaviest-first order
+    const int span = 2 * (128 / P.group);
+    for (int qp = warp; qp < P.n_pairs; qp += kCvtThreads / 32) {
+      int kmin = INT32_MAX, kmax = -1;
+      for (int i = lane; i < span; i += 32) {
+        const int t = qp * span + i;
+        if (t >= P.T) break;
+        const int p = P.positions[(size_t)b * P.T + t];
+        if (p >= 0 && p < cap) {
+          kmin = min(kmin, (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0);
+          kmax = max(kmax, p);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+      }
+      if (lane == 0)
+        P.pair_tiles[(size_t)b * P.n_pairs + qp] = kmax >= 0 ? kmax / kBN - kmin / kBN + 1 : 0;
+    }
+  }
   int pmin = INT32_MAX, pmax = -1;
   for (int t = threadIdx.x; t < P.T; t += kCvtThreads) {
     const int p = P.positions[(size_t)b * P.T + t];
@@ -254,6 +297,45 @@ __global__ void __launch_bounds__(kCvtThreads)
     report(P.error_word, TL_DEVERR_VALUE_RANGE);
 }
 
+// ------------------------------------------------------------ plan --
+// One CTA: counting sort of the pairs by key tiles, most first (pairs with
+// no live token last), into P.order.  Ties keep no particular order; every
+// pair computes the same bits whichever CTA takes it and when.
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PrefillParams P) {
+  __shared__ int cur[kPlanBuckets];  // counts, then each bucket's next slot
+  __shared__ int part[kPlanThreads];
+  constexpr int kPer = kPlanBuckets / kPlanThreads;  // buckets per thread
+  const int tid = threadIdx.x, n_e = P.B * P.n_pairs;
+  for (int k = tid; k < kPlanBuckets; k += kPlanThreads) cur[k] = 0;
+  __syncthreads();
+  for (int e = tid; e < n_e; e += kPlanThreads)
+    atomicAdd(&cur[min(P.pair_tiles[e], kPlanBuckets - 1)], 1);
+  __syncthreads();
+  // slots go to the buckets from the top down: thread t owns buckets
+  // [kPer t, kPer t + kPer); part = the pairs in buckets above its own
+  int local = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) local += cur[kPer * tid + i];
+  part[kPlanThreads - 1 - tid] = local;  // reversed: a prefix sum runs from the top
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int v = tid >= off ? part[tid - off] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int above = part[kPlanThreads - 1 - tid] - local;  // pairs in higher buckets
+#pragma unroll
+  for (int i = kPer - 1; i >= 0; --i) {
+    const int k = kPer * tid + i, c = cur[k];
+    cur[k] = above;
+    above += c;
+  }
+  __syncthreads();
+  for (int e = tid; e < n_e; e += kPlanThreads)
+    P.order[atomicAdd(&cur[min(P.pair_tiles[e], kPlanBuckets - 1)], 1)] = e;
+}
+
 // S_a = Q_a K^T into TMEM columns [128a, 128a+128): eight K=16 steps over
 // the 128-byte-swizzled K-major Q and K tiles; then a commit to s_full_a.
 __device__ __forceinline__ void tc_issue_s(uint32_t tmem, int a, uint32_t kbase, uint32_t qbase,
@@ -277,10 +359,9 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t tmem, int a, uint32_t vbase
                tc::sdesc(vbase + k * 2048, kTcKVBytes / 2, 1024), idPV, (acc || k > 0) ? 1u : 0u);
 }
 
-// One work item: a pair of query tiles of one row and KV head.  Items are
-// numbered heaviest first (the latest pairs of every row and head, whose
-// tokens see the most keys, come first); every warp decodes the same item
-// itself (tc_tile_range is warp-wide).
+// One work item: a pair of query tiles of one row and KV head.  Item idx is
+// KV head idx % h_kv of pair order[idx / h_kv] (pairs most key tiles first);
+// every warp decodes the same item itself (tc_tile_range is warp-wide).
 struct TcItem {
   int b, g, t0, tile0, n_tiles;
   TcRange rg;
@@ -289,10 +370,10 @@ struct TcItem {
 __device__ __forceinline__ TcItem tc_item(const PrefillParams& P, int idx, int tpt, int n_pairs,
                                           int64_t cap) {
   TcItem it;
-  const int bh = P.B * P.h_kv;
-  const int qp = n_pairs - 1 - idx / bh, r = idx % bh;
-  it.b = r / P.h_kv;
-  it.g = r % P.h_kv;
+  const int e = P.order[idx / P.h_kv];
+  const int qp = e % n_pairs;
+  it.b = e / n_pairs;
+  it.g = idx % P.h_kv;
   it.t0 = qp * 2 * tpt;
   it.rg = tc_tile_range(P, it.b, it.t0, 2 * tpt, cap);
   it.tile0 = it.rg.kmax >= 0 ? it.rg.kmin / kBN : 0;
@@ -746,9 +827,11 @@ extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv ||
       max_pages_per_seq <= 0 || page_size <= 0)
     return 0;
-  // a header (the attention kernel's work counter), then the fp16 copy of V:
-  // [B][h_kv][max_pages_per_seq * page_size][d]
-  return tl::kWsHeader + (size_t)B * h_kv * ((size_t)max_pages_per_seq * page_size) * d * 2;
+  // the work counter, the pairs' key-tile counts and order, then the fp16
+  // copy of V: [B][h_kv][max_pages_per_seq * page_size][d]
+  const int tpt = std::max(1, 128 / (h_q / h_kv));
+  const int64_t n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
+  return tl::ws_layout(B, n_pairs, h_kv, (int64_t)max_pages_per_seq * page_size).total;
 }
 
 extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
@@ -805,8 +888,14 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   const int tpt = 128 / group;
   const int box_rows = page_size % 16 == 0 ? 16 : 8;
   const int max_ctx = max_pages_per_seq * page_size;
-  int* counter = static_cast<int*>(workspace);
-  uint16_t* ws_v = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + kWsHeader);
+  const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
+  const WsLayout L = ws_layout(B, n_pairs, h_kv, max_ctx);
+  unsigned char* wsb = static_cast<unsigned char*>(workspace);
+  int* counter = reinterpret_cast<int*>(wsb);
+  uint16_t* ws_v = reinterpret_cast<uint16_t*>(wsb + L.v);
+  P.n_pairs = n_pairs;
+  P.pair_tiles = reinterpret_cast<int32_t*>(wsb + L.tiles);
+  P.order = reinterpret_cast<int32_t*>(wsb + L.order);
   CUtensorMap qmap, kmap, vmap, omap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
@@ -833,12 +922,12 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kTcSmem) != cudaSuccess)
     return TL_ERR_CUDA;
-  const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
   const int64_t n_items = (int64_t)n_pairs * B * h_kv;
   if (n_items > 0x7fffffff - 65536) return TL_ERR_UNSUPPORTED;
   const int grid = (int)std::min<int64_t>(num_sms(), n_items);
   prefill_v_f16_kernel<<<dim3((max_ctx + kBN - 1) / kBN, B), kCvtThreads, 0,
                          (cudaStream_t)stream>>>(P, ws_v, max_ctx, counter);
+  prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(P);
   prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
       P, qmap, kmap, vmap, omap, box_rows, counter);
   return launch_status();

@@ -47,10 +47,11 @@ def test_workspace_sizes(lib):
     assert tl.tl_paged_attn_decode_workspace_size(64, 32, 8, 128) > 0
     assert tl.tl_paged_attn_decode_workspace_size(64, 30, 8, 128) == 0  # h_q % h_kv
     assert tl.tl_paged_attn_decode_workspace_size(0, 32, 8, 128) == 0
-    # a 256-byte header, then the fp16 copy of V:
-    # B * h_kv * (max_pages_per_seq * page_size) * d * 2 bytes
+    # the work counter (256 B), two int32 arrays over the B * n_pairs query-tile
+    # pairs (n_pairs = 2048 / (2 * 128 / 4) = 32, each array rounded to 256 B),
+    # then the fp16 copy of V: B * h_kv * (max_pages_per_seq * page_size) * d * 2
     assert tl.tl_paged_attn_prefill_workspace_size(8, 2048, 32, 8, 128, 512, 16) == \
-        256 + 8 * 8 * 512 * 16 * 128 * 2
+        256 + 2 * 1024 + 8 * 8 * 512 * 16 * 128 * 2
     assert tl.tl_paged_attn_prefill_workspace_size(8, 2048, 32, 8, 128, 0, 16) == 0
     # the decode bound grows with B and h_q but not with context length
     a = tl.tl_paged_attn_decode_workspace_size(64, 32, 8, 128)
