@@ -33,6 +33,11 @@ HBM_FALLBACK_GBS = 6800.0
 BF16_FALLBACK_TFLOPS = 1900.0
 METRIC = "paged decode KV-read GB/s (% of HBM peak); prefill TFLOP/s (% TC peak)"
 WORKLOAD = "Llama-3-8B-shaped decode layer: B=64, Hq=32, Hkv=8, d=128, bf16, page 16, L~U[512,8192]"
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
+# these default workloads (the summaries under profiles/ give the command); they hold
+# only for the kernels as they were captured and for these workloads.
+DECODE_TRAFFIC = (1264400000 + 25200000, "profiles/decode_bf16_llama8b_b64.md")
+PREFILL_TRAFFIC = (336730880 + 207640320, "profiles/prefill_tc_batched_b8.md")
 
 
 def peaks():
@@ -281,7 +286,9 @@ def run_ours(args):
         "frac_of_hbm_peak": round(value / world / hbm, 4),
         "roofline": {"bound": "hbm", "kernel": "decode (plan + split-K bf16 kernel + combine)",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": DECODE_TRAFFIC[0] if B == 64 else None,
+                     "traffic_source": DECODE_TRAFFIC[1] + " (decode_bf16_kernel alone)",
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                      else "fallback", "algorithmic_bytes_per_launch": dec_alg,
                      "ms_per_launch": round(dec_ms, 5)},
@@ -355,7 +362,9 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
                     "Hq=32, Hkv=8, d=128, bf16",
         "tflops": round(pf_tflops, 2), "ms_per_call": round(pf_ms, 4), "flops_per_call": flops,
         "roofline": {"bound": "tensor", "achieved": round(pf_tflops, 2), "peak": bf16,
-                     "unit": "TFLOP/s", "frac": round(pf_tflops / bf16, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(pf_tflops / bf16, 4),
+                     "traffic": PREFILL_TRAFFIC[0],
+                     "traffic_source": PREFILL_TRAFFIC[1] + " (prefill_tc_kernel alone)",
                      "peak_source": f"{src} bf16_tflops (burst)",
                      "frac_of_sustained": round(pf_tflops / bf16_sus, 4)},
         "clocks": pclk.summary()}
