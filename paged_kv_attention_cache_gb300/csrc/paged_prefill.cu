@@ -176,21 +176,23 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 // ------------------------------------------------------- V pre-pass --
-// Grid (key tile of 128, row).  Each CTA first finds its row's live
+// Grid (64-key tile, row).  Each CTA first finds its row's live
 // positions [pmin, pmax]; the attention kernel reads V keys in
 // [start, end): start = the first key any live token can see, rounded down
-// to a tile, end = pmax + 1 rounded up to a tile (clamped to the workspace).
+// to its 128-key tile, end = pmax + 1 rounded up to a 128-key tile (clamped
+// to the workspace).
 // The tile's page numbers go to shared memory; then every thread moves
 // 16-byte units (key-major: one key's h_kv x 128 values are contiguous in
 // the pool), kCvtUnroll independent loads in flight.
-constexpr int kCvtUnroll = 8;
+constexpr int kCvtUnroll = 16;
+constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
 
 __global__ void __launch_bounds__(kCvtThreads)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int max_ctx, int* counter) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;  // work items
-  __shared__ int s_page[kBN];  // page of each key of the tile; -1: write zeros
-  const int b = (int)blockIdx.y, k0 = (int)blockIdx.x * kBN;
+  __shared__ int s_page[kCvtKeys];  // page of each key of the tile; -1: write zeros
+  const int b = (int)blockIdx.y, k0 = (int)blockIdx.x * kCvtKeys;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
   if (blockIdx.x == 0) {
@@ -218,8 +220,9 @@ __global__ void __launch_bounds__(kCvtThreads)
     }
   }
   int pmin = INT32_MAX, pmax = -1;
-  for (int t = threadIdx.x; t < P.T; t += kCvtThreads) {
-    const int p = P.positions[(size_t)b * P.T + t];
+#pragma unroll 8
+  for (int t = threadIdx.x; t < P.T; t += kCvtThreads) {  // eight loads in flight
+    const int p = __ldg(P.positions + (size_t)b * P.T + t);
     if (p >= 0 && p < cap) {
       pmin = min(pmin, p);
       pmax = max(pmax, p);
@@ -243,8 +246,8 @@ __global__ void __launch_bounds__(kCvtThreads)
   if (pmax < 0) return;  // no live token: the attention kernel reads nothing
   const int lo = (P.window > 0 && pmin - P.window + 1 > 0) ? pmin - P.window + 1 : 0;
   const int start = lo / kBN * kBN, end = min((pmax / kBN + 1) * kBN, max_ctx);
-  if (k0 + kBN <= start || k0 >= end) return;
-  for (int r = threadIdx.x; r < kBN; r += kCvtThreads) {
+  if (k0 + kCvtKeys <= start || k0 >= end) return;
+  for (int r = threadIdx.x; r < kCvtKeys; r += kCvtThreads) {
     const int k = k0 + r;
     int page = -1;  // keys past pmax: zeros
     if (k <= pmax) {
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kCvtThreads)
     s_page[r] = page;
   }
   __syncthreads();
-  const int r0 = max(start - k0, 0), r1 = min(end - k0, kBN);  // keys of the tile to write
+  const int r0 = max(start - k0, 0), r1 = min(end - k0, kCvtKeys);  // keys of the tile to write
   const int units = P.h_kv * 16;                                // 16-byte units per key
   const int total = (r1 - r0) * units;
   uint32_t vmax = 0;  // max |bf16 bits| seen, per half-word
@@ -925,7 +928,7 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   const int64_t n_items = (int64_t)n_pairs * B * h_kv;
   if (n_items > 0x7fffffff - 65536) return TL_ERR_UNSUPPORTED;
   const int grid = (int)std::min<int64_t>(num_sms(), n_items);
-  prefill_v_f16_kernel<<<dim3((max_ctx + kBN - 1) / kBN, B), kCvtThreads, 0,
+  prefill_v_f16_kernel<<<dim3((max_ctx + kCvtKeys - 1) / kCvtKeys, B), kCvtThreads, 0,
                          (cudaStream_t)stream>>>(P, ws_v, max_ctx, counter);
   prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(P);
   prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
