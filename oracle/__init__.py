@@ -66,12 +66,14 @@ def _load():
             lib.oracle_kv_cache_write.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64]
             lib.oracle_kv_cache_write.restype = ctypes.c_int
             lib.oracle_paged_decode.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
-                                                i32, i32, i32, f64, vp, i32, vp, i32]
+                                                i32, i32, i32, i32, f64, vp, i32, vp, i32]
             lib.oracle_paged_decode.restype = ctypes.c_int
             lib.oracle_paged_prefill.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
-                                                 i32, i32, i32, i32, f64, i32, i32, vp, i64, vp,
-                                                 i32]
+                                                 i32, i32, i32, i32, i32, f64, i32, i32, vp, i64,
+                                                 vp, i32]
             lib.oracle_paged_prefill.restype = ctypes.c_int
+            lib.oracle_ring_pages.argtypes = [i64, i64, i64]
+            lib.oracle_ring_pages.restype = i64
             lib.oracle_kv_bytes_per_token.argtypes = [i64, i64, i64, i64]
             lib.oracle_kv_bytes_per_token.restype = i64
             lib.oracle_max_threads.argtypes = []
@@ -140,8 +142,9 @@ def kv_cache_write(k_new, v_new, k_cache, v_cache, slot_mapping) -> None:
 
 
 def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale, window=0, seqs=None,
-                 threads=0) -> np.ndarray:
-    """out[i, h, :] for sequence seqs[i] (all sequences by default), float64 [n, H_q, d]."""
+                 threads=0, ring_pages=0) -> np.ndarray:
+    """out[i, h, :] for sequence seqs[i] (all sequences by default), float64 [n, H_q, d].
+    ring_pages > 0: the table's first ring_pages entries are each sequence's ring."""
     lib = _load()
     qa, kc, vc = _c(_np(q)), _c(_np(k_cache)), _c(_np(v_cache))
     bt = _c(_np(block_table), np.int32)
@@ -154,8 +157,8 @@ def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale, window=0
     sq = _c(np.arange(B) if seqs is None else np.asarray(seqs), np.int32)
     out = np.zeros((sq.shape[0], hq, d), dtype=np.float64)
     rc = lib.oracle_paged_decode(_ptr(qa), _ptr(kc), _ptr(vc), dt, _ptr(bt), bt.shape[1],
-                                 _ptr(cl), B, hq, hkv, d, P, ps, int(window), float(scale),
-                                 _ptr(sq), sq.shape[0], _ptr(out), int(threads))
+                                 _ptr(cl), B, hq, hkv, d, P, ps, int(window), int(ring_pages),
+                                 float(scale), _ptr(sq), sq.shape[0], _ptr(out), int(threads))
     if rc != 0:
         raise OracleError(f"oracle_paged_decode failed ({rc})")
     return out
@@ -163,8 +166,9 @@ def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale, window=0
 
 def paged_prefill(q, k_cache, v_cache, block_table, positions, scale, window=0,
                   blockwise=True, key_block=DEFAULT_KEY_BLOCK, tokens=None,
-                  threads=0) -> np.ndarray:
-    """out[i, h, :] for flat token tokens[i] = b*T + t (all by default), float64."""
+                  threads=0, ring_pages=0) -> np.ndarray:
+    """out[i, h, :] for flat token tokens[i] = b*T + t (all by default), float64.
+    ring_pages > 0: the table's first ring_pages entries are each row's ring."""
     lib = _load()
     qa, kc, vc = _c(_np(q)), _c(_np(k_cache)), _c(_np(v_cache))
     bt = _c(_np(block_table), np.int32)
@@ -177,8 +181,9 @@ def paged_prefill(q, k_cache, v_cache, block_table, positions, scale, window=0,
     tk = _c(np.arange(B * T) if tokens is None else np.asarray(tokens), np.int64)
     out = np.zeros((tk.shape[0], hq, d), dtype=np.float64)
     rc = lib.oracle_paged_prefill(_ptr(qa), _ptr(kc), _ptr(vc), dt, _ptr(bt), bt.shape[1],
-                                  _ptr(pos), B, T, hq, hkv, d, P, ps, int(window), float(scale),
-                                  1 if blockwise else 0, int(key_block), _ptr(tk), tk.shape[0],
+                                  _ptr(pos), B, T, hq, hkv, d, P, ps, int(window), int(ring_pages),
+                                  float(scale), 1 if blockwise else 0, int(key_block), _ptr(tk),
+                                  tk.shape[0],
                                   _ptr(out), int(threads))
     if rc != 0:
         raise OracleError(f"oracle_paged_prefill failed ({rc})")
@@ -188,3 +193,9 @@ def paged_prefill(q, k_cache, v_cache, block_table, positions, scale, window=0,
 def kv_bytes_per_token(layers: int, h_kv: int, d_head: int, bytes_per_elem: int) -> int:
     """M_KV/token = 2 * layers * H_kv * d_head * q."""
     return int(_load().oracle_kv_bytes_per_token(layers, h_kv, d_head, bytes_per_elem))
+
+
+def ring_pages(window: int, chunk: int, page_size: int) -> int:
+    """Ring pages for calls of up to `chunk` tokens with window `window`:
+    ceil((window - 1 + chunk) / page_size)."""
+    return int(_load().oracle_ring_pages(window, chunk, page_size))

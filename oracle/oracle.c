@@ -18,6 +18,12 @@
  *     position + 1 (section 1);
  *   - the sliding window (section 3, "Sliding-window layers"): with window W
  *     only positions p-W+1..p are read;
+ *   - the ring (section 2, the bullet on sliding layers whose table is a
+ *     ring; section 3, the windowed KV pool): the first ring_pages entries of
+ *     the table are a ring of N = ring_pages * page_size slots, logical block
+ *     b living on ring page b % ring_pages; slot i holds the position
+ *     (L - 1 - i) mod N behind the row's last one, and is read when that age
+ *     is less than the window and less than L;
  *   - the blockwise form (section 2, "Blockwise attention"): the same result
  *     folded over key blocks of 2,048 positions with a running max, a running
  *     sum and a running P.V;
@@ -191,6 +197,41 @@ static int attend_blockwise(const paged_seq* s, const double* q, int64_t lo, int
   return err;
 }
 
+/* Ring form: the N slots of the ring are visited in slot order; slot i holds
+ * position last - ((last - i) mod N), where last is the row's last written
+ * position, and is read when that position lies in lo..p (for a decode query,
+ * p = last: the slot's age (last - i) mod N is below the window and below
+ * L = last + 1).  One pass: scores, max, softmax, weighted sum of values.
+ * Slot i is logical position i of the ring's table entries. */
+static int attend_ring(const paged_seq* s, const double* q, int64_t lo, int64_t p,
+                       int64_t last, int64_t n_slots, int64_t g, double scale, double* out) {
+  const int64_t d = s->d;
+  for (int64_t e = 0; e < d; ++e) out[e] = 0.0;
+  if (p < lo) return OR_OK;
+  double* sc = (double*)malloc((size_t)n_slots * sizeof(double));
+  if (!sc) return OR_NO_MEM;
+  int err = OR_OK;
+  double m = -INFINITY;
+  for (int64_t i = 0; i < n_slots; ++i) {
+    const int64_t age = ((last - i) % n_slots + n_slots) % n_slots;
+    const int64_t pos = last - age;
+    if (pos < lo || pos > p) { sc[i] = -INFINITY; continue; }
+    sc[i] = score(s, q, i, g, scale, &err);
+    if (sc[i] > m) m = sc[i];
+  }
+  double l = 0.0;
+  for (int64_t i = 0; i < n_slots; ++i) {
+    if (sc[i] == -INFINITY) continue;
+    const double w = exp(sc[i] - m);
+    l += w;
+    add_weighted_value(s, i, g, w, out, &err);
+  }
+  if (l > 0.0)
+    for (int64_t e = 0; e < d; ++e) out[e] /= l;
+  free(sc);
+  return err;
+}
+
 static int64_t window_lo(int64_t p, int64_t window) {
   if (window <= 0) return 0;
   const int64_t lo = p - window + 1;
@@ -215,16 +256,19 @@ int oracle_max_threads(void) {
 
 /* Decode: one query token per sequence; sequence b has causal length
  * context_lens[b] (its query sits at position context_lens[b] - 1).
+ * ring_pages > 0: the table's first ring_pages entries are the sequence's
+ * ring (attend_ring); 0: full history.
  * Computes the sequences listed in seqs[0..n_seqs) into out[n_seqs][H_q][d]. */
 int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
                         int32_t dtype, const int32_t* block_table,
                         int32_t max_pages_per_seq, const int32_t* context_lens,
                         int32_t B, int32_t h_q, int32_t h_kv, int32_t d,
                         int32_t num_pages, int32_t page_size, int32_t window,
-                        double scale, const int32_t* seqs, int32_t n_seqs, double* out,
-                        int32_t n_threads) {
+                        int32_t ring_pages, double scale, const int32_t* seqs, int32_t n_seqs,
+                        double* out, int32_t n_threads) {
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 || page_size <= 0 ||
-      num_pages <= 0 || max_pages_per_seq <= 0 || (dtype != OR_F32 && dtype != OR_BF16))
+      num_pages <= 0 || max_pages_per_seq <= 0 || (dtype != OR_F32 && dtype != OR_BF16) ||
+      ring_pages < 0 || ring_pages > max_pages_per_seq)
     return OR_BAD_ARG;
   for (int32_t i = 0; i < n_seqs; ++i)
     if (seqs[i] < 0 || seqs[i] >= B) return OR_BAD_ARG;
@@ -241,7 +285,10 @@ int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
     if (!qv) { status = OR_NO_MEM; continue; }
     for (int64_t e = 0; e < d; ++e) qv[e] = widen(q, (b * h_q + h) * d + e, dtype);
     const int64_t p = (int64_t)context_lens[b] - 1;
-    const int rc = attend_one_pass(&s, qv, window_lo(p, window), p, g, scale, o);
+    const int rc = ring_pages > 0
+                       ? attend_ring(&s, qv, window_lo(p, window), p, p,
+                                     (int64_t)ring_pages * page_size, g, scale, o)
+                       : attend_one_pass(&s, qv, window_lo(p, window), p, g, scale, o);
     if (rc != OR_OK) status = rc;
     free(qv);
   }
@@ -253,6 +300,9 @@ int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
  * blockwise = 0: one-pass form; otherwise the blockwise fold over key blocks of
  * key_block positions, visiting the call's block range from the first block
  * any row can see to the block holding the call's last position.
+ * ring_pages > 0: the table's first ring_pages entries are the row's ring and
+ * every token reads it in one pass (attend_ring), relative to the row's last
+ * live position (blockwise is then ignored).
  * Computes the tokens listed (as b*T+t) in tokens[0..n_tokens) into
  * out[n_tokens][H_q][d]. */
 int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache,
@@ -260,12 +310,13 @@ int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache
                          int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
                          int32_t T, int32_t h_q, int32_t h_kv, int32_t d,
                          int32_t num_pages, int32_t page_size, int32_t window,
-                         double scale, int32_t blockwise, int32_t key_block,
+                         int32_t ring_pages, double scale, int32_t blockwise, int32_t key_block,
                          const int64_t* tokens, int64_t n_tokens, double* out,
                          int32_t n_threads) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 ||
       page_size <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 ||
-      (dtype != OR_F32 && dtype != OR_BF16) || (blockwise && key_block <= 0))
+      (dtype != OR_F32 && dtype != OR_BF16) || (blockwise && key_block <= 0) ||
+      ring_pages < 0 || ring_pages > max_pages_per_seq)
     return OR_BAD_ARG;
   for (int64_t i = 0; i < n_tokens; ++i)
     if (tokens[i] < 0 || tokens[i] >= (int64_t)B * T) return OR_BAD_ARG;
@@ -296,7 +347,12 @@ int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache
     const int64_t p = positions[bt_idx];
     const int64_t lo = window_lo(p, window);
     int rc;
-    if (!blockwise || p < 0)
+    if (ring_pages > 0) {
+      int64_t last = -1; /* the row's last live position */
+      for (int64_t t = 0; t < T; ++t)
+        if (positions[b * T + t] > last) last = positions[b * T + t];
+      rc = attend_ring(&s, qv, lo, p, last, (int64_t)ring_pages * page_size, g, scale, o);
+    } else if (!blockwise || p < 0)
       rc = attend_one_pass(&s, qv, lo, p, g, scale, o);
     else
       rc = attend_blockwise(&s, qv, lo, p, g, scale, key_block, kb_first, kb_last, o);
@@ -316,3 +372,13 @@ int64_t oracle_kv_bytes_per_token(int64_t layers, int64_t h_kv, int64_t d_head,
 }
 
 int64_t oracle_elem_size(int32_t dtype) { return elem_size(dtype); }
+
+/* Ring pages a windowed pool needs so that a call writing up to `chunk` tokens
+ * fits past the window (section 3 and section 4 of "How serving works in
+ * Tlaloc"): a call of n tokens at p0 needs min(p0, W-1) + n positions at once,
+ * so the ring is ceil((W - 1 + chunk) / page_size) pages; a decode step
+ * (chunk = 1) needs ceil(W / page_size). */
+int64_t oracle_ring_pages(int64_t window, int64_t chunk, int64_t page_size) {
+  if (window <= 0 || chunk <= 0 || page_size <= 0) return -1;
+  return (window - 1 + chunk + page_size - 1) / page_size;
+}

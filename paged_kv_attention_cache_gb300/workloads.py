@@ -224,6 +224,87 @@ def prefill_case(pads, p0, *, T, Hq, Hkv, d, page_size=16, dtype=torch.bfloat16,
                        pool, k_cache, v_cache, q, k_new, v_new, slots)
 
 
+@dataclass
+class RingCase:
+    """The same K/V history of B sequences in two layouts: a full-history pool
+    (every position 0..L-1 on its own slot) and a ring pool of ring_pages pages
+    per sequence, where logical block k sits on ring page k % ring_pages, so a
+    later position overwrites the one ring_pages * page_size behind it.  The
+    ring table is as wide as the full one: entry k holds the ring page of
+    block k.  ring_slots / full_slots: where each sequence's last position
+    (the new token) lives in each layout."""
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    page_size: int
+    dtype: torch.dtype
+    window: int
+    ring_pages: int
+    scale: float
+    context_lens: torch.Tensor  # [B] int32
+    q: torch.Tensor  # [B, Hq, d]
+    full_k: torch.Tensor
+    full_v: torch.Tensor
+    full_table: torch.Tensor  # [B, width] int32
+    ring_k: torch.Tensor
+    ring_v: torch.Tensor
+    ring_table: torch.Tensor  # [B, width] int32
+    full_slots: torch.Tensor  # [B] int64
+    ring_slots: torch.Tensor  # [B] int64
+    k_new: torch.Tensor  # [B, Hkv, d]: the last position's K and V
+    v_new: torch.Tensor
+
+
+def ring_case(lengths, *, window, ring_pages, Hq, Hkv, d, page_size=16,
+              dtype=torch.bfloat16, seed=0, device="cpu", outlier_p=0.0) -> RingCase:
+    """Seeded histories in both layouts (see RingCase)."""
+    g = _gen(seed, device)
+    lengths = [int(x) for x in lengths]
+    B = len(lengths)
+    pool = make_pool(lengths, page_size, g)
+    width = pool.block_table.shape[1]
+    if ring_pages > width:
+        raise ValueError("ring_pages is wider than the full table")
+    full_k = torch.zeros((pool.num_pages, page_size, Hkv, d), dtype=dtype, device=device)
+    full_v = torch.zeros_like(full_k)
+    n_ring = B * ring_pages
+    ring_k = torch.zeros((n_ring, page_size, Hkv, d), dtype=dtype, device=device)
+    ring_v = torch.zeros_like(ring_k)
+    perm = torch.randperm(n_ring, generator=g, device=g.device).cpu()
+    ring_of = perm.view(B, ring_pages)
+    ring_table = torch.empty((B, width), dtype=torch.int32)
+    for k in range(width):
+        ring_table[:, k] = ring_of[:, k % ring_pages].to(torch.int32)
+    n_slots = ring_pages * page_size
+    full_slots, ring_slots, k_last, v_last = [], [], [], []
+    for b, L in enumerate(lengths):
+        hk = _randn((L, Hkv, d), dtype, g, device, outlier_p)
+        hv = _randn((L, Hkv, d), dtype, g, device, outlier_p)
+        pos = torch.arange(L)
+        fs = torch.tensor(pool.pages_of[b], dtype=torch.int64)[pos // page_size] * page_size + \
+            pos % page_size
+        full_k.view(-1, Hkv, d)[fs.to(device)] = hk
+        full_v.view(-1, Hkv, d)[fs.to(device)] = hv
+        # the ring keeps the last n_slots positions (older ones were overwritten)
+        keep = pos[max(0, L - n_slots):]
+        rs = ring_of[b][(keep // page_size) % ring_pages].to(torch.int64) * page_size + \
+            keep % page_size
+        ring_k.view(-1, Hkv, d)[rs.to(device)] = hk[keep.to(device)]
+        ring_v.view(-1, Hkv, d)[rs.to(device)] = hv[keep.to(device)]
+        full_slots.append(int(fs[-1]) if L else -1)
+        ring_slots.append(int(rs[-1]) if L else -1)
+        k_last.append(hk[-1] if L else torch.zeros((Hkv, d), dtype=dtype, device=device))
+        v_last.append(hv[-1] if L else torch.zeros((Hkv, d), dtype=dtype, device=device))
+    q = _randn((B, Hq, d), dtype, g, device, outlier_p)
+    return RingCase(B, Hq, Hkv, d, page_size, dtype, window, ring_pages, 1.0 / math.sqrt(d),
+                    torch.tensor(lengths, dtype=torch.int32), q, full_k, full_v,
+                    pool.block_table.clone(), ring_k, ring_v, ring_table,
+                    torch.tensor(full_slots, dtype=torch.int64),
+                    torch.tensor(ring_slots, dtype=torch.int64),
+                    torch.stack(k_last), torch.stack(v_last))
+
+
 # ----------------------------------------------------------------- presets --
 
 def tiny_decode(seed=0, device="cpu") -> DecodeCase:

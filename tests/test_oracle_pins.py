@@ -354,3 +354,100 @@ def test_kv_bytes_per_token_matches_the_pages():
         mha = oracle.kv_bytes_per_token(32, e["h_q"], 128, 2)
         gqa = oracle.kv_bytes_per_token(32, e["h_kv"], 128, 2)
         assert mha // gqa == e["expected_ratio"] and mha % gqa == 0, e["source"]
+
+
+# -------------------------------------------------------------------- ring --
+# A sliding layer whose table is a ring reads only the ring ("How serving works
+# in Tlaloc", section 2, the bullet on sliding layers; section 3, the windowed
+# KV pool).  The ring layout below is built by the test from the contiguous
+# histories (position j on ring page (j // ps) % R at offset j % ps, later
+# positions overwriting earlier ones) and checked against dense attention
+# over the histories: independent of the oracle's page arithmetic.
+
+def _ring_layout(case, ring_pages, seed=0):
+    """(k_ring, v_ring, ring_table) holding the last ring_pages * ps positions
+    of every history, stored like the case's pool; the table is as wide as the
+    full one (entry k holds the ring page of block k)."""
+    rng = np.random.default_rng(seed)
+    B, ps = len(case.lengths), case.page_size
+    n_slots = ring_pages * ps
+    perm = rng.permutation(B * ring_pages).reshape(B, ring_pages)
+    width = max(case.block_table.shape[1], ring_pages)
+    table = np.stack([perm[b][np.arange(width) % ring_pages] for b in range(B)]).astype(np.int32)
+    kr = np.zeros((B * ring_pages, ps) + case.k_cache.shape[2:], dtype=case.k_cache.dtype)
+    vr = np.zeros_like(kr)
+    for b, L in enumerate(case.lengths):
+        for j in range(max(0, L - n_slots), L):  # the positions still in the ring
+            src_pg, dst_pg = case.pages_of[b][j // ps], perm[b][(j // ps) % ring_pages]
+            kr[dst_pg, j % ps] = case.k_cache[src_pg, j % ps]
+            vr[dst_pg, j % ps] = case.v_cache[src_pg, j % ps]
+    return kr, vr, table
+
+
+@pytest.mark.parametrize("window,ring_pages", [(20, 3), (20, 4), (32, 4), (7, 1), (40, 6)])
+def test_ring_decode_equals_dense_over_the_window(window, ring_pages):
+    lengths = [100, 37, 8, 1, 61]  # several wraps of the ring, and no wrap at all
+    case = history_case(lengths, Hq=4, Hkv=2, d=16, page_size=8, seed=21)
+    assert ring_pages * case.page_size >= window
+    kr, vr, table = _ring_layout(case, ring_pages)
+    q_st, q_vals = _queries(case, len(lengths), 22)
+    out = oracle.paged_decode(q_st, kr, vr, table, lengths, case.scale, window=window,
+                              ring_pages=ring_pages)
+    for b, L in enumerate(lengths):
+        ref = dense_reference(case, q_vals[b], b, L - 1, window)
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ring_one_page_short_changes_the_result():
+    # negative control: a ring that cannot hold the window has overwritten
+    # the window's oldest positions
+    lengths = [100, 61, 12]
+    window, ring_pages = 20, 2  # 16 slots < 20
+    case = history_case(lengths, Hq=4, Hkv=2, d=16, page_size=8, seed=23)
+    kr, vr, table = _ring_layout(case, ring_pages)
+    q_st, q_vals = _queries(case, len(lengths), 24)
+    out = oracle.paged_decode(q_st, kr, vr, table, lengths, case.scale, window=window,
+                              ring_pages=ring_pages)
+    for b, L in enumerate(lengths):
+        ref = dense_reference(case, q_vals[b], b, L - 1, window)
+        if L > ring_pages * case.page_size:
+            assert np.abs(out[b] - ref).max() > 1e-3
+        else:
+            np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ring_prefill_chunk_equals_dense_and_needs_its_pages():
+    # a call of n tokens at p0 needs min(p0, W - 1) + n positions of ring
+    window, n, ps = 24, 10, 8
+    p0 = [50, 5]  # the second row has not filled a window yet
+    lengths = [p + n for p in p0]
+    case = history_case(lengths, Hq=2, Hkv=1, d=16, page_size=ps, seed=25)
+    T = n
+    positions = np.array([[p + t for t in range(T)] for p in p0], dtype=np.int32)
+    rng = np.random.default_rng(26)
+    q_st, q_vals = round_to(rng.standard_normal((len(p0), T, case.Hq, case.d)), case.dtype)
+    need = oracle.ring_pages(window, n, ps)
+    assert need == -(-(window - 1 + n) // ps)
+    for ring_pages, ok in ((need, True), (need - 1, False)):
+        kr, vr, table = _ring_layout(case, ring_pages)
+        out = oracle.paged_prefill(q_st, kr, vr, table, positions, case.scale, window=window,
+                                   ring_pages=ring_pages).reshape(len(p0), T, case.Hq, case.d)
+        worst = 0.0
+        for b in range(len(p0)):
+            for t in range(T):
+                ref = dense_reference(case, q_vals[b, t], b, int(positions[b, t]), window)
+                worst = max(worst, float(np.abs(out[b, t] - ref).max()))
+        if ok:
+            assert worst <= 1e-12
+        else:
+            assert worst > 1e-3  # the first row's oldest window positions are gone
+
+
+def test_ring_sizes_match_the_pages():
+    with open(os.path.join(GOLDEN, "ring_sizing.json")) as f:
+        g = json.load(f)
+    for e in g["rings"]:
+        got = oracle.ring_pages(e["window"], e["chunk"], e["page_size"])
+        assert got == e["expected_pages"], e["source"]
+        if "default_pages" in e:
+            assert got + 1 == e["default_pages"], e["source"]
