@@ -175,9 +175,9 @@ tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const
  * kernel's work counter (256 bytes), the key-tile count and the schedule of
  * every query-tile pair (two int32 arrays of B * n_pairs entries, each
  * rounded up to 256 bytes; n_pairs = ceil(T / (2 * floor(128 / (h_q/h_kv))))),
- * and an fp16 copy of the V rows the call reads,
- * [B][h_kv][max_pages_per_seq * page_size][d] (B * h_kv * max_pages_per_seq *
- * page_size * d * 2 bytes).
+ * each row's first key (B int32, rounded up to 256 bytes), and an fp16 copy of
+ * the V rows the call reads, [B][h_kv][max_pages_per_seq * page_size][d]
+ * (B * h_kv * max_pages_per_seq * page_size * d * 2 bytes).
  */
 size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
                                             int32_t d, int32_t max_pages_per_seq,
@@ -221,6 +221,49 @@ tl_status tl_paged_attn_prefill(const void* q, const void* k_cache, const void* 
                                 int32_t page_size, int32_t window, float scale, tl_dtype dtype,
                                 void* workspace, size_t workspace_bytes, uint32_t* error_word,
                                 void* stream);
+
+/*
+ * Sliding-window attention over a ring ("How serving works in Tlaloc",
+ * section 2, the bullet on sliding layers whose table is a ring; section 3,
+ * the windowed KV pool).  Each sequence holds a ring of ring_pages pages:
+ * logical block k lives on the page block_table[b][k % ring_pages], so
+ * position p overwrites position p - ring_pages * page_size, which has left
+ * the window; the caller's slot_mapping for tl_kv_cache_write follows the
+ * same rule.  Only the first ring_pages entries of each table row are read,
+ * and positions / context lengths are not bounded by the table's width.
+ * Keys are visited in position order, so the result is bit-identical to the
+ * same call over a full-history table.
+ * The ring must hold the window: 0 < ring_pages <= max_pages_per_seq,
+ * window > 0 and ring_pages * page_size >= window; otherwise
+ * TL_ERR_INVALID_ARG.  For prefill, a call of n tokens starting at position
+ * p0 needs min(p0, window - 1) + n positions of ring; a row whose call spans
+ * more sets TL_DEVERR_CONTEXT_RANGE (its outputs are undefined).
+ * All other arguments, layouts and errors as for tl_paged_attn_decode /
+ * tl_paged_attn_prefill.
+ */
+tl_status tl_paged_attn_decode_ring(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_table, int32_t max_pages_per_seq,
+                                    const int32_t* context_lens, float* out, int32_t B,
+                                    int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                    int32_t page_size, int32_t window, int32_t ring_pages,
+                                    float scale, tl_dtype dtype, void* workspace,
+                                    size_t workspace_bytes, uint32_t* error_word, void* stream);
+
+/* Workspace bytes of tl_paged_attn_prefill_ring (0 for invalid sizes or
+ * ring_pages <= 0): as for tl_paged_attn_prefill, but the fp16 V copy holds
+ * align_up(ring_pages * page_size, 128) + 256 keys per row and KV head. */
+size_t tl_paged_attn_prefill_ring_workspace_size(int32_t B, int32_t T, int32_t h_q,
+                                                 int32_t h_kv, int32_t d,
+                                                 int32_t max_pages_per_seq, int32_t page_size,
+                                                 int32_t ring_pages);
+
+tl_status tl_paged_attn_prefill_ring(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, int32_t max_pages_per_seq,
+                                     const int32_t* positions, float* out, int32_t B, int32_t T,
+                                     int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                     int32_t page_size, int32_t window, int32_t ring_pages,
+                                     float scale, tl_dtype dtype, void* workspace,
+                                     size_t workspace_bytes, uint32_t* error_word, void* stream);
 
 #ifdef __cplusplus
 }

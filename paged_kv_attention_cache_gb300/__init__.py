@@ -11,6 +11,8 @@ from .api import (TL_BF16, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noq
                   TL_DECODE_NOALLOC_SCRATCH_BYTES, tl_kv_cache_write, tl_paged_attn_decode,
                   tl_paged_attn_decode_noalloc, tl_paged_attn_decode_workspace_size,
                   tl_paged_attn_prefill, tl_paged_attn_prefill_workspace_size, tl_status_string,
+                  tl_paged_attn_decode_ring, tl_paged_attn_prefill_ring,
+                  tl_paged_attn_prefill_ring_workspace_size,
                   tl_version)
 from . import build as _build_module
 
@@ -23,5 +25,7 @@ __all__ = [
     "tl_kv_cache_write", "tl_paged_attn_decode", "tl_paged_attn_decode_noalloc",
     "tl_paged_attn_prefill",
     "tl_paged_attn_decode_workspace_size", "tl_paged_attn_prefill_workspace_size",
+    "tl_paged_attn_decode_ring", "tl_paged_attn_prefill_ring",
+    "tl_paged_attn_prefill_ring_workspace_size",
     "tl_status_string", "tl_version", "TLError", "build_library", "alloc_workspace",
 ]

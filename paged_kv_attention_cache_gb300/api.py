@@ -174,3 +174,68 @@ def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         _stream(stream))
     _check(st, "tl_paged_attn_prefill")
     return out
+
+
+def tl_paged_attn_decode_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                              window: int, ring_pages: int, out: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None,
+                              error_word: Optional[torch.Tensor] = None,
+                              stream=None) -> torch.Tensor:
+    """Decode over a ring: the first ring_pages entries of each table row hold
+    the sequence's ring (logical block k on entry k % ring_pages)."""
+    _need(q, "q", k_cache.dtype)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    B, hq, d = q.shape
+    P, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(tl_paged_attn_decode_workspace_size(B, hq, hkv, d), q.device)
+    st = _lib.load().tl_paged_attn_decode_ring(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(context_lens), _ptr(out), B, hq, hkv, d, P, ps, int(window), int(ring_pages),
+        float(scale), _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), workspace.numel(),
+        _ptr(error_word), _stream(stream))
+    _check(st, "tl_paged_attn_decode_ring")
+    return out
+
+
+def tl_paged_attn_prefill_ring_workspace_size(B: int, T: int, h_q: int, h_kv: int, d: int,
+                                              max_pages_per_seq: int, page_size: int,
+                                              ring_pages: int) -> int:
+    return int(_lib.load().tl_paged_attn_prefill_ring_workspace_size(
+        B, T, h_q, h_kv, d, max_pages_per_seq, page_size, ring_pages))
+
+
+def tl_paged_attn_prefill_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_table: torch.Tensor, positions: torch.Tensor, scale: float,
+                               window: int, ring_pages: int, out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               error_word: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """Batched prefill over rings (see tl_paged_attn_decode_ring)."""
+    _need(q, "q", k_cache.dtype)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(positions, "positions", torch.int32)
+    B, T, hq, d = q.shape
+    P, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, T, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(tl_paged_attn_prefill_ring_workspace_size(
+            B, T, hq, hkv, d, block_table.shape[1], ps, ring_pages), q.device)
+    st = _lib.load().tl_paged_attn_prefill_ring(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window), int(ring_pages),
+        float(scale), _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), workspace.numel(),
+        _ptr(error_word), _stream(stream))
+    _check(st, "tl_paged_attn_prefill_ring")
+    return out

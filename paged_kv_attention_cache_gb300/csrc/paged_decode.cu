@@ -88,10 +88,20 @@ struct DecodeParams {
   int32_t max_pages_per_seq;
   int32_t B, h_q, h_kv, group, d;
   int32_t num_pages, page_size, window;
-  float scale_log2;  // scale * log2(e): scores are kept in log2 units
+  int32_t ring_pages;  // > 0: the table's first ring_pages entries are a ring
+  float scale_log2;    // scale * log2(e): scores are kept in log2 units
   DecodeWorkspace ws;
   uint32_t* error_word;
 };
+
+// Block-table entry of logical block blk of sequence b.  With a ring
+// ("How serving works in Tlaloc", section 3, windowed KV pool) logical block
+// blk lives on ring page blk % ring_pages, so keys keep their position order
+// and a ring gives the same bits as a full-history table.
+__device__ __forceinline__ int32_t table_entry(const DecodeParams& P, int b, int blk) {
+  const int e = P.ring_pages > 0 ? blk % P.ring_pages : blk;
+  return __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + e);
+}
 
 // Causal range of sequence b: keys lo..p (empty when L <= 0 or L too long).
 __device__ __forceinline__ void seq_range(const DecodeParams& P, int b, int& lo, int& p,
@@ -99,7 +109,7 @@ __device__ __forceinline__ void seq_range(const DecodeParams& P, int b, int& lo,
   const int L = P.context_lens[b];
   const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
   p = L - 1;
-  if (L > cap) {
+  if (P.ring_pages == 0 && L > cap) {  // a ring's positions are not bounded by its width
     if (report_errors) report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
     p = -1;
   }
@@ -311,7 +321,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       nwin_blk0 = inext.c_begin * kChunk / P.page_size;
       const int blk = nwin_blk0 + lane;
       nwin = blk <= inext.p / P.page_size
-                 ? __ldg(P.block_table + (size_t)inext.b * P.max_pages_per_seq + blk)
+                 ? table_entry(P, inext.b, blk)
                  : -1;
     }
     if (id_next2 < total_items) describe_item(P, id_next2, inext2);
@@ -346,7 +356,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       nwin_blk0 = inext.c_begin * kChunk / P.page_size;
       const int blk = nwin_blk0 + lane;
       nwin = blk <= inext.p / P.page_size
-                 ? __ldg(P.block_table + (size_t)inext.b * P.max_pages_per_seq + blk)
+                 ? table_entry(P, inext.b, blk)
                  : -1;
     }
     id_next2 = __shfl_sync(0xffffffffu, grab, 0);
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       iwin_blk0 = bmin;
       const int blk = iwin_blk0 + lane;
       iwin = blk <= last_blk
-                 ? __ldg(P.block_table + (size_t)icur.b * P.max_pages_per_seq + blk)
+                 ? table_entry(P, icur.b, blk)
                  : -1;
     }
     const int jr = j0 + (lane & 15);
@@ -671,7 +681,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_f32_kernel(DecodeParams
         const int j = c * kChunk + jj;
         if (j < it.lo || j > it.p) continue;
         const int64_t page =
-            __ldg(P.block_table + (size_t)it.b * P.max_pages_per_seq + j / P.page_size);
+            table_entry(P, it.b, j / P.page_size);
         if (page < 0 || page >= P.num_pages) {
           if (lane == 0) report(P.error_word, TL_DEVERR_PAGE_RANGE);
           continue;
@@ -813,16 +823,14 @@ extern "C" size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, in
   return tl::decode_ws_layout(B, h_q, h_kv, d, nullptr, nullptr);
 }
 
-extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
-                                          const void* v_cache, const int32_t* block_table,
-                                          int32_t max_pages_per_seq,
-                                          const int32_t* context_lens, float* out, int32_t B,
-                                          int32_t h_q, int32_t h_kv, int32_t d,
-                                          int32_t num_pages, int32_t page_size, int32_t window,
-                                          float scale, tl_dtype dtype, void* workspace,
-                                          size_t workspace_bytes, uint32_t* error_word,
-                                          void* stream) {
-  using namespace tl;
+namespace tl {
+static tl_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, int32_t max_pages_per_seq,
+                             const int32_t* context_lens, float* out, int32_t B, int32_t h_q,
+                             int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size,
+                             int32_t window, int32_t ring_pages, float scale, tl_dtype dtype,
+                             void* workspace, size_t workspace_bytes, uint32_t* error_word,
+                             void* stream) {
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || num_pages <= 0 || page_size <= 0 ||
       max_pages_per_seq <= 0 || window < 0)
     return TL_ERR_INVALID_ARG;
@@ -859,6 +867,7 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   P.num_pages = num_pages;
   P.page_size = page_size;
   P.window = window;
+  P.ring_pages = ring_pages;
   P.scale_log2 = scale * kLog2e;
   decode_ws_layout(B, h_q, h_kv, d, &P.ws, static_cast<char*>(workspace));
   P.error_word = error_word;
@@ -909,4 +918,34 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   if (d == 128) decode_combine_kernel<128><<<cblocks, 256, 0, st>>>(P, 0);
   else decode_combine_kernel<64><<<cblocks, 256, 0, st>>>(P, 0);
   return launch_status();
+}
+}  // namespace tl
+
+extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_table,
+                                          int32_t max_pages_per_seq,
+                                          const int32_t* context_lens, float* out, int32_t B,
+                                          int32_t h_q, int32_t h_kv, int32_t d,
+                                          int32_t num_pages, int32_t page_size, int32_t window,
+                                          float scale, tl_dtype dtype, void* workspace,
+                                          size_t workspace_bytes, uint32_t* error_word,
+                                          void* stream) {
+  return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
+                         B, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
+                         workspace, workspace_bytes, error_word, stream);
+}
+
+extern "C" tl_status tl_paged_attn_decode_ring(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+    int32_t max_pages_per_seq, const int32_t* context_lens, float* out, int32_t B, int32_t h_q,
+    int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size, int32_t window,
+    int32_t ring_pages, float scale, tl_dtype dtype, void* workspace, size_t workspace_bytes,
+    uint32_t* error_word, void* stream) {
+  // the ring must be part of the table and must hold one window
+  if (ring_pages <= 0 || ring_pages > max_pages_per_seq || window <= 0 || page_size <= 0 ||
+      (int64_t)ring_pages * page_size < window)
+    return TL_ERR_INVALID_ARG;
+  return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
+                         B, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale, dtype,
+                         workspace, workspace_bytes, error_word, stream);
 }

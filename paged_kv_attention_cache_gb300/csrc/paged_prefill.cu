@@ -73,7 +73,22 @@ struct PrefillParams {
   int32_t n_pairs;       // query-tile pairs per row
   int32_t* pair_tiles;   // [B][n_pairs] key tiles each pair reads (0: no live token)
   int32_t* order;        // [B * n_pairs] pairs, most key tiles first
+  int32_t* row_start;    // [B] first key of each row's fp16 V copy (a multiple of kBN)
+  int32_t v_keys;        // keys per row (and KV head) of the fp16 V copy
+  int32_t ring_pages;    // > 0: the table's first ring_pages entries are a ring
 };
+
+// Position bound of the call: the table width, or none for a ring (whose
+// positions are not bounded by its width).
+__host__ __device__ __forceinline__ int64_t position_cap(const PrefillParams& P) {
+  return P.ring_pages > 0 ? (int64_t)INT32_MAX + 1 : (int64_t)P.max_pages_per_seq * P.page_size;
+}
+// Block-table entry index of logical block blk ("How serving works in
+// Tlaloc", section 3, windowed KV pool: block blk lives on ring page
+// blk % ring_pages).
+__device__ __forceinline__ int table_index(const PrefillParams& P, int blk) {
+  return P.ring_pages > 0 ? blk % P.ring_pages : blk;
+}
 
 constexpr int kBN = 128;             // keys per tile
 constexpr int kTcQB = 3;             // query-tile buffers (two in use, one filling)
@@ -90,19 +105,26 @@ constexpr int kTcSmem = kTcQB * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 8192;   // key-tile counts at or above 8191 share the last bucket
 
-// Workspace layout: [counter | pair_tiles | order | fp16 V], each part
-// 256-byte aligned.
+// Workspace layout: [counter | pair_tiles | order | row_start | fp16 V], each
+// part 256-byte aligned; the V copy is [B][h_kv][v_keys][128].
 struct WsLayout {
-  size_t tiles, order, v, total;
+  size_t tiles, order, rows, v, total;
 };
-inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t max_ctx) {
+inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_keys) {
   const size_t pairs = (size_t)(B * n_pairs) * 4;
   WsLayout L;
   L.tiles = 256;
   L.order = L.tiles + align_up(pairs, 256);
-  L.v = L.order + align_up(pairs, 256);
-  L.total = L.v + (size_t)B * h_kv * (size_t)max_ctx * 128 * 2;
+  L.rows = L.order + align_up(pairs, 256);
+  L.v = L.rows + align_up((size_t)B * 4, 256);
+  L.total = L.v + (size_t)B * h_kv * (size_t)v_keys * 128 * 2;
   return L;
+}
+// Keys per row of the V copy: the table's positions, or for a ring the
+// ring's positions plus the rounding of the copy's start and end to tiles.
+inline int64_t v_copy_keys(int64_t max_pages_per_seq, int64_t page_size, int64_t ring_pages) {
+  if (ring_pages > 0) return align_up((size_t)(ring_pages * page_size), kBN) + 2 * kBN;
+  return max_pages_per_seq * page_size;
 }
 constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;
@@ -188,13 +210,13 @@ constexpr int kCvtUnroll = 16;
 constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
 
 __global__ void __launch_bounds__(kCvtThreads)
-    prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int max_ctx, int* counter) {
+    prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int* counter) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;  // work items
   __shared__ int s_page[kCvtKeys];  // page of each key of the tile; -1: write zeros
-  const int b = (int)blockIdx.y, k0 = (int)blockIdx.x * kCvtKeys;
+  const int b = (int)blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
+  const int64_t cap = position_cap(P);
   if (blockIdx.x == 0) {
     // the key tiles every query-tile pair of row b reads (the attention
     // kernel's own range rule), for the heaviest-first order
@@ -243,15 +265,27 @@ __global__ void __launch_bounds__(kCvtThreads)
     pmin = min(pmin, s_min[w]);
     pmax = max(pmax, s_max[w]);
   }
-  if (pmax < 0) return;  // no live token: the attention kernel reads nothing
+  if (pmax < 0) {  // no live token: the attention kernel reads nothing
+    if (blockIdx.x == 0 && threadIdx.x == 0) P.row_start[b] = 0;
+    return;
+  }
   const int lo = (P.window > 0 && pmin - P.window + 1 > 0) ? pmin - P.window + 1 : 0;
-  const int start = lo / kBN * kBN, end = min((pmax / kBN + 1) * kBN, max_ctx);
-  if (k0 + kCvtKeys <= start || k0 >= end) return;
+  const int start = lo / kBN * kBN;
+  const int end = (int)min((int64_t)(pmax / kBN + 1) * kBN, (int64_t)start + P.v_keys);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    P.row_start[b] = start;
+    // a ring holds the call only if every key a token needs is still in it:
+    // the call spans lo..pmax, at most ring_pages * page_size positions
+    if (P.ring_pages > 0 && (int64_t)pmax - lo + 1 > (int64_t)P.ring_pages * P.page_size)
+      report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
+  }
+  const int k0 = start + (int)blockIdx.x * kCvtKeys;  // this CTA's keys of the copy
+  if (k0 >= end) return;
   for (int r = threadIdx.x; r < kCvtKeys; r += kCvtThreads) {
     const int k = k0 + r;
     int page = -1;  // keys past pmax: zeros
     if (k <= pmax) {
-      page = __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + k / P.page_size);
+      page = __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + table_index(P, k / P.page_size));
       if (page < 0 || page >= P.num_pages) {
         report(P.error_word, TL_DEVERR_PAGE_RANGE);
         page = -1;  // bad page: zeros
@@ -260,7 +294,7 @@ __global__ void __launch_bounds__(kCvtThreads)
     s_page[r] = page;
   }
   __syncthreads();
-  const int r0 = max(start - k0, 0), r1 = min(end - k0, kCvtKeys);  // keys of the tile to write
+  const int r0 = 0, r1 = min(end - k0, kCvtKeys);  // keys of the tile to write
   const int units = P.h_kv * 16;                                // 16-byte units per key
   const int total = (r1 - r0) * units;
   uint32_t vmax = 0;  // max |bf16 bits| seen, per half-word
@@ -290,8 +324,9 @@ __global__ void __launch_bounds__(kCvtThreads)
                                          max_u16x2(y.z & 0x7fff7fffu, y.w & 0x7fff7fffu)));
         y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z),
                        bf16x2_to_f16x2(y.w));
-        *reinterpret_cast<uint4*>(ws + (((size_t)b * P.h_kv + (u >> 4)) * max_ctx + k0 + r) * 128 +
-                                  (u & 15) * 8) = y;
+        *reinterpret_cast<uint4*>(
+            ws + (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 +
+            (u & 15) * 8) = y;
       }
     }
   }
@@ -433,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int rows_used = tpt * P.group;
   const int n_pairs = (P.T + 2 * tpt - 1) / (2 * tpt);
   const int n_items = n_pairs * P.B * P.h_kv;
-  const int64_t cap = (int64_t)P.max_pages_per_seq * P.page_size;
+  const int64_t cap = position_cap(P);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcQB; ++i) {
@@ -502,6 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (it.rg.kmax < 0) continue;
       const int32_t* bt_row = P.block_table + (size_t)it.b * P.max_pages_per_seq;
       const int last_blk = it.rg.kmax / P.page_size;
+      const int vstart = __ldg(P.row_start + it.b);  // the row's first key in the V copy
       int win_blk0 = -1, win = -1;
       load_q(0)
       for (int j = 0; j < it.n_tiles && ok; ++j) {
@@ -511,7 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (win_blk0 < 0 || bmin < win_blk0 || bmax >= win_blk0 + 32) {
           win_blk0 = bmin;
           const int blk = win_blk0 + lane;
-          win = blk <= last_blk ? __ldg(bt_row + blk) : -1;
+          win = blk <= last_blk ? __ldg(bt_row + table_index(P, blk)) : -1;
         }
         // this lane's boxes: lanes < 2*nbox (two row halves); box bi of half
         const int half = lane / nbox, bi = lane % nbox;
@@ -545,8 +581,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) {
             mbar_arrive_expect_tx(smem_u32(&sh.v_full[st]), kTcKVBytes);
             for (int hh = 0; hh < 2; ++hh)
-              tma_load_3d(sV + st * kTcKVBytes + hh * (kTcKVBytes / 2), &vmap, hh * 64, key0,
-                          it.b * P.h_kv + it.g, smem_u32(&sh.v_full[st]));
+              tma_load_3d(sV + st * kTcKVBytes + hh * (kTcKVBytes / 2), &vmap, hh * 64,
+                          key0 - vstart, it.b * P.h_kv + it.g, smem_u32(&sh.v_full[st]));
           }
           __syncwarp();
           ++v_issued;
@@ -823,30 +859,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace tl
 
-extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q,
-                                                       int32_t h_kv, int32_t d,
-                                                       int32_t max_pages_per_seq,
-                                                       int32_t page_size) {
+namespace tl {
+
+static size_t prefill_ws_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv, int32_t d,
+                              int32_t max_pages_per_seq, int32_t page_size, int32_t ring_pages) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv ||
-      max_pages_per_seq <= 0 || page_size <= 0)
+      max_pages_per_seq <= 0 || page_size <= 0 || ring_pages < 0)
     return 0;
-  // the work counter, the pairs' key-tile counts and order, then the fp16
-  // copy of V: [B][h_kv][max_pages_per_seq * page_size][d]
   const int tpt = std::max(1, 128 / (h_q / h_kv));
   const int64_t n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
-  return tl::ws_layout(B, n_pairs, h_kv, (int64_t)max_pages_per_seq * page_size).total;
+  return ws_layout(B, n_pairs, h_kv, v_copy_keys(max_pages_per_seq, page_size, ring_pages)).total;
 }
 
-extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
-                                           const void* v_cache, const int32_t* block_table,
-                                           int32_t max_pages_per_seq, const int32_t* positions,
-                                           float* out, int32_t B, int32_t T, int32_t h_q,
-                                           int32_t h_kv, int32_t d, int32_t num_pages,
-                                           int32_t page_size, int32_t window, float scale,
-                                           tl_dtype dtype, void* workspace,
-                                           size_t workspace_bytes, uint32_t* error_word,
-                                           void* stream) {
-  using namespace tl;
+static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, int32_t max_pages_per_seq,
+                              const int32_t* positions, float* out, int32_t B, int32_t T,
+                              int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                              int32_t page_size, int32_t window, int32_t ring_pages, float scale,
+                              tl_dtype dtype, void* workspace, size_t workspace_bytes,
+                              uint32_t* error_word, void* stream) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || num_pages <= 0 ||
       page_size <= 0 || max_pages_per_seq <= 0 || window < 0)
     return TL_ERR_INVALID_ARG;
@@ -862,8 +893,8 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
       page_size > 128)
     return TL_ERR_UNSUPPORTED;
   if ((int64_t)max_pages_per_seq * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
-  const size_t ws_need = tl_paged_attn_prefill_workspace_size(B, T, h_q, h_kv, d,
-                                                              max_pages_per_seq, page_size);
+  const size_t ws_need = prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size,
+                                         ring_pages);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < ws_need)
     return TL_ERR_WORKSPACE;
   PrefillParams P;
@@ -882,6 +913,7 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   P.num_pages = num_pages;
   P.page_size = page_size;
   P.window = window;
+  P.ring_pages = ring_pages;
   P.scale_log2 = scale * kLog2e;
   P.error_word = error_word;
   if (h_q / h_kv > 128 || B > 65535 || h_kv > 65535) return TL_ERR_UNSUPPORTED;
@@ -890,15 +922,18 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   const int group = h_q / h_kv;
   const int tpt = 128 / group;
   const int box_rows = page_size % 16 == 0 ? 16 : 8;
-  const int max_ctx = max_pages_per_seq * page_size;
+  const int64_t v_keys = v_copy_keys(max_pages_per_seq, page_size, ring_pages);
+  if (v_keys >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
-  const WsLayout L = ws_layout(B, n_pairs, h_kv, max_ctx);
+  const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   int* counter = reinterpret_cast<int*>(wsb);
   uint16_t* ws_v = reinterpret_cast<uint16_t*>(wsb + L.v);
   P.n_pairs = n_pairs;
   P.pair_tiles = reinterpret_cast<int32_t*>(wsb + L.tiles);
   P.order = reinterpret_cast<int32_t*>(wsb + L.order);
+  P.row_start = reinterpret_cast<int32_t*>(wsb + L.rows);
+  P.v_keys = (int32_t)v_keys;
   CUtensorMap qmap, kmap, vmap, omap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
@@ -907,9 +942,10 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
     const uint64_t kd[3] = {128, (uint64_t)h_kv, (uint64_t)num_pages * page_size};
     const uint64_t ks[2] = {128 * 2, (uint64_t)h_kv * 128 * 2};
     const uint32_t kb[3] = {64, 1, (uint32_t)box_rows};
-    // the workspace's fp16 V: (d, key, row x KV head), 16-bit elements like bf16
-    const uint64_t vd[3] = {128, (uint64_t)max_ctx, (uint64_t)B * h_kv};
-    const uint64_t vs[2] = {128 * 2, (uint64_t)max_ctx * 128 * 2};
+    // the workspace's fp16 V: (d, key - row start, row x KV head), 16-bit
+    // elements like bf16
+    const uint64_t vd[3] = {128, (uint64_t)v_keys, (uint64_t)B * h_kv};
+    const uint64_t vs[2] = {128 * 2, (uint64_t)v_keys * 128 * 2};
     const uint32_t vb[3] = {64, (uint32_t)kBN, 1};
     // the output, f32 (d, h_q, T, B): a TMA store box is one d quarter of a
     // query tile, clipped at T
@@ -928,10 +964,62 @@ extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
   const int64_t n_items = (int64_t)n_pairs * B * h_kv;
   if (n_items > 0x7fffffff - 65536) return TL_ERR_UNSUPPORTED;
   const int grid = (int)std::min<int64_t>(num_sms(), n_items);
-  prefill_v_f16_kernel<<<dim3((max_ctx + kCvtKeys - 1) / kCvtKeys, B), kCvtThreads, 0,
-                         (cudaStream_t)stream>>>(P, ws_v, max_ctx, counter);
+  prefill_v_f16_kernel<<<dim3((unsigned)((v_keys + kCvtKeys - 1) / kCvtKeys), B), kCvtThreads, 0,
+                         (cudaStream_t)stream>>>(P, ws_v, counter);
   prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(P);
   prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
       P, qmap, kmap, vmap, omap, box_rows, counter);
   return launch_status();
+}
+
+// The ring must be part of the table and hold one window.
+static bool ring_args_ok(int32_t max_pages_per_seq, int32_t page_size, int32_t window,
+                         int32_t ring_pages) {
+  return ring_pages > 0 && ring_pages <= max_pages_per_seq && window > 0 && page_size > 0 &&
+         (int64_t)ring_pages * page_size >= window;
+}
+
+}  // namespace tl
+
+extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q,
+                                                       int32_t h_kv, int32_t d,
+                                                       int32_t max_pages_per_seq,
+                                                       int32_t page_size) {
+  return tl::prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size, 0);
+}
+
+extern "C" size_t tl_paged_attn_prefill_ring_workspace_size(int32_t B, int32_t T, int32_t h_q,
+                                                            int32_t h_kv, int32_t d,
+                                                            int32_t max_pages_per_seq,
+                                                            int32_t page_size,
+                                                            int32_t ring_pages) {
+  if (ring_pages <= 0) return 0;
+  return tl::prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size, ring_pages);
+}
+
+extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_table,
+                                           int32_t max_pages_per_seq, const int32_t* positions,
+                                           float* out, int32_t B, int32_t T, int32_t h_q,
+                                           int32_t h_kv, int32_t d, int32_t num_pages,
+                                           int32_t page_size, int32_t window, float scale,
+                                           tl_dtype dtype, void* workspace,
+                                           size_t workspace_bytes, uint32_t* error_word,
+                                           void* stream) {
+  return tl::prefill_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, positions, out, B,
+                          T, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
+                          workspace, workspace_bytes, error_word, stream);
+}
+
+extern "C" tl_status tl_paged_attn_prefill_ring(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+    int32_t max_pages_per_seq, const int32_t* positions, float* out, int32_t B, int32_t T,
+    int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size, int32_t window,
+    int32_t ring_pages, float scale, tl_dtype dtype, void* workspace, size_t workspace_bytes,
+    uint32_t* error_word, void* stream) {
+  if (!tl::ring_args_ok(max_pages_per_seq, page_size, window, ring_pages))
+    return TL_ERR_INVALID_ARG;
+  return tl::prefill_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, positions, out, B,
+                          T, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale, dtype,
+                          workspace, workspace_bytes, error_word, stream);
 }

@@ -354,6 +354,36 @@ def swa_decode(seed=0, device="cpu", B=128, layer=0) -> DecodeCase:
                        seed=seed + 17 * layer, device=device, outlier_p=0.01)
 
 
+def swa_ring_decode(seed=0, device="cpu", B=128, window=4096, ring_pages=None) -> DecodeCase:
+    """The sliding-window layer of the mix over a windowed pool: each sequence
+    holds a ring of ring_pages pages (default ceil(window / 16) + 1, the
+    pages' default of one spare page) with random contents, lengths
+    U[1024, 32768] (most rings have wrapped), Hq=40, Hkv=8, d=128, bf16, 1%
+    of values x8.  The table is ring_pages wide; the new token of sequence b
+    goes to the ring slot of position L_b - 1 (logical block k on ring page
+    k % ring_pages).  extra["ring_pages"] holds the ring size."""
+    ps, hkv, d, hq = 16, 8, 128, 40
+    ring = ring_pages or (window + ps - 1) // ps + 1
+    g = _gen(seed + 4000, device)
+    lengths = swa_lengths(seed, B)
+    n_pages = B * ring
+    perm = torch.randperm(n_pages, generator=g, device=g.device).cpu()
+    table = perm.view(B, ring).to(torch.int32).contiguous()
+    pages_of = [table[b].tolist() for b in range(B)]
+    pool = PagedPool(n_pages, ps, table, pages_of)
+    shape = (n_pages, ps, hkv, d)
+    k_cache = _randn(shape, torch.bfloat16, g, device, 0.01)
+    v_cache = _randn(shape, torch.bfloat16, g, device, 0.01)
+    q = _randn((B, hq, d), torch.bfloat16, g, device, 0.01)
+    slots = [pages_of[b][((L - 1) // ps) % ring] * ps + (L - 1) % ps for b, L in enumerate(lengths)]
+    k_new = _randn((B, hkv, d), torch.bfloat16, g, device, 0.01)
+    v_new = _randn((B, hkv, d), torch.bfloat16, g, device, 0.01)
+    return DecodeCase(B, hq, hkv, d, ps, torch.bfloat16, window, 1.0 / math.sqrt(d),
+                      torch.tensor(lengths, dtype=torch.int32), pool, k_cache, v_cache, q,
+                      k_new, v_new, torch.tensor(slots, dtype=torch.int64),
+                      extra={"ring_pages": ring})
+
+
 def longctx_lengths(seed=0, B=256):
     g = _gen(seed + 4000, "cpu")
     z = torch.randn(B, generator=g, dtype=torch.float64)

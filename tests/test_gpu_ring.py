@@ -1,0 +1,143 @@
+"""Sliding-window attention over a ring (the windowed KV pool of "How serving
+works in Tlaloc", sections 2-3) on the GPU, through the C ABI: a ring gives the
+same bits as a full-history table, agrees with the oracle's ring form, and a
+ring that cannot hold the call is refused (decode) or reported (prefill)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_cache_gb300 as tl
+from paged_kv_attention_cache_gb300 import workloads as wl
+from tests.gpu_util import gpu_write, on_gpu, sample_rows, sub_pool
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _ring_case(lengths, **kw):
+    c = wl.ring_case(lengths, device=DEV, **kw)
+    c.full_table, c.ring_table = c.full_table.to(DEV), c.ring_table.to(DEV)
+    c.context_lens = c.context_lens.to(DEV)
+    return c
+
+
+def _write_new_tokens(c):
+    """Clear each sequence's last position in both layouts and write it back
+    through the cache write (the ring's slot follows the ring rule)."""
+    hkv, d = c.Hkv, c.d
+    for k, v, slots in ((c.full_k, c.full_v, c.full_slots), (c.ring_k, c.ring_v, c.ring_slots)):
+        s = slots.to(DEV)
+        live = s >= 0
+        k.view(-1, hkv, d)[s[live]] = 0
+        v.view(-1, hkv, d)[s[live]] = 0
+        err = _err()
+        tl.tl_kv_cache_write(c.k_new.contiguous(), c.v_new.contiguous(), k, v, s, error_word=err)
+        assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,ps,window,ring", [
+    (torch.bfloat16, 40, 8, 128, 16, 300, 20),
+    (torch.bfloat16, 32, 8, 128, 16, 256, 16),
+    (torch.bfloat16, 8, 2, 64, 8, 40, 6),
+    (torch.float32, 4, 2, 64, 16, 50, 4),
+])
+def test_decode_ring_equals_full_history_bit_for_bit(dtype, hq, hkv, d, ps, window, ring):
+    lengths = [1, 37, 300, 301, 1000, 2047, 5000]
+    c = _ring_case(lengths, window=window, ring_pages=ring, Hq=hq, Hkv=hkv, d=d, page_size=ps,
+                   dtype=dtype, seed=31)
+    _write_new_tokens(c)
+    e1, e2 = _err(), _err()
+    full = tl.tl_paged_attn_decode(c.q, c.full_k, c.full_v, c.full_table, c.context_lens,
+                                   c.scale, window=window, error_word=e1)
+    ring_out = tl.tl_paged_attn_decode_ring(c.q, c.ring_k, c.ring_v, c.ring_table,
+                                            c.context_lens, c.scale, window, ring, error_word=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) == 0 and int(e2.item()) == 0
+    assert torch.equal(full, ring_out)
+    ref = oracle.paged_decode(c.q.cpu(), c.ring_k.cpu(), c.ring_v.cpu(), c.ring_table.cpu(),
+                              c.context_lens.cpu(), c.scale, window=window, ring_pages=ring)
+    assert_close(ring_out, ref, "ring decode vs oracle")
+
+
+def test_decode_ring_that_cannot_hold_the_window_is_refused():
+    c = _ring_case([100, 400], window=64, ring_pages=4, Hq=8, Hkv=2, d=128, page_size=16,
+                   dtype=torch.bfloat16, seed=32)
+    for window, ring in ((65, 4), (64, 0), (0, 4), (64, c.ring_table.shape[1] + 1)):
+        with pytest.raises(tl.TLError) as e:
+            tl.tl_paged_attn_decode_ring(c.q, c.ring_k, c.ring_v, c.ring_table, c.context_lens,
+                                         c.scale, window, ring)
+        assert e.value.status == tl.TL_ERR_INVALID_ARG
+
+
+def _prefill_inputs(c, p0, n, pads, seed):
+    B, T = len(p0), n + max(pads)
+    positions = torch.full((B, T), -1, dtype=torch.int32)
+    for b in range(B):
+        positions[b, T - n:] = torch.arange(p0[b], p0[b] + n, dtype=torch.int32)
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    q = torch.randn((B, T, c.Hq, c.d), generator=g, device=DEV).to(c.dtype)
+    return q, positions.to(DEV)
+
+
+def test_prefill_chunk_through_a_ring_equals_full_history_bit_for_bit():
+    # a call of n tokens at p0 needs min(p0, W - 1) + n positions of ring
+    window, n, ps = 300, 200, 16
+    p0 = [0, 50, 700, 3000]
+    ring = oracle.ring_pages(window, n, ps)
+    c = _ring_case([p + n for p in p0], window=window, ring_pages=ring, Hq=32, Hkv=8, d=128,
+                   page_size=ps, dtype=torch.bfloat16, seed=33)
+    q, positions = _prefill_inputs(c, p0, n, pads=[0, 7, 0, 3], seed=34)
+    e1, e2 = _err(), _err()
+    full = tl.tl_paged_attn_prefill(q, c.full_k, c.full_v, c.full_table, positions, c.scale,
+                                    window=window, error_word=e1)
+    ring_out = tl.tl_paged_attn_prefill_ring(q, c.ring_k, c.ring_v, c.ring_table, positions,
+                                             c.scale, window, ring, error_word=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) == 0 and int(e2.item()) == 0
+    assert torch.equal(full, ring_out)
+    T = positions.shape[1]
+    rng = np.random.default_rng(35)
+    for b in range(len(p0)):
+        ts = sorted({0, T - 1, T - n} | set(rng.integers(0, T, 12).tolist()))
+        ref = oracle.paged_prefill(q[b:b + 1].cpu(), c.ring_k.cpu(), c.ring_v.cpu(),
+                                   c.ring_table[b:b + 1].cpu(), positions[b:b + 1].cpu(),
+                                   c.scale, window=window, ring_pages=ring,
+                                   tokens=np.asarray(ts, np.int64))
+        assert_close(ring_out[b, ts], ref, f"ring prefill row {b}")
+
+
+def test_prefill_ring_one_page_short_is_reported():
+    window, n, ps = 300, 200, 16
+    p0 = [3000]  # the call spans W - 1 + n = 499 positions > (32 - 1) * 16
+    ring = oracle.ring_pages(window, n, ps) - 1
+    c = _ring_case([p + n for p in p0], window=window, ring_pages=ring, Hq=32, Hkv=8, d=128,
+                   page_size=ps, dtype=torch.bfloat16, seed=36)
+    q, positions = _prefill_inputs(c, p0, n, pads=[0], seed=37)
+    err = _err()
+    tl.tl_paged_attn_prefill_ring(q, c.ring_k, c.ring_v, c.ring_table, positions, c.scale,
+                                  window, ring, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & tl.TL_DEVERR_CONTEXT_RANGE
+
+
+def test_full_size_sliding_layer_over_rings_sampled():
+    case = wl.swa_ring_decode(seed=0, device=DEV)
+    ring = case.extra["ring_pages"]
+    g = on_gpu(case)
+    gpu_write(g)
+    err = _err()
+    out = tl.tl_paged_attn_decode_ring(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                       g.scale, g.window, ring, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = sample_rows(case.context_lens.tolist(), 10)
+    kc, vc, bt = sub_pool(g.k_cache, g.v_cache, g.block_table, rows, [ring] * len(rows))
+    ref = oracle.paged_decode(g.q[rows].cpu(), kc, vc, bt, case.context_lens[rows], g.scale,
+                              window=g.window, ring_pages=ring)
+    assert_close(out[rows], ref, "sliding layer over rings")
