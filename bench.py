@@ -255,9 +255,14 @@ def run_ours(args):
     hbm, bf16, bf16_sus, src = peaks()
     dec_alg = kvb + q_bytes + bt_bytes + B * hq * d * 4
     achieved = dec_alg / (dec_ms * 1e-3) / 1e9
-    prefill_line, write_line = None, None
+    prefill_line, write_line, ring_line = None, None, None
     if args.only in ("all", "prefill"):
         prefill_line, write_line = run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src)
+    if args.only in ("all", "ring"):
+        ring_line = run_ring(args, dev, stream, hbm)
+    verify_line = None
+    if args.only in ("all", "verify"):
+        verify_line = run_verify(args, dev, stream, hbm, bf16)
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -294,6 +299,8 @@ def run_ours(args):
                      "ms_per_launch": round(dec_ms, 5)},
         "prefill": prefill_line,
         "kv_cache_write": write_line,
+        "ring_decode": ring_line,
+        "verify_decode": verify_line,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": 4 * args.steps,
@@ -303,6 +310,91 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_ring(args, dev, stream, hbm):
+    """The sliding-window layer (window 4,096) over a windowed pool of rings
+    (257 pages per sequence): GB/s of the window's K/V the decode reads."""
+    import torch
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
+    case = wl.swa_ring_decode(seed=args.seed, device=dev)
+    ring = case.extra["ring_pages"]
+    g = wl.to_device(case, dev)
+    B, hq, hkv, d = case.B, case.Hq, case.Hkv, case.d
+    tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping)
+    out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+    ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
+    keys = sum(min(int(L), case.window) for L in case.context_lens.tolist())
+    kvb = keys * 2 * hkv * d * 2
+    alg = kvb + B * hq * d * 2 + B * hq * d * 4 + B * ring * 4
+
+    def call():
+        tl.tl_paged_attn_decode_ring(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                     case.scale, case.window, ring, out=out, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    n = 50
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        call()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"workload": "sliding-window layer over rings: B=128, Hq=40, Hkv=8, d=128, bf16, "
+                        f"window 4096, rings of {ring} pages of 16, L~U[1024,32768]",
+            "kv_bytes_per_call": kvb, "ms_per_call": round(ms, 4),
+            "gbs": round(alg / (ms * 1e-3) / 1e9, 1), "frac": round(alg / (ms * 1e-3) / 1e9 / hbm, 4),
+            "l2": "ring pool %.2f GB vs 129 MB L2" % (g.k_cache.numel() * 4 / 1e9)}
+
+
+def run_verify(args, dev, stream, hbm, bf16, q_len=4):
+    """Multi-token decode (the speculative-verify shape) through
+    tl_paged_attn_decode_multi: the Llama-3-8B-shaped batch (B=64) with q_len
+    new tokens per sequence at positions L - q_len .. L - 1."""
+    import torch
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
+    lengths = wl.llama8b_lengths(seed=args.seed, B=64)
+    case = wl.prefill_case([0] * 64, [L - q_len for L in lengths], T=q_len, Hq=32, Hkv=8, d=128,
+                           seed=args.seed + 7, device=dev)
+    g = wl.to_device(case, dev)
+    tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping)
+    out = torch.empty((64, q_len, 32, 128), dtype=torch.float32, device=dev)
+    ws = tl.alloc_workspace(tl.tl_paged_attn_decode_multi_workspace_size(64, q_len, 32, 8, 128),
+                            dev)
+    cl = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    kvb = sum(lengths) * 2 * 8 * 128 * 2
+    flops = prefill_flops(case.positions, 32, 128)
+
+    def call():
+        tl.tl_paged_attn_decode_multi(g.q, g.k_cache, g.v_cache, g.block_table, cl, case.scale,
+                                      out=out, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    n = 50
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        call()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"workload": f"Llama-3-8B-shaped batch B=64, {q_len} query tokens per sequence at its "
+                        "end (speculative verify), L~U[512,8192], through tl_paged_attn_prefill",
+            "kv_bytes_per_call": kvb, "ms_per_call": round(ms, 4),
+            "kv_gbs": round(kvb / (ms * 1e-3) / 1e9, 1),
+            "kv_frac_of_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
 
 
 def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
@@ -454,7 +546,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=2.0)
     ap.add_argument("--batch", type=int, default=64, help="decode batch (64 = the workload)")
-    ap.add_argument("--only", choices=["all", "decode", "decode-e2e", "prefill"], default="all")
+    ap.add_argument("--only", choices=["all", "decode", "decode-e2e", "prefill", "ring",
+                                       "verify"], default="all")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -249,6 +249,33 @@ tl_status tl_paged_attn_decode_ring(const void* q, const void* k_cache, const vo
                                     float scale, tl_dtype dtype, void* workspace,
                                     size_t workspace_bytes, uint32_t* error_word, void* stream);
 
+/*
+ * Multi-token decode: q_len query tokens at the end of each sequence, at
+ * positions L - q_len .. L - 1 with L = context_lens[b] (their K/V written
+ * first), each attending with its own causal length (and window) over the
+ * sequence's pages.  This is the verify step of speculative decoding (the
+ * DGX Spark optimization-ladder page, rung D6: draft blocks of 6 to 8 tokens
+ * checked by a multi-token attention kernel) and a short chunk of chunked
+ * prefill ("How serving works in Tlaloc", section 4); it gives the same
+ * results as tl_paged_attn_prefill on the same tokens, within the tolerance,
+ * and for q_len = 1 is tl_paged_attn_decode.  K and V of each sequence are
+ * read once for all its tokens, as in decode.
+ *   q    [B][q_len][h_q][d] bf16;  out [B][q_len][h_q][d] float32.
+ * Supported: bf16, d in {64, 128}, q_len * (h_q / h_kv) <= 16 (the tokens'
+ * heads of one KV head form the MMA rows); otherwise TL_ERR_UNSUPPORTED.
+ * Workspace: tl_paged_attn_decode_multi_workspace_size(B, q_len, h_q, h_kv, d).
+ * Other arguments and errors as for tl_paged_attn_decode.
+ */
+size_t tl_paged_attn_decode_multi_workspace_size(int32_t B, int32_t q_len, int32_t h_q,
+                                                 int32_t h_kv, int32_t d);
+tl_status tl_paged_attn_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, int32_t max_pages_per_seq,
+                                     const int32_t* context_lens, float* out, int32_t B,
+                                     int32_t q_len, int32_t h_q, int32_t h_kv, int32_t d,
+                                     int32_t num_pages, int32_t page_size, int32_t window,
+                                     float scale, tl_dtype dtype, void* workspace,
+                                     size_t workspace_bytes, uint32_t* error_word, void* stream);
+
 /* Workspace bytes of tl_paged_attn_prefill_ring (0 for invalid sizes or
  * ring_pages <= 0): as for tl_paged_attn_prefill, but the fp16 V copy holds
  * align_up(ring_pages * page_size, 128) + 256 keys per row and KV head. */

@@ -12,7 +12,8 @@ from .api import (TL_BF16, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noq
                   tl_paged_attn_decode_noalloc, tl_paged_attn_decode_workspace_size,
                   tl_paged_attn_prefill, tl_paged_attn_prefill_workspace_size, tl_status_string,
                   tl_paged_attn_decode_ring, tl_paged_attn_prefill_ring,
-                  tl_paged_attn_prefill_ring_workspace_size,
+                  tl_paged_attn_prefill_ring_workspace_size, tl_paged_attn_decode_multi,
+                  tl_paged_attn_decode_multi_workspace_size,
                   tl_version)
 from . import build as _build_module
 
@@ -26,6 +27,7 @@ __all__ = [
     "tl_paged_attn_prefill",
     "tl_paged_attn_decode_workspace_size", "tl_paged_attn_prefill_workspace_size",
     "tl_paged_attn_decode_ring", "tl_paged_attn_prefill_ring",
-    "tl_paged_attn_prefill_ring_workspace_size",
+    "tl_paged_attn_prefill_ring_workspace_size", "tl_paged_attn_decode_multi",
+    "tl_paged_attn_decode_multi_workspace_size",
     "tl_status_string", "tl_version", "TLError", "build_library", "alloc_workspace",
 ]

@@ -33,6 +33,9 @@ SIGNATURES = {
     "tl_paged_attn_decode_ring": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                    i32, i32, f32, ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
     "tl_paged_attn_prefill_ring_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, i32], sz),
+    "tl_paged_attn_decode_multi_workspace_size": ([i32, i32, i32, i32, i32], sz),
+    "tl_paged_attn_decode_multi": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+                                    i32, i32, f32, ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
     "tl_paged_attn_prefill_ring": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                     i32, i32, i32, f32, ctypes.c_int, vp, sz, u32p, vp],
                                    ctypes.c_int),

@@ -239,3 +239,38 @@ def tl_paged_attn_prefill_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         _ptr(error_word), _stream(stream))
     _check(st, "tl_paged_attn_prefill_ring")
     return out
+
+
+def tl_paged_attn_decode_multi_workspace_size(B: int, q_len: int, h_q: int, h_kv: int,
+                                              d: int) -> int:
+    return int(_lib.load().tl_paged_attn_decode_multi_workspace_size(B, q_len, h_q, h_kv, d))
+
+
+def tl_paged_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_table: torch.Tensor, context_lens: torch.Tensor,
+                               scale: float, window: int = 0, out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               error_word: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """out[B, q_len, H_q, d] (float32): q_len query tokens at positions
+    L - q_len .. L - 1 of each sequence (L = context_lens[b])."""
+    _need(q, "q", k_cache.dtype)
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    B, q_len, hq, d = q.shape
+    P, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, q_len, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(
+            tl_paged_attn_decode_multi_workspace_size(B, q_len, hq, hkv, d), q.device)
+    st = _lib.load().tl_paged_attn_decode_multi(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(context_lens), _ptr(out), B, q_len, hq, hkv, d, P, ps, int(window), float(scale),
+        _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), workspace.numel(), _ptr(error_word),
+        _stream(stream))
+    _check(st, "tl_paged_attn_decode_multi")
+    return out

@@ -89,6 +89,9 @@ struct DecodeParams {
   int32_t B, h_q, h_kv, group, d;
   int32_t num_pages, page_size, window;
   int32_t ring_pages;  // > 0: the table's first ring_pages entries are a ring
+  int32_t q_len;       // query tokens per sequence (positions L - q_len .. L - 1)
+  int32_t rows;        // q_len * group: M rows of one work item (token-major)
+  int32_t hq_all;      // q_len * h_q: outputs per sequence
   float scale_log2;    // scale * log2(e): scores are kept in log2 units
   DecodeWorkspace ws;
   uint32_t* error_word;
@@ -103,7 +106,9 @@ __device__ __forceinline__ int32_t table_entry(const DecodeParams& P, int b, int
   return __ldg(P.block_table + (size_t)b * P.max_pages_per_seq + e);
 }
 
-// Causal range of sequence b: keys lo..p (empty when L <= 0 or L too long).
+// Key range of sequence b: lo..p, the union over its q_len queries (the last
+// at position p = L - 1, the first at L - q_len); empty when L <= 0 or L is
+// past the table.
 __device__ __forceinline__ void seq_range(const DecodeParams& P, int b, int& lo, int& p,
                                           bool report_errors) {
   const int L = P.context_lens[b];
@@ -113,7 +118,8 @@ __device__ __forceinline__ void seq_range(const DecodeParams& P, int b, int& lo,
     if (report_errors) report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
     p = -1;
   }
-  lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
+  const int first = p - (P.q_len - 1);
+  lo = (P.window > 0 && first - P.window + 1 > 0) ? first - P.window + 1 : 0;
 }
 
 __device__ __forceinline__ int seq_chunks(const DecodeParams& P, int b, bool report_errors) {
@@ -245,11 +251,11 @@ struct WarpSmem {
   static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one half
   static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
   static constexpr int kStageBytes = 2 * kChunkBytes;       // multiple of 1024
-  __host__ __device__ static int qslot_bytes(int group) {
-    return (group * D * 2 + 1023) / 1024 * 1024;
+  __host__ __device__ static int qslot_bytes(int rows) {
+    return (rows * D * 2 + 1023) / 1024 * 1024;
   }
-  __host__ __device__ static int warp_bytes(int group) {
-    return kRingW * (kStageBytes + qslot_bytes(group));
+  __host__ __device__ static int warp_bytes(int rows) {
+    return kRingW * (kStageBytes + qslot_bytes(rows));
   }
 };
 
@@ -285,8 +291,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   }
   __syncthreads();
 
-  const int qslot = L::qslot_bytes(P.group);
-  const uint32_t ring = sbase0 + w * L::warp_bytes(P.group);
+  const int qslot = L::qslot_bytes(P.rows);
+  const uint32_t ring = sbase0 + w * L::warp_bytes(P.rows);
   const uint32_t qbase = ring + kRingW * L::kStageBytes;
   const unsigned char* qbase_ptr = smem0 + (qbase - sbase0);
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
@@ -342,11 +348,13 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       d.b = icur.b; d.g = icur.g; d.lo = icur.lo; d.p = icur.p;
       d.c_begin = icur.c_begin; d.c_end = icur.c_end;
       d.s_global = icur.s_global; d.nsplits = icur.nsplits;
+      // the item's rows: the group's heads of each of the q_len tokens
       const uint32_t qbytes = (uint32_t)(P.group * D * 2);
-      mbar_arrive_expect_tx(smem_u32(&sh.qfull[w][q]), qbytes);
-      bulk_g2s(qbase + q * qslot,
-               qg + ((size_t)icur.b * P.h_q + (size_t)icur.g * P.group) * D, qbytes,
-               smem_u32(&sh.qfull[w][q]));
+      mbar_arrive_expect_tx(smem_u32(&sh.qfull[w][q]), qbytes * P.q_len);
+      for (int t = 0; t < P.q_len; ++t)
+        bulk_g2s(qbase + q * qslot + t * qbytes,
+                 qg + (((size_t)icur.b * P.q_len + t) * P.h_q + (size_t)icur.g * P.group) * D,
+                 qbytes, smem_u32(&sh.qfull[w][q]));
     }
     ++items_issued;
     // pipeline: next2 -> next (its descriptor has arrived: load its window)
@@ -423,14 +431,14 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const int e0 = ks * 16 + qc;
-      qa[ks][0] = qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0) * 2) : 0u;
+      qa[ks][0] = qr < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0) * 2) : 0u;
       qa[ks][2] =
-          qr < P.group ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0 + 8) * 2) : 0u;
+          qr < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0 + 8) * 2) : 0u;
       if (TWO_ROWS) {
-        qa[ks][1] = qr + 8 < P.group
+        qa[ks][1] = qr + 8 < P.rows
                         ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0) * 2)
                         : 0u;
-        qa[ks][3] = qr + 8 < P.group
+        qa[ks][3] = qr + 8 < P.rows
                         ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0 + 8) * 2)
                         : 0u;
       } else {
@@ -444,6 +452,12 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    // with several query tokens, each row has its own key range: row r is
+    // token r / group, at position p - (q_len - 1 - r / group)
+    const int pr0 = it.p - (P.q_len - 1 - qr / P.group);
+    const int pr1 = it.p - (P.q_len - 1 - (qr + 8) / P.group);
+    const int lr0 = (P.window > 0 && pr0 - P.window + 1 > 0) ? pr0 - P.window + 1 : 0;
+    const int lr1 = (P.window > 0 && pr1 - P.window + 1 > 0) ? pr1 - P.window + 1 : 0;
     for (int c = it.c_begin; c < it.c_end; ++c, ++gs_c) {
       issue_next();  // keeps kRingW-1 chunks in flight ahead of this one
       const int stage = (int)(gs_c % kRingW);
@@ -492,8 +506,14 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         for (int e = 0; e < 2; ++e) {
           const int key = n * 8 + qc + e;
           const bool ok = (mask >> key) & 1u;
-          s[n][e] = ok ? s[n][e] * P.scale_log2 : -INFINITY;
-          s[n][2 + e] = ok ? s[n][2 + e] * P.scale_log2 : -INFINITY;
+          bool ok0 = ok, ok1 = ok;
+          if (P.q_len > 1) {
+            const int kp = c * kChunk + key;
+            ok0 = ok && kp >= lr0 && kp <= pr0;
+            ok1 = ok && kp >= lr1 && kp <= pr1;
+          }
+          s[n][e] = ok0 ? s[n][e] * P.scale_log2 : -INFINITY;
+          s[n][2 + e] = ok1 ? s[n][2 + e] * P.scale_log2 : -INFINITY;
           mx0 = fmaxf(mx0, s[n][e]);
           mx1 = fmaxf(mx1, s[n][2 + e]);
         }
@@ -582,11 +602,13 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     }
     const bool single = it.nsplits == 1;
-    const int h0r = it.g * P.group + qr, h1r = h0r + 8;
+    // output index of rows qr and qr + 8 among the sequence's q_len * h_q
+    const int h0r = (qr / P.group) * P.h_q + it.g * P.group + qr % P.group;
+    const int h1r = ((qr + 8) / P.group) * P.h_q + it.g * P.group + (qr + 8) % P.group;
     if (single) {
       const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-      if (qr < P.group) {
-        float* dst = P.out + ((size_t)it.b * P.h_q + h0r) * D + qc;
+      if (qr < P.rows) {
+        float* dst = P.out + ((size_t)it.b * P.hq_all + h0r) * D + qc;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
           const float a = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
@@ -594,15 +616,15 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           *reinterpret_cast<float2*>(dst + n * 8) = make_float2(a * i0, bb * i0);
         }
       }
-      if (TWO_ROWS && qr + 8 < P.group) {
-        float* dst = P.out + ((size_t)it.b * P.h_q + h1r) * D + qc;
+      if (TWO_ROWS && qr + 8 < P.rows) {
+        float* dst = P.out + ((size_t)it.b * P.hq_all + h1r) * D + qc;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n)
           *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2] * i1, o[n][3] * i1);
       }
     } else {
-      if (qr < P.group) {
-        const size_t rowi = (size_t)it.s_global * P.h_q + h0r;
+      if (qr < P.rows) {
+        const size_t rowi = (size_t)it.s_global * P.hq_all + h0r;
         float* dst = P.ws.acc + rowi * D + qc;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
@@ -612,8 +634,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         }
         if ((lane & 3) == 0) *reinterpret_cast<float2*>(P.ws.ml + rowi * 2) = make_float2(m0, l0);
       }
-      if (TWO_ROWS && qr + 8 < P.group) {
-        const size_t rowi = (size_t)it.s_global * P.h_q + h1r;
+      if (TWO_ROWS && qr + 8 < P.rows) {
+        const size_t rowi = (size_t)it.s_global * P.hq_all + h1r;
         float* dst = P.ws.acc + rowi * D + qc;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n)
@@ -758,8 +780,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams P, int
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t wi = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (wi >= (int64_t)P.B * P.h_q) return;
-  const int b = (int)(wi / P.h_q), h = (int)(wi - (int64_t)b * P.h_q);
+  if (wi >= (int64_t)P.B * P.hq_all) return;
+  const int b = (int)(wi / P.hq_all), h = (int)(wi - (int64_t)b * P.hq_all);
   const int s0 = __ldg(P.ws.split_off + b), ns = __ldg(P.ws.split_off + b + 1) - s0;
   if (ns == 0) {  // nothing to read: the output is 0
     float* out = P.out + (size_t)wi * D + lane * E;
@@ -768,9 +790,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams P, int
     return;
   }
   if (ns == 1 && skip_single) return;
-  const float* ml = P.ws.ml + ((size_t)s0 * P.h_q + h) * 2;
-  const float* acc = P.ws.acc + ((size_t)s0 * P.h_q + h) * D + lane * E;
-  const size_t ml_stride = (size_t)P.h_q * 2, acc_stride = (size_t)P.h_q * D;
+  const float* ml = P.ws.ml + ((size_t)s0 * P.hq_all + h) * 2;
+  const float* acc = P.ws.acc + ((size_t)s0 * P.hq_all + h) * D + lane * E;
+  const size_t ml_stride = (size_t)P.hq_all * 2, acc_stride = (size_t)P.hq_all * D;
   float M = -INFINITY;
   for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, __ldg(ml + sp * ml_stride));
   M = warp_max(M);
@@ -826,11 +848,11 @@ extern "C" size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, in
 namespace tl {
 static tl_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                              const int32_t* block_table, int32_t max_pages_per_seq,
-                             const int32_t* context_lens, float* out, int32_t B, int32_t h_q,
-                             int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size,
-                             int32_t window, int32_t ring_pages, float scale, tl_dtype dtype,
-                             void* workspace, size_t workspace_bytes, uint32_t* error_word,
-                             void* stream) {
+                             const int32_t* context_lens, float* out, int32_t B, int32_t q_len,
+                             int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                             int32_t page_size, int32_t window, int32_t ring_pages, float scale,
+                             tl_dtype dtype, void* workspace, size_t workspace_bytes,
+                             uint32_t* error_word, void* stream) {
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || num_pages <= 0 || page_size <= 0 ||
       max_pages_per_seq <= 0 || window < 0)
     return TL_ERR_INVALID_ARG;
@@ -840,14 +862,17 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
       (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
       (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return TL_ERR_INVALID_ARG;
-  if (h_q % h_kv) return TL_ERR_INVALID_ARG;
+  if (h_q % h_kv || q_len <= 0) return TL_ERR_INVALID_ARG;
   const int group = h_q / h_kv;
+  // the M rows of a work item: the group's heads of each query token
+  if ((int64_t)q_len * group > 16 || (q_len > 1 && dtype != TL_BF16)) return TL_ERR_UNSUPPORTED;
+  const int rows = q_len * group;
   if (dtype != TL_BF16 && dtype != TL_F32) return TL_ERR_UNSUPPORTED;
   if ((d != 64 && d != 128) || group > 16 || page_size > 256) return TL_ERR_UNSUPPORTED;
   // the bf16 path moves pages with TMA boxes of 8 or 16 rows
   if (dtype == TL_BF16 && page_size % 8 != 0) return TL_ERR_UNSUPPORTED;
   if ((int64_t)num_pages * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
-  const size_t need = decode_ws_layout(B, h_q, h_kv, d, nullptr, nullptr);
+  const size_t need = decode_ws_layout(B, q_len * h_q, h_kv, d, nullptr, nullptr);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TL_ERR_WORKSPACE;
 
@@ -868,8 +893,11 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   P.page_size = page_size;
   P.window = window;
   P.ring_pages = ring_pages;
+  P.q_len = q_len;
+  P.rows = rows;
+  P.hq_all = q_len * h_q;
   P.scale_log2 = scale * kLog2e;
-  decode_ws_layout(B, h_q, h_kv, d, &P.ws, static_cast<char*>(workspace));
+  decode_ws_layout(B, q_len * h_q, h_kv, d, &P.ws, static_cast<char*>(workspace));
   P.error_word = error_word;
   cudaStream_t st = (cudaStream_t)stream;
 
@@ -890,7 +918,7 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
 #define TL_LAUNCH_W(DD, TWO)                                                              \
   do {                                                                                    \
     auto kern = decode_bf16_kernel<DD, TWO>;                                              \
-    const int per_warp = WarpSmem<DD>::warp_bytes(group);                                 \
+    const int per_warp = WarpSmem<DD>::warp_bytes(rows);                                  \
     const int warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);               \
     const int sm = warps * per_warp + 1024;                                               \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
@@ -899,13 +927,13 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
     kern<<<num_sms(), warps * 32, sm, st>>>(P, kmap, vmap, box_rows);                     \
   } while (0)
     if (d == 128) {
-      if (group > 8) TL_LAUNCH_W(128, true); else TL_LAUNCH_W(128, false);
+      if (rows > 8) TL_LAUNCH_W(128, true); else TL_LAUNCH_W(128, false);
     } else {
-      if (group > 8) TL_LAUNCH_W(64, true); else TL_LAUNCH_W(64, false);
+      if (rows > 8) TL_LAUNCH_W(64, true); else TL_LAUNCH_W(64, false);
     }
 #undef TL_LAUNCH_W
     if (launch_status() != TL_OK) return TL_ERR_CUDA;
-    const unsigned cblocks = (unsigned)(((int64_t)B * h_q + 7) / 8);
+    const unsigned cblocks = (unsigned)(((int64_t)B * P.hq_all + 7) / 8);
     if (d == 128) decode_combine_kernel<128><<<cblocks, 256, 0, st>>>(P, 1);
     else decode_combine_kernel<64><<<cblocks, 256, 0, st>>>(P, 1);
     return launch_status();
@@ -931,7 +959,7 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
                                           size_t workspace_bytes, uint32_t* error_word,
                                           void* stream) {
   return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
-                         B, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
+                         B, 1, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
                          workspace, workspace_bytes, error_word, stream);
 }
 
@@ -946,6 +974,23 @@ extern "C" tl_status tl_paged_attn_decode_ring(
       (int64_t)ring_pages * page_size < window)
     return TL_ERR_INVALID_ARG;
   return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
-                         B, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale, dtype,
+                         B, 1, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale,
+                         dtype, workspace, workspace_bytes, error_word, stream);
+}
+
+extern "C" size_t tl_paged_attn_decode_multi_workspace_size(int32_t B, int32_t q_len,
+                                                            int32_t h_q, int32_t h_kv, int32_t d) {
+  if (B <= 0 || q_len <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv) return 0;
+  return tl::decode_ws_layout(B, q_len * h_q, h_kv, d, nullptr, nullptr);
+}
+
+extern "C" tl_status tl_paged_attn_decode_multi(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+    int32_t max_pages_per_seq, const int32_t* context_lens, float* out, int32_t B, int32_t q_len,
+    int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size, int32_t window,
+    float scale, tl_dtype dtype, void* workspace, size_t workspace_bytes, uint32_t* error_word,
+    void* stream) {
+  return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
+                         B, q_len, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
                          workspace, workspace_bytes, error_word, stream);
 }
