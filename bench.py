@@ -390,7 +390,7 @@ def run_verify(args, dev, stream, hbm, bf16, q_len=4):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / n
     return {"workload": f"Llama-3-8B-shaped batch B=64, {q_len} query tokens per sequence at its "
-                        "end (speculative verify), L~U[512,8192], through tl_paged_attn_prefill",
+                        "end (speculative verify), L~U[512,8192], through tl_paged_attn_decode_multi",
             "kv_bytes_per_call": kvb, "ms_per_call": round(ms, 4),
             "kv_gbs": round(kvb / (ms * 1e-3) / 1e9, 1),
             "kv_frac_of_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4),
