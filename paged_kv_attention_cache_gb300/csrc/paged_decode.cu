@@ -1,5 +1,8 @@
-// PAGED_ATTENTION, decode: one query token per sequence, split-K over the
+// PAGED_ATTENTION, decode: one query token per sequence (or q_len tokens at
+// its end: the multi-token / speculative-verify shape), split-K over the
 // sequence's keys ("flash-decoding") with a log-sum-exp merge of the splits.
+// The table may be a ring (the windowed pool of section 3): logical block k
+// is then read from entry k % ring_pages, keys still in position order.
 //
 // What it computes is defined in "How serving works in Tlaloc", section 2
 // (gather through the block table, dot, masked softmax, dot; causal length =
@@ -16,8 +19,9 @@
 //      independent: a warp takes work items (split x KV head) from an atomic
 //      counter and streams their chunks (16 keys of K and V, 8 KiB at d=128)
 //      through its own ring of shared-memory stages filled by TMA; Q.K^T and
-//      P.V run on mma.sync m16n8k16 with the query-head group as the M rows,
-//      online softmax in registers (details below).  At the end of an item
+//      P.V run on mma.sync m16n8k16 with the query-head group (times the
+//      q_len tokens, token-major) as the M rows, each row masked to its own
+//      causal range, online softmax in registers (details below).  At the end of an item
 //      the warp writes from its registers:
 //      a sequence with one split writes its output directly, otherwise the
 //      item writes a partial.
