@@ -37,7 +37,7 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2
 DEFAULT_KEY_BLOCK = 2048
 
 _lib = None
@@ -73,6 +73,13 @@ def _load():
                                                  vp, i32]
             lib.oracle_paged_prefill.restype = ctypes.c_int
             lib.oracle_ring_pages.argtypes = [i64, i64, i64]
+            lib.oracle_fp8_value.argtypes = [i32]
+            lib.oracle_fp8_value.restype = f64
+            lib.oracle_fp8_code.argtypes = [f64]
+            lib.oracle_fp8_code.restype = i32
+            lib.oracle_kv_cache_write_fp8.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i64, i64,
+                                                      i64]
+            lib.oracle_kv_cache_write_fp8.restype = ctypes.c_int
             lib.oracle_ring_pages.restype = i64
             lib.oracle_kv_bytes_per_token.argtypes = [i64, i64, i64, i64]
             lib.oracle_kv_bytes_per_token.restype = i64
@@ -98,6 +105,8 @@ def _np(x):
             raise OracleError("the oracle takes host arrays")
         if x.dtype == torch.bfloat16:
             return x.contiguous().view(torch.int16).numpy().view(np.uint16)
+        if x.dtype == torch.float8_e4m3fn:
+            return x.contiguous().view(torch.uint8).numpy()
         return x.contiguous().numpy()
     return np.asarray(x)
 
@@ -107,7 +116,14 @@ def _dtype_code(a: np.ndarray) -> int:
         return F32
     if a.dtype in (np.uint16, np.int16):
         return BF16
-    raise OracleError(f"unsupported element type {a.dtype} (float32 or bf16 bits)")
+    if a.dtype == np.uint8:
+        return FP8
+    raise OracleError(f"unsupported element type {a.dtype} (float32, bf16 or e4m3 bits)")
+
+
+def _query_code(kv_code: int) -> int:
+    """The query of an fp8 pool is bf16."""
+    return BF16 if kv_code == FP8 else kv_code
 
 
 def _c(a: np.ndarray, dtype=None) -> np.ndarray:
@@ -141,6 +157,36 @@ def kv_cache_write(k_new, v_new, k_cache, v_cache, slot_mapping) -> None:
         raise OracleError(f"oracle_kv_cache_write failed ({rc})")
 
 
+def fp8_value(code: int) -> float:
+    """Value of one e4m3fn code."""
+    return float(_load().oracle_fp8_value(int(code)))
+
+
+def fp8_code(x: float) -> int:
+    """The e4m3fn code of x: nearest, ties to even mantissa, clamped to +-448."""
+    return int(_load().oracle_fp8_code(float(x)))
+
+
+def kv_cache_write_fp8(k_new, v_new, k_cache, v_cache, slot_mapping) -> None:
+    """In place: the e4m3fn codes of new[t] into the fp8 pools (uint8 or
+    torch.float8_e4m3fn, CPU) at slot[t], for every t with slot[t] != -1."""
+    lib = _load()
+    kn, vn = _c(_np(k_new)), _c(_np(v_new))
+    kc, vc = _np(k_cache), _np(v_cache)
+    if kc.dtype != np.uint8 or vc.dtype != np.uint8:
+        raise OracleError("fp8 pools hold e4m3 codes (uint8)")
+    if not (kc.flags.c_contiguous and vc.flags.c_contiguous):
+        raise OracleError("caches must be contiguous (written in place)")
+    sm = _c(_np(slot_mapping), np.int64)
+    P, ps, hkv, d = kc.shape
+    if kn.shape != (sm.shape[0], hkv, d) or vn.shape != kn.shape or vc.shape != kc.shape:
+        raise OracleError("shape mismatch")
+    rc = lib.oracle_kv_cache_write_fp8(_ptr(kn), _ptr(vn), _dtype_code(kn), _ptr(kc), _ptr(vc),
+                                       _ptr(sm), sm.shape[0], P, ps, hkv, d)
+    if rc != 0:
+        raise OracleError(f"oracle_kv_cache_write_fp8 failed ({rc})")
+
+
 def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale, window=0, seqs=None,
                  threads=0, ring_pages=0) -> np.ndarray:
     """out[i, h, :] for sequence seqs[i] (all sequences by default), float64 [n, H_q, d].
@@ -152,7 +198,7 @@ def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale, window=0
     B, hq, d = qa.shape
     P, ps, hkv, d2 = kc.shape
     dt = _dtype_code(kc)
-    if _dtype_code(qa) != dt or vc.shape != kc.shape or d2 != d or bt.shape[0] != B:
+    if _dtype_code(qa) != _query_code(dt) or vc.shape != kc.shape or d2 != d or bt.shape[0] != B:
         raise OracleError("shape / dtype mismatch")
     sq = _c(np.arange(B) if seqs is None else np.asarray(seqs), np.int32)
     out = np.zeros((sq.shape[0], hq, d), dtype=np.float64)
@@ -176,7 +222,8 @@ def paged_prefill(q, k_cache, v_cache, block_table, positions, scale, window=0,
     B, T, hq, d = qa.shape
     P, ps, hkv, d2 = kc.shape
     dt = _dtype_code(kc)
-    if _dtype_code(qa) != dt or vc.shape != kc.shape or d2 != d or pos.shape != (B, T):
+    if _dtype_code(qa) != _query_code(dt) or vc.shape != kc.shape or d2 != d or \
+            pos.shape != (B, T):
         raise OracleError("shape / dtype mismatch")
     tk = _c(np.arange(B * T) if tokens is None else np.asarray(tokens), np.int64)
     out = np.zeros((tk.shape[0], hq, d), dtype=np.float64)

@@ -28,7 +28,15 @@
  *     folded over key blocks of 2,048 positions with a running max, a running
  *     sum and a running P.V;
  *   - the KV sizing closed form ("Serving Models", "Count KV heads and
- *     distinct stored tensors"): 2 * layers * H_kv * d_head * bytes per token.
+ *     distinct stored tensors"): 2 * layers * H_kv * d_head * bytes per token;
+ *   - the fp8 KV cache ("How serving works in Tlaloc", the FP8 KV cache
+ *     paragraph of its quantisation section, after "Int8 weights (opt-in)"):
+ *     pools of e4m3fn codes (1 sign bit, 4 exponent bits with bias 7, 3
+ *     mantissa bits, no infinities, S.1111.111 is NaN) with no scale; the
+ *     write clamps each value to +-448 (the largest finite code) and rounds
+ *     it to the nearest code, ties to an even mantissa (the rounding the same
+ *     section states for e4m3 weight codes); attention reads the codes'
+ *     exact values.
  *
  * Everything is the plain definition written out: widen each stored value
  * exactly to double, accumulate in double, in index order, one output at a
@@ -50,20 +58,72 @@
 #include <omp.h>
 #endif
 
-enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_FP8 = 2 };
 enum { OR_OK = 0, OR_BAD_ARG = 1, OR_BAD_PAGE = 2, OR_NO_MEM = 3 };
 
+/* Value of one e4m3fn code: (-1)^s 2^(e-7) (1 + m/8) for e > 0,
+ * (-1)^s 2^-6 (m/8) for e = 0; e = 15 with m = 7 is NaN. */
+static double fp8_value(uint8_t code) {
+  const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* The e4m3fn code nearest to x (ties to the even mantissa), clamped to
+ * +-448; NaN gives the NaN code 0x7F.  The sign of zero is kept. */
+static uint8_t fp8_code(double x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E; /* clamp (448 itself is a code) */
+  int e;                               /* exponent of the code's binade */
+  double steps;                        /* a in units of the binade's spacing */
+  if (a < ldexp(1.0, -6)) {            /* subnormal codes: spacing 2^-9 */
+    e = 0;
+    steps = ldexp(a, 9);
+  } else {
+    int E;
+    frexp(a, &E);                      /* a = f 2^E, f in [0.5, 1) */
+    e = E - 1 + 7;                     /* biased exponent */
+    steps = ldexp(a, 3 - (E - 1));     /* in [8, 16): 8 + mantissa */
+  }
+  double r = floor(steps);
+  const double frac = steps - r;
+  if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  int m;
+  if (e == 0) {
+    m = (int)r; /* 0..8; 8 is the smallest normal code 0x08 */
+    return sign | (uint8_t)m;
+  }
+  m = (int)r - 8; /* 0..8 */
+  if (m == 8) {
+    m = 0;
+    e += 1;
+  }
+  if (e > 15 || (e == 15 && m == 7)) return sign | 0x7E; /* rounded past 448 */
+  return sign | (uint8_t)((e << 3) | m);
+}
+
 /* Exact widening of one stored element to double.  bf16 is the upper half of
- * an IEEE binary32, so the widening is a 16-bit shift. */
+ * an IEEE binary32, so the widening is a 16-bit shift; fp8 codes widen to
+ * their value. */
 static double widen(const void* base, int64_t idx, int dtype) {
   if (dtype == OR_F32) return (double)((const float*)base)[idx];
+  if (dtype == OR_FP8) return fp8_value(((const uint8_t*)base)[idx]);
   uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
   return (double)f;
 }
 
-static int64_t elem_size(int dtype) { return dtype == OR_F32 ? 4 : 2; }
+static int64_t elem_size(int dtype) { return dtype == OR_F32 ? 4 : dtype == OR_FP8 ? 1 : 2; }
+
+/* The query of an fp8 cache is bf16. */
+static int query_dtype(int kv_dtype) { return kv_dtype == OR_FP8 ? OR_BF16 : kv_dtype; }
+
+double oracle_fp8_value(int32_t code) { return fp8_value((uint8_t)code); }
+int32_t oracle_fp8_code(double x) { return fp8_code(x); }
 
 /* ---------------------------------------------------------------- write -- */
 
@@ -84,6 +144,28 @@ int oracle_kv_cache_write(const void* k_new, const void* v_new, void* k_cache,
     const int64_t dst = (page * page_size + offset) * row_bytes;
     memcpy((char*)k_cache + dst, (const char*)k_new + t * row_bytes, (size_t)row_bytes);
     memcpy((char*)v_cache + dst, (const char*)v_new + t * row_bytes, (size_t)row_bytes);
+  }
+  return OR_OK;
+}
+
+/* The write into an fp8 pool: each element of the new rows (f32 or bf16) is
+ * converted to its e4m3fn code (fp8_code); slot -1 writes nothing. */
+int oracle_kv_cache_write_fp8(const void* k_new, const void* v_new, int32_t src_dtype,
+                              uint8_t* k_cache, uint8_t* v_cache, const int64_t* slot_mapping,
+                              int64_t n_tokens, int64_t num_pages, int64_t page_size,
+                              int64_t h_kv, int64_t d) {
+  if (n_tokens < 0 || num_pages <= 0 || page_size <= 0 || h_kv <= 0 || d <= 0 ||
+      (src_dtype != OR_F32 && src_dtype != OR_BF16))
+    return OR_BAD_ARG;
+  const int64_t row = h_kv * d; /* elements of one token (all KV heads) */
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_pages * page_size) return OR_BAD_PAGE;
+    for (int64_t e = 0; e < row; ++e) {
+      k_cache[slot * row + e] = fp8_code(widen(k_new, t * row + e, src_dtype));
+      v_cache[slot * row + e] = fp8_code(widen(v_new, t * row + e, src_dtype));
+    }
   }
   return OR_OK;
 }
@@ -267,8 +349,9 @@ int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
                         int32_t ring_pages, double scale, const int32_t* seqs, int32_t n_seqs,
                         double* out, int32_t n_threads) {
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 || page_size <= 0 ||
-      num_pages <= 0 || max_pages_per_seq <= 0 || (dtype != OR_F32 && dtype != OR_BF16) ||
-      ring_pages < 0 || ring_pages > max_pages_per_seq)
+      num_pages <= 0 || max_pages_per_seq <= 0 ||
+      (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_FP8) || ring_pages < 0 ||
+      ring_pages > max_pages_per_seq)
     return OR_BAD_ARG;
   for (int32_t i = 0; i < n_seqs; ++i)
     if (seqs[i] < 0 || seqs[i] >= B) return OR_BAD_ARG;
@@ -283,7 +366,7 @@ int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
     double* qv = (double*)malloc((size_t)d * sizeof(double));
     double* o = out + item * d;
     if (!qv) { status = OR_NO_MEM; continue; }
-    for (int64_t e = 0; e < d; ++e) qv[e] = widen(q, (b * h_q + h) * d + e, dtype);
+    for (int64_t e = 0; e < d; ++e) qv[e] = widen(q, (b * h_q + h) * d + e, query_dtype(dtype));
     const int64_t p = (int64_t)context_lens[b] - 1;
     const int rc = ring_pages > 0
                        ? attend_ring(&s, qv, window_lo(p, window), p, p,
@@ -315,8 +398,8 @@ int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache
                          int32_t n_threads) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 ||
       page_size <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 ||
-      (dtype != OR_F32 && dtype != OR_BF16) || (blockwise && key_block <= 0) ||
-      ring_pages < 0 || ring_pages > max_pages_per_seq)
+      (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_FP8) ||
+      (blockwise && key_block <= 0) || ring_pages < 0 || ring_pages > max_pages_per_seq)
     return OR_BAD_ARG;
   for (int64_t i = 0; i < n_tokens; ++i)
     if (tokens[i] < 0 || tokens[i] >= (int64_t)B * T) return OR_BAD_ARG;
@@ -343,7 +426,8 @@ int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache
     double* qv = (double*)malloc((size_t)d * sizeof(double));
     double* o = out + item * d;
     if (!qv) { status = OR_NO_MEM; continue; }
-    for (int64_t e = 0; e < d; ++e) qv[e] = widen(q, (bt_idx * h_q + h) * d + e, dtype);
+    for (int64_t e = 0; e < d; ++e)
+      qv[e] = widen(q, (bt_idx * h_q + h) * d + e, query_dtype(dtype));
     const int64_t p = positions[bt_idx];
     const int64_t lo = window_lo(p, window);
     int rc;

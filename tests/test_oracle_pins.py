@@ -451,3 +451,106 @@ def test_ring_sizes_match_the_pages():
         assert got == e["expected_pages"], e["source"]
         if "default_pages" in e:
             assert got + 1 == e["default_pages"], e["source"]
+
+
+# --------------------------------------------------------------------- fp8 --
+# The fp8 KV cache ("How serving works in Tlaloc", the FP8 KV cache paragraph
+# of its quantisation section): e4m3fn codes with no scale, the write clamps
+# to +-448 and rounds to nearest (ties to even); attention widens the codes.
+# torch's float8_e4m3fn conversions are an independent implementation of the
+# same format (they give NaN instead of clamping out-of-range values).
+
+def _torch_codes(x):
+    return torch.tensor(np.asarray(x, np.float64)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_values(codes):
+    return torch.tensor(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def test_fp8_code_values_match_torch_and_the_format():
+    vals = np.array([oracle.fp8_value(c) for c in range(256)])
+    ref = _torch_values(np.arange(256))
+    assert np.all((vals == ref) | (np.isnan(vals) & np.isnan(ref)))
+    # anchors of the format: smallest subnormal 2^-9, smallest normal 2^-6, 1, max 448, NaN
+    assert oracle.fp8_value(0x01) == 2.0 ** -9 and oracle.fp8_value(0x08) == 2.0 ** -6
+    assert oracle.fp8_value(0x38) == 1.0 and oracle.fp8_value(0x7E) == 448.0
+    assert oracle.fp8_value(0xB8) == -1.0 and np.isnan(oracle.fp8_value(0x7F))
+
+
+def test_fp8_rounding_is_nearest_with_ties_to_even():
+    finite = [c for c in range(0x7F)]  # 0 .. 448, increasing
+    v = _torch_values(finite)
+    mids = (v[:-1] + v[1:]) / 2  # exact midpoints (ties)
+    rng = np.random.default_rng(61)
+    xs = np.concatenate([v, mids, -mids, rng.standard_normal(5000) * 10.0 ** rng.uniform(-4, 2.6, 5000)])
+    xs = xs[np.abs(xs) < 448]
+    mine = np.array([oracle.fp8_code(x) for x in xs])
+    assert np.array_equal(mine, _torch_codes(xs))
+    # a tie goes to the even mantissa: 1 + 1/16 lies between 1 (0x38) and 1.125 (0x39)
+    assert oracle.fp8_code(1.0625) == 0x38 and oracle.fp8_code(1.1875) == 0x3A
+
+
+def test_fp8_write_clamps_to_448_and_keeps_nan():
+    for x, code in ((448.0, 0x7E), (460.0, 0x7E), (464.0, 0x7E), (1e9, 0x7E), (float("inf"), 0x7E),
+                    (-1e9, 0xFE), (float("-inf"), 0xFE), (-448.0, 0xFE)):
+        assert oracle.fp8_code(x) == code, x
+    assert oracle.fp8_code(float("nan")) == 0x7F
+    assert oracle.fp8_code(0.0) == 0x00 and oracle.fp8_code(-0.0) == 0x80
+
+
+def test_fp8_cache_write_converts_and_skips_pads():
+    rng = np.random.default_rng(62)
+    P, ps, hkv, d = 5, 4, 2, 16
+    kc = rng.integers(0, 256, (P, ps, hkv, d)).astype(np.uint8)
+    vc = rng.integers(0, 256, (P, ps, hkv, d)).astype(np.uint8)
+    before_k, before_v = kc.copy(), vc.copy()
+    slots = np.array([3, -1, 17, 0, -1], dtype=np.int64)
+    kn = (rng.standard_normal((5, hkv, d)) * 50).astype(np.float32)
+    vn = (rng.standard_normal((5, hkv, d)) * 50).astype(np.float32)
+    kn[0, 0, 0], vn[2, 1, 3] = 1000.0, -700.0  # past the range: clamped
+    oracle.kv_cache_write_fp8(kn, vn, kc, vc, slots)
+    exp_k, exp_v = before_k.copy(), before_v.copy()
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        exp_k[s // ps, s % ps] = _torch_codes(np.clip(kn[t].astype(np.float64), -448, 448))
+        exp_v[s // ps, s % ps] = _torch_codes(np.clip(vn[t].astype(np.float64), -448, 448))
+    assert np.array_equal(kc, exp_k) and np.array_equal(vc, exp_v)
+
+
+@pytest.mark.parametrize("window", [0, 9])
+def test_fp8_decode_equals_dense_attention_over_the_codes_values(window):
+    # fp8 pools (codes from torch), bf16 queries: the oracle against dense
+    # attention over the codes' exact values, with library matrix products
+    rng = np.random.default_rng(63)
+    lengths, ps, hq, hkv, d = [30, 5, 64], 8, 4, 2, 16
+    need = [(L + ps - 1) // ps for L in lengths]
+    P = sum(need)
+    perm = rng.permutation(P)
+    bt = np.full((len(lengths), max(need)), -1, np.int32)
+    kc = np.zeros((P, ps, hkv, d), np.uint8)
+    vc = np.zeros_like(kc)
+    hist = []
+    off = 0
+    for b, L in enumerate(lengths):
+        pages = perm[off:off + need[b]]
+        off += need[b]
+        bt[b, :need[b]] = pages
+        kcode = _torch_codes(rng.standard_normal((L, hkv, d)) * 3)
+        vcode = _torch_codes(rng.standard_normal((L, hkv, d)) * 3)
+        for j in range(L):
+            kc[pages[j // ps], j % ps] = kcode[j]
+            vc[pages[j // ps], j % ps] = vcode[j]
+        hist.append((_torch_values(kcode), _torch_values(vcode)))
+    q_st, q_vals = round_to(rng.standard_normal((len(lengths), hq, d)), torch.bfloat16)
+    scale = 0.25
+    out = oracle.paged_decode(q_st, kc, vc, bt, lengths, scale, window=window)
+    import scipy.special
+    for b, L in enumerate(lengths):
+        lo = 0 if window <= 0 else max(0, L - window)
+        kv, vv = hist[b]
+        for h in range(hq):
+            g = h // (hq // hkv)
+            w = scipy.special.softmax(scale * (kv[lo:L, g] @ q_vals[b, h]))
+            np.testing.assert_allclose(out[b, h], w @ vv[lo:L, g], rtol=1e-12, atol=1e-12)
