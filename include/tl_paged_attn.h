@@ -67,8 +67,9 @@ typedef enum {
 } tl_status;
 
 typedef enum {
-  TL_F32 = 0, /* IEEE binary32 */
-  TL_BF16 = 1 /* bfloat16 */
+  TL_F32 = 0,      /* IEEE binary32 */
+  TL_BF16 = 1,     /* bfloat16 */
+  TL_FP8_E4M3 = 2  /* e4m3fn codes (fp8 KV pools only; see tl_kv_cache_write_fp8) */
 } tl_dtype;
 
 /* Bits OR-ed into *error_word by the device-side checks. */
@@ -101,6 +102,22 @@ tl_status tl_kv_cache_write(const void* k_new, const void* v_new, void* k_cache,
                             const int64_t* slot_mapping, int32_t n_tokens, int32_t num_pages,
                             int32_t page_size, int32_t h_kv, int32_t d, tl_dtype dtype,
                             uint32_t* error_word, void* stream);
+
+/*
+ * KV_CACHE_WRITE into fp8 pools ("How serving works in Tlaloc", the FP8 KV
+ * cache paragraph of its quantisation section): the pools hold e4m3fn codes
+ * (1 byte per element, no scale), the layout and the slot rule as above.
+ * Each element of the new rows (k_new / v_new: [n_tokens][h_kv][d] of
+ * src_dtype TL_F32 or TL_BF16) is clamped to +-448 and rounded to the
+ * nearest code, ties to an even mantissa; NaN gives the code 0x7F.
+ *   k_cache, v_cache  [num_pages][page_size][h_kv][d] uint8 codes, 8-byte
+ *                     aligned; other arguments and errors as above
+ *                     (h_kv * d a multiple of 16).
+ */
+tl_status tl_kv_cache_write_fp8(const void* k_new, const void* v_new, tl_dtype src_dtype,
+                                void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                                int32_t n_tokens, int32_t num_pages, int32_t page_size,
+                                int32_t h_kv, int32_t d, uint32_t* error_word, void* stream);
 
 /*
  * Bytes of workspace tl_paged_attn_decode needs for these sizes (an upper

@@ -5,7 +5,7 @@ declared in include/tl_paged_attn.h); this package builds it in-tree and binds
 it with the same names.  There is no CPU or framework fallback: calling an op
 without the built library, or without a CUDA device, raises.
 """
-from .api import (TL_BF16, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noqa: F401
+from .api import (TL_BF16, TL_FP8_E4M3, tl_kv_cache_write_fp8, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noqa: F401
                   TL_DEVERR_SLOT_RANGE, TL_DEVERR_TIMEOUT, TL_DEVERR_VALUE_RANGE, TL_ERR_CUDA, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED,
                   TL_ERR_WORKSPACE, TL_F32, TL_OK, TLError, alloc_workspace,
                   TL_DECODE_NOALLOC_SCRATCH_BYTES, tl_kv_cache_write, tl_paged_attn_decode,
@@ -23,7 +23,8 @@ def build_library(force: bool = False) -> str:
     return _build_module.build(force=force)
 
 __all__ = [
-    "tl_kv_cache_write", "tl_paged_attn_decode", "tl_paged_attn_decode_noalloc",
+    "tl_kv_cache_write", "tl_kv_cache_write_fp8", "tl_paged_attn_decode",
+    "tl_paged_attn_decode_noalloc",
     "tl_paged_attn_prefill",
     "tl_paged_attn_decode_workspace_size", "tl_paged_attn_prefill_workspace_size",
     "tl_paged_attn_decode_ring", "tl_paged_attn_prefill_ring",

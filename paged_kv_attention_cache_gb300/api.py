@@ -14,11 +14,16 @@ import torch
 from . import _lib
 
 TL_OK, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED, TL_ERR_CUDA, TL_ERR_WORKSPACE = range(5)
-TL_F32, TL_BF16 = 0, 1
+TL_F32, TL_BF16, TL_FP8_E4M3 = 0, 1, 2
 TL_DEVERR_SLOT_RANGE, TL_DEVERR_PAGE_RANGE, TL_DEVERR_CONTEXT_RANGE = 1, 2, 4
 TL_DEVERR_TIMEOUT, TL_DEVERR_VALUE_RANGE = 8, 16
 
-_DTYPES = {torch.float32: TL_F32, torch.bfloat16: TL_BF16}
+_DTYPES = {torch.float32: TL_F32, torch.bfloat16: TL_BF16, torch.float8_e4m3fn: TL_FP8_E4M3}
+
+
+def _query_dtype(cache_dtype):
+    """Queries against an e4m3 pool are bf16; otherwise the pool's dtype."""
+    return torch.bfloat16 if cache_dtype == torch.float8_e4m3fn else cache_dtype
 
 
 class TLError(RuntimeError):
@@ -77,6 +82,25 @@ def tl_kv_cache_write(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.T
     _check(st, "tl_kv_cache_write")
 
 
+def tl_kv_cache_write_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                          error_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """In place: the e4m3 codes of new[t] (f32 or bf16, [N, H_kv, d]) into the
+    fp8 pools (torch.float8_e4m3fn [num_pages, page_size, H_kv, d]) at slot[t],
+    for every t with slot != -1; values clamp to +-448."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n)
+    _need(k_cache, "k_cache", torch.float8_e4m3fn)
+    _need(v_cache, "v_cache", torch.float8_e4m3fn)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    P, ps, hkv, d = k_cache.shape
+    st = _lib.load().tl_kv_cache_write_fp8(
+        _ptr(k_new), _ptr(v_new), _DTYPES.get(k_new.dtype, -1), _ptr(k_cache), _ptr(v_cache),
+        _ptr(slot_mapping), slot_mapping.numel(), P, ps, hkv, d, _ptr(error_word),
+        _stream(stream))
+    _check(st, "tl_kv_cache_write_fp8")
+
+
 def tl_paged_attn_decode_workspace_size(B: int, h_q: int, h_kv: int, d: int) -> int:
     return int(_lib.load().tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d))
 
@@ -98,7 +122,7 @@ def tl_paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
                          workspace: Optional[torch.Tensor] = None,
                          error_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """out[B, H_q, d] (float32): one query per sequence, causal length context_lens[b]."""
-    _need(q, "q", k_cache.dtype)
+    _need(q, "q", _query_dtype(k_cache.dtype))
     _need(k_cache, "k_cache")
     _need(v_cache, "v_cache", k_cache.dtype)
     _need(block_table, "block_table", torch.int32)
@@ -130,7 +154,7 @@ def tl_paged_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache
     """Decode into a caller-provided `out` without any device allocation: the
     scratch is a fixed array inside the library (see the C header); calls on a
     device share it, so calls that overlap on the GPU must be serialised."""
-    _need(q, "q", k_cache.dtype)
+    _need(q, "q", _query_dtype(k_cache.dtype))
     _need(k_cache, "k_cache")
     _need(v_cache, "v_cache", k_cache.dtype)
     _need(block_table, "block_table", torch.int32)
@@ -153,7 +177,7 @@ def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
                           error_word: Optional[torch.Tensor] = None,
                           stream=None) -> torch.Tensor:
     """out[B, T, H_q, d] (float32): right-aligned batched prefill, padding at position -1."""
-    _need(q, "q", k_cache.dtype)
+    _need(q, "q", _query_dtype(k_cache.dtype))
     _need(k_cache, "k_cache")
     _need(v_cache, "v_cache", k_cache.dtype)
     _need(block_table, "block_table", torch.int32)
@@ -184,7 +208,7 @@ def tl_paged_attn_decode_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
                               stream=None) -> torch.Tensor:
     """Decode over a ring: the first ring_pages entries of each table row hold
     the sequence's ring (logical block k on entry k % ring_pages)."""
-    _need(q, "q", k_cache.dtype)
+    _need(q, "q", _query_dtype(k_cache.dtype))
     _need(k_cache, "k_cache")
     _need(v_cache, "v_cache", k_cache.dtype)
     _need(block_table, "block_table", torch.int32)
@@ -219,7 +243,7 @@ def tl_paged_attn_prefill_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
                                error_word: Optional[torch.Tensor] = None,
                                stream=None) -> torch.Tensor:
     """Batched prefill over rings (see tl_paged_attn_decode_ring)."""
-    _need(q, "q", k_cache.dtype)
+    _need(q, "q", _query_dtype(k_cache.dtype))
     _need(k_cache, "k_cache")
     _need(v_cache, "v_cache", k_cache.dtype)
     _need(block_table, "block_table", torch.int32)
@@ -254,7 +278,7 @@ def tl_paged_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
                                stream=None) -> torch.Tensor:
     """out[B, q_len, H_q, d] (float32): q_len query tokens at positions
     L - q_len .. L - 1 of each sequence (L = context_lens[b])."""
-    _need(q, "q", k_cache.dtype)
+    _need(q, "q", _query_dtype(k_cache.dtype))
     _need(k_cache, "k_cache")
     _need(v_cache, "v_cache", k_cache.dtype)
     _need(block_table, "block_table", torch.int32)

@@ -48,6 +48,12 @@ bool encode_bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const 
                            swizzle128);
 }
 
+bool encode_u8_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box, bool swizzle128) {
+  return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides, box,
+                           swizzle128);
+}
+
 bool encode_f32_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides, const uint32_t* box, bool swizzle128) {
   return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides, box,

@@ -212,6 +212,9 @@ bool encode_bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const 
 // The same for f32 elements.
 bool encode_f32_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides, const uint32_t* box, bool swizzle128);
+// The same for 8-bit elements (e4m3 codes).
+bool encode_u8_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box, bool swizzle128);
 
 inline tl_status launch_status() {
   cudaError_t e = cudaGetLastError();

@@ -249,19 +249,114 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 constexpr int kRingW = TL_DECODE_RING;      // stages per warp
 constexpr int kMaxWarpsW = TL_DECODE_WARPS;
 
-template <int D>
+// Per-warp shared memory: kRingW stages of one chunk of K and V as the TMA
+// lands them (16-bit or e4m3 elements, rows split in 128-byte parts), kRingW
+// Q slots, and for e4m3 pools one buffer of the chunk widened to fp16 in the
+// 16-bit stage layout.
+template <int D, bool KV8 = false>
 struct WarpSmem {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one half
+  static constexpr int kRowBytes = D * (KV8 ? 1 : 2);
+  static constexpr int kHalves = kRowBytes / 128;          // 128-byte parts of a row
+  static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one part
   static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
   static constexpr int kStageBytes = 2 * kChunkBytes;       // multiple of 1024
+  static constexpr int kWideBytes = KV8 ? 2 * (D * 2 / 128) * kHalfBytes : 0;
   __host__ __device__ static int qslot_bytes(int rows) {
     return (rows * D * 2 + 1023) / 1024 * 1024;
   }
   __host__ __device__ static int warp_bytes(int rows) {
-    return kRingW * (kStageBytes + qslot_bytes(rows));
+    return kRingW * (kStageBytes + qslot_bytes(rows)) + kWideBytes;
   }
 };
+
+// m16n8k16 with f32 accumulation on bf16 or fp16 operands.
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  if (F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+}
+
+// (a, b) ~ hi + lo as fp16 pairs (about 22 significant bits together).
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(hi) : "f"(b), "f"(a));
+  float ah, bh;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+      : "=f"(ah), "=f"(bh)
+      : "r"(hi));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(lo) : "f"(b - bh), "f"(a - ah));
+}
+
+template <bool F16>
+__device__ __forceinline__ void split16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  if (F16)
+    split_f16x2(a, b, hi, lo);
+  else
+    split_bf16x2(a, b, hi, lo);
+}
+
+// One bf16 pair as an fp16 pair (queries against an e4m3 pool; finite
+// values beyond +-65504 become infinite).
+__device__ __forceinline__ uint32_t bf16x2_as_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n"
+      : "=r"(r)
+      : "f"(__uint_as_float(x & 0xffff0000u)), "f"(__uint_as_float(x << 16)));
+  return r;
+}
+
+// Two e4m3 codes (low byte first) as an fp16 pair; exact (every e4m3 value is
+// an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_as_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const uint16_t c = (uint16_t)two_codes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(c));
+  return r;
+}
+
+// Widen one chunk tile (16 rows x 128 codes, 128-byte swizzle, as the TMA
+// lands it) into the 16-bit stage layout (two 128-byte parts per row, same
+// swizzle); rows from first_dead on become zeros.  Lane-strided over the
+// tile's 16-byte units.
+__device__ __forceinline__ void widen_e4m3_tile(uint32_t src, uint32_t dst, int first_dead,
+                                                int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int u = i * 32 + lane;  // physical unit: row u / 8, slot u % 8
+    const int r = u >> 3, cl = (u & 7) ^ (r & 7);  // logical unit: codes 16cl .. 16cl+15
+    uint32_t x0, x1, x2, x3;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                 : "r"(src + u * 16));
+    uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (r < first_dead) {
+      h[0] = e4m3x2_as_f16x2(x0);
+      h[1] = e4m3x2_as_f16x2(x0 >> 16);
+      h[2] = e4m3x2_as_f16x2(x1);
+      h[3] = e4m3x2_as_f16x2(x1 >> 16);
+      h[4] = e4m3x2_as_f16x2(x2);
+      h[5] = e4m3x2_as_f16x2(x2 >> 16);
+      h[6] = e4m3x2_as_f16x2(x3);
+      h[7] = e4m3x2_as_f16x2(x3 >> 16);
+    }
+    // fp16 units 2cl, 2cl+1: part cl / 4, units 2(cl % 4), 2(cl % 4) + 1 of the row
+    const uint32_t base = dst + (cl >> 2) * (kChunk * 128) + r * 128;
+    const int uh = 2 * (cl & 3);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(base + ((uh ^ (r & 7)) << 4)),
+                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                     base + (((uh + 1) ^ (r & 7)) << 4)),
+                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                 : "memory");
+  }
+}
 
 struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits;
@@ -274,11 +369,11 @@ struct WarpShared {
   int abort_flag;
 };
 
-template <int D, bool TWO_ROWS>
+template <int D, bool TWO_ROWS, bool KV8>
 __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     decode_bf16_kernel(DecodeParams P, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, int box_rows) {
-  using L = WarpSmem<D>;
+  using L = WarpSmem<D, KV8>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ WarpShared sh;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -298,6 +393,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const int qslot = L::qslot_bytes(P.rows);
   const uint32_t ring = sbase0 + w * L::warp_bytes(P.rows);
   const uint32_t qbase = ring + kRingW * L::kStageBytes;
+  const uint32_t wide = qbase + kRingW * qslot;  // e4m3 pools: the widened chunk
   const unsigned char* qbase_ptr = smem0 + (qbase - sbase0);
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
@@ -414,7 +510,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     if (lane < nreq)
       tma_load_3d(ring + stage * L::kStageBytes + rq_kind * L::kChunkBytes +
                       rq_half * L::kHalfBytes + rq_box * box_rows * 128,
-                  rq_map, rq_half * 64, icur.g, slot0, bar);
+                  rq_map, rq_half * (KV8 ? 128 : 64), icur.g, slot0, bar);
     ++gs_issue;
     if (++icur_c == icur.c_end) icur_live = false;
   };
@@ -449,6 +545,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         qa[ks][1] = 0u;
         qa[ks][3] = 0u;
       }
+      if (KV8) {  // the tensor core takes fp16 for both operands here
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qa[ks][k] = bf16x2_as_f16x2(qa[ks][k]);
+      }
     }
     __syncwarp();
 
@@ -470,8 +570,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         break;
       }
       const uint32_t mask = sh.stage_mask[w][stage];
-      const uint32_t kaddr = ring + stage * L::kStageBytes;
-      const uint32_t vaddr = kaddr + L::kChunkBytes;
+      uint32_t kaddr = ring + stage * L::kStageBytes;
+      uint32_t vaddr = kaddr + L::kChunkBytes;
       {
         // V rows past the sequence's end (its last chunk only) may hold anything
         const int first_dead = it.p + 1 - c * kChunk;
@@ -488,6 +588,15 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           __syncwarp();
         }
       }
+      if (KV8) {
+        // widen K and V to fp16 in the 16-bit stage layout; the loads below
+        // then read the wide buffer (the dead V rows above are zeros already)
+        widen_e4m3_tile(kaddr, wide, kChunk, lane);
+        widen_e4m3_tile(vaddr, wide + 2 * kChunk * 128, kChunk, lane);
+        __syncwarp();
+        kaddr = wide;
+        vaddr = wide + 2 * kChunk * 128;
+      }
       // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys)
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       {
@@ -499,8 +608,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4),
                       b0, b1, b2, b3);
-          mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          mma_16816<KV8>(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_16816<KV8>(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
         }
       }
       float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -561,8 +670,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       }
       // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
       uint32_t h0, l0w, h2, l2w;
-      split_bf16x2(p[0][0], p[0][1], h0, l0w);
-      split_bf16x2(p[1][0], p[1][1], h2, l2w);
+      split16<KV8>(p[0][0], p[0][1], h0, l0w);
+      split16<KV8>(p[1][0], p[1][1], h2, l2w);
       {
         const int mi = lane >> 3, ri = lane & 7;
         const int tok = (mi & 1) * 8 + ri;
@@ -574,13 +683,13 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
             ldmatrix_x4_trans(
                 vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
                 b1, b2, b3);
-            mma_bf16_16816(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
-            mma_bf16_16816(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+            mma_16816<KV8>(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
+            mma_16816<KV8>(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
           }
         } else {
           uint32_t h1, l1w, h3, l3w;
-          split_bf16x2(p[0][2], p[0][3], h1, l1w);
-          split_bf16x2(p[1][2], p[1][3], h3, l3w);
+          split16<KV8>(p[0][2], p[0][3], h1, l1w);
+          split16<KV8>(p[1][2], p[1][3], h3, l3w);
 #pragma unroll
           for (int nd2 = 0; nd2 < D / 16; ++nd2) {
             const int u = 2 * nd2 + (mi >> 1);
@@ -588,10 +697,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
             ldmatrix_x4_trans(
                 vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
                 b1, b2, b3);
-            mma_bf16_16816(o[2 * nd2], h0, h1, h2, h3, b0, b1);
-            mma_bf16_16816(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
-            mma_bf16_16816(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
-            mma_bf16_16816(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+            mma_16816<KV8>(o[2 * nd2], h0, h1, h2, h3, b0, b1);
+            mma_16816<KV8>(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
+            mma_16816<KV8>(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
+            mma_16816<KV8>(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
           }
         }
       }
@@ -869,12 +978,14 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   if (h_q % h_kv || q_len <= 0) return TL_ERR_INVALID_ARG;
   const int group = h_q / h_kv;
   // the M rows of a work item: the group's heads of each query token
-  if ((int64_t)q_len * group > 16 || (q_len > 1 && dtype != TL_BF16)) return TL_ERR_UNSUPPORTED;
+  if ((int64_t)q_len * group > 16 || (q_len > 1 && dtype == TL_F32)) return TL_ERR_UNSUPPORTED;
   const int rows = q_len * group;
-  if (dtype != TL_BF16 && dtype != TL_F32) return TL_ERR_UNSUPPORTED;
+  if (dtype != TL_BF16 && dtype != TL_F32 && dtype != TL_FP8_E4M3) return TL_ERR_UNSUPPORTED;
   if ((d != 64 && d != 128) || group > 16 || page_size > 256) return TL_ERR_UNSUPPORTED;
-  // the bf16 path moves pages with TMA boxes of 8 or 16 rows
-  if (dtype == TL_BF16 && page_size % 8 != 0) return TL_ERR_UNSUPPORTED;
+  // the bf16 and e4m3 paths move pages with TMA boxes of 8 or 16 rows; e4m3
+  // rows are one 128-byte box wide
+  if (dtype != TL_F32 && page_size % 8 != 0) return TL_ERR_UNSUPPORTED;
+  if (dtype == TL_FP8_E4M3 && d != 128) return TL_ERR_UNSUPPORTED;
   if ((int64_t)num_pages * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
   const size_t need = decode_ws_layout(B, q_len * h_q, h_kv, d, nullptr, nullptr);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -909,20 +1020,25 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   decode_plan_kernel<<<1, 1024, 0, st>>>(P, target_splits);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
 
-  if (dtype == TL_BF16) {
-    // 3-D tensor maps of the pools: (d, H_kv, slot), boxes of 64 x 1 x box_rows
+  if (dtype == TL_BF16 || dtype == TL_FP8_E4M3) {
+    // 3-D tensor maps of the pools: (d, H_kv, slot), boxes of one 128-byte
+    // row part x 1 x box_rows (64 bf16 or 128 e4m3 elements)
+    const bool kv8 = dtype == TL_FP8_E4M3;
+    const int esz = kv8 ? 1 : 2;
     const int box_rows = page_size % 16 == 0 ? 16 : 8;
     CUtensorMap kmap, vmap;
     const uint64_t dims[3] = {(uint64_t)d, (uint64_t)h_kv, (uint64_t)num_pages * page_size};
-    const uint64_t strides[2] = {(uint64_t)d * 2, (uint64_t)h_kv * d * 2};
-    const uint32_t box[3] = {64, 1, (uint32_t)box_rows};
-    if (!encode_bf16_tensor_map(&kmap, k_cache, 3, dims, strides, box, true) ||
-        !encode_bf16_tensor_map(&vmap, v_cache, 3, dims, strides, box, true))
-      return TL_ERR_CUDA;
-#define TL_LAUNCH_W(DD, TWO)                                                              \
+    const uint64_t strides[2] = {(uint64_t)d * esz, (uint64_t)h_kv * d * esz};
+    const uint32_t box[3] = {(uint32_t)(128 / esz), 1, (uint32_t)box_rows};
+    const bool enc = kv8 ? (encode_u8_tensor_map(&kmap, k_cache, 3, dims, strides, box, true) &&
+                            encode_u8_tensor_map(&vmap, v_cache, 3, dims, strides, box, true))
+                         : (encode_bf16_tensor_map(&kmap, k_cache, 3, dims, strides, box, true) &&
+                            encode_bf16_tensor_map(&vmap, v_cache, 3, dims, strides, box, true));
+    if (!enc) return TL_ERR_CUDA;
+#define TL_LAUNCH_W(DD, TWO, K8)                                                          \
   do {                                                                                    \
-    auto kern = decode_bf16_kernel<DD, TWO>;                                              \
-    const int per_warp = WarpSmem<DD>::warp_bytes(rows);                                  \
+    auto kern = decode_bf16_kernel<DD, TWO, K8>;                                          \
+    const int per_warp = WarpSmem<DD, K8>::warp_bytes(rows);                              \
     const int warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);               \
     const int sm = warps * per_warp + 1024;                                               \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
@@ -930,10 +1046,12 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
       return TL_ERR_CUDA;                                                                 \
     kern<<<num_sms(), warps * 32, sm, st>>>(P, kmap, vmap, box_rows);                     \
   } while (0)
-    if (d == 128) {
-      if (rows > 8) TL_LAUNCH_W(128, true); else TL_LAUNCH_W(128, false);
+    if (kv8) {
+      if (rows > 8) TL_LAUNCH_W(128, true, true); else TL_LAUNCH_W(128, false, true);
+    } else if (d == 128) {
+      if (rows > 8) TL_LAUNCH_W(128, true, false); else TL_LAUNCH_W(128, false, false);
     } else {
-      if (rows > 8) TL_LAUNCH_W(64, true); else TL_LAUNCH_W(64, false);
+      if (rows > 8) TL_LAUNCH_W(64, true, false); else TL_LAUNCH_W(64, false, false);
     }
 #undef TL_LAUNCH_W
     if (launch_status() != TL_OK) return TL_ERR_CUDA;

@@ -1,0 +1,137 @@
+"""The fp8 (e4m3fn) KV cache on the GPU ("How serving works in Tlaloc", the
+FP8 KV cache paragraph of its quantisation section): the converting write is
+bit-exact against the oracle, and decode over e4m3 pools matches the oracle
+reading the same codes.  The pools handed to both sides are built on the host
+(torch's float8 conversion of seeded values, the oracle's write for the new
+rows), so no oracle input comes from the CUDA path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_cache_gb300 as tl
+from paged_kv_attention_cache_gb300 import workloads as wl
+from tests.gpu_util import sample_rows, sub_pool
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+@pytest.mark.parametrize("src", [torch.bfloat16, torch.float32])
+def test_fp8_write_is_bit_exact(src):
+    g = torch.Generator().manual_seed(71)
+    P, ps, hkv, d, N = 40, 16, 8, 128, 300
+    kn = torch.randn((N, hkv, d), generator=g) * torch.exp(torch.randn((N, hkv, d), generator=g) * 3)
+    vn = torch.randn((N, hkv, d), generator=g) * 50
+    # exact ties between codes, the clamp, NaN, infinities, signed zeros
+    codes = torch.arange(0, 0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).double()
+    mids = ((codes[:-1] + codes[1:]) / 2).float()
+    kn.view(-1)[:mids.numel()] = mids
+    kn.view(-1)[mids.numel():mids.numel() + 8] = torch.tensor(
+        [448.0, 460.0, 464.0, 1e9, -1e9, float("inf"), float("-inf"), -0.0])
+    vn.view(-1)[:3] = torch.tensor([float("nan"), -float("nan"), 0.0])
+    kn, vn = kn.to(src), vn.to(src)
+    slots = torch.randperm(P * ps, generator=g)[:N].to(torch.int64)
+    slots[::7] = -1  # pads
+    kc0 = torch.randint(0, 256, (P, ps, hkv, d), generator=g, dtype=torch.uint8)
+    vc0 = torch.randint(0, 256, (P, ps, hkv, d), generator=g, dtype=torch.uint8)
+    kc_ref, vc_ref = kc0.clone().numpy(), vc0.clone().numpy()
+    oracle.kv_cache_write_fp8(kn, vn, kc_ref, vc_ref, slots)
+    kc = kc0.to(DEV).view(torch.float8_e4m3fn)
+    vc = vc0.to(DEV).view(torch.float8_e4m3fn)
+    err = _err()
+    tl.tl_kv_cache_write_fp8(kn.to(DEV), vn.to(DEV), kc, vc, slots.to(DEV), error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(kc.view(torch.uint8).cpu().numpy(), kc_ref)
+    assert np.array_equal(vc.view(torch.uint8).cpu().numpy(), vc_ref)
+
+
+def _fp8_case(case):
+    """Host e4m3 pools of a bf16 case (torch's conversion of the stored
+    values), the new rows written by the oracle; then on the GPU."""
+    k8 = case.k_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    v8 = case.v_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    oracle.kv_cache_write_fp8(case.k_new, case.v_new, k8, v8, case.slot_mapping)
+    return (torch.from_numpy(k8).view(torch.float8_e4m3fn), torch.from_numpy(v8).view(torch.float8_e4m3fn))
+
+
+def _decode_fp8(case, k8, v8, rows, window=None, ring=0):
+    w = case.window if window is None else window
+    dev = lambda t: t.to(DEV)
+    err = _err()
+    if ring:
+        out = tl.tl_paged_attn_decode_ring(dev(case.q), dev(k8), dev(v8), dev(case.block_table),
+                                           dev(case.context_lens), case.scale, w, ring,
+                                           error_word=err)
+    else:
+        out = tl.tl_paged_attn_decode(dev(case.q), dev(k8), dev(v8), dev(case.block_table),
+                                      dev(case.context_lens), case.scale, window=w,
+                                      error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ps = case.page_size
+    lens = case.context_lens.tolist()
+    n_pages = [ring] * len(rows) if ring else [(max(lens[b], 0) + ps - 1) // ps for b in rows]
+    kc, vc, bt = sub_pool(k8.view(torch.uint8), v8.view(torch.uint8), case.block_table, rows,
+                          n_pages)
+    ref = oracle.paged_decode(case.q[rows], kc.numpy(), vc.numpy(), bt, case.context_lens[rows],
+                              case.scale, window=w, ring_pages=ring)
+    return out, ref
+
+
+@pytest.mark.parametrize("maker", [wl.llama8b_decode, lambda **k: wl.swa_decode(layer=0, **k),
+                                   wl.longctx_decode])
+def test_fp8_decode_full_size_sampled(maker):
+    case = maker(seed=0)
+    k8, v8 = _fp8_case(case)
+    rows = sample_rows(case.context_lens.tolist(), 8)
+    out, ref = _decode_fp8(case, k8, v8, rows)
+    assert_close(out[rows], ref, "fp8 decode")
+
+
+@pytest.mark.parametrize("window", [0, 1, 16, 100])
+def test_fp8_decode_edge_lengths(window):
+    case = wl.decode_case([1, 15, 16, 17, 100, 257, 1000], Hq=32, Hkv=8, d=128, seed=72,
+                          window=window)
+    k8, v8 = _fp8_case(case)
+    rows = list(range(case.B))
+    out, ref = _decode_fp8(case, k8, v8, rows)
+    assert_close(out, ref, f"fp8 decode window {window}")
+
+
+def test_fp8_decode_over_rings():
+    case = wl.swa_ring_decode(seed=1, B=32)
+    ring = case.extra["ring_pages"]
+    k8, v8 = _fp8_case(case)
+    rows = sample_rows(case.context_lens.tolist(), 6)
+    out, ref = _decode_fp8(case, k8, v8, rows, ring=ring)
+    assert_close(out[rows], ref, "fp8 ring decode")
+
+
+def test_fp8_multi_token_decode():
+    q_len = 4
+    lengths = wl.llama8b_lengths(seed=9, B=12)
+    p0 = [L - q_len for L in lengths]
+    case = wl.prefill_case([0] * len(lengths), p0, T=q_len, Hq=32, Hkv=8, d=128, seed=73)
+    k8 = case.k_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    v8 = case.v_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    oracle.kv_cache_write_fp8(case.k_new, case.v_new, k8, v8, case.slot_mapping)
+    k8t = torch.from_numpy(k8).view(torch.float8_e4m3fn)
+    v8t = torch.from_numpy(v8).view(torch.float8_e4m3fn)
+    cl = torch.tensor(lengths, dtype=torch.int32)
+    err = _err()
+    out = tl.tl_paged_attn_decode_multi(case.q.to(DEV), k8t.to(DEV), v8t.to(DEV),
+                                        case.block_table.to(DEV), cl.to(DEV), case.scale,
+                                        error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for row in (0, 6, 11):
+        ref = oracle.paged_prefill(case.q[row:row + 1], k8, v8, case.block_table[row:row + 1],
+                                   case.positions[row:row + 1], case.scale)
+        assert_close(out[row], ref, f"fp8 multi-token row {row}")
