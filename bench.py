@@ -263,6 +263,9 @@ def run_ours(args):
     verify_line = None
     if args.only in ("all", "verify"):
         verify_line = run_verify(args, dev, stream, hbm, bf16)
+    fp8_line = None
+    if args.only in ("all", "fp8"):
+        fp8_line = run_fp8(args, dev, stream, hbm)
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -301,6 +304,7 @@ def run_ours(args):
         "kv_cache_write": write_line,
         "ring_decode": ring_line,
         "verify_decode": verify_line,
+        "fp8_decode": fp8_line,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": 4 * args.steps,
@@ -351,6 +355,52 @@ def run_ring(args, dev, stream, hbm):
             "kv_bytes_per_call": kvb, "ms_per_call": round(ms, 4),
             "gbs": round(alg / (ms * 1e-3) / 1e9, 1), "frac": round(alg / (ms * 1e-3) / 1e9 / hbm, 4),
             "l2": "ring pool %.2f GB vs 129 MB L2" % (g.k_cache.numel() * 4 / 1e9)}
+
+
+def run_fp8(args, dev, stream, hbm):
+    """Decode of the Llama-3-8B-shaped batch (B=64) over e4m3 pools: the pools
+    are the bf16 pools written through tl_kv_cache_write_fp8 (every slot), the
+    step is the write of the 64 new rows plus the decode, as for bf16."""
+    import torch
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
+    case = wl.llama8b_decode(seed=args.seed, device=dev)
+    g = wl.to_device(case, dev)
+    P, ps, hkv, d = g.k_cache.shape
+    B, hq = case.B, case.Hq
+    k8 = torch.empty((P, ps, hkv, d), dtype=torch.float8_e4m3fn, device=dev)
+    v8 = torch.empty_like(k8)
+    every = torch.arange(P * ps, dtype=torch.int64, device=dev)
+    tl.tl_kv_cache_write_fp8(g.k_cache.view(-1, hkv, d), g.v_cache.view(-1, hkv, d), k8, v8, every)
+    del g.k_cache, g.v_cache
+    out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+    ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
+    kvb = int(case.context_lens.sum().item()) * 2 * hkv * d  # one byte per element
+
+    def step():
+        tl.tl_kv_cache_write_fp8(g.k_new, g.v_new, k8, v8, g.slot_mapping)
+        tl.tl_paged_attn_decode(g.q, k8, v8, g.block_table, g.context_lens, case.scale,
+                                out=out, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = 100
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"workload": "Llama-3-8B-shaped decode layer over e4m3 pools: B=64, Hq=32, Hkv=8, "
+                        "d=128, page 16, L~U[512,8192] (write of 64 rows + decode)",
+            "kv_bytes_per_step": kvb, "ms_per_step": round(ms, 4),
+            "kv_gbs": round(kvb / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4),
+            "tokens_per_s": round(B / (ms * 1e-3), 1)}
 
 
 def run_verify(args, dev, stream, hbm, bf16, q_len=4):
@@ -547,7 +597,7 @@ def main():
     ap.add_argument("--soak-seconds", type=float, default=2.0)
     ap.add_argument("--batch", type=int, default=64, help="decode batch (64 = the workload)")
     ap.add_argument("--only", choices=["all", "decode", "decode-e2e", "prefill", "ring",
-                                       "verify"], default="all")
+                                       "verify", "fp8"], default="all")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -149,7 +149,10 @@ size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, int32_t h_kv,
  *                256-byte aligned; its contents need no initialisation and
  *                are garbage afterwards.  Calls that overlap in time must not
  *                share a workspace.
- * Supported: dtype TL_BF16 or TL_F32, d in {64, 128}, h_q % h_kv == 0 with
+ * Supported: dtype TL_BF16 or TL_F32, or TL_FP8_E4M3 for e4m3 pools (q bf16,
+ * d = 128; the codes widen exactly to fp16 for the tensor core, and q is
+ * rounded to fp16: finite |q| beyond 65504 is out of range), d in {64, 128},
+ * h_q % h_kv == 0 with
  * h_q/h_kv <= 16, page_size in [1, 256] (a multiple of 8 for TL_BF16, whose
  * pages move as TMA boxes of 8 or 16 rows), num_pages*page_size < 2^31.
  * Otherwise TL_ERR_UNSUPPORTED.
@@ -200,6 +203,15 @@ size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, i
                                             int32_t d, int32_t max_pages_per_seq,
                                             int32_t page_size);
 
+/* Workspace bytes of any prefill call (0 for invalid sizes): ring_pages 0 for
+ * a full-history table (tl_paged_attn_prefill) or > 0 for a ring
+ * (tl_paged_attn_prefill_ring); dtype TL_BF16, or TL_FP8_E4M3 for e4m3
+ * pools, which add a bf16 copy of K as large as the V copy. */
+size_t tl_paged_attn_prefill_workspace_size_ex(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
+                                               int32_t d, int32_t max_pages_per_seq,
+                                               int32_t page_size, int32_t ring_pages,
+                                               tl_dtype dtype);
+
 /*
  * PAGED_ATTENTION, batched prefill ("How serving works in Tlaloc", sections
  * 1-2, "Blockwise attention"): B rows of T tokens.  Token (b,t) with position
@@ -219,8 +231,11 @@ size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, i
  *                the call's fp16 copy of V and work counter, so calls that may
  *                overlap on the GPU must not share one.
  *   other arguments as for decode.
- * Supported: dtype TL_BF16, d = 128, h_q % h_kv == 0 with h_q/h_kv <= 128,
- * page_size a power of two in [8, 128].  Otherwise TL_ERR_UNSUPPORTED.
+ * Supported: dtype TL_BF16, or TL_FP8_E4M3 for e4m3 pools (q stays bf16; the
+ * codes widen exactly: K to a bf16 copy, V to an fp16 copy in the workspace,
+ * sized by tl_paged_attn_prefill_workspace_size_ex), d = 128,
+ * h_q % h_kv == 0 with h_q/h_kv <= 128, page_size a power of two in
+ * [8, 128].  Otherwise TL_ERR_UNSUPPORTED.
  * scale must be positive and finite (TL_ERR_INVALID_ARG otherwise).
  * Arithmetic: Q.K^T with bf16 operands and f32 accumulation; P.V with P
  * rounded to fp16 and V converted bf16 -> fp16 (exact for |v| in

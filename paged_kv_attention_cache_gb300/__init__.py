@@ -14,6 +14,7 @@ from .api import (TL_BF16, TL_FP8_E4M3, tl_kv_cache_write_fp8, TL_DEVERR_CONTEXT
                   tl_paged_attn_decode_ring, tl_paged_attn_prefill_ring,
                   tl_paged_attn_prefill_ring_workspace_size, tl_paged_attn_decode_multi,
                   tl_paged_attn_decode_multi_workspace_size,
+                  tl_paged_attn_prefill_workspace_size_ex,
                   tl_version)
 from . import build as _build_module
 

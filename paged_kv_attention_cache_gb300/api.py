@@ -101,6 +101,13 @@ def tl_kv_cache_write_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: tor
     _check(st, "tl_kv_cache_write_fp8")
 
 
+def tl_paged_attn_prefill_workspace_size_ex(B: int, T: int, h_q: int, h_kv: int, d: int,
+                                            max_pages_per_seq: int, page_size: int,
+                                            ring_pages: int, dtype: int) -> int:
+    return int(_lib.load().tl_paged_attn_prefill_workspace_size_ex(
+        B, T, h_q, h_kv, d, max_pages_per_seq, page_size, ring_pages, dtype))
+
+
 def tl_paged_attn_decode_workspace_size(B: int, h_q: int, h_kv: int, d: int) -> int:
     return int(_lib.load().tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d))
 
@@ -189,8 +196,8 @@ def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
     _need(out, "out", torch.float32)
     if workspace is None:
         workspace = alloc_workspace(
-            tl_paged_attn_prefill_workspace_size(B, T, hq, hkv, d, block_table.shape[1], ps),
-            q.device)
+            tl_paged_attn_prefill_workspace_size_ex(B, T, hq, hkv, d, block_table.shape[1], ps, 0,
+                                                    _DTYPES.get(k_cache.dtype, -1)), q.device)
     st = _lib.load().tl_paged_attn_prefill(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window), float(scale),
@@ -254,8 +261,9 @@ def tl_paged_attn_prefill_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         out = torch.empty((B, T, hq, d), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32)
     if workspace is None:
-        workspace = alloc_workspace(tl_paged_attn_prefill_ring_workspace_size(
-            B, T, hq, hkv, d, block_table.shape[1], ps, ring_pages), q.device)
+        workspace = alloc_workspace(tl_paged_attn_prefill_workspace_size_ex(
+            B, T, hq, hkv, d, block_table.shape[1], ps, ring_pages,
+            _DTYPES.get(k_cache.dtype, -1)), q.device)
     st = _lib.load().tl_paged_attn_prefill_ring(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window), int(ring_pages),

@@ -38,6 +38,7 @@
 namespace tl {
 
 constexpr int kChunk = 16;            // keys per step (one mma N=16 / K=16 tile)
+constexpr float kLazyLog2 = 8.f;      // the running max moves by more than 2^8 only
 #ifndef TL_DECODE_ITEMS
 #define TL_DECODE_ITEMS 12288
 #endif
@@ -93,6 +94,7 @@ struct DecodeParams {
   int32_t B, h_q, h_kv, group, d;
   int32_t num_pages, page_size, window;
   int32_t ring_pages;  // > 0: the table's first ring_pages entries are a ring
+  int32_t ps_shift;    // log2(page_size) when it is a power of two, else -1
   int32_t q_len;       // query tokens per sequence (positions L - q_len .. L - 1)
   int32_t rows;        // q_len * group: M rows of one work item (token-major)
   int32_t hq_all;      // q_len * h_q: outputs per sequence
@@ -100,6 +102,16 @@ struct DecodeParams {
   DecodeWorkspace ws;
   uint32_t* error_word;
 };
+
+// Logical block of key j and its offset in the page (a shift and a mask for
+// power-of-two page sizes: a division by a runtime value costs dozens of
+// dependent instructions, and the producer computes several per chunk).
+__device__ __forceinline__ int page_of(const DecodeParams& P, int j) {
+  return P.ps_shift >= 0 ? j >> P.ps_shift : j / P.page_size;
+}
+__device__ __forceinline__ int in_page(const DecodeParams& P, int j) {
+  return P.ps_shift >= 0 ? j & (P.page_size - 1) : j % P.page_size;
+}
 
 // Block-table entry of logical block blk of sequence b.  With a ring
 // ("How serving works in Tlaloc", section 3, windowed KV pool) logical block
@@ -246,7 +258,11 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 #ifndef TL_DECODE_WARPS
 #define TL_DECODE_WARPS 8
 #endif
-constexpr int kRingW = TL_DECODE_RING;      // stages per warp
+constexpr int kRingW = TL_DECODE_RING;      // stages per warp (16-bit pools)
+// e4m3 pools move half the bytes per chunk: one stage more keeps more bytes
+// in flight per warp (the stream is bound by bytes in flight x latency)
+constexpr int kRingW8 = kRingW + 1;
+constexpr int kMaxRing = kRingW8;
 constexpr int kMaxWarpsW = TL_DECODE_WARPS;
 
 // Per-warp shared memory: kRingW stages of one chunk of K and V as the TMA
@@ -255,6 +271,7 @@ constexpr int kMaxWarpsW = TL_DECODE_WARPS;
 // 16-bit stage layout.
 template <int D, bool KV8 = false>
 struct WarpSmem {
+  static constexpr int kRing = KV8 ? kRingW8 : kRingW;   // stages (and Q slots) per warp
   static constexpr int kRowBytes = D * (KV8 ? 1 : 2);
   static constexpr int kHalves = kRowBytes / 128;          // 128-byte parts of a row
   static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one part
@@ -265,7 +282,7 @@ struct WarpSmem {
     return (rows * D * 2 + 1023) / 1024 * 1024;
   }
   __host__ __device__ static int warp_bytes(int rows) {
-    return kRingW * (kStageBytes + qslot_bytes(rows)) + kWideBytes;
+    return kRing * (kStageBytes + qslot_bytes(rows)) + kWideBytes;
   }
 };
 
@@ -363,9 +380,9 @@ struct ItemSlot {
 };
 
 struct WarpShared {
-  unsigned long long full[kMaxWarpsW][kRingW], qfull[kMaxWarpsW][kRingW];
-  uint32_t stage_mask[kMaxWarpsW][kRingW];
-  ItemSlot slot[kMaxWarpsW][kRingW];
+  unsigned long long full[kMaxWarpsW][kMaxRing], qfull[kMaxWarpsW][kMaxRing];
+  uint32_t stage_mask[kMaxWarpsW][kMaxRing];
+  ItemSlot slot[kMaxWarpsW][kMaxRing];
   int abort_flag;
 };
 
@@ -374,6 +391,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     decode_bf16_kernel(DecodeParams P, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, int box_rows) {
   using L = WarpSmem<D, KV8>;
+  constexpr int R = L::kRing;  // stages per warp
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ WarpShared sh;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -381,8 +399,12 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   unsigned char* smem0 = smem_raw + (sbase0 - smem_u32(smem_raw));
   volatile int* abort_flag = &sh.abort_flag;
   if (threadIdx.x == 0) sh.abort_flag = 0;
+  if (threadIdx.x == 32) {  // the pools' tensor maps into the descriptor cache
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+  }
   if (lane == 0) {
-    for (int i = 0; i < kRingW; ++i) {
+    for (int i = 0; i < R; ++i) {
       mbar_init(smem_u32(&sh.full[w][i]), 1);
       mbar_init(smem_u32(&sh.qfull[w][i]), 1);
     }
@@ -392,8 +414,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 
   const int qslot = L::qslot_bytes(P.rows);
   const uint32_t ring = sbase0 + w * L::warp_bytes(P.rows);
-  const uint32_t qbase = ring + kRingW * L::kStageBytes;
-  const uint32_t wide = qbase + kRingW * qslot;  // e4m3 pools: the widened chunk
+  const uint32_t qbase = ring + R * L::kStageBytes;
+  const uint32_t wide = qbase + R * qslot;  // e4m3 pools: the widened chunk
   const unsigned char* qbase_ptr = smem0 + (qbase - sbase0);
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
@@ -410,6 +432,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   // inext2 (descriptor loading), grab (lane 0: the atomic for the one after)
   ItemInfo icur, inext, inext2;
   bool icur_live = false;
+  int icur_last_blk = 0;
   int icur_c = 0, iwin_blk0 = 0, iwin = -1, nwin_blk0 = 0, nwin = -1;
   int id_next = total_items, id_next2 = total_items;
   int grab = 0;
@@ -424,9 +447,9 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
     if (id_next < total_items) {
       describe_item(P, id_next, inext);
-      nwin_blk0 = inext.c_begin * kChunk / P.page_size;
+      nwin_blk0 = page_of(P, inext.c_begin * kChunk);
       const int blk = nwin_blk0 + lane;
-      nwin = blk <= inext.p / P.page_size
+      nwin = blk <= page_of(P, inext.p)
                  ? table_entry(P, inext.b, blk)
                  : -1;
     }
@@ -438,11 +461,12 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   auto start_item = [&]() -> bool {
     if (id_next >= total_items) return false;
     icur = inext;
+    icur_last_blk = page_of(P, icur.p);
     iwin_blk0 = nwin_blk0;
     iwin = nwin;
     icur_c = icur.c_begin;
     icur_live = true;
-    const int q = items_issued % kRingW;
+    const int q = items_issued % R;
     if (lane == 0) {
       ItemSlot& d = sh.slot[w][q];
       d.b = icur.b; d.g = icur.g; d.lo = icur.lo; d.p = icur.p;
@@ -461,9 +485,9 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     id_next = id_next2;
     inext = inext2;
     if (id_next < total_items) {
-      nwin_blk0 = inext.c_begin * kChunk / P.page_size;
+      nwin_blk0 = page_of(P, inext.c_begin * kChunk);
       const int blk = nwin_blk0 + lane;
-      nwin = blk <= inext.p / P.page_size
+      nwin = blk <= page_of(P, inext.p)
                  ? table_entry(P, inext.b, blk)
                  : -1;
     }
@@ -476,11 +500,11 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   // Issue the next chunk of the stream (starting a new item when needed).
   auto issue_next = [&]() {
     if (!icur_live && !start_item()) return;
-    const int stage = (int)(gs_issue % kRingW);
+    const int stage = (int)(gs_issue % R);
     const int j0 = icur_c * kChunk;
-    const int last_blk = icur.p / P.page_size;
-    const int bmin = j0 / P.page_size;
-    const int bmax = min((j0 + kChunk - 1) / P.page_size, last_blk);
+    const int last_blk = icur_last_blk;
+    const int bmin = page_of(P, j0);
+    const int bmax = min(page_of(P, j0 + kChunk - 1), last_blk);
     if (bmin < iwin_blk0 || bmax >= iwin_blk0 + 32) {  // the next 32 blocks
       iwin_blk0 = bmin;
       const int blk = iwin_blk0 + lane;
@@ -489,7 +513,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
                  : -1;
     }
     const int jr = j0 + (lane & 15);
-    const int pr = __shfl_sync(0xffffffffu, iwin, (jr / P.page_size - iwin_blk0) & 31);
+    const int pr = __shfl_sync(0xffffffffu, iwin, (page_of(P, jr) - iwin_blk0) & 31);
     bool live = jr >= icur.lo && jr <= icur.p;
     if (live && (pr < 0 || pr >= P.num_pages)) {
       if (lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
@@ -497,10 +521,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     }
     const uint32_t mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
     const int jb = j0 + rq_box * box_rows;
-    const int blk = jb / P.page_size;
+    const int blk = page_of(P, jb);
     const int pb = __shfl_sync(0xffffffffu, iwin, (blk - iwin_blk0) & 31);
     const bool box_ok = blk <= last_blk && pb >= 0 && pb < P.num_pages;
-    const int slot0 = box_ok ? pb * P.page_size + jb % P.page_size : n_slots;
+    const int slot0 = box_ok ? pb * P.page_size + in_page(P, jb) : n_slots;
     const uint32_t bar = smem_u32(&sh.full[w][stage]);
     if (lane == 0) {
       sh.stage_mask[w][stage] = mask;
@@ -515,7 +539,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     if (++icur_c == icur.c_end) icur_live = false;
   };
 
-  for (int t = 0; t < kRingW - 1; ++t) issue_next();
+  for (int t = 0; t < R - 1; ++t) issue_next();
 
   // -------------------------------------------------------- compute side
   const int qr = lane >> 2, qc = (lane & 3) * 2;
@@ -523,8 +547,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   int items_c = 0;
   bool stop = false;
   while (!stop && items_c < items_issued) {
-    const int q = items_c % kRingW;
-    if (!mbar_wait(smem_u32(&sh.qfull[w][q]), (items_c / kRingW) & 1, abort_flag)) break;
+    const int q = items_c % R;
+    if (!mbar_wait(smem_u32(&sh.qfull[w][q]), (items_c / R) & 1, abort_flag)) break;
     const ItemSlot it = sh.slot[w][q];
     const unsigned char* qs = qbase_ptr + q * qslot;
     uint32_t qa[D / 16][4];
@@ -563,9 +587,9 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     const int lr0 = (P.window > 0 && pr0 - P.window + 1 > 0) ? pr0 - P.window + 1 : 0;
     const int lr1 = (P.window > 0 && pr1 - P.window + 1 > 0) ? pr1 - P.window + 1 : 0;
     for (int c = it.c_begin; c < it.c_end; ++c, ++gs_c) {
-      issue_next();  // keeps kRingW-1 chunks in flight ahead of this one
-      const int stage = (int)(gs_c % kRingW);
-      if (!mbar_wait(smem_u32(&sh.full[w][stage]), (gs_c / kRingW) & 1, abort_flag)) {
+      issue_next();  // keeps R-1 chunks in flight ahead of this one
+      const int stage = (int)(gs_c % R);
+      if (!mbar_wait(smem_u32(&sh.full[w][stage]), (gs_c / R) & 1, abort_flag)) {
         stop = true;
         break;
       }
@@ -597,9 +621,11 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         kaddr = wide;
         vaddr = wide + 2 * kChunk * 128;
       }
-      // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys)
+      // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys); even and
+      // odd K steps accumulate separately (two independent MMA chains)
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       {
+        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int mi = lane >> 3, ri = lane & 7;
         const int tok = (mi >> 1) * 8 + ri;
 #pragma unroll
@@ -608,9 +634,14 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4),
                       b0, b1, b2, b3);
-          mma_16816<KV8>(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_16816<KV8>(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          float(*acc)[4] = (ks & 1) ? s2 : s;
+          mma_16816<KV8>(acc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_16816<KV8>(acc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
         }
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[n][e] += s2[n][e];
       }
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -633,7 +664,9 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       }
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      const float mn0 = fmaxf(m0, mx0);
+      // lazy running max: the base moves only when the chunk's max passes it
+      // by more than 2^8 (P stays below 256), so O is rescaled rarely
+      const float mn0 = (m0 == -INFINITY || mx0 > m0 + kLazyLog2) ? fmaxf(m0, mx0) : m0;
       const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
       const float c0 = fast_exp2(m0 - base0);
       m0 = mn0;
@@ -648,7 +681,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       if (TWO_ROWS) {
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn1 = fmaxf(m1, mx1);
+        const float mn1 = (m1 == -INFINITY || mx1 > m1 + kLazyLog2) ? fmaxf(m1, mx1) : m1;
         const float base1 = mn1 == -INFINITY ? 0.f : mn1;
         c1 = fast_exp2(m1 - base1);
         m1 = mn1;
@@ -661,12 +694,14 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       }
       // rows 8-15 hold either the second half of the group (TWO_ROWS) or the
       // low bf16 part of rows 0-7's probabilities; both rescale with their row
+      if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= c0;
-        o[n][1] *= c0;
-        o[n][2] *= c1;
-        o[n][3] *= c1;
+        for (int n = 0; n < D / 8; ++n) {
+          o[n][0] *= c0;
+          o[n][1] *= c0;
+          o[n][2] *= c1;
+          o[n][3] *= c1;
+        }
       }
       // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
       uint32_t h0, l0w, h2, l2w;
@@ -762,9 +797,9 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   // the latest phase of its barrier)
   bool drained = true;
   for (uint32_t i = gs_c; i < gs_issue; ++i)
-    drained &= mbar_drain(smem_u32(&sh.full[w][i % kRingW]), (i / kRingW) & 1);
+    drained &= mbar_drain(smem_u32(&sh.full[w][i % R]), (i / R) & 1);
   for (int i = items_c; i < items_issued; ++i)
-    drained &= mbar_drain(smem_u32(&sh.qfull[w][i % kRingW]), (i / kRingW) & 1);
+    drained &= mbar_drain(smem_u32(&sh.qfull[w][i % R]), (i / R) & 1);
   if (!drained) *abort_flag = 1;
   __syncthreads();  // every wait above is bounded, so every thread gets here
   if (threadIdx.x == 0 && sh.abort_flag) report(P.error_word, TL_DEVERR_TIMEOUT);
@@ -1008,6 +1043,10 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   P.page_size = page_size;
   P.window = window;
   P.ring_pages = ring_pages;
+  P.ps_shift = -1;
+  if ((page_size & (page_size - 1)) == 0)
+    for (int s = 0; s < 31; ++s)
+      if ((1 << s) == page_size) P.ps_shift = s;
   P.q_len = q_len;
   P.rows = rows;
   P.hq_all = q_len * h_q;

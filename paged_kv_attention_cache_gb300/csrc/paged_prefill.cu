@@ -76,6 +76,8 @@ struct PrefillParams {
   int32_t* row_start;    // [B] first key of each row's fp16 V copy (a multiple of kBN)
   int32_t v_keys;        // keys per row (and KV head) of the fp16 V copy
   int32_t ring_pages;    // > 0: the table's first ring_pages entries are a ring
+  int32_t kv8;           // e4m3 pools: K is read from a bf16 copy like V
+  uint16_t* ws_k;        // e4m3 pools: the bf16 copy of K, laid out like the V copy
 };
 
 // Position bound of the call: the table width, or none for a ring (whose
@@ -105,19 +107,22 @@ constexpr int kTcSmem = kTcQB * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 8192;   // key-tile counts at or above 8191 share the last bucket
 
-// Workspace layout: [counter | pair_tiles | order | row_start | fp16 V], each
-// part 256-byte aligned; the V copy is [B][h_kv][v_keys][128].
+// Workspace layout: [counter | pair_tiles | order | row_start | fp16 V
+// (| bf16 K for e4m3 pools)], each part 256-byte aligned; the copies are
+// [B][h_kv][v_keys][128].
 struct WsLayout {
-  size_t tiles, order, rows, v, total;
+  size_t tiles, order, rows, v, k, total;
 };
-inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_keys) {
+inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_keys, bool kv8) {
   const size_t pairs = (size_t)(B * n_pairs) * 4;
+  const size_t copy = (size_t)B * h_kv * (size_t)v_keys * 128 * 2;
   WsLayout L;
   L.tiles = 256;
   L.order = L.tiles + align_up(pairs, 256);
   L.rows = L.order + align_up(pairs, 256);
   L.v = L.rows + align_up((size_t)B * 4, 256);
-  L.total = L.v + (size_t)B * h_kv * (size_t)v_keys * 128 * 2;
+  L.k = L.v + copy;
+  L.total = L.k + (kv8 ? copy : 0);
   return L;
 }
 // Keys per row of the V copy: the table's positions, or for a ring the
@@ -209,6 +214,23 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 constexpr int kCvtUnroll = 16;
 constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
 
+// Two e4m3 codes (low byte first) as an fp16 pair, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  const uint16_t c = (uint16_t)two;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(c));
+  return r;
+}
+// Two e4m3 codes as a bf16 pair, exact (every e4m3 value is a bf16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  float lo, hi;
+  unpack_f16x2(e4m3x2_to_f16x2(two), lo, hi);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool KV8>
 __global__ void __launch_bounds__(kCvtThreads)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int* counter) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
@@ -298,8 +320,9 @@ __global__ void __launch_bounds__(kCvtThreads)
   const int units = P.h_kv * 16;                                // 16-byte units per key
   const int total = (r1 - r0) * units;
   uint32_t vmax = 0;  // max |bf16 bits| seen, per half-word
+  // units of 8 elements: 16 bytes of a bf16 row, 8 bytes of an e4m3 row
   for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
-    uint4 x[kCvtUnroll];
+    uint4 x[kCvtUnroll];  // bf16 V, or (e4m3) V in .x.y and K in .z.w
 #pragma unroll
     for (int i = 0; i < kCvtUnroll; ++i) {
       const int idx = base + i * kCvtThreads + (int)threadIdx.x;
@@ -307,11 +330,18 @@ __global__ void __launch_bounds__(kCvtThreads)
       if (idx < total) {
         const int r = r0 + idx / units, u = idx % units;
         const int page = s_page[r];
-        if (page >= 0)
-          x[i] = __ldg(reinterpret_cast<const uint4*>(
-                           P.v_cache +
-                           ((size_t)page * P.page_size + (k0 + r) % P.page_size) * P.h_kv * 128) +
-                       u);
+        if (page >= 0) {
+          const size_t row = ((size_t)page * P.page_size + (k0 + r) % P.page_size) * P.h_kv * 128;
+          if (KV8) {
+            const uint8_t* v8 = reinterpret_cast<const uint8_t*>(P.v_cache);
+            const uint8_t* k8 = reinterpret_cast<const uint8_t*>(P.k_cache);
+            const uint2 a = __ldg(reinterpret_cast<const uint2*>(v8 + row) + u);
+            const uint2 c = __ldg(reinterpret_cast<const uint2*>(k8 + row) + u);
+            x[i] = make_uint4(a.x, a.y, c.x, c.y);
+          } else {
+            x[i] = __ldg(reinterpret_cast<const uint4*>(P.v_cache + row) + u);
+          }
+        }
       }
     }
 #pragma unroll
@@ -319,14 +349,23 @@ __global__ void __launch_bounds__(kCvtThreads)
       const int idx = base + i * kCvtThreads + (int)threadIdx.x;
       if (idx < total) {
         const int r = r0 + idx / units, u = idx % units;
+        const size_t dst =
+            (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 + (u & 15) * 8;
         uint4 y = x[i];
-        vmax = max_u16x2(vmax, max_u16x2(max_u16x2(y.x & 0x7fff7fffu, y.y & 0x7fff7fffu),
-                                         max_u16x2(y.z & 0x7fff7fffu, y.w & 0x7fff7fffu)));
-        y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z),
-                       bf16x2_to_f16x2(y.w));
-        *reinterpret_cast<uint4*>(
-            ws + (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 +
-            (u & 15) * 8) = y;
+        if (KV8) {  // e4m3 values are exact in both fp16 and bf16
+          *reinterpret_cast<uint4*>(ws + dst) =
+              make_uint4(e4m3x2_to_f16x2(y.x), e4m3x2_to_f16x2(y.x >> 16),
+                         e4m3x2_to_f16x2(y.y), e4m3x2_to_f16x2(y.y >> 16));
+          *reinterpret_cast<uint4*>(P.ws_k + dst) =
+              make_uint4(e4m3x2_to_bf16x2(y.z), e4m3x2_to_bf16x2(y.z >> 16),
+                         e4m3x2_to_bf16x2(y.w), e4m3x2_to_bf16x2(y.w >> 16));
+        } else {
+          vmax = max_u16x2(vmax, max_u16x2(max_u16x2(y.x & 0x7fff7fffu, y.y & 0x7fff7fffu),
+                                           max_u16x2(y.z & 0x7fff7fffu, y.w & 0x7fff7fffu)));
+          y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z),
+                         bf16x2_to_f16x2(y.w));
+          *reinterpret_cast<uint4*>(ws + dst) = y;
+        }
       }
     }
   }
@@ -567,9 +606,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.k_full[st]), kTcKVBytes);
           __syncwarp();
-          if (lane < 2 * nbox)
+          if (P.kv8) {  // e4m3 pools: the bf16 copy, laid out like the V copy
+            if (lane < 2)
+              tma_load_3d(sK + st * kTcKVBytes + lane * (kTcKVBytes / 2), &kmap, lane * 64,
+                          key0 - vstart, it.b * P.h_kv + it.g, smem_u32(&sh.k_full[st]));
+          } else if (lane < 2 * nbox) {
             tma_load_3d(sK + st * kTcKVBytes + boff, &kmap, half * 64, it.g, slot0,
                         smem_u32(&sh.k_full[st]));
+          }
           ++k_issued;
         }
         {
@@ -862,13 +906,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 namespace tl {
 
 static size_t prefill_ws_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv, int32_t d,
-                              int32_t max_pages_per_seq, int32_t page_size, int32_t ring_pages) {
+                              int32_t max_pages_per_seq, int32_t page_size, int32_t ring_pages,
+                              tl_dtype dtype) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv ||
-      max_pages_per_seq <= 0 || page_size <= 0 || ring_pages < 0)
+      max_pages_per_seq <= 0 || page_size <= 0 || ring_pages < 0 ||
+      (dtype != TL_BF16 && dtype != TL_FP8_E4M3))
     return 0;
   const int tpt = std::max(1, 128 / (h_q / h_kv));
   const int64_t n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
-  return ws_layout(B, n_pairs, h_kv, v_copy_keys(max_pages_per_seq, page_size, ring_pages)).total;
+  return ws_layout(B, n_pairs, h_kv, v_copy_keys(max_pages_per_seq, page_size, ring_pages),
+                   dtype == TL_FP8_E4M3)
+      .total;
 }
 
 static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_cache,
@@ -889,12 +937,15 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
     return TL_ERR_INVALID_ARG;
   if (h_q % h_kv) return TL_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale > 3.0e38f) return TL_ERR_INVALID_ARG;
-  if (dtype != TL_BF16 || d != 128 || (page_size & (page_size - 1)) || page_size < 8 ||
-      page_size > 128)
+  // (e4m3 pools: q and out as for bf16; the pools hold one byte per element)
+  if ((dtype != TL_BF16 && dtype != TL_FP8_E4M3) || d != 128 || (page_size & (page_size - 1)) ||
+      page_size < 8 || page_size > 128)
     return TL_ERR_UNSUPPORTED;
   if ((int64_t)max_pages_per_seq * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
+  const bool kv8 = dtype == TL_FP8_E4M3;
+  if (kv8 && (!aligned16(k_cache) || !aligned16(v_cache))) return TL_ERR_INVALID_ARG;
   const size_t ws_need = prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size,
-                                         ring_pages);
+                                         ring_pages, dtype);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < ws_need)
     return TL_ERR_WORKSPACE;
   PrefillParams P;
@@ -925,7 +976,7 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   const int64_t v_keys = v_copy_keys(max_pages_per_seq, page_size, ring_pages);
   if (v_keys >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
-  const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys);
+  const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys, kv8);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   int* counter = reinterpret_cast<int*>(wsb);
   uint16_t* ws_v = reinterpret_cast<uint16_t*>(wsb + L.v);
@@ -934,6 +985,8 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   P.order = reinterpret_cast<int32_t*>(wsb + L.order);
   P.row_start = reinterpret_cast<int32_t*>(wsb + L.rows);
   P.v_keys = (int32_t)v_keys;
+  P.kv8 = kv8 ? 1 : 0;
+  P.ws_k = kv8 ? reinterpret_cast<uint16_t*>(wsb + L.k) : nullptr;
   CUtensorMap qmap, kmap, vmap, omap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
@@ -953,8 +1006,10 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
     const uint64_t os[3] = {128 * 4, (uint64_t)h_q * 128 * 4, (uint64_t)T * h_q * 128 * 4};
     const uint32_t ob[4] = {32, (uint32_t)group, (uint32_t)tpt, 1};
     if (!encode_f32_tensor_map(&omap, out, 4, od, os, ob, true)) return TL_ERR_CUDA;
+    // e4m3 pools: K is read from its bf16 copy, with the V copy's map shape
     if (!encode_bf16_tensor_map(&qmap, q, 3, qd, qs, qb, true) ||
-        !encode_bf16_tensor_map(&kmap, k_cache, 3, kd, ks, kb, true) ||
+        !(kv8 ? encode_bf16_tensor_map(&kmap, P.ws_k, 3, vd, vs, vb, true)
+              : encode_bf16_tensor_map(&kmap, k_cache, 3, kd, ks, kb, true)) ||
         !encode_bf16_tensor_map(&vmap, ws_v, 3, vd, vs, vb, true))
       return TL_ERR_CUDA;
   }
@@ -964,8 +1019,11 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   const int64_t n_items = (int64_t)n_pairs * B * h_kv;
   if (n_items > 0x7fffffff - 65536) return TL_ERR_UNSUPPORTED;
   const int grid = (int)std::min<int64_t>(num_sms(), n_items);
-  prefill_v_f16_kernel<<<dim3((unsigned)((v_keys + kCvtKeys - 1) / kCvtKeys), B), kCvtThreads, 0,
-                         (cudaStream_t)stream>>>(P, ws_v, counter);
+  const dim3 cvt_grid((unsigned)((v_keys + kCvtKeys - 1) / kCvtKeys), B);
+  if (kv8)
+    prefill_v_f16_kernel<true><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
+  else
+    prefill_v_f16_kernel<false><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
   prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(P);
   prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
       P, qmap, kmap, vmap, omap, box_rows, counter);
@@ -985,7 +1043,15 @@ extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int
                                                        int32_t h_kv, int32_t d,
                                                        int32_t max_pages_per_seq,
                                                        int32_t page_size) {
-  return tl::prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size, 0);
+  return tl::prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size, 0, TL_BF16);
+}
+
+extern "C" size_t tl_paged_attn_prefill_workspace_size_ex(int32_t B, int32_t T, int32_t h_q,
+                                                          int32_t h_kv, int32_t d,
+                                                          int32_t max_pages_per_seq,
+                                                          int32_t page_size, int32_t ring_pages,
+                                                          tl_dtype dtype) {
+  return tl::prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size, ring_pages, dtype);
 }
 
 extern "C" size_t tl_paged_attn_prefill_ring_workspace_size(int32_t B, int32_t T, int32_t h_q,
@@ -994,7 +1060,8 @@ extern "C" size_t tl_paged_attn_prefill_ring_workspace_size(int32_t B, int32_t T
                                                             int32_t page_size,
                                                             int32_t ring_pages) {
   if (ring_pages <= 0) return 0;
-  return tl::prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size, ring_pages);
+  return tl::prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size, ring_pages,
+                             TL_BF16);
 }
 
 extern "C" tl_status tl_paged_attn_prefill(const void* q, const void* k_cache,

@@ -135,3 +135,50 @@ def test_fp8_multi_token_decode():
         ref = oracle.paged_prefill(case.q[row:row + 1], k8, v8, case.block_table[row:row + 1],
                                    case.positions[row:row + 1], case.scale)
         assert_close(out[row], ref, f"fp8 multi-token row {row}")
+
+
+def _fp8_prefill_case(case):
+    k8 = case.k_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    v8 = case.v_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    kn, vn = case.k_new.view(-1, case.Hkv, case.d), case.v_new.view(-1, case.Hkv, case.d)
+    oracle.kv_cache_write_fp8(kn, vn, k8, v8, case.slot_mapping)
+    return k8, v8
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_fp8_prefill_matches_the_oracle(window):
+    case = wl.prefill_case([0, 40, 500], [100, 3000, 0], T=512, Hq=32, Hkv=8, d=128, seed=74,
+                           window=window)
+    k8, v8 = _fp8_prefill_case(case)
+    k8t = torch.from_numpy(k8).view(torch.float8_e4m3fn).to(DEV)
+    v8t = torch.from_numpy(v8).view(torch.float8_e4m3fn).to(DEV)
+    err = _err()
+    out = tl.tl_paged_attn_prefill(case.q.to(DEV), k8t, v8t, case.block_table.to(DEV),
+                                   case.positions.to(DEV), case.scale, window=window,
+                                   error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rng = np.random.default_rng(75)
+    for row in range(case.B):
+        ts = sorted({0, case.T - 1, case.pads[row]} | set(rng.integers(0, case.T, 10).tolist()))
+        ts = [t for t in ts if t < case.T]
+        ref = oracle.paged_prefill(case.q[row:row + 1], k8, v8, case.block_table[row:row + 1],
+                                   case.positions[row:row + 1], case.scale, window=window,
+                                   tokens=np.asarray(ts, np.int64))
+        assert_close(out[row, ts], ref, f"fp8 prefill row {row}")
+
+
+def test_fp8_prefill_full_size_sampled():
+    case = wl.batched_prefill(seed=0)
+    k8, v8 = _fp8_prefill_case(case)
+    out = tl.tl_paged_attn_prefill(case.q.to(DEV), torch.from_numpy(k8).view(torch.float8_e4m3fn).to(DEV),
+                                   torch.from_numpy(v8).view(torch.float8_e4m3fn).to(DEV),
+                                   case.block_table.to(DEV), case.positions.to(DEV), case.scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(76)
+    for row in (0, 4, 7):
+        ts = sorted(set(rng.integers(case.pads[row], case.T, 8).tolist()) | {case.T - 1})
+        ref = oracle.paged_prefill(case.q[row:row + 1], k8, v8, case.block_table[row:row + 1],
+                                   case.positions[row:row + 1], case.scale,
+                                   tokens=np.asarray(ts, np.int64), threads=0)
+        assert_close(out[row, ts], ref, f"fp8 prefill (full size) row {row}")
