@@ -134,6 +134,33 @@ TL_DEVINLINE void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int 
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+// The same load with an L2 eviction-priority policy (see l2_evict_first).
+TL_DEVINLINE void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                   uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar),
+      "l"(policy)
+      : "memory");
+}
+// L2 policies: data read once (the KV pools in decode) goes first when L2
+// needs room; data written to be read back soon (split partials) stays.
+TL_DEVINLINE uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+TL_DEVINLINE uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+TL_DEVINLINE void st_f32x2_hint(float* ptr, float a, float b, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(ptr), "f"(a), "f"(b),
+               "l"(policy)
+               : "memory");
+}
 // Tiled TMA store of a 4-D box from shared memory (bulk-group completion);
 // elements past the tensor's extent are not written.
 TL_DEVINLINE void tma_store_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3,

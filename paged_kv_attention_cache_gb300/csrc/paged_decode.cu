@@ -12,23 +12,31 @@
 //
 // Launches on the caller's stream:
 //   1. decode_plan_kernel (1 CTA): per sequence the 16-key chunks it reads
-//      ([lo/16, p/16]); a split size (in chunks) giving about kTargetItems
-//      work items for the batch; an exclusive scan of the splits per
-//      sequence, and one descriptor per split.  Zeroes the work counter.
-//   2. bf16: decode_bf16_kernel, persistent, one CTA per SM, every warp
-//      independent: a warp takes work items (split x KV head) from an atomic
-//      counter and streams their chunks (16 keys of K and V, 8 KiB at d=128)
-//      through its own ring of shared-memory stages filled by TMA; Q.K^T and
-//      P.V run on mma.sync m16n8k16 with the query-head group (times the
-//      q_len tokens, token-major) as the M rows, each row masked to its own
-//      causal range, online softmax in registers (details below).  At the end of an item
-//      the warp writes from its registers:
-//      a sequence with one split writes its output directly, otherwise the
-//      item writes a partial.
+//      ([lo/16, p/16]), cut into pieces (splits): bulk pieces sized for about
+//      kTargetItems work items, then a last round of small pieces from every
+//      long sequence's end; one descriptor per piece in item order, partial
+//      indices contiguous per sequence.  Zeroes the work counter and writes
+//      the zero output of sequences with nothing to read.
+//   2. bf16 / e4m3: decode_bf16_kernel, a programmatic dependent launch of
+//      the plan (it becomes resident while the plan runs and waits for its
+//      results), persistent, one CTA per SM, every warp independent: a warp
+//      takes work items (piece x KV head) from an atomic counter and streams
+//      their chunks (16 keys of K and V, 8 KiB at d=128) through its own ring
+//      of shared-memory stages filled by TMA; Q.K^T and P.V run on mma.sync
+//      m16n8k16 with the query-head group (times the q_len tokens,
+//      token-major) as the M rows, each row masked to its own causal range,
+//      online softmax in registers (details below).  At the end of an item
+//      the warp writes from its registers: a sequence with one piece writes
+//      its output directly, otherwise the item writes a partial.
 //      f32: decode_f32_kernel (CUDA-core dots in f32) writes partials.
 //   3. decode_combine_kernel merges the partials of sequences with several
-//      splits, one warp per (sequence, query head), and writes the zero
-//      output of sequences with nothing to read.
+//      pieces, one warp per (sequence, query head); after the bf16 / e4m3
+//      kernel it is a programmatic dependent launch too.  (Merging inside
+//      the attention kernel, by the last piece of each (sequence, KV head)
+//      to finish, measured slower: every sequence's last piece is in the
+//      small round, so all merges fall in the kernel's last microseconds,
+//      each a chain of dependent partial reads against a saturated memory
+//      system.)
 // Every reduction has a fixed order, so results repeat bit for bit and do not
 // depend on the pool's page placement.
 #include <algorithm>
@@ -47,8 +55,10 @@ constexpr int kMinSplitChunks = 8;    // 128 keys
 constexpr int kDecodeWarps = 4;       // f32 kernel
 constexpr int kDecodeThreads = kDecodeWarps * 32;
 
+// Pieces per call: the plan keeps them within ceil(kTargetItems / h_kv) + 2B
+// (each of its two rounds rounds up once per sequence).
 inline int64_t decode_max_splits(int B, int h_kv) {
-  return (int64_t)(kTargetItems + h_kv - 1) / h_kv + B;
+  return (int64_t)(kTargetItems + h_kv - 1) / h_kv + 2 * (int64_t)B;
 }
 
 struct DecodeWorkspace {
@@ -145,69 +155,172 @@ __device__ __forceinline__ int seq_chunks(const DecodeParams& P, int b, bool rep
 }
 
 // ------------------------------------------------------------------ plan --
+//
+// Work items are pieces of a sequence's chunk range (times the KV heads),
+// taken by the warps in item order from an atomic counter.  The order ends
+// with a round of small pieces: the last ~15% of every sequence longer than
+// 2 * kMinSplitChunks chunks is cut into pieces of kSmallChunks (or more, to
+// stay in the split budget), and those pieces come after every bulk piece.
+// The warps that finish their last bulk piece early then take the small
+// ones, so they all run out of work within about one small piece of each
+// other.  A piece's partial index keeps a sequence's pieces contiguous for
+// the merge whatever their place in the order.
 
-__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int target_splits) {
-  __shared__ long long red[32];
-  __shared__ int warp_incl[32];
-  __shared__ int carry_s;
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5;
-  const int nwarps = nt >> 5;
-  long long total = 0;
-  for (int b = tid; b < P.B; b += nt) total += seq_chunks(P, b, true);
+constexpr int kSmallChunks = 4;  // 64 keys
+
+__device__ __forceinline__ int tail_chunks(int n) {
+  return n < 2 * kMinSplitChunks ? 0 : min(n, (3 * n + 19) / 20);
+}
+
+// Sums of two values over the block (every thread gets them); red holds one
+// slot per warp for each.
+__device__ __forceinline__ void block_sum2(long long& x, long long& y, long long (*red)[32]) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-  if (lane == 0) red[wid] = total;
-  if (tid == 0) carry_s = 0;
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y += __shfl_xor_sync(0xffffffffu, y, o);
+  }
+  if (lane == 0) {
+    red[0][wid] = x;
+    red[1][wid] = y;
+  }
   __syncthreads();
-  long long total_chunks = 0;
-  for (int w = 0; w < nwarps; ++w) total_chunks += red[w];
-  const long long s = (total_chunks + target_splits - 1) / target_splits;
-  const int split = (int)(s < kMinSplitChunks ? kMinSplitChunks : s);
-  // exclusive scan of the splits per sequence, nt sequences at a time
-  for (int base = 0; base < P.B; base += nt) {
-    const int b = base + tid;
-    const int n = b < P.B ? (seq_chunks(P, b, false) + split - 1) / split : 0;
-    int x = n;  // inclusive scan within the warp
+  x = lane < nw ? red[0][lane] : 0;
+  y = lane < nw ? red[1][lane] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y += __shfl_xor_sync(0xffffffffu, y, o);
+  }
+  __syncthreads();  // red is reused by the next call
+}
+
+// Exclusive scan of x over the block in thread order; total gets the sum.
+__device__ __forceinline__ long long block_excl_scan(long long x, long long* tmp,
+                                                     long long& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  long long inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) tmp[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    long long v = lane < nw ? tmp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const long long y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
     }
-    if (lane == 31) warp_incl[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-      int v = lane < nwarps ? warp_incl[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
+    tmp[lane] = v;
+  }
+  __syncthreads();
+  const long long before = (wid > 0 ? tmp[wid - 1] : 0) + inc - x;
+  total = tmp[nw - 1];
+  __syncthreads();
+  return before;
+}
+
+// One CTA.  Thread t keeps sequence t's range in registers (sequences past
+// the block size are re-read in each pass); three block reductions fix the
+// piece sizes, and one scan of (bulk pieces << 32 | small pieces) places
+// every piece; a warp per sequence then writes its pieces' descriptors.  first_dynamic: items below it are taken without the counter
+// (the attention kernel's warp w starts with item w).
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int target_splits,
+                                                           int first_dynamic) {
+  __shared__ long long red[2][32];
+  __shared__ long long tmp[32];
+  __shared__ int4 rec[1024];  // per sequence of a round: first bulk / small position, counts
+  __shared__ int2 rng[1024];  // its lo, p
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+  // the attention kernel may launch now: it waits for this grid's results
+  // (griddepcontrol.wait) after its own set-up
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  int lo0 = 0, p0 = -1, n0 = 0;  // sequence tid
+  if (tid < P.B) {
+    seq_range(P, tid, lo0, p0, true);
+    n0 = p0 < 0 ? 0 : p0 / kChunk - lo0 / kChunk + 1;
+  }
+  // chunks of the batch and of the small-piece round
+  long long C = tid < P.B ? n0 : 0, T = tail_chunks(n0);
+  for (int b = tid + nt; b < P.B; b += nt) {
+    const int n = seq_chunks(P, b, true);
+    C += n;
+    T += tail_chunks(n);
+  }
+  block_sum2(C, T, red);
+  // small pieces: at most target/2 + B of them
+  const long long half = max(target_splits / 2, 1);
+  const int small = (int)max((long long)kSmallChunks, (T + P.B + half - 1) / half);
+  long long TP = (tail_chunks(n0) + small - 1) / small, unused = 0;
+  for (int b = tid + nt; b < P.B; b += nt) TP += (tail_chunks(seq_chunks(P, b, false)) + small - 1) / small;
+  block_sum2(TP, unused, red);
+  // bulk pieces: at most (target + B - TP) + B of them, so every piece fits
+  // the target + 2B descriptors and partials the workspace holds
+  const long long budget = (long long)target_splits + P.B - TP;
+  const long long sb = (C - T + budget - 1) / budget;
+  const int split = (int)(sb < kMinSplitChunks ? kMinSplitChunks : sb);
+  long long NB = (n0 - tail_chunks(n0) + split - 1) / split;
+  for (int b = tid + nt; b < P.B; b += nt) {
+    const int n = seq_chunks(P, b, false);
+    NB += (n - tail_chunks(n) + split - 1) / split;
+  }
+  block_sum2(NB, unused, red);
+  // descriptors: bulk pieces at [0, NB) and small pieces at [NB, NB + TP) in
+  // sequence order; partial indices split_off[b] + k, bulk pieces first
+  long long carry = 0;  // (bulk << 32) | small pieces before this round of sequences
+  for (int base = 0; base < P.B; base += nt) {
+    const int b = base + tid;
+    int lo = lo0, p = p0, n = n0;
+    if (base > 0) {
+      lo = 0; p = -1; n = 0;
+      if (b < P.B) {
+        seq_range(P, b, lo, p, false);
+        n = p < 0 ? 0 : p / kChunk - lo / kChunk + 1;
       }
-      warp_incl[lane] = v;
+    } else if (b >= P.B) {
+      n = 0;
     }
-    __syncthreads();
-    const int carry = carry_s;
-    const int before = carry + (wid > 0 ? warp_incl[wid - 1] : 0) + x - n;
+    const int t = tail_chunks(n);
+    const int nb = (n - t + split - 1) / split, ntl = (t + small - 1) / small;
+    long long tot;
+    const long long pos = carry + block_excl_scan(((long long)nb << 32) | ntl, tmp, tot);
     if (b < P.B) {
-      P.ws.split_off[b] = before;
-      int lo, p;
-      seq_range(P, b, lo, p, false);
-      const int c0 = lo / kChunk, c1 = p / kChunk + 1;
-      for (int k = 0; k < n; ++k) {
+      const int pos_b = (int)(pos >> 32), pos_t = (int)(pos & 0xffffffffll);
+      P.ws.split_off[b] = pos_b + pos_t;  // partial index of the sequence's first piece
+      rec[tid] = make_int4(pos_b, pos_t, nb, ntl);
+      rng[tid] = make_int2(lo, p);
+    }
+    __syncthreads();
+    for (int j = wid; j < min(nt, P.B - base); j += nw) {
+      const int4 r = rec[j];
+      const int lo_j = rng[j].x, p_j = rng[j].y, bj = base + j;
+      const int n_j = p_j < 0 ? 0 : p_j / kChunk - lo_j / kChunk + 1;
+      const int c0 = lo_j / kChunk, c1 = c0 + n_j, cm = c1 - tail_chunks(n_j);
+      const int first = r.x + r.y, pieces = r.z + r.w;
+      for (int k = lane; k < r.z; k += 32) {
         const int cb = c0 + k * split;
-        P.ws.desc[2 * (before + k)] = make_int4(b, cb, min(c1, cb + split), n);
-        P.ws.desc[2 * (before + k) + 1] = make_int4(lo, p, before, 0);
+        P.ws.desc[2 * (r.x + k)] = make_int4(bj, cb, min(cm, cb + split), pieces);
+        P.ws.desc[2 * (r.x + k) + 1] = make_int4(lo_j, p_j, first + k, 0);
+      }
+      for (int k = lane; k < r.w; k += 32) {
+        const int cb = cm + k * small;
+        P.ws.desc[2 * (NB + r.y + k)] = make_int4(bj, cb, min(c1, cb + small), pieces);
+        P.ws.desc[2 * (NB + r.y + k) + 1] = make_int4(lo_j, p_j, first + r.z + k, 0);
       }
     }
-    const int chunk_total = warp_incl[nwarps - 1];
-    __syncthreads();
-    if (tid == 0) carry_s = carry + chunk_total;
-    __syncthreads();
+    __syncthreads();  // rec and rng are rewritten by the next round
+    carry += tot;
   }
   if (tid == 0) {
-    P.ws.split_off[P.B] = carry_s;
+    const int total = (int)(carry >> 32) + (int)(carry & 0xffffffffll);
+    P.ws.split_off[P.B] = total;
     P.ws.ctrl[0] = split;
-    P.ws.ctrl[1] = carry_s;
-    P.ws.ctrl[2] = 0;
+    P.ws.ctrl[1] = total;
+    P.ws.ctrl[2] = first_dynamic;
   }
 }
 
@@ -216,8 +329,8 @@ struct ItemInfo {
   int s_global, nsplits;            // split index in the partial arrays; splits of b
 };
 
-// Split descriptor written by the plan kernel: {b, c_begin, c_end, nsplits},
-// {lo, p, first split of b, 0}.
+// Piece descriptor written by the plan kernel, in item order: {b, c_begin,
+// c_end, pieces of b}, {lo, p, partial index, 0}.
 __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, ItemInfo& it) {
   const int s = item / P.h_kv;
   const int4 d0 = __ldcg(P.ws.desc + 2 * s), d1 = __ldcg(P.ws.desc + 2 * s + 1);
@@ -228,7 +341,7 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
   it.nsplits = d0.w;
   it.lo = d1.x;
   it.p = d1.y;
-  it.s_global = s;
+  it.s_global = d1.z;
 }
 
 // ------------------------------------------------------ bf16 decode kernel --
@@ -240,9 +353,10 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 // (a 3-D tensor map of the pool (d, H_kv, slot), boxes of 8 or 16 rows = one
 // page run, 4 boxes per 8 KiB chunk at page size 16) completing on the stage's
 // mbarrier by transaction bytes, kRingW-1 chunks ahead of the chunk the warp
-// computes.  The stream runs across item boundaries: the next items'
-// descriptors and block-table windows are loaded two items ahead, and each
-// item's Q rows arrive by a bulk copy into one of kRingW Q slots.  Stage
+// computes.  The stream runs across item boundaries: the next item's
+// descriptor and block-table window are fetched during the current item's
+// last kGrabLead chunks, and each item's Q rows arrive by a bulk copy into
+// one of kRingW Q slots.  Stage
 // layout: K then V as [row half (64 elements = 128 B)][16 rows][128 B] in the
 // TMA 128-byte swizzle (16-byte unit u of row r at unit u ^ (r & 7), so
 // ldmatrix reads of 8 rows hit 8 different bank groups).  A box of a block
@@ -264,6 +378,7 @@ constexpr int kRingW = TL_DECODE_RING;      // stages per warp (16-bit pools)
 constexpr int kRingW8 = kRingW + 1;
 constexpr int kMaxRing = kRingW8;
 constexpr int kMaxWarpsW = TL_DECODE_WARPS;
+constexpr int kGrabLead = 4;  // chunks left to issue when a warp starts fetching its next item
 
 // Per-warp shared memory: kRingW stages of one chunk of K and V as the TMA
 // lands them (16-bit or e4m3 elements, rows split in 128-byte parts), kRingW
@@ -412,7 +527,13 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   }
   __syncthreads();
 
+  // launched as a programmatic dependent of the plan kernel: its results
+  // (work counter, descriptors, offsets) are read only after this wait
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // the combine kernel may launch now (it too waits for this grid's results)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int qslot = L::qslot_bytes(P.rows);
+  const uint64_t kv_policy = l2_evict_first();
   const uint32_t ring = sbase0 + w * L::warp_bytes(P.rows);
   const uint32_t qbase = ring + R * L::kStageBytes;
   const uint32_t wide = qbase + R * qslot;  // e4m3 pools: the widened chunk
@@ -428,39 +549,48 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const CUtensorMap* rq_map = rq_kind == 0 ? &kmap : &vmap;
 
   // ---------------------------------------------------------- issue side
-  // items: icur (being issued), inext (descriptor and window loaded),
-  // inext2 (descriptor loading), grab (lane 0: the atomic for the one after)
-  ItemInfo icur, inext, inext2;
+  // items: icur (being issued) and inext, fetched in three steps, one per
+  // issued chunk, once icur has kGrabLead chunks left to issue: the atomic,
+  // the descriptor, the block-table window.  Taking the next item this late
+  // (instead of items ahead) keeps the warps' finishing times close.
+  ItemInfo icur, inext;
   bool icur_live = false;
   int icur_last_blk = 0;
   int icur_c = 0, iwin_blk0 = 0, iwin = -1, nwin_blk0 = 0, nwin = -1;
-  int id_next = total_items, id_next2 = total_items;
-  int grab = 0;
+  // the first item is the warp's index in the grid (the counter starts past
+  // them); later ones come from the counter
+  int grab = blockIdx.x * (blockDim.x >> 5) + w;
+  int nstate = 1;  // 0 idle, 1 item id known, 2 descriptor loading, 3 ready, 4 no items left
   uint32_t gs_issue = 0;
   int items_issued = 0;
-  {
-    int g0 = 0;
-    if (lane == 0) g0 = atomicAdd(P.ws.ctrl + 2, 1);
-    id_next = __shfl_sync(0xffffffffu, g0, 0);
-    if (lane == 0) g0 = atomicAdd(P.ws.ctrl + 2, 1);
-    id_next2 = __shfl_sync(0xffffffffu, g0, 0);
-    if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
-    if (id_next < total_items) {
-      describe_item(P, id_next, inext);
+  auto fetch_step = [&]() {
+    if (nstate == 0) {
+      if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
+      nstate = 1;
+    } else if (nstate == 1) {
+      const int id = __shfl_sync(0xffffffffu, grab, 0);
+      if (id >= total_items) {
+        nstate = 4;
+      } else {
+        describe_item(P, id, inext);
+        nstate = 2;
+      }
+    } else if (nstate == 2) {
       nwin_blk0 = page_of(P, inext.c_begin * kChunk);
       const int blk = nwin_blk0 + lane;
-      nwin = blk <= page_of(P, inext.p)
-                 ? table_entry(P, inext.b, blk)
-                 : -1;
+      nwin = blk <= page_of(P, inext.p) ? table_entry(P, inext.b, blk) : -1;
+      nstate = 3;
     }
-    if (id_next2 < total_items) describe_item(P, id_next2, inext2);
-  }
+  };
+  while (nstate < 3) fetch_step();
 
-  // Start issuing the next item: publish its descriptor, copy its Q rows,
-  // advance the prefetch pipeline.  False when there is no item left.
+  // Start issuing the next item: publish its descriptor, copy its Q rows.
+  // False when there is no item left.
   auto start_item = [&]() -> bool {
-    if (id_next >= total_items) return false;
+    while (nstate < 3) fetch_step();  // a fetch that started late completes here
+    if (nstate == 4) return false;
     icur = inext;
+    nstate = 0;
     icur_last_blk = page_of(P, icur.p);
     iwin_blk0 = nwin_blk0;
     iwin = nwin;
@@ -481,25 +611,13 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
                  qbytes, smem_u32(&sh.qfull[w][q]));
     }
     ++items_issued;
-    // pipeline: next2 -> next (its descriptor has arrived: load its window)
-    id_next = id_next2;
-    inext = inext2;
-    if (id_next < total_items) {
-      nwin_blk0 = page_of(P, inext.c_begin * kChunk);
-      const int blk = nwin_blk0 + lane;
-      nwin = blk <= page_of(P, inext.p)
-                 ? table_entry(P, inext.b, blk)
-                 : -1;
-    }
-    id_next2 = __shfl_sync(0xffffffffu, grab, 0);
-    if (lane == 0) grab = atomicAdd(P.ws.ctrl + 2, 1);
-    if (id_next2 < total_items) describe_item(P, id_next2, inext2);
     return true;
   };
 
   // Issue the next chunk of the stream (starting a new item when needed).
   auto issue_next = [&]() {
     if (!icur_live && !start_item()) return;
+    if (nstate < 3 && icur.c_end - icur_c <= kGrabLead) fetch_step();
     const int stage = (int)(gs_issue % R);
     const int j0 = icur_c * kChunk;
     const int last_blk = icur_last_blk;
@@ -531,10 +649,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       mbar_arrive_expect_tx(bar, L::kStageBytes);
     }
     __syncwarp();
-    if (lane < nreq)
-      tma_load_3d(ring + stage * L::kStageBytes + rq_kind * L::kChunkBytes +
-                      rq_half * L::kHalfBytes + rq_box * box_rows * 128,
-                  rq_map, rq_half * (KV8 ? 128 : 64), icur.g, slot0, bar);
+    if (lane < nreq)  // the pools are read once per call: first out of L2
+      tma_load_3d_hint(ring + stage * L::kStageBytes + rq_kind * L::kChunkBytes +
+                           rq_half * L::kHalfBytes + rq_box * box_rows * 128,
+                       rq_map, rq_half * (KV8 ? 128 : 64), icur.g, slot0, bar, kv_policy);
     ++gs_issue;
     if (++icur_c == icur.c_end) icur_live = false;
   };
@@ -771,6 +889,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2] * i1, o[n][3] * i1);
       }
     } else {
+      // partials stay in L2 for the combine kernel that follows
+      const uint64_t keep = l2_evict_last();
       if (qr < P.rows) {
         const size_t rowi = (size_t)it.s_global * P.hq_all + h0r;
         float* dst = P.ws.acc + rowi * D + qc;
@@ -778,17 +898,16 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         for (int n = 0; n < D / 8; ++n) {
           const float a = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
           const float bb = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
-          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(a, bb);
+          st_f32x2_hint(dst + n * 8, a, bb, keep);
         }
-        if ((lane & 3) == 0) *reinterpret_cast<float2*>(P.ws.ml + rowi * 2) = make_float2(m0, l0);
+        if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m0, l0, keep);
       }
       if (TWO_ROWS && qr + 8 < P.rows) {
         const size_t rowi = (size_t)it.s_global * P.hq_all + h1r;
         float* dst = P.ws.acc + rowi * D + qc;
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n)
-          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2], o[n][3]);
-        if ((lane & 3) == 0) *reinterpret_cast<float2*>(P.ws.ml + rowi * 2) = make_float2(m1, l1);
+        for (int n = 0; n < D / 8; ++n) st_f32x2_hint(dst + n * 8, o[n][2], o[n][3], keep);
+        if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m1, l1, keep);
       }
     }
     ++items_c;
@@ -916,71 +1035,70 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_f32_kernel(DecodeParams
 
 // --------------------------------------------------------------- combine --
 //
-// One warp per (sequence, query head) merges the sequence's split partials in
-// split order: the lanes read the splits' (max, sum) pairs (32 at a time) and
-// reduce the maximum; each split's weight exp2(m_i - M) is broadcast from its
-// lane while the lanes sum the weighted P.V rows (8 splits in flight).
-// Sequences with one split were written by the main kernel when
-// skip_single is set; sequences with none output 0.
-
+// Merges each sequence's piece partials.  Sequences with one piece were
+// written by the main kernel when skip_single is set; sequences with none
+// output 0.
+//
+// One thread per 4 outputs of a (sequence, output row): a warp covers one
+// row at d = 128 (two at d = 64).  The pieces are folded in partial-index
+// order, 8 at a time: their (m, l) and partial rows are loaded together (one
+// round of loads per 8 pieces), then
+//   M' = max(M, m_s),  a = a 2^(M - M') + sum_s 2^(m_s - M') acc_s,
+//   l = l 2^(M - M') + sum_s 2^(m_s - M') l_s,   out = a / l.
+// The partials come from the previous kernel: reads go to L2 (ld.global.cg).
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams P, int skip_single) {
-  constexpr int E = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t wi = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (wi >= (int64_t)P.B * P.hq_all) return;
-  const int b = (int)(wi / P.hq_all), h = (int)(wi - (int64_t)b * P.hq_all);
-  const int s0 = __ldg(P.ws.split_off + b), ns = __ldg(P.ws.split_off + b + 1) - s0;
+  constexpr int kTpr = D / 4;   // threads per output row
+  constexpr int kBatch = 8;     // pieces per round of loads
+  // a no-op unless launched as a programmatic dependent of the attention kernel
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = gid / kTpr;  // b * hq_all + h
+  if (row >= (int64_t)P.B * P.hq_all) return;
+  const int col = (int)(gid % kTpr) * 4;
+  const int b = (int)(row / P.hq_all), h = (int)(row - (int64_t)b * P.hq_all);
+  const int s0 = __ldcg(P.ws.split_off + b), ns = __ldcg(P.ws.split_off + b + 1) - s0;
+  float4* out = reinterpret_cast<float4*>(P.out + row * D + col);
   if (ns == 0) {  // nothing to read: the output is 0
-    float* out = P.out + (size_t)wi * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = 0.f;
+    *out = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   if (ns == 1 && skip_single) return;
-  const float* ml = P.ws.ml + ((size_t)s0 * P.hq_all + h) * 2;
-  const float* acc = P.ws.acc + ((size_t)s0 * P.hq_all + h) * D + lane * E;
-  const size_t ml_stride = (size_t)P.hq_all * 2, acc_stride = (size_t)P.hq_all * D;
-  float M = -INFINITY;
-  for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, __ldg(ml + sp * ml_stride));
-  M = warp_max(M);
-  float a[E], lsum = 0.f;
+  const float2* ml = reinterpret_cast<const float2*>(P.ws.ml) + (size_t)s0 * P.hq_all + h;
+  const float4* acc = reinterpret_cast<const float4*>(P.ws.acc + ((size_t)s0 * P.hq_all + h) * D + col);
+  const size_t acc_stride = (size_t)P.hq_all * D / 4;  // float4 units
+  float M = -INFINITY, l = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < ns; s += kBatch) {
+    float2 mlv[kBatch];
+    float4 av[kBatch];
 #pragma unroll
-  for (int e = 0; e < E; ++e) a[e] = 0.f;
-  for (int base = 0; base < ns; base += 32) {
-    const int sp = base + lane;
-    float f = 0.f;
-    if (sp < ns) {
-      const float mi = __ldg(ml + sp * ml_stride);
-      f = mi == -INFINITY ? 0.f : fast_exp2(mi - M);
-      lsum += f * __ldg(ml + sp * ml_stride + 1);
-    }
-    const int cnt = min(32, ns - base);
-    int j = 0;
-    for (; j + 8 <= cnt; j += 8) {
-      float v[8][E], fj[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        fj[u] = __shfl_sync(0xffffffffu, f, j + u);
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[u][e] = __ldg(acc + (size_t)(base + j + u) * acc_stride + e);
+    for (int u = 0; u < kBatch; ++u) {
+      if (s + u < ns) {
+        mlv[u] = __ldcg(ml + (size_t)(s + u) * P.hq_all);
+        av[u] = __ldcg(acc + (size_t)(s + u) * acc_stride);
+      } else {
+        mlv[u] = make_float2(-INFINITY, 0.f);
+        av[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int e = 0; e < E; ++e) a[e] += fj[u] * v[u][e];
     }
-    for (; j < cnt; ++j) {
-      const float fj = __shfl_sync(0xffffffffu, f, j);
+    float Mn = M;
 #pragma unroll
-      for (int e = 0; e < E; ++e) a[e] += fj * __ldg(acc + (size_t)(base + j) * acc_stride + e);
+    for (int u = 0; u < kBatch; ++u) Mn = fmaxf(Mn, mlv[u].x);
+    if (Mn == -INFINITY) continue;  // no key seen yet by any piece
+    const float c = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+    l *= c;
+    a.x *= c; a.y *= c; a.z *= c; a.w *= c;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float f = mlv[u].x == -INFINITY ? 0.f : fast_exp2(mlv[u].x - Mn);
+      l += f * mlv[u].y;
+      a.x += f * av[u].x; a.y += f * av[u].y; a.z += f * av[u].z; a.w += f * av[u].w;
     }
+    M = Mn;
   }
-  lsum = warp_sum(lsum);
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  float* out = P.out + (size_t)wi * D + lane * E;
-#pragma unroll
-  for (int e = 0; e < E; ++e) out[e] = a[e] * inv;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  *out = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
 }
 
 }  // namespace tl
@@ -1055,14 +1173,22 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   P.error_word = error_word;
   cudaStream_t st = (cudaStream_t)stream;
 
+  // warps per CTA of the bf16 / e4m3 kernel (as many as the stages fit)
+  const bool kv8 = dtype == TL_FP8_E4M3;
+  int warps = 0;
+  if (dtype != TL_F32) {
+    const int per_warp = kv8 ? WarpSmem<128, true>::warp_bytes(rows)
+                             : (d == 128 ? WarpSmem<128, false>::warp_bytes(rows)
+                                         : WarpSmem<64, false>::warp_bytes(rows));
+    warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);
+  }
   const int target_splits = (kTargetItems + h_kv - 1) / h_kv;
-  decode_plan_kernel<<<1, 1024, 0, st>>>(P, target_splits);
+  decode_plan_kernel<<<1, 1024, 0, st>>>(P, target_splits, num_sms() * warps);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
 
   if (dtype == TL_BF16 || dtype == TL_FP8_E4M3) {
     // 3-D tensor maps of the pools: (d, H_kv, slot), boxes of one 128-byte
     // row part x 1 x box_rows (64 bf16 or 128 e4m3 elements)
-    const bool kv8 = dtype == TL_FP8_E4M3;
     const int esz = kv8 ? 1 : 2;
     const int box_rows = page_size % 16 == 0 ? 16 : 8;
     CUtensorMap kmap, vmap;
@@ -1077,13 +1203,22 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
 #define TL_LAUNCH_W(DD, TWO, K8)                                                          \
   do {                                                                                    \
     auto kern = decode_bf16_kernel<DD, TWO, K8>;                                          \
-    const int per_warp = WarpSmem<DD, K8>::warp_bytes(rows);                              \
-    const int warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);               \
-    const int sm = warps * per_warp + 1024;                                               \
+    const int sm = warps * WarpSmem<DD, K8>::warp_bytes(rows) + 1024;                     \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
         cudaSuccess)                                                                      \
       return TL_ERR_CUDA;                                                                 \
-    kern<<<num_sms(), warps * 32, sm, st>>>(P, kmap, vmap, box_rows);                     \
+    cudaLaunchAttribute attr[1];                                                          \
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                      \
+    attr[0].val.programmaticStreamSerializationAllowed = 1;                               \
+    cudaLaunchConfig_t cfg = {};                                                          \
+    cfg.gridDim = dim3(num_sms());                                                        \
+    cfg.blockDim = dim3(warps * 32);                                                      \
+    cfg.dynamicSmemBytes = sm;                                                            \
+    cfg.stream = st;                                                                      \
+    cfg.attrs = attr;                                                                     \
+    cfg.numAttrs = 1;                                                                     \
+    if (cudaLaunchKernelEx(&cfg, kern, P, kmap, vmap, box_rows) != cudaSuccess)           \
+      return TL_ERR_CUDA;                                                                 \
   } while (0)
     if (kv8) {
       if (rows > 8) TL_LAUNCH_W(128, true, true); else TL_LAUNCH_W(128, false, true);
@@ -1094,16 +1229,28 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
     }
 #undef TL_LAUNCH_W
     if (launch_status() != TL_OK) return TL_ERR_CUDA;
-    const unsigned cblocks = (unsigned)(((int64_t)B * P.hq_all + 7) / 8);
-    if (d == 128) decode_combine_kernel<128><<<cblocks, 256, 0, st>>>(P, 1);
-    else decode_combine_kernel<64><<<cblocks, 256, 0, st>>>(P, 1);
+    // the merge, a programmatic dependent of the attention kernel: its CTAs
+    // take the SMs as the attention CTAs leave
+    const unsigned cblocks = (unsigned)(((int64_t)B * P.hq_all * (d / 4) + 255) / 256);
+    cudaLaunchAttribute cattr[1];
+    cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    cattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(cblocks);
+    ccfg.blockDim = dim3(256);
+    ccfg.stream = st;
+    ccfg.attrs = cattr;
+    ccfg.numAttrs = 1;
+    const cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&ccfg, decode_combine_kernel<128>, P, 1)
+                                    : cudaLaunchKernelEx(&ccfg, decode_combine_kernel<64>, P, 1);
+    if (ce != cudaSuccess) return TL_ERR_CUDA;
     return launch_status();
   }
   const int grid = num_sms() * 2;
   if (d == 128) decode_f32_kernel<128><<<grid, kDecodeThreads, 0, st>>>(P);
   else decode_f32_kernel<64><<<grid, kDecodeThreads, 0, st>>>(P);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
-  const unsigned cblocks = (unsigned)(((int64_t)B * h_q + 7) / 8);
+  const unsigned cblocks = (unsigned)(((int64_t)B * h_q * (d / 4) + 255) / 256);
   if (d == 128) decode_combine_kernel<128><<<cblocks, 256, 0, st>>>(P, 0);
   else decode_combine_kernel<64><<<cblocks, 256, 0, st>>>(P, 0);
   return launch_status();
