@@ -77,7 +77,9 @@ typedef enum {
 #define TL_DEVERR_PAGE_RANGE 2u    /* a needed block-table entry outside [0, num_pages) */
 #define TL_DEVERR_CONTEXT_RANGE 4u /* a length / position past max_pages_per_seq*page_size */
 #define TL_DEVERR_TIMEOUT 8u       /* an internal pipeline wait gave up (outputs invalid) */
-#define TL_DEVERR_VALUE_RANGE 16u  /* prefill: a finite V entry beyond +-65504 (outputs invalid) */
+#define TL_DEVERR_VALUE_RANGE 16u  /* a finite value beyond fp16's +-65504 where the path rounds to
+                                      fp16: V in prefill, q in decode over e4m3 pools (outputs
+                                      invalid) */
 
 /* Name of a status, for messages (never NULL). */
 const char* tl_status_string(tl_status status);
@@ -151,7 +153,8 @@ size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, int32_t h_kv,
  *                share a workspace.
  * Supported: dtype TL_BF16 or TL_F32, or TL_FP8_E4M3 for e4m3 pools (q bf16,
  * d = 128; the codes widen exactly to fp16 for the tensor core, and q is
- * rounded to fp16: finite |q| beyond 65504 is out of range), d in {64, 128},
+ * rounded to fp16: a finite |q| beyond 65504 sets TL_DEVERR_VALUE_RANGE),
+ * d in {64, 128},
  * h_q % h_kv == 0 with
  * h_q/h_kv <= 16, page_size in [1, 256] (a multiple of 8 for TL_BF16, whose
  * pages move as TMA boxes of 8 or 16 rows), num_pages*page_size < 2^31.

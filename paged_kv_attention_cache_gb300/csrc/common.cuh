@@ -156,6 +156,11 @@ TL_DEVINLINE uint64_t l2_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
+TL_DEVINLINE void st_f32x4_hint(float* ptr, float a, float b, float c, float d, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;\n" ::"l"(ptr), "f"(a),
+               "f"(b), "f"(c), "f"(d), "l"(policy)
+               : "memory");
+}
 TL_DEVINLINE void st_f32x2_hint(float* ptr, float a, float b, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(ptr), "f"(a), "f"(b),
                "l"(policy)

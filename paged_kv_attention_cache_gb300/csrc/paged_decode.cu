@@ -381,9 +381,8 @@ constexpr int kMaxWarpsW = TL_DECODE_WARPS;
 constexpr int kGrabLead = 4;  // chunks left to issue when a warp starts fetching its next item
 
 // Per-warp shared memory: kRingW stages of one chunk of K and V as the TMA
-// lands them (16-bit or e4m3 elements, rows split in 128-byte parts), kRingW
-// Q slots, and for e4m3 pools one buffer of the chunk widened to fp16 in the
-// 16-bit stage layout.
+// lands them (16-bit or e4m3 elements, rows split in 128-byte parts) and
+// kRingW Q slots.
 template <int D, bool KV8 = false>
 struct WarpSmem {
   static constexpr int kRing = KV8 ? kRingW8 : kRingW;   // stages (and Q slots) per warp
@@ -392,12 +391,11 @@ struct WarpSmem {
   static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one part
   static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
   static constexpr int kStageBytes = 2 * kChunkBytes;       // multiple of 1024
-  static constexpr int kWideBytes = KV8 ? 2 * (D * 2 / 128) * kHalfBytes : 0;
   __host__ __device__ static int qslot_bytes(int rows) {
     return (rows * D * 2 + 1023) / 1024 * 1024;
   }
   __host__ __device__ static int warp_bytes(int rows) {
-    return kRing * (kStageBytes + qslot_bytes(rows)) + kWideBytes;
+    return kRing * (kStageBytes + qslot_bytes(rows));
   }
 };
 
@@ -443,6 +441,14 @@ __device__ __forceinline__ uint32_t bf16x2_as_f16x2(uint32_t x) {
   return r;
 }
 
+// True when a finite bf16 element of the pair x became infinite in the fp16
+// pair h (|x| > 65504).
+__device__ __forceinline__ bool f16_overflowed(uint32_t x, uint32_t h) {
+  const bool lo = ((x >> 7) & 0xffu) != 0xffu && (h & 0x7fffu) == 0x7c00u;
+  const bool hi = ((x >> 23) & 0xffu) != 0xffu && ((h >> 16) & 0x7fffu) == 0x7c00u;
+  return lo || hi;
+}
+
 // Two e4m3 codes (low byte first) as an fp16 pair; exact (every e4m3 value is
 // an fp16 value).
 __device__ __forceinline__ uint32_t e4m3x2_as_f16x2(uint32_t two_codes) {
@@ -452,42 +458,19 @@ __device__ __forceinline__ uint32_t e4m3x2_as_f16x2(uint32_t two_codes) {
   return r;
 }
 
-// Widen one chunk tile (16 rows x 128 codes, 128-byte swizzle, as the TMA
-// lands it) into the 16-bit stage layout (two 128-byte parts per row, same
-// swizzle); rows from first_dead on become zeros.  Lane-strided over the
-// tile's 16-byte units.
-__device__ __forceinline__ void widen_e4m3_tile(uint32_t src, uint32_t dst, int first_dead,
-                                                int lane) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int u = i * 32 + lane;  // physical unit: row u / 8, slot u % 8
-    const int r = u >> 3, cl = (u & 7) ^ (r & 7);  // logical unit: codes 16cl .. 16cl+15
-    uint32_t x0, x1, x2, x3;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                 : "r"(src + u * 16));
-    uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (r < first_dead) {
-      h[0] = e4m3x2_as_f16x2(x0);
-      h[1] = e4m3x2_as_f16x2(x0 >> 16);
-      h[2] = e4m3x2_as_f16x2(x1);
-      h[3] = e4m3x2_as_f16x2(x1 >> 16);
-      h[4] = e4m3x2_as_f16x2(x2);
-      h[5] = e4m3x2_as_f16x2(x2 >> 16);
-      h[6] = e4m3x2_as_f16x2(x3);
-      h[7] = e4m3x2_as_f16x2(x3 >> 16);
-    }
-    // fp16 units 2cl, 2cl+1: part cl / 4, units 2(cl % 4), 2(cl % 4) + 1 of the row
-    const uint32_t base = dst + (cl >> 2) * (kChunk * 128) + r * 128;
-    const int uh = 2 * (cl & 3);
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(base + ((uh ^ (r & 7)) << 4)),
-                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                 : "memory");
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                     base + (((uh + 1) ^ (r & 7)) << 4)),
-                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                 : "memory");
-  }
+// Transpose of an 8 x 8 matrix of 16-bit elements held one row pair per
+// lane (lane l: row l / 4, columns 2(l % 4), +1): lane l gets row l / 4 of
+// the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(r) : "r"(addr));
+  return r;
 }
 
 struct ItemSlot {
@@ -536,7 +519,6 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const uint64_t kv_policy = l2_evict_first();
   const uint32_t ring = sbase0 + w * L::warp_bytes(P.rows);
   const uint32_t qbase = ring + R * L::kStageBytes;
-  const uint32_t wide = qbase + R * qslot;  // e4m3 pools: the widened chunk
   const unsigned char* qbase_ptr = smem0 + (qbase - sbase0);
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
@@ -547,6 +529,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const int rq_rem = lane % (L::kHalves * nbox);
   const int rq_half = rq_rem / nbox, rq_box = rq_rem % nbox;
   const CUtensorMap* rq_map = rq_kind == 0 ? &kmap : &vmap;
+  const bool one_page = P.page_size % kChunk == 0;
 
   // ---------------------------------------------------------- issue side
   // items: icur (being issued) and inext, fetched in three steps, one per
@@ -630,25 +613,43 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
                  ? table_entry(P, icur.b, blk)
                  : -1;
     }
-    const int jr = j0 + (lane & 15);
-    const int pr = __shfl_sync(0xffffffffu, iwin, (page_of(P, jr) - iwin_blk0) & 31);
-    bool live = jr >= icur.lo && jr <= icur.p;
-    if (live && (pr < 0 || pr >= P.num_pages)) {
-      if (lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
-      live = false;
+    uint32_t mask;  // live keys of the chunk
+    int slot0;      // first pool slot of this lane's box (n_slots: read as zeros)
+    if (one_page) {
+      // pages of a multiple of 16 keys: the chunk is one run of page bmin,
+      // its live keys the range [lo, p] clipped to the chunk
+      const int pr = __shfl_sync(0xffffffffu, iwin, (bmin - iwin_blk0) & 31);
+      const int first = min(max(icur.lo - j0, 0), kChunk), last = min(icur.p - j0, kChunk - 1);
+      mask = first <= last ? (0xffffffffu >> (31 - last)) & (0xffffffffu << first) : 0u;
+      const bool page_ok = pr >= 0 && pr < P.num_pages;
+      if (mask != 0u && !page_ok) {
+        if (lane == 0) report(P.error_word, TL_DEVERR_PAGE_RANGE);
+        mask = 0u;
+      }
+      slot0 = page_ok ? pr * P.page_size + in_page(P, j0) : n_slots;
+    } else {
+      const int jr = j0 + (lane & 15);
+      const int pr = __shfl_sync(0xffffffffu, iwin, (page_of(P, jr) - iwin_blk0) & 31);
+      bool live = jr >= icur.lo && jr <= icur.p;
+      if (live && (pr < 0 || pr >= P.num_pages)) {
+        if (lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
+        live = false;
+      }
+      mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
+      const int jb = j0 + rq_box * box_rows;
+      const int blk = page_of(P, jb);
+      const int pb = __shfl_sync(0xffffffffu, iwin, (blk - iwin_blk0) & 31);
+      const bool box_ok = blk <= last_blk && pb >= 0 && pb < P.num_pages;
+      slot0 = box_ok ? pb * P.page_size + in_page(P, jb) : n_slots;
     }
-    const uint32_t mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
-    const int jb = j0 + rq_box * box_rows;
-    const int blk = page_of(P, jb);
-    const int pb = __shfl_sync(0xffffffffu, iwin, (blk - iwin_blk0) & 31);
-    const bool box_ok = blk <= last_blk && pb >= 0 && pb < P.num_pages;
-    const int slot0 = box_ok ? pb * P.page_size + in_page(P, jb) : n_slots;
     const uint32_t bar = smem_u32(&sh.full[w][stage]);
     if (lane == 0) {
       sh.stage_mask[w][stage] = mask;
       mbar_arrive_expect_tx(bar, L::kStageBytes);
     }
-    __syncwarp();
+    // no warp barrier here: a box may land before lane 0's expectation (the
+    // transaction count then runs negative), and the phase cannot complete
+    // before lane 0 has arrived
     if (lane < nreq)  // the pools are read once per call: first out of L2
       tma_load_3d_hint(ring + stage * L::kStageBytes + rq_kind * L::kChunkBytes +
                            rq_half * L::kHalfBytes + rq_box * box_rows * 128,
@@ -670,18 +671,25 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     const ItemSlot it = sh.slot[w][q];
     const unsigned char* qs = qbase_ptr + q * qslot;
     uint32_t qa[D / 16][4];
+    bool q_over = false;  // a finite query element beyond fp16's range (e4m3 pools)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      const int e0 = ks * 16 + qc;
+      // K step ks covers d = 16ks .. 16ks+15.  16-bit pools: the A fragment's
+      // columns (2t, 2t+1) and (2t+8, 2t+9) are those d.  e4m3 pools: they are
+      // d = 16ks+4t+(0,1) and 16ks+4t+(2,3), the order in which a lane's one
+      // 4-byte read of a K row lands (the same permutation of the summed d
+      // on both operands leaves Q.K^T unchanged)
+      const int e0 = ks * 16 + (KV8 ? 4 * (lane & 3) : qc);
+      const int e2 = KV8 ? e0 + 2 : e0 + 8;
       qa[ks][0] = qr < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0) * 2) : 0u;
       qa[ks][2] =
-          qr < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0 + 8) * 2) : 0u;
+          qr < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e2) * 2) : 0u;
       if (TWO_ROWS) {
         qa[ks][1] = qr + 8 < P.rows
                         ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0) * 2)
                         : 0u;
         qa[ks][3] = qr + 8 < P.rows
-                        ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0 + 8) * 2)
+                        ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e2) * 2)
                         : 0u;
       } else {
         qa[ks][1] = 0u;
@@ -689,9 +697,15 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       }
       if (KV8) {  // the tensor core takes fp16 for both operands here
 #pragma unroll
-        for (int k = 0; k < 4; ++k) qa[ks][k] = bf16x2_as_f16x2(qa[ks][k]);
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t h = bf16x2_as_f16x2(qa[ks][k]);
+          q_over |= f16_overflowed(qa[ks][k], h);
+          qa[ks][k] = h;
+        }
       }
     }
+    if (KV8 && __any_sync(0xffffffffu, q_over) && lane == 0)
+      report(P.error_word, TL_DEVERR_VALUE_RANGE);
     __syncwarp();
 
     float o[D / 8][4];
@@ -712,8 +726,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         break;
       }
       const uint32_t mask = sh.stage_mask[w][stage];
-      uint32_t kaddr = ring + stage * L::kStageBytes;
-      uint32_t vaddr = kaddr + L::kChunkBytes;
+      const uint32_t kaddr = ring + stage * L::kStageBytes;
+      const uint32_t vaddr = kaddr + L::kChunkBytes;
       {
         // V rows past the sequence's end (its last chunk only) may hold anything
         const int first_dead = it.p + 1 - c * kChunk;
@@ -730,31 +744,41 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           __syncwarp();
         }
       }
-      if (KV8) {
-        // widen K and V to fp16 in the 16-bit stage layout; the loads below
-        // then read the wide buffer (the dead V rows above are zeros already)
-        widen_e4m3_tile(kaddr, wide, kChunk, lane);
-        widen_e4m3_tile(vaddr, wide + 2 * kChunk * 128, kChunk, lane);
-        __syncwarp();
-        kaddr = wide;
-        vaddr = wide + 2 * kChunk * 128;
-      }
       // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys); even and
       // odd K steps accumulate separately (two independent MMA chains)
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       {
         float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int mi = lane >> 3, ri = lane & 7;
-        const int tok = (mi >> 1) * 8 + ri;
+        if constexpr (KV8) {
+          // the B fragment of key row n0 + g straight from the e4m3 codes: one
+          // 4-byte read (codes 16ks+4t .. +3, the stage's 128-byte swizzle)
+          // widened exactly to two fp16 pairs
+          const int g = lane >> 2, t4 = 4 * (lane & 3);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int u = 2 * ks + (mi & 1);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4),
-                      b0, b1, b2, b3);
-          float(*acc)[4] = (ks & 1) ? s2 : s;
-          mma_16816<KV8>(acc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_16816<KV8>(acc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            float(*acc)[4] = (ks & 1) ? s2 : s;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const int row = nt * 8 + g;
+              const uint32_t w4 = lds_u32(kaddr + row * 128 + ((ks ^ (row & 7)) << 4) + t4);
+              mma_16816<true>(acc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3],
+                              e4m3x2_as_f16x2(w4), e4m3x2_as_f16x2(w4 >> 16));
+            }
+          }
+        } else {
+          const int mi = lane >> 3, ri = lane & 7;
+          const int tok = (mi >> 1) * 8 + ri;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int u = 2 * ks + (mi & 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(
+                kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                b1, b2, b3);
+            float(*acc)[4] = (ks & 1) ? s2 : s;
+            mma_16816<KV8>(acc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            mma_16816<KV8>(acc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          }
         }
 #pragma unroll
         for (int n = 0; n < 2; ++n)
@@ -825,7 +849,38 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       uint32_t h0, l0w, h2, l2w;
       split16<KV8>(p[0][0], p[0][1], h0, l0w);
       split16<KV8>(p[1][0], p[1][1], h2, l2w);
-      {
+      if constexpr (KV8) {
+        // V's B fragments from the e4m3 codes: lane (g, t) reads codes
+        // 16j+4t .. +3 of key rows g and 8+g, widens them to fp16 pairs (a
+        // row pair of two 8 x 8 blocks each: columns = d 16j+4t'+(0,1) and
+        // 16j+4t'+(2,3)) and transposes the blocks in registers, giving keys
+        // (2t, 2t+1) and (2t+8, 2t+9) at one d per lane.  The n-tiles 2j and
+        // 2j+1 then hold output columns 16j+4t+(0,1) and 16j+4t+(2,3).
+        const int g = lane >> 2, t4 = 4 * (lane & 3);
+        uint32_t h1 = 0u, l1w = 0u, h3 = 0u, l3w = 0u;
+        if (TWO_ROWS) {
+          split16<true>(p[0][2], p[0][3], h1, l1w);
+          split16<true>(p[1][2], p[1][3], h3, l3w);
+        }
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          const uint32_t w0 = lds_u32(vaddr + g * 128 + ((j ^ (g & 7)) << 4) + t4);
+          const uint32_t w1 = lds_u32(vaddr + (8 + g) * 128 + ((j ^ (g & 7)) << 4) + t4);
+          const uint32_t a0 = movmatrix_trans(e4m3x2_as_f16x2(w0));
+          const uint32_t a1 = movmatrix_trans(e4m3x2_as_f16x2(w1));
+          const uint32_t b0 = movmatrix_trans(e4m3x2_as_f16x2(w0 >> 16));
+          const uint32_t b1 = movmatrix_trans(e4m3x2_as_f16x2(w1 >> 16));
+          if (!TWO_ROWS) {
+            mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
+            mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
+          } else {
+            mma_16816<true>(o[2 * j], h0, h1, h2, h3, a0, a1);
+            mma_16816<true>(o[2 * j], l0w, l1w, l2w, l3w, a0, a1);
+            mma_16816<true>(o[2 * j + 1], h0, h1, h2, h3, b0, b1);
+            mma_16816<true>(o[2 * j + 1], l0w, l1w, l2w, l3w, b0, b1);
+          }
+        }
+      } else {
         const int mi = lane >> 3, ri = lane & 7;
         const int tok = (mi & 1) * 8 + ri;
         if (!TWO_ROWS) {
@@ -871,42 +926,55 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     // output index of rows qr and qr + 8 among the sequence's q_len * h_q
     const int h0r = (qr / P.group) * P.h_q + it.g * P.group + qr % P.group;
     const int h1r = ((qr + 8) / P.group) * P.h_q + it.g * P.group + (qr + 8) % P.group;
-    if (single) {
-      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-      if (qr < P.rows) {
-        float* dst = P.out + ((size_t)it.b * P.hq_all + h0r) * D + qc;
+    // One output row of this lane, times f: 16-bit pools hold float pairs at
+    // columns 8n + 2t (n-tile n), e4m3 pools float quads at 16j + 4t (n-tiles
+    // 2j and 2j+1).  Row qr adds the low part of P carried in rows 8-15
+    // unless TWO_ROWS; with TWO_ROWS, rows 8-15 are row qr + 8.
+    auto write_row = [&](float* dst, bool second, float f, bool keep_in_l2, uint64_t pol) {
+      if constexpr (KV8) {
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          const float* x = o[2 * j];
+          const float* y = o[2 * j + 1];
+          const float v0 = second ? x[2] : (TWO_ROWS ? x[0] : x[0] + x[2]);
+          const float v1 = second ? x[3] : (TWO_ROWS ? x[1] : x[1] + x[3]);
+          const float v2 = second ? y[2] : (TWO_ROWS ? y[0] : y[0] + y[2]);
+          const float v3 = second ? y[3] : (TWO_ROWS ? y[1] : y[1] + y[3]);
+          float* d4 = dst + 16 * j + 4 * (lane & 3);
+          if (keep_in_l2)
+            st_f32x4_hint(d4, v0 * f, v1 * f, v2 * f, v3 * f, pol);
+          else
+            *reinterpret_cast<float4*>(d4) = make_float4(v0 * f, v1 * f, v2 * f, v3 * f);
+        }
+      } else {
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
-          const float a = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
-          const float bb = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
-          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(a * i0, bb * i0);
+          const float v0 = second ? o[n][2] : (TWO_ROWS ? o[n][0] : o[n][0] + o[n][2]);
+          const float v1 = second ? o[n][3] : (TWO_ROWS ? o[n][1] : o[n][1] + o[n][3]);
+          float* d2 = dst + n * 8 + qc;
+          if (keep_in_l2)
+            st_f32x2_hint(d2, v0 * f, v1 * f, pol);
+          else
+            *reinterpret_cast<float2*>(d2) = make_float2(v0 * f, v1 * f);
         }
       }
-      if (TWO_ROWS && qr + 8 < P.rows) {
-        float* dst = P.out + ((size_t)it.b * P.hq_all + h1r) * D + qc;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n)
-          *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2] * i1, o[n][3] * i1);
-      }
+    };
+    if (single) {
+      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      if (qr < P.rows) write_row(P.out + ((size_t)it.b * P.hq_all + h0r) * D, false, i0, false, 0);
+      if (TWO_ROWS && qr + 8 < P.rows)
+        write_row(P.out + ((size_t)it.b * P.hq_all + h1r) * D, true, i1, false, 0);
     } else {
       // partials stay in L2 for the combine kernel that follows
       const uint64_t keep = l2_evict_last();
       if (qr < P.rows) {
         const size_t rowi = (size_t)it.s_global * P.hq_all + h0r;
-        float* dst = P.ws.acc + rowi * D + qc;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          const float a = TWO_ROWS ? o[n][0] : o[n][0] + o[n][2];
-          const float bb = TWO_ROWS ? o[n][1] : o[n][1] + o[n][3];
-          st_f32x2_hint(dst + n * 8, a, bb, keep);
-        }
+        write_row(P.ws.acc + rowi * D, false, 1.f, true, keep);
         if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m0, l0, keep);
       }
       if (TWO_ROWS && qr + 8 < P.rows) {
         const size_t rowi = (size_t)it.s_global * P.hq_all + h1r;
-        float* dst = P.ws.acc + rowi * D + qc;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) st_f32x2_hint(dst + n * 8, o[n][2], o[n][3], keep);
+        write_row(P.ws.acc + rowi * D, true, 1.f, true, keep);
         if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m1, l1, keep);
       }
     }

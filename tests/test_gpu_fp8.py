@@ -105,6 +105,23 @@ def test_fp8_decode_edge_lengths(window):
     assert_close(out, ref, f"fp8 decode window {window}")
 
 
+def test_fp8_decode_reports_a_query_beyond_fp16():
+    """The query is rounded to fp16 for the e4m3 MMAs: a finite element beyond
+    65504 is reported (TL_DEVERR_VALUE_RANGE), not silently made infinite;
+    an in-range query on the same pools reports nothing."""
+    case = wl.decode_case([40, 100], Hq=8, Hkv=2, d=128, seed=73)
+    k8, v8 = _fp8_case(case)
+    dev = lambda t: t.to(DEV)
+    for big, want in [(60000.0, 0), (1e5, tl.TL_DEVERR_VALUE_RANGE)]:
+        q = case.q.clone()
+        q[1, 3, 17] = big
+        err = _err()
+        tl.tl_paged_attn_decode(dev(q), dev(k8), dev(v8), dev(case.block_table),
+                                dev(case.context_lens), case.scale, error_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == want
+
+
 def test_fp8_decode_over_rings():
     case = wl.swa_ring_decode(seed=1, B=32)
     ring = case.extra["ring_pages"]
