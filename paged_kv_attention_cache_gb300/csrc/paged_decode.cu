@@ -467,12 +467,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t r;
-  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(r) : "r"(addr));
-  return r;
-}
-
 struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits;
 };
@@ -750,20 +744,24 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       {
         float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if constexpr (KV8) {
-          // the B fragment of key row n0 + g straight from the e4m3 codes: one
-          // 4-byte read (codes 16ks+4t .. +3, the stage's 128-byte swizzle)
-          // widened exactly to two fp16 pairs
-          const int g = lane >> 2, t4 = 4 * (lane & 3);
+          // the B fragment of key row n0 + g straight from the e4m3 codes:
+          // lane (g, t) takes codes 16ks+4t .. +3 of the row (an 8 x 8 b16
+          // ldmatrix fragment of the 16-byte unit), widened exactly to two
+          // fp16 pairs; one ldmatrix.x4 covers both key halves of two K steps
+          const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            float(*acc)[4] = (ks & 1) ? s2 : s;
+          for (int ks = 0; ks < D / 16; ks += 2) {
+            const int u = ks + (mi >> 1);
+            uint32_t w[4];
+            ldmatrix_x4(kaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              const int row = nt * 8 + g;
-              const uint32_t w4 = lds_u32(kaddr + row * 128 + ((ks ^ (row & 7)) << 4) + t4);
-              mma_16816<true>(acc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3],
-                              e4m3x2_as_f16x2(w4), e4m3x2_as_f16x2(w4 >> 16));
-            }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                const uint32_t w4 = w[2 * h + nt];
+                mma_16816<true>((h ? s2 : s)[nt], qa[ks + h][0], qa[ks + h][1], qa[ks + h][2],
+                                qa[ks + h][3], e4m3x2_as_f16x2(w4), e4m3x2_as_f16x2(w4 >> 16));
+              }
           }
         } else {
           const int mi = lane >> 3, ri = lane & 7;
@@ -856,28 +854,35 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         // 16j+4t'+(2,3)) and transposes the blocks in registers, giving keys
         // (2t, 2t+1) and (2t+8, 2t+9) at one d per lane.  The n-tiles 2j and
         // 2j+1 then hold output columns 16j+4t+(0,1) and 16j+4t+(2,3).
-        const int g = lane >> 2, t4 = 4 * (lane & 3);
+        const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
         uint32_t h1 = 0u, l1w = 0u, h3 = 0u, l3w = 0u;
         if (TWO_ROWS) {
           split16<true>(p[0][2], p[0][3], h1, l1w);
           split16<true>(p[1][2], p[1][3], h3, l3w);
         }
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-          const uint32_t w0 = lds_u32(vaddr + g * 128 + ((j ^ (g & 7)) << 4) + t4);
-          const uint32_t w1 = lds_u32(vaddr + (8 + g) * 128 + ((j ^ (g & 7)) << 4) + t4);
-          const uint32_t a0 = movmatrix_trans(e4m3x2_as_f16x2(w0));
-          const uint32_t a1 = movmatrix_trans(e4m3x2_as_f16x2(w1));
-          const uint32_t b0 = movmatrix_trans(e4m3x2_as_f16x2(w0 >> 16));
-          const uint32_t b1 = movmatrix_trans(e4m3x2_as_f16x2(w1 >> 16));
-          if (!TWO_ROWS) {
-            mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
-            mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
-          } else {
-            mma_16816<true>(o[2 * j], h0, h1, h2, h3, a0, a1);
-            mma_16816<true>(o[2 * j], l0w, l1w, l2w, l3w, a0, a1);
-            mma_16816<true>(o[2 * j + 1], h0, h1, h2, h3, b0, b1);
-            mma_16816<true>(o[2 * j + 1], l0w, l1w, l2w, l3w, b0, b1);
+        for (int j0 = 0; j0 < D / 16; j0 += 2) {
+          // units j0 and j0 + 1 of key rows 0-7 and 8-15
+          const int u = j0 + (mi >> 1);
+          uint32_t w[4];
+          ldmatrix_x4(vaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = j0 + h;
+            const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1];
+            const uint32_t a0 = movmatrix_trans(e4m3x2_as_f16x2(w0));
+            const uint32_t a1 = movmatrix_trans(e4m3x2_as_f16x2(w1));
+            const uint32_t b0 = movmatrix_trans(e4m3x2_as_f16x2(w0 >> 16));
+            const uint32_t b1 = movmatrix_trans(e4m3x2_as_f16x2(w1 >> 16));
+            if (!TWO_ROWS) {
+              mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
+              mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
+            } else {
+              mma_16816<true>(o[2 * j], h0, h1, h2, h3, a0, a1);
+              mma_16816<true>(o[2 * j], l0w, l1w, l2w, l3w, a0, a1);
+              mma_16816<true>(o[2 * j + 1], h0, h1, h2, h3, b0, b1);
+              mma_16816<true>(o[2 * j + 1], l0w, l1w, l2w, l3w, b0, b1);
+            }
           }
         }
       } else {
