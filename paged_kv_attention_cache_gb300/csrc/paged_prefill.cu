@@ -188,6 +188,29 @@ __device__ __forceinline__ void unpack_f16x2(uint32_t x, float& lo, float& hi) {
       : "=f"(lo), "=f"(hi)
       : "r"(x));
 }
+// (d0, d1) = (a0, a1) * b + c, two f32 FMAs in one packed instruction
+// (b and c hold the same value twice).
+__device__ __forceinline__ void fma_f32x2(float a0, float a1, uint64_t b, uint64_t c, float& d0,
+                                          float& d1) {
+  uint64_t a, d;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+__device__ __forceinline__ uint64_t f32_twice(float x) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};\n" : "=l"(r) : "f"(x));
+  return r;
+}
+// acc + lo + hi of an f16x2 register, each half widened exactly to f32 by
+// the add itself.
+__device__ __forceinline__ float add_f16x2_halves(float acc, uint32_t x) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.f16 %0, l, %0;\n"
+      " add.rn.f32.f16 %0, h, %0;\n}\n"
+      : "+f"(acc)
+      : "r"(x));
+  return acc;
+}
 // Two bf16 (one register) -> two fp16 (one register).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
   return pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
@@ -799,19 +822,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (m_used == -INFINITY) m_used = mt;  // first live key of this row
         const float base = m_used == -INFINITY ? 0.f : m_used;
         // P = fp16(exp2(s*sc - base)), keys 2c and 2c+1 in column c; the sum
-        // takes the same rounded values
+        // takes the same rounded values.  Packed f32x2 FMAs scale two scores
+        // at once; the sum widens each fp16 half inside its add.
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
 #pragma unroll
         for (int q = 0; q < kBN / 32; ++q) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float x0 = fast_exp2(fmaf(s[q * 32 + 2 * i], sc, -base));
-            const float x1 = fast_exp2(fmaf(s[q * 32 + 2 * i + 1], sc, -base));
-            pk[i] = pack_f16x2(x0, x1);
-            float r0, r1;
-            unpack_f16x2(pk[i], r0, r1);
-            ls[i & 3] += r0 + r1;
+            float y0, y1;
+            fma_f32x2(s[q * 32 + 2 * i], s[q * 32 + 2 * i + 1], sc2, nb2, y0, y1);
+            pk[i] = pack_f16x2(fast_exp2(y0), fast_exp2(y1));
+            ls[i & 3] = add_f16x2_halves(ls[i & 3], pk[i]);
           }
           tc::st16(tmem + lane_base + colS + q * 16, pk);
         }
