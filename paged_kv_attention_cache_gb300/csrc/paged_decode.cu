@@ -375,22 +375,23 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 constexpr int kRingW = TL_DECODE_RING;      // stages per warp (16-bit pools)
 // e4m3 pools move half the bytes per chunk: one stage more keeps more bytes
 // in flight per warp (the stream is bound by bytes in flight x latency)
-constexpr int kRingW8 = kRingW + 1;
-constexpr int kMaxRing = kRingW8;
+constexpr int kMaxRing = kRingW;
 constexpr int kMaxWarpsW = TL_DECODE_WARPS;
 constexpr int kGrabLead = 4;  // chunks left to issue when a warp starts fetching its next item
 
-// Per-warp shared memory: kRingW stages of one chunk of K and V as the TMA
-// lands them (16-bit or e4m3 elements, rows split in 128-byte parts) and
-// kRingW Q slots.
+// Per-warp shared memory: kRingW stages of kCps chunks of K and V as the TMA
+// lands them (16-bit or e4m3 elements, rows split in 128-byte parts; an e4m3
+// stage holds two chunks, the same 8 KiB as one 16-bit chunk, so each stage's
+// issue and wait serve 32 keys) and kRingW Q slots.
 template <int D, bool KV8 = false>
 struct WarpSmem {
-  static constexpr int kRing = KV8 ? kRingW8 : kRingW;   // stages (and Q slots) per warp
+  static constexpr int kRing = kRingW;                    // stages (and Q slots) per warp
+  static constexpr int kCps = KV8 ? 2 : 1;                 // chunks per stage
   static constexpr int kRowBytes = D * (KV8 ? 1 : 2);
   static constexpr int kHalves = kRowBytes / 128;          // 128-byte parts of a row
   static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one part
   static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
-  static constexpr int kStageBytes = 2 * kChunkBytes;       // multiple of 1024
+  static constexpr int kStageBytes = 2 * kCps * kChunkBytes;  // K chunks, then V chunks
   __host__ __device__ static int qslot_bytes(int rows) {
     return (rows * D * 2 + 1023) / 1024 * 1024;
   }
@@ -517,11 +518,15 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
   const int n_slots = P.num_pages * P.page_size;
-  const int nbox = kChunk / box_rows;      // boxes per row half
-  const int nreq = 2 * L::kHalves * nbox;  // TMA requests per chunk
-  const int rq_kind = lane / (L::kHalves * nbox);
-  const int rq_rem = lane % (L::kHalves * nbox);
-  const int rq_half = rq_rem / nbox, rq_box = rq_rem % nbox;
+  constexpr int CPS = L::kCps;
+  const int nbox = kChunk / box_rows;             // boxes per row half of a chunk
+  const int per_kind = CPS * L::kHalves * nbox;   // boxes of K (or V) per stage
+  const int nreq = 2 * per_kind;                  // TMA requests per stage
+  const int rq_kind = lane / per_kind;            // lane's box: K or V,
+  const int rq_rem = lane % per_kind;
+  const int rq_sub = rq_rem / (L::kHalves * nbox);  // chunk of the stage,
+  const int rq_rem2 = rq_rem % (L::kHalves * nbox);
+  const int rq_half = rq_rem2 / nbox, rq_box = rq_rem2 % nbox;  // row part and rows
   const CUtensorMap* rq_map = rq_kind == 0 ? &kmap : &vmap;
   const bool one_page = P.page_size % kChunk == 0;
 
@@ -591,15 +596,17 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     return true;
   };
 
-  // Issue the next chunk of the stream (starting a new item when needed).
+  // Issue the next stage of the stream: CPS chunks of the current item
+  // (starting a new item when needed; a stage past the item's last chunk
+  // reads zeros there and the compute side skips it).
   auto issue_next = [&]() {
     if (!icur_live && !start_item()) return;
-    if (nstate < 3 && icur.c_end - icur_c <= kGrabLead) fetch_step();
+    if (nstate < 3 && icur.c_end - icur_c <= kGrabLead * CPS) fetch_step();
     const int stage = (int)(gs_issue % R);
     const int j0 = icur_c * kChunk;
     const int last_blk = icur_last_blk;
     const int bmin = page_of(P, j0);
-    const int bmax = min(page_of(P, j0 + kChunk - 1), last_blk);
+    const int bmax = min(page_of(P, j0 + CPS * kChunk - 1), last_blk);
     if (bmin < iwin_blk0 || bmax >= iwin_blk0 + 32) {  // the next 32 blocks
       iwin_blk0 = bmin;
       const int blk = iwin_blk0 + lane;
@@ -607,34 +614,40 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
                  ? table_entry(P, icur.b, blk)
                  : -1;
     }
-    uint32_t mask;  // live keys of the chunk
-    int slot0;      // first pool slot of this lane's box (n_slots: read as zeros)
+    uint32_t mask = 0u;  // live keys of the stage (16 bits per chunk)
+    int slot0 = n_slots;  // first pool slot of this lane's box (n_slots: read as zeros)
     if (one_page) {
-      // pages of a multiple of 16 keys: the chunk is one run of page bmin,
-      // its live keys the range [lo, p] clipped to the chunk
-      const int pr = __shfl_sync(0xffffffffu, iwin, (bmin - iwin_blk0) & 31);
-      const int first = min(max(icur.lo - j0, 0), kChunk), last = min(icur.p - j0, kChunk - 1);
+      // pages of a multiple of 16 keys: each chunk is one run of one page.
+      // The stage's live keys are the range [lo, p] clipped to it; each
+      // lane looks up the page of its own box's chunk, and chunks on a bad
+      // page (any lane of that chunk sees it) are reported and read as zeros
+      const int jm = j0 + rq_sub * kChunk;
+      const int pr = __shfl_sync(0xffffffffu, iwin, (page_of(P, jm) - iwin_blk0) & 31);
+      const int first = min(max(icur.lo - j0, 0), CPS * kChunk);
+      const int last = min(icur.p - j0, CPS * kChunk - 1);
       mask = first <= last ? (0xffffffffu >> (31 - last)) & (0xffffffffu << first) : 0u;
-      const bool page_ok = pr >= 0 && pr < P.num_pages;
-      if (mask != 0u && !page_ok) {
+      const bool page_ok = jm <= icur.p && pr >= 0 && pr < P.num_pages;
+      const uint32_t sub_bits = 0xffffu << (16 * rq_sub);
+      const uint32_t bad = __reduce_or_sync(0xffffffffu, (!page_ok && (mask & sub_bits)) ? sub_bits : 0u);
+      if (bad != 0u) {
         if (lane == 0) report(P.error_word, TL_DEVERR_PAGE_RANGE);
-        mask = 0u;
+        mask &= ~bad;
       }
-      slot0 = page_ok ? pr * P.page_size + in_page(P, j0) : n_slots;
+      if (page_ok) slot0 = pr * P.page_size + in_page(P, jm);
     } else {
-      const int jr = j0 + (lane & 15);
+      const int jr = j0 + (CPS == 2 ? lane : (lane & 15));
       const int pr = __shfl_sync(0xffffffffu, iwin, (page_of(P, jr) - iwin_blk0) & 31);
       bool live = jr >= icur.lo && jr <= icur.p;
       if (live && (pr < 0 || pr >= P.num_pages)) {
-        if (lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
+        if (CPS == 2 || lane < 16) report(P.error_word, TL_DEVERR_PAGE_RANGE);
         live = false;
       }
-      mask = __ballot_sync(0xffffffffu, live) & 0xffffu;
-      const int jb = j0 + rq_box * box_rows;
+      mask = __ballot_sync(0xffffffffu, live) & (CPS == 2 ? 0xffffffffu : 0xffffu);
+      const int jb = j0 + rq_sub * kChunk + rq_box * box_rows;
       const int blk = page_of(P, jb);
       const int pb = __shfl_sync(0xffffffffu, iwin, (blk - iwin_blk0) & 31);
-      const bool box_ok = blk <= last_blk && pb >= 0 && pb < P.num_pages;
-      slot0 = box_ok ? pb * P.page_size + in_page(P, jb) : n_slots;
+      const bool box_ok = jb <= icur.p && blk <= last_blk && pb >= 0 && pb < P.num_pages;
+      if (box_ok) slot0 = pb * P.page_size + in_page(P, jb);
     }
     const uint32_t bar = smem_u32(&sh.full[w][stage]);
     if (lane == 0) {
@@ -645,11 +658,12 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     // transaction count then runs negative), and the phase cannot complete
     // before lane 0 has arrived
     if (lane < nreq)  // the pools are read once per call: first out of L2
-      tma_load_3d_hint(ring + stage * L::kStageBytes + rq_kind * L::kChunkBytes +
+      tma_load_3d_hint(ring + stage * L::kStageBytes + (rq_kind * CPS + rq_sub) * L::kChunkBytes +
                            rq_half * L::kHalfBytes + rq_box * box_rows * 128,
                        rq_map, rq_half * (KV8 ? 128 : 64), icur.g, slot0, bar, kv_policy);
     ++gs_issue;
-    if (++icur_c == icur.c_end) icur_live = false;
+    icur_c += CPS;
+    if (icur_c >= icur.c_end) icur_live = false;
   };
 
   for (int t = 0; t < R - 1; ++t) issue_next();
@@ -712,16 +726,21 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     const int pr1 = it.p - (P.q_len - 1 - (qr + 8) / P.group);
     const int lr0 = (P.window > 0 && pr0 - P.window + 1 > 0) ? pr0 - P.window + 1 : 0;
     const int lr1 = (P.window > 0 && pr1 - P.window + 1 > 0) ? pr1 - P.window + 1 : 0;
-    for (int c = it.c_begin; c < it.c_end; ++c, ++gs_c) {
-      issue_next();  // keeps R-1 chunks in flight ahead of this one
+    for (int c0 = it.c_begin; c0 < it.c_end; c0 += CPS, ++gs_c) {
+      issue_next();  // keeps R-1 stages in flight ahead of this one
       const int stage = (int)(gs_c % R);
       if (!mbar_wait(smem_u32(&sh.full[w][stage]), (gs_c / R) & 1, abort_flag)) {
         stop = true;
         break;
       }
-      const uint32_t mask = sh.stage_mask[w][stage];
-      const uint32_t kaddr = ring + stage * L::kStageBytes;
-      const uint32_t vaddr = kaddr + L::kChunkBytes;
+      const uint32_t smask = sh.stage_mask[w][stage];
+#pragma unroll 1
+    for (int sub = 0; sub < CPS; ++sub) {
+      const int c = c0 + sub;  // the chunk
+      if (CPS > 1 && c >= it.c_end) break;
+      const uint32_t mask = (smask >> (16 * sub)) & 0xffffu;
+      const uint32_t kaddr = ring + stage * L::kStageBytes + sub * L::kChunkBytes;
+      const uint32_t vaddr = ring + stage * L::kStageBytes + (CPS + sub) * L::kChunkBytes;
       {
         // V rows past the sequence's end (its last chunk only) may hold anything
         const int first_dead = it.p + 1 - c * kChunk;
@@ -918,6 +937,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         }
       }
       __syncwarp();
+    }
     }
     if (stop) break;
     // ------------------------------------------------------ finish the item
