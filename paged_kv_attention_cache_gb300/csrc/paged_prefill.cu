@@ -5,12 +5,15 @@
 // keys are folded block by block into a running max, sum and P.V, so no score
 // tensor wider than one tile exists).
 //
-// Two launches.  A pre-pass converts the V rows each row's tokens can see
-// from the bf16 pages to fp16, once, into the workspace, laid out as
-// [row][KV head][key][d] (exact for |v| in [2^-14, 65504]; larger finite
-// values are reported; keys past the row's last position are zeros).  Then
-// the attention kernel runs one CTA per (pair of query tiles, KV head, row)
-// on the 5th-generation tensor core.  A query tile packs tokens_per_tile =
+// Three launches, the last two programmatic dependents of their predecessor
+// (resident while it finishes, waiting for its results).  A pre-pass converts
+// the V rows each row's tokens can see from the bf16 pages to fp16, once,
+// into the workspace, laid out as [row][KV head][key][d] (exact for |v| in
+// [2^-14, 65504]; larger finite values are reported; keys past the row's
+// last position are zeros), and counts each query-tile pair's key tiles; a
+// one-CTA plan orders the pairs heaviest first.  Then the persistent
+// attention kernel (one CTA per SM) takes work items (pair of query tiles,
+// KV head, row) and runs them on the 5th-generation tensor core.  A query tile packs tokens_per_tile =
 // 128/group consecutive tokens of one row with all `group` query heads that
 // share the KV head, as the 128 M rows (row r = token r/group, head
 // r%group); the CTA holds two consecutive tiles (Q0, Q1), so every K/V tile
@@ -258,6 +261,7 @@ __global__ void __launch_bounds__(kCvtThreads)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int* counter) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;  // work items
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   __shared__ int s_page[kCvtKeys];  // page of each key of the tile; -1: write zeros
   const int b = (int)blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -403,28 +407,43 @@ __global__ void __launch_bounds__(kCvtThreads)
 // pair computes the same bits whichever CTA takes it and when.
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PrefillParams P) {
   __shared__ int cur[kPlanBuckets];  // counts, then each bucket's next slot
-  __shared__ int part[kPlanThreads];
+  __shared__ int wsum[kPlanThreads / 32];
   constexpr int kPer = kPlanBuckets / kPlanThreads;  // buckets per thread
-  const int tid = threadIdx.x, n_e = P.B * P.n_pairs;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, n_e = P.B * P.n_pairs;
   for (int k = tid; k < kPlanBuckets; k += kPlanThreads) cur[k] = 0;
+  // the pre-pass (this grid's predecessor) writes the pair counts; the
+  // attention kernel may launch now and waits for this grid in turn
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   __syncthreads();
   for (int e = tid; e < n_e; e += kPlanThreads)
     atomicAdd(&cur[min(P.pair_tiles[e], kPlanBuckets - 1)], 1);
   __syncthreads();
   // slots go to the buckets from the top down: thread t owns buckets
-  // [kPer t, kPer t + kPer); part = the pairs in buckets above its own
+  // [kPer t, kPer t + kPer); above = the pairs in the buckets of higher
+  // threads = total - (inclusive prefix sum over threads up to t)
   int local = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) local += cur[kPer * tid + i];
-  part[kPlanThreads - 1 - tid] = local;  // reversed: a prefix sum runs from the top
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int v = tid >= off ? part[tid - off] : 0;
-    __syncthreads();
-    part[tid] += v;
-    __syncthreads();
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  int above = part[kPlanThreads - 1 - tid] - local;  // pairs in higher buckets
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int v = lane < kPlanThreads / 32 ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane < kPlanThreads / 32) wsum[lane] = v;
+  }
+  __syncthreads();
+  int above = wsum[kPlanThreads / 32 - 1] - (incl + (wid > 0 ? wsum[wid - 1] : 0));
 #pragma unroll
   for (int i = kPer - 1; i >= 0; --i) {
     const int k = kPer * tid + i, c = cur[k];
@@ -566,6 +585,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = sh.tmem_base;
+  // launched as a programmatic dependent of the plan kernel: the workspace
+  // (work counter, schedule, V copy) is read only after this wait
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------ K / V producer
@@ -1047,9 +1069,26 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
     prefill_v_f16_kernel<true><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
   else
     prefill_v_f16_kernel<false><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
-  prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(P);
-  prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, (cudaStream_t)stream>>>(
-      P, qmap, kmap, vmap, omap, box_rows, counter);
+  if (launch_status() != TL_OK) return TL_ERR_CUDA;
+  // the plan and the attention kernel are programmatic dependent launches:
+  // each becomes resident while its predecessor finishes and waits for its
+  // results (griddepcontrol.wait)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  if (cudaLaunchKernelEx(&cfg, prefill_plan_kernel, P) != cudaSuccess) return TL_ERR_CUDA;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmem;
+  if (cudaLaunchKernelEx(&cfg, prefill_tc_kernel, P, qmap, kmap, vmap, omap, box_rows, counter) !=
+      cudaSuccess)
+    return TL_ERR_CUDA;
   return launch_status();
 }
 
