@@ -237,7 +237,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // The tile's page numbers go to shared memory; then every thread moves
 // 16-byte units (key-major: one key's h_kv x 128 values are contiguous in
 // the pool), kCvtUnroll independent loads in flight.
-constexpr int kCvtUnroll = 16;
+constexpr int kCvtUnroll = 8;
+constexpr int kCvtBlocksPerSm = 4;  // register bound: the scan and page-lookup phases of
+                                    // one CTA overlap the copies of the others
 constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
 
 // Two e4m3 codes (low byte first) as an fp16 pair, exact.
@@ -257,7 +259,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
 }
 
 template <bool KV8>
-__global__ void __launch_bounds__(kCvtThreads)
+__global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int* counter) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;  // work items
