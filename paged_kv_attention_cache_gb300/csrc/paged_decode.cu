@@ -1276,7 +1276,10 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
     warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);
   }
   const int target_splits = (kTargetItems + h_kv - 1) / h_kv;
-  decode_plan_kernel<<<1, 1024, 0, st>>>(P, target_splits, num_sms() * warps);
+  // plan block: sequences are spread over its threads (larger batches loop),
+  // and a smaller block makes its reductions and scan cheaper
+  const int plan_threads = (int)std::min<int64_t>(1024, std::max<int64_t>(256, align_up((size_t)B, 32)));
+  decode_plan_kernel<<<1, plan_threads, 0, st>>>(P, target_splits, num_sms() * warps);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
 
   if (dtype == TL_BF16 || dtype == TL_FP8_E4M3) {
