@@ -151,3 +151,29 @@ def test_workspace_is_reused_across_calls_of_different_shapes():
         ref = oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_table,
                                   case.context_lens, case.scale)
         assert_close(out, ref, f"workspace reuse {seed}")
+
+
+@pytest.mark.parametrize("shape", ["many_short", "one_long", "mixed"])
+def test_piece_plan_extremes(shape):
+    """The decode plan cuts each sequence into bulk pieces and a last round of
+    small pieces (the last ~15% of every sequence longer than 256 keys), all
+    within ceil(12288 / H_kv) + 2B pieces.  Batches at the ends of that range
+    (thousands of short sequences, one very long one, both mixed) against the
+    oracle on sampled sequences, every output finite and no device error."""
+    g = torch.Generator().manual_seed(91)
+    if shape == "many_short":
+        lens = torch.randint(1, 400, (2048,), generator=g).tolist()
+    elif shape == "one_long":
+        lens = [131072]
+    else:
+        lens = torch.randint(1, 300, (500,), generator=g).tolist() + [65536, 257, 4096, 0, 1]
+    case = wl.decode_case(lens, Hq=32, Hkv=8, d=128, seed=92, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g_ = on_gpu(case)
+    out = gpu_decode(g_, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isfinite(out).all()
+    rows = sample_rows(lens, 6, seed=3)
+    ref = oracle_decode_rows(g_, rows)
+    assert_close(out[rows], ref, f"piece plan {shape}")
