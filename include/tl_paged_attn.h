@@ -137,9 +137,13 @@ size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, int32_t h_kv,
  *     s_j = scale * <q[b][h], K_g(j)>,  j = lo..p,  K_g(j) found through
  *           page block_table[b][j / page_size], offset j % page_size
  *     out[b][h] = sum_j softmax(s)_j * V_g(j)
- * L <= 0 gives out[b][h] = 0.  Work is split across CTAs by ranges of pages
- * (split-K) and merged with a log-sum-exp combine; the result does not depend
- * on where the pages are in the pool, and repeats bit for bit.
+ * L <= 0 gives out[b][h] = 0.  Each sequence's keys are cut into pieces
+ * attended independently (split-K) and merged with a log-sum-exp combine in a
+ * fixed order; the result does not depend on where the pages are in the pool,
+ * and repeats bit for bit.  The call enqueues three kernels on `stream` (a
+ * plan, the attention kernel, the merge); the last two are programmatic
+ * dependent launches of their predecessor within the call, and the call as a
+ * whole keeps ordinary stream order with the work around it.
  *   q            [B][h_q][d] in `dtype`
  *   k_cache, v_cache  as above, in `dtype` (read only)
  *   block_table  [B][max_pages_per_seq] int32
