@@ -105,6 +105,22 @@ def test_fp8_decode_edge_lengths(window):
     assert_close(out, ref, f"fp8 decode window {window}")
 
 
+@pytest.mark.parametrize("page_size", [8, 24, 32, 40])
+@pytest.mark.parametrize("window", [0, 37])
+def test_fp8_decode_page_sizes(page_size, window):
+    """e4m3 pipeline stages hold two 16-key chunks; pages that are not a
+    multiple of 16 keys (8, 24, 40) take the per-key page lookup, a page size
+    that is not a power of two the division path; lengths around chunk, stage
+    and page boundaries."""
+    lens = [1, 15, 16, 17, 31, 32, 33, 47, 48, 49, 95, 96, 97, 300, 1000]
+    case = wl.decode_case(lens, Hq=16, Hkv=4, d=128, page_size=page_size, seed=74,
+                          window=window, nan_unused=True)  # dead rows hold NaN codes
+    k8, v8 = _fp8_case(case)
+    rows = list(range(case.B))
+    out, ref = _decode_fp8(case, k8, v8, rows)
+    assert_close(out, ref, f"fp8 decode page {page_size} window {window}")
+
+
 def test_fp8_decode_reports_a_query_beyond_fp16():
     """The query is rounded to fp16 for the e4m3 MMAs: a finite element beyond
     65504 is reported (TL_DEVERR_VALUE_RANGE), not silently made infinite;
