@@ -450,13 +450,14 @@ __device__ __forceinline__ bool f16_overflowed(uint32_t x, uint32_t h) {
   return lo || hi;
 }
 
-// Two e4m3 codes (low byte first) as an fp16 pair; exact (every e4m3 value is
-// an fp16 value).
-__device__ __forceinline__ uint32_t e4m3x2_as_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  const uint16_t c = (uint16_t)two_codes;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(c));
-  return r;
+// Four e4m3 codes (one 32-bit register, low byte first) as two fp16 pairs:
+// codes 0,1 in lo and 2,3 in hi; exact.  The register's halves feed the two
+// conversions directly.
+__device__ __forceinline__ void e4m3x4_as_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Transpose of an 8 x 8 matrix of 16-bit elements held one row pair per
@@ -777,9 +778,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
             for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t w4 = w[2 * h + nt];
+                uint32_t b0, b1;
+                e4m3x4_as_f16x2x2(w[2 * h + nt], b0, b1);
                 mma_16816<true>((h ? s2 : s)[nt], qa[ks + h][0], qa[ks + h][1], qa[ks + h][2],
-                                qa[ks + h][3], e4m3x2_as_f16x2(w4), e4m3x2_as_f16x2(w4 >> 16));
+                                qa[ks + h][3], b0, b1);
               }
           }
         } else {
@@ -888,11 +890,11 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int j = j0 + h;
-            const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1];
-            const uint32_t a0 = movmatrix_trans(e4m3x2_as_f16x2(w0));
-            const uint32_t a1 = movmatrix_trans(e4m3x2_as_f16x2(w1));
-            const uint32_t b0 = movmatrix_trans(e4m3x2_as_f16x2(w0 >> 16));
-            const uint32_t b1 = movmatrix_trans(e4m3x2_as_f16x2(w1 >> 16));
+            uint32_t x0, y0, x1, y1;
+            e4m3x4_as_f16x2x2(w[2 * h], x0, y0);
+            e4m3x4_as_f16x2x2(w[2 * h + 1], x1, y1);
+            const uint32_t a0 = movmatrix_trans(x0), a1 = movmatrix_trans(x1);
+            const uint32_t b0 = movmatrix_trans(y0), b1 = movmatrix_trans(y1);
             if (!TWO_ROWS) {
               mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
               mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
