@@ -347,17 +347,18 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 // ------------------------------------------------------ bf16 decode kernel --
 //
 // Persistent, one CTA per SM, every warp independent (no CTA barrier after
-// set-up).  A warp owns whole work items (split x KV head), taken from an
+// set-up).  A warp owns whole work items (piece x KV head), taken from an
 // atomic counter, and streams their 16-key chunks through a private ring of
-// kRingW shared-memory stages: one lane issues the chunk's tiled TMA boxes
-// (a 3-D tensor map of the pool (d, H_kv, slot), boxes of 8 or 16 rows = one
-// page run, 4 boxes per 8 KiB chunk at page size 16) completing on the stage's
-// mbarrier by transaction bytes, kRingW-1 chunks ahead of the chunk the warp
-// computes.  The stream runs across item boundaries: the next item's
-// descriptor and block-table window are fetched during the current item's
-// last kGrabLead chunks, and each item's Q rows arrive by a bulk copy into
-// one of kRingW Q slots.  Stage
-// layout: K then V as [row half (64 elements = 128 B)][16 rows][128 B] in the
+// kRingW shared-memory stages (one chunk per stage, two for e4m3 pools): one
+// lane per box issues the stage's tiled TMA boxes (a 3-D tensor map of the
+// pool (d, H_kv, slot), boxes of 8 or 16 rows = one page run, 4 boxes per
+// 8 KiB stage at page size 16) completing on the stage's mbarrier by
+// transaction bytes, kRingW-1 stages ahead of the one the warp computes.  The
+// stream runs across item boundaries: the next item's descriptor and
+// block-table window are fetched during the current item's last kGrabLead
+// stages, and each item's Q rows arrive by a bulk copy into one of kRingW Q
+// slots.  Stage layout: the stage's K chunks then its V chunks, each as
+// [row half (64 elements = 128 B)][16 rows][128 B] in the
 // TMA 128-byte swizzle (16-byte unit u of row r at unit u ^ (r & 7), so
 // ldmatrix reads of 8 rows hit 8 different bank groups).  A box of a block
 // past the sequence's last page, or of a bad page, gets an out-of-range slot
@@ -372,12 +373,10 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 #ifndef TL_DECODE_WARPS
 #define TL_DECODE_WARPS 8
 #endif
-constexpr int kRingW = TL_DECODE_RING;      // stages per warp (16-bit pools)
-// e4m3 pools move half the bytes per chunk: one stage more keeps more bytes
-// in flight per warp (the stream is bound by bytes in flight x latency)
+constexpr int kRingW = TL_DECODE_RING;      // stages per warp
 constexpr int kMaxRing = kRingW;
 constexpr int kMaxWarpsW = TL_DECODE_WARPS;
-constexpr int kGrabLead = 4;  // chunks left to issue when a warp starts fetching its next item
+constexpr int kGrabLead = 4;  // stages left to issue when a warp starts fetching its next item
 
 // Per-warp shared memory: kRingW stages of kCps chunks of K and V as the TMA
 // lands them (16-bit or e4m3 elements, rows split in 128-byte parts; an e4m3
