@@ -172,6 +172,35 @@ tl_status tl_paged_attn_decode(const void* q, const void* k_cache, const void* v
                                size_t workspace_bytes, uint32_t* error_word, void* stream);
 
 /*
+ * KV_CACHE_WRITE then PAGED_ATTENTION decode in one call ("How serving works
+ * in Tlaloc", section 1: each step writes its tokens' K/V, then attends):
+ * the result, the pools afterwards and the error bits are those of
+ * tl_kv_cache_write (tl_kv_cache_write_fp8 for e4m3 pools) of the n_new rows
+ * k_new / v_new [n_new][h_kv][d] at slot_mapping [n_new] (int64, -1 =
+ * padding, never written) followed by tl_paged_attn_decode on the same
+ * stream.  The rows are written by extra CTAs of the decode's first launch,
+ * so the call enqueues three kernels instead of four.
+ *   new_dtype    dtype of k_new / v_new: the pool's dtype for TL_BF16 and
+ *                TL_F32 pools (a copy); TL_BF16 or TL_F32 for TL_FP8_E4M3
+ *                pools (converted to e4m3 codes, nearest with ties to even,
+ *                clamped to +-448, NaN to the NaN code)
+ *   k_cache, v_cache  the pools, written in place, then read
+ *   other arguments, workspace size and support as tl_paged_attn_decode.
+ * Errors: as the two calls; a slot outside the pools sets
+ * TL_DEVERR_SLOT_RANGE and that row is skipped.  Duplicate live slots are a
+ * caller error (which row lands is unspecified).
+ */
+tl_status tl_paged_attn_decode_write(const void* q, const void* k_new, const void* v_new,
+                                     tl_dtype new_dtype, const int64_t* slot_mapping,
+                                     int32_t n_new, void* k_cache, void* v_cache,
+                                     const int32_t* block_table, int32_t max_pages_per_seq,
+                                     const int32_t* context_lens, float* out, int32_t B,
+                                     int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                     int32_t page_size, int32_t window, float scale,
+                                     tl_dtype dtype, void* workspace, size_t workspace_bytes,
+                                     uint32_t* error_word, void* stream);
+
+/*
  * Decode without any device allocation, for callers that cannot allocate on
  * this path: a host framework that owns all device memory through its own
  * pool, or a latency-bound loop that cannot afford an allocator call.  There

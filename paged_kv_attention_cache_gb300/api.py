@@ -150,6 +150,43 @@ def tl_paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
     return out
 
 
+def tl_paged_attn_decode_write(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                               slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                               v_cache: torch.Tensor, block_table: torch.Tensor,
+                               context_lens: torch.Tensor, scale: float, window: int = 0,
+                               out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               error_word: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """The write of the new rows k_new / v_new [N, H_kv, d] at slot_mapping
+    [N] (int64, -1 = padding) into the pools (in place; e4m3 pools take bf16
+    or f32 rows and convert them), then decode as tl_paged_attn_decode, in
+    one call: out[B, H_q, d] (float32)."""
+    _need(q, "q", _query_dtype(k_cache.dtype))
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    _need(k_new, "k_new")
+    _need(v_new, "v_new", k_new.dtype)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    B, hq, d = q.shape
+    P, ps, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(tl_paged_attn_decode_workspace_size(B, hq, hkv, d), q.device)
+    st = _lib.load().tl_paged_attn_decode_write(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _DTYPES.get(k_new.dtype, -1), _ptr(slot_mapping),
+        slot_mapping.numel(), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(context_lens), _ptr(out), B, hq, hkv, d, P, ps, int(window),
+        float(scale), _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), workspace.numel(),
+        _ptr(error_word), _stream(stream))
+    _check(st, "tl_paged_attn_decode_write")
+    return out
+
+
 TL_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 

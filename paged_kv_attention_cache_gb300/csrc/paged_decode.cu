@@ -42,6 +42,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "kv_write.cuh"
 
 namespace tl {
 
@@ -111,6 +112,16 @@ struct DecodeParams {
   float scale_log2;    // scale * log2(e): scores are kept in log2 units
   DecodeWorkspace ws;
   uint32_t* error_word;
+  // new rows written by the call itself (tl_paged_attn_decode_write; n_new 0
+  // otherwise): the plan launch's extra CTAs scatter them into the pools
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  void* k_dst;
+  void* v_dst;
+  int32_t n_new;
+  int32_t new_kind;   // 0 copy (same dtype), 1 e4m3 codes of bf16 rows, 2 of f32 rows
+  int32_t row_units;  // 16-byte vectors (copy) or 8-element steps (e4m3) of one row
 };
 
 // Logical block of key j and its offset in the page (a shift and a mask for
@@ -239,6 +250,34 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
   // the attention kernel may launch now: it waits for this grid's results
   // (griddepcontrol.wait) after its own set-up
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  if (blockIdx.x > 0) {
+    // CTAs past the first write the call's new rows: one warp per token,
+    // slot -1 skipped, a slot outside the pools reported and skipped
+    const int64_t first = (int64_t)(blockIdx.x - 1) * nw + wid;
+    const int64_t stride = (int64_t)(gridDim.x - 1) * nw;
+    const int64_t n_slots = (int64_t)P.num_pages * P.page_size;
+    for (int64_t t = first; t < P.n_new; t += stride) {
+      const int64_t slot = P.slot_mapping[t];
+      if (slot == -1) continue;
+      if (slot < 0 || slot >= n_slots) {
+        if (lane == 0) report(P.error_word, TL_DEVERR_SLOT_RANGE);
+        continue;
+      }
+      const int u = P.row_units;
+      if (P.new_kind == 0)
+        write_token_rows(static_cast<const int4*>(P.k_new) + t * u,
+                         static_cast<const int4*>(P.v_new) + t * u,
+                         static_cast<int4*>(P.k_dst) + slot * u,
+                         static_cast<int4*>(P.v_dst) + slot * u, u, lane);
+      else if (P.new_kind == 1)
+        write_token_rows_e4m3<false>(P.k_new, P.v_new, static_cast<uint2*>(P.k_dst),
+                                     static_cast<uint2*>(P.v_dst), t, slot, u, lane);
+      else
+        write_token_rows_e4m3<true>(P.k_new, P.v_new, static_cast<uint2*>(P.k_dst),
+                                    static_cast<uint2*>(P.v_dst), t, slot, u, lane);
+    }
+    return;
+  }
   int lo0 = 0, p0 = -1, n0 = 0;  // sequence tid
   if (tid < P.B) {
     seq_range(P, tid, lo0, p0, true);
@@ -1206,13 +1245,25 @@ extern "C" size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, in
 }
 
 namespace tl {
+// The new rows a decode call writes itself (tl_paged_attn_decode_write):
+// n rows of k_new / v_new in new_dtype, scattered by slot into the pools.
+struct NewRows {
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int64_t* slot_mapping = nullptr;
+  int32_t n = 0;
+  tl_dtype new_dtype = TL_BF16;
+  void* k_dst = nullptr;
+  void* v_dst = nullptr;
+};
+
 static tl_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                              const int32_t* block_table, int32_t max_pages_per_seq,
                              const int32_t* context_lens, float* out, int32_t B, int32_t q_len,
                              int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
                              int32_t page_size, int32_t window, int32_t ring_pages, float scale,
                              tl_dtype dtype, void* workspace, size_t workspace_bytes,
-                             uint32_t* error_word, void* stream) {
+                             uint32_t* error_word, void* stream, const NewRows& nr = NewRows()) {
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || num_pages <= 0 || page_size <= 0 ||
       max_pages_per_seq <= 0 || window < 0)
     return TL_ERR_INVALID_ARG;
@@ -1265,6 +1316,37 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   P.scale_log2 = scale * kLog2e;
   decode_ws_layout(B, q_len * h_q, h_kv, d, &P.ws, static_cast<char*>(workspace));
   P.error_word = error_word;
+  // the call's own new rows: validated like tl_kv_cache_write / _fp8
+  P.k_new = nr.k_new;
+  P.v_new = nr.v_new;
+  P.slot_mapping = nr.slot_mapping;
+  P.k_dst = nr.k_dst;
+  P.v_dst = nr.v_dst;
+  P.n_new = 0;
+  P.new_kind = 0;
+  P.row_units = 0;
+  if (nr.n < 0) return TL_ERR_INVALID_ARG;
+  if (nr.n > 0) {
+    if (!nr.k_new || !nr.v_new || !nr.slot_mapping || !nr.k_dst || !nr.v_dst)
+      return TL_ERR_INVALID_ARG;
+    if (!aligned16(nr.k_new) || !aligned16(nr.v_new) ||
+        (reinterpret_cast<uintptr_t>(nr.slot_mapping) & 7u))
+      return TL_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)h_kv * d;
+    if (dtype == TL_FP8_E4M3) {
+      if (nr.new_dtype != TL_BF16 && nr.new_dtype != TL_F32) return TL_ERR_UNSUPPORTED;
+      if (row % 16 != 0) return TL_ERR_INVALID_ARG;
+      P.new_kind = nr.new_dtype == TL_BF16 ? 1 : 2;
+      P.row_units = (int32_t)(row / 8);
+    } else {
+      if (nr.new_dtype != dtype) return TL_ERR_UNSUPPORTED;
+      const int64_t row_bytes = row * (dtype == TL_F32 ? 4 : 2);
+      if (row_bytes % 16 != 0) return TL_ERR_INVALID_ARG;
+      P.new_kind = 0;
+      P.row_units = (int32_t)(row_bytes / 16);
+    }
+    P.n_new = nr.n;
+  }
   cudaStream_t st = (cudaStream_t)stream;
 
   // warps per CTA of the bf16 / e4m3 kernel (as many as the stages fit)
@@ -1280,7 +1362,13 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   // plan block: sequences are spread over its threads (larger batches loop),
   // and a smaller block makes its reductions and scan cheaper
   const int plan_threads = (int)std::min<int64_t>(1024, std::max<int64_t>(256, align_up((size_t)B, 32)));
-  decode_plan_kernel<<<1, plan_threads, 0, st>>>(P, target_splits, num_sms() * warps);
+  // the plan CTA, then (for a call that writes its new rows) CTAs with one
+  // warp per new row, up to one per SM
+  const int64_t write_ctas =
+      P.n_new > 0 ? std::min<int64_t>(num_sms(), (P.n_new + plan_threads / 32 - 1) / (plan_threads / 32))
+                  : 0;
+  decode_plan_kernel<<<(unsigned)(1 + write_ctas), plan_threads, 0, st>>>(P, target_splits,
+                                                                          num_sms() * warps);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
 
   if (dtype == TL_BF16 || dtype == TL_FP8_E4M3) {
@@ -1366,6 +1454,26 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
                          B, 1, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
                          workspace, workspace_bytes, error_word, stream);
+}
+
+extern "C" tl_status tl_paged_attn_decode_write(
+    const void* q, const void* k_new, const void* v_new, tl_dtype new_dtype,
+    const int64_t* slot_mapping, int32_t n_new, void* k_cache, void* v_cache,
+    const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* context_lens,
+    float* out, int32_t B, int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+    int32_t page_size, int32_t window, float scale, tl_dtype dtype, void* workspace,
+    size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  tl::NewRows nr;
+  nr.k_new = k_new;
+  nr.v_new = v_new;
+  nr.slot_mapping = slot_mapping;
+  nr.n = n_new;
+  nr.new_dtype = new_dtype;
+  nr.k_dst = k_cache;
+  nr.v_dst = v_cache;
+  return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
+                         B, 1, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
+                         workspace, workspace_bytes, error_word, stream, nr);
 }
 
 extern "C" tl_status tl_paged_attn_decode_ring(

@@ -92,6 +92,21 @@ def test_host_validation_refuses_before_any_launch(lib):
     assert dec() == tl.TL_ERR_WORKSPACE
     assert dec(ws=2048 + 16, wsb=1 << 30) == tl.TL_ERR_WORKSPACE  # not 256-byte aligned
 
+    # decode that writes its new rows first: the write's own checks, before
+    # any launch (a 256-aligned fake workspace passes the size check)
+    def decw(nk=2304, nv=2560, nd=1, sm=2816, n=2, **kw):
+        a = dict(args, ws=4096, wsb=1 << 30, **kw)
+        return lib.tl_paged_attn_decode_write(a["q"], nk, nv, nd, sm, n, a["k"], a["v"], a["bt"],
+                                              a["maxp"], a["cl"], a["out"], a["B"], a["hq"],
+                                              a["hkv"], a["d"], a["P"], a["ps"], a["w"], a["sc"],
+                                              a["dt"], a["ws"], a["wsb"], a["err"], a["st"])
+    assert decw(n=-1) == tl.TL_ERR_INVALID_ARG
+    assert decw(nk=None) == tl.TL_ERR_INVALID_ARG
+    assert decw(sm=2820) == tl.TL_ERR_INVALID_ARG  # slots not 8-byte aligned
+    assert decw(nk=2312) == tl.TL_ERR_INVALID_ARG  # new rows not 16-byte aligned
+    assert decw(nd=0) == tl.TL_ERR_UNSUPPORTED  # f32 rows into bf16 pools
+    assert decw(nd=2, dt=2) == tl.TL_ERR_UNSUPPORTED  # e4m3 rows into e4m3 pools
+
     def pre(**kw):
         a = dict(args, **kw)
         return lib.tl_paged_attn_prefill(a["q"], a["k"], a["v"], a["bt"], a["maxp"], a["cl"],
