@@ -3,9 +3,12 @@
 One step = one pass of the decode hot path over one batch: KV_CACHE_WRITE of
 the batch's new tokens, then paged-attention decode (plan + split-K kernel +
 combine), on the Llama-3-8B-shaped layer (B=64, H_q=32, H_kv=8, d=128, bf16,
-pages of 16, context lengths U[512, 8192], shuffled pool).  value = KV bytes
-the decode must read (sum over sequences of L * 2 * H_kv * d * 2 bytes) per
-second.  The batched-prefill workload (B=8 rows of 2,048 tokens) is timed
+pages of 16, context lengths U[512, 8192], shuffled pool), through
+tl_paged_attn_decode_write (the write runs inside the decode call's first
+launch).  value = KV bytes the decode must read (sum over sequences of
+L * 2 * H_kv * d * 2 bytes) per second.  The same step as the two separate
+calls is reported too ("separate_step"), and the roofline is the decode call
+timed on its own.  The batched-prefill workload (B=8 rows of 2,048 tokens) is timed
 after it and reported under "prefill" in TFLOP/s.
 
 --impl reference times the CPU oracle (the plain C double-precision
@@ -170,18 +173,29 @@ def run_ours(args):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
+        """One decode step through the fused call: the write of the 64 new
+        rows and the decode, tl_paged_attn_decode_write (three kernels)."""
+        tl.tl_paged_attn_decode_write(g.q, g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache,
+                                      g.block_table, g.context_lens, case.scale, out=out,
+                                      workspace=ws, error_word=err)
+
+    def write():
         tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping,
                              error_word=err)
+
+    def decode():
         tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
                                 case.scale, out=out, workspace=ws, error_word=err)
 
     for _ in range(args.warmup):
         step()
+        write()
+        decode()
     torch.cuda.synchronize()
-    n_ev = args.steps
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n_ev)]
+              for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_start, s_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -193,15 +207,21 @@ def run_ours(args):
             for _ in range(20):
                 step()
             torch.cuda.synchronize()
+        # the timed region: args.steps fused steps
         start.record(stream)
-        for i in range(args.steps):
-            tl.tl_kv_cache_write(g.k_new, g.v_new, g.k_cache, g.v_cache, g.slot_mapping,
-                                 error_word=err)
-            dec_ev[i][0].record(stream)
-            tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
-                                    case.scale, out=out, workspace=ws, error_word=err)
-            dec_ev[i][1].record(stream)
+        for _ in range(args.steps):
+            step()
         stop.record(stream)
+        torch.cuda.synchronize()
+        # the same steps as the two separate calls, the decode call timed on
+        # its own (the roofline's kernel)
+        s_start.record(stream)
+        for i in range(args.steps):
+            write()
+            dec_ev[i][0].record(stream)
+            decode()
+            dec_ev[i][1].record(stream)
+        s_stop.record(stream)
         torch.cuda.synchronize()
         t_end = time.time() + (0.5 if args.soak_seconds > 0 else 0.0)
         while time.time() < t_end:
@@ -213,6 +233,7 @@ def run_ours(args):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during the timed decode steps")
     elapsed_ms = start.elapsed_time(stop)
+    sep_ms = s_start.elapsed_time(s_stop) / args.steps
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
     elapsed_ms, total_kvb = reduce_over_ranks(elapsed_ms, kvb, dev)
     ms_per_step = elapsed_ms / args.steps
@@ -265,10 +286,10 @@ def run_ours(args):
             x = dev_in[slot]
             stream.wait_event(landed[slot])
             stream.wait_event(read[slot])  # the slot's previous output has been read
-            tl.tl_kv_cache_write(x["k_new"], x["v_new"], g.k_cache, g.v_cache,
-                                 x["slot_mapping"])
-            tl.tl_paged_attn_decode(x["q"], g.k_cache, g.v_cache, x["block_table"],
-                                    x["context_lens"], case.scale, out=outs[slot], workspace=ws)
+            tl.tl_paged_attn_decode_write(x["q"], x["k_new"], x["v_new"], x["slot_mapping"],
+                                          g.k_cache, g.v_cache, x["block_table"],
+                                          x["context_lens"], case.scale, out=outs[slot],
+                                          workspace=ws)
             consumed[slot].record(stream)
             cstream.wait_event(consumed[slot])
             with torch.cuda.stream(cstream):
@@ -352,8 +373,12 @@ def run_ours(args):
         "verify_decode": verify_line,
         "fp8_decode": fp8_line,
         "e2e": e2e,
+        "separate_step": {"calls": "tl_kv_cache_write, then tl_paged_attn_decode (four kernels)",
+                          "ms_per_step": round(sep_ms, 5),
+                          "gbs": round(kvb / (sep_ms * 1e-3) / 1e9, 1),
+                          "frac": round(kvb / (sep_ms * 1e-3) / 1e9 / hbm, 4)},
         "cpu_baseline": cpu,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
