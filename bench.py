@@ -431,7 +431,8 @@ def run_ring(args, dev, stream, hbm):
 def run_fp8(args, dev, stream, hbm):
     """Decode of the Llama-3-8B-shaped batch (B=64) over e4m3 pools: the pools
     are the bf16 pools written through tl_kv_cache_write_fp8 (every slot), the
-    step is the write of the 64 new rows plus the decode, as for bf16."""
+    step is the write of the 64 new rows plus the decode in one call
+    (tl_paged_attn_decode_write), as for bf16."""
     import torch
 
     import paged_kv_attention_cache_gb300 as tl
@@ -450,10 +451,10 @@ def run_fp8(args, dev, stream, hbm):
     ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
     kvb = int(case.context_lens.sum().item()) * 2 * hkv * d  # one byte per element
 
-    def step():
-        tl.tl_kv_cache_write_fp8(g.k_new, g.v_new, k8, v8, g.slot_mapping)
-        tl.tl_paged_attn_decode(g.q, k8, v8, g.block_table, g.context_lens, case.scale,
-                                out=out, workspace=ws)
+    def step():  # the write of the new rows (converted to e4m3) and the decode, one call
+        tl.tl_paged_attn_decode_write(g.q, g.k_new, g.v_new, g.slot_mapping, k8, v8,
+                                      g.block_table, g.context_lens, case.scale, out=out,
+                                      workspace=ws)
 
     for _ in range(max(3, args.warmup)):
         step()
