@@ -639,9 +639,16 @@ def cpu_baseline(case, g, args):
         if time.perf_counter() - t0 >= args.cpu_seconds:
             break
     dt = (time.perf_counter() - t0) / reps
+    # one repetition on a single thread, beside the all-cores figure
+    t1 = time.perf_counter()
+    oracle.kv_cache_write(kn, vn, kc, vc, sm)
+    oracle.paged_decode(q, kc, vc, bt, cl, case.scale, window=case.window, threads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": round(kvb / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "sample": f"the full decode step ({case.B} sequences), "
-                                        f"{reps} repetitions, {dt:.3f} s each"}
+                                        f"{reps} repetitions, {dt:.3f} s each",
+            "single_thread": {"value": round(kvb / dt1 / 1e9, 3), "unit": "GB/s",
+                              "sample": f"one full decode step, {dt1:.3f} s"}}
 
 
 # ------------------------------------------------------------- reference --
