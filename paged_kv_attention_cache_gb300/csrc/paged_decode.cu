@@ -498,14 +498,6 @@ __device__ __forceinline__ void e4m3x4_as_f16x2x2(uint32_t w, uint32_t& lo, uint
       : "r"(w));
 }
 
-// Transpose of an 8 x 8 matrix of 16-bit elements held one row pair per
-// lane (lane l: row l / 4, columns 2(l % 4), +1): lane l gets row l / 4 of
-// the transpose.
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
-  return r;
-}
 
 struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits;
@@ -558,6 +550,9 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
   const int n_slots = P.num_pages * P.page_size;
   constexpr int CPS = L::kCps;
+  // chunks of a stage that share one softmax step: both of an e4m3 stage
+  // when the group fits rows 0-7 (registers allow it there), else one
+  constexpr int NJ = (KV8 && !TWO_ROWS) ? CPS : 1;
   const int nbox = kChunk / box_rows;             // boxes per row half of a chunk
   const int per_kind = CPS * L::kHalves * nbox;   // boxes of K (or V) per stage
   const int nreq = 2 * per_kind;                  // TMA requests per stage
@@ -773,15 +768,17 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         break;
       }
       const uint32_t smask = sh.stage_mask[w][stage];
+      const int nlive = min(CPS, it.c_end - c0);  // the stage's chunks inside the item
 #pragma unroll 1
-    for (int sub = 0; sub < CPS; ++sub) {
-      const int c = c0 + sub;  // the chunk
-      if (CPS > 1 && c >= it.c_end) break;
-      const uint32_t mask = (smask >> (16 * sub)) & 0xffffu;
-      const uint32_t kaddr = ring + stage * L::kStageBytes + sub * L::kChunkBytes;
-      const uint32_t vaddr = ring + stage * L::kStageBytes + (CPS + sub) * L::kChunkBytes;
-      {
+    for (int sub0 = 0; sub0 < nlive; sub0 += NJ) {
+      // chunks sub0 .. sub0+nj-1 of the stage share one softmax step
+      const int nj = min(NJ, nlive - sub0);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        if (j >= nj) break;
         // V rows past the sequence's end (its last chunk only) may hold anything
+        const int c = c0 + sub0 + j;
+        const uint32_t vaddr = ring + stage * L::kStageBytes + (CPS + sub0 + j) * L::kChunkBytes;
         const int first_dead = it.p + 1 - c * kChunk;
         if (first_dead < kChunk) {
           const int n_dead = kChunk - max(first_dead, 0);
@@ -796,10 +793,15 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           __syncwarp();
         }
       }
-      // S = Q K^T over the chunk's 16 keys (two n-tiles of 8 keys); even and
+      // S = Q K^T over each chunk's 16 keys (two n-tiles of 8 keys); even and
       // odd K steps accumulate separately (two independent MMA chains)
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
+      float s[NJ][2][4];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) s[j][n][0] = s[j][n][1] = s[j][n][2] = s[j][n][3] = 0.f;
+        if (j >= nj) continue;
+        const uint32_t kaddr = ring + stage * L::kStageBytes + (sub0 + j) * L::kChunkBytes;
         float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if constexpr (KV8) {
           // the B fragment of key row n0 + g straight from the e4m3 codes:
@@ -818,8 +820,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
               for (int nt = 0; nt < 2; ++nt) {
                 uint32_t b0, b1;
                 e4m3x4_as_f16x2x2(w[2 * h + nt], b0, b1);
-                mma_16816<true>((h ? s2 : s)[nt], qa[ks + h][0], qa[ks + h][1], qa[ks + h][2],
-                                qa[ks + h][3], b0, b1);
+                mma_16816<true>((h ? s2 : s[j])[nt], qa[ks + h][0], qa[ks + h][1],
+                                qa[ks + h][2], qa[ks + h][3], b0, b1);
               }
           }
         } else {
@@ -832,7 +834,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
             ldmatrix_x4(
                 kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
                 b1, b2, b3);
-            float(*acc)[4] = (ks & 1) ? s2 : s;
+            float(*acc)[4] = (ks & 1) ? s2 : s[j];
             mma_16816<KV8>(acc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
             mma_16816<KV8>(acc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
           }
@@ -840,42 +842,49 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[n][e] += s2[n][e];
+          for (int e = 0; e < 4; ++e) s[j][n][e] += s2[n][e];
       }
       float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int key = n * 8 + qc + e;
-          const bool ok = (mask >> key) & 1u;
+          const bool ok = j < nj && ((smask >> (16 * (sub0 + j) + key)) & 1u);
           bool ok0 = ok, ok1 = ok;
           if (P.q_len > 1) {
-            const int kp = c * kChunk + key;
+            const int kp = (c0 + sub0 + j) * kChunk + key;
             ok0 = ok && kp >= lr0 && kp <= pr0;
             ok1 = ok && kp >= lr1 && kp <= pr1;
           }
-          s[n][e] = ok0 ? s[n][e] * P.scale_log2 : -INFINITY;
-          s[n][2 + e] = ok1 ? s[n][2 + e] * P.scale_log2 : -INFINITY;
-          mx0 = fmaxf(mx0, s[n][e]);
-          mx1 = fmaxf(mx1, s[n][2 + e]);
+          s[j][n][e] = ok0 ? s[j][n][e] * P.scale_log2 : -INFINITY;
+          s[j][n][2 + e] = ok1 ? s[j][n][2 + e] * P.scale_log2 : -INFINITY;
+          mx0 = fmaxf(mx0, s[j][n][e]);
+          mx1 = fmaxf(mx1, s[j][n][2 + e]);
         }
       }
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      // lazy running max: the base moves only when the chunk's max passes it
+      // lazy running max: the base moves only when the step's max passes it
       // by more than 2^8 (P stays below 256), so O is rescaled rarely
       const float mn0 = (m0 == -INFINITY || mx0 > m0 + kLazyLog2) ? fmaxf(m0, mx0) : m0;
       const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
       const float c0 = fast_exp2(m0 - base0);
       m0 = mn0;
-      float p[2][4];
+      float p[NJ][2][4];
+      float sum0 = 0.f;
 #pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        p[n][0] = fast_exp2(s[n][0] - base0);
-        p[n][1] = fast_exp2(s[n][1] - base0);
+      for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          p[j][n][0] = fast_exp2(s[j][n][0] - base0);
+          p[j][n][1] = fast_exp2(s[j][n][1] - base0);
+        }
+        sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
       }
-      l0 = l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+      l0 = l0 * c0 + sum0;
       float c1 = c0;
       if (TWO_ROWS) {
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -884,12 +893,17 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         const float base1 = mn1 == -INFINITY ? 0.f : mn1;
         c1 = fast_exp2(m1 - base1);
         m1 = mn1;
+        float sum1 = 0.f;
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          p[n][2] = fast_exp2(s[n][2] - base1);
-          p[n][3] = fast_exp2(s[n][3] - base1);
+        for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            p[j][n][2] = fast_exp2(s[j][n][2] - base1);
+            p[j][n][3] = fast_exp2(s[j][n][3] - base1);
+          }
+          sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
         }
-        l1 = l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        l1 = l1 * c1 + sum1;
       }
       // rows 8-15 hold either the second half of the group (TWO_ROWS) or the
       // low bf16 part of rows 0-7's probabilities; both rescale with their row
@@ -902,77 +916,85 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           o[n][3] *= c1;
         }
       }
-      // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
-      uint32_t h0, l0w, h2, l2w;
-      split16<KV8>(p[0][0], p[0][1], h0, l0w);
-      split16<KV8>(p[1][0], p[1][1], h2, l2w);
-      if constexpr (KV8) {
-        // V's B fragments from the e4m3 codes: lane (g, t) reads codes
-        // 16j+4t .. +3 of key rows g and 8+g, widens them to fp16 pairs (a
-        // row pair of two 8 x 8 blocks each: columns = d 16j+4t'+(0,1) and
-        // 16j+4t'+(2,3)) and transposes the blocks in registers, giving keys
-        // (2t, 2t+1) and (2t+8, 2t+9) at one d per lane.  The n-tiles 2j and
-        // 2j+1 then hold output columns 16j+4t+(0,1) and 16j+4t+(2,3).
-        const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
-        uint32_t h1 = 0u, l1w = 0u, h3 = 0u, l3w = 0u;
-        if (TWO_ROWS) {
-          split16<true>(p[0][2], p[0][3], h1, l1w);
-          split16<true>(p[1][2], p[1][3], h3, l3w);
-        }
 #pragma unroll
-        for (int j0 = 0; j0 < D / 16; j0 += 2) {
-          // units j0 and j0 + 1 of key rows 0-7 and 8-15
-          const int u = j0 + (mi >> 1);
-          uint32_t w[4];
-          ldmatrix_x4(vaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+      for (int jc = 0; jc < NJ; ++jc) {
+        if (jc >= nj) break;
+        const uint32_t vaddr =
+            ring + stage * L::kStageBytes + (CPS + sub0 + jc) * L::kChunkBytes;
+        // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
+        uint32_t h0, l0w, h2, l2w;
+        split16<KV8>(p[jc][0][0], p[jc][0][1], h0, l0w);
+        split16<KV8>(p[jc][1][0], p[jc][1][1], h2, l2w);
+        if constexpr (KV8) {
+          // V's B fragments from the e4m3 codes: a transposing ldmatrix of
+          // 16-byte unit j (its 16-bit elements being code pairs) hands lane
+          // (g, t) the codes 2g and 2g+1 of keys 2t and 2t+1 (and of 2t+8,
+          // 2t+9 from the second key half).  One byte permute pairs the keys
+          // per code, and the two conversions give the B fragments of d
+          // 16j+2g (n-tile 2j) and 16j+2g+1 (n-tile 2j+1).  The accumulators
+          // of n-tiles 2j and 2j+1 then hold output columns 16j+4t+(0,2) and
+          // 16j+4t+(1,3).
+          const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
+          uint32_t h1 = 0u, l1w = 0u, h3 = 0u, l3w = 0u;
+          if (TWO_ROWS) {
+            split16<true>(p[jc][0][2], p[jc][0][3], h1, l1w);
+            split16<true>(p[jc][1][2], p[jc][1][3], h3, l3w);
+          }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = j0 + h;
-            uint32_t x0, y0, x1, y1;
-            e4m3x4_as_f16x2x2(w[2 * h], x0, y0);
-            e4m3x4_as_f16x2x2(w[2 * h + 1], x1, y1);
-            const uint32_t a0 = movmatrix_trans(x0), a1 = movmatrix_trans(x1);
-            const uint32_t b0 = movmatrix_trans(y0), b1 = movmatrix_trans(y1);
-            if (!TWO_ROWS) {
-              mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
-              mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
-            } else {
-              mma_16816<true>(o[2 * j], h0, h1, h2, h3, a0, a1);
-              mma_16816<true>(o[2 * j], l0w, l1w, l2w, l3w, a0, a1);
-              mma_16816<true>(o[2 * j + 1], h0, h1, h2, h3, b0, b1);
-              mma_16816<true>(o[2 * j + 1], l0w, l1w, l2w, l3w, b0, b1);
+          for (int j0 = 0; j0 < D / 16; j0 += 2) {
+            // units j0 and j0 + 1 of key rows 0-7 and 8-15
+            const int u = j0 + (mi >> 1);
+            uint32_t w[4];
+            ldmatrix_x4_trans(vaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2],
+                              w[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int j = j0 + h;
+              // bytes (k 2t: 2g, 2g+1; k 2t+1: 2g, 2g+1) -> (2g: k, k+1; 2g+1: k, k+1)
+              uint32_t a0, b0, a1, b1;
+              e4m3x4_as_f16x2x2(__byte_perm(w[2 * h], 0u, 0x3120u), a0, b0);
+              e4m3x4_as_f16x2x2(__byte_perm(w[2 * h + 1], 0u, 0x3120u), a1, b1);
+              if (!TWO_ROWS) {
+                mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
+                mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
+              } else {
+                mma_16816<true>(o[2 * j], h0, h1, h2, h3, a0, a1);
+                mma_16816<true>(o[2 * j], l0w, l1w, l2w, l3w, a0, a1);
+                mma_16816<true>(o[2 * j + 1], h0, h1, h2, h3, b0, b1);
+                mma_16816<true>(o[2 * j + 1], l0w, l1w, l2w, l3w, b0, b1);
+              }
             }
           }
-        }
-      } else {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int tok = (mi & 1) * 8 + ri;
-        if (!TWO_ROWS) {
-#pragma unroll
-          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-            const int u = 2 * nd2 + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(
-                vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
-                b1, b2, b3);
-            mma_16816<KV8>(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
-            mma_16816<KV8>(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
-          }
         } else {
-          uint32_t h1, l1w, h3, l3w;
-          split16<KV8>(p[0][2], p[0][3], h1, l1w);
-          split16<KV8>(p[1][2], p[1][3], h3, l3w);
+          const int mi = lane >> 3, ri = lane & 7;
+          const int tok = (mi & 1) * 8 + ri;
+          if (!TWO_ROWS) {
 #pragma unroll
-          for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-            const int u = 2 * nd2 + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(
-                vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
-                b1, b2, b3);
-            mma_16816<KV8>(o[2 * nd2], h0, h1, h2, h3, b0, b1);
-            mma_16816<KV8>(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
-            mma_16816<KV8>(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
-            mma_16816<KV8>(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+              const int u = 2 * nd2 + (mi >> 1);
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4_trans(
+                  vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                  b1, b2, b3);
+              mma_16816<KV8>(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
+              mma_16816<KV8>(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+            }
+          } else {
+            uint32_t h1, l1w, h3, l3w;
+            split16<KV8>(p[jc][0][2], p[jc][0][3], h1, l1w);
+            split16<KV8>(p[jc][1][2], p[jc][1][3], h3, l3w);
+#pragma unroll
+            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+              const int u = 2 * nd2 + (mi >> 1);
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4_trans(
+                  vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                  b1, b2, b3);
+              mma_16816<KV8>(o[2 * nd2], h0, h1, h2, h3, b0, b1);
+              mma_16816<KV8>(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
+              mma_16816<KV8>(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
+              mma_16816<KV8>(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+            }
           }
         }
       }
@@ -992,9 +1014,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     const int h0r = (qr / P.group) * P.h_q + it.g * P.group + qr % P.group;
     const int h1r = ((qr + 8) / P.group) * P.h_q + it.g * P.group + (qr + 8) % P.group;
     // One output row of this lane, times f: 16-bit pools hold float pairs at
-    // columns 8n + 2t (n-tile n), e4m3 pools float quads at 16j + 4t (n-tiles
-    // 2j and 2j+1).  Row qr adds the low part of P carried in rows 8-15
-    // unless TWO_ROWS; with TWO_ROWS, rows 8-15 are row qr + 8.
+    // columns 8n + 2t (n-tile n), e4m3 pools float quads at 16j + 4t (n-tile
+    // 2j: columns +0 and +2; n-tile 2j+1: +1 and +3).  Row qr adds the low
+    // part of P carried in rows 8-15 unless TWO_ROWS; with TWO_ROWS, rows
+    // 8-15 are row qr + 8.
     auto write_row = [&](float* dst, bool second, float f, bool keep_in_l2, uint64_t pol) {
       if constexpr (KV8) {
 #pragma unroll
@@ -1002,8 +1025,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           const float* x = o[2 * j];
           const float* y = o[2 * j + 1];
           const float v0 = second ? x[2] : (TWO_ROWS ? x[0] : x[0] + x[2]);
-          const float v1 = second ? x[3] : (TWO_ROWS ? x[1] : x[1] + x[3]);
-          const float v2 = second ? y[2] : (TWO_ROWS ? y[0] : y[0] + y[2]);
+          const float v1 = second ? y[2] : (TWO_ROWS ? y[0] : y[0] + y[2]);
+          const float v2 = second ? x[3] : (TWO_ROWS ? x[1] : x[1] + x[3]);
           const float v3 = second ? y[3] : (TWO_ROWS ? y[1] : y[1] + y[3]);
           float* d4 = dst + 16 * j + 4 * (lane & 3);
           if (keep_in_l2)
