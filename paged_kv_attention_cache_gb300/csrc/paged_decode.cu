@@ -499,6 +499,12 @@ __device__ __forceinline__ void e4m3x4_as_f16x2x2(uint32_t w, uint32_t& lo, uint
 }
 
 
+// a compile-time int for generic lambdas
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
+
 struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits;
 };
@@ -553,6 +559,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   // chunks of a stage that share one softmax step: both of an e4m3 stage
   // when the group fits rows 0-7 (registers allow it there), else one
   constexpr int NJ = (KV8 && !TWO_ROWS) ? CPS : 1;
+  static_assert(NJ == 1 || NJ == 2, "a stage holds one or two chunks");
   const int nbox = kChunk / box_rows;             // boxes per row half of a chunk
   const int per_kind = CPS * L::kHalves * nbox;   // boxes of K (or V) per stage
   const int nreq = 2 * per_kind;                  // TMA requests per stage
@@ -771,8 +778,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       const int nlive = min(CPS, it.c_end - c0);  // the stage's chunks inside the item
 #pragma unroll 1
     for (int sub0 = 0; sub0 < nlive; sub0 += NJ) {
-      // chunks sub0 .. sub0+nj-1 of the stage share one softmax step
-      const int nj = min(NJ, nlive - sub0);
+      // chunks sub0 .. sub0+nj-1 of the stage share one softmax step; nj is a
+      // compile-time count, so a full stage runs as straight-line code
+      auto step = [&](auto nj_c) {
+      constexpr int nj = decltype(nj_c)::value;
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
         if (j >= nj) break;
@@ -844,7 +853,21 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) s[j][n][e] += s2[n][e];
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      // scores in log2 units; keys outside the stage's live set (or, with
+      // several query tokens, outside a row's own range) score -inf.  A stage
+      // whose keys are all live skips the per-key tests.
+      constexpr uint32_t all_keys = nj == 1 ? 0xffffu : 0xffffffffu;
+      if (P.q_len == 1 && ((smask >> (16 * sub0)) & all_keys) == all_keys) {
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              s[j][n][e] = j < nj ? s[j][n][e] * P.scale_log2 : -INFINITY;
+              s[j][n][2 + e] = j < nj ? s[j][n][2 + e] * P.scale_log2 : -INFINITY;
+            }
+      } else {
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
 #pragma unroll
@@ -861,59 +884,108 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           }
           s[j][n][e] = ok0 ? s[j][n][e] * P.scale_log2 : -INFINITY;
           s[j][n][2 + e] = ok1 ? s[j][n][2 + e] * P.scale_log2 : -INFINITY;
-          mx0 = fmaxf(mx0, s[j][n][e]);
-          mx1 = fmaxf(mx1, s[j][n][2 + e]);
         }
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      // lazy running max: the base moves only when the step's max passes it
-      // by more than 2^8 (P stays below 256), so O is rescaled rarely
-      const float mn0 = (m0 == -INFINITY || mx0 > m0 + kLazyLog2) ? fmaxf(m0, mx0) : m0;
-      const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
-      const float c0 = fast_exp2(m0 - base0);
-      m0 = mn0;
+      }
+      // Lazy running max: the base moves only when a score passes it by more
+      // than 2^8 (P stays below 256), so O is rescaled rarely.  When no score
+      // of the warp passes its row's base (one vote), P is taken against the
+      // base as it stands; otherwise the rows' maxima are reduced, the bases
+      // moved and O rescaled.  Both give the same bits where the base stays.
+      bool over = m0 == -INFINITY || (TWO_ROWS && m1 == -INFINITY);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            over |= s[j][n][e] > m0 + kLazyLog2;
+            if (TWO_ROWS) over |= s[j][n][2 + e] > m1 + kLazyLog2;
+          }
       float p[NJ][2][4];
-      float sum0 = 0.f;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          p[j][n][0] = fast_exp2(s[j][n][0] - base0);
-          p[j][n][1] = fast_exp2(s[j][n][1] - base0);
-        }
-        sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
-      }
-      l0 = l0 * c0 + sum0;
-      float c1 = c0;
-      if (TWO_ROWS) {
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn1 = (m1 == -INFINITY || mx1 > m1 + kLazyLog2) ? fmaxf(m1, mx1) : m1;
-        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        c1 = fast_exp2(m1 - base1);
-        m1 = mn1;
-        float sum1 = 0.f;
+      if (!__any_sync(0xffffffffu, over)) {
+        float sum0 = 0.f;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
-            p[j][n][2] = fast_exp2(s[j][n][2] - base1);
-            p[j][n][3] = fast_exp2(s[j][n][3] - base1);
+            p[j][n][0] = fast_exp2(s[j][n][0] - m0);
+            p[j][n][1] = fast_exp2(s[j][n][1] - m0);
           }
-          sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
+          sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
         }
-        l1 = l1 * c1 + sum1;
-      }
-      // rows 8-15 hold either the second half of the group (TWO_ROWS) or the
-      // low bf16 part of rows 0-7's probabilities; both rescale with their row
-      if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
+        l0 = l0 + sum0;
+        if (TWO_ROWS) {
+          float sum1 = 0.f;
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          o[n][0] *= c0;
-          o[n][1] *= c0;
-          o[n][2] *= c1;
-          o[n][3] *= c1;
+          for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+              p[j][n][2] = fast_exp2(s[j][n][2] - m1);
+              p[j][n][3] = fast_exp2(s[j][n][3] - m1);
+            }
+            sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
+          }
+          l1 = l1 + sum1;
+        }
+      } else {
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              mx0 = fmaxf(mx0, s[j][n][e]);
+              mx1 = fmaxf(mx1, s[j][n][2 + e]);
+            }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        const float mn0 = (m0 == -INFINITY || mx0 > m0 + kLazyLog2) ? fmaxf(m0, mx0) : m0;
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
+        const float c0 = fast_exp2(m0 - base0);
+        m0 = mn0;
+        float sum0 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            p[j][n][0] = fast_exp2(s[j][n][0] - base0);
+            p[j][n][1] = fast_exp2(s[j][n][1] - base0);
+          }
+          sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
+        }
+        l0 = l0 * c0 + sum0;
+        float c1 = c0;
+        if (TWO_ROWS) {
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+          const float mn1 = (m1 == -INFINITY || mx1 > m1 + kLazyLog2) ? fmaxf(m1, mx1) : m1;
+          const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+          c1 = fast_exp2(m1 - base1);
+          m1 = mn1;
+          float sum1 = 0.f;
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+              p[j][n][2] = fast_exp2(s[j][n][2] - base1);
+              p[j][n][3] = fast_exp2(s[j][n][3] - base1);
+            }
+            sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
+          }
+          l1 = l1 * c1 + sum1;
+        }
+        // rows 8-15 hold either the second half of the group (TWO_ROWS) or
+        // the low part of rows 0-7's probabilities; both rescale with their row
+        if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            o[n][0] *= c0;
+            o[n][1] *= c0;
+            o[n][2] *= c1;
+            o[n][3] *= c1;
+          }
         }
       }
 #pragma unroll
@@ -999,6 +1071,13 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         }
       }
       __syncwarp();
+      };
+      if constexpr (NJ == 1)
+        step(IntC<1>());
+      else if (nlive - sub0 >= NJ)
+        step(IntC<NJ>());
+      else
+        step(IntC<1>());
     }
     }
     if (stop) break;
