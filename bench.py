@@ -39,7 +39,7 @@ WORKLOAD = "Llama-3-8B-shaped decode layer: B=64, Hq=32, Hkv=8, d=128, bf16, pag
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
 # these default workloads (the summaries under profiles/ give the command); they hold
 # only for the kernels as they were captured and for these workloads.
-DECODE_TRAFFIC = (1264517120 + 4213504, "profiles/decode_bf16_llama8b_b64.md")
+DECODE_TRAFFIC = (1264400896 + 4529408, "profiles/decode_bf16_llama8b_b64.md")
 PREFILL_TRAFFIC = (334014976 + 207454976, "profiles/prefill_tc_batched_b8.md")
 
 
