@@ -61,7 +61,7 @@ extern "C" {
 typedef enum {
   TL_OK = 0,
   TL_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, misalignment */
-  TL_ERR_UNSUPPORTED = 2, /* valid, but not a shape or dtype this build runs */
+  TL_ERR_UNSUPPORTED = 2, /* valid, but not a shape or dtype the library runs */
   TL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
   TL_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
 } tl_status;

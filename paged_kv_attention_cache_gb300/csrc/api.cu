@@ -81,7 +81,7 @@ extern "C" const char* tl_status_string(tl_status status) {
   switch (status) {
     case TL_OK: return "TL_OK";
     case TL_ERR_INVALID_ARG: return "TL_ERR_INVALID_ARG: a null pointer, bad size or misaligned pointer";
-    case TL_ERR_UNSUPPORTED: return "TL_ERR_UNSUPPORTED: valid arguments, but not a shape or dtype this build runs";
+    case TL_ERR_UNSUPPORTED: return "TL_ERR_UNSUPPORTED: valid arguments, but not a shape or dtype the library runs";
     case TL_ERR_CUDA: return "TL_ERR_CUDA: a CUDA call or kernel launch failed";
     case TL_ERR_WORKSPACE: return "TL_ERR_WORKSPACE: workspace missing or too small";
   }
