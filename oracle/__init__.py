@@ -18,10 +18,18 @@ pages defines it, is stated in ``oracle.c``:
 * ``paged_prefill(blockwise=True)`` -- same page, section 2 "Blockwise
   attention" (online softmax folded over 2,048-key blocks);
 * ``kv_bytes_per_token`` -- "Serving Models", "Count KV heads and distinct
-  stored tensors" (M = 2 L H_kv d q).
+  stored tensors" (M = 2 L H_kv d q);
+* ``kv_cache_write_fp8`` / ``fp8_value`` / ``fp8_code`` -- "How serving works
+  in Tlaloc", the FP8 KV cache paragraph (e4m3fn codes, clamp to +-448, ties
+  to even);
+* ``kv_cache_write_int8`` / ``paged_decode_int8`` -- same page: int8 KV pools
+  are named as a next step without a format, read here from its "Int8 weights
+  (opt-in)" paragraph (one f32 scale per row, max |x| / 127, codes rounded
+  half to even; a value is code x scale).
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against facts the
-pages or the mathematics fix; none is "parity unpinned".
+Every function here is pinned by ``tests/test_oracle_pins.py`` (int8:
+``tests/test_oracle_int8.py``) against facts the pages or the mathematics fix;
+none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -80,6 +88,13 @@ def _load():
             lib.oracle_kv_cache_write_fp8.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i64, i64,
                                                       i64]
             lib.oracle_kv_cache_write_fp8.restype = ctypes.c_int
+            lib.oracle_kv_cache_write_int8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i64, i64,
+                                                       i64, i64, i64, vp]
+            lib.oracle_kv_cache_write_int8.restype = ctypes.c_int
+            lib.oracle_paged_decode_int8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                                     i32, i32, i32, i32, i32, i32, f64, vp, i32,
+                                                     vp, i32]
+            lib.oracle_paged_decode_int8.restype = ctypes.c_int
             lib.oracle_ring_pages.restype = i64
             lib.oracle_kv_bytes_per_token.argtypes = [i64, i64, i64, i64]
             lib.oracle_kv_bytes_per_token.restype = i64
@@ -185,6 +200,60 @@ def kv_cache_write_fp8(k_new, v_new, k_cache, v_cache, slot_mapping) -> None:
                                        _ptr(sm), sm.shape[0], P, ps, hkv, d)
     if rc != 0:
         raise OracleError(f"oracle_kv_cache_write_fp8 failed ({rc})")
+
+
+def kv_cache_write_int8(k_new, v_new, k_codes, v_codes, k_scales, v_scales,
+                        slot_mapping) -> int:
+    """In place: the int8 codes and per-(token, KV head) scales of new[t] into
+    the int8 pools (codes int8 [P, ps, H_kv, d], scales float32 [P, H_kv, ps])
+    at slot[t], for every t with slot[t] != -1.  Returns the number of
+    non-finite new values (written as code 0)."""
+    lib = _load()
+    kn, vn = _c(_np(k_new)), _c(_np(v_new))
+    kc, vc, ks, vs = _np(k_codes), _np(v_codes), _np(k_scales), _np(v_scales)
+    if kc.dtype != np.int8 or vc.dtype != np.int8 or ks.dtype != np.float32 or \
+            vs.dtype != np.float32:
+        raise OracleError("int8 pools: int8 codes and float32 scales")
+    if not all(a.flags.c_contiguous for a in (kc, vc, ks, vs)):
+        raise OracleError("pools must be contiguous (written in place)")
+    sm = _c(_np(slot_mapping), np.int64)
+    P, ps, hkv, d = kc.shape
+    if kn.shape != (sm.shape[0], hkv, d) or vn.shape != kn.shape or vc.shape != kc.shape or \
+            ks.shape != (P, hkv, ps) or vs.shape != ks.shape:
+        raise OracleError("shape mismatch")
+    bad = np.zeros(1, dtype=np.int64)
+    rc = lib.oracle_kv_cache_write_int8(_ptr(kn), _ptr(vn), _dtype_code(kn), _ptr(kc), _ptr(vc),
+                                        _ptr(ks), _ptr(vs), _ptr(sm), sm.shape[0], P, ps, hkv, d,
+                                        _ptr(bad))
+    if rc != 0:
+        raise OracleError(f"oracle_kv_cache_write_int8 failed ({rc})")
+    return int(bad[0])
+
+
+def paged_decode_int8(q, k_codes, v_codes, k_scales, v_scales, block_table, context_lens, scale,
+                      window=0, seqs=None, threads=0, ring_pages=0) -> np.ndarray:
+    """paged_decode over int8 pools: each element read as code x its row's scale."""
+    lib = _load()
+    qa = _c(_np(q))
+    kc, vc = _c(_np(k_codes)), _c(_np(v_codes))
+    ks, vs = _c(_np(k_scales)), _c(_np(v_scales))
+    bt = _c(_np(block_table), np.int32)
+    cl = _c(_np(context_lens), np.int32)
+    B, hq, d = qa.shape
+    P, ps, hkv, d2 = kc.shape
+    if _dtype_code(qa) != BF16 or kc.dtype != np.int8 or vc.shape != kc.shape or d2 != d or \
+            ks.dtype != np.float32 or ks.shape != (P, hkv, ps) or vs.shape != ks.shape or \
+            bt.shape[0] != B:
+        raise OracleError("shape / dtype mismatch")
+    sq = _c(np.arange(B) if seqs is None else np.asarray(seqs), np.int32)
+    out = np.zeros((sq.shape[0], hq, d), dtype=np.float64)
+    rc = lib.oracle_paged_decode_int8(_ptr(qa), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
+                                      bt.shape[1], _ptr(cl), B, hq, hkv, d, P, ps, int(window),
+                                      int(ring_pages), float(scale), _ptr(sq), sq.shape[0],
+                                      _ptr(out), int(threads))
+    if rc != 0:
+        raise OracleError(f"oracle_paged_decode_int8 failed ({rc})")
+    return out
 
 
 def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale, window=0, seqs=None,

@@ -36,7 +36,14 @@
  *     write clamps each value to +-448 (the largest finite code) and rounds
  *     it to the nearest code, ties to an even mantissa (the rounding the same
  *     section states for e4m3 weight codes); attention reads the codes'
- *     exact values.
+ *     exact values;
+ *   - int8 KV pools (same page: "What would make it faster" lists int8 KV
+ *     pools as a next step without a format; the format is read from its
+ *     "Int8 weights (opt-in)" paragraph, one f32 scale per output channel,
+ *     max |W| / 127, codes rounded half to even): each (token, KV head) row
+ *     of d values gets one scale s = max |x| / 127 and each value the code
+ *     round-half-even(x / s), both computed in binary32; attention reads code
+ *     x s exactly.
  *
  * Everything is the plain definition written out: widen each stored value
  * exactly to double, accumulate in double, in index order, one output at a
@@ -58,7 +65,7 @@
 #include <omp.h>
 #endif
 
-enum { OR_F32 = 0, OR_BF16 = 1, OR_FP8 = 2 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_FP8 = 2, OR_INT8 = 3 };
 enum { OR_OK = 0, OR_BAD_ARG = 1, OR_BAD_PAGE = 2, OR_NO_MEM = 3 };
 
 /* Value of one e4m3fn code: (-1)^s 2^(e-7) (1 + m/8) for e > 0,
@@ -111,16 +118,21 @@ static uint8_t fp8_code(double x) {
 static double widen(const void* base, int64_t idx, int dtype) {
   if (dtype == OR_F32) return (double)((const float*)base)[idx];
   if (dtype == OR_FP8) return fp8_value(((const uint8_t*)base)[idx]);
+  if (dtype == OR_INT8) return (double)((const int8_t*)base)[idx]; /* the code; x scale apart */
   uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
   return (double)f;
 }
 
-static int64_t elem_size(int dtype) { return dtype == OR_F32 ? 4 : dtype == OR_FP8 ? 1 : 2; }
+static int64_t elem_size(int dtype) {
+  return dtype == OR_F32 ? 4 : (dtype == OR_FP8 || dtype == OR_INT8) ? 1 : 2;
+}
 
-/* The query of an fp8 cache is bf16. */
-static int query_dtype(int kv_dtype) { return kv_dtype == OR_FP8 ? OR_BF16 : kv_dtype; }
+/* The query of an fp8 or int8 cache is bf16. */
+static int query_dtype(int kv_dtype) {
+  return (kv_dtype == OR_FP8 || kv_dtype == OR_INT8) ? OR_BF16 : kv_dtype;
+}
 
 double oracle_fp8_value(int32_t code) { return fp8_value((uint8_t)code); }
 int32_t oracle_fp8_code(double x) { return fp8_code(x); }
@@ -170,6 +182,66 @@ int oracle_kv_cache_write_fp8(const void* k_new, const void* v_new, int32_t src_
   return OR_OK;
 }
 
+/* The write into an int8 pool: each (token, KV head) row of d new values (f32
+ * or bf16, widened exactly to binary32) gets the scale s = m / 127 with m the
+ * largest magnitude of its finite values, and each finite value x the code
+ * round-half-even(x / s), clamped to +-127; s and x / s are binary32 divisions.
+ * A row with s = 0 (all zeros, or m so small that m / 127 underflows) writes
+ * codes 0 and scale 0.  A non-finite value writes code 0 and is counted in
+ * *n_bad.  Codes sit at the pool layout [num_pages][page_size][H_kv][d], the
+ * scales at [num_pages][H_kv][page_size] (a page's scales of one head are
+ * contiguous).  Slot -1 writes nothing. */
+static void quantize_row_int8(const void* src, int64_t idx0, int src_dtype, int64_t d,
+                              int8_t* codes, float* scale, int64_t* n_bad) {
+  float m = 0.0f;
+  for (int64_t e = 0; e < d; ++e) {
+    const float x = (float)widen(src, idx0 + e, src_dtype);
+    if (!isfinite(x)) {
+      ++*n_bad;
+      continue;
+    }
+    if (fabsf(x) > m) m = fabsf(x);
+  }
+  const float sc = m / 127.0f;
+  for (int64_t e = 0; e < d; ++e) {
+    const float x = (float)widen(src, idx0 + e, src_dtype);
+    float r = 0.0f;
+    if (isfinite(x) && sc > 0.0f) {
+      r = rintf(x / sc); /* the default rounding mode: to nearest, ties to even */
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+    }
+    codes[e] = (int8_t)r;
+  }
+  *scale = sc;
+}
+
+int oracle_kv_cache_write_int8(const void* k_new, const void* v_new, int32_t src_dtype,
+                               int8_t* k_codes, int8_t* v_codes, float* k_scales,
+                               float* v_scales, const int64_t* slot_mapping, int64_t n_tokens,
+                               int64_t num_pages, int64_t page_size, int64_t h_kv, int64_t d,
+                               int64_t* n_bad) {
+  if (n_tokens < 0 || num_pages <= 0 || page_size <= 0 || h_kv <= 0 || d <= 0 ||
+      (src_dtype != OR_F32 && src_dtype != OR_BF16))
+    return OR_BAD_ARG;
+  *n_bad = 0;
+  const int64_t row = h_kv * d; /* elements of one token (all KV heads) */
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_pages * page_size) return OR_BAD_PAGE;
+    const int64_t page = slot / page_size, offset = slot % page_size;
+    for (int64_t g = 0; g < h_kv; ++g) {
+      const int64_t si = (page * h_kv + g) * page_size + offset;
+      quantize_row_int8(k_new, t * row + g * d, src_dtype, d, k_codes + slot * row + g * d,
+                        k_scales + si, n_bad);
+      quantize_row_int8(v_new, t * row + g * d, src_dtype, d, v_codes + slot * row + g * d,
+                        v_scales + si, n_bad);
+    }
+  }
+  return OR_OK;
+}
+
 /* ------------------------------------------------------------ attention -- */
 
 typedef struct {
@@ -179,33 +251,48 @@ typedef struct {
   const int32_t* bt_row; /* this sequence's block table row */
   int32_t max_pages_per_seq;
   int32_t num_pages, page_size, h_kv, d;
+  const float* k_scales; /* int8 pools: [num_pages][H_kv][page_size] */
+  const float* v_scales;
 } paged_seq;
 
-/* Element e of the K (or V) row of logical position j, KV head g. */
-static int kv_index(const paged_seq* s, int64_t j, int64_t g, int64_t* row_base) {
+/* Element e of the K (or V) row of logical position j, KV head g; *scale_idx
+ * is the row's entry in an int8 pool's scales. */
+static int kv_index(const paged_seq* s, int64_t j, int64_t g, int64_t* row_base,
+                    int64_t* scale_idx) {
   const int64_t logical_block = j / s->page_size;
   if (logical_block >= s->max_pages_per_seq) return OR_BAD_PAGE;
   const int64_t page = s->bt_row[logical_block];
   if (page < 0 || page >= s->num_pages) return OR_BAD_PAGE;
   const int64_t offset = j % s->page_size;
   *row_base = ((page * s->page_size + offset) * s->h_kv + g) * s->d;
+  *scale_idx = (page * s->h_kv + g) * s->page_size + offset;
   return OR_OK;
+}
+
+/* Stored element e of a row, exactly: the widened value, or for an int8 pool
+ * code x scale (8 + 24 significant bits: exact in double). */
+static double kv_value(const paged_seq* s, const void* pool, const float* scales,
+                       int64_t base, int64_t e, int64_t scale_idx) {
+  const double x = widen(pool, base + e, s->dtype);
+  return s->dtype == OR_INT8 ? x * (double)scales[scale_idx] : x;
 }
 
 static double score(const paged_seq* s, const double* q, int64_t j, int64_t g,
                     double scale, int* err) {
-  int64_t base;
-  if (kv_index(s, j, g, &base) != OR_OK) { *err = OR_BAD_PAGE; return 0.0; }
+  int64_t base, si;
+  if (kv_index(s, j, g, &base, &si) != OR_OK) { *err = OR_BAD_PAGE; return 0.0; }
   double dot = 0.0;
-  for (int64_t e = 0; e < s->d; ++e) dot += q[e] * widen(s->k_cache, base + e, s->dtype);
+  for (int64_t e = 0; e < s->d; ++e)
+    dot += q[e] * kv_value(s, s->k_cache, s->k_scales, base, e, si);
   return scale * dot;
 }
 
 static void add_weighted_value(const paged_seq* s, int64_t j, int64_t g, double w,
                                double* acc, int* err) {
-  int64_t base;
-  if (kv_index(s, j, g, &base) != OR_OK) { *err = OR_BAD_PAGE; return; }
-  for (int64_t e = 0; e < s->d; ++e) acc[e] += w * widen(s->v_cache, base + e, s->dtype);
+  int64_t base, si;
+  if (kv_index(s, j, g, &base, &si) != OR_OK) { *err = OR_BAD_PAGE; return; }
+  for (int64_t e = 0; e < s->d; ++e)
+    acc[e] += w * kv_value(s, s->v_cache, s->v_scales, base, e, si);
 }
 
 /* One-pass form: scores of keys lo..p, softmax, weighted sum of values. */
@@ -341,16 +428,17 @@ int oracle_max_threads(void) {
  * ring_pages > 0: the table's first ring_pages entries are the sequence's
  * ring (attend_ring); 0: full history.
  * Computes the sequences listed in seqs[0..n_seqs) into out[n_seqs][H_q][d]. */
-int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
-                        int32_t dtype, const int32_t* block_table,
-                        int32_t max_pages_per_seq, const int32_t* context_lens,
-                        int32_t B, int32_t h_q, int32_t h_kv, int32_t d,
-                        int32_t num_pages, int32_t page_size, int32_t window,
-                        int32_t ring_pages, double scale, const int32_t* seqs, int32_t n_seqs,
-                        double* out, int32_t n_threads) {
+static int decode_common(const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scales, const float* v_scales, int32_t dtype,
+                         const int32_t* block_table, int32_t max_pages_per_seq,
+                         const int32_t* context_lens, int32_t B, int32_t h_q, int32_t h_kv,
+                         int32_t d, int32_t num_pages, int32_t page_size, int32_t window,
+                         int32_t ring_pages, double scale, const int32_t* seqs,
+                         int32_t n_seqs, double* out, int32_t n_threads) {
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 || page_size <= 0 ||
       num_pages <= 0 || max_pages_per_seq <= 0 ||
-      (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_FP8) || ring_pages < 0 ||
+      (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_FP8 && dtype != OR_INT8) ||
+      (dtype == OR_INT8 && (!k_scales || !v_scales)) || ring_pages < 0 ||
       ring_pages > max_pages_per_seq)
     return OR_BAD_ARG;
   for (int32_t i = 0; i < n_seqs; ++i)
@@ -362,7 +450,7 @@ int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
   for (int64_t item = 0; item < (int64_t)n_seqs * h_q; ++item) {
     const int64_t b = seqs[item / h_q], h = item % h_q, g = h / group;
     paged_seq s = {k_cache, v_cache, dtype, block_table + b * max_pages_per_seq,
-                   max_pages_per_seq, num_pages, page_size, h_kv, d};
+                   max_pages_per_seq, num_pages, page_size, h_kv, d, k_scales, v_scales};
     double* qv = (double*)malloc((size_t)d * sizeof(double));
     double* o = out + item * d;
     if (!qv) { status = OR_NO_MEM; continue; }
@@ -376,6 +464,33 @@ int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
     free(qv);
   }
   return status;
+}
+
+int oracle_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                        int32_t dtype, const int32_t* block_table,
+                        int32_t max_pages_per_seq, const int32_t* context_lens,
+                        int32_t B, int32_t h_q, int32_t h_kv, int32_t d,
+                        int32_t num_pages, int32_t page_size, int32_t window,
+                        int32_t ring_pages, double scale, const int32_t* seqs, int32_t n_seqs,
+                        double* out, int32_t n_threads) {
+  if (dtype == OR_INT8) return OR_BAD_ARG; /* int8 pools come with their scales */
+  return decode_common(q, k_cache, v_cache, NULL, NULL, dtype, block_table, max_pages_per_seq,
+                       context_lens, B, h_q, h_kv, d, num_pages, page_size, window, ring_pages,
+                       scale, seqs, n_seqs, out, n_threads);
+}
+
+/* Decode over int8 pools: codes k_codes / v_codes at the pool layout, scales
+ * [num_pages][H_kv][page_size]; each element read as code x scale. */
+int oracle_paged_decode_int8(const void* q, const int8_t* k_codes, const int8_t* v_codes,
+                             const float* k_scales, const float* v_scales,
+                             const int32_t* block_table, int32_t max_pages_per_seq,
+                             const int32_t* context_lens, int32_t B, int32_t h_q, int32_t h_kv,
+                             int32_t d, int32_t num_pages, int32_t page_size, int32_t window,
+                             int32_t ring_pages, double scale, const int32_t* seqs,
+                             int32_t n_seqs, double* out, int32_t n_threads) {
+  return decode_common(q, k_codes, v_codes, k_scales, v_scales, OR_INT8, block_table,
+                       max_pages_per_seq, context_lens, B, h_q, h_kv, d, num_pages, page_size,
+                       window, ring_pages, scale, seqs, n_seqs, out, n_threads);
 }
 
 /* Prefill: q[B][T][H_q][d], positions[B][T] (-1 = padding).  Token (b,t) has
@@ -422,7 +537,7 @@ int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache
     const int64_t bt_idx = tokens[item / h_q], h = item % h_q, g = h / group;
     const int64_t b = bt_idx / T;
     paged_seq s = {k_cache, v_cache, dtype, block_table + b * max_pages_per_seq,
-                   max_pages_per_seq, num_pages, page_size, h_kv, d};
+                   max_pages_per_seq, num_pages, page_size, h_kv, d, NULL, NULL};
     double* qv = (double*)malloc((size_t)d * sizeof(double));
     double* o = out + item * d;
     if (!qv) { status = OR_NO_MEM; continue; }
