@@ -333,6 +333,9 @@ def run_ours(args):
     fp8_line = None
     if args.only in ("all", "fp8"):
         fp8_line = run_fp8(args, dev, stream, hbm)
+    int8_line = None
+    if args.only in ("all", "int8"):
+        int8_line = run_int8(args, dev, stream, hbm)
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -372,6 +375,7 @@ def run_ours(args):
         "ring_decode": ring_line,
         "verify_decode": verify_line,
         "fp8_decode": fp8_line,
+        "int8_decode": int8_line,
         "e2e": e2e,
         "separate_step": {"calls": "tl_kv_cache_write, then tl_paged_attn_decode (four kernels)",
                           "ms_per_step": round(sep_ms, 5),
@@ -426,6 +430,57 @@ def run_ring(args, dev, stream, hbm):
             "kv_bytes_per_call": kvb, "ms_per_call": round(ms, 4),
             "gbs": round(alg / (ms * 1e-3) / 1e9, 1), "frac": round(alg / (ms * 1e-3) / 1e9 / hbm, 4),
             "l2": "ring pool %.2f GB vs 129 MB L2" % (g.k_cache.numel() * 4 / 1e9)}
+
+
+def run_int8(args, dev, stream, hbm):
+    """Decode of the Llama-3-8B-shaped batch (B=64) over int8 pools (codes and
+    one f32 scale per slot and KV head): the pools are the bf16 pools written
+    through tl_kv_cache_write_int8 (every slot); the step is the int8 write of
+    the 64 new rows, then tl_paged_attn_decode_int8 (two calls)."""
+    import torch
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
+    case = wl.llama8b_decode(seed=args.seed, device=dev)
+    g = wl.to_device(case, dev)
+    P, ps, hkv, d = g.k_cache.shape
+    B, hq = case.B, case.Hq
+    kc = torch.empty((P, ps, hkv, d), dtype=torch.int8, device=dev)
+    vc = torch.empty_like(kc)
+    ks = torch.empty((P, hkv, ps), dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    every = torch.arange(P * ps, dtype=torch.int64, device=dev)
+    tl.tl_kv_cache_write_int8(g.k_cache.view(-1, hkv, d), g.v_cache.view(-1, hkv, d), kc, vc, ks,
+                              vs, every)
+    del g.k_cache, g.v_cache
+    out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+    ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
+    keys = int(case.context_lens.sum().item())
+    kvb = keys * 2 * hkv * (d + 4)  # codes, and one f32 scale per key, K and V
+
+    def step():
+        tl.tl_kv_cache_write_int8(g.k_new, g.v_new, kc, vc, ks, vs, g.slot_mapping)
+        tl.tl_paged_attn_decode_int8(g.q, kc, vc, ks, vs, g.block_table, g.context_lens,
+                                     case.scale, out=out, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = 100
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"workload": "Llama-3-8B-shaped decode layer over int8 pools: B=64, Hq=32, Hkv=8, "
+                        "d=128, page 16, L~U[512,8192] (int8 write of 64 rows, then decode)",
+            "kv_bytes_per_step": kvb, "ms_per_step": round(ms, 4),
+            "kv_gbs": round(kvb / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4),
+            "tokens_per_s": round(B / (ms * 1e-3), 1)}
 
 
 def run_fp8(args, dev, stream, hbm):
@@ -707,7 +762,7 @@ def main():
     ap.add_argument("--soak-seconds", type=float, default=2.0)
     ap.add_argument("--batch", type=int, default=64, help="decode batch (64 = the workload)")
     ap.add_argument("--only", choices=["all", "decode", "decode-e2e", "prefill", "ring",
-                                       "verify", "fp8"], default="all")
+                                       "verify", "fp8", "int8"], default="all")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

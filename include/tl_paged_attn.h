@@ -78,8 +78,9 @@ typedef enum {
 #define TL_DEVERR_CONTEXT_RANGE 4u /* a length / position past max_pages_per_seq*page_size */
 #define TL_DEVERR_TIMEOUT 8u       /* an internal pipeline wait gave up (outputs invalid) */
 #define TL_DEVERR_VALUE_RANGE 16u  /* a finite value beyond fp16's +-65504 where the path rounds to
-                                      fp16: V in prefill, q in decode over e4m3 pools (outputs
-                                      invalid) */
+                                      fp16: V in prefill, q in decode over e4m3 or int8 pools
+                                      (outputs invalid); or a non-finite value written into an
+                                      int8 pool (written as code 0) */
 
 /* Name of a status, for messages (never NULL). */
 const char* tl_status_string(tl_status status);
@@ -120,6 +121,34 @@ tl_status tl_kv_cache_write_fp8(const void* k_new, const void* v_new, tl_dtype s
                                 void* k_cache, void* v_cache, const int64_t* slot_mapping,
                                 int32_t n_tokens, int32_t num_pages, int32_t page_size,
                                 int32_t h_kv, int32_t d, uint32_t* error_word, void* stream);
+
+/*
+ * KV_CACHE_WRITE into int8 pools.  "How serving works in Tlaloc" names int8
+ * KV pools as a next step ("What would make it faster") without a format;
+ * the format is read from the same page's "Int8 weights (opt-in)" paragraph
+ * (one f32 scale per output channel, max |W| / 127, codes rounded half to
+ * even), with a (token, KV head) row of d values as the channel.  For every
+ * token t with slot_mapping[t] != -1 and every KV head g, the row x =
+ * new[t][g][0..d) (src_dtype TL_F32 or TL_BF16, widened exactly) gets
+ *     s = m / 127   (m the largest magnitude of the row's finite values)
+ *     code_e = round-half-even(x_e / s), clamped to +-127
+ * with both divisions in binary32.  A row whose s is 0 writes codes 0 and
+ * scale 0; a non-finite value writes code 0 and sets TL_DEVERR_VALUE_RANGE.
+ * Slot -1 writes nothing; no other byte of the pools changes.
+ *   k_new, v_new       [n_tokens][h_kv][d] in src_dtype, 16-byte aligned
+ *   k_codes, v_codes   [num_pages][page_size][h_kv][d] int8, in place
+ *   k_scales, v_scales [num_pages][h_kv][page_size] float32, in place (the
+ *                      scales of one page and head are contiguous)
+ *   slot_mapping       [n_tokens] int64
+ * Returns TL_ERR_INVALID_ARG for null pointers (n_tokens > 0), non-positive
+ * sizes or misaligned pointers; TL_ERR_UNSUPPORTED for d > 1024 or another
+ * src_dtype.
+ */
+tl_status tl_kv_cache_write_int8(const void* k_new, const void* v_new, tl_dtype src_dtype,
+                                 int8_t* k_codes, int8_t* v_codes, float* k_scales,
+                                 float* v_scales, const int64_t* slot_mapping, int32_t n_tokens,
+                                 int32_t num_pages, int32_t page_size, int32_t h_kv, int32_t d,
+                                 uint32_t* error_word, void* stream);
 
 /*
  * Bytes of workspace tl_paged_attn_decode needs for these sizes (an upper
@@ -170,6 +199,31 @@ tl_status tl_paged_attn_decode(const void* q, const void* k_cache, const void* v
                                int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size,
                                int32_t window, float scale, tl_dtype dtype, void* workspace,
                                size_t workspace_bytes, uint32_t* error_word, void* stream);
+
+/*
+ * PAGED_ATTENTION decode over int8 pools (written by tl_kv_cache_write_int8):
+ * tl_paged_attn_decode with every K/V element read as code x its row's
+ * scale.  The scores are s_j = scale * k_scale(j) * <q, codes of K_g(j)>
+ * (the codes widen exactly to fp16, q is rounded to fp16: a finite |q|
+ * beyond 65504 sets TL_DEVERR_VALUE_RANGE), and each probability is
+ * multiplied by its key's v_scale before the P.V product.
+ *   q                  [B][h_q][d] bf16
+ *   k_codes, v_codes, k_scales, v_scales  as tl_kv_cache_write_int8 writes
+ *                      them (read only; the scales 16-byte aligned)
+ *   the other arguments, the workspace (tl_paged_attn_decode_workspace_size)
+ *   and the errors as tl_paged_attn_decode.
+ * Supported: d = 128, h_q % h_kv == 0 with h_q/h_kv <= 16, page_size a
+ * multiple of 16 in [16, 256] (a chunk of 16 keys' scales of one head is one
+ * 64-byte copy), num_pages*page_size < 2^31.  Otherwise TL_ERR_UNSUPPORTED.
+ */
+tl_status tl_paged_attn_decode_int8(const void* q, const int8_t* k_codes, const int8_t* v_codes,
+                                    const float* k_scales, const float* v_scales,
+                                    const int32_t* block_table, int32_t max_pages_per_seq,
+                                    const int32_t* context_lens, float* out, int32_t B,
+                                    int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                    int32_t page_size, int32_t window, float scale,
+                                    void* workspace, size_t workspace_bytes,
+                                    uint32_t* error_word, void* stream);
 
 /*
  * KV_CACHE_WRITE then PAGED_ATTENTION decode in one call ("How serving works

@@ -101,6 +101,65 @@ def tl_kv_cache_write_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: tor
     _check(st, "tl_kv_cache_write_fp8")
 
 
+def _need_int8_pools(k_codes, v_codes, k_scales, v_scales):
+    _need(k_codes, "k_codes", torch.int8)
+    _need(v_codes, "v_codes", torch.int8)
+    _need(k_scales, "k_scales", torch.float32)
+    _need(v_scales, "v_scales", torch.float32)
+    P, ps, hkv, d = k_codes.shape
+    if v_codes.shape != k_codes.shape or tuple(k_scales.shape) != (P, hkv, ps) or \
+            v_scales.shape != k_scales.shape:
+        raise ValueError("int8 pools: codes [num_pages, page_size, H_kv, d], "
+                         "scales [num_pages, H_kv, page_size]")
+    return P, ps, hkv, d
+
+
+def tl_kv_cache_write_int8(k_new: torch.Tensor, v_new: torch.Tensor, k_codes: torch.Tensor,
+                           v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                           slot_mapping: torch.Tensor, error_word: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """In place: for every t with slot != -1 and every KV head, the row of
+    new[t] (f32 or bf16 [N, H_kv, d]) as int8 codes (pool int8 [num_pages,
+    page_size, H_kv, d]) and its scale max |x| / 127 (float32 [num_pages,
+    H_kv, page_size]); codes are x / scale rounded half to even."""
+    _need(k_new, "k_new")
+    _need(v_new, "v_new", k_new.dtype)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    P, ps, hkv, d = _need_int8_pools(k_codes, v_codes, k_scales, v_scales)
+    st = _lib.load().tl_kv_cache_write_int8(
+        _ptr(k_new), _ptr(v_new), _DTYPES.get(k_new.dtype, -1), _ptr(k_codes), _ptr(v_codes),
+        _ptr(k_scales), _ptr(v_scales), _ptr(slot_mapping), slot_mapping.numel(), P, ps, hkv, d,
+        _ptr(error_word), _stream(stream))
+    _check(st, "tl_kv_cache_write_int8")
+
+
+def tl_paged_attn_decode_int8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                              k_scales: torch.Tensor, v_scales: torch.Tensor,
+                              block_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                              window: int = 0, out: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None,
+                              error_word: Optional[torch.Tensor] = None,
+                              stream=None) -> torch.Tensor:
+    """tl_paged_attn_decode over int8 pools (bf16 q): out[B, H_q, d] float32,
+    every K/V element read as code x its row's scale."""
+    _need(q, "q", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    P, ps, hkv, _ = _need_int8_pools(k_codes, v_codes, k_scales, v_scales)
+    B, hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(tl_paged_attn_decode_workspace_size(B, hq, hkv, d), q.device)
+    st = _lib.load().tl_paged_attn_decode_int8(
+        _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+        block_table.shape[1], _ptr(context_lens), _ptr(out), B, hq, hkv, d, P, ps, int(window),
+        float(scale), _ptr(workspace), workspace.numel(), _ptr(error_word), _stream(stream))
+    _check(st, "tl_paged_attn_decode_int8")
+    return out
+
+
 def tl_paged_attn_prefill_workspace_size_ex(B: int, T: int, h_q: int, h_kv: int, d: int,
                                             max_pages_per_seq: int, page_size: int,
                                             ring_pages: int, dtype: int) -> int:

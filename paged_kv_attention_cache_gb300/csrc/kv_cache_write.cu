@@ -50,6 +50,74 @@ __global__ void __launch_bounds__(256) kv_cache_write_fp8_kernel(
   }
 }
 
+// int8 pools: one (token, KV head) row of d new values as int8 codes and its
+// f32 scale, by one warp.  The format is read from the int8 weight
+// quantisation of "How serving works in Tlaloc" ("Int8 weights (opt-in)":
+// one scale per channel, max |x| / 127, codes rounded half to even), with
+// the row as the channel: s = m / 127 over the row's finite values, code =
+// rint(x / s) clamped to +-127, both IEEE binary32 divisions.  A row whose s
+// is 0 gets codes 0; a non-finite value gets code 0 and is reported.
+template <bool SRC_F32>
+__device__ __forceinline__ float new_value(const void* src, int64_t i) {
+  if (SRC_F32) return __ldg(static_cast<const float*>(src) + i);
+  return __uint_as_float((uint32_t)__ldg(static_cast<const unsigned short*>(src) + i) << 16);
+}
+
+template <bool SRC_F32>
+__device__ void quantize_row_int8(const void* src, int64_t base, int d, int8_t* codes,
+                                  float* scale, int lane, uint32_t* error_word) {
+  float m = 0.f;
+  bool bad = false;
+  for (int e = lane; e < d; e += 32) {
+    const float x = new_value<SRC_F32>(src, base + e);
+    if (isfinite(x))
+      m = fmaxf(m, fabsf(x));
+    else
+      bad = true;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float sc = __fdiv_rn(m, 127.f);
+  for (int e = lane; e < d; e += 32) {
+    const float x = new_value<SRC_F32>(src, base + e);
+    float r = 0.f;
+    if (isfinite(x) && sc > 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x, sc)), -127.f), 127.f);
+    codes[e] = (int8_t)__float2int_rn(r);
+  }
+  if (lane == 0) *scale = sc;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) report(error_word, TL_DEVERR_VALUE_RANGE);
+}
+
+// One warp per (token, KV head): its K row and its V row.  Codes at the pool
+// layout [num_pages][page_size][H_kv][d], scales at [num_pages][H_kv][page_size].
+template <bool SRC_F32>
+__global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(
+    const void* __restrict__ k_new, const void* __restrict__ v_new, int8_t* __restrict__ k_codes,
+    int8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales,
+    const int64_t* __restrict__ slot_mapping, int32_t n_tokens, int32_t page_size, int32_t h_kv,
+    int32_t d, int64_t n_slots, uint32_t* error_word) {
+  const int lane = threadIdx.x & 31;
+  const int warps_per_cta = blockDim.x >> 5;
+  const int64_t first = (int64_t)blockIdx.x * warps_per_cta + (threadIdx.x >> 5);
+  const int64_t stride = (int64_t)gridDim.x * warps_per_cta;
+  const int64_t rows = (int64_t)n_tokens * h_kv;
+  for (int64_t r = first; r < rows; r += stride) {
+    const int64_t t = r / h_kv;
+    const int g = (int)(r % h_kv);
+    const int64_t slot = slot_mapping[t];
+    if (slot == -1) continue;  // padding
+    if (slot < 0 || slot >= n_slots) {
+      if (lane == 0 && g == 0) report(error_word, TL_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const int64_t page = slot / page_size, off = slot % page_size;
+    const int64_t src = (t * h_kv + g) * d, dst = (slot * h_kv + g) * d;
+    const int64_t si = (page * h_kv + g) * page_size + off;
+    quantize_row_int8<SRC_F32>(k_new, src, d, k_codes + dst, k_scales + si, lane, error_word);
+    quantize_row_int8<SRC_F32>(v_new, src, d, v_codes + dst, v_scales + si, lane, error_word);
+  }
+}
+
 }  // namespace tl
 
 extern "C" tl_status tl_kv_cache_write_fp8(const void* k_new, const void* v_new,
@@ -110,5 +178,40 @@ extern "C" tl_status tl_kv_cache_write(const void* k_new, const void* v_new, voi
   kv_cache_write_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
       (const int4*)k_new, (const int4*)v_new, (int4*)k_cache, (int4*)v_cache, slot_mapping,
       n_tokens, (int64_t)num_pages * page_size, (int32_t)(row_bytes / 16), error_word);
+  return launch_status();
+}
+
+extern "C" tl_status tl_kv_cache_write_int8(const void* k_new, const void* v_new,
+                                            tl_dtype src_dtype, int8_t* k_codes, int8_t* v_codes,
+                                            float* k_scales, float* v_scales,
+                                            const int64_t* slot_mapping, int32_t n_tokens,
+                                            int32_t num_pages, int32_t page_size, int32_t h_kv,
+                                            int32_t d, uint32_t* error_word, void* stream) {
+  using namespace tl;
+  if (n_tokens < 0 || num_pages <= 0 || page_size <= 0 || h_kv <= 0 || d <= 0)
+    return TL_ERR_INVALID_ARG;
+  if (src_dtype != TL_F32 && src_dtype != TL_BF16) return TL_ERR_UNSUPPORTED;
+  if (d > 1024) return TL_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return TL_OK;
+  if (!k_new || !v_new || !k_codes || !v_codes || !k_scales || !v_scales || !slot_mapping)
+    return TL_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(k_scales) & 3u) ||
+      (reinterpret_cast<uintptr_t>(v_scales) & 3u) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return TL_ERR_INVALID_ARG;
+  const int threads = 256;
+  const int warps = threads / 32;
+  int64_t blocks = ((int64_t)n_tokens * h_kv + warps - 1) / warps;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  const int64_t n_slots = (int64_t)num_pages * page_size;
+  if (src_dtype == TL_F32)
+    kv_cache_write_int8_kernel<true><<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        k_new, v_new, k_codes, v_codes, k_scales, v_scales, slot_mapping, n_tokens, page_size,
+        h_kv, d, n_slots, error_word);
+  else
+    kv_cache_write_int8_kernel<false><<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        k_new, v_new, k_codes, v_codes, k_scales, v_scales, slot_mapping, n_tokens, page_size,
+        h_kv, d, n_slots, error_word);
   return launch_status();
 }

@@ -122,6 +122,9 @@ struct DecodeParams {
   int32_t n_new;
   int32_t new_kind;   // 0 copy (same dtype), 1 e4m3 codes of bf16 rows, 2 of f32 rows
   int32_t row_units;  // 16-byte vectors (copy) or 8-element steps (e4m3) of one row
+  // int8 pools: the per-(slot, KV head) scales, [num_pages][H_kv][page_size]
+  const float* k_scales;
+  const float* v_scales;
 };
 
 // Logical block of key j and its offset in the page (a shift and a mask for
@@ -421,7 +424,7 @@ constexpr int kGrabLead = 4;  // stages left to issue when a warp starts fetchin
 // lands them (16-bit or e4m3 elements, rows split in 128-byte parts; an e4m3
 // stage holds two chunks, the same 8 KiB as one 16-bit chunk, so each stage's
 // issue and wait serve 32 keys) and kRingW Q slots.
-template <int D, bool KV8 = false>
+template <int D, bool KV8 = false, bool I8 = false>
 struct WarpSmem {
   static constexpr int kRing = kRingW;                    // stages (and Q slots) per warp
   static constexpr int kCps = KV8 ? 2 : 1;                 // chunks per stage
@@ -430,11 +433,15 @@ struct WarpSmem {
   static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one part
   static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
   static constexpr int kStageBytes = 2 * kCps * kChunkBytes;  // K chunks, then V chunks
+  // int8 pools: a stage's key scales, [K, V][chunk][16] f32, after the ring's
+  // stages (their area rounded to 1 KiB keeps the next warp's ring aligned)
+  static constexpr int kScaleBytes = I8 ? 2 * kCps * kChunk * 4 : 0;
+  static constexpr int kScaleArea = (kRing * kScaleBytes + 1023) / 1024 * 1024;
   __host__ __device__ static int qslot_bytes(int rows) {
     return (rows * D * 2 + 1023) / 1024 * 1024;
   }
   __host__ __device__ static int warp_bytes(int rows) {
-    return kRing * (kStageBytes + qslot_bytes(rows));
+    return kRing * (kStageBytes + qslot_bytes(rows)) + kScaleArea;
   }
 };
 
@@ -505,6 +512,27 @@ struct IntC {
   static constexpr int value = N;
 };
 
+// Four int8 codes (one 32-bit register, low byte first) as two fp16 pairs:
+// codes 0,1 in lo and 2,3 in hi; exact.  A code c + 128 as the low byte
+// under the high byte 0x64 is the fp16 1024 + c + 128, so one packed
+// subtraction of 1152 leaves c.
+__device__ __forceinline__ void i8x4_as_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140u);
+  hi = __byte_perm(u, 0x64646464u, 0x4342u);
+  asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(hi) : "r"(0x64806480u));
+}
+// The same for a transposed pair of code pairs (bytes: key k codes c, c+1;
+// key k+1 codes c, c+1): lo = (key k, key k+1) at code c, hi at code c+1.
+__device__ __forceinline__ void i8x4_keys_as_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4240u);
+  hi = __byte_perm(u, 0x64646464u, 0x4341u);
+  asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(hi) : "r"(0x64806480u));
+}
+
 struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits;
 };
@@ -516,11 +544,12 @@ struct WarpShared {
   int abort_flag;
 };
 
-template <int D, bool TWO_ROWS, bool KV8>
+template <int D, bool TWO_ROWS, bool KV8, bool I8 = false>
 __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     decode_bf16_kernel(DecodeParams P, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, int box_rows) {
-  using L = WarpSmem<D, KV8>;
+  static_assert(!I8 || KV8, "int8 pools take the one-byte path");
+  using L = WarpSmem<D, KV8, I8>;
   constexpr int R = L::kRing;  // stages per warp
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ WarpShared sh;
@@ -550,7 +579,8 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const int qslot = L::qslot_bytes(P.rows);
   const uint64_t kv_policy = l2_evict_first();
   const uint32_t ring = sbase0 + w * L::warp_bytes(P.rows);
-  const uint32_t qbase = ring + R * L::kStageBytes;
+  const uint32_t scale_ring = ring + R * L::kStageBytes;  // int8 pools: the stages' scales
+  const uint32_t qbase = scale_ring + L::kScaleArea;
   const unsigned char* qbase_ptr = smem0 + (qbase - sbase0);
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
@@ -657,6 +687,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     }
     uint32_t mask = 0u;  // live keys of the stage (16 bits per chunk)
     int slot0 = n_slots;  // first pool slot of this lane's box (n_slots: read as zeros)
+    int64_t scale0 = 0;   // int8 pools: the lane's chunk's first scale (0: a stand-in)
     if (one_page) {
       // pages of a multiple of 16 keys: each chunk is one run of one page.
       // The stage's live keys are the range [lo, p] clipped to it; each
@@ -674,7 +705,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         if (lane == 0) report(P.error_word, TL_DEVERR_PAGE_RANGE);
         mask &= ~bad;
       }
-      if (page_ok) slot0 = pr * P.page_size + in_page(P, jm);
+      if (page_ok) {
+        slot0 = pr * P.page_size + in_page(P, jm);
+        if (I8) scale0 = ((int64_t)pr * P.h_kv + icur.g) * P.page_size + in_page(P, jm);
+      }
     } else {
       const int jr = j0 + (CPS == 2 ? lane : (lane & 15));
       const int pr = __shfl_sync(0xffffffffu, iwin, (page_of(P, jr) - iwin_blk0) & 31);
@@ -693,7 +727,7 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     const uint32_t bar = smem_u32(&sh.full[w][stage]);
     if (lane == 0) {
       sh.stage_mask[w][stage] = mask;
-      mbar_arrive_expect_tx(bar, L::kStageBytes);
+      mbar_arrive_expect_tx(bar, L::kStageBytes + L::kScaleBytes);
     }
     // no warp barrier here: a box may land before lane 0's expectation (the
     // transaction count then runs negative), and the phase cannot complete
@@ -702,6 +736,16 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       tma_load_3d_hint(ring + stage * L::kStageBytes + (rq_kind * CPS + rq_sub) * L::kChunkBytes +
                            rq_half * L::kHalfBytes + rq_box * box_rows * 128,
                        rq_map, rq_half * (KV8 ? 128 : 64), icur.g, slot0, bar, kv_policy);
+    if constexpr (I8) {
+      // the stage's key scales: lanes nreq .. nreq + 2 CPS - 1 copy the 16
+      // scales (64 bytes, contiguous within a page and head) of K, then V,
+      // of chunk rq_sub; a chunk the item does not read copies a stand-in
+      // (the pool's first 16 scales) so that the byte count always holds
+      const int li = lane - nreq;
+      if (li >= 0 && li < 2 * CPS)
+        bulk_g2s(scale_ring + stage * L::kScaleBytes + (li / CPS * CPS + rq_sub) * kChunk * 4,
+                 (li < CPS ? P.k_scales : P.v_scales) + scale0, kChunk * 4, bar);
+    }
     ++gs_issue;
     icur_c += CPS;
     if (icur_c >= icur.c_end) icur_live = false;
@@ -828,7 +872,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt) {
                 uint32_t b0, b1;
-                e4m3x4_as_f16x2x2(w[2 * h + nt], b0, b1);
+                if constexpr (I8)
+                  i8x4_as_f16x2x2(w[2 * h + nt], b0, b1);
+                else
+                  e4m3x4_as_f16x2x2(w[2 * h + nt], b0, b1);
                 mma_16816<true>((h ? s2 : s[j])[nt], qa[ks + h][0], qa[ks + h][1],
                                 qa[ks + h][2], qa[ks + h][3], b0, b1);
               }
@@ -852,6 +899,26 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e) s[j][n][e] += s2[n][e];
+      }
+      if constexpr (I8) {
+        // int8 pools: each key's dot product times its K scale (this lane's
+        // keys 8n + qc and 8n + qc + 1 of each chunk)
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          if (j >= nj) break;
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            float k0, k1;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n"
+                         : "=f"(k0), "=f"(k1)
+                         : "r"(scale_ring + stage * L::kScaleBytes +
+                               ((sub0 + j) * kChunk + n * 8 + qc) * 4));
+            s[j][n][0] *= k0;
+            s[j][n][1] *= k1;
+            s[j][n][2] *= k0;
+            s[j][n][3] *= k1;
+          }
+        }
       }
       // scores in log2 units; keys outside the stage's live set (or, with
       // several query tokens, outside a row's own range) score -inf.  A stage
@@ -993,6 +1060,24 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         if (jc >= nj) break;
         const uint32_t vaddr =
             ring + stage * L::kStageBytes + (CPS + sub0 + jc) * L::kChunkBytes;
+        if constexpr (I8) {
+          // int8 pools: each probability times its key's V scale (a key
+          // outside the live set has p = 0 and keeps it, whatever its scale)
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            float v0, v1;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n"
+                         : "=f"(v0), "=f"(v1)
+                         : "r"(scale_ring + stage * L::kScaleBytes +
+                               ((CPS + sub0 + jc) * kChunk + n * 8 + qc) * 4));
+            p[jc][n][0] = p[jc][n][0] > 0.f ? p[jc][n][0] * v0 : 0.f;
+            p[jc][n][1] = p[jc][n][1] > 0.f ? p[jc][n][1] * v1 : 0.f;
+            if (TWO_ROWS) {
+              p[jc][n][2] = p[jc][n][2] > 0.f ? p[jc][n][2] * v0 : 0.f;
+              p[jc][n][3] = p[jc][n][3] > 0.f ? p[jc][n][3] * v1 : 0.f;
+            }
+          }
+        }
         // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
         uint32_t h0, l0w, h2, l2w;
         split16<KV8>(p[jc][0][0], p[jc][0][1], h0, l0w);
@@ -1024,8 +1109,13 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
               const int j = j0 + h;
               // bytes (k 2t: 2g, 2g+1; k 2t+1: 2g, 2g+1) -> (2g: k, k+1; 2g+1: k, k+1)
               uint32_t a0, b0, a1, b1;
-              e4m3x4_as_f16x2x2(__byte_perm(w[2 * h], 0u, 0x3120u), a0, b0);
-              e4m3x4_as_f16x2x2(__byte_perm(w[2 * h + 1], 0u, 0x3120u), a1, b1);
+              if constexpr (I8) {
+                i8x4_keys_as_f16x2x2(w[2 * h], a0, b0);
+                i8x4_keys_as_f16x2x2(w[2 * h + 1], a1, b1);
+              } else {
+                e4m3x4_as_f16x2x2(__byte_perm(w[2 * h], 0u, 0x3120u), a0, b0);
+                e4m3x4_as_f16x2x2(__byte_perm(w[2 * h + 1], 0u, 0x3120u), a1, b1);
+              }
               if (!TWO_ROWS) {
                 mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
                 mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
@@ -1365,7 +1455,8 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
                              int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
                              int32_t page_size, int32_t window, int32_t ring_pages, float scale,
                              tl_dtype dtype, void* workspace, size_t workspace_bytes,
-                             uint32_t* error_word, void* stream, const NewRows& nr = NewRows()) {
+                             uint32_t* error_word, void* stream, const NewRows& nr = NewRows(),
+                             const float* k_scales = nullptr, const float* v_scales = nullptr) {
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || num_pages <= 0 || page_size <= 0 ||
       max_pages_per_seq <= 0 || window < 0)
     return TL_ERR_INVALID_ARG;
@@ -1387,6 +1478,14 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   if (dtype != TL_F32 && page_size % 8 != 0) return TL_ERR_UNSUPPORTED;
   if (dtype == TL_FP8_E4M3 && d != 128) return TL_ERR_UNSUPPORTED;
   if ((int64_t)num_pages * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
+  // int8 pools (the one-byte path with per-key scales): a chunk's 16 scales
+  // of one head are one aligned 64-byte copy
+  const bool i8 = k_scales != nullptr || v_scales != nullptr;
+  if (i8) {
+    if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales) || nr.n != 0)
+      return TL_ERR_INVALID_ARG;
+    if (dtype != TL_FP8_E4M3 || page_size % 16 != 0) return TL_ERR_UNSUPPORTED;
+  }
   const size_t need = decode_ws_layout(B, q_len * h_q, h_kv, d, nullptr, nullptr);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TL_ERR_WORKSPACE;
@@ -1427,6 +1526,8 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   P.n_new = 0;
   P.new_kind = 0;
   P.row_units = 0;
+  P.k_scales = k_scales;
+  P.v_scales = v_scales;
   if (nr.n < 0) return TL_ERR_INVALID_ARG;
   if (nr.n > 0) {
     if (!nr.k_new || !nr.v_new || !nr.slot_mapping || !nr.k_dst || !nr.v_dst)
@@ -1455,9 +1556,10 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   const bool kv8 = dtype == TL_FP8_E4M3;
   int warps = 0;
   if (dtype != TL_F32) {
-    const int per_warp = kv8 ? WarpSmem<128, true>::warp_bytes(rows)
-                             : (d == 128 ? WarpSmem<128, false>::warp_bytes(rows)
-                                         : WarpSmem<64, false>::warp_bytes(rows));
+    const int per_warp = i8    ? WarpSmem<128, true, true>::warp_bytes(rows)
+                         : kv8 ? WarpSmem<128, true>::warp_bytes(rows)
+                               : (d == 128 ? WarpSmem<128, false>::warp_bytes(rows)
+                                           : WarpSmem<64, false>::warp_bytes(rows));
     warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);
   }
   const int target_splits = (kTargetItems + h_kv - 1) / h_kv;
@@ -1487,10 +1589,10 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
                          : (encode_bf16_tensor_map(&kmap, k_cache, 3, dims, strides, box, true) &&
                             encode_bf16_tensor_map(&vmap, v_cache, 3, dims, strides, box, true));
     if (!enc) return TL_ERR_CUDA;
-#define TL_LAUNCH_W(DD, TWO, K8)                                                          \
+#define TL_LAUNCH_W(DD, TWO, K8, I8V)                                                     \
   do {                                                                                    \
-    auto kern = decode_bf16_kernel<DD, TWO, K8>;                                          \
-    const int sm = warps * WarpSmem<DD, K8>::warp_bytes(rows) + 1024;                     \
+    auto kern = decode_bf16_kernel<DD, TWO, K8, I8V>;                                     \
+    const int sm = warps * WarpSmem<DD, K8, I8V>::warp_bytes(rows) + 1024;                \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
         cudaSuccess)                                                                      \
       return TL_ERR_CUDA;                                                                 \
@@ -1507,12 +1609,19 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
     if (cudaLaunchKernelEx(&cfg, kern, P, kmap, vmap, box_rows) != cudaSuccess)           \
       return TL_ERR_CUDA;                                                                 \
   } while (0)
-    if (kv8) {
-      if (rows > 8) TL_LAUNCH_W(128, true, true); else TL_LAUNCH_W(128, false, true);
+    // template arguments: d, two row groups (rows > 8), one-byte codes, int8
+    if (i8) {
+      if (rows > 8) TL_LAUNCH_W(128, true, true, true);
+      else TL_LAUNCH_W(128, false, true, true);
+    } else if (kv8) {
+      if (rows > 8) TL_LAUNCH_W(128, true, true, false);
+      else TL_LAUNCH_W(128, false, true, false);
     } else if (d == 128) {
-      if (rows > 8) TL_LAUNCH_W(128, true, false); else TL_LAUNCH_W(128, false, false);
+      if (rows > 8) TL_LAUNCH_W(128, true, false, false);
+      else TL_LAUNCH_W(128, false, false, false);
     } else {
-      if (rows > 8) TL_LAUNCH_W(64, true, false); else TL_LAUNCH_W(64, false, false);
+      if (rows > 8) TL_LAUNCH_W(64, true, false, false);
+      else TL_LAUNCH_W(64, false, false, false);
     }
 #undef TL_LAUNCH_W
     if (launch_status() != TL_OK) return TL_ERR_CUDA;
@@ -1556,6 +1665,19 @@ extern "C" tl_status tl_paged_attn_decode(const void* q, const void* k_cache,
   return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
                          B, 1, h_q, h_kv, d, num_pages, page_size, window, 0, scale, dtype,
                          workspace, workspace_bytes, error_word, stream);
+}
+
+extern "C" tl_status tl_paged_attn_decode_int8(
+    const void* q, const int8_t* k_codes, const int8_t* v_codes, const float* k_scales,
+    const float* v_scales, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* context_lens, float* out, int32_t B, int32_t h_q, int32_t h_kv, int32_t d,
+    int32_t num_pages, int32_t page_size, int32_t window, float scale, void* workspace,
+    size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  if (!k_scales || !v_scales) return TL_ERR_INVALID_ARG;
+  return tl::decode_impl(q, k_codes, v_codes, block_table, max_pages_per_seq, context_lens, out,
+                         B, 1, h_q, h_kv, d, num_pages, page_size, window, 0, scale,
+                         TL_FP8_E4M3, workspace, workspace_bytes, error_word, stream,
+                         tl::NewRows(), k_scales, v_scales);
 }
 
 extern "C" tl_status tl_paged_attn_decode_write(

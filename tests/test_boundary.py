@@ -107,6 +107,31 @@ def test_host_validation_refuses_before_any_launch(lib):
     assert decw(nd=0) == tl.TL_ERR_UNSUPPORTED  # f32 rows into bf16 pools
     assert decw(nd=2, dt=2) == tl.TL_ERR_UNSUPPORTED  # e4m3 rows into e4m3 pools
 
+    # int8 pools: the write's and the decode's own checks
+    def w8(kn=2304, vn=2560, sd=1, ks=12288, vs=16384, sm=2816, n=2, d=128):
+        return lib.tl_kv_cache_write_int8(kn, vn, sd, 4096, 8192, ks, vs, sm, n, 4, 16, 8, d,
+                                          None, None)
+    assert w8(n=-1) == tl.TL_ERR_INVALID_ARG
+    assert w8(n=0, kn=None) == tl.TL_OK  # no rows: a no-op
+    assert w8(sd=2) == tl.TL_ERR_UNSUPPORTED  # e4m3 rows
+    assert w8(d=2048) == tl.TL_ERR_UNSUPPORTED
+    assert w8(ks=None) == tl.TL_ERR_INVALID_ARG
+    assert w8(ks=12290) == tl.TL_ERR_INVALID_ARG  # scales not 4-byte aligned
+    assert w8(kn=2312) == tl.TL_ERR_INVALID_ARG  # new rows not 16-byte aligned
+    assert w8(sm=2820) == tl.TL_ERR_INVALID_ARG  # slots not 8-byte aligned
+
+    def d8(ks=12288, vs=16384, **kw):
+        a = dict(args, ws=4096, wsb=1 << 30, **kw)
+        return lib.tl_paged_attn_decode_int8(a["q"], a["k"], a["v"], ks, vs, a["bt"], a["maxp"],
+                                             a["cl"], a["out"], a["B"], a["hq"], a["hkv"], a["d"],
+                                             a["P"], a["ps"], a["w"], a["sc"], a["ws"], a["wsb"],
+                                             a["err"], a["st"])
+    assert d8(ks=None) == tl.TL_ERR_INVALID_ARG
+    assert d8(vs=16392) == tl.TL_ERR_INVALID_ARG  # scales not 16-byte aligned
+    assert d8(ps=24) == tl.TL_ERR_UNSUPPORTED  # a chunk's scales would span pages
+    assert d8(d=64) == tl.TL_ERR_UNSUPPORTED
+    assert d8(q=None) == tl.TL_ERR_INVALID_ARG
+
     def pre(**kw):
         a = dict(args, **kw)
         return lib.tl_paged_attn_prefill(a["q"], a["k"], a["v"], a["bt"], a["maxp"], a["cl"],

@@ -1,0 +1,132 @@
+"""int8 KV pools on the GPU against the oracle.  "How serving works in
+Tlaloc" names int8 KV pools as a next step without a format; the format is
+read from its "Int8 weights (opt-in)" paragraph: one f32 scale per (token, KV
+head) row, max |x| / 127, codes x / scale rounded half to even.  The write is
+compared bit for bit (codes and scale bits); decode within the attention
+tolerance, the pools coming from the seeded generator on the host."""
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_cache_gb300 as tl
+from paged_kv_attention_cache_gb300 import workloads as wl
+from tests.gpu_util import sample_rows
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+@pytest.mark.parametrize("src", [torch.float32, torch.bfloat16])
+def test_int8_write_matches_the_oracle_bit_for_bit(src):
+    g = torch.Generator().manual_seed(91)
+    P, ps, hkv, d, n = 40, 16, 8, 128, 300
+    mag = torch.exp(torch.randn((n, hkv, 1), generator=g) * 2)
+    kn = (torch.randn((n, hkv, d), generator=g) * mag).to(src)
+    vn = torch.randn((n, hkv, d), generator=g).to(src)
+    kn[5, 3, 7] = float("nan")
+    vn[9, 0, 0] = float("inf")
+    vn[11, 2] = 0.0  # a zero row: scale 0, codes 0
+    slots = torch.randperm(P * ps, generator=g)[:n].to(torch.int64)
+    slots[::17] = -1  # pads
+    slots[3] = P * ps + 2  # out of range: reported, not written
+    kc = torch.full((P, ps, hkv, d), 0x55, dtype=torch.int8)
+    ks = torch.full((P, hkv, ps), 12345.0, dtype=torch.float32)
+    vc, vs = kc.clone(), ks.clone()
+    dev = [t.to(DEV) for t in (kc, vc, ks, vs)]
+    err = _err()
+    tl.tl_kv_cache_write_int8(kn.to(DEV), vn.to(DEV), *dev, slots.to(DEV), error_word=err)
+    torch.cuda.synchronize()
+    ok = slots.clone()
+    ok[3] = -1  # the oracle refuses an out-of-range slot; the kernel skips it
+    n_bad = oracle.kv_cache_write_int8(kn, vn, kc, vc, ks, vs, ok)
+    assert n_bad > 0
+    e = int(err.item())
+    assert e & tl.TL_DEVERR_SLOT_RANGE and e & tl.TL_DEVERR_VALUE_RANGE
+    assert torch.equal(dev[0].cpu(), kc) and torch.equal(dev[1].cpu(), vc)
+    assert torch.equal(dev[2].cpu().view(torch.int32), ks.view(torch.int32))
+    assert torch.equal(dev[3].cpu().view(torch.int32), vs.view(torch.int32))
+
+
+def _sub_pool(case, pools, rows):
+    """Host copies of the pages the rows use, tables renumbered to the copy."""
+    ps = case.page_size
+    lens = case.context_lens.tolist()
+    pages, tables = [], []
+    for b in rows:
+        n = (max(lens[b], 0) + ps - 1) // ps
+        ids = case.block_table[b, :n].tolist()
+        tables.append(list(range(len(pages), len(pages) + n)))
+        pages += ids
+    idx = torch.tensor(pages or [0], dtype=torch.long)
+    sub = [t.index_select(0, idx) for t in pools]
+    bt = torch.full((len(rows), max(1, max(len(t) for t in tables))), -1, dtype=torch.int32)
+    for i, t in enumerate(tables):
+        if t:
+            bt[i, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    return sub, bt
+
+
+def _check(case, pools, window, rows=None, what=""):
+    kc, vc, ks, vs = (t.to(DEV) for t in pools)
+    err = _err()
+    out = tl.tl_paged_attn_decode_int8(case.q.to(DEV), kc, vc, ks, vs,
+                                       case.block_table.to(DEV), case.context_lens.to(DEV),
+                                       case.scale, window=window, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, int(err.item())
+    out = out.cpu()
+    if rows is None:
+        ref = oracle.paged_decode_int8(case.q, *pools, case.block_table, case.context_lens,
+                                       case.scale, window=window)
+        assert_close(out, ref, what)
+    else:
+        sub, bt = _sub_pool(case, pools, rows)
+        ref = oracle.paged_decode_int8(case.q[rows], *sub, bt, case.context_lens[rows],
+                                       case.scale, window=window)
+        assert_close(out[rows], ref, what)
+    return out
+
+
+@pytest.mark.parametrize("window", [0, 37])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 8), (32, 2)])  # groups 4, 4 and 16
+def test_int8_decode_matches_the_oracle(hq, hkv, window):
+    case = wl.decode_case([0, 1, 15, 16, 17, 33, 300, 1000], Hq=hq, Hkv=hkv, d=128, seed=92,
+                          window=window)
+    _check(case, wl.int8_pools(case, 93), window, what=f"int8 {hq}/{hkv} w{window}")
+
+
+@pytest.mark.parametrize("ps", [32, 64])
+def test_int8_decode_page_sizes(ps):
+    case = wl.decode_case([3, 64, 65, 500, 2049], Hq=16, Hkv=4, d=128, page_size=ps, seed=94)
+    _check(case, wl.int8_pools(case, 95), 0, what=f"int8 page {ps}")
+
+
+def test_int8_decode_ignores_the_garbage_of_unread_slots():
+    # slots no position maps to hold code -128 and NaN scales; keys past a
+    # sequence's end share a chunk (and a scale copy) with its live keys
+    case = wl.decode_case([1, 17, 31, 100, 257], Hq=8, Hkv=2, d=128, seed=96, extra_pages=3)
+    out = _check(case, wl.int8_pools(case, 97, nan_unused=True), 0, what="int8 nan unused")
+    assert torch.isfinite(out).all()
+
+
+def test_int8_decode_llama8b_shape_sampled():
+    case = wl.llama8b_decode(seed=5)
+    rows = sample_rows(case.context_lens.tolist(), 6, seed=5)
+    _check(case, wl.int8_pools(case, 98), 0, rows=rows, what="int8 llama8b B=64")
+
+
+def test_int8_decode_reports_a_query_beyond_fp16():
+    case = wl.decode_case([40, 70], Hq=8, Hkv=2, d=128, seed=99)
+    pools = [t.to(DEV) for t in wl.int8_pools(case, 100)]
+    q = case.q.clone()
+    q[1, 3, 5] = 1e6
+    err = _err()
+    tl.tl_paged_attn_decode_int8(q.to(DEV), *pools, case.block_table.to(DEV),
+                                 case.context_lens.to(DEV), case.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & tl.TL_DEVERR_VALUE_RANGE
