@@ -226,6 +226,25 @@ tl_status tl_paged_attn_decode_int8(const void* q, const int8_t* k_codes, const 
                                     uint32_t* error_word, void* stream);
 
 /*
+ * tl_kv_cache_write_int8 of the n_new rows k_new / v_new ([n_new][h_kv][d],
+ * new_dtype TL_BF16 or TL_F32) at slot_mapping [n_new] (int64, -1 = padding)
+ * followed by tl_paged_attn_decode_int8, in one call (the write runs in the
+ * decode's first launch, as in tl_paged_attn_decode_write): the result, the
+ * pools (codes and scales) afterwards and the error bits are those of the two
+ * calls.  Arguments and support as the two calls.
+ */
+tl_status tl_paged_attn_decode_write_int8(const void* q, const void* k_new, const void* v_new,
+                                          tl_dtype new_dtype, const int64_t* slot_mapping,
+                                          int32_t n_new, int8_t* k_codes, int8_t* v_codes,
+                                          float* k_scales, float* v_scales,
+                                          const int32_t* block_table, int32_t max_pages_per_seq,
+                                          const int32_t* context_lens, float* out, int32_t B,
+                                          int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                          int32_t page_size, int32_t window, float scale,
+                                          void* workspace, size_t workspace_bytes,
+                                          uint32_t* error_word, void* stream);
+
+/*
  * KV_CACHE_WRITE then PAGED_ATTENTION decode in one call ("How serving works
  * in Tlaloc", section 1: each step writes its tokens' K/V, then attends):
  * the result, the pools afterwards and the error bits are those of

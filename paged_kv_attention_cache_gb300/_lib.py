@@ -29,6 +29,9 @@ SIGNATURES = {
     "tl_paged_attn_decode_workspace_size": ([i32, i32, i32, i32], sz),
     "tl_paged_attn_decode_int8": ([vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                    i32, i32, f32, vp, sz, u32p, vp], ctypes.c_int),
+    "tl_paged_attn_decode_write_int8": ([vp, vp, vp, ctypes.c_int, vp, i32, vp, vp, vp, vp, vp,
+                                         i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp,
+                                         sz, u32p, vp], ctypes.c_int),
     "tl_paged_attn_decode": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                               ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
     "tl_paged_attn_decode_write": ([vp, vp, vp, ctypes.c_int, vp, i32, vp, vp, vp, i32, vp, vp,

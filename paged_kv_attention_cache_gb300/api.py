@@ -160,6 +160,41 @@ def tl_paged_attn_decode_int8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: t
     return out
 
 
+def tl_paged_attn_decode_write_int8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                    slot_mapping: torch.Tensor, k_codes: torch.Tensor,
+                                    v_codes: torch.Tensor, k_scales: torch.Tensor,
+                                    v_scales: torch.Tensor, block_table: torch.Tensor,
+                                    context_lens: torch.Tensor, scale: float, window: int = 0,
+                                    out: Optional[torch.Tensor] = None,
+                                    workspace: Optional[torch.Tensor] = None,
+                                    error_word: Optional[torch.Tensor] = None,
+                                    stream=None) -> torch.Tensor:
+    """tl_kv_cache_write_int8 of the new rows (f32 or bf16 [N, H_kv, d] at
+    slot_mapping [N], -1 = padding), then tl_paged_attn_decode_int8, in one
+    call: out[B, H_q, d] float32; the pools are updated in place."""
+    _need(q, "q", torch.bfloat16)
+    _need(k_new, "k_new")
+    _need(v_new, "v_new", k_new.dtype)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    P, ps, hkv, _ = _need_int8_pools(k_codes, v_codes, k_scales, v_scales)
+    B, hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(tl_paged_attn_decode_workspace_size(B, hq, hkv, d), q.device)
+    st = _lib.load().tl_paged_attn_decode_write_int8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _DTYPES.get(k_new.dtype, -1), _ptr(slot_mapping),
+        slot_mapping.numel(), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales),
+        _ptr(block_table), block_table.shape[1], _ptr(context_lens), _ptr(out), B, hq, hkv, d,
+        P, ps, int(window), float(scale), _ptr(workspace), workspace.numel(), _ptr(error_word),
+        _stream(stream))
+    _check(st, "tl_paged_attn_decode_write_int8")
+    return out
+
+
 def tl_paged_attn_prefill_workspace_size_ex(B: int, T: int, h_q: int, h_kv: int, d: int,
                                             max_pages_per_seq: int, page_size: int,
                                             ring_pages: int, dtype: int) -> int:

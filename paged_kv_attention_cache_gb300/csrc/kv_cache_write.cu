@@ -50,44 +50,6 @@ __global__ void __launch_bounds__(256) kv_cache_write_fp8_kernel(
   }
 }
 
-// int8 pools: one (token, KV head) row of d new values as int8 codes and its
-// f32 scale, by one warp.  The format is read from the int8 weight
-// quantisation of "How serving works in Tlaloc" ("Int8 weights (opt-in)":
-// one scale per channel, max |x| / 127, codes rounded half to even), with
-// the row as the channel: s = m / 127 over the row's finite values, code =
-// rint(x / s) clamped to +-127, both IEEE binary32 divisions.  A row whose s
-// is 0 gets codes 0; a non-finite value gets code 0 and is reported.
-template <bool SRC_F32>
-__device__ __forceinline__ float new_value(const void* src, int64_t i) {
-  if (SRC_F32) return __ldg(static_cast<const float*>(src) + i);
-  return __uint_as_float((uint32_t)__ldg(static_cast<const unsigned short*>(src) + i) << 16);
-}
-
-template <bool SRC_F32>
-__device__ void quantize_row_int8(const void* src, int64_t base, int d, int8_t* codes,
-                                  float* scale, int lane, uint32_t* error_word) {
-  float m = 0.f;
-  bool bad = false;
-  for (int e = lane; e < d; e += 32) {
-    const float x = new_value<SRC_F32>(src, base + e);
-    if (isfinite(x))
-      m = fmaxf(m, fabsf(x));
-    else
-      bad = true;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const float sc = __fdiv_rn(m, 127.f);
-  for (int e = lane; e < d; e += 32) {
-    const float x = new_value<SRC_F32>(src, base + e);
-    float r = 0.f;
-    if (isfinite(x) && sc > 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x, sc)), -127.f), 127.f);
-    codes[e] = (int8_t)__float2int_rn(r);
-  }
-  if (lane == 0) *scale = sc;
-  if (__any_sync(0xffffffffu, bad) && lane == 0) report(error_word, TL_DEVERR_VALUE_RANGE);
-}
-
 // One warp per (token, KV head): its K row and its V row.  Codes at the pool
 // layout [num_pages][page_size][H_kv][d], scales at [num_pages][H_kv][page_size].
 template <bool SRC_F32>

@@ -69,4 +69,60 @@ __device__ __forceinline__ void write_token_rows_e4m3(const void* k_new, const v
   }
 }
 
+// int8 pools: one (token, KV head) row of d new values as int8 codes and its
+// f32 scale, by one warp.  The format is read from the int8 weight
+// quantisation of "How serving works in Tlaloc" ("Int8 weights (opt-in)":
+// one scale per channel, max |x| / 127, codes rounded half to even), with
+// the row as the channel: s = m / 127 over the row's finite values, code =
+// rint(x / s) clamped to +-127, both IEEE binary32 divisions.  A row whose s
+// is 0 gets codes 0; a non-finite value gets code 0 and is reported.
+template <bool SRC_F32>
+__device__ __forceinline__ float new_value(const void* src, int64_t i) {
+  if (SRC_F32) return __ldg(static_cast<const float*>(src) + i);
+  return __uint_as_float((uint32_t)__ldg(static_cast<const unsigned short*>(src) + i) << 16);
+}
+
+template <bool SRC_F32>
+__device__ void quantize_row_int8(const void* src, int64_t base, int d, int8_t* codes,
+                                  float* scale, int lane, uint32_t* error_word) {
+  float m = 0.f;
+  bool bad = false;
+  for (int e = lane; e < d; e += 32) {
+    const float x = new_value<SRC_F32>(src, base + e);
+    if (isfinite(x))
+      m = fmaxf(m, fabsf(x));
+    else
+      bad = true;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float sc = __fdiv_rn(m, 127.f);
+  for (int e = lane; e < d; e += 32) {
+    const float x = new_value<SRC_F32>(src, base + e);
+    float r = 0.f;
+    if (isfinite(x) && sc > 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x, sc)), -127.f), 127.f);
+    codes[e] = (int8_t)__float2int_rn(r);
+  }
+  if (lane == 0) *scale = sc;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) report(error_word, TL_DEVERR_VALUE_RANGE);
+}
+
+// All KV heads of one token into int8 pools, by one warp: codes at the pool
+// layout, scales at [num_pages][H_kv][page_size].
+template <bool SRC_F32>
+__device__ __forceinline__ void write_token_rows_int8(const void* k_new, const void* v_new,
+                                                      int8_t* k_codes, int8_t* v_codes,
+                                                      float* k_scales, float* v_scales,
+                                                      int64_t t, int64_t slot, int page_size,
+                                                      int h_kv, int d, int lane,
+                                                      uint32_t* error_word) {
+  const int64_t page = slot / page_size, off = slot % page_size;
+  for (int g = 0; g < h_kv; ++g) {
+    const int64_t src = (t * h_kv + g) * d, dst = (slot * h_kv + g) * d;
+    const int64_t si = (page * h_kv + g) * page_size + off;
+    quantize_row_int8<SRC_F32>(k_new, src, d, k_codes + dst, k_scales + si, lane, error_word);
+    quantize_row_int8<SRC_F32>(v_new, src, d, v_codes + dst, v_scales + si, lane, error_word);
+  }
+}
+
 }  // namespace tl

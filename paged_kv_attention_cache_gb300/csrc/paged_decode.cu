@@ -120,7 +120,8 @@ struct DecodeParams {
   void* k_dst;
   void* v_dst;
   int32_t n_new;
-  int32_t new_kind;   // 0 copy (same dtype), 1 e4m3 codes of bf16 rows, 2 of f32 rows
+  int32_t new_kind;   // 0 copy (same dtype), 1 e4m3 codes of bf16 rows, 2 of f32 rows,
+                      // 3 int8 codes and scales of bf16 rows, 4 of f32 rows
   int32_t row_units;  // 16-byte vectors (copy) or 8-element steps (e4m3) of one row
   // int8 pools: the per-(slot, KV head) scales, [num_pages][H_kv][page_size]
   const float* k_scales;
@@ -275,9 +276,19 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
       else if (P.new_kind == 1)
         write_token_rows_e4m3<false>(P.k_new, P.v_new, static_cast<uint2*>(P.k_dst),
                                      static_cast<uint2*>(P.v_dst), t, slot, u, lane);
-      else
+      else if (P.new_kind == 2)
         write_token_rows_e4m3<true>(P.k_new, P.v_new, static_cast<uint2*>(P.k_dst),
                                     static_cast<uint2*>(P.v_dst), t, slot, u, lane);
+      else if (P.new_kind == 3)  // int8 pools: the scales are written here, read after
+        write_token_rows_int8<false>(P.k_new, P.v_new, static_cast<int8_t*>(P.k_dst),
+                                     static_cast<int8_t*>(P.v_dst), const_cast<float*>(P.k_scales),
+                                     const_cast<float*>(P.v_scales), t, slot, P.page_size,
+                                     P.h_kv, P.d, lane, P.error_word);
+      else
+        write_token_rows_int8<true>(P.k_new, P.v_new, static_cast<int8_t*>(P.k_dst),
+                                    static_cast<int8_t*>(P.v_dst), const_cast<float*>(P.k_scales),
+                                    const_cast<float*>(P.v_scales), t, slot, P.page_size,
+                                    P.h_kv, P.d, lane, P.error_word);
     }
     return;
   }
@@ -1482,7 +1493,7 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   // of one head are one aligned 64-byte copy
   const bool i8 = k_scales != nullptr || v_scales != nullptr;
   if (i8) {
-    if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales) || nr.n != 0)
+    if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales))
       return TL_ERR_INVALID_ARG;
     if (dtype != TL_FP8_E4M3 || page_size % 16 != 0) return TL_ERR_UNSUPPORTED;
   }
@@ -1536,7 +1547,11 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
         (reinterpret_cast<uintptr_t>(nr.slot_mapping) & 7u))
       return TL_ERR_INVALID_ARG;
     const int64_t row = (int64_t)h_kv * d;
-    if (dtype == TL_FP8_E4M3) {
+    if (i8) {
+      if (nr.new_dtype != TL_BF16 && nr.new_dtype != TL_F32) return TL_ERR_UNSUPPORTED;
+      P.new_kind = nr.new_dtype == TL_BF16 ? 3 : 4;
+      P.row_units = 0;
+    } else if (dtype == TL_FP8_E4M3) {
       if (nr.new_dtype != TL_BF16 && nr.new_dtype != TL_F32) return TL_ERR_UNSUPPORTED;
       if (row % 16 != 0) return TL_ERR_INVALID_ARG;
       P.new_kind = nr.new_dtype == TL_BF16 ? 1 : 2;
@@ -1678,6 +1693,28 @@ extern "C" tl_status tl_paged_attn_decode_int8(
                          B, 1, h_q, h_kv, d, num_pages, page_size, window, 0, scale,
                          TL_FP8_E4M3, workspace, workspace_bytes, error_word, stream,
                          tl::NewRows(), k_scales, v_scales);
+}
+
+extern "C" tl_status tl_paged_attn_decode_write_int8(
+    const void* q, const void* k_new, const void* v_new, tl_dtype new_dtype,
+    const int64_t* slot_mapping, int32_t n_new, int8_t* k_codes, int8_t* v_codes,
+    float* k_scales, float* v_scales, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* context_lens, float* out, int32_t B, int32_t h_q, int32_t h_kv, int32_t d,
+    int32_t num_pages, int32_t page_size, int32_t window, float scale, void* workspace,
+    size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  if (!k_scales || !v_scales) return TL_ERR_INVALID_ARG;
+  tl::NewRows nr;
+  nr.k_new = k_new;
+  nr.v_new = v_new;
+  nr.slot_mapping = slot_mapping;
+  nr.n = n_new;
+  nr.new_dtype = new_dtype;
+  nr.k_dst = k_codes;
+  nr.v_dst = v_codes;
+  return tl::decode_impl(q, k_codes, v_codes, block_table, max_pages_per_seq, context_lens, out,
+                         B, 1, h_q, h_kv, d, num_pages, page_size, window, 0, scale,
+                         TL_FP8_E4M3, workspace, workspace_bytes, error_word, stream, nr,
+                         k_scales, v_scales);
 }
 
 extern "C" tl_status tl_paged_attn_decode_write(

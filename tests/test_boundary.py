@@ -132,6 +132,19 @@ def test_host_validation_refuses_before_any_launch(lib):
     assert d8(d=64) == tl.TL_ERR_UNSUPPORTED
     assert d8(q=None) == tl.TL_ERR_INVALID_ARG
 
+    def d8w(nd=1, sm=2816, n=2, ks=12288, **kw):
+        a = dict(args, ws=4096, wsb=1 << 30, **kw)
+        return lib.tl_paged_attn_decode_write_int8(a["q"], 2304, 2560, nd, sm, n, a["k"], a["v"],
+                                                   ks, 16384, a["bt"], a["maxp"], a["cl"],
+                                                   a["out"], a["B"], a["hq"], a["hkv"], a["d"],
+                                                   a["P"], a["ps"], a["w"], a["sc"], a["ws"],
+                                                   a["wsb"], a["err"], a["st"])
+    assert d8w(ks=None) == tl.TL_ERR_INVALID_ARG
+    assert d8w(n=-1) == tl.TL_ERR_INVALID_ARG
+    assert d8w(sm=2820) == tl.TL_ERR_INVALID_ARG  # slots not 8-byte aligned
+    assert d8w(nd=2) == tl.TL_ERR_UNSUPPORTED  # e4m3 rows into int8 pools
+    assert d8w(ps=24) == tl.TL_ERR_UNSUPPORTED
+
     def pre(**kw):
         a = dict(args, **kw)
         return lib.tl_paged_attn_prefill(a["q"], a["k"], a["v"], a["bt"], a["maxp"], a["cl"],

@@ -130,3 +130,42 @@ def test_int8_decode_reports_a_query_beyond_fp16():
                                  case.context_lens.to(DEV), case.scale, error_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) & tl.TL_DEVERR_VALUE_RANGE
+
+
+@pytest.mark.parametrize("src", [torch.bfloat16, torch.float32])
+def test_int8_fused_write_equals_the_two_calls(src):
+    # tl_paged_attn_decode_write_int8 == tl_kv_cache_write_int8, then
+    # tl_paged_attn_decode_int8: output, pools and error bits, bit for bit
+    case = wl.decode_case([5, 17, 100, 1000, 2049], Hq=16, Hkv=4, d=128, seed=101, n_pad=3)
+    pools = wl.int8_pools(case, 102)
+    slots = case.slot_mapping.clone()
+    live = (slots >= 0).nonzero().flatten()
+    slots[live[0]] = case.num_pages * case.page_size + 9  # reported, not written
+    kn, vn = case.k_new.to(src).to(DEV), case.v_new.to(src).to(DEV)
+    args = (case.block_table.to(DEV), case.context_lens.to(DEV), case.scale)
+    res = []
+    for fused in (False, True):
+        kc, vc, ks, vs = (t.to(DEV) for t in pools)
+        err = _err()
+        if fused:
+            out = tl.tl_paged_attn_decode_write_int8(case.q.to(DEV), kn, vn, slots.to(DEV), kc,
+                                                     vc, ks, vs, *args, error_word=err)
+        else:
+            tl.tl_kv_cache_write_int8(kn, vn, kc, vc, ks, vs, slots.to(DEV), error_word=err)
+            out = tl.tl_paged_attn_decode_int8(case.q.to(DEV), kc, vc, ks, vs, *args,
+                                               error_word=err)
+        torch.cuda.synchronize()
+        res.append((out.cpu(), kc.cpu(), vc.cpu(), ks.cpu(), vs.cpu(), int(err.item())))
+    (o1, *p1, e1), (o2, *p2, e2) = res
+    assert e1 == e2 and e1 & tl.TL_DEVERR_SLOT_RANGE
+    assert all(torch.equal(a.view(torch.uint8), b.view(torch.uint8)) for a, b in zip(p1, p2))
+    assert torch.equal(o1, o2)
+    # and against the oracle: its write on the host pools, then its decode
+    kc, vc, ks, vs = (t.clone() for t in pools)
+    ok = slots.clone()
+    ok[live[0]] = -1
+    oracle.kv_cache_write_int8(case.k_new.to(src), case.v_new.to(src), kc, vc, ks, vs, ok)
+    assert torch.equal(p2[0], kc) and torch.equal(p2[2].view(torch.int32), ks.view(torch.int32))
+    ref = oracle.paged_decode_int8(case.q, kc, vc, ks, vs, case.block_table, case.context_lens,
+                                   case.scale)
+    assert_close(o2, ref, f"fused int8 from {src}")
