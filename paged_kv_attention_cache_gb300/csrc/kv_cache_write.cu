@@ -72,11 +72,8 @@ __global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(
       if (lane == 0 && g == 0) report(error_word, TL_DEVERR_SLOT_RANGE);
       continue;
     }
-    const int64_t page = slot / page_size, off = slot % page_size;
-    const int64_t src = (t * h_kv + g) * d, dst = (slot * h_kv + g) * d;
-    const int64_t si = (page * h_kv + g) * page_size + off;
-    quantize_row_int8<SRC_F32>(k_new, src, d, k_codes + dst, k_scales + si, lane, error_word);
-    quantize_row_int8<SRC_F32>(v_new, src, d, v_codes + dst, v_scales + si, lane, error_word);
+    write_head_rows_int8<SRC_F32>(k_new, v_new, k_codes, v_codes, k_scales, v_scales, t, g, slot,
+                                  page_size, h_kv, d, lane, error_word);
   }
 }
 

@@ -107,22 +107,19 @@ __device__ void quantize_row_int8(const void* src, int64_t base, int d, int8_t* 
   if (__any_sync(0xffffffffu, bad) && lane == 0) report(error_word, TL_DEVERR_VALUE_RANGE);
 }
 
-// All KV heads of one token into int8 pools, by one warp: codes at the pool
-// layout, scales at [num_pages][H_kv][page_size].
+// The K and V rows of token t, KV head g into int8 pools, by one warp: codes
+// at the pool layout, scales at [num_pages][H_kv][page_size].
 template <bool SRC_F32>
-__device__ __forceinline__ void write_token_rows_int8(const void* k_new, const void* v_new,
-                                                      int8_t* k_codes, int8_t* v_codes,
-                                                      float* k_scales, float* v_scales,
-                                                      int64_t t, int64_t slot, int page_size,
-                                                      int h_kv, int d, int lane,
-                                                      uint32_t* error_word) {
+__device__ __forceinline__ void write_head_rows_int8(const void* k_new, const void* v_new,
+                                                     int8_t* k_codes, int8_t* v_codes,
+                                                     float* k_scales, float* v_scales, int64_t t,
+                                                     int g, int64_t slot, int page_size, int h_kv,
+                                                     int d, int lane, uint32_t* error_word) {
   const int64_t page = slot / page_size, off = slot % page_size;
-  for (int g = 0; g < h_kv; ++g) {
-    const int64_t src = (t * h_kv + g) * d, dst = (slot * h_kv + g) * d;
-    const int64_t si = (page * h_kv + g) * page_size + off;
-    quantize_row_int8<SRC_F32>(k_new, src, d, k_codes + dst, k_scales + si, lane, error_word);
-    quantize_row_int8<SRC_F32>(v_new, src, d, v_codes + dst, v_scales + si, lane, error_word);
-  }
+  const int64_t src = (t * h_kv + g) * d, dst = (slot * h_kv + g) * d;
+  const int64_t si = (page * h_kv + g) * page_size + off;
+  quantize_row_int8<SRC_F32>(k_new, src, d, k_codes + dst, k_scales + si, lane, error_word);
+  quantize_row_int8<SRC_F32>(v_new, src, d, v_codes + dst, v_scales + si, lane, error_word);
 }
 
 }  // namespace tl

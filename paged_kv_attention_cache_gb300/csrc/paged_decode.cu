@@ -255,11 +255,37 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
   // (griddepcontrol.wait) after its own set-up
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (blockIdx.x > 0) {
-    // CTAs past the first write the call's new rows: one warp per token,
-    // slot -1 skipped, a slot outside the pools reported and skipped
+    // CTAs past the first write the call's new rows: one warp per token (per
+    // token and KV head for int8 pools), slot -1 skipped, a slot outside the
+    // pools reported and skipped
     const int64_t first = (int64_t)(blockIdx.x - 1) * nw + wid;
     const int64_t stride = (int64_t)(gridDim.x - 1) * nw;
     const int64_t n_slots = (int64_t)P.num_pages * P.page_size;
+    if (P.new_kind >= 3) {
+      // int8 pools: one warp per (token, KV head) row; the scales written
+      // here are read by the attention kernel after this grid
+      for (int64_t r = first; r < (int64_t)P.n_new * P.h_kv; r += stride) {
+        const int64_t t = r / P.h_kv;
+        const int g = (int)(r % P.h_kv);
+        const int64_t slot = P.slot_mapping[t];
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= n_slots) {
+          if (lane == 0 && g == 0) report(P.error_word, TL_DEVERR_SLOT_RANGE);
+          continue;
+        }
+        int8_t* kd = static_cast<int8_t*>(P.k_dst);
+        int8_t* vd = static_cast<int8_t*>(P.v_dst);
+        float* ksc = const_cast<float*>(P.k_scales);
+        float* vsc = const_cast<float*>(P.v_scales);
+        if (P.new_kind == 3)
+          write_head_rows_int8<false>(P.k_new, P.v_new, kd, vd, ksc, vsc, t, g, slot,
+                                      P.page_size, P.h_kv, P.d, lane, P.error_word);
+        else
+          write_head_rows_int8<true>(P.k_new, P.v_new, kd, vd, ksc, vsc, t, g, slot,
+                                     P.page_size, P.h_kv, P.d, lane, P.error_word);
+      }
+      return;
+    }
     for (int64_t t = first; t < P.n_new; t += stride) {
       const int64_t slot = P.slot_mapping[t];
       if (slot == -1) continue;
@@ -276,19 +302,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
       else if (P.new_kind == 1)
         write_token_rows_e4m3<false>(P.k_new, P.v_new, static_cast<uint2*>(P.k_dst),
                                      static_cast<uint2*>(P.v_dst), t, slot, u, lane);
-      else if (P.new_kind == 2)
+      else
         write_token_rows_e4m3<true>(P.k_new, P.v_new, static_cast<uint2*>(P.k_dst),
                                     static_cast<uint2*>(P.v_dst), t, slot, u, lane);
-      else if (P.new_kind == 3)  // int8 pools: the scales are written here, read after
-        write_token_rows_int8<false>(P.k_new, P.v_new, static_cast<int8_t*>(P.k_dst),
-                                     static_cast<int8_t*>(P.v_dst), const_cast<float*>(P.k_scales),
-                                     const_cast<float*>(P.v_scales), t, slot, P.page_size,
-                                     P.h_kv, P.d, lane, P.error_word);
-      else
-        write_token_rows_int8<true>(P.k_new, P.v_new, static_cast<int8_t*>(P.k_dst),
-                                    static_cast<int8_t*>(P.v_dst), const_cast<float*>(P.k_scales),
-                                    const_cast<float*>(P.v_scales), t, slot, P.page_size,
-                                    P.h_kv, P.d, lane, P.error_word);
     }
     return;
   }
@@ -1583,8 +1599,10 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   const int plan_threads = (int)std::min<int64_t>(1024, std::max<int64_t>(256, align_up((size_t)B, 32)));
   // the plan CTA, then (for a call that writes its new rows) CTAs with one
   // warp per new row, up to one per SM
+  // (int8 pools: one warp per token and KV head)
+  const int64_t write_warps = P.new_kind >= 3 ? (int64_t)P.n_new * h_kv : P.n_new;
   const int64_t write_ctas =
-      P.n_new > 0 ? std::min<int64_t>(num_sms(), (P.n_new + plan_threads / 32 - 1) / (plan_threads / 32))
+      P.n_new > 0 ? std::min<int64_t>(num_sms(), (write_warps + plan_threads / 32 - 1) / (plan_threads / 32))
                   : 0;
   decode_plan_kernel<<<(unsigned)(1 + write_ctas), plan_threads, 0, st>>>(P, target_splits,
                                                                           num_sms() * warps);
