@@ -60,10 +60,14 @@ extern "C" {
 
 typedef enum {
   TL_OK = 0,
-  TL_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, misalignment */
-  TL_ERR_UNSUPPORTED = 2, /* valid, but not a shape or dtype the library runs */
-  TL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
-  TL_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+  TL_ERR_INVALID_ARG = 1,   /* a null pointer, a bad size, misalignment */
+  TL_ERR_UNSUPPORTED = 2,   /* valid, but not a shape or dtype the library runs */
+  TL_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  TL_ERR_DEVICE_BOUNDS = 4, /* tl_get_device_error only: a device-side check found a value
+                               out of range (any TL_DEVERR_* bit but TL_DEVERR_TIMEOUT) */
+  TL_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required */
+  TL_ERR_DEVICE_TIMEOUT = 6 /* tl_get_device_error only: an in-kernel wait gave up
+                               (TL_DEVERR_TIMEOUT; outputs invalid) */
 } tl_status;
 
 typedef enum {
@@ -81,6 +85,26 @@ typedef enum {
                                       fp16: V in prefill, q in decode over e4m3 or int8 pools
                                       (outputs invalid); or a non-finite value written into an
                                       int8 pool (written as code 0) */
+#define TL_DEVERR_PLAN_CAPACITY 32u /* the decode plan cut the batch into more pieces than its
+                                       workspace holds: nothing was attended and every output
+                                       is 0 (a library fault; the plan's arithmetic keeps the
+                                       pieces within the bound) */
+
+/*
+ * The device-side error word ("How serving works in Tlaloc", the Triton
+ * backend bullets: a request the pool cannot serve is refused by name).
+ * Every entry point that launches work takes an optional `error_word`
+ * (a device uint32, owned by the caller, zeroed by the caller before the
+ * calls it should cover); kernels OR TL_DEVERR_* bits into it and never
+ * clear it.  tl_get_device_error reads it once the work enqueued on `stream`
+ * before this call has finished (it synchronises `stream`), stores the bits
+ * in *bits (when bits is not NULL) and, with clear != 0, zeroes the word
+ * afterwards on the same stream.  Returns TL_OK when no bit is set,
+ * TL_ERR_DEVICE_TIMEOUT when TL_DEVERR_TIMEOUT is set, TL_ERR_DEVICE_BOUNDS
+ * when any other bit is set, TL_ERR_INVALID_ARG for a NULL or misaligned
+ * error_word and TL_ERR_CUDA when the copy or the synchronisation fails.
+ */
+tl_status tl_get_device_error(uint32_t* error_word, uint32_t* bits, int32_t clear, void* stream);
 
 /* Name of a status, for messages (never NULL). */
 const char* tl_status_string(tl_status status);
@@ -290,6 +314,10 @@ tl_status tl_paged_attn_decode_write(const void* q, const void* k_new, const voi
  * All calls on a device share the array, which keeps the last call's
  * contents (nothing in it needs to start at zero); calls whose GPU work
  * overlaps (other streams or host threads) race on it and must be serialised.
+ * The address is kept per device for the process's primary context: calls
+ * from another context (cuCtxCreate) or after cudaDeviceReset would use a
+ * stale address, so this entry point is for callers on the primary context
+ * that do not reset the device while the library is loaded.
  */
 #define TL_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
 tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,

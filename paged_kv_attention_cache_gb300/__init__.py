@@ -7,7 +7,9 @@ without the built library, or without a CUDA device, raises.
 """
 from .api import (TL_BF16, TL_FP8_E4M3, tl_kv_cache_write_fp8, TL_DEVERR_CONTEXT_RANGE, TL_DEVERR_PAGE_RANGE,  # noqa: F401
                   TL_DEVERR_SLOT_RANGE, TL_DEVERR_TIMEOUT, TL_DEVERR_VALUE_RANGE, TL_ERR_CUDA, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED,
-                  TL_ERR_WORKSPACE, TL_F32, TL_OK, TLError, alloc_workspace,
+                  TL_ERR_WORKSPACE, TL_ERR_DEVICE_BOUNDS, TL_ERR_DEVICE_TIMEOUT,
+                  TL_DEVERR_PLAN_CAPACITY, TL_F32, TL_OK, TLError, alloc_workspace,
+                  tl_get_device_error,
                   TL_DECODE_NOALLOC_SCRATCH_BYTES, tl_kv_cache_write, tl_paged_attn_decode,
                   tl_paged_attn_decode_noalloc, tl_paged_attn_decode_workspace_size,
                   tl_paged_attn_decode_write, tl_kv_cache_write_int8, tl_paged_attn_decode_int8,
@@ -34,5 +36,5 @@ __all__ = [
     "tl_paged_attn_decode_ring", "tl_paged_attn_prefill_ring",
     "tl_paged_attn_prefill_ring_workspace_size", "tl_paged_attn_decode_multi",
     "tl_paged_attn_decode_multi_workspace_size",
-    "tl_status_string", "tl_version", "TLError", "build_library", "alloc_workspace",
+    "tl_status_string", "tl_version", "tl_get_device_error", "TLError", "build_library", "alloc_workspace",
 ]

@@ -20,6 +20,7 @@ i32, i64, u32p, vp, sz, f32 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, 
 SIGNATURES = {
     "tl_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tl_version": ([], i32),
+    "tl_get_device_error": ([vp, vp, i32, vp], ctypes.c_int),
     "tl_kv_cache_write": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, u32p, vp],
                           ctypes.c_int),
     "tl_kv_cache_write_fp8": ([vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, i32, i32, u32p,

@@ -74,5 +74,39 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, sources, defines, force: bool = False) -> str:
+    """A separate library built from some of the sources with extra -D
+    definitions, at _build/variants/<name>/libtlpa.so.  Used by tests that
+    need a build-time setting the product library does not have (a short
+    in-kernel wait bound with one wait made to run out)."""
+    out_dir = os.path.join(BUILD, "variants", name)
+    lib = os.path.join(out_dir, "libtlpa.so")
+    deps = [os.path.join(CSRC, s) for s in sources] + _deps()
+    if not force and os.path.exists(lib) and all(os.path.getmtime(f) <= os.path.getmtime(lib)
+                                                 for f in deps):
+        return lib
+    nvcc = _nvcc()
+    os.makedirs(out_dir, exist_ok=True)
+    flags = [*ARCH, *NVCC_FLAGS, *("-D" + d for d in defines)]
+
+    def compile_one(src):
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
+        r = subprocess.run([nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(sources)) as ex:
+        objs = list(ex.map(compile_one, sources))
+    tmp = lib + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force=True, verbose=True))

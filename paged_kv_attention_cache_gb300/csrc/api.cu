@@ -83,9 +83,29 @@ extern "C" const char* tl_status_string(tl_status status) {
     case TL_ERR_INVALID_ARG: return "TL_ERR_INVALID_ARG: a null pointer, bad size or misaligned pointer";
     case TL_ERR_UNSUPPORTED: return "TL_ERR_UNSUPPORTED: valid arguments, but not a shape or dtype the library runs";
     case TL_ERR_CUDA: return "TL_ERR_CUDA: a CUDA call or kernel launch failed";
+    case TL_ERR_DEVICE_BOUNDS: return "TL_ERR_DEVICE_BOUNDS: a device-side check found a value out of range";
     case TL_ERR_WORKSPACE: return "TL_ERR_WORKSPACE: workspace missing or too small";
+    case TL_ERR_DEVICE_TIMEOUT: return "TL_ERR_DEVICE_TIMEOUT: an in-kernel wait gave up (outputs invalid)";
   }
   return "unknown tl_status";
 }
 
-extern "C" int32_t tl_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+extern "C" int32_t tl_version(void) { return 1 * 10000 + 1 * 100 + 0; }
+
+// The error word is read after the stream's earlier work (a copy ordered on
+// the stream, then a synchronisation of the stream), and cleared after the
+// read on the same stream when asked.
+extern "C" tl_status tl_get_device_error(uint32_t* error_word, uint32_t* bits, int32_t clear,
+                                         void* stream) {
+  if (!error_word || (reinterpret_cast<uintptr_t>(error_word) & 3u)) return TL_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, error_word, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return TL_ERR_CUDA;
+  if (clear && cudaMemsetAsync(error_word, 0, sizeof(uint32_t), st) != cudaSuccess)
+    return TL_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TL_ERR_CUDA;
+  if (bits) *bits = word;
+  if (word & TL_DEVERR_TIMEOUT) return TL_ERR_DEVICE_TIMEOUT;
+  return word ? TL_ERR_DEVICE_BOUNDS : TL_OK;
+}

@@ -96,7 +96,10 @@ TL_DEVINLINE float warp_sum(float v) {
 // the CTA's abort flag and gives up, and every other wait of the CTA gives up
 // as soon as it sees the flag, so no kernel can spin forever.
 
-constexpr long long kWaitCycles = 1ll << 31;  // about one second at 2 GHz
+#ifndef TL_WAIT_CYCLES
+#define TL_WAIT_CYCLES (1ll << 31)  // about one second at 2 GHz
+#endif
+constexpr long long kWaitCycles = TL_WAIT_CYCLES;
 
 TL_DEVINLINE void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");

@@ -11,7 +11,9 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its TL_DECODE_NOALLOC_SCRATCH_BYTES until the process exits.
 // Its device address is looked up once per device, on the first call made
-// while that device is current; later calls reuse it.
+// while that device is current; later calls reuse it.  The address belongs to
+// the device's primary context: a caller that resets the device, or calls
+// from a context of its own, must not use this entry point.
 //
 // All calls on a device share the one array and leave the last call's
 // contents in it.  Nothing in it needs to start at zero: the decode's plan

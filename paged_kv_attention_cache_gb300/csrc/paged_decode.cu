@@ -58,7 +58,7 @@ constexpr int kDecodeThreads = kDecodeWarps * 32;
 
 // Pieces per call: the plan keeps them within ceil(kTargetItems / h_kv) + 2B
 // (each of its two rounds rounds up once per sequence).
-inline int64_t decode_max_splits(int B, int h_kv) {
+__host__ __device__ inline int64_t decode_max_splits(int B, int h_kv) {
   return (int64_t)(kTargetItems + h_kv - 1) / h_kv + 2 * (int64_t)B;
 }
 
@@ -338,6 +338,19 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
     NB += (n - tail_chunks(n) + split - 1) / split;
   }
   block_sum2(NB, unused, red);
+  // the workspace holds decode_max_splits(B, h_kv) descriptors and partials;
+  // the two rounds above stay within it by construction, and a total past it
+  // is refused here (nothing is attended, every output comes out 0)
+  if (NB + TP > decode_max_splits(P.B, P.h_kv)) {
+    for (int b = tid; b <= P.B; b += nt) P.ws.split_off[b] = 0;
+    if (tid == 0) {
+      report(P.error_word, TL_DEVERR_PLAN_CAPACITY);
+      P.ws.ctrl[0] = split;
+      P.ws.ctrl[1] = 0;
+      P.ws.ctrl[2] = first_dynamic;
+    }
+    return;
+  }
   // descriptors: bulk pieces at [0, NB) and small pieces at [NB, NB + TP) in
   // sequence order; partial indices split_off[b] + k, bulk pieces first
   long long carry = 0;  // (bulk << 32) | small pieces before this round of sequences
@@ -754,7 +767,14 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     const uint32_t bar = smem_u32(&sh.full[w][stage]);
     if (lane == 0) {
       sh.stage_mask[w][stage] = mask;
-      mbar_arrive_expect_tx(bar, L::kStageBytes + L::kScaleBytes);
+      uint32_t tx = L::kStageBytes + L::kScaleBytes;
+#ifdef TL_TEST_STALL_FIRST_STAGE
+      // failure-path test build only: the first stage of warp 0 of CTA 0
+      // expects 16 bytes that no copy delivers, so the wait for it runs out
+      // (the copies it does issue all land before the CTA exits)
+      if (blockIdx.x == 0 && w == 0 && gs_issue == 0) tx += 16;
+#endif
+      mbar_arrive_expect_tx(bar, tx);
     }
     // no warp barrier here: a box may land before lane 0's expectation (the
     // transaction count then runs negative), and the phase cannot complete

@@ -38,9 +38,34 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(5):
+    for s in range(7):
         assert lib.tl_status_string(s).decode().startswith("TL_")
-    assert tl.tl_version() >= 10000
+    assert lib.tl_status_string(99).decode() == "unknown tl_status"
+    assert tl.tl_version() >= 10100
+
+
+def test_status_and_error_bit_values_follow_the_header():
+    """The binding's constants are the header's: TL_ERR_DEVICE_BOUNDS is 4 and
+    TL_ERR_WORKSPACE 5; the TL_DEVERR_* bits are distinct powers of two."""
+    from paged_kv_attention_cache_gb300 import api
+    text = open(HEADER).read()
+    statuses = {k: int(v) for k, v in re.findall(r"\b(TL_(?:OK|ERR_[A-Z_]+))\s*=\s*(\d+)", text)}
+    assert statuses == {"TL_OK": 0, "TL_ERR_INVALID_ARG": 1, "TL_ERR_UNSUPPORTED": 2,
+                        "TL_ERR_CUDA": 3, "TL_ERR_DEVICE_BOUNDS": 4, "TL_ERR_WORKSPACE": 5,
+                        "TL_ERR_DEVICE_TIMEOUT": 6}
+    for name, v in statuses.items():
+        assert getattr(api, name) == v, name
+    bits = {k: int(v) for k, v in re.findall(r"#define (TL_DEVERR_[A-Z_]+) (\d+)u", text)}
+    assert len(bits) == 6
+    for name, v in bits.items():
+        assert getattr(api, name) == v, name
+        assert v & (v - 1) == 0
+    assert len(set(bits.values())) == len(bits)
+
+
+def test_device_error_query_refuses_a_bad_word_before_any_cuda_call(lib):
+    assert lib.tl_get_device_error(None, None, 0, None) == tl.TL_ERR_INVALID_ARG
+    assert lib.tl_get_device_error(4098, None, 1, None) == tl.TL_ERR_INVALID_ARG  # misaligned
 
 
 def test_workspace_sizes(lib):

@@ -77,3 +77,27 @@ def test_out_of_range_slot_is_skipped_and_reported():
     live[(bad < 0) | (bad >= n_slots)] = -1
     oracle.kv_cache_write(case.k_new, case.v_new, kc, vc, live)
     assert same_bytes(g.k_cache, kc) and same_bytes(g.v_cache, vc)
+
+
+def test_device_error_query_reads_and_clears_the_word():
+    """tl_get_device_error after a write with an out-of-range slot: the slot
+    bit, status TL_ERR_DEVICE_BOUNDS through the C ABI, and a cleared word."""
+    import ctypes
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import _lib
+
+    case = wl.decode_case([20, 33], Hq=4, Hkv=2, d=64, dtype=torch.bfloat16, seed=6)
+    case.slot_mapping[0] = case.num_pages * case.page_size + 3
+    g = on_gpu(case)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_write(g, error_word=err)
+    lib = _lib.load()
+    bits = ctypes.c_uint32(0)
+    st = lib.tl_get_device_error(err.data_ptr(), ctypes.byref(bits), 1,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == tl.TL_ERR_DEVICE_BOUNDS and bits.value == tl.TL_DEVERR_SLOT_RANGE
+    assert int(err.item()) == 0  # cleared
+    st = lib.tl_get_device_error(err.data_ptr(), ctypes.byref(bits), 0, None)
+    assert st == tl.TL_OK and bits.value == 0
+    assert tl.tl_get_device_error(err) == 0
