@@ -221,7 +221,7 @@ class PrefillCase:
 
 def prefill_case(pads, p0, *, T, Hq, Hkv, d, page_size=16, dtype=torch.bfloat16, window=0,
                  seed=0, device="cpu", extra_pages=0, nan_unused=False, scale=None,
-                 max_pages_per_seq=None) -> PrefillCase:
+                 max_pages_per_seq=None, outlier_p=0.0) -> PrefillCase:
     g = _gen(seed, device)
     pads = [int(x) for x in pads]
     p0 = [int(x) for x in p0]
@@ -229,11 +229,11 @@ def prefill_case(pads, p0, *, T, Hq, Hkv, d, page_size=16, dtype=torch.bfloat16,
     lengths = [p0[b] + (T - pads[b]) if T - pads[b] > 0 else p0[b] for b in range(B)]
     pool = make_pool(lengths, page_size, g, extra_pages, max_pages_per_seq)
     shape = (pool.num_pages, page_size, Hkv, d)
-    k_cache = _randn(shape, dtype, g, device)
-    v_cache = _randn(shape, dtype, g, device)
-    q = _randn((B, T, Hq, d), dtype, g, device)
-    k_new = _randn((B * T, Hkv, d), dtype, g, device)
-    v_new = _randn((B * T, Hkv, d), dtype, g, device)
+    k_cache = _randn(shape, dtype, g, device, outlier_p)
+    v_cache = _randn(shape, dtype, g, device, outlier_p)
+    q = _randn((B, T, Hq, d), dtype, g, device, outlier_p)
+    k_new = _randn((B * T, Hkv, d), dtype, g, device, outlier_p)
+    v_new = _randn((B * T, Hkv, d), dtype, g, device, outlier_p)
     positions = torch.full((B, T), -1, dtype=torch.int32)
     slots = torch.full((B * T,), -1, dtype=torch.int64)
     for b in range(B):
@@ -357,12 +357,13 @@ def prefill_rows(seed=0, B=8, T=2048, max_pad=1500, max_p0=6144):
     return pads, p0
 
 
-def batched_prefill(seed=0, device="cpu", B=8, T=2048) -> PrefillCase:
+def batched_prefill(seed=0, device="cpu", B=8, T=2048, outlier_p=0.0) -> PrefillCase:
     """B=8 rows of 2,048 tokens, 0-1,500 left pads, prior context 0-6,144,
-    Hq=32, Hkv=8, d=128, bf16, pages of 16."""
+    Hq=32, Hkv=8, d=128, bf16, pages of 16 (outlier_p: that share of Q, K and
+    V values multiplied by 8, as in the sliding-window mix)."""
     pads, p0 = prefill_rows(seed, B, T)
     return prefill_case(pads, p0, T=T, Hq=32, Hkv=8, d=128, page_size=16,
-                        dtype=torch.bfloat16, seed=seed, device=device)
+                        dtype=torch.bfloat16, seed=seed, device=device, outlier_p=outlier_p)
 
 
 def swa_lengths(seed=0, B=128):

@@ -126,3 +126,107 @@ def permuted_pool(g, seed=123):
 
 def on_gpu(case):
     return wl.to_device(case, DEV)
+
+
+def assert_decode_all(out, q, k_cache, v_cache, block_table, context_lens, scale, window=0,
+                      ring_pages=0, k_scales=None, v_scales=None, chunk=16, what="decode",
+                      new_rows=None):
+    """Every sequence's output against the oracle, `chunk` sequences at a
+    time (host copies of only their pages, their tables renumbered; int8
+    pools bring their scale pages along).  With new_rows = (k_new, v_new,
+    slot_mapping), the pools are those before the step's write and the
+    oracle applies its own write of those rows to its copies first, so no
+    oracle input comes from a GPU kernel.  Returns the worst (abs, rel)."""
+    from tests.parity import assert_close
+
+    if new_rows is not None:
+        kn_all, vn_all, sm_all = (t.cpu() for t in new_rows)
+        sm_list = sm_all.tolist()
+
+    B = q.shape[0]
+    ps = k_cache.shape[1]
+    lens = context_lens.cpu().tolist()
+    bt = block_table.cpu()
+    worst = (0.0, 0.0)
+    view8 = k_cache.dtype == torch.float8_e4m3fn
+    for r0 in range(0, B, chunk):
+        rows = list(range(r0, min(B, r0 + chunk)))
+        n_pages = [ring_pages if ring_pages else (max(lens[b], 0) + ps - 1) // ps for b in rows]
+        pages, tables = [], []
+        for b, n in zip(rows, n_pages):
+            tables.append(list(range(len(pages), len(pages) + n)))
+            pages += bt[b, :n].tolist()
+        idx = torch.tensor(pages or [0], dtype=torch.long, device=k_cache.device)
+        kc = k_cache.index_select(0, idx).cpu()
+        vc = v_cache.index_select(0, idx).cpu()
+        if view8:
+            kc, vc = kc.view(torch.uint8).numpy(), vc.view(torch.uint8).numpy()
+        sub_bt = torch.full((len(rows), max(1, max(len(t) for t in tables))), -1,
+                            dtype=torch.int32)
+        for i, t in enumerate(tables):
+            if t:
+                sub_bt[i, :len(t)] = torch.tensor(t, dtype=torch.int32)
+        qs = q[rows].cpu()
+        cl = torch.tensor([lens[b] for b in rows], dtype=torch.int32)
+        if k_scales is not None:
+            ks = k_scales.index_select(0, idx.to(k_scales.device)).cpu()
+            vs = v_scales.index_select(0, idx.to(v_scales.device)).cpu()
+        if new_rows is not None:
+            # the step's rows that land on this chunk's pages, renumbered
+            where = {pg: i for i, pg in enumerate(pages)}
+            sub_sm = torch.tensor([where[s // ps] * ps + s % ps if s >= 0 and s // ps in where
+                                   else -1 for s in sm_list], dtype=torch.int64)
+            if k_scales is not None:
+                oracle.kv_cache_write_int8(kn_all, vn_all, kc, vc, ks, vs, sub_sm)
+            elif view8:
+                oracle.kv_cache_write_fp8(kn_all, vn_all, kc, vc, sub_sm)
+            else:
+                oracle.kv_cache_write(kn_all, vn_all, kc, vc, sub_sm)
+        if k_scales is not None:
+            ref = oracle.paged_decode_int8(qs, kc, vc, ks, vs, sub_bt, cl, scale, window=window,
+                                           ring_pages=ring_pages)
+        else:
+            ref = oracle.paged_decode(qs, kc, vc, sub_bt, cl, scale, window=window,
+                                      ring_pages=ring_pages)
+        e, r = assert_close(out[rows], ref, f"{what}, sequences {rows[0]}..{rows[-1]}")
+        worst = (max(worst[0], e), max(worst[1], r))
+    return worst
+
+
+def assert_prefill_rows(out, g, rows, window=None, ring_pages=0, what="prefill", pools=None,
+                        new_rows=None):
+    """Every token of the given prefill rows against the oracle's blockwise
+    fold (pads: exactly 0).  pools = (k_cache, v_cache) before the call's
+    write (default: g's), and new_rows = (k_new, v_new, slot_mapping) the
+    rows the oracle writes into its own copies first."""
+    from tests.parity import assert_close
+
+    k_src, v_src = (g.k_cache, g.v_cache) if pools is None else pools
+    ps = k_src.shape[1]
+    w = g.window if window is None else window
+    if new_rows is not None:
+        kn_all, vn_all, sm_all = (t.cpu() for t in new_rows)
+        sm_list = sm_all.tolist()
+    for row in rows:
+        pos = g.positions[row].cpu()
+        last = int(pos.max().item())
+        n = ring_pages if ring_pages else max((last + ps) // ps, 1)
+        kc, vc, bt = sub_pool(k_src, v_src, g.block_table, [row], [n])
+        if new_rows is not None:
+            pages = g.block_table[row, :n].cpu().tolist()
+            where = {pg: i for i, pg in enumerate(pages)}
+            sub_sm = torch.tensor([where[s // ps] * ps + s % ps if s >= 0 and s // ps in where
+                                   else -1 for s in sm_list], dtype=torch.int64)
+            if kc.dtype == torch.float8_e4m3fn:
+                k8, v8 = kc.view(torch.uint8).numpy(), vc.view(torch.uint8).numpy()
+                oracle.kv_cache_write_fp8(kn_all, vn_all, k8, v8, sub_sm)
+            else:
+                oracle.kv_cache_write(kn_all, vn_all, kc, vc, sub_sm)
+        if kc.dtype == torch.float8_e4m3fn:
+            kc, vc = kc.view(torch.uint8).numpy(), vc.view(torch.uint8).numpy()
+        ref = oracle.paged_prefill(g.q[row:row + 1].cpu(), kc, vc, bt, pos.view(1, -1), g.scale,
+                                   window=w, ring_pages=ring_pages)
+        assert_close(out[row], ref, f"{what}, row {row}")
+        dead = (pos < 0).nonzero().flatten().tolist()
+        if dead:
+            assert torch.all(out[row, dead] == 0), f"{what}, row {row}: pads not 0"

@@ -9,7 +9,8 @@ import torch
 import oracle
 import paged_kv_attention_cache_gb300 as tl
 from paged_kv_attention_cache_gb300 import workloads as wl
-from tests.gpu_util import gpu_prefill, gpu_write, on_gpu, oracle_prefill_tokens
+from tests.gpu_util import (assert_prefill_rows, gpu_prefill, gpu_write, on_gpu,
+                            oracle_prefill_tokens)
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -92,6 +93,30 @@ def test_multi_token_decode_kernel(q_len, hq, hkv, d, window):
         pf = gpu_prefill(g)
         torch.cuda.synchronize()
         assert_close(out.cpu(), pf.double().cpu().numpy(), "decode_multi vs prefill")
+
+
+@pytest.mark.parametrize("window", [0, 4096])
+def test_multi_token_decode_outliers_every_token(window):
+    """The multi-token decode on the sliding-window mix's shape and values
+    (H_q=40, H_kv=8, lengths U[1024, 32768], 1% of Q, K and V values x8), 3
+    tokens per sequence: every token against the oracle."""
+    q_len = 3
+    lengths = wl.swa_lengths(seed=2, B=16)
+    p0 = [L - q_len for L in lengths]
+    case = wl.prefill_case([0] * len(lengths), p0, T=q_len, Hq=40, Hkv=8, d=128, seed=45,
+                           window=window, outlier_p=0.01, device=DEV)
+    g = on_gpu(case)
+    k0, v0 = g.k_cache.clone(), g.v_cache.clone()
+    gpu_write(g)
+    cl = torch.tensor(lengths, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tl.tl_paged_attn_decode_multi(g.q, g.k_cache, g.v_cache, g.block_table, cl, g.scale,
+                                        window=window, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_prefill_rows(out, g, range(case.B), pools=(k0, v0),
+                        new_rows=(g.k_new, g.v_new, g.slot_mapping),
+                        what=f"multi-token outliers w{window}")
 
 
 def test_multi_token_decode_refuses_too_many_rows():

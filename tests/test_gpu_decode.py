@@ -1,5 +1,5 @@
 """PAGED_ATTENTION decode on the GPU against the oracle: the five workloads at
-full size (sampled sequences), edge cases, invariants, device-side checks."""
+full size (every sequence), edge cases, invariants, device-side checks."""
 import numpy as np
 import pytest
 import torch
@@ -7,8 +7,7 @@ import torch
 import oracle
 import paged_kv_attention_cache_gb300 as tl
 from paged_kv_attention_cache_gb300 import workloads as wl
-from tests.gpu_util import (gpu_decode, gpu_write, on_gpu, oracle_decode_rows, permuted_pool,
-                            sample_rows)
+from tests.gpu_util import assert_decode_all, gpu_decode, gpu_write, on_gpu, permuted_pool
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -31,24 +30,32 @@ def test_tiny_f32_all_outputs():
     assert_close(out, ref, "tiny f32")
 
 
-@pytest.mark.parametrize("maker,n", [(wl.llama8b_decode, 10), (wl.longctx_decode, 8)])
-def test_full_size_workloads_sampled(maker, n):
-    case = maker(seed=0, device="cuda")
-    g, out = _write_then_decode(case)
-    rows = sample_rows(case.context_lens.tolist(), n)
-    ref = oracle_decode_rows(g, rows)
-    assert_close(out[rows], ref, maker.__name__)
+def _step_every_sequence(case, what):
+    """The step (write of the new rows, then decode) on the GPU; the oracle
+    writes the same rows into its own copies of the pools as they were before
+    the step, then attends; every sequence compared."""
+    g = on_gpu(case)
+    k0, v0 = g.k_cache.clone(), g.v_cache.clone()
+    gpu_write(g)
+    out = gpu_decode(g)
+    torch.cuda.synchronize()
     assert torch.isfinite(out).all()
+    assert_decode_all(out, g.q, k0, v0, g.block_table, g.context_lens, g.scale,
+                      window=case.window, new_rows=(g.k_new, g.v_new, g.slot_mapping), what=what)
+
+
+@pytest.mark.parametrize("maker", [wl.llama8b_decode, wl.longctx_decode])
+def test_full_size_workloads_every_sequence(maker):
+    _step_every_sequence(maker(seed=0, device="cuda"), maker.__name__)
 
 
 @pytest.mark.parametrize("layer", [0, 1])
-def test_sliding_window_mix_sampled(layer):
+def test_sliding_window_mix_every_sequence(layer):
+    """Both layers of the sliding-window mix (separate pools, window 4,096 then
+    full attention, 1% of Q, K and V values x8), every sequence."""
     case = wl.swa_decode(seed=0, device="cuda", layer=layer)
     assert case.window == (4096 if layer == 0 else 0)
-    g, out = _write_then_decode(case)
-    rows = sample_rows(case.context_lens.tolist(), 6, seed=layer)
-    ref = oracle_decode_rows(g, rows)
-    assert_close(out[rows], ref, f"swa layer {layer}")
+    _step_every_sequence(case, f"swa layer {layer}")
 
 
 EDGE_LENGTHS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 2047, 2048, 2049, 5000]
@@ -159,7 +166,7 @@ def test_piece_plan_extremes(shape):
     small pieces (the last ~15% of every sequence longer than 256 keys), all
     within ceil(12288 / H_kv) + 2B pieces.  Batches at the ends of that range
     (thousands of short sequences, one very long one, both mixed) against the
-    oracle on sampled sequences, every output finite and no device error."""
+    oracle on every sequence, every output finite and no device error."""
     g = torch.Generator().manual_seed(91)
     if shape == "many_short":
         lens = torch.randint(1, 400, (2048,), generator=g).tolist()
@@ -174,6 +181,5 @@ def test_piece_plan_extremes(shape):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.isfinite(out).all()
-    rows = sample_rows(lens, 6, seed=3)
-    ref = oracle_decode_rows(g_, rows)
-    assert_close(out[rows], ref, f"piece plan {shape}")
+    assert_decode_all(out, g_.q, g_.k_cache, g_.v_cache, g_.block_table, g_.context_lens,
+                      g_.scale, chunk=256, what=f"piece plan {shape}")

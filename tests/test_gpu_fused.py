@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_kv_attention_cache_gb300 as tl
 from paged_kv_attention_cache_gb300 import workloads as wl
-from tests.gpu_util import oracle_decode_rows, on_gpu, sample_rows
+from tests.gpu_util import assert_decode_all, on_gpu
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -85,13 +85,11 @@ def test_fused_over_e4m3_pools(src):
     v8 = g.v_cache.float().to(torch.float8_e4m3fn)
     res = _both(g, k8, v8, g.k_new.to(src), g.v_new.to(src), g.slot_mapping)
     _same(res)
-    rows = sample_rows(case.context_lens.tolist(), 4)
-    out = res[1][0]
-    kc = res[1][1].view(torch.uint8).cpu().numpy()
-    vc = res[1][2].view(torch.uint8).cpu().numpy()
-    ref = oracle.paged_decode(case.q[rows], kc, vc, case.block_table[rows],
-                              case.context_lens[rows], case.scale)
-    assert_close(out[rows], ref, f"fused e4m3 from {src}")
+    # every sequence: the oracle converts the same new rows into its own
+    # copies of the pools as they were before the call, then attends
+    assert_decode_all(res[1][0], g.q, k8, v8, g.block_table, g.context_lens, g.scale,
+                      new_rows=(g.k_new.to(src), g.v_new.to(src), g.slot_mapping),
+                      what=f"fused e4m3 from {src}")
 
 
 def test_fused_reports_a_bad_slot_and_skips_pads():

@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_kv_attention_cache_gb300 as tl
 from paged_kv_attention_cache_gb300 import workloads as wl
-from tests.gpu_util import sample_rows
+from tests.gpu_util import assert_decode_all, sample_rows
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -114,10 +114,16 @@ def test_int8_decode_ignores_the_garbage_of_unread_slots():
     assert torch.isfinite(out).all()
 
 
-def test_int8_decode_llama8b_shape_sampled():
-    case = wl.llama8b_decode(seed=5)
-    rows = sample_rows(case.context_lens.tolist(), 6, seed=5)
-    _check(case, wl.int8_pools(case, 98), 0, rows=rows, what="int8 llama8b B=64")
+def test_int8_decode_llama8b_shape_every_sequence():
+    case = wl.llama8b_decode(seed=5, device=DEV)
+    pools = [t.to(DEV) for t in wl.int8_pools(case, 98)]
+    err = _err()
+    out = tl.tl_paged_attn_decode_int8(case.q, *pools, case.block_table.to(DEV),
+                                       case.context_lens.to(DEV), case.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_decode_all(out, case.q, pools[0], pools[1], case.block_table, case.context_lens,
+                      case.scale, k_scales=pools[2], v_scales=pools[3], what="int8 llama8b B=64")
 
 
 def test_int8_decode_reports_a_query_beyond_fp16():

@@ -9,7 +9,7 @@ import torch
 import oracle
 import paged_kv_attention_cache_gb300 as tl
 from paged_kv_attention_cache_gb300 import workloads as wl
-from tests.gpu_util import gpu_write, on_gpu, sample_rows, sub_pool
+from tests.gpu_util import assert_decode_all, gpu_write, on_gpu
 from tests.parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -75,14 +75,16 @@ def test_decode_ring_that_cannot_hold_the_window_is_refused():
         assert e.value.status == tl.TL_ERR_INVALID_ARG
 
 
-def _prefill_inputs(c, p0, n, pads, seed):
+def _prefill_inputs(c, p0, n, pads, seed, outlier_p=0.0):
     B, T = len(p0), n + max(pads)
     positions = torch.full((B, T), -1, dtype=torch.int32)
     for b in range(B):
         positions[b, T - n:] = torch.arange(p0[b], p0[b] + n, dtype=torch.int32)
     g = torch.Generator(device=DEV).manual_seed(seed)
-    q = torch.randn((B, T, c.Hq, c.d), generator=g, device=DEV).to(c.dtype)
-    return q, positions.to(DEV)
+    q = torch.randn((B, T, c.Hq, c.d), generator=g, device=DEV)
+    if outlier_p > 0:  # that share of the values x8, as in the sliding-window mix
+        q = torch.where(torch.rand(q.shape, generator=g, device=DEV) < outlier_p, q * 8, q)
+    return q.to(c.dtype), positions.to(DEV)
 
 
 def test_prefill_chunk_through_a_ring_equals_full_history_bit_for_bit():
@@ -112,6 +114,26 @@ def test_prefill_chunk_through_a_ring_equals_full_history_bit_for_bit():
         assert_close(ring_out[b, ts], ref, f"ring prefill row {b}")
 
 
+def test_prefill_ring_with_outliers_every_token():
+    """A sliding layer's prefill chunk (window 4,096) through rings, on the
+    sliding-window mix's value distribution (1% of Q, K and V values x8):
+    every token against the oracle's ring form."""
+    window, n, ps = 4096, 512, 16
+    p0 = [0, 3000, 9000, 20000]
+    ring = oracle.ring_pages(window, n, ps)
+    c = _ring_case([p + n for p in p0], window=window, ring_pages=ring, Hq=40, Hkv=8, d=128,
+                   page_size=ps, dtype=torch.bfloat16, seed=38, outlier_p=0.01)
+    q, positions = _prefill_inputs(c, p0, n, pads=[0, 5, 0, 9], seed=39, outlier_p=0.01)
+    err = _err()
+    out = tl.tl_paged_attn_prefill_ring(q, c.ring_k, c.ring_v, c.ring_table, positions, c.scale,
+                                        window, ring, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.paged_prefill(q.cpu(), c.ring_k.cpu(), c.ring_v.cpu(), c.ring_table.cpu(),
+                               positions.cpu(), c.scale, window=window, ring_pages=ring)
+    assert_close(out.reshape(ref.shape), ref, "ring prefill with outliers")
+
+
 def test_prefill_ring_one_page_short_is_reported():
     window, n, ps = 300, 200, 16
     p0 = [3000]  # the call spans W - 1 + n = 499 positions > (32 - 1) * 16
@@ -126,18 +148,21 @@ def test_prefill_ring_one_page_short_is_reported():
     assert int(err.item()) & tl.TL_DEVERR_CONTEXT_RANGE
 
 
-def test_full_size_sliding_layer_over_rings_sampled():
+def test_full_size_sliding_layer_over_rings_every_sequence():
+    """The sliding layer of the mix (B=128, window 4,096) over rings of 257
+    pages, the step's new rows written first: every sequence against the
+    oracle's ring form (the oracle writes the rows into its own copies of
+    the rings as they were before the step)."""
     case = wl.swa_ring_decode(seed=0, device=DEV)
     ring = case.extra["ring_pages"]
     g = on_gpu(case)
+    k0, v0 = g.k_cache.clone(), g.v_cache.clone()
     gpu_write(g)
     err = _err()
     out = tl.tl_paged_attn_decode_ring(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
                                        g.scale, g.window, ring, error_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    rows = sample_rows(case.context_lens.tolist(), 10)
-    kc, vc, bt = sub_pool(g.k_cache, g.v_cache, g.block_table, rows, [ring] * len(rows))
-    ref = oracle.paged_decode(g.q[rows].cpu(), kc, vc, bt, case.context_lens[rows], g.scale,
-                              window=g.window, ring_pages=ring)
-    assert_close(out[rows], ref, "sliding layer over rings")
+    assert_decode_all(out, g.q, k0, v0, g.block_table, g.context_lens, g.scale,
+                      window=g.window, ring_pages=ring,
+                      new_rows=(g.k_new, g.v_new, g.slot_mapping), what="sliding layer over rings")
