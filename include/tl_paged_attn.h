@@ -332,9 +332,11 @@ tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const
  * kernel's work counter (256 bytes), the key-tile count and the schedule of
  * every query-tile pair (two int32 arrays of B * n_pairs entries, each
  * rounded up to 256 bytes; n_pairs = ceil(T / (2 * floor(128 / (h_q/h_kv))))),
- * each row's first key (B int32, rounded up to 256 bytes), and an fp16 copy of
- * the V rows the call reads, [B][h_kv][max_pages_per_seq * page_size][d]
- * (B * h_kv * max_pages_per_seq * page_size * d * 2 bytes).
+ * each row's first key (B int32, rounded up to 256 bytes), a flag per 64 keys
+ * of each row (B * ceil(max_pages_per_seq * page_size / 64) int32, rounded up
+ * to 256 bytes), a flag per row (B int32, rounded up to 256 bytes), and an
+ * fp16 copy of the V rows the call reads, [B][h_kv][max_pages_per_seq *
+ * page_size][d] (B * h_kv * max_pages_per_seq * page_size * d * 2 bytes).
  */
 size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
                                             int32_t d, int32_t max_pages_per_seq,
@@ -374,14 +376,17 @@ size_t tl_paged_attn_prefill_workspace_size_ex(int32_t B, int32_t T, int32_t h_q
  * h_q % h_kv == 0 with h_q/h_kv <= 128, page_size a power of two in
  * [8, 128].  Otherwise TL_ERR_UNSUPPORTED.
  * scale must be positive and finite (TL_ERR_INVALID_ARG otherwise).
- * Arithmetic: Q.K^T with bf16 operands and f32 accumulation; P.V with P
- * rounded to fp16 and V converted bf16 -> fp16 (exact for |v| in
- * [2^-14, 65504]; smaller magnitudes land on fp16's subnormal grid, a change
- * below 2^-25), f32 accumulation, and the softmax sum taken over the same
- * rounded P, so each output is a convex combination of V rows with weights
- * within 2^-11 relative of the exact ones.  A finite V entry beyond +-65504
- * in a key range the call reads sets TL_DEVERR_VALUE_RANGE and leaves the
- * outputs undefined.
+ * Arithmetic: Q.K^T with bf16 operands and f32 accumulation; P.V with V
+ * converted bf16 -> fp16 (exact for |v| in [2^-14, 65504]; smaller
+ * magnitudes land on fp16's subnormal grid, a change below 2^-25) and f32
+ * accumulation.  For a row whose V (in the keys the call reads) holds no
+ * value of magnitude above 8, P is rounded to fp16 and the softmax sum is
+ * taken over the same rounded P, so each output is a convex combination of
+ * V rows with weights within 2^-11 relative of the exact ones; any other row
+ * takes P as the sum of two fp16 parts (a second P.V product, about 22
+ * significant bits), so a large |v| does not magnify the rounding.  A finite
+ * V entry beyond +-65504 in a key range the call reads sets
+ * TL_DEVERR_VALUE_RANGE and leaves the outputs undefined.
  */
 tl_status tl_paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int32_t max_pages_per_seq,

@@ -5,15 +5,19 @@
 // keys are folded block by block into a running max, sum and P.V, so no score
 // tensor wider than one tile exists).
 //
-// Three launches, the last two programmatic dependents of their predecessor
+// Four launches, the last three programmatic dependents of their predecessor
 // (resident while it finishes, waiting for its results).  A pre-pass converts
 // the V rows each row's tokens can see from the bf16 pages to fp16, once,
 // into the workspace, laid out as [row][KV head][key][d] (exact for |v| in
 // [2^-14, 65504]; larger finite values are reported; keys past the row's
-// last position are zeros), and counts each query-tile pair's key tiles; a
-// one-CTA plan orders the pairs heaviest first.  Then the persistent
-// attention kernel (one CTA per SM) takes work items (pair of query tiles,
-// KV head, row) and runs them on the 5th-generation tensor core.  A query tile packs tokens_per_tile =
+// last position are zeros), notes whether any of them exceeds 8 in
+// magnitude, and counts each query-tile pair's key tiles; a one-CTA plan
+// orders the pairs heaviest first and sets each row's flag.  Then the
+// persistent attention kernel (one CTA per SM) takes work items (pair of
+// query tiles, KV head, row) and runs them on the 5th-generation tensor
+// core: once for the rows without a flag (P as one fp16 value), then once
+// for the flagged rows (P as the sum of two fp16 parts), each launch
+// skipping the other's rows.  A query tile packs tokens_per_tile =
 // 128/group consecutive tokens of one row with all `group` query heads that
 // share the KV head, as the 128 M rows (row r = token r/group, head
 // r%group); the CTA holds two consecutive tiles (Q0, Q1), so every K/V tile
@@ -81,6 +85,11 @@ struct PrefillParams {
   int32_t ring_pages;    // > 0: the table's first ring_pages entries are a ring
   int32_t kv8;           // e4m3 pools: K is read from a bf16 copy like V
   uint16_t* ws_k;        // e4m3 pools: the bf16 copy of K, laid out like the V copy
+  int32_t* ctrl;         // [0], [1] work counters of the two attention kernels,
+                         // [2] first work item of the flagged rows
+  int32_t cvt_gx;        // pre-pass CTAs per row (64-key tiles of the V copy)
+  int32_t* cta_big;      // [B][cvt_gx] 1: the pre-pass CTA saw a V value with |v| > 8
+  int32_t* row_big;      // [B] 1: the row reads a V value with |v| > 8 (P split in two)
 };
 
 // Position bound of the call: the table width, or none for a ring (whose
@@ -108,22 +117,27 @@ constexpr int kTcQBytes = 32768;     // one query tile: 128 rows x 128 d x bf16
 constexpr int kTcKVBytes = kBN * 256;  // 128 keys x 128 d x 16-bit (two 16 KiB halves)
 constexpr int kTcSmem = kTcQB * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
 constexpr int kPlanThreads = 1024;
-constexpr int kPlanBuckets = 8192;   // key-tile counts at or above 8191 share the last bucket
+constexpr int kPlanBuckets = 8192;   // two halves (rows without and with the split-P flag);
+                                     // key-tile counts at or above 4095 share a half's last bucket
 
 // Workspace layout: [counter | pair_tiles | order | row_start | fp16 V
 // (| bf16 K for e4m3 pools)], each part 256-byte aligned; the copies are
 // [B][h_kv][v_keys][128].
 struct WsLayout {
-  size_t tiles, order, rows, v, k, total;
+  size_t tiles, order, rows, cta_big, row_big, v, k, total;
 };
+constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
 inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_keys, bool kv8) {
   const size_t pairs = (size_t)(B * n_pairs) * 4;
   const size_t copy = (size_t)B * h_kv * (size_t)v_keys * 128 * 2;
+  const size_t gx = (size_t)((v_keys + kCvtKeys - 1) / kCvtKeys);
   WsLayout L;
   L.tiles = 256;
   L.order = L.tiles + align_up(pairs, 256);
   L.rows = L.order + align_up(pairs, 256);
-  L.v = L.rows + align_up((size_t)B * 4, 256);
+  L.cta_big = L.rows + align_up((size_t)B * 4, 256);
+  L.row_big = L.cta_big + align_up((size_t)B * gx * 4, 256);
+  L.v = L.row_big + align_up((size_t)B * 4, 256);
   L.k = L.v + copy;
   L.total = L.k + (kv8 ? copy : 0);
   return L;
@@ -140,6 +154,13 @@ constexpr float kRescaleLog2 = 8.f;
 // [65536, max finite]; 65280 (0x477F) is the largest bf16 below fp16's
 // overflow threshold.
 constexpr uint32_t kBf16TooBig = 0x4780u, kBf16Inf = 0x7F80u;
+// A row whose V holds a value of magnitude above 8 (bf16 bits 0x4100, e4m3
+// code 0x50, sign cleared; NaN and infinities included) takes P.V with P
+// split into two fp16 parts.  P rounded once to fp16 moves an output by up
+// to 2^-11 * max |v_j - o|: far below 1e-3 for V of N(0,1) scale (|v| < 8),
+// but up to several 1e-3 for values beyond 8; hi + lo carries about 22
+// significant bits.
+constexpr uint32_t kBf16Big = 0x4100u, kE4m3Big = 0x50u;
 
 struct TcShared {
   unsigned long long q_full[kTcQB], q_free[kTcQB];
@@ -240,7 +261,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 constexpr int kCvtUnroll = 8;
 constexpr int kCvtBlocksPerSm = 4;  // register bound: the scan and page-lookup phases of
                                     // one CTA overlap the copies of the others
-constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
 
 // Two e4m3 codes (low byte first) as an fp16 pair, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
@@ -262,7 +282,10 @@ template <bool KV8>
 __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int* counter) {
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *counter = 0;  // work items
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    counter[0] = 0;  // work items of the single-fp16 attention kernel
+    counter[1] = 0;  // and of the split-P one
+  }
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   __shared__ int s_page[kCvtKeys];  // page of each key of the tile; -1: write zeros
   const int b = (int)blockIdx.y;
@@ -316,8 +339,10 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     pmin = min(pmin, s_min[w]);
     pmax = max(pmax, s_max[w]);
   }
+  int32_t* big_flag = P.cta_big + (size_t)b * P.cvt_gx + blockIdx.x;
   if (pmax < 0) {  // no live token: the attention kernel reads nothing
     if (blockIdx.x == 0 && threadIdx.x == 0) P.row_start[b] = 0;
+    if (threadIdx.x == 0) *big_flag = 0;
     return;
   }
   const int lo = (P.window > 0 && pmin - P.window + 1 > 0) ? pmin - P.window + 1 : 0;
@@ -331,7 +356,10 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
       report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
   }
   const int k0 = start + (int)blockIdx.x * kCvtKeys;  // this CTA's keys of the copy
-  if (k0 >= end) return;
+  if (k0 >= end) {
+    if (threadIdx.x == 0) *big_flag = 0;
+    return;
+  }
   for (int r = threadIdx.x; r < kCvtKeys; r += kCvtThreads) {
     const int k = k0 + r;
     int page = -1;  // keys past pmax: zeros
@@ -349,6 +377,7 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
   const int units = P.h_kv * 16;                                // 16-byte units per key
   const int total = (r1 - r0) * units;
   uint32_t vmax = 0;  // max |bf16 bits| seen, per half-word
+  uint32_t cmax = 0;  // e4m3 pools: max |code| seen, per byte
   // units of 8 elements: 16 bytes of a bf16 row, 8 bytes of an e4m3 row
   for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
     uint4 x[kCvtUnroll];  // bf16 V, or (e4m3) V in .x.y and K in .z.w
@@ -382,6 +411,7 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
             (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 + (u & 15) * 8;
         uint4 y = x[i];
         if (KV8) {  // e4m3 values are exact in both fp16 and bf16
+          cmax = __vmaxu4(cmax, __vmaxu4(y.x & 0x7f7f7f7fu, y.y & 0x7f7f7f7fu));
           *reinterpret_cast<uint4*>(ws + dst) =
               make_uint4(e4m3x2_to_f16x2(y.x), e4m3x2_to_f16x2(y.x >> 16),
                          e4m3x2_to_f16x2(y.y), e4m3x2_to_f16x2(y.y >> 16));
@@ -401,25 +431,53 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
   const uint32_t m0 = vmax & 0xffffu, m1 = vmax >> 16;
   if ((m0 >= kBf16TooBig && m0 < kBf16Inf) || (m1 >= kBf16TooBig && m1 < kBf16Inf))
     report(P.error_word, TL_DEVERR_VALUE_RANGE);
+  cmax = __vmaxu4(cmax, cmax >> 16);
+  cmax = __vmaxu4(cmax, cmax >> 8);
+  const bool big = m0 > kBf16Big || m1 > kBf16Big || (cmax & 0xffu) > kE4m3Big;
+  const int any_big = __syncthreads_or(big);
+  if (threadIdx.x == 0) *big_flag = any_big ? 1 : 0;
 }
 
 // ------------------------------------------------------------ plan --
-// One CTA: counting sort of the pairs by key tiles, most first (pairs with
-// no live token last), into P.order.  Ties keep no particular order; every
+// One CTA.  Each row's split-P flag (any of its pre-pass CTAs saw |v| > 8);
+// then a counting sort of the pairs into P.order: the pairs of rows without
+// the flag first, then those of flagged rows, each group by key tiles, most
+// first (pairs with no live token last).  ctrl[2] = the first work item of
+// the flagged rows: the single-fp16 attention kernel takes the items before
+// it, the split-P kernel the rest.  Ties keep no particular order; every
 // pair computes the same bits whichever CTA takes it and when.
+__device__ __forceinline__ int plan_bucket(const PrefillParams& P, int e) {
+  constexpr int kHalf = kPlanBuckets / 2;
+  const int t = min(P.pair_tiles[e], kHalf - 1);
+  return __ldcg(P.row_big + e / P.n_pairs) ? t : kHalf + t;  // a higher bucket goes first
+}
+
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PrefillParams P) {
   __shared__ int cur[kPlanBuckets];  // counts, then each bucket's next slot
   __shared__ int wsum[kPlanThreads / 32];
+  __shared__ int n_flagged;
   constexpr int kPer = kPlanBuckets / kPlanThreads;  // buckets per thread
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, n_e = P.B * P.n_pairs;
   for (int k = tid; k < kPlanBuckets; k += kPlanThreads) cur[k] = 0;
+  if (tid == 0) n_flagged = 0;
   // the pre-pass (this grid's predecessor) writes the pair counts; the
   // attention kernel may launch now and waits for this grid in turn
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   __syncthreads();
-  for (int e = tid; e < n_e; e += kPlanThreads)
-    atomicAdd(&cur[min(P.pair_tiles[e], kPlanBuckets - 1)], 1);
+  // each row's flag, a warp per row
+  for (int b = wid; b < P.B; b += kPlanThreads / 32) {
+    int any = 0;
+    for (int x = lane; x < P.cvt_gx; x += 32) any |= __ldcg(P.cta_big + (size_t)b * P.cvt_gx + x);
+    any = __reduce_or_sync(0xffffffffu, any);
+    if (lane == 0) {
+      P.row_big[b] = any ? 1 : 0;
+      if (any) atomicAdd(&n_flagged, 1);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) P.ctrl[2] = (P.B - n_flagged) * P.n_pairs * P.h_kv;
+  for (int e = tid; e < n_e; e += kPlanThreads) atomicAdd(&cur[plan_bucket(P, e)], 1);
   __syncthreads();
   // slots go to the buckets from the top down: thread t owns buckets
   // [kPer t, kPer t + kPer); above = the pairs in the buckets of higher
@@ -453,8 +511,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PrefillParam
     above += c;
   }
   __syncthreads();
-  for (int e = tid; e < n_e; e += kPlanThreads)
-    P.order[atomicAdd(&cur[min(P.pair_tiles[e], kPlanBuckets - 1)], 1)] = e;
+  for (int e = tid; e < n_e; e += kPlanThreads) P.order[atomicAdd(&cur[plan_bucket(P, e)], 1)] = e;
 }
 
 // S_a = Q_a K^T into TMEM columns [128a, 128a+128): eight K=16 steps over
@@ -471,13 +528,64 @@ __device__ __forceinline__ void tc_issue_s(uint32_t tmem, int a, uint32_t kbase,
   tc::commit(s_full_a);
 }
 // O_a (+)= P_a V in fp16: P_a from TMEM (keys [16k, 16k+16) in columns
-// [8k, 8k+8) of S_a), V MN-major from shared memory.
-__device__ __forceinline__ void tc_issue_pv(uint32_t tmem, int a, uint32_t vbase, bool acc) {
+// [8k, 8k+8) of S_a), V MN-major from shared memory.  With `split`, P is
+// hi + lo: keys [16k, 16k+16) have hi in columns 32 (k/2) + 8 (k%2) + [0, 8)
+// and lo 16 columns further, and both products are accumulated.
+__device__ __forceinline__ void tc_issue_pv(uint32_t tmem, int a, uint32_t vbase, bool acc,
+                                            bool split) {
   const uint32_t idPV = tc::idesc_f16(128, 128, 0, 1);
+  if (!split) {
 #pragma unroll
-  for (int k = 0; k < kBN / 16; ++k)
-    tc::mma_ts(tmem + 256 + a * 128, tmem + a * 128 + 8 * k,
-               tc::sdesc(vbase + k * 2048, kTcKVBytes / 2, 1024), idPV, (acc || k > 0) ? 1u : 0u);
+    for (int k = 0; k < kBN / 16; ++k)
+      tc::mma_ts(tmem + 256 + a * 128, tmem + a * 128 + 8 * k,
+                 tc::sdesc(vbase + k * 2048, kTcKVBytes / 2, 1024), idPV,
+                 (acc || k > 0) ? 1u : 0u);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kBN / 16; ++k) {
+      const uint32_t col = tmem + a * 128 + 32 * (k >> 1) + 8 * (k & 1);
+      const uint64_t vd = tc::sdesc(vbase + k * 2048, kTcKVBytes / 2, 1024);
+      tc::mma_ts(tmem + 256 + a * 128, col, vd, idPV, (acc || k > 0) ? 1u : 0u);
+      tc::mma_ts(tmem + 256 + a * 128, col + 16, vd, idPV, 1u);
+    }
+  }
+}
+
+// The P of one row of a score tile when the row's V holds a value of
+// magnitude above 8: P = hi + lo, both fp16.  Keys [32q, 32q + 32) put hi in
+// columns [32q, 32q + 16) of the tile's S columns (taddr: this thread's lane
+// at the first of them) and the remainder lo in [32q + 16, 32q + 32), the
+// columns of their own scores, so each chunk of scores is reread just before
+// its P replaces it.  Returns the row's sum of the unrounded f32 values.
+__device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int cmax, bool all_live,
+                                               float sc, float base) {
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
+#pragma unroll 1
+  for (int q = 0; q < kBN / 32; ++q) {
+    float x[32];
+    tc::ld32(taddr + 32 * q, x);
+    tc::wait_ld();
+    if (!all_live) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        x[c] = (32 * q + c >= cmin && 32 * q + c <= cmax) ? x[c] : -INFINITY;
+    }
+    uint32_t pk[16], pl[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float y0, y1, h0, h1;
+      fma_f32x2(x[2 * i], x[2 * i + 1], sc2, nb2, y0, y1);
+      const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
+      pk[i] = pack_f16x2(e0, e1);
+      unpack_f16x2(pk[i], h0, h1);
+      pl[i] = pack_f16x2(e0 - h0, e1 - h1);
+      ls[i & 3] += e0 + e1;
+    }
+    tc::st16(taddr + 32 * q, pk);
+    tc::st16(taddr + 32 * q + 16, pl);
+  }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
 // One work item: a pair of query tiles of one row and KV head.  Item idx is
@@ -506,16 +614,16 @@ __device__ __forceinline__ TcItem tc_item(const PrefillParams& P, int idx, int t
 // CTA aborts.  Warp 0 takes items from the global counter into a ring of
 // kItemSlots slots; the MMA and softmax warps read them (lane 0 frees the
 // slot).
-__device__ __forceinline__ int tc_fetch(TcShared& sh, uint32_t seq, int* counter, int n_items,
-                                        volatile int* abort_flag) {
+__device__ __forceinline__ int tc_fetch(TcShared& sh, uint32_t seq, int* counter, int i_begin,
+                                        int i_end, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   const uint32_t slot = seq % kItemSlots, ph = (seq / kItemSlots) & 1;
   int idx = -1;
   if (threadIdx.x < 32) {
     if (!mbar_wait(smem_u32(&sh.item_empty[slot]), ph ^ 1, abort_flag)) return -1;
     if (lane == 0) {
-      const int v = atomicAdd(counter, 1);
-      sh.item[slot] = v < n_items ? v : -1;
+      const int v = i_begin + atomicAdd(counter, 1);
+      sh.item[slot] = v < i_end ? v : -1;
       mbar_arrive(smem_u32(&sh.item_full[slot]));
     }
     if (!mbar_wait(smem_u32(&sh.item_full[slot]), ph, abort_flag)) return -1;
@@ -535,6 +643,7 @@ __device__ __forceinline__ int tc_fetch(TcShared& sh, uint32_t seq, int* counter
 // s-th tile of this CTA, s = 2 x item + a, lives in buffer s % kTcQB), and a
 // finished tile's buffer stages its output for the TMA stores before the
 // tile three steps later is loaded into it.
+template <bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
@@ -552,6 +661,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_pairs = (P.T + 2 * tpt - 1) / (2 * tpt);
   const int n_items = n_pairs * P.B * P.h_kv;
   const int64_t cap = position_cap(P);
+  if (SPLIT) {
+    // the split-P kernel has work only when some row is flagged: read the
+    // plan's first flagged item before any set-up
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (__ldcg(P.ctrl + 2) >= n_items) return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcQB; ++i) {
@@ -587,9 +702,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = sh.tmem_base;
-  // launched as a programmatic dependent of the plan kernel: the workspace
-  // (work counter, schedule, V copy) is read only after this wait
+  // launched as a programmatic dependent of the plan kernel (the split-P
+  // kernel: of the single-fp16 one): the workspace (work counter, schedule,
+  // V copy, row flags) is read only after this wait
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // the split-P kernel may launch now: its CTAs take the SMs this kernel's
+  // CTAs leave, and it waits for this grid in turn
+  if (!SPLIT) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // this kernel's work items: those of rows without the split-P flag, or
+  // those of flagged rows (the plan puts them last)
+  const int first_split = __ldcg(P.ctrl + 2);
+  const int i_begin = SPLIT ? first_split : 0, i_end = SPLIT ? n_items : first_split;
 
   if (warp == 0) {
     // ------------------------------------------------------ K / V producer
@@ -617,7 +740,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     q_issued = __shfl_sync(0xffffffffu, q_issued, 0);                                           \
   }
     for (uint32_t seq = 0; ok; ++seq) {
-      const int idx = tc_fetch(sh, seq, counter, n_items, abort_flag);
+      const int idx = tc_fetch(sh, seq, counter, i_begin, i_end, abort_flag);
       if (idx < 0) break;
       const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
       if (it.rg.kmax < 0) continue;
@@ -696,11 +819,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #define issue_s(a, kt, qbuf) \
   tc_issue_s(tmem, (a), sK + ((kt) % kTcKS) * kTcKVBytes, sQ + (qbuf) * kTcQBytes, \
              smem_u32(&sh.s_full[(a)]))
-#define issue_pv(a, vt, acc) tc_issue_pv(tmem, (a), sV + ((vt) % kTcVS) * kTcKVBytes, (acc))
+#define issue_pv(a, vt, acc) \
+  tc_issue_pv(tmem, (a), sV + ((vt) % kTcVS) * kTcKVBytes, (acc), SPLIT)
     uint32_t kt = 0, vt = 0, tiles = 0, n = 0;  // K / V tiles, S tiles, live items
     bool ok = true;
     for (uint32_t seq = 0; ok; ++seq) {
-      const int idx = tc_fetch(sh, seq, counter, n_items, abort_flag);
+      const int idx = tc_fetch(sh, seq, counter, i_begin, i_end, abort_flag);
       if (idx < 0) break;
       const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
       if (it.rg.kmax < 0) continue;
@@ -783,7 +907,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t tiles = 0, n = 0;
     bool ok = true;
     for (uint32_t seq = 0; ok; ++seq) {
-      const int idx = tc_fetch(sh, seq, counter, n_items, abort_flag);
+      const int idx = tc_fetch(sh, seq, counter, i_begin, i_end, abort_flag);
       if (idx < 0) break;
       const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
       const int ta0 = it.t0 + a * tpt;  // first token of this tile
@@ -850,17 +974,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // at once; the sum widens each fp16 half inside its add.
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
+        if constexpr (!SPLIT) {
 #pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) {
-          uint32_t pk[16];
+          for (int q = 0; q < kBN / 32; ++q) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float y0, y1;
-            fma_f32x2(s[q * 32 + 2 * i], s[q * 32 + 2 * i + 1], sc2, nb2, y0, y1);
-            pk[i] = pack_f16x2(fast_exp2(y0), fast_exp2(y1));
-            ls[i & 3] = add_f16x2_halves(ls[i & 3], pk[i]);
+            for (int i = 0; i < 16; ++i) {
+              float y0, y1;
+              fma_f32x2(s[q * 32 + 2 * i], s[q * 32 + 2 * i + 1], sc2, nb2, y0, y1);
+              pk[i] = pack_f16x2(fast_exp2(y0), fast_exp2(y1));
+              ls[i & 3] = add_f16x2_halves(ls[i & 3], pk[i]);
+            }
+            tc::st16(tmem + lane_base + colS + q * 16, pk);
           }
-          tc::st16(tmem + lane_base + colS + q * 16, pk);
+        } else {
+          ls[0] = tc_softmax_split(tmem + lane_base + colS, cmin, cmax, all_live, sc, base);
         }
         l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         if (__any_sync(0xffffffffu, need)) {
@@ -1034,6 +1162,10 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   P.v_keys = (int32_t)v_keys;
   P.kv8 = kv8 ? 1 : 0;
   P.ws_k = kv8 ? reinterpret_cast<uint16_t*>(wsb + L.k) : nullptr;
+  P.ctrl = counter;
+  P.cvt_gx = (int32_t)((v_keys + kCvtKeys - 1) / kCvtKeys);
+  P.cta_big = reinterpret_cast<int32_t*>(wsb + L.cta_big);
+  P.row_big = reinterpret_cast<int32_t*>(wsb + L.row_big);
   CUtensorMap qmap, kmap, vmap, omap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
@@ -1060,13 +1192,15 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
         !encode_bf16_tensor_map(&vmap, ws_v, 3, vd, vs, vb, true))
       return TL_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTcSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kTcSmem) != cudaSuccess)
     return TL_ERR_CUDA;
   const int64_t n_items = (int64_t)n_pairs * B * h_kv;
   if (n_items > 0x7fffffff - 65536) return TL_ERR_UNSUPPORTED;
   const int grid = (int)std::min<int64_t>(num_sms(), n_items);
-  const dim3 cvt_grid((unsigned)((v_keys + kCvtKeys - 1) / kCvtKeys), B);
+  const dim3 cvt_grid((unsigned)P.cvt_gx, B);
   if (kv8)
     prefill_v_f16_kernel<true><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
   else
@@ -1088,8 +1222,12 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kTcSmem;
-  if (cudaLaunchKernelEx(&cfg, prefill_tc_kernel, P, qmap, kmap, vmap, omap, box_rows, counter) !=
-      cudaSuccess)
+  // rows whose V holds no value above 8 in magnitude (single fp16 P), then
+  // the others (P split in two); each kernel skips the other's rows
+  if (cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, P, qmap, kmap, vmap, omap, box_rows,
+                         counter) != cudaSuccess ||
+      cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, P, qmap, kmap, vmap, omap, box_rows,
+                         counter + 1) != cudaSuccess)
     return TL_ERR_CUDA;
   return launch_status();
 }

@@ -123,6 +123,13 @@ TC_DEVINLINE void st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[15])
       : "memory");
 }
+// 8 consecutive 32-bit columns (packed 16-bit pairs).
+TC_DEVINLINE void st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
 TC_DEVINLINE void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 }  // namespace tc

@@ -74,13 +74,15 @@ def test_workspace_sizes(lib):
     assert tl.tl_paged_attn_decode_workspace_size(0, 32, 8, 128) == 0
     # the work counter (256 B), two int32 arrays over the B * n_pairs query-tile
     # pairs (n_pairs = 2048 / (2 * 128 / 4) = 32, each array rounded to 256 B),
-    # the rows' first keys (B int32, rounded to 256 B), then the fp16 copy of V:
-    # B * h_kv * (max_pages_per_seq * page_size) * d * 2
+    # the rows' first keys (B int32, rounded to 256 B), a flag per 64 keys of
+    # each row (8 * 8192 / 64 int32) and per row (rounded to 256 B), then the
+    # fp16 copy of V: B * h_kv * (max_pages_per_seq * page_size) * d * 2
     assert tl.tl_paged_attn_prefill_workspace_size(8, 2048, 32, 8, 128, 512, 16) == \
-        256 + 2 * 1024 + 256 + 8 * 8 * 512 * 16 * 128 * 2
-    # over a ring of 257 pages the copy holds align_up(257 * 16, 128) + 256 keys per row
+        256 + 2 * 1024 + 256 + 4096 + 256 + 8 * 8 * 512 * 16 * 128 * 2
+    # over a ring of 257 pages the copy holds align_up(257 * 16, 128) + 256 keys
+    # per row (70 flags of 64 keys per row: 2240 B, rounded to 2304)
     assert tl.tl_paged_attn_prefill_ring_workspace_size(8, 2048, 32, 8, 128, 512, 16, 257) == \
-        256 + 2 * 1024 + 256 + 8 * 8 * (4224 + 256) * 128 * 2
+        256 + 2 * 1024 + 256 + 2304 + 256 + 8 * 8 * (4224 + 256) * 128 * 2
     assert tl.tl_paged_attn_prefill_ring_workspace_size(8, 2048, 32, 8, 128, 512, 16, 0) == 0
     assert tl.tl_paged_attn_prefill_workspace_size(8, 2048, 32, 8, 128, 0, 16) == 0
     # the decode bound grows with B and h_q but not with context length
