@@ -336,6 +336,10 @@ def run_ours(args):
     int8_line = None
     if args.only in ("all", "int8"):
         int8_line = run_int8(args, dev, stream, hbm)
+    swa_line = run_decode_config(args, dev, stream, hbm, "swa") \
+        if args.only in ("all", "swa") else None
+    longctx_line = run_decode_config(args, dev, stream, hbm, "longctx") \
+        if args.only in ("all", "longctx") else None
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -376,6 +380,8 @@ def run_ours(args):
         "verify_decode": verify_line,
         "fp8_decode": fp8_line,
         "int8_decode": int8_line,
+        "swa_decode": swa_line,
+        "longctx_decode": longctx_line,
         "e2e": e2e,
         "separate_step": {"calls": "tl_kv_cache_write, then tl_paged_attn_decode (four kernels)",
                           "ms_per_step": round(sep_ms, 5),
@@ -389,6 +395,73 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def l2_flush_buffer(dev):
+    """A buffer twice the size of L2 (129 MB); writing it evicts what earlier
+    reps left in L2."""
+    import torch
+    return torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+
+def run_decode_config(args, dev, stream, hbm, which):
+    """A decode workload through the plain tl_paged_attn_decode call: the
+    sliding-window mix (two layers, separate pools: window 4,096 then full)
+    or the long-context lognormal batch.  GB/s of the K/V the call must read
+    (window-clipped) plus Q, the tables and the output, per call."""
+    import torch
+
+    import paged_kv_attention_cache_gb300 as tl
+    from paged_kv_attention_cache_gb300 import workloads as wl
+
+    if which == "swa":
+        cases = [wl.swa_decode(seed=args.seed, device=dev, layer=layer) for layer in (0, 1)]
+        name = ("sliding-window mix: B=128, Hq=40, Hkv=8, d=128, bf16, page 16, "
+                "L~U[1024,32768], 1% of values x8; layer 0 window 4096, layer 1 full, "
+                "separate pools")
+    else:
+        cases = [wl.longctx_decode(seed=args.seed, device=dev)]
+        name = ("long-context batch: B=256, Hq=64, Hkv=8, d=128, bf16, page 16, "
+                "L lognormal median 2048 sigma 1 clipped to [64,131072]")
+    layers = []
+    for case in cases:
+        g = wl.to_device(case, dev)
+        B, hq, hkv, d = case.B, case.Hq, case.Hkv, case.d
+        lens = case.context_lens.tolist()
+        keys = sum(min(L, case.window) if case.window > 0 else L for L in lens)
+        kvb = keys * 2 * hkv * d * 2
+        alg = kvb + B * hq * d * 2 + B * hq * d * 4 + sum((L + 15) // 16 for L in lens) * 4
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+        ws = tl.alloc_workspace(tl.tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def call():
+            tl.tl_paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens,
+                                    case.scale, window=case.window, out=out, workspace=ws,
+                                    error_word=err)
+
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        n = 30
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error word {int(err.item())} in the {which} decode")
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        gbs = alg / (ms * 1e-3) / 1e9
+        layers.append({"window": case.window, "kv_bytes_per_call": kvb,
+                       "algorithmic_bytes_per_call": alg, "ms_per_call": round(ms, 4),
+                       "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                       "l2": "pool %.2f GB vs 129 MB L2" % (g.k_cache.numel() * 4 / 1e9)})
+        del g, out, ws
+        torch.cuda.empty_cache()
+    return {"workload": name, "call": "tl_paged_attn_decode", "layers": layers}
 
 
 def run_ring(args, dev, stream, hbm):
@@ -624,17 +697,54 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
             b.record(stream)
         torch.cuda.synchronize()
     pf_ms = statistics.mean(a.elapsed_time(b) for a, b in pev)
-    # chunk write on its own (16K rows), for the write kernel's GB/s
+    # the chunk write on its own (16K rows), for the write kernel's GB/s.
+    # Its 80 MB fit in L2, so the writes rotate over four chunks (this one and
+    # three more of other seeds, each with its own pool): a write never finds
+    # its rows in L2, and the dirty rows of earlier writes are written back
+    # during later ones, as in a serving loop.  Timed two ways: each call
+    # alone between CUDA events (a sleep kernel first, so the host has
+    # enqueued the call before the GPU reaches the first event), and sixteen
+    # calls back to back in a CUDA graph (per call: the graph's time / 16).
+    chunks = [pg] + [wl.to_device(wl.batched_prefill(seed=args.seed + rank + 100 + i, device=dev),
+                                  dev) for i in range(3)]
+
+    def write_chunk(c):
+        tl.tl_kv_cache_write(c.k_new.view(-1, c.Hkv, c.d), c.v_new.view(-1, c.Hkv, c.d),
+                             c.k_cache, c.v_cache, c.slot_mapping)
+
+    for c in chunks:
+        write_chunk(c)
+    torch.cuda.synchronize()
     wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(10)]
-    for a, b in wev:
+           for _ in range(40)]
+    for i, (a, b) in enumerate(wev):
+        torch.cuda._sleep(200000)
         a.record(stream)
-        tl.tl_kv_cache_write(kn, vn, pg.k_cache, pg.v_cache, pg.slot_mapping)
+        write_chunk(chunks[i % 4])
         b.record(stream)
     torch.cuda.synchronize()
-    w_ms = statistics.mean(a.elapsed_time(b) for a, b in wev)
-    n_live = int((pcase.slot_mapping >= 0).sum().item())
-    w_bytes = n_live * pcase.Hkv * pcase.d * 2 * 2 * 2 + pcase.slot_mapping.numel() * 8
+    w_ms_call = statistics.mean(a.elapsed_time(b) for a, b in wev)
+    gstream = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gstream):
+        with torch.cuda.graph(graph, stream=gstream):
+            for i in range(16):
+                write_chunk(chunks[i % 4])
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ga.record(stream)
+    for _ in range(10):
+        graph.replay()
+    gb.record(stream)
+    torch.cuda.synchronize()
+    w_ms = ga.elapsed_time(gb) / 160
+    n_live_all = [int((c.slot_mapping >= 0).sum().item()) for c in chunks]
+    del graph, chunks
+    n_live = sum(n_live_all) / len(n_live_all)  # live rows per chunk (mean of the four)
+    w_bytes = int(n_live * pcase.Hkv * pcase.d * 2 * 2 * 2 + pcase.slot_mapping.numel() * 8)
     pf_tflops = flops / (pf_ms * 1e-3) / 1e12
     prefill_line = {
         "workload": "B=8 x T=2048 right-aligned, pads U{0..1500}, prior U{0..6144}, "
@@ -647,9 +757,19 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
                      "peak_source": f"{src} bf16_tflops (burst)",
                      "frac_of_sustained": round(pf_tflops / bf16_sus, 4)},
         "clocks": pclk.summary()}
-    write_line = {"rows": n_live, "ms": round(w_ms, 5),
-                  "gbs": round(w_bytes / (w_ms * 1e-3) / 1e9, 1),
-                  "frac": round(w_bytes / (w_ms * 1e-3) / 1e9 / hbm, 4)}
+    write_line = {"workload": "the prefill chunk's K/V rows: 16,384 tokens (pads at slot -1), "
+                              "Hkv=8, d=128, bf16, into the shuffled pool; four chunks in turn",
+                  "rows": round(n_live, 1), "algorithmic_bytes": w_bytes,
+                  "ms": round(w_ms, 5), "gbs": round(w_bytes / (w_ms * 1e-3) / 1e9, 1),
+                  "frac": round(w_bytes / (w_ms * 1e-3) / 1e9 / hbm, 4),
+                  "timing": "16 calls back to back in a CUDA graph, 10 replays; per call = "
+                            "time / 160",
+                  "ms_per_call_alone": round(w_ms_call, 5),
+                  "frac_per_call_alone": round(w_bytes / (w_ms_call * 1e-3) / 1e9 / hbm, 4),
+                  "l2": "four chunks in turn (256 MB of new rows, 160 MB of destination rows): "
+                        "no call finds its rows in L2"}
+    if rank == 0 and not args.no_cpu_baseline and args.only == "all":
+        prefill_line["cpu_baseline"] = prefill_cpu_baseline(pcase, pg, args)
     # the same call over e4m3 pools (the bf16 pools written through the
     # converting write): the pre-pass widens K to bf16 and V to fp16 copies
     P_, ps_, hkv_, d_ = pg.k_cache.shape
@@ -716,6 +836,32 @@ def cpu_baseline(case, g, args):
                               "sample": f"one full decode step, {dt1:.3f} s"}}
 
 
+def prefill_cpu_baseline(pcase, pg, args):
+    """The oracle, as it stands, on whole rows of the batched-prefill workload
+    (every token of each row, blockwise fold over 2,048-key blocks), all host
+    cores, rows taken in order until about args.cpu_seconds have passed; the
+    rate is the rows' algorithmic flops over the time."""
+    import numpy as np
+
+    import oracle
+
+    kc, vc = pg.k_cache.cpu(), pg.v_cache.cpu()  # after the chunk's write
+    q, pos, bt = pcase.q.cpu(), pcase.positions.cpu(), pcase.block_table.cpu()
+    threads = os.cpu_count() or 1
+    flops, rows, t0 = 0, 0, time.perf_counter()
+    for b in range(pcase.B):
+        oracle.paged_prefill(q[b:b + 1], kc, vc, bt[b:b + 1], pos[b:b + 1], pcase.scale,
+                             threads=threads)
+        flops += prefill_flops(pos[b:b + 1], pcase.Hq, pcase.d)
+        rows += 1
+        if time.perf_counter() - t0 >= args.cpu_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 5), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{rows} of {pcase.B} rows, every token ({dt:.1f} s)"}
+
+
 # ------------------------------------------------------------- reference --
 
 def run_reference(args):
@@ -772,7 +918,8 @@ def main():
     ap.add_argument("--soak-seconds", type=float, default=2.0)
     ap.add_argument("--batch", type=int, default=64, help="decode batch (64 = the workload)")
     ap.add_argument("--only", choices=["all", "decode", "decode-e2e", "prefill", "ring",
-                                       "verify", "fp8", "int8"], default="all")
+                                       "verify", "fp8", "int8", "swa", "longctx"],
+                    default="all")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

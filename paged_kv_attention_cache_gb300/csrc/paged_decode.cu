@@ -277,12 +277,55 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
         int8_t* vd = static_cast<int8_t*>(P.v_dst);
         float* ksc = const_cast<float*>(P.k_scales);
         float* vsc = const_cast<float*>(P.v_scales);
-        if (P.new_kind == 3)
+        if (P.d == 128) {
+          if (P.new_kind == 3)
+            write_head_rows_int8_d128<false>(P.k_new, P.v_new, kd, vd, ksc, vsc, t, g, slot,
+                                             P.page_size, P.h_kv, lane, P.error_word);
+          else
+            write_head_rows_int8_d128<true>(P.k_new, P.v_new, kd, vd, ksc, vsc, t, g, slot,
+                                            P.page_size, P.h_kv, lane, P.error_word);
+        } else if (P.new_kind == 3) {
           write_head_rows_int8<false>(P.k_new, P.v_new, kd, vd, ksc, vsc, t, g, slot,
                                       P.page_size, P.h_kv, P.d, lane, P.error_word);
-        else
+        } else {
           write_head_rows_int8<true>(P.k_new, P.v_new, kd, vd, ksc, vsc, t, g, slot,
                                      P.page_size, P.h_kv, P.d, lane, P.error_word);
+        }
+      }
+      return;
+    }
+    // rows of 32 x 1, 2, 4 (or 8) units: every load before any store
+    const int u = P.row_units;
+    const int upl = u % 32 == 0 ? u / 32 : 0;
+    if (P.new_kind == 0 && (upl == 1 || upl == 2 || upl == 4 || upl == 8)) {
+      const int4* kn = static_cast<const int4*>(P.k_new);
+      const int4* vn = static_cast<const int4*>(P.v_new);
+      int4* kd = static_cast<int4*>(P.k_dst);
+      int4* vd = static_cast<int4*>(P.v_dst);
+      for (int64_t t = first; t < P.n_new; t += stride) {
+        if (upl == 1) write_tokens_vec<1, 1>(kn, vn, kd, vd, P.slot_mapping, t, P.n_new, n_slots, lane, P.error_word);
+        else if (upl == 2) write_tokens_vec<2, 1>(kn, vn, kd, vd, P.slot_mapping, t, P.n_new, n_slots, lane, P.error_word);
+        else if (upl == 4) write_tokens_vec<4, 1>(kn, vn, kd, vd, P.slot_mapping, t, P.n_new, n_slots, lane, P.error_word);
+        else write_tokens_vec<8, 1>(kn, vn, kd, vd, P.slot_mapping, t, P.n_new, n_slots, lane, P.error_word);
+      }
+      return;
+    }
+    if ((P.new_kind == 1 || P.new_kind == 2) && (upl == 1 || upl == 2 || upl == 4)) {
+      uint2* kd = static_cast<uint2*>(P.k_dst);
+      uint2* vd = static_cast<uint2*>(P.v_dst);
+      for (int64_t t = first; t < P.n_new; t += stride) {
+#define TL_E4M3_VEC(F32, U) \
+  write_tokens_e4m3_vec<F32, U, 1>(P.k_new, P.v_new, kd, vd, P.slot_mapping, t, P.n_new, n_slots, lane, P.error_word)
+        if (P.new_kind == 1) {
+          if (upl == 1) TL_E4M3_VEC(false, 1);
+          else if (upl == 2) TL_E4M3_VEC(false, 2);
+          else TL_E4M3_VEC(false, 4);
+        } else {
+          if (upl == 1) TL_E4M3_VEC(true, 1);
+          else if (upl == 2) TL_E4M3_VEC(true, 2);
+          else TL_E4M3_VEC(true, 4);
+        }
+#undef TL_E4M3_VEC
       }
       return;
     }
@@ -293,7 +336,6 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
         if (lane == 0) report(P.error_word, TL_DEVERR_SLOT_RANGE);
         continue;
       }
-      const int u = P.row_units;
       if (P.new_kind == 0)
         write_token_rows(static_cast<const int4*>(P.k_new) + t * u,
                          static_cast<const int4*>(P.v_new) + t * u,

@@ -60,8 +60,13 @@ def test_all_padding_writes_nothing():
     assert same_bytes(g.k_cache, case.k_cache) and same_bytes(g.v_cache, case.v_cache)
 
 
-def test_out_of_range_slot_is_skipped_and_reported():
-    case = wl.decode_case([20, 33], Hq=4, Hkv=2, d=64, dtype=torch.bfloat16, seed=5, n_pad=1)
+@pytest.mark.parametrize("hkv,d,dtype", [(2, 64, torch.bfloat16),   # rows of 16 vectors
+                                         (8, 128, torch.bfloat16),  # 128: the vectorised path
+                                         (8, 128, torch.float32),   # 256
+                                         (2, 64, torch.float32)])   # 32
+def test_out_of_range_slot_is_skipped_and_reported(hkv, d, dtype):
+    case = wl.decode_case([20, 33, 5, 70, 1], Hq=2 * hkv, Hkv=hkv, d=d, dtype=dtype, seed=5,
+                          n_pad=2)
     n_slots = case.num_pages * case.page_size
     bad = case.slot_mapping.clone()
     bad[0] = n_slots  # one past the end
