@@ -22,7 +22,8 @@ pages defines it, is stated in ``oracle.c``:
 * ``kv_cache_write_fp8`` / ``fp8_value`` / ``fp8_code`` -- "How serving works
   in Tlaloc", the FP8 KV cache paragraph (e4m3fn codes, clamp to +-448, ties
   to even);
-* ``kv_cache_write_int8`` / ``paged_decode_int8`` -- same page: int8 KV pools
+* ``kv_cache_write_int8`` / ``paged_decode_int8`` / ``paged_prefill_int8`` --
+  same page: int8 KV pools
   are named as a next step without a format, read here from its "Int8 weights
   (opt-in)" paragraph (one f32 scale per row, max |x| / 127, codes rounded
   half to even; a value is code x scale).
@@ -95,6 +96,10 @@ def _load():
                                                      i32, i32, i32, i32, i32, i32, f64, vp, i32,
                                                      vp, i32]
             lib.oracle_paged_decode_int8.restype = ctypes.c_int
+            lib.oracle_paged_prefill_int8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                                      i32, i32, i32, i32, i32, i32, i32, f64, i32,
+                                                      i32, vp, i64, vp, i32]
+            lib.oracle_paged_prefill_int8.restype = ctypes.c_int
             lib.oracle_ring_pages.restype = i64
             lib.oracle_kv_bytes_per_token.argtypes = [i64, i64, i64, i64]
             lib.oracle_kv_bytes_per_token.restype = i64
@@ -303,6 +308,34 @@ def paged_prefill(q, k_cache, v_cache, block_table, positions, scale, window=0,
                                   _ptr(out), int(threads))
     if rc != 0:
         raise OracleError(f"oracle_paged_prefill failed ({rc})")
+    return out
+
+
+def paged_prefill_int8(q, k_codes, v_codes, k_scales, v_scales, block_table, positions, scale,
+                       window=0, blockwise=True, key_block=DEFAULT_KEY_BLOCK, tokens=None,
+                       threads=0, ring_pages=0) -> np.ndarray:
+    """paged_prefill over int8 pools: each element read as code x its row's scale."""
+    lib = _load()
+    qa = _c(_np(q))
+    kc, vc = _c(_np(k_codes)), _c(_np(v_codes))
+    ks, vs = _c(_np(k_scales)), _c(_np(v_scales))
+    bt = _c(_np(block_table), np.int32)
+    pos = _c(_np(positions), np.int32)
+    B, T, hq, d = qa.shape
+    P, ps, hkv, d2 = kc.shape
+    if _dtype_code(qa) != BF16 or kc.dtype != np.int8 or vc.shape != kc.shape or d2 != d or \
+            ks.dtype != np.float32 or ks.shape != (P, hkv, ps) or vs.shape != ks.shape or \
+            pos.shape != (B, T) or bt.shape[0] != B:
+        raise OracleError("shape / dtype mismatch")
+    tk = _c(np.arange(B * T) if tokens is None else np.asarray(tokens), np.int64)
+    out = np.zeros((tk.shape[0], hq, d), dtype=np.float64)
+    rc = lib.oracle_paged_prefill_int8(_ptr(qa), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
+                                       bt.shape[1], _ptr(pos), B, T, hq, hkv, d, P, ps,
+                                       int(window), int(ring_pages), float(scale),
+                                       1 if blockwise else 0, int(key_block), _ptr(tk),
+                                       tk.shape[0], _ptr(out), int(threads))
+    if rc != 0:
+        raise OracleError(f"oracle_paged_prefill_int8 failed ({rc})")
     return out
 
 

@@ -503,17 +503,18 @@ int oracle_paged_decode_int8(const void* q, const int8_t* k_codes, const int8_t*
  * live position (blockwise is then ignored).
  * Computes the tokens listed (as b*T+t) in tokens[0..n_tokens) into
  * out[n_tokens][H_q][d]. */
-int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache,
-                         int32_t dtype, const int32_t* block_table,
-                         int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
-                         int32_t T, int32_t h_q, int32_t h_kv, int32_t d,
-                         int32_t num_pages, int32_t page_size, int32_t window,
-                         int32_t ring_pages, double scale, int32_t blockwise, int32_t key_block,
-                         const int64_t* tokens, int64_t n_tokens, double* out,
-                         int32_t n_threads) {
+static int prefill_common(const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scales, const float* v_scales, int32_t dtype,
+                          const int32_t* block_table, int32_t max_pages_per_seq,
+                          const int32_t* positions, int32_t B, int32_t T, int32_t h_q,
+                          int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size,
+                          int32_t window, int32_t ring_pages, double scale, int32_t blockwise,
+                          int32_t key_block, const int64_t* tokens, int64_t n_tokens,
+                          double* out, int32_t n_threads) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 ||
       page_size <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 ||
-      (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_FP8) ||
+      (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_FP8 && dtype != OR_INT8) ||
+      (dtype == OR_INT8 && (!k_scales || !v_scales)) ||
       (blockwise && key_block <= 0) || ring_pages < 0 || ring_pages > max_pages_per_seq)
     return OR_BAD_ARG;
   for (int64_t i = 0; i < n_tokens; ++i)
@@ -537,7 +538,7 @@ int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache
     const int64_t bt_idx = tokens[item / h_q], h = item % h_q, g = h / group;
     const int64_t b = bt_idx / T;
     paged_seq s = {k_cache, v_cache, dtype, block_table + b * max_pages_per_seq,
-                   max_pages_per_seq, num_pages, page_size, h_kv, d, NULL, NULL};
+                   max_pages_per_seq, num_pages, page_size, h_kv, d, k_scales, v_scales};
     double* qv = (double*)malloc((size_t)d * sizeof(double));
     double* o = out + item * d;
     if (!qv) { status = OR_NO_MEM; continue; }
@@ -559,6 +560,37 @@ int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache
     free(qv);
   }
   return status;
+}
+
+int oracle_paged_prefill(const void* q, const void* k_cache, const void* v_cache,
+                         int32_t dtype, const int32_t* block_table,
+                         int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
+                         int32_t T, int32_t h_q, int32_t h_kv, int32_t d,
+                         int32_t num_pages, int32_t page_size, int32_t window,
+                         int32_t ring_pages, double scale, int32_t blockwise, int32_t key_block,
+                         const int64_t* tokens, int64_t n_tokens, double* out,
+                         int32_t n_threads) {
+  if (dtype == OR_INT8) return OR_BAD_ARG; /* int8 pools come with their scales */
+  return prefill_common(q, k_cache, v_cache, NULL, NULL, dtype, block_table, max_pages_per_seq,
+                        positions, B, T, h_q, h_kv, d, num_pages, page_size, window, ring_pages,
+                        scale, blockwise, key_block, tokens, n_tokens, out, n_threads);
+}
+
+/* Prefill over int8 pools (codes at the pool layout, scales
+ * [num_pages][H_kv][page_size]); each element read as code x scale, the rest
+ * as oracle_paged_prefill. */
+int oracle_paged_prefill_int8(const void* q, const int8_t* k_codes, const int8_t* v_codes,
+                              const float* k_scales, const float* v_scales,
+                              const int32_t* block_table, int32_t max_pages_per_seq,
+                              const int32_t* positions, int32_t B, int32_t T, int32_t h_q,
+                              int32_t h_kv, int32_t d, int32_t num_pages, int32_t page_size,
+                              int32_t window, int32_t ring_pages, double scale,
+                              int32_t blockwise, int32_t key_block, const int64_t* tokens,
+                              int64_t n_tokens, double* out, int32_t n_threads) {
+  return prefill_common(q, k_codes, v_codes, k_scales, v_scales, OR_INT8, block_table,
+                        max_pages_per_seq, positions, B, T, h_q, h_kv, d, num_pages, page_size,
+                        window, ring_pages, scale, blockwise, key_block, tokens, n_tokens, out,
+                        n_threads);
 }
 
 /* ---------------------------------------------------------------- sizing -- */

@@ -169,3 +169,65 @@ def test_int8_negative_control_token_major_scales_are_caught():
     swapped = np.ascontiguousarray(ks.reshape(ks.shape[0], ps, hkv).transpose(0, 2, 1))
     bad = oracle.paged_decode_int8(q_st, kc, vc, swapped, vs, bt, lengths, 0.3)
     assert np.max(np.abs(good - bad)) > 1e-3
+
+
+def _int8_prefill_inputs(lengths, n_live, pads, hq, d, seed):
+    """Right-aligned prefill rows at the end of each history: row b holds
+    pads[b] padding tokens (position -1) then the positions
+    L_b - n_live[b] .. L_b - 1; queries bf16."""
+    rng = np.random.default_rng(seed)
+    B, T = len(lengths), max(n + p for n, p in zip(n_live, pads))
+    pos = np.full((B, T), -1, np.int32)
+    for b, (L, n) in enumerate(zip(lengths, n_live)):
+        pos[b, T - n:] = np.arange(L - n, L)
+    q_st, q_vals = round_to(rng.standard_normal((B, T, hq, d)), torch.bfloat16)
+    return q_st, q_vals, pos
+
+
+@pytest.mark.parametrize("window", [0, 9])
+def test_int8_prefill_equals_dense_attention_over_code_times_scale(window):
+    lengths, ps, hq, hkv, d = [30, 12, 64, 1], 8, 4, 2, 16
+    kc, vc, ks, vs, bt, hist = _int8_case(lengths, ps, hkv, d, 81)
+    q_st, q_vals, pos = _int8_prefill_inputs(lengths, [7, 12, 5, 1], [1, 0, 4, 6], hq, d, 82)
+    scale = 0.3
+    B, T = pos.shape
+    out = oracle.paged_prefill_int8(q_st, kc, vc, ks, vs, bt, pos, scale, window=window)
+    out = out.reshape(B, T, hq, d)
+    for b in range(B):
+        kh, vh = hist[b]
+        for t in range(T):
+            p = pos[b, t]
+            if p < 0:
+                assert np.all(out[b, t] == 0)
+                continue
+            lo = 0 if window <= 0 else max(0, p - window + 1)
+            for h in range(hq):
+                g = h // (hq // hkv)
+                w = scipy.special.softmax(scale * (kh[lo:p + 1, g] @ q_vals[b, t, h]))
+                np.testing.assert_allclose(out[b, t, h], w @ vh[lo:p + 1, g], rtol=1e-12,
+                                           atol=1e-12)
+
+
+def test_int8_prefill_with_unit_scales_equals_the_f32_oracle():
+    lengths, ps, hq, hkv, d = [17, 40, 3], 8, 6, 3, 32
+    kc, vc, ks, vs, bt, _ = _int8_case(lengths, ps, hkv, d, 83, unit_scales=True)
+    q_st, q_vals, pos = _int8_prefill_inputs(lengths, [9, 40, 3], [2, 0, 5], hq, d, 84)
+    out = oracle.paged_prefill_int8(q_st, kc, vc, ks, vs, bt, pos, 0.1)
+    ref = oracle.paged_prefill(q_vals.astype(np.float32), kc.astype(np.float32),
+                               vc.astype(np.float32), bt, pos, 0.1)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_int8_prefill_blockwise_equals_one_pass_and_batched_equals_solo():
+    # key blocks of 8 keys: every row folds several blocks, some fully masked
+    lengths, ps, hq, hkv, d = [45, 20, 33], 8, 4, 2, 16
+    kc, vc, ks, vs, bt, _ = _int8_case(lengths, ps, hkv, d, 85)
+    q_st, _, pos = _int8_prefill_inputs(lengths, [30, 20, 3], [0, 10, 27], hq, d, 86)
+    blockwise = oracle.paged_prefill_int8(q_st, kc, vc, ks, vs, bt, pos, 0.25, key_block=8)
+    one_pass = oracle.paged_prefill_int8(q_st, kc, vc, ks, vs, bt, pos, 0.25, blockwise=False)
+    assert np.max(np.abs(blockwise - one_pass)) <= 1e-12
+    B, T = pos.shape
+    for b in range(B):
+        solo = oracle.paged_prefill_int8(q_st[b:b + 1], kc, vc, ks, vs, bt[b:b + 1],
+                                         pos[b:b + 1], 0.25, blockwise=False)
+        assert np.array_equal(solo, one_pass.reshape(B, T, hq, d)[b].reshape(solo.shape))
