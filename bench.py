@@ -801,6 +801,37 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
     prefill_line["fp8_pools"] = {"ms_per_call": round(f_ms, 4), "tflops": round(f_tflops, 2),
                                  "frac": round(f_tflops / bf16, 4)}
     del k8, v8, pws8
+    # and over int8 pools (the bf16 pools through the int8 write: one scale per
+    # slot and KV head): the pre-pass widens the codes and gathers the scales
+    kc8 = torch.empty((P_, ps_, hkv_, d_), dtype=torch.int8, device=dev)
+    vc8 = torch.empty_like(kc8)
+    ks8 = torch.empty((P_, hkv_, ps_), dtype=torch.float32, device=dev)
+    vs8 = torch.empty_like(ks8)
+    tl.tl_kv_cache_write_int8(pg.k_cache.view(-1, hkv_, d_), pg.v_cache.view(-1, hkv_, d_), kc8,
+                              vc8, ks8, vs8, every)
+    pws_i8 = tl.alloc_workspace(tl.tl_paged_attn_prefill_workspace_size_ex(
+        pcase.B, pcase.T, pcase.Hq, pcase.Hkv, pcase.d, pcase.block_table.shape[1],
+        pcase.page_size, 0, tl.TL_INT8), dev)
+
+    def pf_i8():
+        tl.tl_paged_attn_prefill_int8(pg.q, kc8, vc8, ks8, vs8, pg.block_table, pg.positions,
+                                      pcase.scale, out=pout, workspace=pws_i8)
+
+    for _ in range(max(3, args.warmup)):
+        pf_i8()
+    torch.cuda.synchronize()
+    iev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.prefill_steps)]
+    for a, b in iev:
+        a.record(stream)
+        pf_i8()
+        b.record(stream)
+    torch.cuda.synchronize()
+    i_ms = statistics.mean(a.elapsed_time(b) for a, b in iev)
+    i_tflops = flops / (i_ms * 1e-3) / 1e12
+    prefill_line["int8_pools"] = {"ms_per_call": round(i_ms, 4), "tflops": round(i_tflops, 2),
+                                  "frac": round(i_tflops / bf16, 4)}
+    del kc8, vc8, ks8, vs8, pws_i8
     return prefill_line, write_line
 
 

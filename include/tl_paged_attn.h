@@ -71,9 +71,11 @@ typedef enum {
 } tl_status;
 
 typedef enum {
-  TL_F32 = 0,      /* IEEE binary32 */
-  TL_BF16 = 1,     /* bfloat16 */
-  TL_FP8_E4M3 = 2  /* e4m3fn codes (fp8 KV pools only; see tl_kv_cache_write_fp8) */
+  TL_F32 = 0,       /* IEEE binary32 */
+  TL_BF16 = 1,      /* bfloat16 */
+  TL_FP8_E4M3 = 2,  /* e4m3fn codes (fp8 KV pools only; see tl_kv_cache_write_fp8) */
+  TL_INT8 = 3       /* int8 codes with per-row f32 scales (the workspace query of
+                       tl_paged_attn_prefill_int8; the int8 calls take no dtype) */
 } tl_dtype;
 
 /* Bits OR-ed into *error_word by the device-side checks. */
@@ -343,9 +345,12 @@ size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, i
                                             int32_t page_size);
 
 /* Workspace bytes of any prefill call (0 for invalid sizes): ring_pages 0 for
- * a full-history table (tl_paged_attn_prefill) or > 0 for a ring
- * (tl_paged_attn_prefill_ring); dtype TL_BF16, or TL_FP8_E4M3 for e4m3
- * pools, which add a bf16 copy of K as large as the V copy. */
+ * a full-history table (tl_paged_attn_prefill, tl_paged_attn_prefill_int8) or
+ * > 0 for a ring (tl_paged_attn_prefill_ring); dtype TL_BF16, TL_FP8_E4M3 for
+ * e4m3 pools, which add a bf16 copy of K as large as the V copy, or TL_INT8
+ * for int8 pools, which add that copy and the copied keys' K scales, V
+ * scales and reciprocal V scales (three f32 arrays of B * h_kv *
+ * max_pages_per_seq * page_size, each rounded up to 256 bytes). */
 size_t tl_paged_attn_prefill_workspace_size_ex(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
                                                int32_t d, int32_t max_pages_per_seq,
                                                int32_t page_size, int32_t ring_pages,
@@ -395,6 +400,37 @@ tl_status tl_paged_attn_prefill(const void* q, const void* k_cache, const void* 
                                 int32_t page_size, int32_t window, float scale, tl_dtype dtype,
                                 void* workspace, size_t workspace_bytes, uint32_t* error_word,
                                 void* stream);
+
+/*
+ * PAGED_ATTENTION, batched prefill over int8 pools (written by
+ * tl_kv_cache_write_int8): tl_paged_attn_prefill with every K/V element read
+ * as code x its row's scale.  The scores are s_j = scale * k_scale(j) *
+ * <q, codes of K_g(j)> (Q.K^T on the tensor core with bf16 q and the codes
+ * widened exactly to bf16, f32 accumulation, then the K scale in f32); each
+ * probability p_j is multiplied by its key's v_scale before the P.V product
+ * (P.V with the codes widened exactly to fp16 and the product p_j x v_scale
+ * rounded to fp16, the softmax sum taking the weights those rounded products
+ * stand for, fp16(p_j x v_scale) / v_scale, so each output is a convex
+ * combination of V rows; or, for a row whose V holds a value code x scale of
+ * magnitude above 8, the product split into two fp16 parts and the sum over
+ * the unscaled p_j).
+ *   q                  [B][T][h_q][d] bf16;  positions [B][T] int32 (-1 = pad)
+ *   k_codes, v_codes, k_scales, v_scales  as tl_kv_cache_write_int8 writes
+ *                      them (read only; codes 16-byte aligned)
+ *   out                [B][T][h_q][d] float32
+ *   workspace          at least tl_paged_attn_prefill_workspace_size_ex(B, T,
+ *                      h_q, h_kv, d, max_pages_per_seq, page_size, 0, TL_INT8)
+ *                      bytes, 256-byte aligned
+ *   the other arguments, support and errors as tl_paged_attn_prefill.
+ */
+tl_status tl_paged_attn_prefill_int8(const void* q, const int8_t* k_codes, const int8_t* v_codes,
+                                     const float* k_scales, const float* v_scales,
+                                     const int32_t* block_table, int32_t max_pages_per_seq,
+                                     const int32_t* positions, float* out, int32_t B, int32_t T,
+                                     int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+                                     int32_t page_size, int32_t window, float scale,
+                                     void* workspace, size_t workspace_bytes,
+                                     uint32_t* error_word, void* stream);
 
 /*
  * Sliding-window attention over a ring ("How serving works in Tlaloc",

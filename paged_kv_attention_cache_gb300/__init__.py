@@ -13,7 +13,7 @@ from .api import (TL_BF16, TL_FP8_E4M3, tl_kv_cache_write_fp8, TL_DEVERR_CONTEXT
                   TL_DECODE_NOALLOC_SCRATCH_BYTES, tl_kv_cache_write, tl_paged_attn_decode,
                   tl_paged_attn_decode_noalloc, tl_paged_attn_decode_workspace_size,
                   tl_paged_attn_decode_write, tl_kv_cache_write_int8, tl_paged_attn_decode_int8,
-                  tl_paged_attn_decode_write_int8,
+                  tl_paged_attn_decode_write_int8, tl_paged_attn_prefill_int8, TL_INT8,
                   tl_paged_attn_prefill, tl_paged_attn_prefill_workspace_size, tl_status_string,
                   tl_paged_attn_decode_ring, tl_paged_attn_prefill_ring,
                   tl_paged_attn_prefill_ring_workspace_size, tl_paged_attn_decode_multi,
@@ -30,7 +30,7 @@ def build_library(force: bool = False) -> str:
 __all__ = [
     "tl_kv_cache_write", "tl_kv_cache_write_fp8", "tl_kv_cache_write_int8",
     "tl_paged_attn_decode", "tl_paged_attn_decode_int8", "tl_paged_attn_decode_write_int8",
-    "tl_paged_attn_decode_noalloc",
+    "tl_paged_attn_decode_noalloc", "tl_paged_attn_prefill_int8",
     "tl_paged_attn_prefill",
     "tl_paged_attn_decode_workspace_size", "tl_paged_attn_prefill_workspace_size",
     "tl_paged_attn_decode_ring", "tl_paged_attn_prefill_ring",

@@ -15,7 +15,7 @@ from . import _lib
 
 (TL_OK, TL_ERR_INVALID_ARG, TL_ERR_UNSUPPORTED, TL_ERR_CUDA, TL_ERR_DEVICE_BOUNDS,
  TL_ERR_WORKSPACE, TL_ERR_DEVICE_TIMEOUT) = range(7)
-TL_F32, TL_BF16, TL_FP8_E4M3 = 0, 1, 2
+TL_F32, TL_BF16, TL_FP8_E4M3, TL_INT8 = 0, 1, 2, 3
 TL_DEVERR_SLOT_RANGE, TL_DEVERR_PAGE_RANGE, TL_DEVERR_CONTEXT_RANGE = 1, 2, 4
 TL_DEVERR_TIMEOUT, TL_DEVERR_VALUE_RANGE, TL_DEVERR_PLAN_CAPACITY = 8, 16, 32
 
@@ -385,6 +385,33 @@ def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
          _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window), float(scale),
          _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), _ws_bytes(workspace),
          _err_word(error_word, dev))
+    return out
+
+
+def tl_paged_attn_prefill_int8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                               k_scales: torch.Tensor, v_scales: torch.Tensor,
+                               block_table: torch.Tensor, positions: torch.Tensor, scale: float,
+                               window: int = 0, out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               error_word: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """tl_paged_attn_prefill over int8 pools (bf16 q [B, T, H_q, d]): out
+    [B, T, H_q, d] float32, every K/V element read as code x its row's scale."""
+    dev = q.device
+    P, ps, hkv, d = _need_int8_pools(k_codes, v_codes, k_scales, v_scales, dev)
+    _need(q, "q", torch.bfloat16, (None, None, None, d), dev)
+    B, T, hq, _ = q.shape
+    _need(block_table, "block_table", torch.int32, (B, None), dev)
+    if block_table.shape[1] < 1:
+        raise ValueError("block_table needs at least one column")
+    _need(positions, "positions", torch.int32, (B, T), dev)
+    out = _decode_out(out, (B, T, hq, d), dev)
+    workspace = _workspace(workspace, tl_paged_attn_prefill_workspace_size_ex(
+        B, T, hq, hkv, d, block_table.shape[1], ps, 0, TL_INT8), dev)
+    _run("tl_paged_attn_prefill_int8", dev, stream,
+         _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+         block_table.shape[1], _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window),
+         float(scale), _ptr(workspace), _ws_bytes(workspace), _err_word(error_word, dev))
     return out
 
 

@@ -83,8 +83,13 @@ struct PrefillParams {
   int32_t* row_start;    // [B] first key of each row's fp16 V copy (a multiple of kBN)
   int32_t v_keys;        // keys per row (and KV head) of the fp16 V copy
   int32_t ring_pages;    // > 0: the table's first ring_pages entries are a ring
-  int32_t kv8;           // e4m3 pools: K is read from a bf16 copy like V
-  uint16_t* ws_k;        // e4m3 pools: the bf16 copy of K, laid out like the V copy
+  int32_t kv8;           // e4m3 or int8 pools: K is read from a bf16 copy like V
+  uint16_t* ws_k;        // the bf16 copy of K, laid out like the V copy
+  const float* k_scales; // int8 pools: the pools' scales, [num_pages][h_kv][page_size]
+  const float* v_scales;
+  float* ws_ks;          // int8 pools: each copied key's scales, [B][h_kv][v_keys]
+  float* ws_vs;
+  float* ws_ivs;         // and 1 / its V scale (0 for a zero scale)
   int32_t* ctrl;         // [0], [1] work counters of the two attention kernels,
                          // [2] first work item of the flagged rows
   int32_t cvt_gx;        // pre-pass CTAs per row (64-key tiles of the V copy)
@@ -106,6 +111,9 @@ __device__ __forceinline__ int table_index(const PrefillParams& P, int blk) {
 
 constexpr int kBN = 128;             // keys per tile
 constexpr int kTcQB = 3;             // query-tile buffers (two in use, one filling)
+constexpr int kTcQBI8 = 2;           // int8 pools: two (the key-scale ring takes the third's room)
+constexpr int kScR = 4;              // int8 pools: key-scale tiles in flight
+constexpr int kScBytes = 3 * 128 * 4;  // one key tile's K scales, V scales and 1 / V scales
 constexpr int kTcKS = 2;             // K stages
 constexpr int kTcVS = 2;             // V stages
 constexpr int kTcWarps = 10;
@@ -116,6 +124,7 @@ constexpr int kCvtThreads = 256;
 constexpr int kTcQBytes = 32768;     // one query tile: 128 rows x 128 d x bf16
 constexpr int kTcKVBytes = kBN * 256;  // 128 keys x 128 d x 16-bit (two 16 KiB halves)
 constexpr int kTcSmem = kTcQB * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + 1024;
+constexpr int kTcSmemI8 = kTcQBI8 * kTcQBytes + (kTcKS + kTcVS) * kTcKVBytes + kScR * kScBytes + 1024;
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 8192;   // two halves (rows without and with the split-P flag);
                                      // key-tile counts at or above 4095 share a half's last bucket
@@ -124,10 +133,13 @@ constexpr int kPlanBuckets = 8192;   // two halves (rows without and with the sp
 // (| bf16 K for e4m3 pools)], each part 256-byte aligned; the copies are
 // [B][h_kv][v_keys][128].
 struct WsLayout {
-  size_t tiles, order, rows, cta_big, row_big, v, k, total;
+  size_t tiles, order, rows, cta_big, row_big, v, k, ks, vs, ivs, total;
 };
 constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
-inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_keys, bool kv8) {
+// kv8: e4m3 or int8 pools (a bf16 copy of K); i8: int8 pools (and the keys'
+// scales, [B][h_kv][v_keys] f32 each: K, V and 1 / V).
+inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_keys, bool kv8,
+                          bool i8 = false) {
   const size_t pairs = (size_t)(B * n_pairs) * 4;
   const size_t copy = (size_t)B * h_kv * (size_t)v_keys * 128 * 2;
   const size_t gx = (size_t)((v_keys + kCvtKeys - 1) / kCvtKeys);
@@ -139,7 +151,11 @@ inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_ke
   L.row_big = L.cta_big + align_up((size_t)B * gx * 4, 256);
   L.v = L.row_big + align_up((size_t)B * 4, 256);
   L.k = L.v + copy;
-  L.total = L.k + (kv8 ? copy : 0);
+  const size_t scales = align_up((size_t)B * h_kv * (size_t)v_keys * 4, 256);
+  L.ks = L.k + (kv8 ? copy : 0);
+  L.vs = L.ks + (i8 ? scales : 0);
+  L.ivs = L.vs + (i8 ? scales : 0);
+  L.total = L.ivs + (i8 ? scales : 0);
   return L;
 }
 // Keys per row of the V copy: the table's positions, or for a ring the
@@ -161,12 +177,33 @@ constexpr uint32_t kBf16TooBig = 0x4780u, kBf16Inf = 0x7F80u;
 // but up to several 1e-3 for values beyond 8; hi + lo carries about 22
 // significant bits.
 constexpr uint32_t kBf16Big = 0x4100u, kE4m3Big = 0x50u;
+// ... or whose V has a root mean square above 1.25 over a 64-key tile of the
+// pre-pass (N(0, 1) values have 1.0): the rounding error of one fp16 P grows
+// with the spread of V as well as with its largest value.
+constexpr float kRmsBig2 = 1.5625f;  // 1.25^2
+
+// Sum of squares of eight fp16 values.
+__device__ __forceinline__ float sumsq_f16x8(uint4 h) {
+  float a = 0.f;
+  const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float lo, hi;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w[k]));
+    a = fmaf(lo, lo, a);
+    a = fmaf(hi, hi, a);
+  }
+  return a;
+}
 
 struct TcShared {
   unsigned long long q_full[kTcQB], q_free[kTcQB];
   unsigned long long k_full[kTcKS], k_empty[kTcKS], v_full[kTcVS], v_empty[kTcVS];
   unsigned long long s_full[2], p_full[2], o_done[2], o_free[2], stg_full[2], stg_free[2];
   unsigned long long item_full[kItemSlots], item_empty[kItemSlots], mma_drain;
+  unsigned long long sc_full[kScR], sc_empty[kScR];  // int8 pools: the key-scale ring
   int item[kItemSlots];
   uint32_t tmem_base;
   int abort_flag;
@@ -278,9 +315,33 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
   return r;
 }
 
-template <bool KV8>
+// Eight int8 codes (low byte first) as fp16 and as bf16 values, exact (every
+// integer of magnitude at most 128 is both).
+__device__ __forceinline__ void i8x8_to_f16_bf16(uint2 c, uint4& f16, uint4& bf16) {
+  uint32_t h[4], b[4];
+  const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t word = w[k >> 1] >> (16 * (k & 1));
+    const float lo = (float)(int8_t)(word & 0xffu), hi = (float)(int8_t)((word >> 8) & 0xffu);
+    h[k] = pack_f16x2(lo, hi);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(b[k]) : "f"(hi), "f"(lo));
+  }
+  f16 = make_uint4(h[0], h[1], h[2], h[3]);
+  bf16 = make_uint4(b[0], b[1], b[2], b[3]);
+}
+// Largest |code| of eight int8 codes.
+__device__ __forceinline__ uint32_t i8x8_max_abs(uint2 c) {
+  const uint32_t m = __vmaxu4(__vabsss4(c.x), __vabsss4(c.y));
+  return max(max(m & 0xffu, (m >> 8) & 0xffu), max((m >> 16) & 0xffu, m >> 24));
+}
+
+// KIND 0: bf16 pools (V to fp16); 1: e4m3 pools (V to fp16, K to bf16);
+// 2: int8 pools (codes: V to fp16, K to bf16; and each key's two scales).
+template <int KIND>
 __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int* counter) {
+  constexpr bool KV8 = KIND != 0;  // one byte per element
   __shared__ int s_min[kCvtThreads / 32], s_max[kCvtThreads / 32];
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     counter[0] = 0;  // work items of the single-fp16 attention kernel
@@ -374,6 +435,27 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
   }
   __syncthreads();
   const int r0 = 0, r1 = min(end - k0, kCvtKeys);  // keys of the tile to write
+  bool big_i8 = false;  // int8 pools: some |code x scale| of V above 8
+  float sumsq = 0.f;    // sum of squares of this thread's live V values
+  int n_vals = 0;       // and their count
+  if (KIND == 2) {
+    // each key's K and V scale per KV head, next to its copied codes (0 for
+    // keys past pmax and bad pages, whose codes are 0 too)
+    for (int idx = threadIdx.x; idx < (r1 - r0) * P.h_kv; idx += kCvtThreads) {
+      const int r = r0 + idx / P.h_kv, g = idx % P.h_kv;
+      const int page = s_page[r];
+      float ksc = 0.f, vsc = 0.f;
+      if (page >= 0) {
+        const size_t si = ((size_t)page * P.h_kv + g) * P.page_size + (k0 + r) % P.page_size;
+        ksc = __ldg(P.k_scales + si);
+        vsc = __ldg(P.v_scales + si);
+      }
+      const size_t di = ((size_t)b * P.h_kv + g) * P.v_keys + (k0 - start + r);
+      P.ws_ks[di] = ksc;
+      P.ws_vs[di] = vsc;
+      P.ws_ivs[di] = vsc > 0.f ? 1.f / vsc : 0.f;
+    }
+  }
   const int units = P.h_kv * 16;                                // 16-byte units per key
   const int total = (r1 - r0) * units;
   uint32_t vmax = 0;  // max |bf16 bits| seen, per half-word
@@ -410,11 +492,25 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
         const size_t dst =
             (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 + (u & 15) * 8;
         uint4 y = x[i];
-        if (KV8) {  // e4m3 values are exact in both fp16 and bf16
+        const bool live = s_page[r] >= 0;
+        if (KIND == 2) {  // int8 codes: exact in both fp16 and bf16
+          uint4 f16, bf16;
+          i8x8_to_f16_bf16(make_uint2(y.x, y.y), f16, bf16);
+          *reinterpret_cast<uint4*>(ws + dst) = f16;
+          if (live) {
+            const float vsc = __ldg(P.v_scales + ((size_t)s_page[r] * P.h_kv + (u >> 4)) *
+                                                     P.page_size + (k0 + r) % P.page_size);
+            big_i8 |= !((float)i8x8_max_abs(make_uint2(y.x, y.y)) * vsc <= 8.f);
+            sumsq = fmaf(sumsq_f16x8(f16), vsc * vsc, sumsq);
+          }
+          i8x8_to_f16_bf16(make_uint2(y.z, y.w), f16, bf16);
+          *reinterpret_cast<uint4*>(P.ws_k + dst) = bf16;
+        } else if (KV8) {  // e4m3 values are exact in both fp16 and bf16
           cmax = __vmaxu4(cmax, __vmaxu4(y.x & 0x7f7f7f7fu, y.y & 0x7f7f7f7fu));
-          *reinterpret_cast<uint4*>(ws + dst) =
-              make_uint4(e4m3x2_to_f16x2(y.x), e4m3x2_to_f16x2(y.x >> 16),
-                         e4m3x2_to_f16x2(y.y), e4m3x2_to_f16x2(y.y >> 16));
+          const uint4 f16 = make_uint4(e4m3x2_to_f16x2(y.x), e4m3x2_to_f16x2(y.x >> 16),
+                                       e4m3x2_to_f16x2(y.y), e4m3x2_to_f16x2(y.y >> 16));
+          *reinterpret_cast<uint4*>(ws + dst) = f16;
+          if (live) sumsq += sumsq_f16x8(f16);
           *reinterpret_cast<uint4*>(P.ws_k + dst) =
               make_uint4(e4m3x2_to_bf16x2(y.z), e4m3x2_to_bf16x2(y.z >> 16),
                          e4m3x2_to_bf16x2(y.w), e4m3x2_to_bf16x2(y.w >> 16));
@@ -424,7 +520,9 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
           y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z),
                          bf16x2_to_f16x2(y.w));
           *reinterpret_cast<uint4*>(ws + dst) = y;
+          if (live) sumsq += sumsq_f16x8(y);
         }
+        n_vals += live ? 8 : 0;
       }
     }
   }
@@ -433,9 +531,31 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     report(P.error_word, TL_DEVERR_VALUE_RANGE);
   cmax = __vmaxu4(cmax, cmax >> 16);
   cmax = __vmaxu4(cmax, cmax >> 8);
-  const bool big = m0 > kBf16Big || m1 > kBf16Big || (cmax & 0xffu) > kE4m3Big;
+  // the tile's V root mean square: a fixed-order reduction (the flag, and so
+  // the row's arithmetic, must repeat bit for bit)
+  __shared__ float s_sq[kCvtThreads / 32];
+  __shared__ int s_n[kCvtThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sumsq += __shfl_xor_sync(0xffffffffu, sumsq, o);
+    n_vals += __shfl_xor_sync(0xffffffffu, n_vals, o);
+  }
+  if (lane == 0) {
+    s_sq[warp] = sumsq;
+    s_n[warp] = n_vals;
+  }
+  const bool big = m0 > kBf16Big || m1 > kBf16Big || (cmax & 0xffu) > kE4m3Big || big_i8;
   const int any_big = __syncthreads_or(big);
-  if (threadIdx.x == 0) *big_flag = any_big ? 1 : 0;
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    int cnt = 0;
+    for (int w = 0; w < kCvtThreads / 32; ++w) {
+      tot += s_sq[w];
+      cnt += s_n[w];
+    }
+    const bool wide = !(tot <= kRmsBig2 * (float)cnt);  // NaN counts as wide
+    *big_flag = (any_big || wide) ? 1 : 0;
+  }
 }
 
 // ------------------------------------------------------------ plan --
@@ -557,8 +677,14 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t tmem, int a, uint32_t vbase
 // at the first of them) and the remainder lo in [32q + 16, 32q + 32), the
 // columns of their own scores, so each chunk of scores is reread just before
 // its P replaces it.  Returns the row's sum of the unrounded f32 values.
-__device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int cmax, bool all_live,
-                                               float sc, float base) {
+//
+// TWO = false (int8 pools only): P' = fp16(p x v_scale) as one value in
+// columns [16q, 16q + 16) (the layout of the single-fp16 path), and the sum
+// takes the weight each P' stands for, P' / v_scale (p for a zero scale).
+template <bool I8, bool TWO = true>
+__device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int cmax,
+                                                  bool all_live, float sc, float base,
+                                                  const float* scl) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};
   const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
 #pragma unroll 1
@@ -566,6 +692,10 @@ __device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int 
     float x[32];
     tc::ld32(taddr + 32 * q, x);
     tc::wait_ld();
+    if (I8) {  // int8 pools: the K scales (scl[0, 128))
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[c] *= scl[32 * q + c];
+    }
     if (!all_live) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
@@ -577,13 +707,27 @@ __device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int 
       float y0, y1, h0, h1;
       fma_f32x2(x[2 * i], x[2 * i + 1], sc2, nb2, y0, y1);
       const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
-      pk[i] = pack_f16x2(e0, e1);
+      // int8 pools: P' = p x v_scale (scl[128, 256)) into P.V
+      const float v0 = I8 ? scl[kBN + 32 * q + 2 * i] : 1.f;
+      const float v1 = I8 ? scl[kBN + 32 * q + 2 * i + 1] : 1.f;
+      const float w0 = I8 ? (e0 > 0.f ? e0 * v0 : 0.f) : e0;
+      const float w1 = I8 ? (e1 > 0.f ? e1 * v1 : 0.f) : e1;
+      pk[i] = pack_f16x2(w0, w1);
       unpack_f16x2(pk[i], h0, h1);
-      pl[i] = pack_f16x2(e0 - h0, e1 - h1);
-      ls[i & 3] += e0 + e1;
+      if (TWO) {
+        pl[i] = pack_f16x2(w0 - h0, w1 - h1);
+        ls[i & 3] += e0 + e1;
+      } else {  // scl[256, 384): 1 / v_scale
+        ls[i & 3] += (v0 > 0.f ? h0 * scl[2 * kBN + 32 * q + 2 * i] : e0) +
+                     (v1 > 0.f ? h1 * scl[2 * kBN + 32 * q + 2 * i + 1] : e1);
+      }
     }
-    tc::st16(taddr + 32 * q, pk);
-    tc::st16(taddr + 32 * q + 16, pl);
+    if (TWO) {
+      tc::st16(taddr + 32 * q, pk);
+      tc::st16(taddr + 32 * q + 16, pl);
+    } else {
+      tc::st16(taddr + 16 * q, pk);
+    }
   }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
@@ -643,7 +787,7 @@ __device__ __forceinline__ int tc_fetch(TcShared& sh, uint32_t seq, int* counter
 // s-th tile of this CTA, s = 2 x item + a, lives in buffer s % kTcQB), and a
 // finished tile's buffer stages its output for the TMA stores before the
 // tile three steps later is loaded into it.
-template <bool SPLIT>
+template <bool SPLIT, bool I8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(PrefillParams P, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
@@ -653,7 +797,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ TcShared sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase, sK = sbase + kTcQB * kTcQBytes, sV = sK + kTcKS * kTcKVBytes;
+  constexpr int QB = I8 ? kTcQBI8 : kTcQB;  // query-tile buffers
+  const uint32_t sQ = sbase, sK = sbase + QB * kTcQBytes, sV = sK + kTcKS * kTcKVBytes;
+  // int8 pools: a ring of kScR key tiles' scales, [K 128 | V 128] f32 each
+  const uint32_t sSc = sV + kTcVS * kTcKVBytes;
+  const float* sc_ring = reinterpret_cast<const float*>(smem_raw + (sSc - smem_u32(smem_raw)));
   volatile int* abort_flag = &sh.abort_flag;
 
   const int tpt = 128 / P.group;  // tokens per query tile
@@ -669,7 +817,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kTcQB; ++i) {
+    for (int i = 0; i < QB; ++i) {
       mbar_init(smem_u32(&sh.q_full[i]), 1);
       mbar_init(smem_u32(&sh.q_free[i]), 1);
     }
@@ -694,6 +842,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&sh.item_empty[i]), kItemReaders);
     }
     mbar_init(smem_u32(&sh.mma_drain), 1);
+    for (int i = 0; i < kScR; ++i) {
+      mbar_init(smem_u32(&sh.sc_full[i]), 1);
+      mbar_init(smem_u32(&sh.sc_empty[i]), 8);  // the eight softmax warps
+    }
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -718,14 +870,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------ K / V producer
     const int nbox = kBN / box_rows;  // boxes per row half of a tile (8 or 16)
     const int n_slots = P.num_pages * P.page_size;
-    uint32_t k_issued = 0, v_issued = 0, q_issued = 0;  // query tile s goes to buffer s % kTcQB
+    uint32_t k_issued = 0, v_issued = 0, q_issued = 0;  // query tile s goes to buffer s % QB
+    uint32_t sc_issued = 0;                              // int8 pools: scale tiles
     bool ok = true;
     // query tile a of the item (lane 0): wait until its buffer's previous
     // tile has been written out, then load it
 #define load_q(a)                                                                               \
   {                                                                                             \
     if (lane == 0) {                                                                            \
-      const uint32_t buf = q_issued % kTcQB, use = q_issued / kTcQB;                            \
+      const uint32_t buf = q_issued % QB, use = q_issued / QB;                            \
       if (mbar_wait(smem_u32(&sh.q_free[buf]), (use & 1) ^ 1, abort_flag)) {                    \
         mbar_arrive_expect_tx(smem_u32(&sh.q_full[buf]), (uint32_t)(2 * 64 * rows_used * 2));   \
         for (int h = 0; h < 2; ++h)                                                             \
@@ -801,6 +954,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           ++v_issued;
         }
+        if (I8) {
+          // the tile's K and V scales (512 bytes each) into the scale ring
+          const uint32_t st = sc_issued % kScR;
+          if (!mbar_wait(smem_u32(&sh.sc_empty[st]), ((sc_issued / kScR) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const size_t si = ((size_t)it.b * P.h_kv + it.g) * P.v_keys + (key0 - vstart);
+            const uint32_t bar = smem_u32(&sh.sc_full[st]), part = kScBytes / 3;
+            mbar_arrive_expect_tx(bar, kScBytes);
+            bulk_g2s(sSc + st * kScBytes, P.ws_ks + si, part, bar);
+            bulk_g2s(sSc + st * kScBytes + part, P.ws_vs + si, part, bar);
+            bulk_g2s(sSc + st * kScBytes + 2 * part, P.ws_ivs + si, part, bar);
+          }
+          __syncwarp();
+          ++sc_issued;
+        }
         if (j == 0) load_q(1)  // the second tile's buffer frees up later
       }
     }
@@ -811,8 +982,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       drained &= mbar_drain(smem_u32(&sh.k_full[i % kTcKS]), (i / kTcKS) & 1);
     for (uint32_t i = v_issued > (uint32_t)kTcVS ? v_issued - kTcVS : 0; i < v_issued; ++i)
       drained &= mbar_drain(smem_u32(&sh.v_full[i % kTcVS]), (i / kTcVS) & 1);
-    for (uint32_t i = q_issued > (uint32_t)kTcQB ? q_issued - kTcQB : 0; i < q_issued; ++i)
-      drained &= mbar_drain(smem_u32(&sh.q_full[i % kTcQB]), (i / kTcQB) & 1);
+    for (uint32_t i = q_issued > (uint32_t)QB ? q_issued - QB : 0; i < q_issued; ++i)
+      drained &= mbar_drain(smem_u32(&sh.q_full[i % QB]), (i / QB) & 1);
+    for (uint32_t i = sc_issued > (uint32_t)kScR ? sc_issued - kScR : 0; i < sc_issued; ++i)
+      drained &= mbar_drain(smem_u32(&sh.sc_full[i % kScR]), (i / kScR) & 1);
     if (!drained) *abort_flag = 1;
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
@@ -829,14 +1002,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
       if (it.rg.kmax < 0) continue;
       if (lane == 0) {
-        const uint32_t qb0 = (2 * n) % kTcQB, qb1 = (2 * n + 1) % kTcQB;
-        ok = mbar_wait(smem_u32(&sh.q_full[qb0]), ((2 * n) / kTcQB) & 1, abort_flag) &&
+        const uint32_t qb0 = (2 * n) % QB, qb1 = (2 * n + 1) % QB;
+        ok = mbar_wait(smem_u32(&sh.q_full[qb0]), ((2 * n) / QB) & 1, abort_flag) &&
              mbar_wait(smem_u32(&sh.k_full[kt % kTcKS]), (kt / kTcKS) & 1, abort_flag);
         if (ok) {
           tc::fence_after();
           issue_s(0, kt, qb0);
         }
-        ok = ok && mbar_wait(smem_u32(&sh.q_full[qb1]), ((2 * n + 1) / kTcQB) & 1, abort_flag);
+        ok = ok && mbar_wait(smem_u32(&sh.q_full[qb1]), ((2 * n + 1) / QB) & 1, abort_flag);
         if (ok) {
           tc::fence_after();
           issue_s(1, kt, qb1);
@@ -943,11 +1116,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int key0 = (it.tile0 + j) * kBN;
         const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
         const bool all_live = __all_sync(0xffffffffu, cmin <= 0 && cmax >= kBN - 1);
+        // int8 pools: the tile's key scales (K at [0, 128), V at [128, 256),
+        // 1 / V at [256, 384))
+        const float* scl = sc_ring + (tiles % kScR) * (kScBytes / 4);
+        if (I8 && !mbar_wait(smem_u32(&sh.sc_full[tiles % kScR]), (tiles / kScR) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         // the tile's 128 scores of this row: four loads, one wait
         float s[kBN];
 #pragma unroll
         for (int q = 0; q < kBN / 32; ++q) tc::ld32(tmem + lane_base + colS + q * 32, s + q * 32);
         tc::wait_ld();
+        if (I8) {  // s_j = (q . codes_j) x k_scale_j
+#pragma unroll
+          for (int c = 0; c < kBN; c += 4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(scl + c);
+            s[c] *= k4.x;
+            s[c + 1] *= k4.y;
+            s[c + 2] *= k4.z;
+            s[c + 3] *= k4.w;
+          }
+        }
         if (!all_live) {
 #pragma unroll
           for (int c = 0; c < kBN; ++c) s[c] = (c >= cmin && c <= cmax) ? s[c] : -INFINITY;
@@ -974,7 +1164,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // at once; the sum widens each fp16 half inside its add.
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
-        if constexpr (!SPLIT) {
+        if constexpr (!SPLIT && I8) {
+          ls[0] = tc_softmax_split<true, false>(tmem + lane_base + colS, cmin, cmax, all_live, sc,
+                                                base, scl);
+        } else if constexpr (!SPLIT) {
 #pragma unroll
           for (int q = 0; q < kBN / 32; ++q) {
             uint32_t pk[16];
@@ -988,7 +1181,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::st16(tmem + lane_base + colS + q * 16, pk);
           }
         } else {
-          ls[0] = tc_softmax_split(tmem + lane_base + colS, cmin, cmax, all_live, sc, base);
+          ls[0] = tc_softmax_split<I8>(tmem + lane_base + colS, cmin, cmax, all_live, sc, base,
+                                       scl);
         }
         l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         if (__any_sync(0xffffffffu, need)) {
@@ -1009,6 +1203,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[a]));
+        if (I8 && lane == 0) mbar_arrive(smem_u32(&sh.sc_empty[tiles % kScR]));
       }
       if (!ok) break;
       // epilogue: O / l.  The tile's own query buffer, free since its last S
@@ -1016,7 +1211,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // 128-byte-swizzled d quarters (32 KiB each); then O_a is released to
       // the next item's P.V and, after the second store has read it, the
       // buffer to the query tile three steps later.
-      const uint32_t buf = (2 * n + a) % kTcQB, stage = sQ + buf * kTcQBytes;
+      const uint32_t buf = (2 * n + a) % QB, stage = sQ + buf * kTcQBytes;
       const float inv = (p >= 0 && l > 0.f) ? 1.f / l : 0.f;
       ok = mbar_wait(smem_u32(&sh.o_done[a]), n & 1, abort_flag);
       if (ok) tc::fence_after();
@@ -1085,12 +1280,12 @@ static size_t prefill_ws_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv, i
                               tl_dtype dtype) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv ||
       max_pages_per_seq <= 0 || page_size <= 0 || ring_pages < 0 ||
-      (dtype != TL_BF16 && dtype != TL_FP8_E4M3))
+      (dtype != TL_BF16 && dtype != TL_FP8_E4M3 && dtype != TL_INT8))
     return 0;
   const int tpt = std::max(1, 128 / (h_q / h_kv));
   const int64_t n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
   return ws_layout(B, n_pairs, h_kv, v_copy_keys(max_pages_per_seq, page_size, ring_pages),
-                   dtype == TL_FP8_E4M3)
+                   dtype != TL_BF16, dtype == TL_INT8)
       .total;
 }
 
@@ -1100,7 +1295,8 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
                               int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
                               int32_t page_size, int32_t window, int32_t ring_pages, float scale,
                               tl_dtype dtype, void* workspace, size_t workspace_bytes,
-                              uint32_t* error_word, void* stream) {
+                              uint32_t* error_word, void* stream,
+                              const float* k_scales = nullptr, const float* v_scales = nullptr) {
   if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || num_pages <= 0 ||
       page_size <= 0 || max_pages_per_seq <= 0 || window < 0)
     return TL_ERR_INVALID_ARG;
@@ -1112,13 +1308,17 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
     return TL_ERR_INVALID_ARG;
   if (h_q % h_kv) return TL_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale > 3.0e38f) return TL_ERR_INVALID_ARG;
-  // (e4m3 pools: q and out as for bf16; the pools hold one byte per element)
-  if ((dtype != TL_BF16 && dtype != TL_FP8_E4M3) || d != 128 || (page_size & (page_size - 1)) ||
-      page_size < 8 || page_size > 128)
+  // (e4m3 and int8 pools: q and out as for bf16; the pools hold one byte per element)
+  if ((dtype != TL_BF16 && dtype != TL_FP8_E4M3 && dtype != TL_INT8) || d != 128 ||
+      (page_size & (page_size - 1)) || page_size < 8 || page_size > 128)
     return TL_ERR_UNSUPPORTED;
   if ((int64_t)max_pages_per_seq * page_size >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
-  const bool kv8 = dtype == TL_FP8_E4M3;
+  const bool i8 = dtype == TL_INT8;
+  const bool kv8 = dtype == TL_FP8_E4M3 || i8;  // one byte per element, K read from a copy
   if (kv8 && (!aligned16(k_cache) || !aligned16(v_cache))) return TL_ERR_INVALID_ARG;
+  if (i8 && (!k_scales || !v_scales || (reinterpret_cast<uintptr_t>(k_scales) & 3u) ||
+             (reinterpret_cast<uintptr_t>(v_scales) & 3u)))
+    return TL_ERR_INVALID_ARG;
   const size_t ws_need = prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size,
                                          ring_pages, dtype);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < ws_need)
@@ -1151,7 +1351,7 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   const int64_t v_keys = v_copy_keys(max_pages_per_seq, page_size, ring_pages);
   if (v_keys >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
-  const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys, kv8);
+  const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   int* counter = reinterpret_cast<int*>(wsb);
   uint16_t* ws_v = reinterpret_cast<uint16_t*>(wsb + L.v);
@@ -1162,6 +1362,11 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   P.v_keys = (int32_t)v_keys;
   P.kv8 = kv8 ? 1 : 0;
   P.ws_k = kv8 ? reinterpret_cast<uint16_t*>(wsb + L.k) : nullptr;
+  P.k_scales = k_scales;
+  P.v_scales = v_scales;
+  P.ws_ks = i8 ? reinterpret_cast<float*>(wsb + L.ks) : nullptr;
+  P.ws_vs = i8 ? reinterpret_cast<float*>(wsb + L.vs) : nullptr;
+  P.ws_ivs = i8 ? reinterpret_cast<float*>(wsb + L.ivs) : nullptr;
   P.ctrl = counter;
   P.cvt_gx = (int32_t)((v_keys + kCvtKeys - 1) / kCvtKeys);
   P.cta_big = reinterpret_cast<int32_t*>(wsb + L.cta_big);
@@ -1192,19 +1397,24 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
         !encode_bf16_tensor_map(&vmap, ws_v, 3, vd, vs, vb, true))
       return TL_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kTcSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kTcSmem) != cudaSuccess)
+  auto tc_fast = i8 ? prefill_tc_kernel<false, true> : prefill_tc_kernel<false, false>;
+  auto tc_split = i8 ? prefill_tc_kernel<true, true> : prefill_tc_kernel<true, false>;
+  const int tc_smem = i8 ? kTcSmemI8 : kTcSmem;
+  if (cudaFuncSetAttribute(tc_fast, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(tc_split, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem) !=
+          cudaSuccess)
     return TL_ERR_CUDA;
   const int64_t n_items = (int64_t)n_pairs * B * h_kv;
   if (n_items > 0x7fffffff - 65536) return TL_ERR_UNSUPPORTED;
   const int grid = (int)std::min<int64_t>(num_sms(), n_items);
   const dim3 cvt_grid((unsigned)P.cvt_gx, B);
-  if (kv8)
-    prefill_v_f16_kernel<true><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
+  if (i8)
+    prefill_v_f16_kernel<2><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
+  else if (kv8)
+    prefill_v_f16_kernel<1><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
   else
-    prefill_v_f16_kernel<false><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
+    prefill_v_f16_kernel<0><<<cvt_grid, kCvtThreads, 0, (cudaStream_t)stream>>>(P, ws_v, counter);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
   // the plan and the attention kernel are programmatic dependent launches:
   // each becomes resident while its predecessor finishes and waits for its
@@ -1221,13 +1431,13 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   if (cudaLaunchKernelEx(&cfg, prefill_plan_kernel, P) != cudaSuccess) return TL_ERR_CUDA;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.dynamicSmemBytes = tc_smem;
   // rows whose V holds no value above 8 in magnitude (single fp16 P), then
   // the others (P split in two); each kernel skips the other's rows
-  if (cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, P, qmap, kmap, vmap, omap, box_rows,
-                         counter) != cudaSuccess ||
-      cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, P, qmap, kmap, vmap, omap, box_rows,
-                         counter + 1) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, tc_fast, P, qmap, kmap, vmap, omap, box_rows, counter) !=
+          cudaSuccess ||
+      cudaLaunchKernelEx(&cfg, tc_split, P, qmap, kmap, vmap, omap, box_rows, counter + 1) !=
+          cudaSuccess)
     return TL_ERR_CUDA;
   return launch_status();
 }
@@ -1291,4 +1501,16 @@ extern "C" tl_status tl_paged_attn_prefill_ring(
   return tl::prefill_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, positions, out, B,
                           T, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale, dtype,
                           workspace, workspace_bytes, error_word, stream);
+}
+
+extern "C" tl_status tl_paged_attn_prefill_int8(
+    const void* q, const int8_t* k_codes, const int8_t* v_codes, const float* k_scales,
+    const float* v_scales, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* positions, float* out, int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
+    int32_t d, int32_t num_pages, int32_t page_size, int32_t window, float scale,
+    void* workspace, size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  if (!k_scales || !v_scales) return TL_ERR_INVALID_ARG;
+  return tl::prefill_impl(q, k_codes, v_codes, block_table, max_pages_per_seq, positions, out, B,
+                          T, h_q, h_kv, d, num_pages, page_size, window, 0, scale, TL_INT8,
+                          workspace, workspace_bytes, error_word, stream, k_scales, v_scales);
 }

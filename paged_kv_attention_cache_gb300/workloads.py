@@ -161,20 +161,25 @@ def _poison_unused(k_cache, v_cache, pool: PagedPool, lengths) -> None:
         flat[idx] = float("nan")
 
 
-def int8_pools(case: DecodeCase, seed: int = 0, nan_unused: bool = False):
-    """Seeded int8 pools of a decode case's pool shape: codes uniform in
-    [-127, 127] (int8 [P, page_size, H_kv, d]) and per-(slot, KV head) scales
-    uniform in [0.005, 0.05] (float32 [P, H_kv, page_size]), as
+def int8_pools(case, seed: int = 0, nan_unused: bool = False, scale_range=(0.005, 0.05)):
+    """Seeded int8 pools of a decode or prefill case's pool shape: codes
+    uniform in [-127, 127] (int8 [P, page_size, H_kv, d]) and per-(slot, KV
+    head) scales uniform in scale_range (float32 [P, H_kv, page_size]), as
     (k_codes, v_codes, k_scales, v_scales) on the CPU.  With nan_unused, every
     slot no sequence position maps to holds code -128 and scale NaN."""
     g = _gen(seed, "cpu")
     P, ps, hkv, d = case.pool.num_pages, case.page_size, case.Hkv, case.d
     codes = [torch.randint(-127, 128, (P, ps, hkv, d), generator=g, dtype=torch.int8)
              for _ in range(2)]
-    scales = [torch.rand((P, hkv, ps), generator=g) * 0.045 + 0.005 for _ in range(2)]
+    lo, hi = scale_range
+    scales = [torch.rand((P, hkv, ps), generator=g) * (hi - lo) + lo for _ in range(2)]
     if nan_unused:
+        if isinstance(case, PrefillCase):
+            lengths = [p0 + max(case.T - pad, 0) for p0, pad in zip(case.p0, case.pads)]
+        else:
+            lengths = case.context_lens.tolist()
         used = torch.zeros(P * ps, dtype=torch.bool)
-        for b, L in enumerate(case.context_lens.tolist()):
+        for b, L in enumerate(lengths):
             for i, pg in enumerate(case.pool.pages_of[b]):
                 n = min(ps, L - i * ps)
                 used[pg * ps: pg * ps + max(n, 0)] = True

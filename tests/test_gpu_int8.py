@@ -175,3 +175,74 @@ def test_int8_fused_write_equals_the_two_calls(src):
     ref = oracle.paged_decode_int8(case.q, kc, vc, ks, vs, case.block_table, case.context_lens,
                                    case.scale)
     assert_close(o2, ref, f"fused int8 from {src}")
+
+
+# ----------------------------------------------------------------- prefill --
+
+def _prefill_int8(case, pools, window=0, error_word=None):
+    kc, vc, ks, vs = (t.to(DEV) for t in pools)
+    err = _err() if error_word is None else error_word
+    out = tl.tl_paged_attn_prefill_int8(case.q.to(DEV), kc, vc, ks, vs, case.block_table.to(DEV),
+                                        case.positions.to(DEV), case.scale, window=window,
+                                        error_word=err)
+    torch.cuda.synchronize()
+    if error_word is None:
+        assert int(err.item()) == 0, int(err.item())
+    return out
+
+
+def _oracle_prefill_int8(case, pools, window=0, rows=None):
+    rows = range(case.B) if rows is None else rows
+    outs = []
+    for b in rows:
+        outs.append(oracle.paged_prefill_int8(case.q[b:b + 1], *pools, case.block_table[b:b + 1],
+                                              case.positions[b:b + 1], case.scale,
+                                              window=window))
+    return outs
+
+
+def test_int8_prefill_full_batch_every_token():
+    """The B=8 x 2,048 batch (pads 0-1,500, prior context 0-6,144, H_q=32,
+    H_kv=8) over seeded int8 pools: every token of every row."""
+    case = wl.batched_prefill(seed=0)
+    pools = wl.int8_pools(case, 110)
+    out = _prefill_int8(case, pools).cpu()
+    for b, ref in enumerate(_oracle_prefill_int8(case, pools)):
+        assert_close(out[b], ref, f"int8 prefill row {b}")
+    assert torch.all(out[0, :case.pads[0]] == 0)
+
+
+@pytest.mark.parametrize("window", [0, 100, 2049])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 8), (16, 1)])
+def test_int8_prefill_windows_and_groups(hq, hkv, window):
+    T = 300
+    case = wl.prefill_case([0, 17, T - 1, T], [2000, 0, 4000, 10], T=T, Hq=hq, Hkv=hkv, d=128,
+                           seed=111, window=window)
+    pools = wl.int8_pools(case, 112, nan_unused=True)  # unread slots: code -128, scale NaN
+    out = _prefill_int8(case, pools, window).cpu()
+    for b, ref in enumerate(_oracle_prefill_int8(case, pools, window)):
+        assert_close(out[b], ref, f"int8 prefill {hq}/{hkv} w{window} row {b}")
+    assert torch.all(out[3] == 0)  # the row with no live token
+
+
+def test_int8_prefill_with_values_above_8_takes_the_split_path():
+    """Scales up to 0.1 make |code x scale| reach 12.7: those rows take P as
+    two fp16 parts; a row whose values stay below 8 does not (same bar)."""
+    case = wl.prefill_case([0, 40], [1500, 3000], T=512, Hq=32, Hkv=8, d=128, seed=113)
+    pools = list(wl.int8_pools(case, 114, scale_range=(0.02, 0.1)))
+    out = _prefill_int8(case, pools).cpu()
+    for b, ref in enumerate(_oracle_prefill_int8(case, pools)):
+        assert_close(out[b], ref, f"int8 prefill split row {b}")
+
+
+def test_int8_prefill_batched_equals_solo_bit_for_bit():
+    case = wl.prefill_case([100, 0, 700], [3000, 0, 5000], T=1024, Hq=16, Hkv=4, d=128, seed=115)
+    pools = wl.int8_pools(case, 116)
+    both = _prefill_int8(case, pools)
+    g = [t.to(DEV) for t in pools]
+    for b in range(case.B):
+        solo = tl.tl_paged_attn_prefill_int8(case.q[b:b + 1].to(DEV), *g,
+                                             case.block_table[b:b + 1].to(DEV),
+                                             case.positions[b:b + 1].to(DEV), case.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(solo[0], both[b]), f"row {b}"
