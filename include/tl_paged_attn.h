@@ -337,12 +337,30 @@ tl_status tl_paged_attn_decode_noalloc(const void* q, const void* k_cache, const
  * each row's first key (B int32, rounded up to 256 bytes), a flag per 64 keys
  * of each row (B * ceil(max_pages_per_seq * page_size / 64) int32, rounded up
  * to 256 bytes), a flag per row (B int32, rounded up to 256 bytes), and an
- * fp16 copy of the V rows the call reads, [B][h_kv][max_pages_per_seq *
- * page_size][d] (B * h_kv * max_pages_per_seq * page_size * d * 2 bytes).
+ * fp16 copy of the V rows the call reads, [B][h_kv][n_keys][d] with n_keys =
+ * max_pages_per_seq * page_size rounded up to a multiple of 128
+ * (B * h_kv * n_keys * d * 2 bytes).  It grows with the table's width; a
+ * workspace sized by tl_paged_attn_prefill_workspace_size_keys for the
+ * call's rows instead does not.
  */
 size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
                                             int32_t d, int32_t max_pages_per_seq,
                                             int32_t page_size);
+
+/*
+ * Workspace bytes of a prefill call (tl_paged_attn_prefill, _prefill_int8,
+ * _prefill_ring; dtype TL_BF16, TL_FP8_E4M3 or TL_INT8) whose rows each read
+ * at most max_row_keys keys: from the first key the row's first live token
+ * sees (window-clipped) to the row's last position.  The size does not
+ * depend on the table's width.  A call takes the copies' size from the
+ * workspace it is given (the table's positions when the workspace holds
+ * them, otherwise as many whole 128-key tiles as fit, at least 384); a row
+ * that reads more keys than that sets TL_DEVERR_CONTEXT_RANGE and its
+ * outputs are undefined.  0 for invalid sizes.
+ */
+size_t tl_paged_attn_prefill_workspace_size_keys(int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
+                                                 int32_t d, int32_t max_row_keys,
+                                                 tl_dtype dtype);
 
 /* Workspace bytes of any prefill call (0 for invalid sizes): ring_pages 0 for
  * a full-history table (tl_paged_attn_prefill, tl_paged_attn_prefill_int8) or
@@ -369,11 +387,14 @@ size_t tl_paged_attn_prefill_workspace_size_ex(int32_t B, int32_t T, int32_t h_q
  *   q            [B][T][h_q][d] bf16
  *   positions    [B][T] int32, -1 = padding
  *   out          [B][T][h_q][d] float32
- *   workspace    device scratch of at least tl_paged_attn_prefill_workspace_size(
- *                B, T, h_q, h_kv, d, max_pages_per_seq, page_size) bytes,
- *                256-byte aligned (TL_ERR_WORKSPACE otherwise); it receives
- *                the call's fp16 copy of V and work counter, so calls that may
- *                overlap on the GPU must not share one.
+ *   workspace    device scratch of tl_paged_attn_prefill_workspace_size(B, T,
+ *                h_q, h_kv, d, max_pages_per_seq, page_size) bytes (copies as
+ *                wide as the table), or of tl_paged_attn_prefill_workspace_size_keys
+ *                (copies as wide as the call's rows need), 256-byte aligned;
+ *                TL_ERR_WORKSPACE when it is missing, misaligned or holds less
+ *                than 384 keys per row.  It receives the call's fp16 copy of V
+ *                and work counters, so calls that may overlap on the GPU must
+ *                not share one.
  *   other arguments as for decode.
  * Supported: dtype TL_BF16, or TL_FP8_E4M3 for e4m3 pools (q stays bf16; the
  * codes widen exactly: K to a bf16 copy, V to an fp16 copy in the workspace,

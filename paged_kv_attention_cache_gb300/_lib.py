@@ -47,6 +47,8 @@ SIGNATURES = {
                                    i32, i32, f32, ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
     "tl_paged_attn_prefill_ring_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, i32], sz),
     "tl_paged_attn_decode_multi_workspace_size": ([i32, i32, i32, i32, i32], sz),
+    "tl_paged_attn_prefill_workspace_size_keys": ([i32, i32, i32, i32, i32, i32, ctypes.c_int],
+                                                  sz),
     "tl_paged_attn_prefill_workspace_size_ex": ([i32, i32, i32, i32, i32, i32, i32, i32,
                                                  ctypes.c_int], sz),
     "tl_paged_attn_decode_multi": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,

@@ -262,6 +262,15 @@ def tl_paged_attn_prefill_workspace_size_ex(B: int, T: int, h_q: int, h_kv: int,
         B, T, h_q, h_kv, d, max_pages_per_seq, page_size, ring_pages, dtype))
 
 
+def tl_paged_attn_prefill_workspace_size_keys(B: int, T: int, h_q: int, h_kv: int, d: int,
+                                              max_row_keys: int, dtype: int = TL_BF16) -> int:
+    """Workspace of a prefill call whose rows each read at most max_row_keys
+    keys (from the first key a row's first token sees to its last position);
+    independent of the table's width."""
+    return int(_lib.load().tl_paged_attn_prefill_workspace_size_keys(B, T, h_q, h_kv, d,
+                                                                      max_row_keys, dtype))
+
+
 def tl_paged_attn_decode_workspace_size(B: int, h_q: int, h_kv: int, d: int) -> int:
     return int(_lib.load().tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d))
 
@@ -373,13 +382,18 @@ def tl_paged_attn_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
                           window: int = 0, out: Optional[torch.Tensor] = None,
                           workspace: Optional[torch.Tensor] = None,
                           error_word: Optional[torch.Tensor] = None,
-                          stream=None) -> torch.Tensor:
-    """out[B, T, H_q, d] (float32): right-aligned batched prefill, padding at position -1."""
+                          stream=None, max_row_keys: Optional[int] = None) -> torch.Tensor:
+    """out[B, T, H_q, d] (float32): right-aligned batched prefill, padding at
+    position -1.  Without a workspace, one is allocated: as wide as the table,
+    or, with max_row_keys, as wide as rows reading at most that many keys."""
     dev, P, ps, hkv, d = _prefill_args(q, k_cache, v_cache, block_table, positions)
     B, T, hq, _ = q.shape
     out = _decode_out(out, (B, T, hq, d), dev)
-    workspace = _workspace(workspace, tl_paged_attn_prefill_workspace_size_ex(
-        B, T, hq, hkv, d, block_table.shape[1], ps, 0, _DTYPES.get(k_cache.dtype, -1)), dev)
+    dt = _DTYPES.get(k_cache.dtype, -1)
+    workspace = _workspace(workspace, tl_paged_attn_prefill_workspace_size_keys(
+        B, T, hq, hkv, d, max_row_keys, dt) if max_row_keys else
+        tl_paged_attn_prefill_workspace_size_ex(B, T, hq, hkv, d, block_table.shape[1], ps, 0,
+                                                dt), dev)
     _run("tl_paged_attn_prefill", dev, stream,
          _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
          _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window), float(scale),

@@ -160,10 +160,19 @@ inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_ke
 }
 // Keys per row of the V copy: the table's positions, or for a ring the
 // ring's positions plus the rounding of the copy's start and end to tiles.
+// Always whole 128-key tiles, so a key tile of a row lies wholly inside or
+// wholly outside its copy.
 inline int64_t v_copy_keys(int64_t max_pages_per_seq, int64_t page_size, int64_t ring_pages) {
   if (ring_pages > 0) return align_up((size_t)(ring_pages * page_size), kBN) + 2 * kBN;
-  return max_pages_per_seq * page_size;
+  return align_up((size_t)(max_pages_per_seq * page_size), kBN);
 }
+// Keys per row of a copy that holds any row whose tokens read at most
+// max_row_keys keys (from the first key its first token sees to its last
+// position): the span plus the rounding of its start and end to tiles.
+inline int64_t v_copy_keys_for_span(int64_t max_row_keys) {
+  return align_up((size_t)max_row_keys, kBN) + 2 * kBN;
+}
+constexpr int64_t kMinCopyKeys = 3 * kBN;  // the smallest copy a call accepts (one key + rounding)
 constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 // bf16 bit patterns (sign cleared) of the finite values fp16 cannot hold:
@@ -411,6 +420,10 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
   const int end = (int)min((int64_t)(pmax / kBN + 1) * kBN, (int64_t)start + P.v_keys);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     P.row_start[b] = start;
+    // the copy holds v_keys keys per row (the workspace's size): a row that
+    // reads more, within the table's positions, is reported (its outputs
+    // are undefined; nothing is read or written outside the workspace)
+    if (pmax - start + 1 > P.v_keys) report(P.error_word, TL_DEVERR_CONTEXT_RANGE);
     // a ring holds the call only if every key a token needs is still in it:
     // the call spans lo..pmax, at most ring_pages * page_size positions
     if (P.ring_pages > 0 && (int64_t)pmax - lo + 1 > (int64_t)P.ring_pages * P.page_size)
@@ -962,7 +975,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           if (lane == 0) {
-            const size_t si = ((size_t)it.b * P.h_kv + it.g) * P.v_keys + (key0 - vstart);
+            // (a row that reads past the copy was reported by the pre-pass:
+            // its scale tiles are taken from the copy's start, in bounds)
+            const int kc = key0 - vstart + kBN <= P.v_keys ? key0 - vstart : 0;
+            const size_t si = ((size_t)it.b * P.h_kv + it.g) * P.v_keys + kc;
             const uint32_t bar = smem_u32(&sh.sc_full[st]), part = kScBytes / 3;
             mbar_arrive_expect_tx(bar, kScBytes);
             bulk_g2s(sSc + st * kScBytes, P.ws_ks + si, part, bar);
@@ -1319,10 +1335,7 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   if (i8 && (!k_scales || !v_scales || (reinterpret_cast<uintptr_t>(k_scales) & 3u) ||
              (reinterpret_cast<uintptr_t>(v_scales) & 3u)))
     return TL_ERR_INVALID_ARG;
-  const size_t ws_need = prefill_ws_size(B, T, h_q, h_kv, d, max_pages_per_seq, page_size,
-                                         ring_pages, dtype);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < ws_need)
-    return TL_ERR_WORKSPACE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TL_ERR_WORKSPACE;
   PrefillParams P;
   P.q = static_cast<const __nv_bfloat16*>(q);
   P.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
@@ -1348,9 +1361,27 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   const int group = h_q / h_kv;
   const int tpt = 128 / group;
   const int box_rows = page_size % 16 == 0 ? 16 : 8;
-  const int64_t v_keys = v_copy_keys(max_pages_per_seq, page_size, ring_pages);
-  if (v_keys >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
+  // keys per row of the copies: the table's (or the ring's) positions when
+  // the workspace holds them; otherwise as many 128-key tiles as it holds
+  // (a workspace sized by tl_paged_attn_prefill_workspace_size_keys), at
+  // least kMinCopyKeys
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
+  int64_t v_keys = v_copy_keys(max_pages_per_seq, page_size, ring_pages);
+  if (v_keys >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
+  if (workspace_bytes < ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8).total) {
+    const WsLayout full = ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8);
+    const size_t copies = full.total - full.v;  // copies and scales of every row at v_keys keys
+    const size_t room = workspace_bytes > full.v ? workspace_bytes - full.v : 0;
+    // their bytes per key of a row (over all rows and KV heads; the rounding
+    // of each array to 256 bytes aside: the loop below checks the layout)
+    const size_t per_key = copies / (size_t)v_keys + 1;
+    int64_t fit = (int64_t)(room / per_key);
+    fit = fit / kBN * kBN;
+    while (fit >= kMinCopyKeys && ws_layout(B, n_pairs, h_kv, fit, kv8, i8).total > workspace_bytes)
+      fit -= kBN;
+    if (fit < kMinCopyKeys) return TL_ERR_WORKSPACE;
+    v_keys = fit;
+  }
   const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   int* counter = reinterpret_cast<int*>(wsb);
@@ -1513,4 +1544,18 @@ extern "C" tl_status tl_paged_attn_prefill_int8(
   return tl::prefill_impl(q, k_codes, v_codes, block_table, max_pages_per_seq, positions, out, B,
                           T, h_q, h_kv, d, num_pages, page_size, window, 0, scale, TL_INT8,
                           workspace, workspace_bytes, error_word, stream, k_scales, v_scales);
+}
+
+extern "C" size_t tl_paged_attn_prefill_workspace_size_keys(int32_t B, int32_t T, int32_t h_q,
+                                                            int32_t h_kv, int32_t d,
+                                                            int32_t max_row_keys,
+                                                            tl_dtype dtype) {
+  if (B <= 0 || T <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv || max_row_keys <= 0 ||
+      (dtype != TL_BF16 && dtype != TL_FP8_E4M3 && dtype != TL_INT8))
+    return 0;
+  const int tpt = std::max(1, 128 / (h_q / h_kv));
+  const int64_t n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
+  return tl::ws_layout(B, n_pairs, h_kv, tl::v_copy_keys_for_span(max_row_keys),
+                       dtype != TL_BF16, dtype == TL_INT8)
+      .total;
 }

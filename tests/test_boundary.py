@@ -68,6 +68,10 @@ def test_device_error_query_refuses_a_bad_word_before_any_cuda_call(lib):
     assert lib.tl_get_device_error(4098, None, 1, None) == tl.TL_ERR_INVALID_ARG  # misaligned
 
 
+def align256(x):
+    return (x + 255) // 256 * 256
+
+
 def test_workspace_sizes(lib):
     assert tl.tl_paged_attn_decode_workspace_size(64, 32, 8, 128) > 0
     assert tl.tl_paged_attn_decode_workspace_size(64, 30, 8, 128) == 0  # h_q % h_kv
@@ -85,6 +89,18 @@ def test_workspace_sizes(lib):
         256 + 2 * 1024 + 256 + 2304 + 256 + 8 * 8 * (4224 + 256) * 128 * 2
     assert tl.tl_paged_attn_prefill_ring_workspace_size(8, 2048, 32, 8, 128, 512, 16, 0) == 0
     assert tl.tl_paged_attn_prefill_workspace_size(8, 2048, 32, 8, 128, 0, 16) == 0
+    # sized by the rows' keys instead of the table: the same layout with the
+    # copy holding align_up(max_row_keys, 128) + 256 keys per row, whatever the
+    # table's width (8192 keys -> 8448; 8448 / 64 = 132 flags per row)
+    assert tl.tl_paged_attn_prefill_workspace_size_keys(8, 2048, 32, 8, 128, 8192, 1) == \
+        256 + 2 * 1024 + 256 + align256(8 * 132 * 4) + 256 + 8 * 8 * 8448 * 128 * 2
+    assert tl.tl_paged_attn_prefill_workspace_size_keys(8, 2048, 32, 8, 128, 0, 1) == 0
+    # e4m3 and int8 pools add the bf16 copy of K (int8: and three scale arrays)
+    kv = 8 * 8 * 8448
+    assert tl.tl_paged_attn_prefill_workspace_size_keys(8, 2048, 32, 8, 128, 8192, 2) == \
+        tl.tl_paged_attn_prefill_workspace_size_keys(8, 2048, 32, 8, 128, 8192, 1) + kv * 256
+    assert tl.tl_paged_attn_prefill_workspace_size_keys(8, 2048, 32, 8, 128, 8192, 3) == \
+        tl.tl_paged_attn_prefill_workspace_size_keys(8, 2048, 32, 8, 128, 8192, 2) + 3 * kv * 4
     # the decode bound grows with B and h_q but not with context length
     a = tl.tl_paged_attn_decode_workspace_size(64, 32, 8, 128)
     b = tl.tl_paged_attn_decode_workspace_size(128, 32, 8, 128)

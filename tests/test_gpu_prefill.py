@@ -146,3 +146,53 @@ def test_small_workspace_is_refused():
         tl.tl_paged_attn_prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.positions, g.scale,
                                  workspace=ws)
     assert e.value.status == tl.TL_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3", "int8"])
+def test_workspace_sized_by_the_rows_keys(kind):
+    """A table of 131,072 positions per row (8,192 pages of 16) with rows that
+    read at most ~3,300 keys: a workspace sized by the rows' keys (independent
+    of the table's width) gives the same bits as one as wide as the table."""
+    case = wl.prefill_case([0, 100, 900], [3000, 0, 1200], T=300, Hq=16, Hkv=4, d=128, seed=13,
+                           max_pages_per_seq=8192, device="cuda")
+    g = on_gpu(case)
+    gpu_write(g)
+    B, T, hq, hkv, d = case.B, case.T, case.Hq, case.Hkv, case.d
+    if kind == "int8":
+        pools = [t.to("cuda") for t in wl.int8_pools(case, 14)]
+        dt = tl.TL_INT8
+    elif kind == "e4m3":
+        pools = [g.k_cache.float().to(torch.float8_e4m3fn), g.v_cache.float().to(torch.float8_e4m3fn)]
+        dt = tl.TL_FP8_E4M3
+    else:
+        pools = [g.k_cache, g.v_cache]
+        dt = tl.TL_BF16
+    wide = tl.tl_paged_attn_prefill_workspace_size_ex(B, T, hq, hkv, d, 8192, 16, 0, dt)
+    narrow = tl.tl_paged_attn_prefill_workspace_size_keys(B, T, hq, hkv, d, 3300, dt)
+    assert narrow * 20 < wide
+    outs = []
+    for nbytes in (wide, narrow):
+        ws = tl.alloc_workspace(nbytes, "cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if kind == "int8":
+            o = tl.tl_paged_attn_prefill_int8(g.q, *pools, g.block_table, g.positions, g.scale,
+                                              workspace=ws, error_word=err)
+        else:
+            o = tl.tl_paged_attn_prefill(g.q, *pools, g.block_table, g.positions, g.scale,
+                                         workspace=ws, error_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(o)
+    assert torch.equal(outs[0], outs[1])
+    # a workspace too small for a row's keys: reported, nothing outside it touched
+    ws = tl.alloc_workspace(tl.tl_paged_attn_prefill_workspace_size_keys(B, T, hq, hkv, d, 1000,
+                                                                         dt), "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if kind == "int8":
+        tl.tl_paged_attn_prefill_int8(g.q, *pools, g.block_table, g.positions, g.scale,
+                                      workspace=ws, error_word=err)
+    else:
+        tl.tl_paged_attn_prefill(g.q, *pools, g.block_table, g.positions, g.scale, workspace=ws,
+                                 error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & tl.TL_DEVERR_CONTEXT_RANGE
