@@ -832,6 +832,38 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
     prefill_line["int8_pools"] = {"ms_per_call": round(i_ms, 4), "tflops": round(i_tflops, 2),
                                   "frac": round(i_tflops / bf16, 4)}
     del kc8, vc8, ks8, vs8, pws_i8
+    # the same shape on the sliding-window mix's values (1% of Q, K and V x8):
+    # every row's V holds values above 8, so every row takes P as two fp16 parts
+    ocase = wl.batched_prefill(seed=args.seed + rank + 7, device=dev, outlier_p=0.01)
+    og = wl.to_device(ocase, dev)
+    tl.tl_kv_cache_write(og.k_new.view(-1, ocase.Hkv, ocase.d), og.v_new.view(-1, ocase.Hkv, ocase.d),
+                         og.k_cache, og.v_cache, og.slot_mapping)
+    oflops = prefill_flops(ocase.positions, ocase.Hq, ocase.d)
+    ows = tl.alloc_workspace(tl.tl_paged_attn_prefill_workspace_size(
+        ocase.B, ocase.T, ocase.Hq, ocase.Hkv, ocase.d, ocase.block_table.shape[1],
+        ocase.page_size), dev)
+
+    def pf_o():
+        tl.tl_paged_attn_prefill(og.q, og.k_cache, og.v_cache, og.block_table, og.positions,
+                                 ocase.scale, out=pout, workspace=ows)
+
+    for _ in range(max(3, args.warmup)):
+        pf_o()
+    torch.cuda.synchronize()
+    oev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.prefill_steps)]
+    for a, b in oev:
+        a.record(stream)
+        pf_o()
+        b.record(stream)
+    torch.cuda.synchronize()
+    o_ms = statistics.mean(a.elapsed_time(b) for a, b in oev)
+    o_tflops = oflops / (o_ms * 1e-3) / 1e12
+    prefill_line["outlier_values"] = {
+        "workload": "the same shape, 1% of Q, K and V values x8 (every row takes P as two fp16 "
+                    "parts)", "ms_per_call": round(o_ms, 4), "tflops": round(o_tflops, 2),
+        "frac": round(o_tflops / bf16, 4)}
+    del og, ows
     return prefill_line, write_line
 
 

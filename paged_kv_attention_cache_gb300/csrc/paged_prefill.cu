@@ -110,12 +110,21 @@ __device__ __forceinline__ int table_index(const PrefillParams& P, int blk) {
 }
 
 constexpr int kBN = 128;             // keys per tile
-constexpr int kTcQB = 3;             // query-tile buffers (two in use, one filling)
+#ifndef TL_PREFILL_QB
+#define TL_PREFILL_QB 3
+#endif
+#ifndef TL_PREFILL_KS
+#define TL_PREFILL_KS 2
+#endif
+#ifndef TL_PREFILL_VS
+#define TL_PREFILL_VS 2
+#endif
+constexpr int kTcQB = TL_PREFILL_QB;  // query-tile buffers (two in use, one filling)
 constexpr int kTcQBI8 = 2;           // int8 pools: two (the key-scale ring takes the third's room)
 constexpr int kScR = 4;              // int8 pools: key-scale tiles in flight
 constexpr int kScBytes = 3 * 128 * 4;  // one key tile's K scales, V scales and 1 / V scales
-constexpr int kTcKS = 2;             // K stages
-constexpr int kTcVS = 2;             // V stages
+constexpr int kTcKS = TL_PREFILL_KS;  // K stages
+constexpr int kTcVS = TL_PREFILL_VS;  // V stages
 constexpr int kTcWarps = 10;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kItemSlots = 4;        // work items fetched ahead of their use
@@ -172,6 +181,10 @@ inline int64_t v_copy_keys(int64_t max_pages_per_seq, int64_t page_size, int64_t
 inline int64_t v_copy_keys_for_span(int64_t max_row_keys) {
   return align_up((size_t)max_row_keys, kBN) + 2 * kBN;
 }
+#ifndef TL_PREFILL_REREAD_CH
+#define TL_PREFILL_REREAD_CH 1
+#endif
+constexpr int kRereadCh = TL_PREFILL_REREAD_CH;  // 32-column chunks of S reread per TMEM round trip
 constexpr int64_t kMinCopyKeys = 3 * kBN;  // the smallest copy a call accepts (one key + rounding)
 constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;
@@ -694,17 +707,22 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t tmem, int a, uint32_t vbase
 // TWO = false (int8 pools only): P' = fp16(p x v_scale) as one value in
 // columns [16q, 16q + 16) (the layout of the single-fp16 path), and the sum
 // takes the weight each P' stands for, P' / v_scale (p for a zero scale).
-template <bool I8, bool TWO = true>
+template <bool I8, bool TWO = true, int CH = 1>
 __device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int cmax,
                                                   bool all_live, float sc, float base,
                                                   const float* scl) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};
   const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
 #pragma unroll 1
-  for (int q = 0; q < kBN / 32; ++q) {
-    float x[32];
-    tc::ld32(taddr + 32 * q, x);
-    tc::wait_ld();
+  for (int q0 = 0; q0 < kBN / 32; q0 += CH) {
+  float xx[CH][32];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) tc::ld32(taddr + 32 * (q0 + c), xx[c]);
+  tc::wait_ld();
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int q = q0 + c;
+    float* x = xx[c];
     if (I8) {  // int8 pools: the K scales (scl[0, 128))
 #pragma unroll
       for (int c = 0; c < 32; ++c) x[c] *= scl[32 * q + c];
@@ -741,6 +759,7 @@ __device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int 
     } else {
       tc::st16(taddr + 16 * q, pk);
     }
+  }
   }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
@@ -1181,7 +1200,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
         if constexpr (!SPLIT && I8) {
-          ls[0] = tc_softmax_split<true, false>(tmem + lane_base + colS, cmin, cmax, all_live, sc,
+          ls[0] = tc_softmax_split<true, false, kRereadCh>(tmem + lane_base + colS, cmin, cmax, all_live, sc,
                                                 base, scl);
         } else if constexpr (!SPLIT) {
 #pragma unroll
@@ -1197,7 +1216,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::st16(tmem + lane_base + colS + q * 16, pk);
           }
         } else {
-          ls[0] = tc_softmax_split<I8>(tmem + lane_base + colS, cmin, cmax, all_live, sc, base,
+          ls[0] = tc_softmax_split<I8, true, kRereadCh>(tmem + lane_base + colS, cmin, cmax, all_live, sc, base,
                                        scl);
         }
         l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
