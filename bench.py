@@ -39,8 +39,9 @@ WORKLOAD = "Llama-3-8B-shaped decode layer: B=64, Hq=32, Hkv=8, d=128, bf16, pag
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
 # these default workloads (the summaries under profiles/ give the command); they hold
 # only for the kernels as they were captured and for these workloads.
-DECODE_TRAFFIC = (1264400896 + 4529408, "profiles/decode_bf16_llama8b_b64.md")
-PREFILL_TRAFFIC = (334014976 + 207454976, "profiles/prefill_tc_batched_b8.md")
+DECODE_TRAFFIC = (1264397824 + 3987456, "profiles/decode_bf16_llama8b_b64.md")
+PREFILL_TRAFFIC = (335559424 + 206940672, "profiles/prefill_tc_batched_b8.md")
+WRITE_TRAFFIC = (40167168 + 2732032, "profiles/kv_cache_write_prefill_chunk_16k.md")
 
 
 def peaks():
@@ -767,7 +768,10 @@ def run_prefill(args, rank, dev, stream, hbm, bf16, bf16_sus, src):
                   "ms_per_call_alone": round(w_ms_call, 5),
                   "frac_per_call_alone": round(w_bytes / (w_ms_call * 1e-3) / 1e9 / hbm, 4),
                   "l2": "four chunks in turn (256 MB of new rows, 160 MB of destination rows): "
-                        "no call finds its rows in L2"}
+                        "no call finds its rows in L2",
+                  "traffic": WRITE_TRAFFIC[0],
+                  "traffic_source": WRITE_TRAFFIC[1] + " (one write, cold; its 40 MB of row "
+                                    "writes land in L2 and drain during later work)"}
     if rank == 0 and not args.no_cpu_baseline and args.only == "all":
         prefill_line["cpu_baseline"] = prefill_cpu_baseline(pcase, pg, args)
     # the same call over e4m3 pools (the bf16 pools written through the
