@@ -473,15 +473,15 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 // Persistent, one CTA per SM, every warp independent (no CTA barrier after
 // set-up).  A warp owns whole work items (piece x KV head), taken from an
 // atomic counter, and streams their 16-key chunks through a private ring of
-// kRingW shared-memory stages (one chunk per stage, two for e4m3 pools): one
+// shared-memory stages (one chunk per stage, two for one-byte pools): one
 // lane per box issues the stage's tiled TMA boxes (a 3-D tensor map of the
 // pool (d, H_kv, slot), boxes of 8 or 16 rows = one page run, 4 boxes per
 // 8 KiB stage at page size 16) completing on the stage's mbarrier by
-// transaction bytes, kRingW-1 stages ahead of the one the warp computes.  The
+// transaction bytes, all but one stage ahead of the one the warp computes.  The
 // stream runs across item boundaries: the next item's descriptor and
 // block-table window are fetched during the current item's last kGrabLead
-// stages, and each item's Q rows arrive by a bulk copy into one of kRingW Q
-// slots.  Stage layout: the stage's K chunks then its V chunks, each as
+// stages, and each item's Q rows arrive by a bulk copy into one of the ring's
+// Q slots.  Stage layout: the stage's K chunks then its V chunks, each as
 // [row half (64 elements = 128 B)][16 rows][128 B] in the
 // TMA 128-byte swizzle (16-byte unit u of row r at unit u ^ (r & 7), so
 // ldmatrix reads of 8 rows hit 8 different bank groups).  A box of a block
@@ -491,39 +491,42 @@ __device__ __forceinline__ void describe_item(const DecodeParams& P, int item, I
 // warp writes the output (one split) or a partial straight from its
 // registers.
 
-#ifndef TL_DECODE_RING
-#define TL_DECODE_RING 3
-#endif
-#ifndef TL_DECODE_WARPS
-#define TL_DECODE_WARPS 8
-#endif
-constexpr int kRingW = TL_DECODE_RING;      // stages per warp
-constexpr int kMaxRing = kRingW;
-constexpr int kMaxWarpsW = TL_DECODE_WARPS;
 constexpr int kGrabLead = 4;  // stages left to issue when a warp starts fetching its next item
 
-// Per-warp shared memory: kRingW stages of kCps chunks of K and V as the TMA
-// lands them (16-bit or e4m3 elements, rows split in 128-byte parts; an e4m3
-// stage holds two chunks, the same 8 KiB as one 16-bit chunk, so each stage's
-// issue and wait serve 32 keys) and kRingW Q slots.
-template <int D, bool KV8 = false, bool I8 = false>
+// Warps per CTA and stages per warp of a kernel variant.  The one-byte
+// kernels with at most 8 rows (keys as the MMA's rows) fit 168 registers:
+// 12 warps (three per SMSP) with 2-stage rings, one 8 KiB stage in flight
+// per warp (measured on the 64-sequence Llama-3-8B layer over e4m3 pools:
+// 0.1335 ms per step with 8 warps x 3 stages, 0.1196 ms with 12 x 2).  The
+// others take up to 235 registers: 8 warps (two per SMSP), 3-stage rings.
+template <bool TWO_ROWS, bool KV8>
+struct DecodeShape {
+  static constexpr bool kKeysAsRows = KV8 && !TWO_ROWS;
+  static constexpr int kWarps = kKeysAsRows ? 12 : 8;
+  static constexpr int kRing = kKeysAsRows ? 2 : 3;
+};
+
+// Per-warp shared memory: RING stages of kCps chunks of K and V as the TMA
+// lands them (16-bit or one-byte elements, rows split in 128-byte parts; a
+// one-byte stage holds two chunks, the same 8 KiB as one 16-bit chunk, so
+// each stage's issue and wait serve 32 keys) and RING Q slots.
+template <int D, bool KV8, bool I8, int RING>
 struct WarpSmem {
-  static constexpr int kRing = kRingW;                    // stages (and Q slots) per warp
+  static constexpr int kRing = RING;                      // stages (and Q slots) per warp
   static constexpr int kCps = KV8 ? 2 : 1;                 // chunks per stage
   static constexpr int kRowBytes = D * (KV8 ? 1 : 2);
   static constexpr int kHalves = kRowBytes / 128;          // 128-byte parts of a row
   static constexpr int kHalfBytes = kChunk * 128;          // 16 rows of one part
   static constexpr int kChunkBytes = kHalves * kHalfBytes;  // one of K or V
   static constexpr int kStageBytes = 2 * kCps * kChunkBytes;  // K chunks, then V chunks
-  // int8 pools: a stage's key scales, [K, V][chunk][16] f32, after the ring's
-  // stages (their area rounded to 1 KiB keeps the next warp's ring aligned)
+  // int8 pools: a stage's key scales, [K, V][chunk][16] f32, in static
+  // shared memory (kept out of the 1 KiB-aligned per-warp area)
   static constexpr int kScaleBytes = I8 ? 2 * kCps * kChunk * 4 : 0;
-  static constexpr int kScaleArea = (kRing * kScaleBytes + 1023) / 1024 * 1024;
   __host__ __device__ static int qslot_bytes(int rows) {
     return (rows * D * 2 + 1023) / 1024 * 1024;
   }
   __host__ __device__ static int warp_bytes(int rows) {
-    return kRing * (kStageBytes + qslot_bytes(rows)) + kScaleArea;
+    return kRing * (kStageBytes + qslot_bytes(rows));
   }
 };
 
@@ -557,6 +560,15 @@ __device__ __forceinline__ void split16(float a, float b, uint32_t& hi, uint32_t
     split_f16x2(a, b, hi, lo);
   else
     split_bf16x2(a, b, hi, lo);
+}
+
+// An 8 x 8 matrix of 16-bit elements held as m8n8 fragments (lane 4g + t:
+// row g, columns 2t and 2t + 1 in the low and high halves) transposed
+// across the warp: lane 4g + t gets row g of the transpose.
+__device__ __forceinline__ uint32_t transpose_m8n8_b16(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+  return r;
 }
 
 // One bf16 pair as an fp16 pair (queries against an e4m3 pool; finite
@@ -619,22 +631,25 @@ struct ItemSlot {
   int b, g, lo, p, c_begin, c_end, s_global, nsplits;
 };
 
+template <int NW, int R>
 struct WarpShared {
-  unsigned long long full[kMaxWarpsW][kMaxRing], qfull[kMaxWarpsW][kMaxRing];
-  uint32_t stage_mask[kMaxWarpsW][kMaxRing];
-  ItemSlot slot[kMaxWarpsW][kMaxRing];
+  unsigned long long full[NW][R], qfull[NW][R];
+  uint32_t stage_mask[NW][R];
+  ItemSlot slot[NW][R];
   int abort_flag;
 };
 
 template <int D, bool TWO_ROWS, bool KV8, bool I8 = false>
-__global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
+__global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
     decode_bf16_kernel(DecodeParams P, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, int box_rows) {
   static_assert(!I8 || KV8, "int8 pools take the one-byte path");
-  using L = WarpSmem<D, KV8, I8>;
+  using S = DecodeShape<TWO_ROWS, KV8>;
+  using L = WarpSmem<D, KV8, I8, S::kRing>;
   constexpr int R = L::kRing;  // stages per warp
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ WarpShared sh;
+  __shared__ WarpShared<S::kWarps, R> sh;
+  __shared__ __align__(128) unsigned char scale_sm[I8 ? S::kWarps * R * L::kScaleBytes : 16];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t sbase0 = (smem_u32(smem_raw) + 1023u) & ~1023u;
   unsigned char* smem0 = smem_raw + (sbase0 - smem_u32(smem_raw));
@@ -661,8 +676,9 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
   const int qslot = L::qslot_bytes(P.rows);
   const uint64_t kv_policy = l2_evict_first();
   const uint32_t ring = sbase0 + w * L::warp_bytes(P.rows);
-  const uint32_t scale_ring = ring + R * L::kStageBytes;  // int8 pools: the stages' scales
-  const uint32_t qbase = scale_ring + L::kScaleArea;
+  // int8 pools: the stages' scales
+  const uint32_t scale_ring = smem_u32(scale_sm) + w * R * L::kScaleBytes;
+  const uint32_t qbase = ring + R * L::kStageBytes;
   const unsigned char* qbase_ptr = smem0 + (qbase - sbase0);
   const int total_items = __ldcg(P.ws.ctrl + 1) * P.h_kv;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(P.q);
@@ -844,6 +860,14 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
 
   // -------------------------------------------------------- compute side
   const int qr = lane >> 2, qc = (lane & 3) * 2;
+  // One-byte pools with at most 8 rows take the keys as the MMA's rows:
+  // S^T = K Q^T (16 keys x 8 columns) and O^T += V^T P^T (16 d x 8 columns),
+  // half the MMAs and half the accumulators of rows-as-rows.  Column c holds
+  // row c; with at most 4 rows, columns 4-7 repeat rows 0-3 and carry the
+  // low parts of P (dup).
+  constexpr bool KT = S::kKeysAsRows;
+  const bool dup = KT && P.rows <= 4;
+  const int qrow = dup ? (qr & 3) : qr;  // the query row of this lane's B-operand column
   uint32_t gs_c = 0;
   int items_c = 0;
   bool stop = false;
@@ -863,9 +887,10 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       // on both operands leaves Q.K^T unchanged)
       const int e0 = ks * 16 + (KV8 ? 4 * (lane & 3) : qc);
       const int e2 = KV8 ? e0 + 2 : e0 + 8;
-      qa[ks][0] = qr < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e0) * 2) : 0u;
+      qa[ks][0] =
+          qrow < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qrow * D + e0) * 2) : 0u;
       qa[ks][2] =
-          qr < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qr * D + e2) * 2) : 0u;
+          qrow < P.rows ? *reinterpret_cast<const uint32_t*>(qs + (qrow * D + e2) * 2) : 0u;
       if (TWO_ROWS) {
         qa[ks][1] = qr + 8 < P.rows
                         ? *reinterpret_cast<const uint32_t*>(qs + ((qr + 8) * D + e0) * 2)
@@ -890,14 +915,20 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
       report(P.error_word, TL_DEVERR_VALUE_RANGE);
     __syncwarp();
 
-    float o[D / 8][4];
+    // rows-as-rows: o[n] is n-tile n of O (16 rows x 8 d); keys-as-rows:
+    // o[j] is O^T for d = 16j .. 16j + 15 (16 d x 8 columns)
+    constexpr int NO = KT ? D / 16 : D / 8;
+    float o[NO][4];
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     // with several query tokens, each row has its own key range: row r is
     // token r / group, at position p - (q_len - 1 - r / group)
-    const int pr0 = it.p - (P.q_len - 1 - qr / P.group);
-    const int pr1 = it.p - (P.q_len - 1 - (qr + 8) / P.group);
+    // (keys-as-rows: the rows of columns 2t and 2t + 1)
+    const int ra = KT ? (dup ? (qc & 3) : qc) : qr;
+    const int rb = KT ? ra + 1 : qr + 8;
+    const int pr0 = it.p - (P.q_len - 1 - ra / P.group);
+    const int pr1 = it.p - (P.q_len - 1 - rb / P.group);
     const int lr0 = (P.window > 0 && pr0 - P.window + 1 > 0) ? pr0 - P.window + 1 : 0;
     const int lr1 = (P.window > 0 && pr1 - P.window + 1 > 0) ? pr1 - P.window + 1 : 0;
     for (int c0 = it.c_begin; c0 < it.c_end; c0 += CPS, ++gs_c) {
@@ -935,212 +966,139 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
           __syncwarp();
         }
       }
-      // S = Q K^T over each chunk's 16 keys (two n-tiles of 8 keys); even and
-      // odd K steps accumulate separately (two independent MMA chains)
-      float s[NJ][2][4];
+      if constexpr (KT) {
+      // S^T = K Q^T per chunk: lane (g, t) gets the scores of keys g and
+      // g + 8 in columns 2t and 2t + 1 (s[j] = {(2t, g), (2t+1, g), (2t, g+8),
+      // (2t+1, g+8)}).  K's A fragments are the same widened codes as the B
+      // fragments of rows-as-rows: key rows g and g + 8, d permuted as there.
+      float s[NJ][4];
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-        for (int n = 0; n < 2; ++n) s[j][n][0] = s[j][n][1] = s[j][n][2] = s[j][n][3] = 0.f;
+        s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
         if (j >= nj) continue;
         const uint32_t kaddr = ring + stage * L::kStageBytes + (sub0 + j) * L::kChunkBytes;
-        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if constexpr (KV8) {
-          // the B fragment of key row n0 + g straight from the e4m3 codes:
-          // lane (g, t) takes codes 16ks+4t .. +3 of the row (an 8 x 8 b16
-          // ldmatrix fragment of the 16-byte unit), widened exactly to two
-          // fp16 pairs; one ldmatrix.x4 covers both key halves of two K steps
-          const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
+        float s2[4] = {0.f, 0.f, 0.f, 0.f};
+        const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ks += 2) {
-            const int u = ks + (mi >> 1);
-            uint32_t w[4];
-            ldmatrix_x4(kaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+        for (int ks = 0; ks < D / 16; ks += 2) {
+          const int u = ks + (mi >> 1);
+          uint32_t w[4];
+          ldmatrix_x4(kaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0, b1;
-                if constexpr (I8)
-                  i8x4_as_f16x2x2(w[2 * h + nt], b0, b1);
-                else
-                  e4m3x4_as_f16x2x2(w[2 * h + nt], b0, b1);
-                mma_16816<true>((h ? s2 : s[j])[nt], qa[ks + h][0], qa[ks + h][1],
-                                qa[ks + h][2], qa[ks + h][3], b0, b1);
-              }
-          }
-        } else {
-          const int mi = lane >> 3, ri = lane & 7;
-          const int tok = (mi >> 1) * 8 + ri;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const int u = 2 * ks + (mi & 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(
-                kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
-                b1, b2, b3);
-            float(*acc)[4] = (ks & 1) ? s2 : s[j];
-            mma_16816<KV8>(acc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_16816<KV8>(acc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t a0, a1, a2, a3;
+            if constexpr (I8) {
+              i8x4_as_f16x2x2(w[2 * h], a0, a2);
+              i8x4_as_f16x2x2(w[2 * h + 1], a1, a3);
+            } else {
+              e4m3x4_as_f16x2x2(w[2 * h], a0, a2);
+              e4m3x4_as_f16x2x2(w[2 * h + 1], a1, a3);
+            }
+            mma_16816<true>(h ? s2 : s[j], a0, a1, a2, a3, qa[ks + h][0], qa[ks + h][2]);
           }
         }
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[j][n][e] += s2[n][e];
+        for (int e = 0; e < 4; ++e) s[j][e] += s2[e];
       }
-      if constexpr (I8) {
-        // int8 pools: each key's dot product times its K scale (this lane's
-        // keys 8n + qc and 8n + qc + 1 of each chunk)
+      if constexpr (I8) {  // each key's dot products times its K scale
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
           if (j >= nj) break;
-#pragma unroll
-          for (int n = 0; n < 2; ++n) {
-            float k0, k1;
-            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n"
-                         : "=f"(k0), "=f"(k1)
-                         : "r"(scale_ring + stage * L::kScaleBytes +
-                               ((sub0 + j) * kChunk + n * 8 + qc) * 4));
-            s[j][n][0] *= k0;
-            s[j][n][1] *= k1;
-            s[j][n][2] *= k0;
-            s[j][n][3] *= k1;
-          }
+          float k0, k1;
+          const uint32_t sa = scale_ring + stage * L::kScaleBytes + ((sub0 + j) * kChunk + qr) * 4;
+          asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(k0) : "r"(sa));
+          asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(k1) : "r"(sa + 32));
+          s[j][0] *= k0;
+          s[j][1] *= k0;
+          s[j][2] *= k1;
+          s[j][3] *= k1;
         }
       }
-      // scores in log2 units; keys outside the stage's live set (or, with
-      // several query tokens, outside a row's own range) score -inf.  A stage
-      // whose keys are all live skips the per-key tests.
       constexpr uint32_t all_keys = nj == 1 ? 0xffffu : 0xffffffffu;
       if (P.q_len == 1 && ((smask >> (16 * sub0)) & all_keys) == all_keys) {
 #pragma unroll
         for (int j = 0; j < NJ; ++j)
 #pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              s[j][n][e] = j < nj ? s[j][n][e] * P.scale_log2 : -INFINITY;
-              s[j][n][2 + e] = j < nj ? s[j][n][2 + e] * P.scale_log2 : -INFINITY;
-            }
+          for (int e = 0; e < 4; ++e) s[j][e] = j < nj ? s[j][e] * P.scale_log2 : -INFINITY;
       } else {
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = n * 8 + qc + e;
-          const bool ok = j < nj && ((smask >> (16 * (sub0 + j) + key)) & 1u);
-          bool ok0 = ok, ok1 = ok;
-          if (P.q_len > 1) {
-            const int kp = (c0 + sub0 + j) * kChunk + key;
-            ok0 = ok && kp >= lr0 && kp <= pr0;
-            ok1 = ok && kp >= lr1 && kp <= pr1;
-          }
-          s[j][n][e] = ok0 ? s[j][n][e] * P.scale_log2 : -INFINITY;
-          s[j][n][2 + e] = ok1 ? s[j][n][2 + e] * P.scale_log2 : -INFINITY;
-        }
-      }
-      }
-      // Lazy running max: the base moves only when a score passes it by more
-      // than 2^8 (P stays below 256), so O is rescaled rarely.  When no score
-      // of the warp passes its row's base (one vote), P is taken against the
-      // base as it stands; otherwise the rows' maxima are reduced, the bases
-      // moved and O rescaled.  Both give the same bits where the base stays.
-      bool over = m0 == -INFINITY || (TWO_ROWS && m1 == -INFINITY);
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            over |= s[j][n][e] > m0 + kLazyLog2;
-            if (TWO_ROWS) over |= s[j][n][2 + e] > m1 + kLazyLog2;
-          }
-      float p[NJ][2][4];
-      if (!__any_sync(0xffffffffu, over)) {
-        float sum0 = 0.f;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-          for (int n = 0; n < 2; ++n) {
-            p[j][n][0] = fast_exp2(s[j][n][0] - m0);
-            p[j][n][1] = fast_exp2(s[j][n][1] - m0);
-          }
-          sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
-        }
-        l0 = l0 + sum0;
-        if (TWO_ROWS) {
-          float sum1 = 0.f;
-#pragma unroll
-          for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-              p[j][n][2] = fast_exp2(s[j][n][2] - m1);
-              p[j][n][3] = fast_exp2(s[j][n][3] - m1);
-            }
-            sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
-          }
-          l1 = l1 + sum1;
-        }
-      } else {
-        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int j = 0; j < NJ; ++j)
 #pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              mx0 = fmaxf(mx0, s[j][n][e]);
-              mx1 = fmaxf(mx1, s[j][n][2 + e]);
+          for (int hk = 0; hk < 2; ++hk) {
+            const int key = qr + 8 * hk;
+            const bool ok = j < nj && ((smask >> (16 * (sub0 + j) + key)) & 1u);
+            bool ok0 = ok, ok1 = ok;
+            if (P.q_len > 1) {
+              const int kp = (c0 + sub0 + j) * kChunk + key;
+              ok0 = ok && kp >= lr0 && kp <= pr0;
+              ok1 = ok && kp >= lr1 && kp <= pr1;
             }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        const float mn0 = (m0 == -INFINITY || mx0 > m0 + kLazyLog2) ? fmaxf(m0, mx0) : m0;
-        const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
-        const float c0 = fast_exp2(m0 - base0);
-        m0 = mn0;
-        float sum0 = 0.f;
+            s[j][2 * hk] = ok0 ? s[j][2 * hk] * P.scale_log2 : -INFINITY;
+            s[j][2 * hk + 1] = ok1 ? s[j][2 * hk + 1] * P.scale_log2 : -INFINITY;
+          }
+      }
+      // the lazy running max of rows-as-rows, per column (m0: 2t, m1: 2t + 1);
+      // a column's keys span the 8 lanes of one t
+      bool over = m0 == -INFINITY || m1 == -INFINITY;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk) {
+          over |= s[j][2 * hk] > m0 + kLazyLog2;
+          over |= s[j][2 * hk + 1] > m1 + kLazyLog2;
+        }
+      float p[NJ][4];
+      if (!__any_sync(0xffffffffu, over)) {
+        float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-          for (int n = 0; n < 2; ++n) {
-            p[j][n][0] = fast_exp2(s[j][n][0] - base0);
-            p[j][n][1] = fast_exp2(s[j][n][1] - base0);
-          }
-          sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
+          p[j][0] = fast_exp2(s[j][0] - m0);
+          p[j][1] = fast_exp2(s[j][1] - m1);
+          p[j][2] = fast_exp2(s[j][2] - m0);
+          p[j][3] = fast_exp2(s[j][3] - m1);
+          sum0 += p[j][0] + p[j][2];
+          sum1 += p[j][1] + p[j][3];
         }
-        l0 = l0 * c0 + sum0;
-        float c1 = c0;
-        if (TWO_ROWS) {
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn1 = (m1 == -INFINITY || mx1 > m1 + kLazyLog2) ? fmaxf(m1, mx1) : m1;
-          const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-          c1 = fast_exp2(m1 - base1);
-          m1 = mn1;
-          float sum1 = 0.f;
+        l0 += sum0;
+        l1 += sum1;
+      } else {
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-              p[j][n][2] = fast_exp2(s[j][n][2] - base1);
-              p[j][n][3] = fast_exp2(s[j][n][3] - base1);
-            }
-            sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
-          }
-          l1 = l1 * c1 + sum1;
+        for (int j = 0; j < NJ; ++j) {
+          mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][2]));
+          mx1 = fmaxf(mx1, fmaxf(s[j][1], s[j][3]));
         }
-        // rows 8-15 hold either the second half of the group (TWO_ROWS) or
-        // the low part of rows 0-7's probabilities; both rescale with their row
-        if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
 #pragma unroll
-          for (int n = 0; n < D / 8; ++n) {
-            o[n][0] *= c0;
-            o[n][1] *= c0;
-            o[n][2] *= c1;
-            o[n][3] *= c1;
+        for (int x = 4; x < 32; x <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+        }
+        const float mn0 = (m0 == -INFINITY || mx0 > m0 + kLazyLog2) ? fmaxf(m0, mx0) : m0;
+        const float mn1 = (m1 == -INFINITY || mx1 > m1 + kLazyLog2) ? fmaxf(m1, mx1) : m1;
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float f0 = fast_exp2(m0 - base0), f1 = fast_exp2(m1 - base1);
+        m0 = mn0;
+        m1 = mn1;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          p[j][0] = fast_exp2(s[j][0] - base0);
+          p[j][1] = fast_exp2(s[j][1] - base1);
+          p[j][2] = fast_exp2(s[j][2] - base0);
+          p[j][3] = fast_exp2(s[j][3] - base1);
+          sum0 += p[j][0] + p[j][2];
+          sum1 += p[j][1] + p[j][3];
+        }
+        l0 = l0 * f0 + sum0;
+        l1 = l1 * f1 + sum1;
+        if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
+#pragma unroll
+          for (int n = 0; n < NO; ++n) {
+            o[n][0] *= f0;
+            o[n][1] *= f1;
+            o[n][2] *= f0;
+            o[n][3] *= f1;
           }
         }
       }
@@ -1149,54 +1107,51 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
         if (jc >= nj) break;
         const uint32_t vaddr =
             ring + stage * L::kStageBytes + (CPS + sub0 + jc) * L::kChunkBytes;
-        if constexpr (I8) {
-          // int8 pools: each probability times its key's V scale (a key
-          // outside the live set has p = 0 and keeps it, whatever its scale)
-#pragma unroll
-          for (int n = 0; n < 2; ++n) {
-            float v0, v1;
-            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n"
-                         : "=f"(v0), "=f"(v1)
-                         : "r"(scale_ring + stage * L::kScaleBytes +
-                               ((CPS + sub0 + jc) * kChunk + n * 8 + qc) * 4));
-            p[jc][n][0] = p[jc][n][0] > 0.f ? p[jc][n][0] * v0 : 0.f;
-            p[jc][n][1] = p[jc][n][1] > 0.f ? p[jc][n][1] * v1 : 0.f;
-            if (TWO_ROWS) {
-              p[jc][n][2] = p[jc][n][2] > 0.f ? p[jc][n][2] * v0 : 0.f;
-              p[jc][n][3] = p[jc][n][3] > 0.f ? p[jc][n][3] * v1 : 0.f;
-            }
-          }
+        if constexpr (I8) {  // each probability times its key's V scale
+          float v0, v1;
+          const uint32_t sa =
+              scale_ring + stage * L::kScaleBytes + ((CPS + sub0 + jc) * kChunk + qr) * 4;
+          asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v0) : "r"(sa));
+          asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v1) : "r"(sa + 32));
+          p[jc][0] = p[jc][0] > 0.f ? p[jc][0] * v0 : 0.f;
+          p[jc][1] = p[jc][1] > 0.f ? p[jc][1] * v0 : 0.f;
+          p[jc][2] = p[jc][2] > 0.f ? p[jc][2] * v1 : 0.f;
+          p[jc][3] = p[jc][3] > 0.f ? p[jc][3] * v1 : 0.f;
         }
-        // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
-        uint32_t h0, l0w, h2, l2w;
-        split16<KV8>(p[jc][0][0], p[jc][0][1], h0, l0w);
-        split16<KV8>(p[jc][1][0], p[jc][1][1], h2, l2w);
-        if constexpr (KV8) {
-          // V's B fragments from the e4m3 codes: a transposing ldmatrix of
-          // 16-byte unit j (its 16-bit elements being code pairs) hands lane
-          // (g, t) the codes 2g and 2g+1 of keys 2t and 2t+1 (and of 2t+8,
-          // 2t+9 from the second key half).  One byte permute pairs the keys
-          // per code, and the two conversions give the B fragments of d
-          // 16j+2g (n-tile 2j) and 16j+2g+1 (n-tile 2j+1).  The accumulators
-          // of n-tiles 2j and 2j+1 then hold output columns 16j+4t+(0,2) and
-          // 16j+4t+(1,3).
-          const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
-          uint32_t h1 = 0u, l1w = 0u, h3 = 0u, l3w = 0u;
-          if (TWO_ROWS) {
-            split16<true>(p[jc][0][2], p[jc][0][3], h1, l1w);
-            split16<true>(p[jc][1][2], p[jc][1][3], h3, l3w);
+        // P^T as the B operand: the fp16 pairs (columns 2t, 2t + 1) of keys g
+        // and g + 8 form the 8 x 8 blocks P^T[keys 0-7] and P^T[keys 8-15];
+        // their transposes give lane (g, t) keys 2t, 2t + 1 (and 2t + 8,
+        // 2t + 9) of column g.  P = hi + lo (fp16 pair, ~22 significant bits):
+        // with dup, columns 4-7 take the low parts; otherwise the low parts
+        // go through a second MMA into the same accumulators.
+        uint32_t xh0, xl0, xh1, xl1;
+        split_f16x2(p[jc][0], p[jc][1], xh0, xl0);
+        split_f16x2(p[jc][2], p[jc][3], xh1, xl1);
+        const bool lo_cols = qc >= 4;  // lanes t = 2, 3: columns 4-7
+        const uint32_t bh0 = transpose_m8n8_b16(dup && lo_cols ? xl0 : xh0);
+        const uint32_t bh1 = transpose_m8n8_b16(dup && lo_cols ? xl1 : xh1);
+        // V^T's A fragments from the e4m3 (int8) codes as in rows-as-rows:
+        // the transposing ldmatrix of unit j gives, after the byte permute
+        // and widening, keys (2t, 2t+1) and (2t+8, 2t+9) at d = 16j + 2g
+        // (A rows g) and 16j + 2g + 1 (A rows g + 8).  o[j] then holds
+        // O[column 2t, 2t + 1][d = 16j + 2g] (elements 0, 1) and
+        // [d = 16j + 2g + 1] (elements 2, 3).
+        const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
+        auto pv = [&](auto two_c) {
+          constexpr bool two = decltype(two_c)::value != 0;
+          uint32_t bl0 = 0u, bl1 = 0u;
+          if (two) {
+            bl0 = transpose_m8n8_b16(xl0);
+            bl1 = transpose_m8n8_b16(xl1);
           }
 #pragma unroll
           for (int j0 = 0; j0 < D / 16; j0 += 2) {
-            // units j0 and j0 + 1 of key rows 0-7 and 8-15
             const int u = j0 + (mi >> 1);
             uint32_t w[4];
             ldmatrix_x4_trans(vaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2],
                               w[3]);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const int j = j0 + h;
-              // bytes (k 2t: 2g, 2g+1; k 2t+1: 2g, 2g+1) -> (2g: k, k+1; 2g+1: k, k+1)
               uint32_t a0, b0, a1, b1;
               if constexpr (I8) {
                 i8x4_keys_as_f16x2x2(w[2 * h], a0, b0);
@@ -1205,46 +1160,328 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
                 e4m3x4_as_f16x2x2(__byte_perm(w[2 * h], 0u, 0x3120u), a0, b0);
                 e4m3x4_as_f16x2x2(__byte_perm(w[2 * h + 1], 0u, 0x3120u), a1, b1);
               }
-              if (!TWO_ROWS) {
-                mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
-                mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
-              } else {
-                mma_16816<true>(o[2 * j], h0, h1, h2, h3, a0, a1);
-                mma_16816<true>(o[2 * j], l0w, l1w, l2w, l3w, a0, a1);
-                mma_16816<true>(o[2 * j + 1], h0, h1, h2, h3, b0, b1);
-                mma_16816<true>(o[2 * j + 1], l0w, l1w, l2w, l3w, b0, b1);
+              mma_16816<true>(o[j0 + h], a0, b0, a1, b1, bh0, bh1);
+              if (two) mma_16816<true>(o[j0 + h], a0, b0, a1, b1, bl0, bl1);
+            }
+          }
+        };
+        if (dup)
+          pv(IntC<0>());
+        else
+          pv(IntC<1>());
+      }
+      } else {
+        // S = Q K^T over each chunk's 16 keys (two n-tiles of 8 keys); even and
+        // odd K steps accumulate separately (two independent MMA chains)
+        float s[NJ][2][4];
+  #pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+  #pragma unroll
+          for (int n = 0; n < 2; ++n) s[j][n][0] = s[j][n][1] = s[j][n][2] = s[j][n][3] = 0.f;
+          if (j >= nj) continue;
+          const uint32_t kaddr = ring + stage * L::kStageBytes + (sub0 + j) * L::kChunkBytes;
+          float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          if constexpr (KV8) {
+            // the B fragment of key row n0 + g straight from the e4m3 codes:
+            // lane (g, t) takes codes 16ks+4t .. +3 of the row (an 8 x 8 b16
+            // ldmatrix fragment of the 16-byte unit), widened exactly to two
+            // fp16 pairs; one ldmatrix.x4 covers both key halves of two K steps
+            const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
+  #pragma unroll
+            for (int ks = 0; ks < D / 16; ks += 2) {
+              const int u = ks + (mi >> 1);
+              uint32_t w[4];
+              ldmatrix_x4(kaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+  #pragma unroll
+              for (int h = 0; h < 2; ++h)
+  #pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                  uint32_t b0, b1;
+                  if constexpr (I8)
+                    i8x4_as_f16x2x2(w[2 * h + nt], b0, b1);
+                  else
+                    e4m3x4_as_f16x2x2(w[2 * h + nt], b0, b1);
+                  mma_16816<true>((h ? s2 : s[j])[nt], qa[ks + h][0], qa[ks + h][1],
+                                  qa[ks + h][2], qa[ks + h][3], b0, b1);
+                }
+            }
+          } else {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int tok = (mi >> 1) * 8 + ri;
+  #pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const int u = 2 * ks + (mi & 1);
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4(
+                  kaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                  b1, b2, b3);
+              float(*acc)[4] = (ks & 1) ? s2 : s[j];
+              mma_16816<KV8>(acc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+              mma_16816<KV8>(acc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+            }
+          }
+  #pragma unroll
+          for (int n = 0; n < 2; ++n)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) s[j][n][e] += s2[n][e];
+        }
+        if constexpr (I8) {
+          // int8 pools: each key's dot product times its K scale (this lane's
+          // keys 8n + qc and 8n + qc + 1 of each chunk)
+  #pragma unroll
+          for (int j = 0; j < NJ; ++j) {
+            if (j >= nj) break;
+  #pragma unroll
+            for (int n = 0; n < 2; ++n) {
+              float k0, k1;
+              asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n"
+                           : "=f"(k0), "=f"(k1)
+                           : "r"(scale_ring + stage * L::kScaleBytes +
+                                 ((sub0 + j) * kChunk + n * 8 + qc) * 4));
+              s[j][n][0] *= k0;
+              s[j][n][1] *= k1;
+              s[j][n][2] *= k0;
+              s[j][n][3] *= k1;
+            }
+          }
+        }
+        // scores in log2 units; keys outside the stage's live set (or, with
+        // several query tokens, outside a row's own range) score -inf.  A stage
+        // whose keys are all live skips the per-key tests.
+        constexpr uint32_t all_keys = nj == 1 ? 0xffffu : 0xffffffffu;
+        if (P.q_len == 1 && ((smask >> (16 * sub0)) & all_keys) == all_keys) {
+  #pragma unroll
+          for (int j = 0; j < NJ; ++j)
+  #pragma unroll
+            for (int n = 0; n < 2; ++n)
+  #pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                s[j][n][e] = j < nj ? s[j][n][e] * P.scale_log2 : -INFINITY;
+                s[j][n][2 + e] = j < nj ? s[j][n][2 + e] * P.scale_log2 : -INFINITY;
+              }
+        } else {
+  #pragma unroll
+        for (int j = 0; j < NJ; ++j)
+  #pragma unroll
+        for (int n = 0; n < 2; ++n) {
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = n * 8 + qc + e;
+            const bool ok = j < nj && ((smask >> (16 * (sub0 + j) + key)) & 1u);
+            bool ok0 = ok, ok1 = ok;
+            if (P.q_len > 1) {
+              const int kp = (c0 + sub0 + j) * kChunk + key;
+              ok0 = ok && kp >= lr0 && kp <= pr0;
+              ok1 = ok && kp >= lr1 && kp <= pr1;
+            }
+            s[j][n][e] = ok0 ? s[j][n][e] * P.scale_log2 : -INFINITY;
+            s[j][n][2 + e] = ok1 ? s[j][n][2 + e] * P.scale_log2 : -INFINITY;
+          }
+        }
+        }
+        // Lazy running max: the base moves only when a score passes it by more
+        // than 2^8 (P stays below 256), so O is rescaled rarely.  When no score
+        // of the warp passes its row's base (one vote), P is taken against the
+        // base as it stands; otherwise the rows' maxima are reduced, the bases
+        // moved and O rescaled.  Both give the same bits where the base stays.
+        bool over = m0 == -INFINITY || (TWO_ROWS && m1 == -INFINITY);
+  #pragma unroll
+        for (int j = 0; j < NJ; ++j)
+  #pragma unroll
+          for (int n = 0; n < 2; ++n)
+  #pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              over |= s[j][n][e] > m0 + kLazyLog2;
+              if (TWO_ROWS) over |= s[j][n][2 + e] > m1 + kLazyLog2;
+            }
+        float p[NJ][2][4];
+        if (!__any_sync(0xffffffffu, over)) {
+          float sum0 = 0.f;
+  #pragma unroll
+          for (int j = 0; j < NJ; ++j) {
+  #pragma unroll
+            for (int n = 0; n < 2; ++n) {
+              p[j][n][0] = fast_exp2(s[j][n][0] - m0);
+              p[j][n][1] = fast_exp2(s[j][n][1] - m0);
+            }
+            sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
+          }
+          l0 = l0 + sum0;
+          if (TWO_ROWS) {
+            float sum1 = 0.f;
+  #pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+  #pragma unroll
+              for (int n = 0; n < 2; ++n) {
+                p[j][n][2] = fast_exp2(s[j][n][2] - m1);
+                p[j][n][3] = fast_exp2(s[j][n][3] - m1);
+              }
+              sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
+            }
+            l1 = l1 + sum1;
+          }
+        } else {
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+  #pragma unroll
+          for (int j = 0; j < NJ; ++j)
+  #pragma unroll
+            for (int n = 0; n < 2; ++n)
+  #pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                mx0 = fmaxf(mx0, s[j][n][e]);
+                mx1 = fmaxf(mx1, s[j][n][2 + e]);
+              }
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+          const float mn0 = (m0 == -INFINITY || mx0 > m0 + kLazyLog2) ? fmaxf(m0, mx0) : m0;
+          const float base0 = mn0 == -INFINITY ? 0.f : mn0;  // no live key seen yet
+          const float c0 = fast_exp2(m0 - base0);
+          m0 = mn0;
+          float sum0 = 0.f;
+  #pragma unroll
+          for (int j = 0; j < NJ; ++j) {
+  #pragma unroll
+            for (int n = 0; n < 2; ++n) {
+              p[j][n][0] = fast_exp2(s[j][n][0] - base0);
+              p[j][n][1] = fast_exp2(s[j][n][1] - base0);
+            }
+            sum0 += p[j][0][0] + p[j][0][1] + p[j][1][0] + p[j][1][1];
+          }
+          l0 = l0 * c0 + sum0;
+          float c1 = c0;
+          if (TWO_ROWS) {
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn1 = (m1 == -INFINITY || mx1 > m1 + kLazyLog2) ? fmaxf(m1, mx1) : m1;
+            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+            c1 = fast_exp2(m1 - base1);
+            m1 = mn1;
+            float sum1 = 0.f;
+  #pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+  #pragma unroll
+              for (int n = 0; n < 2; ++n) {
+                p[j][n][2] = fast_exp2(s[j][n][2] - base1);
+                p[j][n][3] = fast_exp2(s[j][n][3] - base1);
+              }
+              sum1 += p[j][0][2] + p[j][0][3] + p[j][1][2] + p[j][1][3];
+            }
+            l1 = l1 * c1 + sum1;
+          }
+          // rows 8-15 hold either the second half of the group (TWO_ROWS) or
+          // the low part of rows 0-7's probabilities; both rescale with their row
+          if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
+  #pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+              o[n][0] *= c0;
+              o[n][1] *= c0;
+              o[n][2] *= c1;
+              o[n][3] *= c1;
+            }
+          }
+        }
+  #pragma unroll
+        for (int jc = 0; jc < NJ; ++jc) {
+          if (jc >= nj) break;
+          const uint32_t vaddr =
+              ring + stage * L::kStageBytes + (CPS + sub0 + jc) * L::kChunkBytes;
+          if constexpr (I8) {
+            // int8 pools: each probability times its key's V scale (a key
+            // outside the live set has p = 0 and keeps it, whatever its scale)
+  #pragma unroll
+            for (int n = 0; n < 2; ++n) {
+              float v0, v1;
+              asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n"
+                           : "=f"(v0), "=f"(v1)
+                           : "r"(scale_ring + stage * L::kScaleBytes +
+                                 ((CPS + sub0 + jc) * kChunk + n * 8 + qc) * 4));
+              p[jc][n][0] = p[jc][n][0] > 0.f ? p[jc][n][0] * v0 : 0.f;
+              p[jc][n][1] = p[jc][n][1] > 0.f ? p[jc][n][1] * v1 : 0.f;
+              if (TWO_ROWS) {
+                p[jc][n][2] = p[jc][n][2] > 0.f ? p[jc][n][2] * v0 : 0.f;
+                p[jc][n][3] = p[jc][n][3] > 0.f ? p[jc][n][3] * v1 : 0.f;
               }
             }
           }
-        } else {
-          const int mi = lane >> 3, ri = lane & 7;
-          const int tok = (mi & 1) * 8 + ri;
-          if (!TWO_ROWS) {
-#pragma unroll
-            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-              const int u = 2 * nd2 + (mi >> 1);
-              uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(
-                  vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
-                  b1, b2, b3);
-              mma_16816<KV8>(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
-              mma_16816<KV8>(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+          // O += P V with P = hi + lo (bf16 pair, ~16 significant bits)
+          uint32_t h0, l0w, h2, l2w;
+          split16<KV8>(p[jc][0][0], p[jc][0][1], h0, l0w);
+          split16<KV8>(p[jc][1][0], p[jc][1][1], h2, l2w);
+          if constexpr (KV8) {
+            // V's B fragments from the e4m3 codes: a transposing ldmatrix of
+            // 16-byte unit j (its 16-bit elements being code pairs) hands lane
+            // (g, t) the codes 2g and 2g+1 of keys 2t and 2t+1 (and of 2t+8,
+            // 2t+9 from the second key half).  One byte permute pairs the keys
+            // per code, and the two conversions give the B fragments of d
+            // 16j+2g (n-tile 2j) and 16j+2g+1 (n-tile 2j+1).  The accumulators
+            // of n-tiles 2j and 2j+1 then hold output columns 16j+4t+(0,2) and
+            // 16j+4t+(1,3).
+            const int mi = lane >> 3, row = (mi & 1) * 8 + (lane & 7);
+            uint32_t h1 = 0u, l1w = 0u, h3 = 0u, l3w = 0u;
+            if (TWO_ROWS) {
+              split16<true>(p[jc][0][2], p[jc][0][3], h1, l1w);
+              split16<true>(p[jc][1][2], p[jc][1][3], h3, l3w);
+            }
+  #pragma unroll
+            for (int j0 = 0; j0 < D / 16; j0 += 2) {
+              // units j0 and j0 + 1 of key rows 0-7 and 8-15
+              const int u = j0 + (mi >> 1);
+              uint32_t w[4];
+              ldmatrix_x4_trans(vaddr + row * 128 + ((u ^ (row & 7)) << 4), w[0], w[1], w[2],
+                                w[3]);
+  #pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int j = j0 + h;
+                // bytes (k 2t: 2g, 2g+1; k 2t+1: 2g, 2g+1) -> (2g: k, k+1; 2g+1: k, k+1)
+                uint32_t a0, b0, a1, b1;
+                if constexpr (I8) {
+                  i8x4_keys_as_f16x2x2(w[2 * h], a0, b0);
+                  i8x4_keys_as_f16x2x2(w[2 * h + 1], a1, b1);
+                } else {
+                  e4m3x4_as_f16x2x2(__byte_perm(w[2 * h], 0u, 0x3120u), a0, b0);
+                  e4m3x4_as_f16x2x2(__byte_perm(w[2 * h + 1], 0u, 0x3120u), a1, b1);
+                }
+                if (!TWO_ROWS) {
+                  mma_16816<true>(o[2 * j], h0, l0w, h2, l2w, a0, a1);
+                  mma_16816<true>(o[2 * j + 1], h0, l0w, h2, l2w, b0, b1);
+                } else {
+                  mma_16816<true>(o[2 * j], h0, h1, h2, h3, a0, a1);
+                  mma_16816<true>(o[2 * j], l0w, l1w, l2w, l3w, a0, a1);
+                  mma_16816<true>(o[2 * j + 1], h0, h1, h2, h3, b0, b1);
+                  mma_16816<true>(o[2 * j + 1], l0w, l1w, l2w, l3w, b0, b1);
+                }
+              }
             }
           } else {
-            uint32_t h1, l1w, h3, l3w;
-            split16<KV8>(p[jc][0][2], p[jc][0][3], h1, l1w);
-            split16<KV8>(p[jc][1][2], p[jc][1][3], h3, l3w);
-#pragma unroll
-            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-              const int u = 2 * nd2 + (mi >> 1);
-              uint32_t b0, b1, b2, b3;
-              ldmatrix_x4_trans(
-                  vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
-                  b1, b2, b3);
-              mma_16816<KV8>(o[2 * nd2], h0, h1, h2, h3, b0, b1);
-              mma_16816<KV8>(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
-              mma_16816<KV8>(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
-              mma_16816<KV8>(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+            const int mi = lane >> 3, ri = lane & 7;
+            const int tok = (mi & 1) * 8 + ri;
+            if (!TWO_ROWS) {
+  #pragma unroll
+              for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+                const int u = 2 * nd2 + (mi >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(
+                    vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                    b1, b2, b3);
+                mma_16816<KV8>(o[2 * nd2], h0, l0w, h2, l2w, b0, b1);
+                mma_16816<KV8>(o[2 * nd2 + 1], h0, l0w, h2, l2w, b2, b3);
+              }
+            } else {
+              uint32_t h1, l1w, h3, l3w;
+              split16<KV8>(p[jc][0][2], p[jc][0][3], h1, l1w);
+              split16<KV8>(p[jc][1][2], p[jc][1][3], h3, l3w);
+  #pragma unroll
+              for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+                const int u = 2 * nd2 + (mi >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(
+                    vaddr + (u >> 3) * L::kHalfBytes + tok * 128 + (((u & 7) ^ (tok & 7)) << 4), b0,
+                    b1, b2, b3);
+                mma_16816<KV8>(o[2 * nd2], h0, h1, h2, h3, b0, b1);
+                mma_16816<KV8>(o[2 * nd2], l0w, l1w, l2w, l3w, b0, b1);
+                mma_16816<KV8>(o[2 * nd2 + 1], h0, h1, h2, h3, b2, b3);
+                mma_16816<KV8>(o[2 * nd2 + 1], l0w, l1w, l2w, l3w, b2, b3);
+              }
             }
           }
         }
@@ -1261,67 +1498,116 @@ __global__ void __launch_bounds__(kMaxWarpsW * 32, 1)
     }
     if (stop) break;
     // ------------------------------------------------------ finish the item
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    if (TWO_ROWS) {
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    }
-    const bool single = it.nsplits == 1;
-    // output index of rows qr and qr + 8 among the sequence's q_len * h_q
-    const int h0r = (qr / P.group) * P.h_q + it.g * P.group + qr % P.group;
-    const int h1r = ((qr + 8) / P.group) * P.h_q + it.g * P.group + (qr + 8) % P.group;
-    // One output row of this lane, times f: 16-bit pools hold float pairs at
-    // columns 8n + 2t (n-tile n), e4m3 pools float quads at 16j + 4t (n-tile
-    // 2j: columns +0 and +2; n-tile 2j+1: +1 and +3).  Row qr adds the low
-    // part of P carried in rows 8-15 unless TWO_ROWS; with TWO_ROWS, rows
-    // 8-15 are row qr + 8.
-    auto write_row = [&](float* dst, bool second, float f, bool keep_in_l2, uint64_t pol) {
-      if constexpr (KV8) {
+    if constexpr (KT) {
+      // a column's sum spans the 8 lanes of one t; with dup, the low parts
+      // (columns 4-7, lanes t = 2, 3) join their rows (lanes t - 2)
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-          const float* x = o[2 * j];
-          const float* y = o[2 * j + 1];
-          const float v0 = second ? x[2] : (TWO_ROWS ? x[0] : x[0] + x[2]);
-          const float v1 = second ? y[2] : (TWO_ROWS ? y[0] : y[0] + y[2]);
-          const float v2 = second ? x[3] : (TWO_ROWS ? x[1] : x[1] + x[3]);
-          const float v3 = second ? y[3] : (TWO_ROWS ? y[1] : y[1] + y[3]);
-          float* d4 = dst + 16 * j + 4 * (lane & 3);
+      for (int x = 4; x < 32; x <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+      }
+      if (dup) {
+#pragma unroll
+        for (int n = 0; n < NO; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[n][e] += __shfl_xor_sync(0xffffffffu, o[n][e], 2);
+      }
+      const bool writer = !dup || qc < 4;
+      const bool live0 = writer && ra < P.rows, live1 = writer && rb < P.rows;
+      const int h0r = (ra / P.group) * P.h_q + it.g * P.group + ra % P.group;
+      const int h1r = (rb / P.group) * P.h_q + it.g * P.group + rb % P.group;
+      // column e (0: 2t, 1: 2t + 1) of this lane: d = 16j + 2g and 16j + 2g + 1
+      auto write_col = [&](float* dst, int e, float f, bool keep_in_l2, uint64_t pol) {
+#pragma unroll
+        for (int j = 0; j < NO; ++j) {
+          float* d2 = dst + 16 * j + 2 * qr;
+          const float v0 = (e ? o[j][1] : o[j][0]) * f, v1 = (e ? o[j][3] : o[j][2]) * f;
           if (keep_in_l2)
-            st_f32x4_hint(d4, v0 * f, v1 * f, v2 * f, v3 * f, pol);
+            st_f32x2_hint(d2, v0, v1, pol);
           else
-            *reinterpret_cast<float4*>(d4) = make_float4(v0 * f, v1 * f, v2 * f, v3 * f);
+            *reinterpret_cast<float2*>(d2) = make_float2(v0, v1);
         }
+      };
+      if (it.nsplits == 1) {
+        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        if (live0) write_col(P.out + ((size_t)it.b * P.hq_all + h0r) * D, 0, i0, false, 0);
+        if (live1) write_col(P.out + ((size_t)it.b * P.hq_all + h1r) * D, 1, i1, false, 0);
       } else {
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          const float v0 = second ? o[n][2] : (TWO_ROWS ? o[n][0] : o[n][0] + o[n][2]);
-          const float v1 = second ? o[n][3] : (TWO_ROWS ? o[n][1] : o[n][1] + o[n][3]);
-          float* d2 = dst + n * 8 + qc;
-          if (keep_in_l2)
-            st_f32x2_hint(d2, v0 * f, v1 * f, pol);
-          else
-            *reinterpret_cast<float2*>(d2) = make_float2(v0 * f, v1 * f);
+        const uint64_t keep = l2_evict_last();
+        if (live0) {
+          const size_t rowi = (size_t)it.s_global * P.hq_all + h0r;
+          write_col(P.ws.acc + rowi * D, 0, 1.f, true, keep);
+          if (qr == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m0, l0, keep);
+        }
+        if (live1) {
+          const size_t rowi = (size_t)it.s_global * P.hq_all + h1r;
+          write_col(P.ws.acc + rowi * D, 1, 1.f, true, keep);
+          if (qr == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m1, l1, keep);
         }
       }
-    };
-    if (single) {
-      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-      if (qr < P.rows) write_row(P.out + ((size_t)it.b * P.hq_all + h0r) * D, false, i0, false, 0);
-      if (TWO_ROWS && qr + 8 < P.rows)
-        write_row(P.out + ((size_t)it.b * P.hq_all + h1r) * D, true, i1, false, 0);
     } else {
-      // partials stay in L2 for the combine kernel that follows
-      const uint64_t keep = l2_evict_last();
-      if (qr < P.rows) {
-        const size_t rowi = (size_t)it.s_global * P.hq_all + h0r;
-        write_row(P.ws.acc + rowi * D, false, 1.f, true, keep);
-        if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m0, l0, keep);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      if (TWO_ROWS) {
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
       }
-      if (TWO_ROWS && qr + 8 < P.rows) {
-        const size_t rowi = (size_t)it.s_global * P.hq_all + h1r;
-        write_row(P.ws.acc + rowi * D, true, 1.f, true, keep);
-        if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m1, l1, keep);
+      const bool single = it.nsplits == 1;
+      // output index of rows qr and qr + 8 among the sequence's q_len * h_q
+      const int h0r = (qr / P.group) * P.h_q + it.g * P.group + qr % P.group;
+      const int h1r = ((qr + 8) / P.group) * P.h_q + it.g * P.group + (qr + 8) % P.group;
+      // One output row of this lane, times f: 16-bit pools hold float pairs at
+      // columns 8n + 2t (n-tile n), e4m3 pools float quads at 16j + 4t (n-tile
+      // 2j: columns +0 and +2; n-tile 2j+1: +1 and +3).  Row qr adds the low
+      // part of P carried in rows 8-15 unless TWO_ROWS; with TWO_ROWS, rows
+      // 8-15 are row qr + 8.
+      auto write_row = [&](float* dst, bool second, float f, bool keep_in_l2, uint64_t pol) {
+        if constexpr (KV8) {
+  #pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            const float* x = o[2 * j];
+            const float* y = o[2 * j + 1];
+            const float v0 = second ? x[2] : (TWO_ROWS ? x[0] : x[0] + x[2]);
+            const float v1 = second ? y[2] : (TWO_ROWS ? y[0] : y[0] + y[2]);
+            const float v2 = second ? x[3] : (TWO_ROWS ? x[1] : x[1] + x[3]);
+            const float v3 = second ? y[3] : (TWO_ROWS ? y[1] : y[1] + y[3]);
+            float* d4 = dst + 16 * j + 4 * (lane & 3);
+            if (keep_in_l2)
+              st_f32x4_hint(d4, v0 * f, v1 * f, v2 * f, v3 * f, pol);
+            else
+              *reinterpret_cast<float4*>(d4) = make_float4(v0 * f, v1 * f, v2 * f, v3 * f);
+          }
+        } else {
+  #pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            const float v0 = second ? o[n][2] : (TWO_ROWS ? o[n][0] : o[n][0] + o[n][2]);
+            const float v1 = second ? o[n][3] : (TWO_ROWS ? o[n][1] : o[n][1] + o[n][3]);
+            float* d2 = dst + n * 8 + qc;
+            if (keep_in_l2)
+              st_f32x2_hint(d2, v0 * f, v1 * f, pol);
+            else
+              *reinterpret_cast<float2*>(d2) = make_float2(v0 * f, v1 * f);
+          }
+        }
+      };
+      if (single) {
+        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        if (qr < P.rows) write_row(P.out + ((size_t)it.b * P.hq_all + h0r) * D, false, i0, false, 0);
+        if (TWO_ROWS && qr + 8 < P.rows)
+          write_row(P.out + ((size_t)it.b * P.hq_all + h1r) * D, true, i1, false, 0);
+      } else {
+        // partials stay in L2 for the combine kernel that follows
+        const uint64_t keep = l2_evict_last();
+        if (qr < P.rows) {
+          const size_t rowi = (size_t)it.s_global * P.hq_all + h0r;
+          write_row(P.ws.acc + rowi * D, false, 1.f, true, keep);
+          if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m0, l0, keep);
+        }
+        if (TWO_ROWS && qr + 8 < P.rows) {
+          const size_t rowi = (size_t)it.s_global * P.hq_all + h1r;
+          write_row(P.ws.acc + rowi * D, true, 1.f, true, keep);
+          if ((lane & 3) == 0) st_f32x2_hint(P.ws.ml + rowi * 2, m1, l1, keep);
+        }
       }
     }
     ++items_c;
@@ -1538,6 +1824,18 @@ struct NewRows {
   void* v_dst = nullptr;
 };
 
+// Warps per CTA of a bf16 / one-byte kernel variant: its shape's count, or
+// as many as the dynamic shared memory holds (227 KiB less 2 KiB for the
+// static state, the int8 scale rings and the 1 KiB alignment pad).
+template <int D, bool TWO, bool K8, bool I8>
+static int decode_warps(int rows) {
+  using S = DecodeShape<TWO, K8>;
+  using L = WarpSmem<D, K8, I8, S::kRing>;
+  static_assert(sizeof(WarpShared<S::kWarps, S::kRing>) <= 2048, "static state over 2 KiB");
+  const int scales = I8 ? S::kWarps * S::kRing * L::kScaleBytes : 0;
+  return std::min(S::kWarps, (227 * 1024 - 3072 - scales) / L::warp_bytes(rows));
+}
+
 static tl_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                              const int32_t* block_table, int32_t max_pages_per_seq,
                              const int32_t* context_lens, float* out, int32_t B, int32_t q_len,
@@ -1645,15 +1943,20 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
   }
   cudaStream_t st = (cudaStream_t)stream;
 
-  // warps per CTA of the bf16 / e4m3 kernel (as many as the stages fit)
+  // warps per CTA of the bf16 / one-byte kernel (up to its shape's count,
+  // as many as the stages fit)
   const bool kv8 = dtype == TL_FP8_E4M3;
+  const bool two = rows > 8;
   int warps = 0;
   if (dtype != TL_F32) {
-    const int per_warp = i8    ? WarpSmem<128, true, true>::warp_bytes(rows)
-                         : kv8 ? WarpSmem<128, true>::warp_bytes(rows)
-                               : (d == 128 ? WarpSmem<128, false>::warp_bytes(rows)
-                                           : WarpSmem<64, false>::warp_bytes(rows));
-    warps = std::min(kMaxWarpsW, (227 * 1024 - 2048) / per_warp);
+    warps = i8    ? (two ? decode_warps<128, true, true, true>(rows)
+                         : decode_warps<128, false, true, true>(rows))
+            : kv8 ? (two ? decode_warps<128, true, true, false>(rows)
+                         : decode_warps<128, false, true, false>(rows))
+            : d == 128 ? (two ? decode_warps<128, true, false, false>(rows)
+                              : decode_warps<128, false, false, false>(rows))
+                       : (two ? decode_warps<64, true, false, false>(rows)
+                              : decode_warps<64, false, false, false>(rows));
   }
   const int target_splits = (kTargetItems + h_kv - 1) / h_kv;
   // plan block: sequences are spread over its threads (larger batches loop),
@@ -1687,7 +1990,8 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
 #define TL_LAUNCH_W(DD, TWO, K8, I8V)                                                     \
   do {                                                                                    \
     auto kern = decode_bf16_kernel<DD, TWO, K8, I8V>;                                     \
-    const int sm = warps * WarpSmem<DD, K8, I8V>::warp_bytes(rows) + 1024;                \
+    const int sm =                                                                        \
+        warps * WarpSmem<DD, K8, I8V, DecodeShape<TWO, K8>::kRing>::warp_bytes(rows) + 1024; \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=    \
         cudaSuccess)                                                                      \
       return TL_ERR_CUDA;                                                                 \

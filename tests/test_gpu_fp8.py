@@ -161,11 +161,16 @@ def test_fp8_decode_over_rings():
     assert_close(out, ref, "fp8 ring decode")
 
 
-def test_fp8_multi_token_decode():
-    q_len = 4
+@pytest.mark.parametrize("q_len,hq,window", [(4, 32, 0), (2, 32, 0), (2, 16, 0), (3, 16, 0),
+                                             (2, 16, 300), (3, 8, 0)])
+def test_fp8_multi_token_decode(q_len, hq, window):
+    """q_len tokens x the group's heads as the kernel's rows: 16 (two row
+    groups), 8, 4 (the low parts of P in columns 4-7), 6 and 3 (unused
+    columns); with and without a window."""
     lengths = wl.llama8b_lengths(seed=9, B=12)
     p0 = [L - q_len for L in lengths]
-    case = wl.prefill_case([0] * len(lengths), p0, T=q_len, Hq=32, Hkv=8, d=128, seed=73)
+    case = wl.prefill_case([0] * len(lengths), p0, T=q_len, Hq=hq, Hkv=8, d=128, seed=73,
+                           window=window)
     k8 = case.k_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
     v8 = case.v_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
     oracle.kv_cache_write_fp8(case.k_new, case.v_new, k8, v8, case.slot_mapping)
@@ -175,12 +180,12 @@ def test_fp8_multi_token_decode():
     err = _err()
     out = tl.tl_paged_attn_decode_multi(case.q.to(DEV), k8t.to(DEV), v8t.to(DEV),
                                         case.block_table.to(DEV), cl.to(DEV), case.scale,
-                                        error_word=err)
+                                        window=window, error_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for row in (0, 6, 11):
+    for row in range(case.B):
         ref = oracle.paged_prefill(case.q[row:row + 1], k8, v8, case.block_table[row:row + 1],
-                                   case.positions[row:row + 1], case.scale)
+                                   case.positions[row:row + 1], case.scale, window=window)
         assert_close(out[row], ref, f"fp8 multi-token row {row}")
 
 

@@ -93,7 +93,8 @@ def _check(case, pools, window, rows=None, what=""):
 
 
 @pytest.mark.parametrize("window", [0, 37])
-@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 8), (32, 2)])  # groups 4, 4 and 16
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 8), (32, 2), (40, 8), (64, 8), (8, 8)])
+# groups 4, 4, 16, 5, 8 and 1
 def test_int8_decode_matches_the_oracle(hq, hkv, window):
     case = wl.decode_case([0, 1, 15, 16, 17, 33, 300, 1000], Hq=hq, Hkv=hkv, d=128, seed=92,
                           window=window)
