@@ -498,12 +498,16 @@ constexpr int kGrabLead = 4;  // stages left to issue when a warp starts fetchin
 // 12 warps (three per SMSP) with 2-stage rings, one 8 KiB stage in flight
 // per warp (measured on the 64-sequence Llama-3-8B layer over e4m3 pools:
 // 0.1335 ms per step with 8 warps x 3 stages, 0.1196 ms with 12 x 2).  The
-// others take up to 235 registers: 8 warps (two per SMSP), 3-stage rings.
+// others take up to 235 registers: 8 warps (two per SMSP).  With more than
+// 8 rows a Q slot is 4 KiB and three stages would leave room for 6 warps:
+// two stages keep 8 (the 4-token verify batch: 0.2605 ms per call with
+// 6 x 3, 0.2369 ms with 8 x 2); with at most 8 rows three stages fit 7-8
+// warps and time within 1% of two.
 template <bool TWO_ROWS, bool KV8>
 struct DecodeShape {
   static constexpr bool kKeysAsRows = KV8 && !TWO_ROWS;
   static constexpr int kWarps = kKeysAsRows ? 12 : 8;
-  static constexpr int kRing = kKeysAsRows ? 2 : 3;
+  static constexpr int kRing = (kKeysAsRows || TWO_ROWS) ? 2 : 3;
 };
 
 // Per-warp shared memory: RING stages of kCps chunks of K and V as the TMA
