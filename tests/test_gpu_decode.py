@@ -164,7 +164,7 @@ def test_workspace_is_reused_across_calls_of_different_shapes():
 def test_piece_plan_extremes(shape):
     """The decode plan cuts each sequence into bulk pieces and a last round of
     small pieces (the last ~15% of every sequence longer than 256 keys), all
-    within ceil(12288 / H_kv) + 2B pieces.  Batches at the ends of that range
+    within ceil(6144 / H_kv) + 2B pieces.  Batches at the ends of that range
     (thousands of short sequences, one very long one, both mixed) against the
     oracle on every sequence, every output finite and no device error."""
     g = torch.Generator().manual_seed(91)
