@@ -352,6 +352,17 @@ __device__ __forceinline__ void i8x8_to_f16_bf16(uint2 c, uint4& f16, uint4& bf1
   f16 = make_uint4(h[0], h[1], h[2], h[3]);
   bf16 = make_uint4(b[0], b[1], b[2], b[3]);
 }
+// Eight int8 codes times one scale, each product rounded to fp16.
+__device__ __forceinline__ uint4 i8x8_scaled_f16(uint2 c, float sc) {
+  uint32_t h[4];
+  const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t word = w[k >> 1] >> (16 * (k & 1));
+    h[k] = pack_f16x2((float)(int8_t)(word & 0xffu) * sc, (float)(int8_t)((word >> 8) & 0xffu) * sc);
+  }
+  return make_uint4(h[0], h[1], h[2], h[3]);
+}
 // Largest |code| of eight int8 codes.
 __device__ __forceinline__ uint32_t i8x8_max_abs(uint2 c) {
   const uint32_t m = __vmaxu4(__vabsss4(c.x), __vabsss4(c.y));
@@ -359,7 +370,8 @@ __device__ __forceinline__ uint32_t i8x8_max_abs(uint2 c) {
 }
 
 // KIND 0: bf16 pools (V to fp16); 1: e4m3 pools (V to fp16, K to bf16);
-// 2: int8 pools (codes: V to fp16, K to bf16; and each key's two scales).
+// 2: int8 pools (K codes to bf16; V to fp16 as codes in a tile with the
+// split-P flag, else as code x V scale; and each key's scales).
 template <int KIND>
 __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     prefill_v_f16_kernel(PrefillParams P, uint16_t* __restrict__ ws, int* counter) {
@@ -461,26 +473,128 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
   }
   __syncthreads();
   const int r0 = 0, r1 = min(end - k0, kCvtKeys);  // keys of the tile to write
-  bool big_i8 = false;  // int8 pools: some |code x scale| of V above 8
   float sumsq = 0.f;    // sum of squares of this thread's live V values
   int n_vals = 0;       // and their count
-  if (KIND == 2) {
-    // each key's K and V scale per KV head, next to its copied codes (0 for
-    // keys past pmax and bad pages, whose codes are 0 too)
+  if constexpr (KIND == 2) {
+    // int8 pools, two passes over the tile's V codes.  First the tile's
+    // split-P flag (some |code x v_scale| above 8, NaN included, or an RMS
+    // above 1.25); then the copies.  A flagged tile keeps V as its codes
+    // (exact in fp16; the attention kernel applies the V scales to the
+    // probabilities), any other tile is copied as fp16(code x v_scale) with
+    // unit V scales beside it, so that a row with no flagged tile takes P.V
+    // exactly as 16-bit pools do.  K is copied as its codes (bf16, exact).
+    const int units = P.h_kv * 16;  // 8-code units per key
+    const int total = (r1 - r0) * units;
+    const uint8_t* v8 = reinterpret_cast<const uint8_t*>(P.v_cache);
+    const uint8_t* k8 = reinterpret_cast<const uint8_t*>(P.k_cache);
+    auto scale_index = [&](int r, int g) {
+      return ((size_t)s_page[r] * P.h_kv + g) * P.page_size + (k0 + r) % P.page_size;
+    };
+    bool big_i8 = false;
+    for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
+      uint2 c[kCvtUnroll];
+      float vs[kCvtUnroll];
+#pragma unroll
+      for (int i = 0; i < kCvtUnroll; ++i) {
+        const int idx = base + i * kCvtThreads + (int)threadIdx.x;
+        c[i] = make_uint2(0u, 0u);
+        vs[i] = 0.f;
+        if (idx < total) {
+          const int r = r0 + idx / units, u = idx % units;
+          if (s_page[r] >= 0) {
+            const size_t row = ((size_t)s_page[r] * P.page_size + (k0 + r) % P.page_size) * P.h_kv * 128;
+            c[i] = __ldg(reinterpret_cast<const uint2*>(v8 + row) + u);
+            vs[i] = __ldg(P.v_scales + scale_index(r, u >> 4));
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kCvtUnroll; ++i) {
+        const int idx = base + i * kCvtThreads + (int)threadIdx.x;
+        if (idx < total && s_page[r0 + idx / units] >= 0) {
+          uint4 f16, bf16;
+          i8x8_to_f16_bf16(c[i], f16, bf16);
+          big_i8 |= !((float)i8x8_max_abs(c[i]) * vs[i] <= 8.f);
+          sumsq = fmaf(sumsq_f16x8(f16), vs[i] * vs[i], sumsq);
+          n_vals += 8;
+        }
+      }
+    }
+    // the tile's flag: a fixed-order reduction (it must repeat bit for bit)
+    __shared__ float s_sq2[kCvtThreads / 32];
+    __shared__ int s_n2[kCvtThreads / 32];
+    __shared__ int s_big;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sumsq += __shfl_xor_sync(0xffffffffu, sumsq, o);
+      n_vals += __shfl_xor_sync(0xffffffffu, n_vals, o);
+    }
+    if (lane == 0) {
+      s_sq2[warp] = sumsq;
+      s_n2[warp] = n_vals;
+    }
+    const int any_big = __syncthreads_or(big_i8);
+    if (threadIdx.x == 0) {
+      float tot = 0.f;
+      int cnt = 0;
+      for (int w = 0; w < kCvtThreads / 32; ++w) {
+        tot += s_sq2[w];
+        cnt += s_n2[w];
+      }
+      const bool wide = !(tot <= kRmsBig2 * (float)cnt);  // NaN counts as wide
+      s_big = (any_big || wide) ? 1 : 0;
+      *big_flag = s_big;
+    }
+    __syncthreads();
+    const bool tile_big = s_big != 0;
+    // each key's K scale and (a flagged tile) V scale per KV head, or unit V
+    // scales (0 for keys past pmax and bad pages, whose copies are 0)
     for (int idx = threadIdx.x; idx < (r1 - r0) * P.h_kv; idx += kCvtThreads) {
       const int r = r0 + idx / P.h_kv, g = idx % P.h_kv;
-      const int page = s_page[r];
       float ksc = 0.f, vsc = 0.f;
-      if (page >= 0) {
-        const size_t si = ((size_t)page * P.h_kv + g) * P.page_size + (k0 + r) % P.page_size;
-        ksc = __ldg(P.k_scales + si);
-        vsc = __ldg(P.v_scales + si);
+      if (s_page[r] >= 0) {
+        ksc = __ldg(P.k_scales + scale_index(r, g));
+        vsc = tile_big ? __ldg(P.v_scales + scale_index(r, g)) : 1.f;
       }
       const size_t di = ((size_t)b * P.h_kv + g) * P.v_keys + (k0 - start + r);
       P.ws_ks[di] = ksc;
       P.ws_vs[di] = vsc;
       P.ws_ivs[di] = vsc > 0.f ? 1.f / vsc : 0.f;
     }
+    for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
+      uint2 a[kCvtUnroll], c[kCvtUnroll];
+      float vs[kCvtUnroll];
+#pragma unroll
+      for (int i = 0; i < kCvtUnroll; ++i) {
+        const int idx = base + i * kCvtThreads + (int)threadIdx.x;
+        a[i] = c[i] = make_uint2(0u, 0u);
+        vs[i] = 0.f;
+        if (idx < total) {
+          const int r = r0 + idx / units, u = idx % units;
+          if (s_page[r] >= 0) {
+            const size_t row = ((size_t)s_page[r] * P.page_size + (k0 + r) % P.page_size) * P.h_kv * 128;
+            a[i] = __ldg(reinterpret_cast<const uint2*>(v8 + row) + u);
+            c[i] = __ldg(reinterpret_cast<const uint2*>(k8 + row) + u);
+            if (!tile_big) vs[i] = __ldg(P.v_scales + scale_index(r, u >> 4));
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kCvtUnroll; ++i) {
+        const int idx = base + i * kCvtThreads + (int)threadIdx.x;
+        if (idx < total) {
+          const int r = r0 + idx / units, u = idx % units;
+          const size_t dst =
+              (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 + (u & 15) * 8;
+          uint4 f16, bf16;
+          i8x8_to_f16_bf16(a[i], f16, bf16);
+          *reinterpret_cast<uint4*>(ws + dst) = tile_big ? f16 : i8x8_scaled_f16(a[i], vs[i]);
+          i8x8_to_f16_bf16(c[i], f16, bf16);
+          *reinterpret_cast<uint4*>(P.ws_k + dst) = bf16;
+        }
+      }
+    }
+    return;
   }
   const int units = P.h_kv * 16;                                // 16-byte units per key
   const int total = (r1 - r0) * units;
@@ -519,19 +633,7 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
             (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 + (u & 15) * 8;
         uint4 y = x[i];
         const bool live = s_page[r] >= 0;
-        if (KIND == 2) {  // int8 codes: exact in both fp16 and bf16
-          uint4 f16, bf16;
-          i8x8_to_f16_bf16(make_uint2(y.x, y.y), f16, bf16);
-          *reinterpret_cast<uint4*>(ws + dst) = f16;
-          if (live) {
-            const float vsc = __ldg(P.v_scales + ((size_t)s_page[r] * P.h_kv + (u >> 4)) *
-                                                     P.page_size + (k0 + r) % P.page_size);
-            big_i8 |= !((float)i8x8_max_abs(make_uint2(y.x, y.y)) * vsc <= 8.f);
-            sumsq = fmaf(sumsq_f16x8(f16), vsc * vsc, sumsq);
-          }
-          i8x8_to_f16_bf16(make_uint2(y.z, y.w), f16, bf16);
-          *reinterpret_cast<uint4*>(P.ws_k + dst) = bf16;
-        } else if (KV8) {  // e4m3 values are exact in both fp16 and bf16
+        if (KV8) {  // e4m3 values are exact in both fp16 and bf16
           cmax = __vmaxu4(cmax, __vmaxu4(y.x & 0x7f7f7f7fu, y.y & 0x7f7f7f7fu));
           const uint4 f16 = make_uint4(e4m3x2_to_f16x2(y.x), e4m3x2_to_f16x2(y.x >> 16),
                                        e4m3x2_to_f16x2(y.y), e4m3x2_to_f16x2(y.y >> 16));
@@ -570,7 +672,7 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     s_sq[warp] = sumsq;
     s_n[warp] = n_vals;
   }
-  const bool big = m0 > kBf16Big || m1 > kBf16Big || (cmax & 0xffu) > kE4m3Big || big_i8;
+  const bool big = m0 > kBf16Big || m1 > kBf16Big || (cmax & 0xffu) > kE4m3Big;
   const int any_big = __syncthreads_or(big);
   if (threadIdx.x == 0) {
     float tot = 0.f;
@@ -704,10 +806,9 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t tmem, int a, uint32_t vbase
 // columns of their own scores, so each chunk of scores is reread just before
 // its P replaces it.  Returns the row's sum of the unrounded f32 values.
 //
-// TWO = false (int8 pools only): P' = fp16(p x v_scale) as one value in
-// columns [16q, 16q + 16) (the layout of the single-fp16 path), and the sum
-// takes the weight each P' stands for, P' / v_scale (p for a zero scale).
-template <bool I8, bool TWO = true, int CH = 1>
+// int8 pools: P' = p x v_scale goes into P.V (hi + lo as above) and the sum
+// takes p.  A tile whose V copy already carries its scales has unit scales.
+template <bool I8, int CH = 1>
 __device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int cmax,
                                                   bool all_live, float sc, float base,
                                                   const float* scl) {
@@ -745,20 +846,11 @@ __device__ __forceinline__ float tc_softmax_split(uint32_t taddr, int cmin, int 
       const float w1 = I8 ? (e1 > 0.f ? e1 * v1 : 0.f) : e1;
       pk[i] = pack_f16x2(w0, w1);
       unpack_f16x2(pk[i], h0, h1);
-      if (TWO) {
-        pl[i] = pack_f16x2(w0 - h0, w1 - h1);
-        ls[i & 3] += e0 + e1;
-      } else {  // scl[256, 384): 1 / v_scale
-        ls[i & 3] += (v0 > 0.f ? h0 * scl[2 * kBN + 32 * q + 2 * i] : e0) +
-                     (v1 > 0.f ? h1 * scl[2 * kBN + 32 * q + 2 * i + 1] : e1);
-      }
+      pl[i] = pack_f16x2(w0 - h0, w1 - h1);
+      ls[i & 3] += e0 + e1;
     }
-    if (TWO) {
-      tc::st16(taddr + 32 * q, pk);
-      tc::st16(taddr + 32 * q + 16, pl);
-    } else {
-      tc::st16(taddr + 16 * q, pk);
-    }
+    tc::st16(taddr + 32 * q, pk);
+    tc::st16(taddr + 32 * q + 16, pl);
   }
   }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
@@ -1165,12 +1257,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::wait_ld();
         if (I8) {  // s_j = (q . codes_j) x k_scale_j
 #pragma unroll
-          for (int c = 0; c < kBN; c += 4) {
-            const float4 k4 = *reinterpret_cast<const float4*>(scl + c);
-            s[c] *= k4.x;
-            s[c + 1] *= k4.y;
-            s[c + 2] *= k4.z;
-            s[c + 3] *= k4.w;
+          for (int c = 0; c < kBN; c += 2) {  // packed: two keys per multiply
+            uint64_t sv, kv;
+            asm("mov.b64 %0, {%1, %2};\n" : "=l"(sv) : "f"(s[c]), "f"(s[c + 1]));
+            asm("ld.shared.b64 %0, [%1];\n" : "=l"(kv) : "r"(smem_u32(scl + c)));
+            asm("mul.rn.f32x2 %0, %0, %1;\n" : "+l"(sv) : "l"(kv));
+            asm("mov.b64 {%0, %1}, %2;\n" : "=f"(s[c]), "=f"(s[c + 1]) : "l"(sv));
           }
         }
         if (!all_live) {
@@ -1199,10 +1291,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // at once; the sum widens each fp16 half inside its add.
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         const uint64_t sc2 = f32_twice(sc), nb2 = f32_twice(-base);
-        if constexpr (!SPLIT && I8) {
-          ls[0] = tc_softmax_split<true, false, kRereadCh>(tmem + lane_base + colS, cmin, cmax, all_live, sc,
-                                                base, scl);
-        } else if constexpr (!SPLIT) {
+        if constexpr (!SPLIT) {
+          // (int8 pools: the scores above carry their K scales, and a row
+          // without the split-P flag has every V tile copied with its V
+          // scales applied, so P.V takes P as for 16-bit pools)
 #pragma unroll
           for (int q = 0; q < kBN / 32; ++q) {
             uint32_t pk[16];
@@ -1216,8 +1308,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::st16(tmem + lane_base + colS + q * 16, pk);
           }
         } else {
-          ls[0] = tc_softmax_split<I8, true, kRereadCh>(tmem + lane_base + colS, cmin, cmax, all_live, sc, base,
-                                       scl);
+          ls[0] = tc_softmax_split<I8, kRereadCh>(tmem + lane_base + colS, cmin, cmax, all_live, sc,
+                                                 base, scl);
         }
         l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         if (__any_sync(0xffffffffu, need)) {

@@ -161,11 +161,13 @@ def _poison_unused(k_cache, v_cache, pool: PagedPool, lengths) -> None:
         flat[idx] = float("nan")
 
 
-def int8_pools(case, seed: int = 0, nan_unused: bool = False, scale_range=(0.005, 0.05)):
+def int8_pools(case, seed: int = 0, nan_unused: bool = False, scale_range=(0.005, 0.05),
+               boost_p: float = 0.0, boost: float = 1.0):
     """Seeded int8 pools of a decode or prefill case's pool shape: codes
     uniform in [-127, 127] (int8 [P, page_size, H_kv, d]) and per-(slot, KV
     head) scales uniform in scale_range (float32 [P, H_kv, page_size]), as
-    (k_codes, v_codes, k_scales, v_scales) on the CPU.  With nan_unused, every
+    (k_codes, v_codes, k_scales, v_scales) on the CPU; each scale is then
+    multiplied by `boost` with probability boost_p.  With nan_unused, every
     slot no sequence position maps to holds code -128 and scale NaN."""
     g = _gen(seed, "cpu")
     P, ps, hkv, d = case.pool.num_pages, case.page_size, case.Hkv, case.d
@@ -173,6 +175,9 @@ def int8_pools(case, seed: int = 0, nan_unused: bool = False, scale_range=(0.005
              for _ in range(2)]
     lo, hi = scale_range
     scales = [torch.rand((P, hkv, ps), generator=g) * (hi - lo) + lo for _ in range(2)]
+    if boost_p > 0.0:
+        for sc in scales:
+            sc[torch.rand(sc.shape, generator=g) < boost_p] *= boost
     if nan_unused:
         if isinstance(case, PrefillCase):
             lengths = [p0 + max(case.T - pad, 0) for p0, pad in zip(case.p0, case.pads)]

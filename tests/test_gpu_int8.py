@@ -236,6 +236,31 @@ def test_int8_prefill_with_values_above_8_takes_the_split_path():
         assert_close(out[b], ref, f"int8 prefill split row {b}")
 
 
+def test_int8_prefill_small_values_take_the_scaled_copy():
+    """The B=8 x 2,048 batch over int8 pools whose values stay small (scales
+    0.004-0.012, |v| <= 1.5, an RMS near 0.5): no tile is flagged, every V
+    tile is copied as fp16(code x scale) and P goes into P.V as one fp16
+    value, as for 16-bit pools; every token against the oracle."""
+    case = wl.batched_prefill(seed=3)
+    pools = wl.int8_pools(case, 117, scale_range=(0.004, 0.012))
+    out = _prefill_int8(case, pools).cpu()
+    for b, ref in enumerate(_oracle_prefill_int8(case, pools)):
+        assert_close(out[b], ref, f"int8 prefill small values row {b}")
+
+
+@pytest.mark.parametrize("window", [0, 700])
+def test_int8_prefill_mixed_tiles(window):
+    """Small values with 0.2% of the scales x40 (|v| up to ~19): the tiles
+    holding one are flagged and keep their codes, the others are copied
+    scaled; flagged rows take P as two fp16 parts over both kinds of tile."""
+    case = wl.prefill_case([0, 40, 300], [1500, 3000, 200], T=1024, Hq=32, Hkv=8, d=128,
+                           seed=118, window=window)
+    pools = wl.int8_pools(case, 119, scale_range=(0.004, 0.012), boost_p=0.002, boost=40.0)
+    out = _prefill_int8(case, pools, window).cpu()
+    for b, ref in enumerate(_oracle_prefill_int8(case, pools, window)):
+        assert_close(out[b], ref, f"int8 prefill mixed tiles w{window} row {b}")
+
+
 def test_int8_prefill_batched_equals_solo_bit_for_bit():
     case = wl.prefill_case([100, 0, 700], [3000, 0, 5000], T=1024, Hq=16, Hkv=4, d=128, seed=115)
     pools = wl.int8_pools(case, 116)
