@@ -427,14 +427,14 @@ tl_status tl_paged_attn_prefill(const void* q, const void* k_cache, const void* 
  * tl_kv_cache_write_int8): tl_paged_attn_prefill with every K/V element read
  * as code x its row's scale.  The scores are s_j = scale * k_scale(j) *
  * <q, codes of K_g(j)> (Q.K^T on the tensor core with bf16 q and the codes
- * widened exactly to bf16, f32 accumulation, then the K scale in f32); each
- * probability p_j is multiplied by its key's v_scale before the P.V product
- * (P.V with the codes widened exactly to fp16 and the product p_j x v_scale
- * rounded to fp16, the softmax sum taking the weights those rounded products
- * stand for, fp16(p_j x v_scale) / v_scale, so each output is a convex
- * combination of V rows; or, for a row whose V holds a value code x scale of
- * magnitude above 8, the product split into two fp16 parts and the sum over
- * the unscaled p_j).
+ * widened exactly to bf16, f32 accumulation, then the K scale in f32).  V is
+ * read in 64-key tiles: a tile whose values code x v_scale all lie within
+ * +-8 with a root mean square up to 1.25 is used as fp16(code x v_scale)
+ * (one rounding, 2^-12 relative), and a row made only of such tiles takes
+ * P.V as tl_paged_attn_prefill does (P rounded once to fp16, the softmax
+ * sum over the same rounded values); any other tile keeps its codes (exact
+ * in fp16) and its row takes each p_j x v_scale split into two fp16 parts,
+ * with the sum over the unscaled p_j.
  *   q                  [B][T][h_q][d] bf16;  positions [B][T] int32 (-1 = pad)
  *   k_codes, v_codes, k_scales, v_scales  as tl_kv_cache_write_int8 writes
  *                      them (read only; codes 16-byte aligned)
