@@ -135,6 +135,30 @@ def test_fp8_decode_page_sizes(page_size, window):
     assert_close(out, ref, f"fp8 decode page {page_size} window {window}")
 
 
+@pytest.mark.parametrize("shape", ["many_short", "one_long", "mixed"])
+def test_fp8_piece_plan_extremes(shape):
+    """The piece plan's extremes over e4m3 pools (the one-byte kernel takes
+    32 keys per stage): 2,048 short sequences, one of 131,072 keys, and both
+    mixed with empty and one-key sequences; every sequence against the
+    oracle."""
+    g = torch.Generator().manual_seed(93)
+    if shape == "many_short":
+        lens = torch.randint(1, 400, (2048,), generator=g).tolist()
+    elif shape == "one_long":
+        lens = [131072]
+    else:
+        lens = torch.randint(1, 300, (500,), generator=g).tolist() + [65536, 257, 4096, 0, 1]
+    case = wl.decode_case(lens, Hq=32, Hkv=8, d=128, seed=94)
+    k8, v8 = (t.to(DEV) for t in _fp8_case(case))
+    q, bt, cl = case.q.to(DEV), case.block_table.to(DEV), case.context_lens.to(DEV)
+    err = _err()
+    out = tl.tl_paged_attn_decode(q, k8, v8, bt, cl, case.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isfinite(out).all()
+    assert_decode_all(out, q, k8, v8, bt, cl, case.scale, chunk=256, what=f"fp8 piece plan {shape}")
+
+
 def test_fp8_decode_reports_a_query_beyond_fp16():
     """The query is rounded to fp16 for the e4m3 MMAs: a finite element beyond
     65504 is reported (TL_DEVERR_VALUE_RANGE), not silently made infinite;

@@ -127,6 +127,28 @@ def test_int8_decode_llama8b_shape_every_sequence():
                       case.scale, k_scales=pools[2], v_scales=pools[3], what="int8 llama8b B=64")
 
 
+@pytest.mark.parametrize("shape", ["many_short", "one_long"])
+def test_int8_piece_plan_extremes(shape):
+    """The piece plan's extremes over int8 pools: 2,048 short sequences (with
+    empty and one-key ones) and one of 131,072 keys; every sequence."""
+    g = torch.Generator().manual_seed(95)
+    if shape == "many_short":
+        lens = torch.randint(1, 400, (2046,), generator=g).tolist() + [0, 1]
+    else:
+        lens = [131072]
+    case = wl.decode_case(lens, Hq=32, Hkv=8, d=128, seed=96)
+    pools = [t.to(DEV) for t in wl.int8_pools(case, 97)]
+    err = _err()
+    out = tl.tl_paged_attn_decode_int8(case.q.to(DEV), *pools, case.block_table.to(DEV),
+                                       case.context_lens.to(DEV), case.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isfinite(out).all()
+    assert_decode_all(out, case.q, pools[0], pools[1], case.block_table, case.context_lens,
+                      case.scale, k_scales=pools[2], v_scales=pools[3], chunk=256,
+                      what=f"int8 piece plan {shape}")
+
+
 def test_int8_decode_reports_a_query_beyond_fp16():
     case = wl.decode_case([40, 70], Hq=8, Hkv=2, d=128, seed=99)
     pools = [t.to(DEV) for t in wl.int8_pools(case, 100)]
