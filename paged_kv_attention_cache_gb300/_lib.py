@@ -72,6 +72,8 @@ def lib_path() -> str:
 def load(build_if_missing: bool = False):
     """The loaded library; with build_if_missing, compile it first if needed."""
     global _lib
+    if _lib is not None:  # loaded: no lock needed to read it
+        return _lib
     with _lock:
         if _lib is None:
             if build_if_missing:
