@@ -17,20 +17,22 @@
 //      long sequence's end; one descriptor per piece in item order, partial
 //      indices contiguous per sequence.  Zeroes the work counter and writes
 //      the zero output of sequences with nothing to read.
-//   2. bf16 / e4m3: decode_bf16_kernel, a programmatic dependent launch of
-//      the plan (it becomes resident while the plan runs and waits for its
-//      results), persistent, one CTA per SM, every warp independent: a warp
-//      takes work items (piece x KV head) from an atomic counter and streams
-//      their chunks (16 keys of K and V, 8 KiB at d=128) through its own ring
-//      of shared-memory stages filled by TMA; Q.K^T and P.V run on mma.sync
-//      m16n8k16 with the query-head group (times the q_len tokens,
-//      token-major) as the M rows, each row masked to its own causal range,
-//      online softmax in registers (details below).  At the end of an item
-//      the warp writes from its registers: a sequence with one piece writes
-//      its output directly, otherwise the item writes a partial.
+//   2. bf16 / e4m3 / int8: decode_bf16_kernel, a programmatic dependent
+//      launch of the plan (it becomes resident while the plan runs and waits
+//      for its results), persistent, one CTA per SM, every warp independent:
+//      a warp takes work items (piece x KV head) from an atomic counter and
+//      streams their chunks (16 keys of K and V, 8 KiB at d=128 in 16 bits)
+//      through its own ring of shared-memory stages filled by TMA; Q.K^T and
+//      P.V run on mma.sync m16n8k16, with the query-head group (times the
+//      q_len tokens, token-major) as the M rows, or, for one-byte pools with
+//      at most 8 rows, with the keys as the M rows and the group as the N
+//      columns; each row masked to its own causal range, online softmax in
+//      registers (details below).  At the end of an item the warp writes
+//      from its registers: a sequence with one piece writes its output
+//      directly, otherwise the item writes a partial.
 //      f32: decode_f32_kernel (CUDA-core dots in f32) writes partials.
 //   3. decode_combine_kernel merges the partials of sequences with several
-//      pieces, one warp per (sequence, query head); after the bf16 / e4m3
+//      pieces, one thread per 4 outputs; after the bf16 / one-byte
 //      kernel it is a programmatic dependent launch too.  (Merging inside
 //      the attention kernel, by the last piece of each (sequence, KV head)
 //      to finish, measured slower: every sequence's last piece is in the
