@@ -1,8 +1,8 @@
-"""A seeded sweep of decode shapes over bf16, e4m3 and int8 pools: random
-head groupings (1-16 query heads per KV head), page sizes, windows, batch
-sizes and lengths (with the edge lengths 0, 1, 15, 16, 17 mixed in), and
-2-4 query tokens per sequence for the multi-token call; every output against
-the oracle.  It reaches the layouts the kernels switch between (rows-as-rows
+"""Seeded sweeps of decode and prefill shapes over bf16, e4m3 and int8
+pools: random head groupings (1-16 query heads per KV head), page sizes,
+windows, batch sizes and lengths (with the edge lengths 0, 1, 15, 16, 17
+mixed in), 2-4 query tokens per sequence for the multi-token call, and
+padded prefill chunks of any length; every output against the oracle.  It reaches the layouts the kernels switch between (rows-as-rows
 and keys-as-rows, duplicated columns or not, one or two row groups) in
 combinations no hand-written case lists."""
 import random
@@ -98,4 +98,53 @@ def test_multi_token_sweep(kind, draw):
     assert int(err.item()) == 0, what
     ref = oracle.paged_prefill(case.q, kc, vc, case.block_table, case.positions, case.scale,
                                window=window)
+    assert_close(out.cpu().reshape(ref.shape), ref, what)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3", "int8"])
+@pytest.mark.parametrize("draw", range(12))
+def test_prefill_sweep(kind, draw):
+    """Right-aligned prefill calls of random shape: 1-4 rows, chunks of 1-160
+    tokens (not a multiple of the tile), any padding, prior context 0-1,500,
+    1-16 query heads per KV head, windows; the chunk's rows are written into
+    host copies of the pools by the oracle, and both sides read those."""
+    rng = random.Random(9000 + 1000 * draw + {"bf16": 1, "e4m3": 2, "int8": 3}[kind])
+    hkv = rng.choice([1, 2, 4, 8])
+    group = rng.choice([g for g in (1, 2, 3, 4, 5, 8, 16) if g * hkv <= 32])
+    B = rng.randint(1, 4)
+    T = rng.randint(1, 160)
+    pads = [rng.choice([0, rng.randint(0, T)]) for _ in range(B)]
+    p0 = [rng.choice([0, rng.randint(0, 1500)]) for _ in range(B)]
+    window = rng.choice([0, 0, rng.randint(1, 600)])
+    ps = rng.choice([16, 32])
+    case = wl.prefill_case(pads, p0, T=T, Hq=hkv * group, Hkv=hkv, d=128, page_size=ps,
+                           window=window, seed=rng.randint(0, 10**6))
+    what = f"{kind} prefill B={B} T={T} hkv={hkv} group={group} ps={ps} window={window}"
+    kn, vn = case.k_new.view(-1, hkv, 128), case.v_new.view(-1, hkv, 128)
+    err = _err()
+    if kind == "int8":
+        pools = [t.clone() for t in wl.int8_pools(case, rng.randint(0, 10**6))]
+        oracle.kv_cache_write_int8(kn, vn, *pools, case.slot_mapping)
+        out = tl.tl_paged_attn_prefill_int8(case.q.to(DEV), *(t.to(DEV) for t in pools),
+                                            case.block_table.to(DEV), case.positions.to(DEV),
+                                            case.scale, window=window, error_word=err)
+        ref = oracle.paged_prefill_int8(case.q, *pools, case.block_table, case.positions,
+                                        case.scale, window=window)
+    else:
+        if kind == "e4m3":
+            k8 = case.k_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+            v8 = case.v_cache.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+            oracle.kv_cache_write_fp8(kn, vn, k8, v8, case.slot_mapping)
+            kc = torch.from_numpy(k8).view(torch.float8_e4m3fn)
+            vc = torch.from_numpy(v8).view(torch.float8_e4m3fn)
+        else:
+            kc, vc = case.k_cache.clone(), case.v_cache.clone()
+            oracle.kv_cache_write(kn, vn, kc, vc, case.slot_mapping)
+        out = tl.tl_paged_attn_prefill(case.q.to(DEV), kc.to(DEV), vc.to(DEV),
+                                       case.block_table.to(DEV), case.positions.to(DEV),
+                                       case.scale, window=window, error_word=err)
+        ref = oracle.paged_prefill(case.q, kc, vc, case.block_table, case.positions, case.scale,
+                                   window=window)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, what
     assert_close(out.cpu().reshape(ref.shape), ref, what)
