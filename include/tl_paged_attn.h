@@ -523,6 +523,37 @@ tl_status tl_paged_attn_prefill_ring(const void* q, const void* k_cache, const v
                                      float scale, tl_dtype dtype, void* workspace,
                                      size_t workspace_bytes, uint32_t* error_word, void* stream);
 
+/*
+ * Sliding-window decode and prefill over rings of int8 pools: the ring rule
+ * of tl_paged_attn_decode_ring / tl_paged_attn_prefill_ring ("How serving
+ * works in Tlaloc", section 3, the windowed KV pool) over the int8 pools and
+ * arithmetic of tl_paged_attn_decode_int8 / tl_paged_attn_prefill_int8 (the
+ * pools as tl_kv_cache_write_int8 writes them, its scales per slot and KV
+ * head following their slots through the ring).  Arguments, refusals and
+ * errors as there; the prefill's workspace is
+ * tl_paged_attn_prefill_workspace_size_ex(B, T, h_q, h_kv, d,
+ * max_pages_per_seq, page_size, ring_pages, TL_INT8) bytes, the decode's
+ * tl_paged_attn_decode_workspace_size(B, h_q, h_kv, d).
+ */
+tl_status tl_paged_attn_decode_ring_int8(const void* q, const int8_t* k_codes,
+                                         const int8_t* v_codes, const float* k_scales,
+                                         const float* v_scales, const int32_t* block_table,
+                                         int32_t max_pages_per_seq, const int32_t* context_lens,
+                                         float* out, int32_t B, int32_t h_q, int32_t h_kv,
+                                         int32_t d, int32_t num_pages, int32_t page_size,
+                                         int32_t window, int32_t ring_pages, float scale,
+                                         void* workspace, size_t workspace_bytes,
+                                         uint32_t* error_word, void* stream);
+tl_status tl_paged_attn_prefill_ring_int8(const void* q, const int8_t* k_codes,
+                                          const int8_t* v_codes, const float* k_scales,
+                                          const float* v_scales, const int32_t* block_table,
+                                          int32_t max_pages_per_seq, const int32_t* positions,
+                                          float* out, int32_t B, int32_t T, int32_t h_q,
+                                          int32_t h_kv, int32_t d, int32_t num_pages,
+                                          int32_t page_size, int32_t window, int32_t ring_pages,
+                                          float scale, void* workspace, size_t workspace_bytes,
+                                          uint32_t* error_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -498,6 +498,60 @@ def tl_paged_attn_prefill_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
     return out
 
 
+def tl_paged_attn_decode_ring_int8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                                   k_scales: torch.Tensor, v_scales: torch.Tensor,
+                                   block_table: torch.Tensor, context_lens: torch.Tensor,
+                                   scale: float, window: int, ring_pages: int,
+                                   out: Optional[torch.Tensor] = None,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   error_word: Optional[torch.Tensor] = None,
+                                   stream=None) -> torch.Tensor:
+    """tl_paged_attn_decode_ring over int8 pools (bf16 q): out[B, H_q, d]
+    float32."""
+    dev = q.device
+    P, ps, hkv, d = _need_int8_pools(k_codes, v_codes, k_scales, v_scales, dev)
+    _need(q, "q", torch.bfloat16, (None, None, d), dev)
+    B, hq, _ = q.shape
+    _need_table(block_table, context_lens, B, dev)
+    out = _decode_out(out, (B, hq, d), dev)
+    workspace = _workspace(workspace, tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
+    _run("tl_paged_attn_decode_ring_int8", dev, stream,
+         _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+         block_table.shape[1], _ptr(context_lens), _ptr(out), B, hq, hkv, d, P, ps, int(window),
+         int(ring_pages), float(scale), _ptr(workspace), _ws_bytes(workspace),
+         _err_word(error_word, dev))
+    return out
+
+
+def tl_paged_attn_prefill_ring_int8(q: torch.Tensor, k_codes: torch.Tensor,
+                                    v_codes: torch.Tensor, k_scales: torch.Tensor,
+                                    v_scales: torch.Tensor, block_table: torch.Tensor,
+                                    positions: torch.Tensor, scale: float, window: int,
+                                    ring_pages: int, out: Optional[torch.Tensor] = None,
+                                    workspace: Optional[torch.Tensor] = None,
+                                    error_word: Optional[torch.Tensor] = None,
+                                    stream=None) -> torch.Tensor:
+    """tl_paged_attn_prefill_ring over int8 pools (bf16 q [B, T, H_q, d]):
+    out [B, T, H_q, d] float32."""
+    dev = q.device
+    P, ps, hkv, d = _need_int8_pools(k_codes, v_codes, k_scales, v_scales, dev)
+    _need(q, "q", torch.bfloat16, (None, None, None, d), dev)
+    B, T, hq, _ = q.shape
+    _need(block_table, "block_table", torch.int32, (B, None), dev)
+    if block_table.shape[1] < 1:
+        raise ValueError("block_table needs at least one column")
+    _need(positions, "positions", torch.int32, (B, T), dev)
+    out = _decode_out(out, (B, T, hq, d), dev)
+    workspace = _workspace(workspace, tl_paged_attn_prefill_workspace_size_ex(
+        B, T, hq, hkv, d, block_table.shape[1], ps, ring_pages, TL_INT8), dev)
+    _run("tl_paged_attn_prefill_ring_int8", dev, stream,
+         _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+         block_table.shape[1], _ptr(positions), _ptr(out), B, T, hq, hkv, d, P, ps, int(window),
+         int(ring_pages), float(scale), _ptr(workspace), _ws_bytes(workspace),
+         _err_word(error_word, dev))
+    return out
+
+
 def tl_paged_attn_decode_multi_workspace_size(B: int, q_len: int, h_q: int, h_kv: int,
                                               d: int) -> int:
     return int(_lib.load().tl_paged_attn_decode_multi_workspace_size(B, q_len, h_q, h_kv, d))

@@ -2160,6 +2160,23 @@ extern "C" tl_status tl_paged_attn_decode_ring(
                          dtype, workspace, workspace_bytes, error_word, stream);
 }
 
+extern "C" tl_status tl_paged_attn_decode_ring_int8(
+    const void* q, const int8_t* k_codes, const int8_t* v_codes, const float* k_scales,
+    const float* v_scales, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* context_lens, float* out, int32_t B, int32_t h_q, int32_t h_kv, int32_t d,
+    int32_t num_pages, int32_t page_size, int32_t window, int32_t ring_pages, float scale,
+    void* workspace, size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  if (!k_scales || !v_scales) return TL_ERR_INVALID_ARG;
+  // the ring must be part of the table and must hold one window
+  if (ring_pages <= 0 || ring_pages > max_pages_per_seq || window <= 0 || page_size <= 0 ||
+      (int64_t)ring_pages * page_size < window)
+    return TL_ERR_INVALID_ARG;
+  return tl::decode_impl(q, k_codes, v_codes, block_table, max_pages_per_seq, context_lens, out,
+                         B, 1, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale,
+                         TL_FP8_E4M3, workspace, workspace_bytes, error_word, stream,
+                         tl::NewRows(), k_scales, v_scales);
+}
+
 extern "C" size_t tl_paged_attn_decode_multi_workspace_size(int32_t B, int32_t q_len,
                                                             int32_t h_q, int32_t h_kv, int32_t d) {
   if (B <= 0 || q_len <= 0 || h_q <= 0 || h_kv <= 0 || d <= 0 || h_q % h_kv) return 0;

@@ -1657,6 +1657,21 @@ extern "C" tl_status tl_paged_attn_prefill_int8(
                           workspace, workspace_bytes, error_word, stream, k_scales, v_scales);
 }
 
+extern "C" tl_status tl_paged_attn_prefill_ring_int8(
+    const void* q, const int8_t* k_codes, const int8_t* v_codes, const float* k_scales,
+    const float* v_scales, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* positions, float* out, int32_t B, int32_t T, int32_t h_q, int32_t h_kv,
+    int32_t d, int32_t num_pages, int32_t page_size, int32_t window, int32_t ring_pages,
+    float scale, void* workspace, size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  if (!k_scales || !v_scales) return TL_ERR_INVALID_ARG;
+  if (!tl::ring_args_ok(max_pages_per_seq, page_size, window, ring_pages))
+    return TL_ERR_INVALID_ARG;
+  return tl::prefill_impl(q, k_codes, v_codes, block_table, max_pages_per_seq, positions, out, B,
+                          T, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale,
+                          TL_INT8, workspace, workspace_bytes, error_word, stream, k_scales,
+                          v_scales);
+}
+
 extern "C" size_t tl_paged_attn_prefill_workspace_size_keys(int32_t B, int32_t T, int32_t h_q,
                                                             int32_t h_kv, int32_t d,
                                                             int32_t max_row_keys,

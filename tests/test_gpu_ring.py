@@ -166,3 +166,78 @@ def test_full_size_sliding_layer_over_rings_every_sequence():
     assert_decode_all(out, g.q, k0, v0, g.block_table, g.context_lens, g.scale,
                       window=g.window, ring_pages=ring,
                       new_rows=(g.k_new, g.v_new, g.slot_mapping), what="sliding layer over rings")
+
+
+def _int8_layouts(c):
+    """Int8 pools of both layouts of a ring case: every slot's row quantised by
+    the oracle's int8 write (zero rows get scale 0 and codes 0), so a ring's
+    slots hold the same codes and scales as the full history's."""
+    out = []
+    for k, v in ((c.full_k, c.full_v), (c.ring_k, c.ring_v)):
+        P, ps, hkv, d = k.shape
+        kc = torch.zeros((P, ps, hkv, d), dtype=torch.int8)
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros((P, hkv, ps), dtype=torch.float32)
+        vs = torch.zeros_like(ks)
+        slots = torch.arange(P * ps, dtype=torch.int64)
+        oracle.kv_cache_write_int8(k.cpu().view(-1, hkv, d), v.cpu().view(-1, hkv, d), kc, vc, ks,
+                                   vs, slots)
+        out.append([t.to(DEV) for t in (kc, vc, ks, vs)])
+    return out
+
+
+@pytest.mark.parametrize("hq,hkv,window,ring", [(40, 8, 300, 20), (32, 8, 256, 16),
+                                                (16, 4, 100, 8), (64, 8, 4096, 257)])
+def test_decode_ring_int8_equals_full_history_bit_for_bit(hq, hkv, window, ring):
+    lengths = [1, 37, 300, 301, 1000, 2047, 5000]
+    c = _ring_case(lengths, window=window, ring_pages=ring, Hq=hq, Hkv=hkv, d=128, page_size=16,
+                   dtype=torch.bfloat16, seed=41)
+    full, rg = _int8_layouts(c)
+    e1, e2 = _err(), _err()
+    full_out = tl.tl_paged_attn_decode_int8(c.q, *full, c.full_table, c.context_lens, c.scale,
+                                            window=window, error_word=e1)
+    ring_out = tl.tl_paged_attn_decode_ring_int8(c.q, *rg, c.ring_table, c.context_lens, c.scale,
+                                                 window, ring, error_word=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) == 0 and int(e2.item()) == 0
+    assert torch.equal(full_out, ring_out)
+    ref = oracle.paged_decode_int8(c.q.cpu(), *(t.cpu() for t in rg), c.ring_table.cpu(),
+                                   c.context_lens.cpu(), c.scale, window=window, ring_pages=ring)
+    assert_close(ring_out, ref, "int8 ring decode vs oracle")
+
+
+def test_decode_ring_int8_that_cannot_hold_the_window_is_refused():
+    c = _ring_case([100, 400], window=64, ring_pages=4, Hq=8, Hkv=2, d=128, page_size=16,
+                   dtype=torch.bfloat16, seed=42)
+    _, rg = _int8_layouts(c)
+    for window, ring in ((65, 4), (64, 0), (0, 4)):
+        with pytest.raises(tl.TLError) as e:
+            tl.tl_paged_attn_decode_ring_int8(c.q, *rg, c.ring_table, c.context_lens, c.scale,
+                                              window, ring)
+        assert e.value.status == tl.TL_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("outlier_p", [0.0, 0.01])
+def test_prefill_ring_int8_equals_full_history_bit_for_bit(outlier_p):
+    """A chunk through rings of int8 pools: the same bits as the full history
+    (values of N(0,1) scale: every V tile copied scaled; with 1% of the
+    values x8: flagged tiles keep their codes), and every token against the
+    oracle's ring form."""
+    window, n, ps = 300, 200, 16
+    p0 = [0, 50, 700, 3000]
+    ring = oracle.ring_pages(window, n, ps)
+    c = _ring_case([p + n for p in p0], window=window, ring_pages=ring, Hq=32, Hkv=8, d=128,
+                   page_size=ps, dtype=torch.bfloat16, seed=43, outlier_p=outlier_p)
+    q, positions = _prefill_inputs(c, p0, n, pads=[0, 7, 0, 3], seed=44, outlier_p=outlier_p)
+    full, rg = _int8_layouts(c)
+    e1, e2 = _err(), _err()
+    full_out = tl.tl_paged_attn_prefill_int8(q, *full, c.full_table, positions, c.scale,
+                                             window=window, error_word=e1)
+    ring_out = tl.tl_paged_attn_prefill_ring_int8(q, *rg, c.ring_table, positions, c.scale,
+                                                  window, ring, error_word=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) == 0 and int(e2.item()) == 0
+    assert torch.equal(full_out, ring_out)
+    ref = oracle.paged_prefill_int8(q.cpu(), *(t.cpu() for t in rg), c.ring_table.cpu(),
+                                    positions.cpu(), c.scale, window=window, ring_pages=ring)
+    assert_close(ring_out.reshape(ref.shape), ref, f"int8 ring prefill outliers {outlier_p}")
