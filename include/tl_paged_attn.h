@@ -492,8 +492,11 @@ tl_status tl_paged_attn_decode_ring(const void* q, const void* k_cache, const vo
  * and for q_len = 1 is tl_paged_attn_decode.  K and V of each sequence are
  * read once for all its tokens, as in decode.
  *   q    [B][q_len][h_q][d] bf16;  out [B][q_len][h_q][d] float32.
- * Supported: bf16, d in {64, 128}, q_len * (h_q / h_kv) <= 16 (the tokens'
- * heads of one KV head form the MMA rows); otherwise TL_ERR_UNSUPPORTED.
+ * Supported: bf16 pools with d in {64, 128}, or TL_FP8_E4M3 pools with
+ * d = 128 (bf16 q, as for tl_paged_attn_decode), q_len * (h_q / h_kv) <= 16
+ * (the tokens' heads of one KV head form the MMA rows); otherwise
+ * TL_ERR_UNSUPPORTED.  tl_paged_attn_decode_multi_int8 is the same over int8
+ * pools (arguments as tl_paged_attn_decode_int8, plus q_len).
  * Workspace: tl_paged_attn_decode_multi_workspace_size(B, q_len, h_q, h_kv, d).
  * Other arguments and errors as for tl_paged_attn_decode.
  */
@@ -552,6 +555,16 @@ tl_status tl_paged_attn_prefill_ring_int8(const void* q, const int8_t* k_codes,
                                           int32_t h_kv, int32_t d, int32_t num_pages,
                                           int32_t page_size, int32_t window, int32_t ring_pages,
                                           float scale, void* workspace, size_t workspace_bytes,
+                                          uint32_t* error_word, void* stream);
+
+tl_status tl_paged_attn_decode_multi_int8(const void* q, const int8_t* k_codes,
+                                          const int8_t* v_codes, const float* k_scales,
+                                          const float* v_scales, const int32_t* block_table,
+                                          int32_t max_pages_per_seq, const int32_t* context_lens,
+                                          float* out, int32_t B, int32_t q_len, int32_t h_q,
+                                          int32_t h_kv, int32_t d, int32_t num_pages,
+                                          int32_t page_size, int32_t window, float scale,
+                                          void* workspace, size_t workspace_bytes,
                                           uint32_t* error_word, void* stream);
 
 #ifdef __cplusplus

@@ -577,3 +577,29 @@ def tl_paged_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
          _DTYPES.get(k_cache.dtype, -1), _ptr(workspace), _ws_bytes(workspace),
          _err_word(error_word, dev))
     return out
+
+
+def tl_paged_attn_decode_multi_int8(q: torch.Tensor, k_codes: torch.Tensor,
+                                    v_codes: torch.Tensor, k_scales: torch.Tensor,
+                                    v_scales: torch.Tensor, block_table: torch.Tensor,
+                                    context_lens: torch.Tensor, scale: float, window: int = 0,
+                                    out: Optional[torch.Tensor] = None,
+                                    workspace: Optional[torch.Tensor] = None,
+                                    error_word: Optional[torch.Tensor] = None,
+                                    stream=None) -> torch.Tensor:
+    """tl_paged_attn_decode_multi over int8 pools (bf16 q [B, q_len, H_q, d]):
+    out [B, q_len, H_q, d] float32."""
+    dev = q.device
+    P, ps, hkv, d = _need_int8_pools(k_codes, v_codes, k_scales, v_scales, dev)
+    _need(q, "q", torch.bfloat16, (None, None, None, d), dev)
+    B, q_len, hq, _ = q.shape
+    _need_table(block_table, context_lens, B, dev)
+    out = _decode_out(out, (B, q_len, hq, d), dev)
+    workspace = _workspace(
+        workspace, tl_paged_attn_decode_multi_workspace_size(B, q_len, hq, hkv, d), dev)
+    _run("tl_paged_attn_decode_multi_int8", dev, stream,
+         _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+         block_table.shape[1], _ptr(context_lens), _ptr(out), B, q_len, hq, hkv, d, P, ps,
+         int(window), float(scale), _ptr(workspace), _ws_bytes(workspace),
+         _err_word(error_word, dev))
+    return out

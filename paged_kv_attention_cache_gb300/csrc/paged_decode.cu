@@ -2183,6 +2183,19 @@ extern "C" size_t tl_paged_attn_decode_multi_workspace_size(int32_t B, int32_t q
   return tl::decode_ws_layout(B, q_len * h_q, h_kv, d, nullptr, nullptr);
 }
 
+extern "C" tl_status tl_paged_attn_decode_multi_int8(
+    const void* q, const int8_t* k_codes, const int8_t* v_codes, const float* k_scales,
+    const float* v_scales, const int32_t* block_table, int32_t max_pages_per_seq,
+    const int32_t* context_lens, float* out, int32_t B, int32_t q_len, int32_t h_q, int32_t h_kv,
+    int32_t d, int32_t num_pages, int32_t page_size, int32_t window, float scale,
+    void* workspace, size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  if (!k_scales || !v_scales) return TL_ERR_INVALID_ARG;
+  return tl::decode_impl(q, k_codes, v_codes, block_table, max_pages_per_seq, context_lens, out,
+                         B, q_len, h_q, h_kv, d, num_pages, page_size, window, 0, scale,
+                         TL_FP8_E4M3, workspace, workspace_bytes, error_word, stream,
+                         tl::NewRows(), k_scales, v_scales);
+}
+
 extern "C" tl_status tl_paged_attn_decode_multi(
     const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
     int32_t max_pages_per_seq, const int32_t* context_lens, float* out, int32_t B, int32_t q_len,

@@ -294,3 +294,23 @@ def test_int8_prefill_batched_equals_solo_bit_for_bit():
                                              case.positions[b:b + 1].to(DEV), case.scale)
         torch.cuda.synchronize()
         assert torch.equal(solo[0], both[b]), f"row {b}"
+
+
+@pytest.mark.parametrize("q_len,hq,hkv", [(4, 32, 8), (2, 32, 8), (3, 16, 8), (2, 8, 8)])
+def test_int8_multi_token_decode(q_len, hq, hkv):
+    """q_len tokens at the end of each sequence over int8 pools (16, 8, 6 and
+    2 rows per KV head: both row layouts), every token against the oracle."""
+    lengths = wl.llama8b_lengths(seed=11, B=10)
+    p0 = [L - q_len for L in lengths]
+    case = wl.prefill_case([0] * len(lengths), p0, T=q_len, Hq=hq, Hkv=hkv, d=128, seed=120)
+    pools = [t.clone() for t in wl.int8_pools(case, 121)]
+    oracle.kv_cache_write_int8(case.k_new, case.v_new, *pools, case.slot_mapping)
+    err = _err()
+    out = tl.tl_paged_attn_decode_multi_int8(case.q.to(DEV), *(t.to(DEV) for t in pools),
+                                             case.block_table.to(DEV),
+                                             torch.tensor(lengths, dtype=torch.int32, device=DEV),
+                                             case.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.paged_prefill_int8(case.q, *pools, case.block_table, case.positions, case.scale)
+    assert_close(out.cpu().reshape(ref.shape), ref, f"int8 multi-token q_len={q_len} hq={hq}")

@@ -1,7 +1,7 @@
 """Seeded sweeps of decode and prefill shapes over bf16, e4m3 and int8
 pools: random head groupings (1-16 query heads per KV head), page sizes,
 windows, batch sizes and lengths (with the edge lengths 0, 1, 15, 16, 17
-mixed in), 2-4 query tokens per sequence for the multi-token call, and
+mixed in), 2-4 query tokens per sequence for the multi-token calls, and
 padded prefill chunks of any length; every output against the oracle.  It reaches the layouts the kernels switch between (rows-as-rows
 and keys-as-rows, duplicated columns or not, one or two row groups) in
 combinations no hand-written case lists."""
@@ -64,10 +64,10 @@ def test_decode_sweep(kind, draw):
     assert_close(out.cpu(), ref, what)
 
 
-@pytest.mark.parametrize("kind", ["bf16", "e4m3"])
+@pytest.mark.parametrize("kind", ["bf16", "e4m3", "int8"])
 @pytest.mark.parametrize("draw", range(16))
 def test_multi_token_sweep(kind, draw):
-    rng = random.Random(5000 + 1000 * draw + (kind == "e4m3"))
+    rng = random.Random(5000 + 1000 * draw + {"bf16": 0, "e4m3": 1, "int8": 2}[kind])
     hkv = rng.choice([1, 2, 4, 8])
     q_len = rng.randint(2, 4)
     group = rng.choice([g for g in (1, 2, 3, 4, 5, 8) if g * q_len <= 16])
@@ -78,6 +78,22 @@ def test_multi_token_sweep(kind, draw):
     p0 = [L - q_len for L in lengths]
     case = wl.prefill_case([0] * B, p0, T=q_len, Hq=hkv * group, Hkv=hkv, d=128, page_size=ps,
                            window=window, seed=rng.randint(0, 10**6))
+    what = f"{kind} multi q_len={q_len} hkv={hkv} group={group} ps={ps} window={window}"
+    if kind == "int8":
+        pools = [t.clone() for t in wl.int8_pools(case, rng.randint(0, 10**6))]
+        oracle.kv_cache_write_int8(case.k_new.view(-1, hkv, 128), case.v_new.view(-1, hkv, 128),
+                                   *pools, case.slot_mapping)
+        err = _err()
+        out = tl.tl_paged_attn_decode_multi_int8(
+            case.q.to(DEV), *(t.to(DEV) for t in pools), case.block_table.to(DEV),
+            torch.tensor(lengths, dtype=torch.int32, device=DEV), case.scale, window=window,
+            error_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, what
+        ref = oracle.paged_prefill_int8(case.q, *pools, case.block_table, case.positions,
+                                        case.scale, window=window)
+        assert_close(out.cpu().reshape(ref.shape), ref, what)
+        return
     kc, vc = case.k_cache.clone(), case.v_cache.clone()
     if kind == "e4m3":
         k8 = kc.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
@@ -88,7 +104,6 @@ def test_multi_token_sweep(kind, draw):
     else:
         oracle.kv_cache_write(case.k_new.view(-1, hkv, 128), case.v_new.view(-1, hkv, 128), kc, vc,
                               case.slot_mapping)
-    what = f"{kind} multi q_len={q_len} hkv={hkv} group={group} ps={ps} window={window}"
     err = _err()
     out = tl.tl_paged_attn_decode_multi(case.q.to(DEV), kc.to(DEV), vc.to(DEV),
                                         case.block_table.to(DEV),
