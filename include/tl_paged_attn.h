@@ -557,6 +557,24 @@ tl_status tl_paged_attn_prefill_ring_int8(const void* q, const int8_t* k_codes,
                                           float scale, void* workspace, size_t workspace_bytes,
                                           uint32_t* error_word, void* stream);
 
+/*
+ * tl_paged_attn_decode_write over rings: the step's rows written at their
+ * ring slots (the caller's slot_mapping follows the ring rule: position p of
+ * sequence b at page block_table[b][(p / page_size) % ring_pages], offset
+ * p % page_size), then tl_paged_attn_decode_ring, in one call.  Arguments,
+ * refusals and errors as those two calls.
+ */
+tl_status tl_paged_attn_decode_write_ring(const void* q, const void* k_new, const void* v_new,
+                                          tl_dtype new_dtype, const int64_t* slot_mapping,
+                                          int32_t n_new, void* k_cache, void* v_cache,
+                                          const int32_t* block_table, int32_t max_pages_per_seq,
+                                          const int32_t* context_lens, float* out, int32_t B,
+                                          int32_t h_q, int32_t h_kv, int32_t d,
+                                          int32_t num_pages, int32_t page_size, int32_t window,
+                                          int32_t ring_pages, float scale, tl_dtype dtype,
+                                          void* workspace, size_t workspace_bytes,
+                                          uint32_t* error_word, void* stream);
+
 tl_status tl_paged_attn_decode_multi_int8(const void* q, const int8_t* k_codes,
                                           const int8_t* v_codes, const float* k_scales,
                                           const float* v_scales, const int32_t* block_table,

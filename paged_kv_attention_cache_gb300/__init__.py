@@ -17,7 +17,7 @@ from .api import (TL_BF16, TL_FP8_E4M3, tl_kv_cache_write_fp8, TL_DEVERR_CONTEXT
                   tl_paged_attn_prefill, tl_paged_attn_prefill_workspace_size, tl_status_string,
                   tl_paged_attn_decode_ring, tl_paged_attn_prefill_ring,
                   tl_paged_attn_decode_ring_int8, tl_paged_attn_prefill_ring_int8,
-                  tl_paged_attn_decode_multi_int8,
+                  tl_paged_attn_decode_multi_int8, tl_paged_attn_decode_write_ring,
                   tl_paged_attn_prefill_ring_workspace_size, tl_paged_attn_decode_multi,
                   tl_paged_attn_decode_multi_workspace_size,
                   tl_paged_attn_prefill_workspace_size_ex,
@@ -38,7 +38,7 @@ __all__ = [
     "tl_paged_attn_decode_workspace_size", "tl_paged_attn_prefill_workspace_size",
     "tl_paged_attn_decode_ring", "tl_paged_attn_prefill_ring",
     "tl_paged_attn_decode_ring_int8", "tl_paged_attn_prefill_ring_int8",
-    "tl_paged_attn_decode_multi_int8",
+    "tl_paged_attn_decode_multi_int8", "tl_paged_attn_decode_write_ring",
     "tl_paged_attn_prefill_ring_workspace_size", "tl_paged_attn_decode_multi",
     "tl_paged_attn_decode_multi_workspace_size", "tl_paged_attn_prefill_workspace_size_keys",
     "tl_status_string", "tl_version", "tl_get_device_error", "TLError", "build_library", "alloc_workspace",

@@ -53,6 +53,9 @@ SIGNATURES = {
                                                  ctypes.c_int], sz),
     "tl_paged_attn_decode_multi": ([vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                     i32, i32, f32, ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
+    "tl_paged_attn_decode_write_ring": ([vp, vp, vp, ctypes.c_int, vp, i32, vp, vp, vp, i32, vp,
+                                         vp, i32, i32, i32, i32, i32, i32, i32, i32, f32,
+                                         ctypes.c_int, vp, sz, u32p, vp], ctypes.c_int),
     "tl_paged_attn_decode_multi_int8": ([vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                          i32, i32, i32, i32, f32, vp, sz, u32p, vp],
                                         ctypes.c_int),

@@ -498,6 +498,30 @@ def tl_paged_attn_prefill_ring(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
     return out
 
 
+def tl_paged_attn_decode_write_ring(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                    slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                                    v_cache: torch.Tensor, block_table: torch.Tensor,
+                                    context_lens: torch.Tensor, scale: float, window: int,
+                                    ring_pages: int, out: Optional[torch.Tensor] = None,
+                                    workspace: Optional[torch.Tensor] = None,
+                                    error_word: Optional[torch.Tensor] = None,
+                                    stream=None) -> torch.Tensor:
+    """tl_paged_attn_decode_write over rings: the new rows at their ring slots
+    (slot_mapping follows the ring rule), then tl_paged_attn_decode_ring."""
+    dev, P, ps, hkv, d = _decode_args(q, k_cache, v_cache, block_table, context_lens)
+    _need_new_rows(k_new, v_new, slot_mapping, hkv, d, dev)
+    B, hq, _ = q.shape
+    out = _decode_out(out, (B, hq, d), dev)
+    workspace = _workspace(workspace, tl_paged_attn_decode_workspace_size(B, hq, hkv, d), dev)
+    _run("tl_paged_attn_decode_write_ring", dev, stream,
+         _ptr(q), _ptr(k_new), _ptr(v_new), _DTYPES.get(k_new.dtype, -1), _ptr(slot_mapping),
+         slot_mapping.numel(), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+         block_table.shape[1], _ptr(context_lens), _ptr(out), B, hq, hkv, d, P, ps, int(window),
+         int(ring_pages), float(scale), _DTYPES.get(k_cache.dtype, -1), _ptr(workspace),
+         _ws_bytes(workspace), _err_word(error_word, dev))
+    return out
+
+
 def tl_paged_attn_decode_ring_int8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
                                    k_scales: torch.Tensor, v_scales: torch.Tensor,
                                    block_table: torch.Tensor, context_lens: torch.Tensor,

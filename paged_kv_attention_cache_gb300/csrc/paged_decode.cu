@@ -2145,6 +2145,29 @@ extern "C" tl_status tl_paged_attn_decode_write(
                          workspace, workspace_bytes, error_word, stream, nr);
 }
 
+extern "C" tl_status tl_paged_attn_decode_write_ring(
+    const void* q, const void* k_new, const void* v_new, tl_dtype new_dtype,
+    const int64_t* slot_mapping, int32_t n_new, void* k_cache, void* v_cache,
+    const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* context_lens,
+    float* out, int32_t B, int32_t h_q, int32_t h_kv, int32_t d, int32_t num_pages,
+    int32_t page_size, int32_t window, int32_t ring_pages, float scale, tl_dtype dtype,
+    void* workspace, size_t workspace_bytes, uint32_t* error_word, void* stream) {
+  if (ring_pages <= 0 || ring_pages > max_pages_per_seq || window <= 0 || page_size <= 0 ||
+      (int64_t)ring_pages * page_size < window)
+    return TL_ERR_INVALID_ARG;
+  tl::NewRows nr;
+  nr.k_new = k_new;
+  nr.v_new = v_new;
+  nr.slot_mapping = slot_mapping;
+  nr.n = n_new;
+  nr.new_dtype = new_dtype;
+  nr.k_dst = k_cache;
+  nr.v_dst = v_cache;
+  return tl::decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, context_lens, out,
+                         B, 1, h_q, h_kv, d, num_pages, page_size, window, ring_pages, scale,
+                         dtype, workspace, workspace_bytes, error_word, stream, nr);
+}
+
 extern "C" tl_status tl_paged_attn_decode_ring(
     const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
     int32_t max_pages_per_seq, const int32_t* context_lens, float* out, int32_t B, int32_t h_q,

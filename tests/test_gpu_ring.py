@@ -241,3 +241,46 @@ def test_prefill_ring_int8_equals_full_history_bit_for_bit(outlier_p):
     ref = oracle.paged_prefill_int8(q.cpu(), *(t.cpu() for t in rg), c.ring_table.cpu(),
                                     positions.cpu(), c.scale, window=window, ring_pages=ring)
     assert_close(ring_out.reshape(ref.shape), ref, f"int8 ring prefill outliers {outlier_p}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float8_e4m3fn])
+def test_fused_write_and_ring_decode_equal_the_two_calls(dtype):
+    """tl_paged_attn_decode_write_ring: the step's rows written at their ring
+    slots and the ring decode in one call give the pools and the outputs of
+    the cache write followed by tl_paged_attn_decode_ring, bit for bit."""
+    window, ring = 300, 20
+    c = _ring_case([1, 37, 300, 301, 1000, 2047, 5000], window=window, ring_pages=ring, Hq=40,
+                   Hkv=8, d=128, page_size=16, dtype=torch.bfloat16, seed=45)
+    hkv, d = c.Hkv, c.d
+    s = c.ring_slots.to(DEV)
+    kn, vn = c.k_new.contiguous(), c.v_new.contiguous()
+    pools = []
+    for _ in range(2):
+        k, v = c.ring_k.clone(), c.ring_v.clone()
+        live = s >= 0
+        k.view(-1, hkv, d)[s[live]] = 0
+        v.view(-1, hkv, d)[s[live]] = 0
+        if dtype == torch.float8_e4m3fn:
+            k, v = k.float().to(dtype), v.float().to(dtype)
+        pools.append((k, v))
+    e1, e2 = _err(), _err()
+    (k1, v1), (k2, v2) = pools
+    fused = tl.tl_paged_attn_decode_write_ring(c.q, kn, vn, s, k1, v1, c.ring_table,
+                                               c.context_lens, c.scale, window, ring,
+                                               error_word=e1)
+    if dtype == torch.float8_e4m3fn:
+        tl.tl_kv_cache_write_fp8(kn, vn, k2, v2, s, error_word=e2)
+    else:
+        tl.tl_kv_cache_write(kn, vn, k2, v2, s, error_word=e2)
+    two = tl.tl_paged_attn_decode_ring(c.q, k2, v2, c.ring_table, c.context_lens, c.scale, window,
+                                       ring, error_word=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) == 0 and int(e2.item()) == 0
+    assert torch.equal(k1.view(torch.uint8), k2.view(torch.uint8))
+    assert torch.equal(v1.view(torch.uint8), v2.view(torch.uint8))
+    assert torch.equal(fused, two)
+    for window, ring in ((301, 18), (0, ring)):  # too short a ring; no window
+        with pytest.raises(tl.TLError) as e:
+            tl.tl_paged_attn_decode_write_ring(c.q, kn, vn, s, k1, v1, c.ring_table,
+                                               c.context_lens, c.scale, window, ring)
+        assert e.value.status == tl.TL_ERR_INVALID_ARG
