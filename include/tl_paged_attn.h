@@ -108,6 +108,34 @@ typedef enum {
  */
 tl_status tl_get_device_error(uint32_t* error_word, uint32_t* bits, int32_t clear, void* stream);
 
+/* ---- Decode timeline (tracing; a build option) ---------------------------
+ * A library built with -DTL_DECODE_TRACE=1 (the default build has none of
+ * it; `python -m paged_kv_attention_cache_gb300.trace` builds one beside the
+ * default library and runs it) records, in every bf16 and one-byte decode
+ * call, %globaltimer stamps (ns, one clock for the whole GPU) of the call's
+ * phases into a device array: slot TL_TRACE_* below.  A stamp taken once is
+ * one thread's; TL_TRACE_ATTN_END and TL_TRACE_COMBINE_END keep the latest CTA,
+ * TL_TRACE_COMBINE_START the earliest, across calls since the last reset.
+ * tl_decode_trace_reset zeroes the stamps (the combine's start to all ones)
+ * after synchronising the device; tl_decode_trace_read synchronises the
+ * device and copies the first n (1..TL_TRACE_SLOTS) stamps to host memory at
+ * `stamps`.  Trace one call at a time: reset, call, read.  Both return
+ * TL_ERR_UNSUPPORTED from a library built without the option (nothing else
+ * is done), TL_ERR_INVALID_ARG for a NULL `stamps` or n out of range, and
+ * TL_ERR_CUDA when the synchronisation or the copy fails.
+ */
+#define TL_TRACE_PLAN_START 0       /* the plan kernel's first instruction (block 0) */
+#define TL_TRACE_PLAN_PLACED 1      /* every piece placed (batches of up to 128 sequences) */
+#define TL_TRACE_PLAN_END 2         /* every descriptor written */
+#define TL_TRACE_ATTN_RELEASED 3    /* attention CTA 0 past its wait for the plan */
+#define TL_TRACE_ATTN_FIRST_STAGE 4 /* its warp 0's first stage of keys arrived */
+#define TL_TRACE_ATTN_END 5         /* the last attention CTA done */
+#define TL_TRACE_COMBINE_START 6    /* the first combine CTA past its wait */
+#define TL_TRACE_COMBINE_END 7      /* the last combine CTA done */
+#define TL_TRACE_SLOTS 8
+tl_status tl_decode_trace_reset(void);
+tl_status tl_decode_trace_read(uint64_t* stamps, int32_t n);
+
 /* Name of a status, for messages (never NULL). */
 const char* tl_status_string(tl_status status);
 

@@ -21,6 +21,8 @@ SIGNATURES = {
     "tl_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tl_version": ([], i32),
     "tl_get_device_error": ([vp, vp, i32, vp], ctypes.c_int),
+    "tl_decode_trace_reset": ([], ctypes.c_int),
+    "tl_decode_trace_read": ([vp, i32], ctypes.c_int),
     "tl_kv_cache_write": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, u32p, vp],
                           ctypes.c_int),
     "tl_kv_cache_write_fp8": ([vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, i32, i32, u32p,
@@ -80,21 +82,28 @@ def lib_path() -> str:
     return _build.LIB
 
 
-def load(build_if_missing: bool = False):
-    """The loaded library; with build_if_missing, compile it first if needed."""
+def load(build_if_missing: bool = False, path: str = None):
+    """The loaded library; with build_if_missing, compile it first if needed.
+    path: load that build of the library instead (a variant from
+    build.build_variant, e.g. the decode trace build), before any other
+    call of the process has loaded one."""
     global _lib
     if _lib is not None:  # loaded: no lock needed to read it
+        if path is not None and getattr(_lib, "_name", None) != path:
+            raise RuntimeError(f"{_lib._name} is already loaded in this process")
         return _lib
     with _lock:
         if _lib is None:
-            if build_if_missing:
-                _build.build()
-            if not os.path.exists(_build.LIB):
-                raise TLNotBuilt(
-                    f"{_build.LIB} is missing: build it with "
-                    "`python -c 'import __graft_entry__ as g; g.build()'` "
-                    "(or python -m paged_kv_attention_cache_gb300.build)")
-            lib = ctypes.CDLL(_build.LIB)
+            if path is None:
+                if build_if_missing:
+                    _build.build()
+                path = _build.LIB
+                if not os.path.exists(path):
+                    raise TLNotBuilt(
+                        f"{path} is missing: build it with "
+                        "`python -c 'import __graft_entry__ as g; g.build()'` "
+                        "(or python -m paged_kv_attention_cache_gb300.build)")
+            lib = ctypes.CDLL(path)
             for name, (args, res) in SIGNATURES.items():
                 fn = getattr(lib, name)
                 fn.argtypes = args

@@ -32,8 +32,10 @@
 //      directly, otherwise the item writes a partial.
 //      f32: decode_f32_kernel (CUDA-core dots in f32) writes partials.
 //   3. decode_combine_kernel merges the partials of sequences with several
-//      pieces, one thread per 4 outputs; after the bf16 / one-byte
-//      kernel it is a programmatic dependent launch too.  (Merging inside
+//      pieces, one thread per 4 outputs and G groups of such threads per
+//      output row (G grows as the batch shrinks and the pieces of a sequence
+//      multiply); after the bf16 / one-byte kernel it is a programmatic
+//      dependent launch too.  (Merging inside
 //      the attention kernel, by the last piece of each (sequence, KV head)
 //      to finish, measured slower: every sequence's last piece is in the
 //      small round, so all merges fall in the kernel's last microseconds,
@@ -47,6 +49,31 @@
 #include "kv_write.cuh"
 
 namespace tl {
+
+// Decode timeline, a build option (-DTL_DECODE_TRACE=1; the default library
+// has none of it): %globaltimer stamps (ns) of the phases of a call, in a
+// device array read by tl_decode_trace_read.  Slots as in the header's
+// TL_TRACE_*: a stamp taken once is one thread's, the attention kernel's end
+// is the latest of its CTAs', the combine's start the earliest and its end
+// the latest.
+#ifndef TL_DECODE_TRACE
+#define TL_DECODE_TRACE 0
+#endif
+#if TL_DECODE_TRACE
+__device__ unsigned long long g_trace[TL_TRACE_SLOTS];
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define TL_TRACE_SET(slot) (g_trace[slot] = trace_now())
+#define TL_TRACE_MAX(slot) atomicMax(&g_trace[slot], trace_now())
+#define TL_TRACE_MIN(slot) atomicMin(&g_trace[slot], trace_now())
+#else
+#define TL_TRACE_SET(slot) ((void)0)
+#define TL_TRACE_MAX(slot) ((void)0)
+#define TL_TRACE_MIN(slot) ((void)0)
+#endif
 
 constexpr int kChunk = 16;            // keys per step (one mma N=16 / K=16 tile)
 constexpr float kLazyLog2 = 8.f;      // the running max moves by more than 2^8 only
@@ -259,10 +286,81 @@ __device__ __forceinline__ long long block_excl_scan(long long x, long long* tmp
   return before;
 }
 
-// One CTA.  Thread t keeps sequence t's range in registers (sequences past
-// the block size are re-read in each pass); three block reductions fix the
-// piece sizes, and one scan of (bulk pieces << 32 | small pieces) places
-// every piece; a warp per sequence then writes its pieces' descriptors.  first_dynamic: items below it are taken without the counter
+// Sum of x over the warp (every lane gets it).
+__device__ __forceinline__ long long warp_sum64(long long x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Descriptors of one round of nseq sequences (base .. base + nseq - 1):
+// rec[j] = {first bulk piece, first small piece, bulk pieces, small pieces}
+// of sequence base + j, rng[j] = its {lo, p}.  Thread i writes the round's
+// pieces i, i + nthreads, ...: bulk pieces bulk0 .. bulk0 + nb - 1 (at
+// [bulk0, ...)), then small pieces small0 .. small0 + ns - 1 (at NB + ...);
+// a piece's sequence is the last one whose first piece of that kind is at or
+// before it (a binary search of rec).  Each piece also asks L2 for the
+// block-table entries its first chunk reads, so the attention kernel's
+// first table load of the item hits.
+__device__ __forceinline__ void write_piece_descs(const DecodeParams& P, const int4* rec,
+                                                  const int2* rng, int base, int nseq, int bulk0,
+                                                  int nb, int small0, int ns, int NB, int split,
+                                                  int small, int i, int nthreads) {
+  for (; i < nb + ns; i += nthreads) {
+    const bool bulk = i < nb;
+    const int pidx = bulk ? bulk0 + i : small0 + (i - nb);
+    int lo_s = 0, hi_s = nseq;
+    while (lo_s < hi_s) {
+      const int mid = (lo_s + hi_s) >> 1;
+      const int st = bulk ? rec[mid].x : rec[mid].y;
+      if (st <= pidx) lo_s = mid + 1;
+      else hi_s = mid;
+    }
+    const int j = lo_s - 1;
+    const int4 r = rec[j];
+    const int lo_j = rng[j].x, p_j = rng[j].y, bj = base + j;
+    const int n_j = p_j < 0 ? 0 : p_j / kChunk - lo_j / kChunk + 1;
+    const int c0 = lo_j / kChunk, c1 = c0 + n_j, cm = c1 - tail_chunks(n_j);
+    const int first = r.x + r.y, pieces = r.z + r.w;
+    int cb, ce, slot, part;
+    if (bulk) {
+      const int k = pidx - r.x;
+      cb = c0 + k * split;
+      ce = min(cm, cb + split);
+      slot = pidx;
+      part = first + k;
+    } else {
+      const int k = pidx - r.y;
+      cb = cm + k * small;
+      ce = min(c1, cb + small);
+      slot = NB + pidx;
+      part = first + r.z + k;
+    }
+    P.ws.desc[2 * slot] = make_int4(bj, cb, ce, pieces);
+    P.ws.desc[2 * slot + 1] = make_int4(lo_j, p_j, part, 0);
+    const int blk = page_of(P, cb * kChunk);
+    const int e = P.ring_pages > 0 ? blk % P.ring_pages : blk;
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(P.block_table + (size_t)bj * P.max_pages_per_seq + e));
+  }
+}
+
+// Batches of at most kWarpPlanMax sequences: every thread reads one
+// sequence's range into shared memory, then warp 0 plans alone: lane l takes
+// sequences l*K .. l*K + K - 1 (K = ceil(B / 32)), the sums are warp
+// shuffles and the placement one warp scan of the lanes' (bulk << 32 | small)
+// piece counts, with no block barrier between the steps.  Same arithmetic,
+// same pieces as the block-wide path.  The loops stay rolled: the plan runs
+// once per call from a cold instruction cache, where straight-line code costs
+// more than the loop overhead.
+constexpr int kWarpPlanMax = 128;
+constexpr int kWriteWarps = 8;  // writing warps per CTA of a warp-planned launch
+
+// One CTA.  Up to kWarpPlanMax sequences: warp 0 plans alone (above).
+// Larger batches: thread t keeps sequence t's range in registers (sequences
+// past the block size are re-read in each pass); three block reductions fix
+// the piece sizes, and one scan of (bulk pieces << 32 | small pieces) places
+// every piece.  Either way every thread then writes descriptors, one piece
+// at a time.  first_dynamic: items below it are taken without the counter
 // (the attention kernel's warp w starts with item w).
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int target_splits,
                                                            int first_dynamic) {
@@ -271,6 +369,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
   __shared__ int4 rec[1024];  // per sequence of a round: first bulk / small position, counts
   __shared__ int2 rng[1024];  // its lo, p
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+  if (blockIdx.x == 0 && tid == 0) TL_TRACE_SET(TL_TRACE_PLAN_START);
   // the attention kernel may launch now: it waits for this grid's results
   // (griddepcontrol.wait) after its own set-up
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -278,8 +377,12 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
     // CTAs past the first write the call's new rows: one warp per token (per
     // token and KV head for int8 pools), slot -1 skipped, a slot outside the
     // pools reported and skipped
-    const int64_t first = (int64_t)(blockIdx.x - 1) * nw + wid;
-    const int64_t stride = (int64_t)(gridDim.x - 1) * nw;
+    // a block enlarged for the warp plan writes with kWriteWarps of its
+    // warps, so the rows still spread over as many SMs
+    const int wpc = P.B <= kWarpPlanMax ? min(nw, kWriteWarps) : nw;
+    if (wid >= wpc) return;
+    const int64_t first = (int64_t)(blockIdx.x - 1) * wpc + wid;
+    const int64_t stride = (int64_t)(gridDim.x - 1) * wpc;
     const int64_t n_slots = (int64_t)P.num_pages * P.page_size;
     if (P.new_kind >= 3) {
       // int8 pools: one warp per (token, KV head) row; the scales written
@@ -370,6 +473,97 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
     }
     return;
   }
+  if (P.B <= kWarpPlanMax) {
+    __shared__ int s_plan[4];  // split, small, bulk pieces (-1: refused), small pieces
+    if (tid < P.B) {  // the block holds at least B threads
+      int lo, p;
+      seq_range(P, tid, lo, p, true);
+      rng[tid] = make_int2(lo, p);
+    }
+    __syncthreads();
+    if (wid == 0) {
+      const int K = (P.B + 31) >> 5, b0 = min(lane * K, P.B), b1 = min(b0 + K, P.B);
+      long long C = 0, T = 0;
+#pragma unroll 1
+      for (int b = b0; b < b1; ++b) {
+        const int n = rng[b].y < 0 ? 0 : rng[b].y / kChunk - rng[b].x / kChunk + 1;
+        C += n;
+        T += tail_chunks(n);
+      }
+      C = warp_sum64(C);
+      T = warp_sum64(T);
+      const long long half = max(target_splits / 2, 1);
+      const int small = (int)max((long long)kSmallChunks, (T + P.B + half - 1) / half);
+      long long TP = 0;
+#pragma unroll 1
+      for (int b = b0; b < b1; ++b) {
+        const int n = rng[b].y < 0 ? 0 : rng[b].y / kChunk - rng[b].x / kChunk + 1;
+        TP += (tail_chunks(n) + small - 1) / small;
+      }
+      TP = warp_sum64(TP);
+      const long long budget = (long long)target_splits + P.B - TP;
+      const long long sb = (C - T + budget - 1) / budget;
+      const int split = (int)(sb < kMinSplitChunks ? kMinSplitChunks : sb);
+      long long x = 0;  // this lane's (bulk << 32 | small) pieces
+#pragma unroll 1
+      for (int b = b0; b < b1; ++b) {
+        const int n = rng[b].y < 0 ? 0 : rng[b].y / kChunk - rng[b].x / kChunk + 1;
+        const int t = tail_chunks(n);
+        x += ((long long)((n - t + split - 1) / split) << 32) | ((t + small - 1) / small);
+      }
+      long long inc = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const long long tot = __shfl_sync(0xffffffffu, inc, 31);
+      const int NB = (int)(tot >> 32), NS = (int)(tot & 0xffffffffll);
+      if (NB + NS > decode_max_splits(P.B, P.h_kv)) {
+        // past the workspace's bound (see the block-wide path): refused
+        for (int b = lane; b <= P.B; b += 32) P.ws.split_off[b] = 0;
+        if (lane == 0) {
+          report(P.error_word, TL_DEVERR_PLAN_CAPACITY);
+          P.ws.ctrl[0] = split;
+          P.ws.ctrl[1] = 0;
+          P.ws.ctrl[2] = first_dynamic;
+          s_plan[2] = -1;
+        }
+      } else {
+        long long pos = inc - x;
+#pragma unroll 1
+        for (int b = b0; b < b1; ++b) {
+          const int n = rng[b].y < 0 ? 0 : rng[b].y / kChunk - rng[b].x / kChunk + 1;
+          const int t = tail_chunks(n);
+          const int nb = (n - t + split - 1) / split, ntl = (t + small - 1) / small;
+          const int pos_b = (int)(pos >> 32), pos_t = (int)(pos & 0xffffffffll);
+          P.ws.split_off[b] = pos_b + pos_t;
+          rec[b] = make_int4(pos_b, pos_t, nb, ntl);
+          pos += ((long long)nb << 32) | ntl;
+        }
+        if (lane == 0) {
+          P.ws.split_off[P.B] = NB + NS;
+          P.ws.ctrl[0] = split;
+          P.ws.ctrl[1] = NB + NS;
+          P.ws.ctrl[2] = first_dynamic;
+          s_plan[0] = split;
+          s_plan[1] = small;
+          s_plan[2] = NB;
+          s_plan[3] = NS;
+        }
+      }
+    }
+    __syncthreads();
+    if (s_plan[2] < 0) return;
+    if (tid == 0) TL_TRACE_SET(TL_TRACE_PLAN_PLACED);
+    write_piece_descs(P, rec, rng, 0, P.B, 0, s_plan[2], 0, s_plan[3], s_plan[2], s_plan[0],
+                      s_plan[1], tid, nt);
+#if TL_DECODE_TRACE
+    __syncthreads();
+    if (tid == 0) TL_TRACE_SET(TL_TRACE_PLAN_END);
+#endif
+    return;
+  }
   int lo0 = 0, p0 = -1, n0 = 0;  // sequence tid
   if (tid < P.B) {
     seq_range(P, tid, lo0, p0, true);
@@ -439,23 +633,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
       rng[tid] = make_int2(lo, p);
     }
     __syncthreads();
-    for (int j = wid; j < min(nt, P.B - base); j += nw) {
-      const int4 r = rec[j];
-      const int lo_j = rng[j].x, p_j = rng[j].y, bj = base + j;
-      const int n_j = p_j < 0 ? 0 : p_j / kChunk - lo_j / kChunk + 1;
-      const int c0 = lo_j / kChunk, c1 = c0 + n_j, cm = c1 - tail_chunks(n_j);
-      const int first = r.x + r.y, pieces = r.z + r.w;
-      for (int k = lane; k < r.z; k += 32) {
-        const int cb = c0 + k * split;
-        P.ws.desc[2 * (r.x + k)] = make_int4(bj, cb, min(cm, cb + split), pieces);
-        P.ws.desc[2 * (r.x + k) + 1] = make_int4(lo_j, p_j, first + k, 0);
-      }
-      for (int k = lane; k < r.w; k += 32) {
-        const int cb = cm + k * small;
-        P.ws.desc[2 * (NB + r.y + k)] = make_int4(bj, cb, min(c1, cb + small), pieces);
-        P.ws.desc[2 * (NB + r.y + k) + 1] = make_int4(lo_j, p_j, first + r.z + k, 0);
-      }
-    }
+    write_piece_descs(P, rec, rng, base, min(nt, P.B - base), (int)(carry >> 32),
+                      (int)(tot >> 32), (int)(carry & 0xffffffffll), (int)(tot & 0xffffffffll),
+                      (int)NB, split, small, tid, nt);
     __syncthreads();  // rec and rng are rewritten by the next round
     carry += tot;
   }
@@ -465,6 +645,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams P, int t
     P.ws.ctrl[0] = split;
     P.ws.ctrl[1] = total;
     P.ws.ctrl[2] = first_dynamic;
+    TL_TRACE_SET(TL_TRACE_PLAN_END);  // after the last round's barrier
   }
 }
 
@@ -695,6 +876,7 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
   // launched as a programmatic dependent of the plan kernel: its results
   // (work counter, descriptors, offsets) are read only after this wait
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  if (blockIdx.x == 0 && threadIdx.x == 0) TL_TRACE_SET(TL_TRACE_ATTN_RELEASED);
   // the combine kernel may launch now (it too waits for this grid's results)
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int qslot = L::qslot_bytes(P.rows);
@@ -757,6 +939,13 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
       nstate = 3;
     }
   };
+  // the first item's descriptor loads alongside the item count (its piece
+  // index is inside the workspace's descriptors whatever the count: the
+  // grid's warps are fewer than the pieces target)
+  if (grab / P.h_kv < decode_max_splits(P.B, P.h_kv)) {
+    describe_item(P, grab, inext);
+    nstate = grab >= total_items ? 4 : 2;
+  }
   while (nstate < 3) fetch_step();
 
   // Start issuing the next item: publish its descriptor, copy its Q rows.
@@ -962,6 +1151,8 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
         stop = true;
         break;
       }
+      if (TL_DECODE_TRACE && gs_c == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+        TL_TRACE_SET(TL_TRACE_ATTN_FIRST_STAGE);
       const uint32_t smask = sh.stage_mask[w][stage];
       const int nlive = min(CPS, it.c_end - c0);  // the stage's chunks inside the item
 #pragma unroll 1
@@ -1646,6 +1837,7 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
   if (!drained) *abort_flag = 1;
   __syncthreads();  // every wait above is bounded, so every thread gets here
   if (threadIdx.x == 0 && sh.abort_flag) report(P.error_word, TL_DEVERR_TIMEOUT);
+  if (threadIdx.x == 0) TL_TRACE_MAX(TL_TRACE_ATTN_END);
 }
 
 // ------------------------------------------------------------- f32 kernel --
@@ -1763,71 +1955,175 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_f32_kernel(DecodeParams
 // written by the main kernel when skip_single is set; sequences with none
 // output 0.
 //
-// One thread per 4 outputs of a (sequence, output row): a warp covers one
-// row at d = 128 (two at d = 64).  The pieces are folded in partial-index
-// order, 8 at a time: their (m, l) and partial rows are loaded together (one
-// round of loads per 8 pieces), then
+// A (sequence, output row) takes kTpr x G threads: G groups of D/4 threads,
+// each thread 4 outputs.  Group r folds the pieces r, r + G, r + 2G, ... in
+// that order, 8 at a time: their (m, l) and partial rows are loaded together
+// (one round of loads per 8 pieces), then
 //   M' = max(M, m_s),  a = a 2^(M - M') + sum_s 2^(m_s - M') acc_s,
-//   l = l 2^(M - M') + sum_s 2^(m_s - M') l_s,   out = a / l.
-// The partials come from the previous kernel: reads go to L2 (ld.global.cg).
-template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams P, int skip_single) {
-  constexpr int kTpr = D / 4;   // threads per output row
+//   l = l 2^(M - M') + sum_s 2^(m_s - M') l_s.
+// With G > 1 the groups' (M, l, a) meet in shared memory and group 0 folds
+// groups 1 .. G-1 into its own in that order, by the same rule; out = a / l.
+// More groups shorten the chain of dependent load rounds of a sequence with
+// many pieces (few long sequences), at the price of more threads; the host
+// picks G from the pieces a sequence can have.  The partials come from the
+// previous kernel: reads go to L2 (ld.global.cg).
+template <int D, bool GROUPED>
+__global__ void __launch_bounds__(512) decode_combine_kernel(DecodeParams P, int skip_single,
+                                                              int groups) {
+  constexpr int kTpr = D / 4;   // threads per output row and group
   constexpr int kBatch = 8;     // pieces per round of loads
+  const int G = GROUPED ? groups : 1;  // one group: the loop's strides are constants
+  extern __shared__ float4 cmb_sm[];  // G > 1: per thread (a) then (M, l)
   // a no-op unless launched as a programmatic dependent of the attention kernel
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t row = gid / kTpr;  // b * hq_all + h
-  if (row >= (int64_t)P.B * P.hq_all) return;
-  const int col = (int)(gid % kTpr) * 4;
-  const int b = (int)(row / P.hq_all), h = (int)(row - (int64_t)b * P.hq_all);
-  const int s0 = __ldcg(P.ws.split_off + b), ns = __ldcg(P.ws.split_off + b + 1) - s0;
-  float4* out = reinterpret_cast<float4*>(P.out + row * D + col);
-  if (ns == 0) {  // nothing to read: the output is 0
-    *out = make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
+  if (threadIdx.x == 0) TL_TRACE_MIN(TL_TRACE_COMBINE_START);
+  const int t = threadIdx.x;
+  const int c = t % kTpr;
+  const int r = (t / kTpr) % G;
+  const int rows_per_block = blockDim.x / (kTpr * G);
+  const int64_t row = (int64_t)blockIdx.x * rows_per_block + t / (kTpr * G);  // b * hq_all + h
+  const bool live = row < (int64_t)P.B * P.hq_all;
+  int s0 = 0, ns = 0, h = 0;
+  if (live) {
+    const int b = (int)(row / P.hq_all);
+    h = (int)(row - (int64_t)b * P.hq_all);
+    s0 = __ldcg(P.ws.split_off + b);
+    ns = __ldcg(P.ws.split_off + b + 1) - s0;
   }
-  if (ns == 1 && skip_single) return;
-  const float2* ml = reinterpret_cast<const float2*>(P.ws.ml) + (size_t)s0 * P.hq_all + h;
-  const float4* acc = reinterpret_cast<const float4*>(P.ws.acc + ((size_t)s0 * P.hq_all + h) * D + col);
-  const size_t acc_stride = (size_t)P.hq_all * D / 4;  // float4 units
+  const bool fold = live && (ns > 1 || (ns == 1 && !skip_single));
   float M = -INFINITY, l = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < ns; s += kBatch) {
-    float2 mlv[kBatch];
-    float4 av[kBatch];
+  if (fold) {
+    const float2* ml = reinterpret_cast<const float2*>(P.ws.ml) + (size_t)s0 * P.hq_all + h;
+    const float4* acc =
+        reinterpret_cast<const float4*>(P.ws.acc + ((size_t)s0 * P.hq_all + h) * D + 4 * c);
+    const size_t acc_stride = (size_t)P.hq_all * D / 4;  // float4 units
+    for (int s = r; s < ns; s += G * kBatch) {
+      float2 mlv[kBatch];
+      float4 av[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (s + u < ns) {
-        mlv[u] = __ldcg(ml + (size_t)(s + u) * P.hq_all);
-        av[u] = __ldcg(acc + (size_t)(s + u) * acc_stride);
-      } else {
-        mlv[u] = make_float2(-INFINITY, 0.f);
-        av[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kBatch; ++u) {
+        const int su = s + u * G;
+        if (su < ns) {
+          mlv[u] = __ldcg(ml + (size_t)su * P.hq_all);
+          av[u] = __ldcg(acc + (size_t)su * acc_stride);
+        } else {
+          mlv[u] = make_float2(-INFINITY, 0.f);
+          av[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-    }
-    float Mn = M;
+      float Mn = M;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) Mn = fmaxf(Mn, mlv[u].x);
-    if (Mn == -INFINITY) continue;  // no key seen yet by any piece
-    const float c = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
-    l *= c;
-    a.x *= c; a.y *= c; a.z *= c; a.w *= c;
+      for (int u = 0; u < kBatch; ++u) Mn = fmaxf(Mn, mlv[u].x);
+      if (Mn == -INFINITY) continue;  // no key seen yet by any piece
+      const float cm = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+      l *= cm;
+      a.x *= cm; a.y *= cm; a.z *= cm; a.w *= cm;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const float f = mlv[u].x == -INFINITY ? 0.f : fast_exp2(mlv[u].x - Mn);
-      l += f * mlv[u].y;
-      a.x += f * av[u].x; a.y += f * av[u].y; a.z += f * av[u].z; a.w += f * av[u].w;
+      for (int u = 0; u < kBatch; ++u) {
+        const float f = mlv[u].x == -INFINITY ? 0.f : fast_exp2(mlv[u].x - Mn);
+        l += f * mlv[u].y;
+        a.x += f * av[u].x; a.y += f * av[u].y; a.z += f * av[u].z; a.w += f * av[u].w;
+      }
+      M = Mn;
     }
-    M = Mn;
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  *out = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+  if (GROUPED) {
+    cmb_sm[t] = a;
+    cmb_sm[blockDim.x + t] = make_float4(M, l, 0.f, 0.f);
+    __syncthreads();
+  }
+  if (live && r == 0 && (ns == 0 || fold)) {
+    for (int g = 1; g < G; ++g) {
+      const float4 a2 = cmb_sm[t + g * kTpr];
+      const float4 ml2 = cmb_sm[blockDim.x + t + g * kTpr];
+      const float Mn = fmaxf(M, ml2.x);
+      if (Mn == -INFINITY) continue;
+      const float f0 = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+      const float f1 = ml2.x == -INFINITY ? 0.f : fast_exp2(ml2.x - Mn);
+      l = l * f0 + ml2.y * f1;
+      a.x = a.x * f0 + a2.x * f1; a.y = a.y * f0 + a2.y * f1;
+      a.z = a.z * f0 + a2.z * f1; a.w = a.w * f0 + a2.w * f1;
+      M = Mn;
+    }
+    // a sequence with nothing to read (ns == 0) folds nothing: l = 0, out 0
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    *reinterpret_cast<float4*>(P.out + row * D + 4 * c) =
+        make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+  }
+#if TL_DECODE_TRACE
+  __syncthreads();
+  if (t == 0) TL_TRACE_MAX(TL_TRACE_COMBINE_END);
+#endif
+}
+
+// Groups per row of the combine: a sequence has at most about
+// ceil(pieces target / B) + 2 pieces; one group per 24 of them, a power of
+// two up to a 512-thread row (16 groups at d = 128, 32 at d = 64).  Measured on GB300 (Llama-3-8B heads, whole calls): B = 16
+// with ~50 pieces a sequence 56.5 -> 53.9 us with 4 groups; B = 4 at 32K keys
+// 107.4 -> 92.9 us with 8; at B >= 32 (<= 26 pieces) more groups only add
+// CTAs (B = 64: 195.7 us with 1, 199.0 with 4).
+static int combine_groups(int B, int h_kv, int d) {
+  const int64_t est = ((int64_t)kTargetItems / h_kv + B - 1) / B + 2;
+  int g = 1;
+  while (g * 2 * (d / 4) <= 512 && est >= 24 * g) g *= 2;
+  return g;
+}
+
+// Launches the combine over B * rows_per_seq output rows.
+static cudaError_t launch_combine(const DecodeParams& P, int B, int rows_per_seq, int d,
+                                  int skip_single, bool dependent, cudaStream_t st) {
+  const int G = combine_groups(B, P.h_kv, d);
+  const int tpr = d / 4 * G;                      // threads per output row
+  const int threads = std::max(256, tpr);
+  const int64_t rows = (int64_t)B * rows_per_seq;
+  const int64_t per_block = threads / tpr;
+  cudaLaunchAttribute cattr[1];
+  cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cattr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3((unsigned)((rows + per_block - 1) / per_block));
+  ccfg.blockDim = dim3(threads);
+  ccfg.dynamicSmemBytes = G > 1 ? (size_t)threads * 2 * sizeof(float4) : 0;
+  ccfg.stream = st;
+  ccfg.attrs = cattr;
+  ccfg.numAttrs = dependent ? 1 : 0;
+  if (G > 1)
+    return d == 128 ? cudaLaunchKernelEx(&ccfg, decode_combine_kernel<128, true>, P, skip_single, G)
+                    : cudaLaunchKernelEx(&ccfg, decode_combine_kernel<64, true>, P, skip_single, G);
+  return d == 128 ? cudaLaunchKernelEx(&ccfg, decode_combine_kernel<128, false>, P, skip_single, 1)
+                  : cudaLaunchKernelEx(&ccfg, decode_combine_kernel<64, false>, P, skip_single, 1);
 }
 
 }  // namespace tl
 
 // ------------------------------------------------------------------- host --
+
+extern "C" tl_status tl_decode_trace_reset(void) {
+#if TL_DECODE_TRACE
+  unsigned long long init[TL_TRACE_SLOTS] = {};
+  init[TL_TRACE_COMBINE_START] = ~0ull;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TL_ERR_CUDA;
+  if (cudaMemcpyToSymbol(tl::g_trace, init, sizeof(init)) != cudaSuccess) return TL_ERR_CUDA;
+  return TL_OK;
+#else
+  return TL_ERR_UNSUPPORTED;
+#endif
+}
+
+extern "C" tl_status tl_decode_trace_read(uint64_t* stamps, int32_t n) {
+#if TL_DECODE_TRACE
+  if (!stamps || n < 1 || n > TL_TRACE_SLOTS) return TL_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TL_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(stamps, tl::g_trace, sizeof(uint64_t) * n) != cudaSuccess)
+    return TL_ERR_CUDA;
+  return TL_OK;
+#else
+  (void)stamps;
+  (void)n;
+  return TL_ERR_UNSUPPORTED;
+#endif
+}
 
 extern "C" size_t tl_paged_attn_decode_workspace_size(int32_t B, int32_t h_q, int32_t h_kv,
                                                       int32_t d) {
@@ -1983,16 +2279,20 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
                               : decode_warps<64, false, false, false>(rows));
   }
   const int target_splits = (kTargetItems + h_kv - 1) / h_kv;
-  // plan block: sequences are spread over its threads (larger batches loop),
-  // and a smaller block makes its reductions and scan cheaper
-  const int plan_threads = (int)std::min<int64_t>(1024, std::max<int64_t>(256, align_up((size_t)B, 32)));
+  // plan block: up to kWarpPlanMax sequences one warp plans and 1024
+  // threads write the descriptors; larger batches spread their sequences over
+  // the threads (and loop past 1024), where a smaller block makes the block
+  // reductions and the scan cheaper
+  const int plan_threads =
+      B <= kWarpPlanMax ? 1024
+                        : (int)std::min<int64_t>(1024, std::max<int64_t>(256, align_up((size_t)B, 32)));
   // the plan CTA, then (for a call that writes its new rows) CTAs with one
   // warp per new row, up to one per SM
   // (int8 pools: one warp per token and KV head)
   const int64_t write_warps = P.new_kind >= 3 ? (int64_t)P.n_new * h_kv : P.n_new;
+  const int wpc = B <= kWarpPlanMax ? kWriteWarps : plan_threads / 32;
   const int64_t write_ctas =
-      P.n_new > 0 ? std::min<int64_t>(num_sms(), (write_warps + plan_threads / 32 - 1) / (plan_threads / 32))
-                  : 0;
+      P.n_new > 0 ? std::min<int64_t>(num_sms(), (write_warps + wpc - 1) / wpc) : 0;
   decode_plan_kernel<<<(unsigned)(1 + write_ctas), plan_threads, 0, st>>>(P, target_splits,
                                                                           num_sms() * warps);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
@@ -2050,28 +2350,14 @@ static tl_status decode_impl(const void* q, const void* k_cache, const void* v_c
     if (launch_status() != TL_OK) return TL_ERR_CUDA;
     // the merge, a programmatic dependent of the attention kernel: its CTAs
     // take the SMs as the attention CTAs leave
-    const unsigned cblocks = (unsigned)(((int64_t)B * P.hq_all * (d / 4) + 255) / 256);
-    cudaLaunchAttribute cattr[1];
-    cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    cattr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t ccfg = {};
-    ccfg.gridDim = dim3(cblocks);
-    ccfg.blockDim = dim3(256);
-    ccfg.stream = st;
-    ccfg.attrs = cattr;
-    ccfg.numAttrs = 1;
-    const cudaError_t ce = d == 128 ? cudaLaunchKernelEx(&ccfg, decode_combine_kernel<128>, P, 1)
-                                    : cudaLaunchKernelEx(&ccfg, decode_combine_kernel<64>, P, 1);
-    if (ce != cudaSuccess) return TL_ERR_CUDA;
+    if (launch_combine(P, B, P.hq_all, d, 1, true, st) != cudaSuccess) return TL_ERR_CUDA;
     return launch_status();
   }
   const int grid = num_sms() * 2;
   if (d == 128) decode_f32_kernel<128><<<grid, kDecodeThreads, 0, st>>>(P);
   else decode_f32_kernel<64><<<grid, kDecodeThreads, 0, st>>>(P);
   if (launch_status() != TL_OK) return TL_ERR_CUDA;
-  const unsigned cblocks = (unsigned)(((int64_t)B * h_q * (d / 4) + 255) / 256);
-  if (d == 128) decode_combine_kernel<128><<<cblocks, 256, 0, st>>>(P, 0);
-  else decode_combine_kernel<64><<<cblocks, 256, 0, st>>>(P, 0);
+  if (launch_combine(P, B, h_q, d, 0, false, st) != cudaSuccess) return TL_ERR_CUDA;
   return launch_status();
 }
 }  // namespace tl

@@ -206,3 +206,11 @@ def test_ops_refuse_cpu_tensors():
     with pytest.raises(TypeError):
         tl.tl_kv_cache_write(x, x, torch.zeros(2, 4, 2, 8), torch.zeros(2, 4, 2, 8),
                              torch.zeros(4, dtype=torch.int64))
+
+
+def test_the_default_library_has_no_decode_trace(lib):
+    """The trace calls exist in every build; the default one answers that the
+    option is absent, before any CUDA call."""
+    buf = (ctypes.c_uint64 * 8)()
+    assert lib.tl_decode_trace_reset() == tl.TL_ERR_UNSUPPORTED
+    assert lib.tl_decode_trace_read(buf, 8) == tl.TL_ERR_UNSUPPORTED
