@@ -136,6 +136,34 @@ tl_status tl_get_device_error(uint32_t* error_word, uint32_t* bits, int32_t clea
 tl_status tl_decode_trace_reset(void);
 tl_status tl_decode_trace_read(uint64_t* stamps, int32_t n);
 
+/* ---- Prefill step trace (a build option) ---------------------------------
+ * A library built with -DTL_PREFILL_TRACE=1 (absent from the default build;
+ * `python -m paged_kv_attention_cache_gb300.trace --prefill` builds and runs
+ * one) adds, in every prefill call, to one row of TL_PTRACE_FIELDS counters
+ * per attention CTA (row = the CTA's index, up to 1024): the MMA-issuing
+ * thread's clock64 cycles from its first item to its last, the 128-key steps
+ * it issued (both query tiles' S and P.V over one key tile), its items, and
+ * the cycles it waited for the softmax warps' P and for the producer's K and
+ * V tiles; then, summed over the two softmax warpgroups (their first warps),
+ * the cycles they waited for S and the cycles from S's arrival to their P's
+ * release.  tl_prefill_trace_reset zeroes the rows after synchronising the
+ * device; tl_prefill_trace_read synchronises the device and copies the first
+ * n_ctas rows (1..1024) to host memory at `rows` (n_ctas x TL_PTRACE_FIELDS
+ * uint64).  Both return TL_ERR_UNSUPPORTED from a library built without the
+ * option (nothing else is done), TL_ERR_INVALID_ARG for a NULL `rows` or
+ * n_ctas out of range, TL_ERR_CUDA when the synchronisation or copy fails.
+ */
+#define TL_PTRACE_CYCLES 0
+#define TL_PTRACE_STEPS 1
+#define TL_PTRACE_ITEMS 2
+#define TL_PTRACE_WAIT_P 3
+#define TL_PTRACE_WAIT_KV 4
+#define TL_PTRACE_SM_WAIT_S 5
+#define TL_PTRACE_SM_BUSY 6
+#define TL_PTRACE_FIELDS 7
+tl_status tl_prefill_trace_reset(void);
+tl_status tl_prefill_trace_read(uint64_t* rows, int32_t n_ctas);
+
 /* Name of a status, for messages (never NULL). */
 const char* tl_status_string(tl_status status);
 

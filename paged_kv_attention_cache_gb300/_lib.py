@@ -23,6 +23,8 @@ SIGNATURES = {
     "tl_get_device_error": ([vp, vp, i32, vp], ctypes.c_int),
     "tl_decode_trace_reset": ([], ctypes.c_int),
     "tl_decode_trace_read": ([vp, i32], ctypes.c_int),
+    "tl_prefill_trace_reset": ([], ctypes.c_int),
+    "tl_prefill_trace_read": ([vp, i32], ctypes.c_int),
     "tl_kv_cache_write": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, u32p, vp],
                           ctypes.c_int),
     "tl_kv_cache_write_fp8": ([vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, i32, i32, u32p,

@@ -65,6 +65,26 @@
 
 namespace tl {
 
+// Prefill step trace, a build option (-DTL_PREFILL_TRACE=1; the default
+// library has none of it): the MMA-issuing thread of each attention CTA adds
+// its clock64 cycles from its first item to its last, its 128-key steps (one
+// step: both query tiles' S and P.V over one key tile), its items, and the
+// cycles it spent waiting for the softmax warps' P and for the producer's K
+// and V tiles; the first warp of each softmax warpgroup adds the cycles it
+// waited for S and the cycles from S's arrival to its P's release; all to
+// its CTA's row of a device array read by tl_prefill_trace_read (both
+// launches of a call add to the same rows).
+#ifndef TL_PREFILL_TRACE
+#define TL_PREFILL_TRACE 0
+#endif
+#if TL_PREFILL_TRACE
+constexpr int kPtraceCtas = 1024;
+__device__ unsigned long long g_ptrace[kPtraceCtas][TL_PTRACE_FIELDS];
+__device__ __forceinline__ long long ptrace_clk() { return clock64(); }
+#else
+__device__ __forceinline__ long long ptrace_clk() { return 0; }
+#endif
+
 struct PrefillParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_cache;
@@ -1123,15 +1143,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_issue_pv(tmem, (a), sV + ((vt) % kTcVS) * kTcKVBytes, (acc), SPLIT)
     uint32_t kt = 0, vt = 0, tiles = 0, n = 0;  // K / V tiles, S tiles, live items
     bool ok = true;
+    long long t_first = 0, wait_p = 0, wait_kv = 0;  // the step trace (zero without it)
+    // a wait for the softmax's P, or for the producer's K / V, with its cycles
+    auto wait_for_p = [&](uint32_t bar, uint32_t ph) {
+      const long long t0 = ptrace_clk();
+      const bool r = mbar_wait(bar, ph, abort_flag);
+      wait_p += ptrace_clk() - t0;
+      return r;
+    };
+    auto wait_for_kv = [&](uint32_t bar, uint32_t ph) {
+      const long long t0 = ptrace_clk();
+      const bool r = mbar_wait(bar, ph, abort_flag);
+      wait_kv += ptrace_clk() - t0;
+      return r;
+    };
     for (uint32_t seq = 0; ok; ++seq) {
       const int idx = tc_fetch(sh, seq, counter, i_begin, i_end, abort_flag);
       if (idx < 0) break;
       const TcItem it = tc_item(P, idx, tpt, n_pairs, cap);
       if (it.rg.kmax < 0) continue;
       if (lane == 0) {
+        if (n == 0) t_first = ptrace_clk();
         const uint32_t qb0 = (2 * n) % QB, qb1 = (2 * n + 1) % QB;
         ok = mbar_wait(smem_u32(&sh.q_full[qb0]), ((2 * n) / QB) & 1, abort_flag) &&
-             mbar_wait(smem_u32(&sh.k_full[kt % kTcKS]), (kt / kTcKS) & 1, abort_flag);
+             wait_for_kv(smem_u32(&sh.k_full[kt % kTcKS]), (kt / kTcKS) & 1);
         if (ok) {
           tc::fence_after();
           issue_s(0, kt, qb0);
@@ -1144,8 +1179,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int j = 0; j < it.n_tiles && ok; ++j, ++tiles) {
           const bool last = j == it.n_tiles - 1;
-          if (!mbar_wait(smem_u32(&sh.v_full[vt % kTcVS]), (vt / kTcVS) & 1, abort_flag) ||
-              !mbar_wait(smem_u32(&sh.p_full[0]), tiles & 1, abort_flag) ||
+          if (!wait_for_kv(smem_u32(&sh.v_full[vt % kTcVS]), (vt / kTcVS) & 1) ||
+              !wait_for_p(smem_u32(&sh.p_full[0]), tiles & 1) ||
               (j == 0 && n > 0 &&
                !mbar_wait(smem_u32(&sh.o_free[0]), (n - 1) & 1, abort_flag))) {
             ok = false;
@@ -1156,15 +1191,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (last) {
             tc::commit(smem_u32(&sh.o_done[0]));
           } else {
-            if (!mbar_wait(smem_u32(&sh.k_full[(kt + 1) % kTcKS]), ((kt + 1) / kTcKS) & 1,
-                           abort_flag)) {
+            if (!wait_for_kv(smem_u32(&sh.k_full[(kt + 1) % kTcKS]), ((kt + 1) / kTcKS) & 1)) {
               ok = false;
               break;
             }
             tc::fence_after();
             issue_s(0, kt + 1, qb0);
           }
-          if (!mbar_wait(smem_u32(&sh.p_full[1]), tiles & 1, abort_flag) ||
+          if (!wait_for_p(smem_u32(&sh.p_full[1]), tiles & 1) ||
               (j == 0 && n > 0 &&
                !mbar_wait(smem_u32(&sh.o_free[1]), (n - 1) & 1, abort_flag))) {
             ok = false;
@@ -1193,6 +1227,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // every MMA this thread issued is done before TMEM is released
       tc::commit(smem_u32(&sh.mma_drain));
       if (!mbar_drain(smem_u32(&sh.mma_drain), 0)) *abort_flag = 1;
+#if TL_PREFILL_TRACE
+      if (n > 0 && blockIdx.x < kPtraceCtas) {
+        unsigned long long* row = g_ptrace[blockIdx.x];
+        atomicAdd(row + TL_PTRACE_CYCLES, (unsigned long long)(ptrace_clk() - t_first));
+        atomicAdd(row + TL_PTRACE_STEPS, (unsigned long long)tiles);
+        atomicAdd(row + TL_PTRACE_ITEMS, (unsigned long long)n);
+        atomicAdd(row + TL_PTRACE_WAIT_P, (unsigned long long)wait_p);
+        atomicAdd(row + TL_PTRACE_WAIT_KV, (unsigned long long)wait_kv);
+      }
+#endif
     }
     __syncwarp();
   } else {
@@ -1206,6 +1250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sc = P.scale_log2;
     uint32_t tiles = 0, n = 0;
     bool ok = true;
+    long long sm_wait_s = 0, sm_busy = 0;  // the step trace (zero without it)
     for (uint32_t seq = 0; ok; ++seq) {
       const int idx = tc_fetch(sh, seq, counter, i_begin, i_end, abort_flag);
       if (idx < 0) break;
@@ -1235,10 +1280,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int lo = (P.window > 0 && p - P.window + 1 > 0) ? p - P.window + 1 : 0;
       float m_used = -INFINITY, l = 0.f;  // running max of the scores in log2 units
       for (int j = 0; j < it.n_tiles; ++j, ++tiles) {
+        const long long tw = ptrace_clk();
         if (!mbar_wait(smem_u32(&sh.s_full[a]), tiles & 1, abort_flag)) {
           ok = false;
           break;
         }
+        const long long ts = ptrace_clk();
+        sm_wait_s += ts - tw;
         tc::fence_after();
         const int key0 = (it.tile0 + j) * kBN;
         const int cmin = lo - key0, cmax = p - key0;  // live columns [cmin, cmax]
@@ -1331,6 +1379,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[a]));
         if (I8 && lane == 0) mbar_arrive(smem_u32(&sh.sc_empty[tiles % kScR]));
+        sm_busy += ptrace_clk() - ts;
       }
       if (!ok) break;
       // epilogue: O / l.  The tile's own query buffer, free since its last S
@@ -1388,6 +1437,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++n;
       ok = ok && !*abort_flag;
     }
+#if TL_PREFILL_TRACE
+    if (leader && blockIdx.x < kPtraceCtas) {
+      atomicAdd(&g_ptrace[blockIdx.x][TL_PTRACE_SM_WAIT_S], (unsigned long long)sm_wait_s);
+      atomicAdd(&g_ptrace[blockIdx.x][TL_PTRACE_SM_BUSY], (unsigned long long)sm_busy);
+    }
+#endif
   }
   tc::fence_before();
   __syncthreads();  // every wait above is bounded, so every thread gets here
@@ -1592,6 +1647,32 @@ static bool ring_args_ok(int32_t max_pages_per_seq, int32_t page_size, int32_t w
 }
 
 }  // namespace tl
+
+extern "C" tl_status tl_prefill_trace_reset(void) {
+#if TL_PREFILL_TRACE
+  if (cudaDeviceSynchronize() != cudaSuccess) return TL_ERR_CUDA;
+  static unsigned long long zeros[tl::kPtraceCtas][TL_PTRACE_FIELDS];
+  if (cudaMemcpyToSymbol(tl::g_ptrace, zeros, sizeof(zeros)) != cudaSuccess) return TL_ERR_CUDA;
+  return TL_OK;
+#else
+  return TL_ERR_UNSUPPORTED;
+#endif
+}
+
+extern "C" tl_status tl_prefill_trace_read(uint64_t* rows, int32_t n_ctas) {
+#if TL_PREFILL_TRACE
+  if (!rows || n_ctas < 1 || n_ctas > tl::kPtraceCtas) return TL_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TL_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(rows, tl::g_ptrace,
+                           sizeof(uint64_t) * TL_PTRACE_FIELDS * (size_t)n_ctas) != cudaSuccess)
+    return TL_ERR_CUDA;
+  return TL_OK;
+#else
+  (void)rows;
+  (void)n_ctas;
+  return TL_ERR_UNSUPPORTED;
+#endif
+}
 
 extern "C" size_t tl_paged_attn_prefill_workspace_size(int32_t B, int32_t T, int32_t h_q,
                                                        int32_t h_kv, int32_t d,

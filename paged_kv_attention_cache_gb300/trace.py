@@ -13,6 +13,13 @@ instruction (the header's TL_TRACE_* slots), and the spans between them.
 The stamps are %globaltimer reads on the GPU; the traced build adds a few
 stores and atomics and one barrier per plan and combine CTA, nothing else, so
 its times run a little above the default build's.
+
+With --prefill it builds the library with -DTL_PREFILL_TRACE=1 instead and
+runs prefill calls over the B=8 x 2,048-token batch (0-1,500 left pads, prior
+context 0-6,144, Llama-3-8B heads; the cache write of the chunk first), then
+prints, over the attention CTAs, the cycles per 128-key step (both query
+tiles' S and P.V over one key tile) and the share of the MMA issuer's cycles
+spent waiting for the softmax's P and for the producer's K / V tiles.
 """
 from __future__ import annotations
 
@@ -75,8 +82,71 @@ def trace_calls(call, lib, calls: int, warmup: int = 2) -> dict:
     return med
 
 
+def build_prefill_trace_library(force: bool = False) -> str:
+    return build.build_variant("prefill_trace", build.SOURCES, ["TL_PREFILL_TRACE=1"],
+                               force=force)
+
+
+PTRACE_FIELDS = ("cycles", "steps", "items", "wait_p", "wait_kv", "sm_wait_s", "sm_busy")
+
+
+def prefill_step_summary(rows: list) -> dict:
+    """Per-CTA rows of the prefill trace (CTAs that ran no item skipped) as
+    the median and spread of the cycles per step and the waits' shares."""
+    live = [r for r in rows if r[1] > 0]
+    per_step = sorted(r[0] / r[1] for r in live)
+    tot = sum(r[0] for r in live)
+    steps = sum(r[1] for r in live)
+    return {"ctas": len(live), "steps": steps,
+            "items": sum(r[2] for r in live),
+            "cycles_per_step_median": round(statistics.median(per_step), 1),
+            "cycles_per_step_min": round(per_step[0], 1),
+            "cycles_per_step_max": round(per_step[-1], 1),
+            "wait_p_share": round(sum(r[3] for r in live) / tot, 4),
+            "wait_kv_share": round(sum(r[4] for r in live) / tot, 4),
+            # per query tile and step: the softmax's wait for S and its work
+            # from S's arrival to P's release
+            "softmax_wait_s_per_tile": round(sum(r[5] for r in live) / (2 * steps), 1),
+            "softmax_busy_per_tile": round(sum(r[6] for r in live) / (2 * steps), 1)}
+
+
+def trace_prefill(args) -> dict:
+    lib = _lib.load(path=build_prefill_trace_library())
+    from . import api
+    from . import workloads as wl
+
+    dev = torch.device("cuda")
+    case = wl.batched_prefill(seed=args.seed, device=dev)
+    g = wl.to_device(case, dev)
+    ws = api.alloc_workspace(api.tl_paged_attn_prefill_workspace_size(
+        case.B, case.T, case.Hq, case.Hkv, case.d, case.block_table.shape[1], case.page_size), dev)
+    out = torch.empty((case.B, case.T, case.Hq, case.d), dtype=torch.float32, device=dev)
+    api.tl_kv_cache_write(g.k_new.view(-1, case.Hkv, case.d), g.v_new.view(-1, case.Hkv, case.d),
+                          g.k_cache, g.v_cache, g.slot_mapping)
+    n_ctas = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = []
+    for i in range(2 + args.calls):
+        if lib.tl_prefill_trace_reset() != 0:
+            raise RuntimeError("tl_prefill_trace_reset failed")
+        api.tl_paged_attn_prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.positions,
+                                  case.scale, out=out, workspace=ws)
+        buf = (ctypes.c_uint64 * (len(PTRACE_FIELDS) * n_ctas))()
+        st = lib.tl_prefill_trace_read(buf, n_ctas)
+        if st != 0:
+            raise RuntimeError(f"tl_prefill_trace_read: {lib.tl_status_string(st).decode()}")
+        if i >= 2:
+            rows = [list(buf[k * len(PTRACE_FIELDS):(k + 1) * len(PTRACE_FIELDS)])
+                    for k in range(n_ctas)]
+            res.append(prefill_step_summary(rows))
+    med = {k: statistics.median(r[k] for r in res) for k in res[0]}
+    med.update(workload="B=8 x T=2048 prefill batch, Hq=32, Hkv=8, d=128, bf16", calls=args.calls)
+    return med
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--prefill", action="store_true",
+                    help="the prefill step trace instead of the decode timeline")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--length", type=int, default=0,
                     help="every sequence this long (default: the Llama-3-8B step's mix)")
@@ -84,6 +154,9 @@ def main(argv=None) -> None:
     ap.add_argument("--calls", type=int, default=10)
     ap.add_argument("--seed", type=int, default=0)
     args = ap.parse_args(argv)
+    if args.prefill:
+        print(json.dumps(trace_prefill(args)))
+        return
 
     lib = _lib.load(path=build_trace_library())
     from . import api

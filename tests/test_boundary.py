@@ -214,3 +214,9 @@ def test_the_default_library_has_no_decode_trace(lib):
     buf = (ctypes.c_uint64 * 8)()
     assert lib.tl_decode_trace_reset() == tl.TL_ERR_UNSUPPORTED
     assert lib.tl_decode_trace_read(buf, 8) == tl.TL_ERR_UNSUPPORTED
+
+
+def test_the_default_library_has_no_prefill_trace(lib):
+    buf = (ctypes.c_uint64 * 7)()
+    assert lib.tl_prefill_trace_reset() == tl.TL_ERR_UNSUPPORTED
+    assert lib.tl_prefill_trace_read(buf, 1) == tl.TL_ERR_UNSUPPORTED
