@@ -822,6 +822,21 @@ __device__ __forceinline__ void i8x4_as_f16x2x2(uint32_t w, uint32_t& lo, uint32
   asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(lo) : "r"(0x64806480u));
   asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(hi) : "r"(0x64806480u));
 }
+// The two halves of an fp16 pair as floats (exact).
+__device__ __forceinline__ void f16x2_to_floats(uint32_t x, float& lo, float& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+      : "=f"(lo), "=f"(hi)
+      : "r"(x));
+}
+// The same without the subtraction: each value is 1152 + c, exact.  The
+// int8 keys-as-rows path widens K this way and takes 1152 x (the query row's
+// sum) out of each dot product before the K scale, one add per score instead
+// of two packed subtractions per four codes.
+__device__ __forceinline__ void i8x4_as_f16x2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140u);
+  hi = __byte_perm(u, 0x64646464u, 0x4342u);
+}
 // The same for a transposed pair of code pairs (bytes: key k codes c, c+1;
 // key k+1 codes c, c+1): lo = (key k, key k+1) at code c, hi at code c+1.
 __device__ __forceinline__ void i8x4_keys_as_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -1127,6 +1142,25 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
     if (KV8 && __any_sync(0xffffffffu, q_over) && lane == 0)
       report(P.error_word, TL_DEVERR_VALUE_RANGE);
     __syncwarp();
+    // int8 keys as rows: -1152 x the sum of the fp16 query values of the
+    // lane's score columns 2t and 2t + 1 (the B fragments hold column g's
+    // values at four d a K step; the sum over t completes a column)
+    float kb0 = 0.f, kb1 = 0.f;
+    if constexpr (I8 && KT) {
+      float part = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+          float x0, x1;
+          f16x2_to_floats(qa[ks][k], x0, x1);
+          part += x0 + x1;
+        }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      kb0 = -1152.f * __shfl_sync(0xffffffffu, part, 8 * (lane & 3));
+      kb1 = -1152.f * __shfl_sync(0xffffffffu, part, 8 * (lane & 3) + 4);
+    }
 
     // rows-as-rows: o[n] is n-tile n of O (16 rows x 8 d); keys-as-rows:
     // o[j] is O^T for d = 16j .. 16j + 15 (16 d x 8 columns)
@@ -1203,8 +1237,8 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
           for (int h = 0; h < 2; ++h) {
             uint32_t a0, a1, a2, a3;
             if constexpr (I8) {
-              i8x4_as_f16x2x2(w[2 * h], a0, a2);
-              i8x4_as_f16x2x2(w[2 * h + 1], a1, a3);
+              i8x4_as_f16x2x2_biased(w[2 * h], a0, a2);
+              i8x4_as_f16x2x2_biased(w[2 * h + 1], a1, a3);
             } else {
               e4m3x4_as_f16x2x2(w[2 * h], a0, a2);
               e4m3x4_as_f16x2x2(w[2 * h + 1], a1, a3);
@@ -1215,7 +1249,7 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[j][e] += s2[e];
       }
-      if constexpr (I8) {  // each key's dot products times its K scale
+      if constexpr (I8) {  // each key's dot products, less the bias, times its K scale
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
           if (j >= nj) break;
@@ -1223,10 +1257,10 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
           const uint32_t sa = scale_ring + stage * L::kScaleBytes + ((sub0 + j) * kChunk + qr) * 4;
           asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(k0) : "r"(sa));
           asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(k1) : "r"(sa + 32));
-          s[j][0] *= k0;
-          s[j][1] *= k0;
-          s[j][2] *= k1;
-          s[j][3] *= k1;
+          s[j][0] = (s[j][0] + kb0) * k0;
+          s[j][1] = (s[j][1] + kb1) * k0;
+          s[j][2] = (s[j][2] + kb0) * k1;
+          s[j][3] = (s[j][3] + kb1) * k1;
         }
       }
       constexpr uint32_t all_keys = nj == 1 ? 0xffffu : 0xffffffffu;
