@@ -318,6 +318,14 @@ __device__ __forceinline__ float add_f16x2_halves(float acc, uint32_t x) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
   return pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
 }
+// (s0, s1) += (a0, a1)^2 in one packed f32 FMA.
+__device__ __forceinline__ void sq_acc_f32x2(float a0, float a1, float& s0, float& s1) {
+  uint64_t a, acc;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(acc) : "f"(s0), "f"(s1));
+  asm("fma.rn.f32x2 %0, %1, %1, %0;\n" : "+l"(acc) : "l"(a));
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(s0), "=f"(s1) : "l"(acc));
+}
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.u16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
@@ -403,6 +411,7 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
   }
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   __shared__ int s_page[kCvtKeys];  // page of each key of the tile; -1: write zeros
+  __shared__ int s_slot[kCvtKeys];  // its slot in the pool (-1 with the page)
   const int b = (int)blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t cap = position_cap(P);
@@ -490,6 +499,7 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
       }
     }
     s_page[r] = page;
+    s_slot[r] = page < 0 ? -1 : page * P.page_size + k % P.page_size;
   }
   __syncthreads();
   const int r0 = 0, r1 = min(end - k0, kCvtKeys);  // keys of the tile to write
@@ -507,8 +517,22 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
     const int total = (r1 - r0) * units;
     const uint8_t* v8 = reinterpret_cast<const uint8_t*>(P.v_cache);
     const uint8_t* k8 = reinterpret_cast<const uint8_t*>(P.k_cache);
+    // unit idx of the tile: key r, unit u (a shift and a mask when the unit
+    // count is a power of two, as for 1, 2, 4, 8 or 16 KV heads)
+    const int ushift = (units & (units - 1)) == 0 ? __ffs(units) - 1 : -1;
+    auto split_idx = [&](int idx, int& r, int& u) {
+      if (ushift >= 0) {
+        r = r0 + (idx >> ushift);
+        u = idx & (units - 1);
+      } else {
+        r = r0 + idx / units;
+        u = idx - (r - r0) * units;
+      }
+    };
+    // a key's scale of KV head g: [page][g][position in the page]
     auto scale_index = [&](int r, int g) {
-      return ((size_t)s_page[r] * P.h_kv + g) * P.page_size + (k0 + r) % P.page_size;
+      const int in_page = s_slot[r] - s_page[r] * P.page_size;
+      return ((size_t)s_page[r] * P.h_kv + g) * P.page_size + in_page;
     };
     bool big_i8 = false;
     for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
@@ -520,9 +544,10 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
         c[i] = make_uint2(0u, 0u);
         vs[i] = 0.f;
         if (idx < total) {
-          const int r = r0 + idx / units, u = idx % units;
+          int r, u;
+          split_idx(idx, r, u);
           if (s_page[r] >= 0) {
-            const size_t row = ((size_t)s_page[r] * P.page_size + (k0 + r) % P.page_size) * P.h_kv * 128;
+            const size_t row = (size_t)s_slot[r] * P.h_kv * 128;
             c[i] = __ldg(reinterpret_cast<const uint2*>(v8 + row) + u);
             vs[i] = __ldg(P.v_scales + scale_index(r, u >> 4));
           }
@@ -531,7 +556,9 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
 #pragma unroll
       for (int i = 0; i < kCvtUnroll; ++i) {
         const int idx = base + i * kCvtThreads + (int)threadIdx.x;
-        if (idx < total && s_page[r0 + idx / units] >= 0) {
+        int r = 0, u = 0;
+        if (idx < total) split_idx(idx, r, u);
+        if (idx < total && s_page[r] >= 0) {
           uint4 f16, bf16;
           i8x8_to_f16_bf16(c[i], f16, bf16);
           big_i8 |= !((float)i8x8_max_abs(c[i]) * vs[i] <= 8.f);
@@ -590,9 +617,10 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
         a[i] = c[i] = make_uint2(0u, 0u);
         vs[i] = 0.f;
         if (idx < total) {
-          const int r = r0 + idx / units, u = idx % units;
+          int r, u;
+          split_idx(idx, r, u);
           if (s_page[r] >= 0) {
-            const size_t row = ((size_t)s_page[r] * P.page_size + (k0 + r) % P.page_size) * P.h_kv * 128;
+            const size_t row = (size_t)s_slot[r] * P.h_kv * 128;
             a[i] = __ldg(reinterpret_cast<const uint2*>(v8 + row) + u);
             c[i] = __ldg(reinterpret_cast<const uint2*>(k8 + row) + u);
             if (!tile_big) vs[i] = __ldg(P.v_scales + scale_index(r, u >> 4));
@@ -603,7 +631,8 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
       for (int i = 0; i < kCvtUnroll; ++i) {
         const int idx = base + i * kCvtThreads + (int)threadIdx.x;
         if (idx < total) {
-          const int r = r0 + idx / units, u = idx % units;
+          int r, u;
+          split_idx(idx, r, u);
           const size_t dst =
               (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start + r)) * 128 + (u & 15) * 8;
           uint4 f16, bf16;
@@ -620,6 +649,71 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
   const int total = (r1 - r0) * units;
   uint32_t vmax = 0;  // max |bf16 bits| seen, per half-word
   uint32_t cmax = 0;  // e4m3 pools: max |code| seen, per byte
+  if ((units & (units - 1)) == 0 && units <= kCvtThreads) {
+    // a power-of-two unit count: each thread keeps one unit u of every
+    // kpp-th key, so its source and destination offsets are fixed but for
+    // the key (no division per unit); 8 keys' loads in flight
+    const int kpp = kCvtThreads / units;
+    const int u = (int)threadIdx.x & (units - 1), kof = (int)threadIdx.x / units;
+    const size_t dst0 =
+        (((size_t)b * P.h_kv + (u >> 4)) * P.v_keys + (k0 - start)) * 128 + (u & 15) * 8;
+    const int nkeys = r1 - r0;
+    float sq0 = 0.f, sq1 = 0.f;  // bf16 pools: two sums of squares (packed FMAs)
+    for (int rb = kof; rb < nkeys; rb += kpp * kCvtUnroll) {
+      uint4 x[kCvtUnroll];  // bf16 V, or (e4m3) V in .x.y and K in .z.w
+#pragma unroll
+      for (int i = 0; i < kCvtUnroll; ++i) {
+        const int r = rb + i * kpp;
+        x[i] = make_uint4(0u, 0u, 0u, 0u);
+        const int slot = r < nkeys ? s_slot[r] : -1;
+        if (slot >= 0) {
+          const size_t row = (size_t)slot * P.h_kv * 128;
+          if (KV8) {
+            const uint2 a = __ldg(reinterpret_cast<const uint2*>(
+                                      reinterpret_cast<const uint8_t*>(P.v_cache) + row) + u);
+            const uint2 c = __ldg(reinterpret_cast<const uint2*>(
+                                      reinterpret_cast<const uint8_t*>(P.k_cache) + row) + u);
+            x[i] = make_uint4(a.x, a.y, c.x, c.y);
+          } else {
+            x[i] = __ldg(reinterpret_cast<const uint4*>(P.v_cache + row) + u);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kCvtUnroll; ++i) {
+        const int r = rb + i * kpp;
+        if (r >= nkeys) break;
+        const size_t dst = dst0 + (size_t)r * 128;
+        const uint4 y = x[i];
+        const bool live = s_slot[r] >= 0;
+        if (KV8) {  // e4m3 values are exact in both fp16 and bf16
+          cmax = __vmaxu4(cmax, __vmaxu4(y.x & 0x7f7f7f7fu, y.y & 0x7f7f7f7fu));
+          const uint4 f16 = make_uint4(e4m3x2_to_f16x2(y.x), e4m3x2_to_f16x2(y.x >> 16),
+                                       e4m3x2_to_f16x2(y.y), e4m3x2_to_f16x2(y.y >> 16));
+          *reinterpret_cast<uint4*>(ws + dst) = f16;
+          sumsq += sumsq_f16x8(f16);  // zeros for a dead key
+          *reinterpret_cast<uint4*>(P.ws_k + dst) =
+              make_uint4(e4m3x2_to_bf16x2(y.z), e4m3x2_to_bf16x2(y.z >> 16),
+                         e4m3x2_to_bf16x2(y.w), e4m3x2_to_bf16x2(y.w >> 16));
+        } else {
+          vmax = max_u16x2(vmax, max_u16x2(max_u16x2(y.x & 0x7fff7fffu, y.y & 0x7fff7fffu),
+                                           max_u16x2(y.z & 0x7fff7fffu, y.w & 0x7fff7fffu)));
+          const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+          uint32_t h[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // the bf16 pair as f32 (exact): fp16 for the copy, squares for the RMS
+            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+            h[k] = pack_f16x2(lo, hi);
+            sq_acc_f32x2(lo, hi, sq0, sq1);
+          }
+          *reinterpret_cast<uint4*>(ws + dst) = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        n_vals += live ? 8 : 0;
+      }
+    }
+    sumsq += sq0 + sq1;
+  } else
   // units of 8 elements: 16 bytes of a bf16 row, 8 bytes of an e4m3 row
   for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
     uint4 x[kCvtUnroll];  // bf16 V, or (e4m3) V in .x.y and K in .z.w
