@@ -39,8 +39,8 @@ WORKLOAD = "Llama-3-8B-shaped decode layer: B=64, Hq=32, Hkv=8, d=128, bf16, pag
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
 # these default workloads (the summaries under profiles/ give the command); they hold
 # only for the kernels as they were captured and for these workloads.
-DECODE_TRAFFIC = (1264384000 + 2992128, "profiles/decode_bf16_llama8b_b64.md")
-PREFILL_TRAFFIC = (335409152 + 207243008, "profiles/prefill_tc_batched_b8.md")
+DECODE_TRAFFIC = (1264400640 + 2854912, "profiles/decode_bf16_llama8b_b64.md")
+PREFILL_TRAFFIC = (326684160 + 206615296, "profiles/prefill_tc_batched_b8.md")
 WRITE_TRAFFIC = (40167168 + 2732032, "profiles/kv_cache_write_prefill_chunk_16k.md")
 
 

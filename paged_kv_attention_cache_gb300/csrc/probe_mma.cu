@@ -41,6 +41,24 @@
 //  23 TS groups, A fixed (448), D alternating 0 / 256, each group starting
 //     a fresh accumulator (the first MMA of a group does not accumulate)
 //  24 form 22 with every group starting a fresh accumulator
+//  25 one query tile, all TS, no MMA reading what an MMA wrote: S = Q K^T
+//     (A = Q in columns 448..511) into 0..127 or 128..255 in turn, fresh
+//     each group, alternating with O += P V (A = P in columns 384..447,
+//     D = 256..383)
+//  26 form 25 with both groups fp16 and S's B operand K-major (as K tiles
+//     are), P.V's MN-major (as V tiles are)
+//  27 form 26 with S in bf16
+//  28 form 26 with P.V too starting a fresh accumulator each group
+//  29 form 26 with S too accumulating (no fresh accumulator anywhere)
+//  30 TS fp16, A fixed (448), D in turn 0, 256, 128, 256 (three accumulators)
+//  31 TS fp16, A fixed (448), D in turn 0, 128, 256, 384 (four accumulators)
+//  32 TS fp16, D fixed (256), A alternating 384 / 448
+//  33 TS fp16, D fixed (0), A alternating 256 / 384
+//  34 TS fp16, D fixed (256), A alternating 0 / 64
+//  35 TS fp16, (A, D) alternating (448, 0) / (384, 256): one S buffer
+//  36 TS fp16, (A, D) in turn (448, 0), (384, 256), (448, 128), (384, 256)
+//  37 form 36 with both B operands K-major (one instruction descriptor)
+//  38 form 37 with P read from the other S buffer (as when P replaces S)
 // The marginal cost per MMA is (t(n1) - t(n0)) / (n1 - n0), which takes out
 // the issue-to-first-MMA and commit latencies.
 #include <cuda_runtime.h>
@@ -51,7 +69,7 @@
 namespace tl {
 namespace probe {
 
-constexpr int kForms = 25;
+constexpr int kForms = 39;
 constexpr int kSmemBytes = 100 * 1024;
 
 __device__ __forceinline__ long long clk() {
@@ -90,6 +108,46 @@ __device__ __forceinline__ void issue8(uint32_t tm, uint32_t sb, uint32_t id_ss,
       const uint64_t a2 = tc::sdesc(sb + (i8 & 1) * 65536 + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
                                     1024);
       tc::mma_ss(tm + 128 * (i8 & 1), a2, b_ss, id_ss, kk > 0);
+    } else if (F == 37 || F == 38) {
+      const int g = i8 & 3;
+      const uint32_t id = tc::idesc_f16(128, 128, 0, 0);
+      if ((g & 1) == 0)
+        tc::mma_ts(tm + 128 * (g >> 1), tm + 448 + 8 * kk, b_ss, id, 1u);
+      else
+        tc::mma_ts(tm + 256, tm + (F == 37 ? 384u : 128u * ((g >> 1) ^ 1)) + 8 * kk, b_ss, id, 1u);
+    } else if (F >= 35) {
+      const int g = i8 & 3;
+      const uint32_t a = (g & 1) ? 384u : 448u;
+      const uint32_t d = (g & 1) ? 256u : (F == 35 ? 0u : 128u * (g >> 1));
+      tc::mma_ts(tm + d, tm + a + 8 * kk, b_ts, id_ts, 1u);
+    } else if (F >= 32) {
+      const uint32_t a0 = F == 32 ? 384u : F == 33 ? 256u : 0u;
+      const uint32_t a1 = F == 32 ? 448u : F == 33 ? 384u : 64u;
+      const uint32_t d = F == 33 ? 0u : 256u;
+      tc::mma_ts(tm + d, tm + ((i8 & 1) ? a1 : a0) + 8 * kk, b_ts, id_ts, 1u);
+    } else if (F == 30 || F == 31) {
+      const int g = i8 & 3;
+      const uint32_t d = F == 30 ? (g & 1 ? 256u : 128u * (g >> 1)) : 128u * g;
+      tc::mma_ts(tm + d, tm + 448 + 8 * kk, b_ts, id_ts, 1u);
+    } else if (F == 28 || F == 29) {
+      if ((i8 & 1) == 0)
+        tc::mma_ts(tm + 128 * ((i8 >> 1) & 1), tm + 448 + 8 * kk, b_ss,
+                   tc::idesc_f16(128, 128, 0, 0), F == 29 ? 1u : (uint32_t)(kk > 0));
+      else
+        tc::mma_ts(tm + 256, tm + 384 + 8 * kk, b_ts, id_ts, F == 29 ? 1u : (uint32_t)(kk > 0));
+    } else if (F == 26 || F == 27) {
+      if ((i8 & 1) == 0)
+        tc::mma_ts(tm + 128 * ((i8 >> 1) & 1), tm + 448 + 8 * kk, b_ss,
+                   F == 26 ? tc::idesc_f16(128, 128, 0, 0) : tc::idesc_bf16(128, 128, 0, 0),
+                   kk > 0);
+      else
+        tc::mma_ts(tm + 256, tm + 384 + 8 * kk, b_ts, id_ts, 1u);
+    } else if (F == 25) {
+      if ((i8 & 1) == 0)
+        tc::mma_ts(tm + 128 * ((i8 >> 1) & 1), tm + 448 + 8 * kk, b_ts,
+                   tc::idesc_bf16(128, 128, 0, 1), kk > 0);
+      else
+        tc::mma_ts(tm + 256, tm + 384 + 8 * kk, b_ts, id_ts, 1u);
     } else if (F == 23) {
       tc::mma_ts(tm + 256 * (i8 & 1), tm + 448 + 8 * kk, b_ts, id_ts, kk > 0);
     } else if (F == 24) {
@@ -262,7 +320,21 @@ extern "C" int tl_probe_mma_cycles(int form, int n_mma, long long* cycles_ns) {
     case 21: e = launch_probe<21>(n8, d); break;
     case 22: e = launch_probe<22>(n8, d); break;
     case 23: e = launch_probe<23>(n8, d); break;
-    default: e = launch_probe<24>(n8, d); break;
+    case 24: e = launch_probe<24>(n8, d); break;
+    case 25: e = launch_probe<25>(n8, d); break;
+    case 26: e = launch_probe<26>(n8, d); break;
+    case 27: e = launch_probe<27>(n8, d); break;
+    case 28: e = launch_probe<28>(n8, d); break;
+    case 29: e = launch_probe<29>(n8, d); break;
+    case 30: e = launch_probe<30>(n8, d); break;
+    case 31: e = launch_probe<31>(n8, d); break;
+    case 32: e = launch_probe<32>(n8, d); break;
+    case 33: e = launch_probe<33>(n8, d); break;
+    case 34: e = launch_probe<34>(n8, d); break;
+    case 35: e = launch_probe<35>(n8, d); break;
+    case 36: e = launch_probe<36>(n8, d); break;
+    case 37: e = launch_probe<37>(n8, d); break;
+    default: e = launch_probe<38>(n8, d); break;
   }
   if (e == cudaSuccess) e = cudaMemcpy(cycles_ns, d, 2 * sizeof(long long), cudaMemcpyDeviceToHost);
   cudaFree(d);

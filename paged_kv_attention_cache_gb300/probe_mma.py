@@ -34,6 +34,20 @@ FORMS = [  # (name, M, N)
     ("TS: A alternating, D fixed", 128, 128),
     ("TS: D alternating, fresh accumulator per group", 128, 128),
     ("TS: A alternating, D fixed, fresh accumulator per group", 128, 128),
+    ("one tile all TS, P and Q in columns no MMA writes", 128, 128),
+    ("the same, fp16, S's B K-major", 128, 128),
+    ("the same, S in bf16", 128, 128),
+    ("all-TS fp16, every group a fresh accumulator", 128, 128),
+    ("all-TS fp16, every group accumulating", 128, 128),
+    ("TS, three accumulators in turn", 128, 128),
+    ("TS, four accumulators in turn", 128, 128),
+    ("TS, A alternating 384 / 448", 128, 128),
+    ("TS, A alternating 256 / 384", 128, 128),
+    ("TS, A alternating 0 / 64", 128, 128),
+    ("TS, (A, D) pairs alternating, one S buffer", 128, 128),
+    ("TS, (A, D) pairs, two S buffers in turn", 128, 128),
+    ("the same, both B K-major, one descriptor", 128, 128),
+    ("the same, P from the other S buffer", 128, 128),
 ]
 
 
