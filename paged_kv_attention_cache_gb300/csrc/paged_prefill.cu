@@ -115,6 +115,8 @@ struct PrefillParams {
   int32_t cvt_gx;        // pre-pass CTAs per row (64-key tiles of the V copy)
   int32_t* cta_big;      // [B][cvt_gx] 1: the pre-pass CTA saw a V value with |v| > 8
   int32_t* row_big;      // [B] 1: the row reads a V value with |v| > 8 (P split in two)
+  uint16_t* ws_kt;       // 16-bit pools read by the all-TS kernel: an fp16 K^T copy,
+                         // [B][h_kv][key tile][d][128 keys] (else null)
 };
 
 // Position bound of the call: the table width, or none for a ring (whose
@@ -162,13 +164,15 @@ constexpr int kPlanBuckets = 8192;   // two halves (rows without and with the sp
 // (| bf16 K for e4m3 pools)], each part 256-byte aligned; the copies are
 // [B][h_kv][v_keys][128].
 struct WsLayout {
-  size_t tiles, order, rows, cta_big, row_big, v, k, ks, vs, ivs, total;
+  size_t tiles, order, rows, cta_big, row_big, v, k, ks, vs, ivs, kt, total;
 };
 constexpr int kCvtKeys = 64;  // keys per pre-pass CTA (divides kBN)
 // kv8: e4m3 or int8 pools (a bf16 copy of K); i8: int8 pools (and the keys'
 // scales, [B][h_kv][v_keys] f32 each: K, V and 1 / V).
+// kt: 16-bit pools read by the all-TS attention kernel (an fp16 K^T copy
+// the size of the V copy).
 inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_keys, bool kv8,
-                          bool i8 = false) {
+                          bool i8 = false, bool kt = false) {
   const size_t pairs = (size_t)(B * n_pairs) * 4;
   const size_t copy = (size_t)B * h_kv * (size_t)v_keys * 128 * 2;
   const size_t gx = (size_t)((v_keys + kCvtKeys - 1) / kCvtKeys);
@@ -184,8 +188,22 @@ inline WsLayout ws_layout(int64_t B, int64_t n_pairs, int64_t h_kv, int64_t v_ke
   L.ks = L.k + (kv8 ? copy : 0);
   L.vs = L.ks + (i8 ? scales : 0);
   L.ivs = L.vs + (i8 ? scales : 0);
-  L.total = L.ivs + (i8 ? scales : 0);
+  L.kt = L.ivs + (i8 ? scales : 0);
+  L.total = L.kt + (kt ? copy : 0);
   return L;
+}
+// The all-TS attention kernel (prefill_ts.cuh), a build option
+// (-DTL_PREFILL_ALL_TS=1; the default library keeps the paired SS/TS
+// kernel, which measured faster: the single-tile chain exposes the MMAs'
+// completion latency).  With it, the calls that take it: 16-bit pools with
+// 1, 2, 4, 8 or 16 KV heads (a power-of-two unit count for the pre-pass's
+// K^T copy); d is 128 for every prefill call.
+#ifndef TL_PREFILL_ALL_TS
+#define TL_PREFILL_ALL_TS 0
+#endif
+inline bool ts_path(tl_dtype dtype, int64_t h_kv) {
+  return TL_PREFILL_ALL_TS && dtype == TL_BF16 && h_kv >= 1 && h_kv <= 16 &&
+         (h_kv & (h_kv - 1)) == 0;
 }
 // Keys per row of the V copy: the table's positions, or for a ring the
 // ring's positions plus the rounding of the copy's start and end to tiles.
@@ -713,6 +731,48 @@ __global__ void __launch_bounds__(kCvtThreads, kCvtBlocksPerSm)
       }
     }
     sumsq += sq0 + sq1;
+    if (KIND == 0 && P.ws_kt != nullptr) {
+      // the fp16 K^T copy of the all-TS attention kernel: per KV head, key
+      // tile and d, the tile's 128 keys; this CTA's 64 keys are one half of
+      // a tile.  A thread takes a block of 8 keys x 8 d (eight 16-byte row
+      // reads), transposes it in registers (byte permutes of fp16 halves)
+      // and writes 8 d rows of 8 keys, 16 bytes each; keys past the CTA's
+      // range and of bad pages are zeros
+      const int kr0 = k0 - start, kofs = kr0 % kBN;
+      const size_t tile_row = (size_t)(kr0 / kBN) * kBN;
+      bool k_over = false;
+      for (int blk = threadIdx.x; blk < (kCvtKeys / 8) * units; blk += kCvtThreads) {
+        const int uu = blk & (units - 1), kg = blk / units;
+        const int g = uu >> 4, d8 = (uu & 15) * 8;
+        uint32_t h[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = kg * 8 + i;
+          const int slot = r < nkeys ? s_slot[r] : -1;
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (slot >= 0) x = __ldg(reinterpret_cast<const uint4*>(P.k_cache + (size_t)slot * P.h_kv * 128) + uu);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = w[k] & 0x7fffu, hi = (w[k] >> 16) & 0x7fffu;
+            k_over |= (lo >= kBf16TooBig && lo < kBf16Inf) || (hi >= kBf16TooBig && hi < kBf16Inf);
+            h[i][k] = bf16x2_to_f16x2(w[k]);
+          }
+        }
+        uint16_t* dst0 = P.ws_kt + ((size_t)(b * P.h_kv + g) * P.v_keys + tile_row + d8) * 128 +
+                         kofs + kg * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {  // d row d8 + e: keys (2w, 2w + 1) in word w
+          const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+          const uint4 out = make_uint4(__byte_perm(h[0][e >> 1], h[1][e >> 1], sel),
+                                       __byte_perm(h[2][e >> 1], h[3][e >> 1], sel),
+                                       __byte_perm(h[4][e >> 1], h[5][e >> 1], sel),
+                                       __byte_perm(h[6][e >> 1], h[7][e >> 1], sel));
+          *reinterpret_cast<uint4*>(dst0 + (size_t)e * 128) = out;
+        }
+      }
+      if (k_over) report(P.error_word, TL_DEVERR_VALUE_RANGE);
+    }
   } else
   // units of 8 elements: 16 bytes of a bf16 row, 8 bytes of an e4m3 row
   for (int base = 0; base < total; base += kCvtThreads * kCvtUnroll) {
@@ -1549,6 +1609,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace tl
 
+#if TL_PREFILL_ALL_TS
+#include "prefill_ts.cuh"
+#endif
+
 namespace tl {
 
 static size_t prefill_ws_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv, int32_t d,
@@ -1561,7 +1625,7 @@ static size_t prefill_ws_size(int32_t B, int32_t T, int32_t h_q, int32_t h_kv, i
   const int tpt = std::max(1, 128 / (h_q / h_kv));
   const int64_t n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
   return ws_layout(B, n_pairs, h_kv, v_copy_keys(max_pages_per_seq, page_size, ring_pages),
-                   dtype != TL_BF16, dtype == TL_INT8)
+                   dtype != TL_BF16, dtype == TL_INT8, ts_path(dtype, h_kv))
       .total;
 }
 
@@ -1628,8 +1692,9 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   const int n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
   int64_t v_keys = v_copy_keys(max_pages_per_seq, page_size, ring_pages);
   if (v_keys >= ((int64_t)1 << 31)) return TL_ERR_UNSUPPORTED;
-  if (workspace_bytes < ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8).total) {
-    const WsLayout full = ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8);
+  const bool ts = ts_path(dtype, h_kv);
+  if (workspace_bytes < ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8, ts).total) {
+    const WsLayout full = ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8, ts);
     const size_t copies = full.total - full.v;  // copies and scales of every row at v_keys keys
     const size_t room = workspace_bytes > full.v ? workspace_bytes - full.v : 0;
     // their bytes per key of a row (over all rows and KV heads; the rounding
@@ -1637,12 +1702,13 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
     const size_t per_key = copies / (size_t)v_keys + 1;
     int64_t fit = (int64_t)(room / per_key);
     fit = fit / kBN * kBN;
-    while (fit >= kMinCopyKeys && ws_layout(B, n_pairs, h_kv, fit, kv8, i8).total > workspace_bytes)
+    while (fit >= kMinCopyKeys &&
+           ws_layout(B, n_pairs, h_kv, fit, kv8, i8, ts).total > workspace_bytes)
       fit -= kBN;
     if (fit < kMinCopyKeys) return TL_ERR_WORKSPACE;
     v_keys = fit;
   }
-  const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8);
+  const WsLayout L = ws_layout(B, n_pairs, h_kv, v_keys, kv8, i8, ts);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   int* counter = reinterpret_cast<int*>(wsb);
   uint16_t* ws_v = reinterpret_cast<uint16_t*>(wsb + L.v);
@@ -1662,7 +1728,8 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   P.cvt_gx = (int32_t)((v_keys + kCvtKeys - 1) / kCvtKeys);
   P.cta_big = reinterpret_cast<int32_t*>(wsb + L.cta_big);
   P.row_big = reinterpret_cast<int32_t*>(wsb + L.row_big);
-  CUtensorMap qmap, kmap, vmap, omap;
+  P.ws_kt = ts ? reinterpret_cast<uint16_t*>(wsb + L.kt) : nullptr;
+  CUtensorMap qmap, kmap, vmap, omap, ktmap;
   {
     const uint64_t qd[3] = {128, (uint64_t)h_q, (uint64_t)B * T};
     const uint64_t qs[2] = {128 * 2, (uint64_t)h_q * 128 * 2};
@@ -1687,6 +1754,9 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
               : encode_bf16_tensor_map(&kmap, k_cache, 3, kd, ks, kb, true)) ||
         !encode_bf16_tensor_map(&vmap, ws_v, 3, vd, vs, vb, true))
       return TL_ERR_CUDA;
+    // the all-TS kernel's K^T copy: (key in the tile, key tile x 128 + d,
+    // row x KV head), the V copy's shape; boxes of 64 keys x 128 d
+    if (ts && !encode_bf16_tensor_map(&ktmap, P.ws_kt, 3, vd, vs, vb, true)) return TL_ERR_CUDA;
   }
   auto tc_fast = i8 ? prefill_tc_kernel<false, true> : prefill_tc_kernel<false, false>;
   auto tc_split = i8 ? prefill_tc_kernel<true, true> : prefill_tc_kernel<true, false>;
@@ -1721,14 +1791,30 @@ static tl_status prefill_impl(const void* q, const void* k_cache, const void* v_
   cfg.blockDim = dim3(kPlanThreads);
   if (cudaLaunchKernelEx(&cfg, prefill_plan_kernel, P) != cudaSuccess) return TL_ERR_CUDA;
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = tc_smem;
   // rows whose V holds no value above 8 in magnitude (single fp16 P), then
   // the others (P split in two); each kernel skips the other's rows
-  if (cudaLaunchKernelEx(&cfg, tc_fast, P, qmap, kmap, vmap, omap, box_rows, counter) !=
-          cudaSuccess ||
-      cudaLaunchKernelEx(&cfg, tc_split, P, qmap, kmap, vmap, omap, box_rows, counter + 1) !=
-          cudaSuccess)
+  if (ts) {
+#if TL_PREFILL_ALL_TS
+    if (cudaFuncSetAttribute(prefill_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTsSmem) != cudaSuccess)
+      return TL_ERR_CUDA;
+    cfg.blockDim = dim3(kTsThreads);
+    cfg.dynamicSmemBytes = kTsSmem;
+    if (cudaLaunchKernelEx(&cfg, prefill_ts_kernel, P, qmap, ktmap, vmap, omap, counter) !=
+        cudaSuccess)
+      return TL_ERR_CUDA;
+#endif
+  } else {
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = tc_smem;
+    if (cudaLaunchKernelEx(&cfg, tc_fast, P, qmap, kmap, vmap, omap, box_rows, counter) !=
+        cudaSuccess)
+      return TL_ERR_CUDA;
+  }
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = tc_smem;
+  if (cudaLaunchKernelEx(&cfg, tc_split, P, qmap, kmap, vmap, omap, box_rows, counter + 1) !=
+      cudaSuccess)
     return TL_ERR_CUDA;
   return launch_status();
 }
@@ -1857,6 +1943,6 @@ extern "C" size_t tl_paged_attn_prefill_workspace_size_keys(int32_t B, int32_t T
   const int tpt = std::max(1, 128 / (h_q / h_kv));
   const int64_t n_pairs = (T + 2 * tpt - 1) / (2 * tpt);
   return tl::ws_layout(B, n_pairs, h_kv, tl::v_copy_keys_for_span(max_row_keys),
-                       dtype != TL_BF16, dtype == TL_INT8)
+                       dtype != TL_BF16, dtype == TL_INT8, tl::ts_path(dtype, h_kv))
       .total;
 }

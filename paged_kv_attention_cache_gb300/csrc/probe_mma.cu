@@ -59,6 +59,10 @@
 //  36 TS fp16, (A, D) in turn (448, 0), (384, 256), (448, 128), (384, 256)
 //  37 form 36 with both B operands K-major (one instruction descriptor)
 //  38 form 37 with P read from the other S buffer (as when P replaces S)
+//  39 TS fp16 N=64, A fixed (448), D = 0, MN-major B
+//  40 two query tiles with Q in TMEM and 64-key S tiles, all TS fp16
+//     MN-major: per tile, 8 S MMAs N=64 (A = Q_a at 384 + 64a, D = 64a) then
+//     4 P.V MMAs N=128 (A = P_a in S_a's columns, D = O_a at 256 + 128a)
 // The marginal cost per MMA is (t(n1) - t(n0)) / (n1 - n0), which takes out
 // the issue-to-first-MMA and commit latencies.
 #include <cuda_runtime.h>
@@ -69,7 +73,7 @@
 namespace tl {
 namespace probe {
 
-constexpr int kForms = 39;
+constexpr int kForms = 41;
 constexpr int kSmemBytes = 100 * 1024;
 
 __device__ __forceinline__ long long clk() {
@@ -108,6 +112,16 @@ __device__ __forceinline__ void issue8(uint32_t tm, uint32_t sb, uint32_t id_ss,
       const uint64_t a2 = tc::sdesc(sb + (i8 & 1) * 65536 + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
                                     1024);
       tc::mma_ss(tm + 128 * (i8 & 1), a2, b_ss, id_ss, kk > 0);
+    } else if (F == 39) {
+      tc::mma_ts(tm, tm + 448 + 8 * kk, b_ts, tc::idesc_f16(128, 64, 0, 1), 1u);
+    } else if (F == 40) {
+      // groups of 8: S0 (8 x N=64), PV0 (4) + PV0 (4, next K half), S1, PV1
+      const int g = i8 & 3, tile = g >> 1;
+      if ((g & 1) == 0)
+        tc::mma_ts(tm + 64 * tile, tm + 384 + 64 * tile + 8 * kk, b_ts, tc::idesc_f16(128, 64, 0, 1),
+                   kk > 0);
+      else
+        tc::mma_ts(tm + 256 + 128 * tile, tm + 64 * tile + 8 * (kk & 3), b_ts, id_ts, 1u);
     } else if (F == 37 || F == 38) {
       const int g = i8 & 3;
       const uint32_t id = tc::idesc_f16(128, 128, 0, 0);
@@ -334,7 +348,9 @@ extern "C" int tl_probe_mma_cycles(int form, int n_mma, long long* cycles_ns) {
     case 35: e = launch_probe<35>(n8, d); break;
     case 36: e = launch_probe<36>(n8, d); break;
     case 37: e = launch_probe<37>(n8, d); break;
-    default: e = launch_probe<38>(n8, d); break;
+    case 38: e = launch_probe<38>(n8, d); break;
+    case 39: e = launch_probe<39>(n8, d); break;
+    default: e = launch_probe<40>(n8, d); break;
   }
   if (e == cudaSuccess) e = cudaMemcpy(cycles_ns, d, 2 * sizeof(long long), cudaMemcpyDeviceToHost);
   cudaFree(d);

@@ -48,6 +48,8 @@ FORMS = [  # (name, M, N)
     ("TS, (A, D) pairs, two S buffers in turn", 128, 128),
     ("the same, both B K-major, one descriptor", 128, 128),
     ("the same, P from the other S buffer", 128, 128),
+    ("TS N=64 alone", 128, 64),
+    ("two tiles, Q in TMEM, 64-key S, all TS", 128, 96),
 ]
 
 

@@ -14,7 +14,8 @@ The stamps are %globaltimer reads on the GPU; the traced build adds a few
 stores and atomics and one barrier per plan and combine CTA, nothing else, so
 its times run a little above the default build's.
 
-With --prefill it builds the library with -DTL_PREFILL_TRACE=1 instead and
+With --prefill it builds the library with -DTL_PREFILL_TRACE=1 instead (and
+with --all-ts also -DTL_PREFILL_ALL_TS=1, the all-TS attention kernel) and
 runs prefill calls over the B=8 x 2,048-token batch (0-1,500 left pads, prior
 context 0-6,144, Llama-3-8B heads; the cache write of the chunk first), then
 prints, over the attention CTAs, the cycles per 128-key step (both query
@@ -82,7 +83,12 @@ def trace_calls(call, lib, calls: int, warmup: int = 2) -> dict:
     return med
 
 
-def build_prefill_trace_library(force: bool = False) -> str:
+def build_prefill_trace_library(force: bool = False, all_ts: bool = False) -> str:
+    """The prefill trace build; all_ts: with the all-TS attention kernel
+    (-DTL_PREFILL_ALL_TS=1) in place of the paired SS/TS one."""
+    if all_ts:
+        return build.build_variant("prefill_trace_all_ts", build.SOURCES,
+                                   ["TL_PREFILL_TRACE=1", "TL_PREFILL_ALL_TS=1"], force=force)
     return build.build_variant("prefill_trace", build.SOURCES, ["TL_PREFILL_TRACE=1"],
                                force=force)
 
@@ -111,7 +117,7 @@ def prefill_step_summary(rows: list) -> dict:
 
 
 def trace_prefill(args) -> dict:
-    lib = _lib.load(path=build_prefill_trace_library())
+    lib = _lib.load(path=build_prefill_trace_library(all_ts=args.all_ts))
     from . import api
     from . import workloads as wl
 
@@ -139,7 +145,9 @@ def trace_prefill(args) -> dict:
                     for k in range(n_ctas)]
             res.append(prefill_step_summary(rows))
     med = {k: statistics.median(r[k] for r in res) for k in res[0]}
-    med.update(workload="B=8 x T=2048 prefill batch, Hq=32, Hkv=8, d=128, bf16", calls=args.calls)
+    med.update(workload="B=8 x T=2048 prefill batch, Hq=32, Hkv=8, d=128, bf16", calls=args.calls,
+               kernel="all-TS (one query tile: steps are tile-steps)" if args.all_ts
+               else "paired SS/TS (steps cover both query tiles)")
     return med
 
 
@@ -147,6 +155,8 @@ def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--prefill", action="store_true",
                     help="the prefill step trace instead of the decode timeline")
+    ap.add_argument("--all-ts", action="store_true",
+                    help="with --prefill: trace the all-TS attention kernel (a build option)")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--length", type=int, default=0,
                     help="every sequence this long (default: the Llama-3-8B step's mix)")

@@ -3,8 +3,9 @@
 bit, and its timeline stamps come in the order the launches run (plan,
 attention kernel, combine), for the warp-planned and the block-planned batch
 sizes.  The prefill trace build (-DTL_PREFILL_TRACE=1): bit for bit too, and
-its per-CTA step counters add up to the call's key tiles.  The MMA probe runs
-and reports positive costs."""
+its per-CTA step counters add up to the call's key tiles.  The all-TS
+attention kernel (a build option) matches the oracle.  The MMA probe runs and
+reports positive costs."""
 import ctypes
 import json
 import os
@@ -15,7 +16,7 @@ import pytest
 import torch
 
 import paged_kv_attention_cache_gb300 as tl
-from paged_kv_attention_cache_gb300 import _lib, trace, workloads as wl
+from paged_kv_attention_cache_gb300 import _lib, build, trace, workloads as wl
 
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -134,3 +135,38 @@ def test_mma_probe_reports_positive_costs():
     lib = probe_mma.probe_library()
     for form in range(len(probe_mma.FORMS)):
         assert probe_mma.cycles(lib, form, 32, reps=1) > 0
+
+
+def test_all_ts_prefill_variant_matches_the_oracle():
+    """The all-TS attention kernel (a build option) over bf16 pools: every
+    output of a small batched call (pads, prior context, a ragged last query
+    tile) against the oracle."""
+    import oracle
+    from tests.parity import assert_close
+    lib = ctypes.CDLL(build.build_variant("prefill_all_ts", build.SOURCES,
+                                          ["TL_PREFILL_ALL_TS=1"]))
+    for name in ("tl_paged_attn_prefill", "tl_kv_cache_write"):
+        args, res = _lib.SIGNATURES[name]
+        getattr(lib, name).argtypes = args
+        getattr(lib, name).restype = res
+    case = wl.prefill_case([5, 0, 90], [300, 0, 1500], T=200, Hq=8, Hkv=2, d=128, seed=11)
+    g = wl.to_device(case, "cuda")
+    tl.tl_kv_cache_write(g.k_new.view(-1, 2, 128), g.v_new.view(-1, 2, 128), g.k_cache,
+                         g.v_cache, g.slot_mapping)
+    ws = tl.alloc_workspace(4 * tl.tl_paged_attn_prefill_workspace_size(
+        case.B, case.T, 8, 2, 128, case.block_table.shape[1], case.page_size), "cuda")
+    out = torch.empty((case.B, case.T, 8, 128), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = lib.tl_paged_attn_prefill(
+        g.q.data_ptr(), g.k_cache.data_ptr(), g.v_cache.data_ptr(), g.block_table.data_ptr(),
+        case.block_table.shape[1], g.positions.data_ptr(), out.data_ptr(), case.B, case.T, 8, 2,
+        128, g.k_cache.shape[0], case.page_size, 0, case.scale, tl.TL_BF16, ws.data_ptr(),
+        ws.numel(), err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == tl.TL_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    oracle.kv_cache_write(case.k_new.view(-1, 2, 128), case.v_new.view(-1, 2, 128), kc, vc,
+                          case.slot_mapping)
+    ref = oracle.paged_prefill(case.q, kc, vc, case.block_table, case.positions, case.scale)
+    assert_close(out.cpu().reshape(ref.shape), ref, "all-TS prefill")
