@@ -183,3 +183,39 @@ def test_piece_plan_extremes(shape):
     assert torch.isfinite(out).all()
     assert_decode_all(out, g_.q, g_.k_cache, g_.v_cache, g_.block_table, g_.context_lens,
                       g_.scale, chunk=256, what=f"piece plan {shape}")
+
+
+@pytest.mark.parametrize("B", [1, 3, 17, 32, 33, 127, 128, 129])
+@pytest.mark.parametrize("kind", ["bf16", "e4m3", "int8"])
+def test_plan_paths_and_combine_groups(B, kind):
+    """Batch sizes on both sides of the plan's one-warp path (up to 128
+    sequences) and the block-wide one, and across the combine's group counts
+    (16 groups at B = 1 down to one from B = 33 with 8 KV heads): every
+    sequence against the oracle, with lengths that give every sequence several
+    pieces."""
+    g = torch.Generator().manual_seed(300 + B)
+    lens = torch.randint(1, 2400 if B > 32 else 9000, (B,), generator=g).tolist()
+    case = wl.decode_case(lens, Hq=32, Hkv=8, d=128, seed=301 + B)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g_ = on_gpu(case)
+    if kind == "int8":
+        pools = wl.int8_pools(case, 302 + B)
+        kc, vc, ks, vs = (t.to("cuda") for t in pools)
+        out = tl.tl_paged_attn_decode_int8(g_.q, kc, vc, ks, vs, g_.block_table, g_.context_lens,
+                                           case.scale, error_word=err)
+        torch.cuda.synchronize()
+        ref = oracle.paged_decode_int8(case.q, *pools, case.block_table, case.context_lens,
+                                       case.scale)
+        assert int(err.item()) == 0
+        assert_close(out.cpu(), ref, f"int8 B={B}")
+        return
+    kc, vc = g_.k_cache, g_.v_cache
+    if kind == "e4m3":
+        kc, vc = kc.float().to(torch.float8_e4m3fn), vc.float().to(torch.float8_e4m3fn)
+    out = tl.tl_paged_attn_decode(g_.q, kc, vc, g_.block_table, g_.context_lens, case.scale,
+                                  error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isfinite(out).all()
+    assert_decode_all(out, g_.q, kc, vc, g_.block_table, g_.context_lens, g_.scale,
+                      chunk=64, what=f"{kind} B={B}")
