@@ -63,6 +63,9 @@
 //  40 two query tiles with Q in TMEM and 64-key S tiles, all TS fp16
 //     MN-major: per tile, 8 S MMAs N=64 (A = Q_a at 384 + 64a, D = 64a) then
 //     4 P.V MMAs N=128 (A = P_a in S_a's columns, D = O_a at 256 + 128a)
+//  41 the attention order PV0, S0, PV1, S1 with P.V too from shared memory:
+//     S = SS bf16 (B K-major) into 0 / 128, P.V = SS fp16 (A K-major at the
+//     Q tile's place + 32 KiB, B MN-major) into 256 / 384
 // The marginal cost per MMA is (t(n1) - t(n0)) / (n1 - n0), which takes out
 // the issue-to-first-MMA and commit latencies.
 #include <cuda_runtime.h>
@@ -73,7 +76,7 @@
 namespace tl {
 namespace probe {
 
-constexpr int kForms = 41;
+constexpr int kForms = 42;
 constexpr int kSmemBytes = 100 * 1024;
 
 __device__ __forceinline__ long long clk() {
@@ -112,6 +115,14 @@ __device__ __forceinline__ void issue8(uint32_t tm, uint32_t sb, uint32_t id_ss,
       const uint64_t a2 = tc::sdesc(sb + (i8 & 1) * 65536 + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
                                     1024);
       tc::mma_ss(tm + 128 * (i8 & 1), a2, b_ss, id_ss, kk > 0);
+    } else if (F == 41) {
+      const int g = i8 & 3, tile = g >> 1;
+      if ((g & 1) == 0)
+        tc::mma_ss(tm + 256 + 128 * tile,
+                   tc::sdesc(sb + 65536 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), b_ts,
+                   id_ts, 1u);
+      else
+        tc::mma_ss(tm + 128 * tile, a_ss, b_ss, id_ss, kk > 0);
     } else if (F == 39) {
       tc::mma_ts(tm, tm + 448 + 8 * kk, b_ts, tc::idesc_f16(128, 64, 0, 1), 1u);
     } else if (F == 40) {
@@ -350,7 +361,8 @@ extern "C" int tl_probe_mma_cycles(int form, int n_mma, long long* cycles_ns) {
     case 37: e = launch_probe<37>(n8, d); break;
     case 38: e = launch_probe<38>(n8, d); break;
     case 39: e = launch_probe<39>(n8, d); break;
-    default: e = launch_probe<40>(n8, d); break;
+    case 40: e = launch_probe<40>(n8, d); break;
+    default: e = launch_probe<41>(n8, d); break;
   }
   if (e == cudaSuccess) e = cudaMemcpy(cycles_ns, d, 2 * sizeof(long long), cudaMemcpyDeviceToHost);
   cudaFree(d);

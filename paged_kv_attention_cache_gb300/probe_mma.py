@@ -50,6 +50,7 @@ FORMS = [  # (name, M, N)
     ("the same, P from the other S buffer", 128, 128),
     ("TS N=64 alone", 128, 64),
     ("two tiles, Q in TMEM, 64-key S, all TS", 128, 96),
+    ("attention order, P.V from shared memory too (all SS)", 128, 128),
 ]
 
 
