@@ -1362,10 +1362,14 @@ __global__ void __launch_bounds__(DecodeShape<TWO_ROWS, KV8>::kWarps * 32, 1)
               scale_ring + stage * L::kScaleBytes + ((CPS + sub0 + jc) * kChunk + qr) * 4;
           asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v0) : "r"(sa));
           asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v1) : "r"(sa + 32));
-          p[jc][0] = p[jc][0] > 0.f ? p[jc][0] * v0 : 0.f;
-          p[jc][1] = p[jc][1] > 0.f ? p[jc][1] * v0 : 0.f;
-          p[jc][2] = p[jc][2] > 0.f ? p[jc][2] * v1 : 0.f;
-          p[jc][3] = p[jc][3] > 0.f ? p[jc][3] * v1 : 0.f;
+          // a scale of a slot outside the live keys may be anything: bounded
+          // to [0, 3e38] (NaN to 0), it leaves their p = 0 at 0
+          v0 = fminf(fmaxf(v0, 0.f), 3.0e38f);
+          v1 = fminf(fmaxf(v1, 0.f), 3.0e38f);
+          p[jc][0] *= v0;
+          p[jc][1] *= v0;
+          p[jc][2] *= v1;
+          p[jc][3] *= v1;
         }
         // P^T as the B operand: the fp16 pairs (columns 2t, 2t + 1) of keys g
         // and g + 8 form the 8 x 8 blocks P^T[keys 0-7] and P^T[keys 8-15];
