@@ -76,9 +76,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 def build_variant(name: str, sources, defines, force: bool = False) -> str:
     """A separate library built from some of the sources with extra -D
-    definitions, at _build/variants/<name>/libtlpa.so.  Used by tests that
-    need a build-time setting the product library does not have (a short
-    in-kernel wait bound with one wait made to run out)."""
+    definitions, at _build/variants/<name>/libtlpa.so.  Used where a
+    build-time setting the product library does not have is needed: a short
+    in-kernel wait bound with one wait made to run out (the failure test),
+    the decode and prefill trace builds, the all-TS prefill kernel and the
+    MMA probe."""
     out_dir = os.path.join(BUILD, "variants", name)
     lib = os.path.join(out_dir, "libtlpa.so")
     deps = [os.path.join(CSRC, s) for s in sources] + _deps()
